@@ -1,0 +1,417 @@
+"""Benchmark of the KDA mixer on one GB300 (or N replicas, one per GPU).
+
+One step = one pass of the whole mixer (conv+SiLU, ring roll, l2 norm, gates, scan, gated
+RMSNorm) over the prefill workload: 1 sequence x 4096 tokens, 64 heads x 128, bf16 projected
+q/k/v channels, zero initial state and ring (seeded synthetic data).  The same run also measures
+the decode step: 64 sequences x 1 token, 64 heads, random states (4 MiB each), through the fused
+decode kernel, state buffers ping-ponged between steps.
+
+Printed JSON line (rank 0):
+  value       prefill tokens/s, all ranks, inputs resident in HBM, CUDA events
+  e2e         the same through the public API with inputs copied from pinned host memory and the
+              result (y, final state, ring) read back every step
+  roofline    the scan kernel (dominant) against the FP32-pipe peak (bound "alu")
+  decode      decode state GB/s, total GB/s and its roofline against measured HBM bandwidth
+  cpu_baseline  the f64 oracle on a bounded sample of the prefill workload, host cores
+--impl reference times that oracle alone as the reference arm.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "KDA prefill tokens/s (H=64,d=128); decode state HBM GB/s vs peak"
+D = 128
+PREFILL_T, PREFILL_H = 4096, 64
+DEC_N, DEC_H = 64, 64
+FLOP_PER_TOKEN_HEAD = 7 * D * D   # decay D^2 + S^T k 2D^2 + rank-1 update 2D^2 + S^T q 2D^2
+SMS, FP32_LANES, SM_MAX_MHZ = 152, 128, 2070.0
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm_gbs=float(d["hbm_gbs"]), src="measured", sm_max_mhz=float(
+            d.get("sm_max_mhz", SM_MAX_MHZ)))
+    return dict(hbm_gbs=6800.0, src="fallback", sm_max_mhz=SM_MAX_MHZ)
+
+
+def _fp32_peak_tflops(mhz):
+    return SMS * FP32_LANES * 2 * mhz * 1e6 / 1e12
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ------------------------------------------------------------------------------------------
+# clocks
+# ------------------------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.path:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.remove(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        load = [r for r in rows if (num(r[3]) or 0) > 200.0] or rows
+        sm = [num(r[1]) for r in load if num(r[1]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in load for i in range(4)
+                          if r[5 + i].lower() in ("active", "1", "yes")})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": num(load[0][2]), "samples": len(rows),
+                "samples_under_load": len(load), "reasons": reasons}
+
+
+# ------------------------------------------------------------------------------------------
+# our arm
+# ------------------------------------------------------------------------------------------
+
+def _kernel_hash(files):
+    h = hashlib.sha256()
+    for f in files:
+        h.update(open(os.path.join(ROOT, "gated_delta_rule_scan_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def _traffic(kernel, files):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on this source."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p)).get(kernel)
+    if not d or d.get("source_hash") != _kernel_hash(files):
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    ws, rank, local = _dist()
+    if ws > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import __graft_entry__
+    __graft_entry__.build()
+    from gated_delta_rule_scan_gb300 import inputs, kda, mixer
+
+    peaks = _peaks()
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        if ws > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    def max_over_ranks(x):
+        if ws == 1:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    # ---------------- prefill workload (resident) ----------------
+    pre = inputs.prefill(T=PREFILL_T, H=PREFILL_H)
+    H, T = PREFILL_H, PREFILL_T
+    C = H * D
+    d = {k: (None if getattr(pre, k) is None else getattr(pre, k).to(dev)) for k in
+         ("q_raw", "k_raw", "v_raw", "conv_w", "ring_in", "f_raw", "dt_bias", "a_log",
+          "beta_raw", "state_in", "norm_w", "gate_raw")}
+    f32 = lambda *s: torch.empty(*s, dtype=torch.float32, device=dev)  # noqa: E731
+    buf = dict(q_hat=f32(T, C), k_hat=f32(T, C), v_hat=f32(T, C), g=f32(T, C), beta=f32(T, H),
+               o=f32(T, C), y=f32(T, C))
+    state_out = torch.empty_like(d["state_in"])
+    ring_out = torch.empty_like(d["ring_in"])
+    algo = kda.ALGO_AUTO
+
+    ev = {}
+
+    def prefill_step(timed_scan=None):
+        kda.kda_conv_l2norm_prep(d["q_raw"], d["k_raw"], d["v_raw"], d["conv_w"], d["ring_in"],
+                                 ring_out, d["f_raw"], d["dt_bias"], d["a_log"], d["beta_raw"],
+                                 buf["q_hat"], buf["k_hat"], buf["v_hat"], buf["g"],
+                                 buf["beta"], N=1, T=T, H=H)
+        if timed_scan is not None:
+            timed_scan[0].record(stream)
+        kda.kda_scan(buf["q_hat"], buf["k_hat"], buf["v_hat"], buf["g"], buf["beta"],
+                     d["state_in"], state_out, buf["o"], N=1, T=T, H=H, algo=algo)
+        if timed_scan is not None:
+            timed_scan[1].record(stream)
+        kda.kda_gated_rmsnorm_out(buf["o"], d["norm_w"], d["gate_raw"], buf["y"], rows=T * H)
+
+    launches_per_step = 4  # prep, ring roll, scan, gated RMSNorm
+    for _ in range(args.warmup):
+        prefill_step()
+    barrier()
+    K = args.steps
+    scan_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(K)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier()
+        t0.record(stream)
+        for i in range(K):
+            prefill_step(scan_ev[i])
+        t1.record(stream)
+        barrier()
+    clocks = clk.summary()
+    ms = max_over_ranks(t0.elapsed_time(t1))
+    ms_step = ms / K
+    tokens_per_s = ws * T / (ms_step / 1e3)
+    scan_ms = statistics.mean(a.elapsed_time(b) for a, b in scan_ev)
+    scan_flop = FLOP_PER_TOKEN_HEAD * T * H
+    fp32_peak = _fp32_peak_tflops(peaks["sm_max_mhz"])
+    scan_tflops = scan_flop / (scan_ms / 1e3) / 1e12
+    assert kda.kda_device_status() == 0
+
+    # ---------------- prefill end to end from pinned host memory ----------------
+    host = {k: v.cpu().pin_memory() for k, v in d.items() if v is not None}
+    dev_in = {k: torch.empty_like(v) for k, v in d.items() if v is not None}
+    y_host = torch.empty(T, C, dtype=torch.float32).pin_memory()
+    st_host = torch.empty_like(d["state_in"], device="cpu").pin_memory()
+    ring_host = torch.empty_like(d["ring_in"], device="cpu").pin_memory()
+    h2d_bytes = sum(v.numel() * v.element_size() for v in host.values())
+    d2h_bytes = sum(v.numel() * v.element_size() for v in (y_host, st_host, ring_host))
+
+    def e2e_step():
+        for k, v in host.items():
+            dev_in[k].copy_(v, non_blocking=True)
+        out = mixer.kda_forward(H=H, N=1, T=T, algo=algo, out=buf, state_out=state_out,
+                                ring_out=ring_out, **dev_in)
+        y_host.copy_(out["y"], non_blocking=True)
+        st_host.copy_(out["state_out"], non_blocking=True)
+        ring_host.copy_(out["ring_out"], non_blocking=True)
+
+    for _ in range(max(3, args.warmup // 4)):
+        e2e_step()
+    barrier()
+    Ke = max(3, K // 10)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(Ke):
+        e2e_step()
+    e1.record(stream)
+    barrier()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1)) / Ke
+    del host, dev_in
+
+    # ---------------- decode step (fused kernel) ----------------
+    dec = inputs.decode_step(N=DEC_N, T=1, H=DEC_H)
+    dd = {k: getattr(dec, k).to(dev) for k in
+          ("q_raw", "k_raw", "v_raw", "conv_w", "ring_in", "f_raw", "dt_bias", "a_log",
+           "beta_raw", "state_in", "norm_w", "gate_raw")}
+    states = [dd["state_in"], torch.empty_like(dd["state_in"])]
+    ring = dd["ring_in"]
+    y_dec = torch.empty(DEC_N, DEC_H * D, device=dev)
+
+    def decode_step(i):
+        kda.kda_decode_fused(dd["q_raw"], dd["k_raw"], dd["v_raw"], dd["conv_w"], ring, ring,
+                             dd["f_raw"], dd["dt_bias"], dd["a_log"], dd["beta_raw"],
+                             states[i & 1], states[(i + 1) & 1], dd["norm_w"], dd["gate_raw"],
+                             y_dec, N=DEC_N, T=1, H=DEC_H)
+
+    for i in range(max(args.warmup, 3)):
+        decode_step(i)
+    barrier()
+    Kd = max(K, 10)
+    d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    d0.record(stream)
+    for i in range(Kd):
+        decode_step(i)
+    d1.record(stream)
+    barrier()
+    dec_ms = max_over_ranks(d0.elapsed_time(d1)) / Kd
+    C1 = DEC_H * D
+    state_bytes = DEC_N * DEC_H * D * D * 4 * 2
+    per_seq = (DEC_H * D * D * 4 * 2 + 3 * C1 * 3 * 4 * 2 + 3 * C1 * 2 + C1 * 4 * 3 + DEC_H * 4)
+    dec_bytes = DEC_N * per_seq + 3 * C1 * 4 * 4 + C1 * 4 + DEC_H * 4 + D * 4
+    dec_gbs = dec_bytes / (dec_ms / 1e3) / 1e9
+    assert kda.kda_device_status() == 0
+
+    if ws > 1:
+        dist.destroy_process_group()
+    if rank != 0:
+        return None
+
+    cpu = cpu_baseline(pre, args.cpu_sample_heads)
+    return {
+        "metric": METRIC, "value": tokens_per_s, "unit": "tokens/s", "n_gpus": ws,
+        "steps": K, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded numpy default_rng; bf16 raw q/k/v, f32 gates, state, norm)",
+        "config": {"workload": "prefill: 1 sequence x 4096 tokens, H=64, head_dim=128, conv K=4,"
+                               " zero state and ring, full fused path",
+                   "global_batch": ws, "seq_len": T, "heads": H, "head_dim": D,
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
+                   "scan_algo": "auto", "l2": "inputs larger than L2 (470 MB read per step)"},
+        "gpu_launches": launches_per_step * K,
+        "roofline": {"bound": "alu", "kernel": "kda_scan_seq_kernel", "achieved": scan_tflops,
+                     "peak": fp32_peak, "unit": "TFLOP/s", "frac": scan_tflops / fp32_peak,
+                     "traffic": _traffic("kda_scan_seq_kernel",
+                                         ["kda_scan_seq.cu", "kda_device.cuh"]),
+                     "ms_per_launch": scan_ms, "flop_per_launch": scan_flop,
+                     "peak_src": f"152 SMs x 128 FP32 lanes x 2 x {peaks['sm_max_mhz']:.0f} MHz"},
+        "e2e": {"value": ws * T / (e2e_ms / 1e3), "unit": "tokens/s", "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes},
+        "decode": {"workload": "64 sequences x 1 token, H=64, fused decode kernel, states "
+                               "ping-ponged (512 MiB working set)",
+                   "ms_per_step": dec_ms, "seq_per_s": ws * DEC_N / (dec_ms / 1e3),
+                   "state_gbs": state_bytes / (dec_ms / 1e3) / 1e9,
+                   "roofline": {"bound": "hbm", "kernel": "kda_decode_fused_kernel",
+                                "achieved": dec_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                "frac": dec_gbs / peaks["hbm_gbs"],
+                                "peak_src": f"{peaks['src']} hbm_gbs",
+                                "traffic": _traffic("kda_decode_fused_kernel",
+                                                    ["kda_decode.cu", "kda_device.cuh"]),
+                                "bytes_per_launch": dec_bytes}},
+        "clocks": clocks,
+        "cpu_baseline": cpu,
+    }
+
+
+# ------------------------------------------------------------------------------------------
+# oracle (CPU baseline and reference arm)
+# ------------------------------------------------------------------------------------------
+
+def _oracle_sample(pre, heads):
+    """The oracle on the prefill workload restricted to `heads` (heads are independent, so this
+    is the exact work of those heads).  Returns seconds."""
+    import numpy as np
+
+    from oracle import oracle as orc
+    ch = np.concatenate([np.arange(h * D, (h + 1) * D) for h in heads])
+    C = pre.H * D
+    prow = np.concatenate([p * C + ch for p in range(3)])
+    args = dict(q_raw=pre.q_raw[:, ch], k_raw=pre.k_raw[:, ch], v_raw=pre.v_raw[:, ch],
+                f_raw=pre.f_raw[:, ch], dt_bias=pre.dt_bias[ch], a_log=pre.a_log[heads],
+                beta_raw=pre.beta_raw[:, heads], state_in=pre.state_in[:, heads],
+                conv_w=pre.conv_w[prow], ring_in=pre.ring_in[:, prow], norm_w=pre.norm_w,
+                gate_raw=pre.gate_raw[:, ch], H=len(heads), D=D, cu_seqlens=pre.cu_seqlens)
+    t = time.perf_counter()
+    orc.forward(**args)
+    return time.perf_counter() - t
+
+
+def cpu_baseline(pre, n_heads):
+    from oracle import oracle as orc
+    orc.build()
+    heads = list(range(n_heads))
+    secs = _oracle_sample(pre, heads)
+    frac = n_heads / pre.H
+    return {"value": PREFILL_T * frac / secs, "unit": "tokens/s",
+            "cores": min(orc.num_threads(), n_heads), "kind": "oracle",
+            "sample": f"prefill workload, heads 0..{n_heads - 1} of {pre.H} (all {PREFILL_T} "
+                      f"tokens, full mixer), {secs:.1f} s, scaled to 64 heads",
+            "host_cpus": os.cpu_count()}
+
+
+def run_reference(args):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return None
+    from gated_delta_rule_scan_gb300 import inputs
+    from oracle import oracle as orc
+    orc.build()
+    pre = inputs.prefill(T=PREFILL_T, H=PREFILL_H)
+    heads = list(range(args.cpu_sample_heads))
+    for _ in range(args.warmup if args.warmup < 2 else 1):
+        _oracle_sample(pre, heads)
+    ref_steps = min(args.steps, args.ref_steps)
+    secs = [_oracle_sample(pre, heads) for _ in range(ref_steps)]
+    frac = len(heads) / PREFILL_H
+    s = statistics.mean(secs)
+    value = PREFILL_T * frac / s
+    cores = min(orc.num_threads(), len(heads))
+    sample = (f"prefill workload, heads 0..{len(heads) - 1} of 64 per step (all 4096 tokens, "
+              f"full mixer), mean of {ref_steps} steps, scaled to 64 heads")
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": ws, "steps": ref_steps, "warmup": args.warmup,
+            "ms_per_step": s * 1e3 / frac, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "prefill: 1 sequence x 4096 tokens, H=64, head_dim=128",
+                       "seq_len": PREFILL_T, "heads": PREFILL_H},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--cpu-sample-heads", type=int, default=16)
+    ap.add_argument("--ref-steps", type=int, default=5)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    res = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,270 @@
+// kda_api.cu -- the extern "C" boundary of libkda: host-side contract checks, then dispatch to
+// the kernel launchers.  Status bands follow the launcher pattern of "memra_engine/mla_ffi.rs"
+// (memra-engine 0.124.0): 0 ok, 10000 + cudaError_t, 40000 + contract code.  No check touches
+// the GPU, so a violating call launches nothing.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/kda.h"
+#include "kda_internal.h"
+
+namespace {
+
+using namespace kda;
+
+// one device error word per device, raised by kernels that give up a bounded wait
+__device__ int g_kda_dev_err;
+
+constexpr int kMaxDevices = 64;
+constexpr int kMaxGridY = 65535;  // sequences (and heads) map to gridDim.y
+
+int* dev_err_ptr() {
+    static int* ptrs[kMaxDevices] = {nullptr};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    if (!ptrs[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_kda_dev_err) != cudaSuccess) return nullptr;
+        ptrs[dev] = static_cast<int*>(p);
+    }
+    return ptrs[dev];
+}
+
+inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA_BASE + (int)e; }
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline bool overlap(const void* a, const void* b, size_t bytes) {
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + bytes && y < x + bytes;
+}
+
+int check_cu(const int* cu_host, int N, long total) {
+    if (cu_host == nullptr) return KDA_ERR_NULL;
+    if (cu_host[0] != 0) return KDA_ERR_CU_SEQLENS;
+    for (int n = 0; n < N; ++n)
+        if (cu_host[n + 1] < cu_host[n]) return KDA_ERR_CU_SEQLENS;
+    if ((long)cu_host[N] != total) return KDA_ERR_CU_SEQLENS;
+    return KDA_OK;
+}
+
+int prep_impl(const void* q_raw, const void* k_raw, const void* v_raw, int raw_dtype,
+              const float* conv_w, const float* ring_in, float* ring_out, const float* f_raw,
+              const float* dt_bias, const float* a_log, int gate_mode, float gate_lb,
+              const float* beta_raw, float* q_hat, float* k_hat, float* v_hat, float* g,
+              float* beta, const SeqLayout& seq, int H, int D, int K, float l2_eps,
+              void* stream) {
+    if (D != kHeadDim) return KDA_ERR_HEAD_DIM;
+    if (seq.N < 0 || seq.N > kMaxGridY || seq.total_rows < 0 || H <= 0 || H > kMaxGridY)
+        return KDA_ERR_SHAPE;
+    if (raw_dtype != KDA_DTYPE_F32 && raw_dtype != KDA_DTYPE_BF16) return KDA_ERR_ENUM;
+    if (gate_mode != KDA_GATE_PER_CHANNEL && gate_mode != KDA_GATE_PER_HEAD) return KDA_ERR_ENUM;
+    if (conv_w != nullptr && (K < 2 || K > kMaxConvK)) return KDA_ERR_CONV_K;
+    if (seq.N == 0) return KDA_OK;
+    if (conv_w != nullptr && (ring_in == nullptr || ring_out == nullptr)) return KDA_ERR_NULL;
+    if (seq.total_rows > 0) {
+        if (!q_raw || !k_raw || !v_raw || !f_raw || !dt_bias || !a_log || !beta_raw || !q_hat ||
+            !k_hat || !v_hat || !g || !beta)
+            return KDA_ERR_NULL;
+        if (!aligned16(q_hat) || !aligned16(k_hat) || !aligned16(v_hat) || !aligned16(g))
+            return KDA_ERR_ALIGN;
+    }
+    if (conv_w != nullptr && ring_in != ring_out) {
+        const size_t rb = (size_t)seq.N * 3 * H * kHeadDim * (K - 1) * sizeof(float);
+        if (overlap(ring_in, ring_out, rb)) return KDA_ERR_STATE_ALIAS;
+    }
+    PrepArgs a{};
+    a.q_raw = q_raw; a.k_raw = k_raw; a.v_raw = v_raw; a.raw_bf16 = raw_dtype == KDA_DTYPE_BF16;
+    a.conv_w = conv_w; a.ring_in = ring_in; a.ring_out = ring_out;
+    a.f_raw = f_raw; a.dt_bias = dt_bias; a.a_log = a_log; a.gate_mode = gate_mode;
+    a.gate_lb = gate_lb; a.beta_raw = beta_raw;
+    a.q_hat = q_hat; a.k_hat = k_hat; a.v_hat = v_hat; a.g = g; a.beta = beta;
+    a.seq = seq; a.H = H; a.K = conv_w ? K : 1; a.l2_eps = l2_eps;
+    return cuda_status(launch_prep(a, static_cast<cudaStream_t>(stream)));
+}
+
+int scan_impl(const float* q, const float* k, const float* v, const float* g, int gate_mode,
+              const float* beta, const float* state_in, float* state_out, float* o,
+              const SeqLayout& seq, int H, int D, float scale, int algo, void* workspace,
+              size_t workspace_bytes, void* stream) {
+    (void)workspace; (void)workspace_bytes;
+    if (D != kHeadDim) return KDA_ERR_HEAD_DIM;
+    if (seq.N < 0 || seq.N > kMaxGridY || seq.total_rows < 0 || H <= 0) return KDA_ERR_SHAPE;
+    if (gate_mode != KDA_GATE_PER_CHANNEL && gate_mode != KDA_GATE_PER_HEAD) return KDA_ERR_ENUM;
+    if (algo != KDA_ALGO_AUTO && algo != KDA_ALGO_SEQ) return KDA_ERR_ENUM;
+    if (seq.total_rows >= (1L << 31)) return KDA_ERR_SHAPE;
+    if (seq.N == 0) return KDA_OK;
+    if (!state_in || !state_out) return KDA_ERR_NULL;
+    if (!aligned16(state_in) || !aligned16(state_out)) return KDA_ERR_ALIGN;
+    const size_t sb = (size_t)seq.N * H * kHeadDim * kHeadDim * sizeof(float);
+    if (overlap(state_in, state_out, sb)) return KDA_ERR_STATE_ALIAS;
+    if (seq.total_rows > 0) {
+        if (!q || !k || !v || !g || !beta || !o) return KDA_ERR_NULL;
+        if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
+            (gate_mode == KDA_GATE_PER_CHANNEL && !aligned16(g)))
+            return KDA_ERR_ALIGN;
+    }
+    ScanArgs a{};
+    a.q = q; a.k = k; a.v = v; a.g = g; a.gate_mode = gate_mode; a.beta = beta;
+    a.state_in = state_in; a.state_out = state_out; a.o = o;
+    a.seq = seq; a.H = H; a.scale = scale; a.order = nullptr;
+    a.err = dev_err_ptr();  // null only if the symbol lookup failed: waits then report nothing
+    return cuda_status(launch_scan_seq(a, static_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+
+extern "C" {
+
+int kda_abi_version(void) { return 1; }
+
+const char* kda_status_string(int s) {
+    switch (s) {
+        case KDA_OK: return "ok";
+        case KDA_ERR_HEAD_DIM: return "head_dim must be 128";
+        case KDA_ERR_CONV_K: return "conv kernel width K must be in 2..8";
+        case KDA_ERR_STATE_ALIAS: return "state_in/state_out (or ring_in/ring_out) overlap";
+        case KDA_ERR_NULL: return "a required pointer is NULL";
+        case KDA_ERR_SHAPE: return "bad shape (negative size, H == 0, or T out of range)";
+        case KDA_ERR_CU_SEQLENS: return "bad cu_seqlens (must start at 0, not decrease, end at total_T)";
+        case KDA_ERR_ENUM: return "unknown raw_dtype, gate_mode or algo";
+        case KDA_ERR_TIMEOUT: return "a kernel gave up a bounded device wait";
+        case KDA_ERR_WORKSPACE: return "workspace missing or too small";
+        case KDA_ERR_ALIGN: return "a pointer that must be 16-byte aligned is not";
+        default:
+            if (s >= KDA_ERR_CUDA_BASE && s < KDA_ERR_CUDA_BASE + 10000) return "CUDA error";
+            return "unknown status";
+    }
+}
+
+int kda_conv_l2norm_prep(const void* q_raw, const void* k_raw, const void* v_raw, int raw_dtype,
+                         const float* conv_w, const float* ring_in, float* ring_out,
+                         const float* f_raw, const float* dt_bias, const float* a_log,
+                         int gate_mode, float gate_lb, const float* beta_raw, float* q_hat,
+                         float* k_hat, float* v_hat, float* g, float* beta, int N, int T, int H,
+                         int D, int K, float l2_eps, void* stream) {
+    if (N < 0 || T < 0) return KDA_ERR_SHAPE;
+    SeqLayout seq{nullptr, T, N, (long)N * T};
+    if (T == 0 && N > 0) seq.T_uniform = 0;
+    return prep_impl(q_raw, k_raw, v_raw, raw_dtype, conv_w, ring_in, ring_out, f_raw, dt_bias,
+                     a_log, gate_mode, gate_lb, beta_raw, q_hat, k_hat, v_hat, g, beta, seq, H,
+                     D, K, l2_eps, stream);
+}
+
+int kda_conv_l2norm_prep_varlen(const void* q_raw, const void* k_raw, const void* v_raw,
+                                int raw_dtype, const float* conv_w, const float* ring_in,
+                                float* ring_out, const float* f_raw, const float* dt_bias,
+                                const float* a_log, int gate_mode, float gate_lb,
+                                const float* beta_raw, float* q_hat, float* k_hat, float* v_hat,
+                                float* g, float* beta, const int* cu_seqlens,
+                                const int* cu_seqlens_host, int N, int total_T, int H, int D,
+                                int K, float l2_eps, void* stream) {
+    if (N < 0 || total_T < 0) return KDA_ERR_SHAPE;
+    if (N > 0) {
+        if (cu_seqlens == nullptr) return KDA_ERR_NULL;
+        const int rc = check_cu(cu_seqlens_host, N, total_T);
+        if (rc) return rc;
+    }
+    SeqLayout seq{cu_seqlens, 0, N, (long)total_T};
+    return prep_impl(q_raw, k_raw, v_raw, raw_dtype, conv_w, ring_in, ring_out, f_raw, dt_bias,
+                     a_log, gate_mode, gate_lb, beta_raw, q_hat, k_hat, v_hat, g, beta, seq, H,
+                     D, K, l2_eps, stream);
+}
+
+size_t kda_scan_workspace_bytes(int N, int total_T, int H, int D, int gate_mode, int algo) {
+    (void)N; (void)total_T; (void)H; (void)D; (void)gate_mode; (void)algo;
+    return 0;
+}
+
+int kda_scan(const float* q_hat, const float* k_hat, const float* v_hat, const float* g,
+             int gate_mode, const float* beta, const float* state_in, float* state_out,
+             float* o, int N, int T, int H, int D, float scale, int algo, void* workspace,
+             size_t workspace_bytes, void* stream) {
+    if (N < 0 || T < 0) return KDA_ERR_SHAPE;
+    SeqLayout seq{nullptr, T, N, (long)N * T};
+    return scan_impl(q_hat, k_hat, v_hat, g, gate_mode, beta, state_in, state_out, o, seq, H, D,
+                     scale, algo, workspace, workspace_bytes, stream);
+}
+
+int kda_scan_varlen(const float* q_hat, const float* k_hat, const float* v_hat, const float* g,
+                    int gate_mode, const float* beta, const float* state_in, float* state_out,
+                    float* o, const int* cu_seqlens, const int* cu_seqlens_host, int N,
+                    int total_T, int H, int D, float scale, int algo, void* workspace,
+                    size_t workspace_bytes, void* stream) {
+    if (N < 0 || total_T < 0) return KDA_ERR_SHAPE;
+    if (N > 0) {
+        if (cu_seqlens == nullptr) return KDA_ERR_NULL;
+        const int rc = check_cu(cu_seqlens_host, N, total_T);
+        if (rc) return rc;
+    }
+    SeqLayout seq{cu_seqlens, 0, N, (long)total_T};
+    return scan_impl(q_hat, k_hat, v_hat, g, gate_mode, beta, state_in, state_out, o, seq, H, D,
+                     scale, algo, workspace, workspace_bytes, stream);
+}
+
+int kda_gated_rmsnorm_out(const float* o, const float* norm_w, const float* gate_raw, float* y,
+                          long rows, int D, float eps, void* stream) {
+    if (D != kHeadDim) return KDA_ERR_HEAD_DIM;
+    if (rows < 0) return KDA_ERR_SHAPE;
+    if (rows == 0) return KDA_OK;
+    if (!o || !norm_w || !gate_raw || !y) return KDA_ERR_NULL;
+    if (!aligned16(o) || !aligned16(norm_w) || !aligned16(gate_raw) || !aligned16(y))
+        return KDA_ERR_ALIGN;
+    NormArgs a{o, norm_w, gate_raw, y, rows, eps};
+    return cuda_status(launch_gated_rmsnorm(a, static_cast<cudaStream_t>(stream)));
+}
+
+int kda_decode_fused(const void* q_raw, const void* k_raw, const void* v_raw, int raw_dtype,
+                     const float* conv_w, const float* ring_in, float* ring_out,
+                     const float* f_raw, const float* dt_bias, const float* a_log, int gate_mode,
+                     float gate_lb, const float* beta_raw, const float* state_in,
+                     float* state_out, const float* norm_w, const float* gate_raw, float* y,
+                     int N, int T, int H, int D, int K, float l2_eps, float scale, float rms_eps,
+                     void* stream) {
+    if (D != kHeadDim) return KDA_ERR_HEAD_DIM;
+    if (N < 0 || N > kMaxGridY || H <= 0 || H > kMaxGridY || T < 1 || T > kDecodeMaxT)
+        return KDA_ERR_SHAPE;
+    if (raw_dtype != KDA_DTYPE_F32 && raw_dtype != KDA_DTYPE_BF16) return KDA_ERR_ENUM;
+    if (gate_mode != KDA_GATE_PER_CHANNEL && gate_mode != KDA_GATE_PER_HEAD) return KDA_ERR_ENUM;
+    if (K < 2 || K > kMaxConvK) return KDA_ERR_CONV_K;
+    if (N == 0) return KDA_OK;
+    if (!q_raw || !k_raw || !v_raw || !conv_w || !ring_in || !ring_out || !f_raw || !dt_bias ||
+        !a_log || !beta_raw || !state_in || !state_out || !norm_w || !gate_raw || !y)
+        return KDA_ERR_NULL;
+    if (!aligned16(state_in) || !aligned16(state_out) || !aligned16(norm_w) ||
+        !aligned16(gate_raw) || !aligned16(y))
+        return KDA_ERR_ALIGN;
+    const size_t sb = (size_t)N * H * kHeadDim * kHeadDim * sizeof(float);
+    if (overlap(state_in, state_out, sb)) return KDA_ERR_STATE_ALIAS;
+    if (ring_in != ring_out) {
+        const size_t rb = (size_t)N * 3 * H * kHeadDim * (K - 1) * sizeof(float);
+        if (overlap(ring_in, ring_out, rb)) return KDA_ERR_STATE_ALIAS;
+    }
+    DecodeArgs a{};
+    a.q_raw = q_raw; a.k_raw = k_raw; a.v_raw = v_raw; a.raw_bf16 = raw_dtype == KDA_DTYPE_BF16;
+    a.conv_w = conv_w; a.ring_in = ring_in; a.ring_out = ring_out;
+    a.f_raw = f_raw; a.dt_bias = dt_bias; a.a_log = a_log; a.gate_mode = gate_mode;
+    a.gate_lb = gate_lb; a.beta_raw = beta_raw; a.state_in = state_in; a.state_out = state_out;
+    a.norm_w = norm_w; a.gate_raw = gate_raw; a.y = y;
+    a.N = N; a.T = T; a.H = H; a.K = K; a.l2_eps = l2_eps; a.scale = scale; a.rms_eps = rms_eps;
+    return cuda_status(launch_decode_fused(a, static_cast<cudaStream_t>(stream)));
+}
+
+int kda_device_status(void* stream) {
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_status(e);
+    int* p = dev_err_ptr();
+    if (p == nullptr) return cuda_status(cudaErrorUnknown);
+    int v = 0;
+    e = cudaMemcpy(&v, p, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_status(e);
+    if (v != 0) {
+        const int zero = 0;
+        e = cudaMemcpy(p, &zero, sizeof(int), cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) return cuda_status(e);
+        return KDA_ERR_TIMEOUT;
+    }
+    return KDA_OK;
+}
+
+}  // extern "C"

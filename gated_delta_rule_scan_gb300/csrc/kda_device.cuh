@@ -1,0 +1,180 @@
+// kda_device.cuh -- device-side helpers shared by every KDA kernel.
+//
+// The scalar maths here is written once and used by the prep kernel, the fused decode/verify
+// kernel, the sequential scan and the epilogue, so that every path that must agree bit for bit
+// (decode vs multi-token verify, chained T=1 scans vs one T-token scan) runs the same instruction
+// sequence.  All products that feed a reduction use explicit fmaf/__fmul_rn so the compiler has
+// no contraction freedom between call sites.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kda_internal.h"
+
+namespace kda {
+
+constexpr int kWaitSpinLimit = 1 << 22;  // bounded mbarrier wait: ~1 s with the back-off below
+
+// device error word codes (written by kernels, read by kda_device_status)
+constexpr int kDevErrTimeout = 1;
+
+// ------------------------------------------------------------------------------------------
+// scalar maths (f32, IEEE expf / division / sqrt: the library is built without fast-math)
+// ------------------------------------------------------------------------------------------
+
+__device__ __forceinline__ float sigmoid_f(float x) { return 1.0f / (1.0f + expf(-x)); }
+
+__device__ __forceinline__ float silu_f(float x) { return __fmul_rn(x, sigmoid_f(x)); }
+
+// log(1 + e^x) without overflow: max(x, 0) + log1p(e^-|x|)
+__device__ __forceinline__ float softplus_f(float x) {
+    return fmaxf(x, 0.0f) + log1pf(expf(-fabsf(x)));
+}
+
+// KDA per-channel forget gate as a raw log-decay: lb * sigmoid(rate * (f + dt_bias)),
+// rate = exp(A_log[h]) computed once per head by the caller.
+__device__ __forceinline__ float kda_gate_f(float f, float dt_bias, float rate, float lb) {
+    return __fmul_rn(lb, sigmoid_f(__fmul_rn(rate, f + dt_bias)));
+}
+
+// GDN per-head log-decay: -exp(A_log[h]) * softplus(alpha + dt_bias[h]).
+__device__ __forceinline__ float gdn_gate_f(float alpha, float dt_bias, float a_log) {
+    return -__fmul_rn(expf(a_log), softplus_f(alpha + dt_bias));
+}
+
+// 1 / sqrt(sum of squares + eps): the l2-norm scale (eps inside the sqrt, on the SUM).
+__device__ __forceinline__ float l2_inv_f(float ss, float eps) { return 1.0f / sqrtf(ss + eps); }
+
+// 1 / sqrt(mean of squares + eps) over 128 values: the RMSNorm scale.
+__device__ __forceinline__ float rms_inv_f(float ss, float eps) {
+    return 1.0f / sqrtf(__fmul_rn(ss, 1.0f / kHeadDim) + eps);
+}
+
+// one gated-RMSNorm output element: ((o * inv) * w) * sigmoid(z)
+__device__ __forceinline__ float gated_norm_f(float o, float inv, float w, float z) {
+    return __fmul_rn(__fmul_rn(__fmul_rn(o, inv), w), sigmoid_f(z));
+}
+
+// Causal conv taps over a register window win[0..kMaxConvK-1] whose last K slots hold the K
+// samples oldest first (win[kMaxConvK-1] = current token), weights wr likewise aligned to the
+// end.  Taps are accumulated oldest first, one fmaf each, starting from 0.
+__device__ __forceinline__ float conv_taps_f(const float (&wr)[kMaxConvK],
+                                             const float (&win)[kMaxConvK], int K) {
+    float acc = 0.0f;
+#pragma unroll
+    for (int m = 0; m < kMaxConvK; ++m)
+        if (m >= kMaxConvK - K) acc = fmaf(wr[m], win[m], acc);
+    return acc;
+}
+
+__device__ __forceinline__ void window_push(float (&win)[kMaxConvK], float x) {
+#pragma unroll
+    for (int m = 0; m < kMaxConvK - 1; ++m) win[m] = win[m + 1];
+    win[kMaxConvK - 1] = x;
+}
+
+// ------------------------------------------------------------------------------------------
+// reductions
+// ------------------------------------------------------------------------------------------
+
+// Butterfly sum over all 32 lanes; every lane ends with the same bits (a + b == b + a).
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) x += __shfl_xor_sync(0xffffffffu, x, m);
+    return x;
+}
+
+// Butterfly sum over aligned groups of 8 lanes (xor 1, 2, 4).
+__device__ __forceinline__ float group8_sum(float x) {
+    x += __shfl_xor_sync(0xffffffffu, x, 1);
+    x += __shfl_xor_sync(0xffffffffu, x, 2);
+    x += __shfl_xor_sync(0xffffffffu, x, 4);
+    return x;
+}
+
+// Sum of a 128-channel head held one channel per thread across 4 consecutive warps:
+// warp partials are combined in the fixed order ((p0 + p1) + p2) + p3.
+__device__ __forceinline__ float head_sum4(const float* p) { return ((p[0] + p[1]) + p[2]) + p[3]; }
+
+// ------------------------------------------------------------------------------------------
+// loads
+// ------------------------------------------------------------------------------------------
+
+template <bool BF16>
+__device__ __forceinline__ float load_raw(const void* base, long idx) {
+    if constexpr (BF16) {
+        return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(base)[idx]);
+    } else {
+        return reinterpret_cast<const float*>(base)[idx];
+    }
+}
+
+// ------------------------------------------------------------------------------------------
+// mbarrier + TMA (inline PTX, sm_90+ forms valid on sm_103a)
+// ------------------------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+                 : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait on an mbarrier phase.  Returns false (and raises the device error word) when the
+// phase has not completed after ~1 s; the caller then stops issuing work and returns.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, int* err) {
+    for (int it = 0; it < kWaitSpinLimit; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (it > 32) __nanosleep(256);
+    }
+    if (err) atomicOr(err, kDevErrTimeout);
+    return false;
+}
+
+// 2D tiled TMA load global -> shared, completion counted on an mbarrier (bytes).
+// c0 = innermost (element) coordinate, c1 = row coordinate.
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int c0, int c1,
+                                            uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+}  // namespace kda

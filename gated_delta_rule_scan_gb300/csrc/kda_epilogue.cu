@@ -1,0 +1,44 @@
+// kda_epilogue.cu -- sigmoid-gated RMSNorm over head_dim.
+//
+// Method ("memra_engine/kda.rs", memra-engine 0.125.0, kda_core_gated stage 6 and
+// Engine::kda_gated_rmsnorm): per (token, head) row of 128 values,
+//     y_i = o_i / sqrt(mean_i o_i^2 + eps) * w_i * sigmoid(z_i)
+// with w shared by all heads and the gate z not normalised (gdn_ops.rs gdn_gated_rmsnorm_into).
+//
+// One warp per row, one float4 per lane: a 512-byte coalesced load of o and z and store of y, a
+// 5-step butterfly for the mean square.  The arithmetic is the fused decode kernel's epilogue,
+// instruction for instruction.
+#include "kda_device.cuh"
+#include "kda_internal.h"
+
+namespace kda {
+
+__global__ void __launch_bounds__(256) kda_gated_rmsnorm_kernel(NormArgs a) {
+    const long row = (long)blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= a.rows) return;
+    const long base = row * kHeadDim + 4 * lane;
+    const float4 o4 = __ldcs(reinterpret_cast<const float4*>(a.o + base));
+    float ss = __fmul_rn(o4.x, o4.x);
+    ss = ss + __fmul_rn(o4.y, o4.y);
+    ss = ss + __fmul_rn(o4.z, o4.z);
+    ss = ss + __fmul_rn(o4.w, o4.w);
+    const float inv = rms_inv_f(warp_sum(ss), a.eps);
+    const float4 w4 = *reinterpret_cast<const float4*>(a.w + 4 * lane);
+    const float4 z4 = __ldcs(reinterpret_cast<const float4*>(a.z + base));
+    float4 y4;
+    y4.x = gated_norm_f(o4.x, inv, w4.x, z4.x);
+    y4.y = gated_norm_f(o4.y, inv, w4.y, z4.y);
+    y4.z = gated_norm_f(o4.z, inv, w4.z, z4.z);
+    y4.w = gated_norm_f(o4.w, inv, w4.w, z4.w);
+    __stcs(reinterpret_cast<float4*>(a.y + base), y4);
+}
+
+cudaError_t launch_gated_rmsnorm(const NormArgs& a, cudaStream_t s) {
+    if (a.rows == 0) return cudaSuccess;
+    const long blocks = (a.rows + 7) / 8;
+    kda_gated_rmsnorm_kernel<<<(unsigned)blocks, 256, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace kda

@@ -1,0 +1,65 @@
+// kda_internal.h -- host-side launch interface between the C ABI (kda_api.cu) and the kernels.
+// Every launcher assumes its arguments already passed the ABI's contract checks and returns the
+// cudaError_t of its launch(es).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace kda {
+
+constexpr int kHeadDim = 128;      // the only head width the kernels are built for
+constexpr int kMaxConvK = 8;       // conv window held in registers (taps 2..8)
+
+// Row ranges of the packed token-major arrays.  When cu_seqlens is null every sequence has
+// T_uniform tokens and sequence n owns rows [n*T, (n+1)*T).
+struct SeqLayout {
+    const int* cu_seqlens;   // device int32 [N+1] or null
+    int T_uniform;
+    int N;
+    long total_rows;
+};
+
+struct PrepArgs {
+    const void* q_raw; const void* k_raw; const void* v_raw; int raw_bf16;
+    const float* conv_w;                 // [3C, K] or null (no conv, no SiLU)
+    const float* ring_in; float* ring_out;  // [N, 3C, K-1]
+    const float* f_raw; const float* dt_bias; const float* a_log; int gate_mode; float gate_lb;
+    const float* beta_raw;
+    float* q_hat; float* k_hat; float* v_hat; float* g; float* beta;
+    SeqLayout seq;
+    int H; int K; float l2_eps;
+};
+
+struct ScanArgs {
+    const float* q; const float* k; const float* v; const float* g; int gate_mode;
+    const float* beta;
+    const float* state_in; float* state_out; float* o;
+    SeqLayout seq;
+    int H; float scale;
+    const int* order;        // device-side order of sequences (longest first) or null
+    int* err;                // device error word
+};
+
+struct NormArgs {
+    const float* o; const float* w; const float* z; float* y; long rows; float eps;
+};
+
+struct DecodeArgs {
+    const void* q_raw; const void* k_raw; const void* v_raw; int raw_bf16;
+    const float* conv_w; const float* ring_in; float* ring_out;
+    const float* f_raw; const float* dt_bias; const float* a_log; int gate_mode; float gate_lb;
+    const float* beta_raw;
+    const float* state_in; float* state_out;
+    const float* norm_w; const float* gate_raw; float* y;
+    int N; int T; int H; int K; float l2_eps; float scale; float rms_eps;
+};
+
+cudaError_t launch_prep(const PrepArgs& a, cudaStream_t s);
+cudaError_t launch_scan_seq(const ScanArgs& a, cudaStream_t s);
+cudaError_t launch_gated_rmsnorm(const NormArgs& a, cudaStream_t s);
+cudaError_t launch_decode_fused(const DecodeArgs& a, cudaStream_t s);
+
+constexpr int kDecodeMaxT = 16;   // tokens one fused decode/verify call may carry
+
+}  // namespace kda

@@ -1,0 +1,269 @@
+// kda_scan_seq.cu -- the per-channel gated delta-rule scan, sequential form.
+//
+// Method ("memra_engine/kda.rs", memra-engine 0.125.0: module doc and kda_core_gated stage 5,
+// Engine::kda_scan "the per-channel-decay delta-rule scan"), per (sequence, head), per token t:
+//     S <- Diag(exp g_t) S        (decay along the key dim i)
+//     u  = v_t - S^T k_t
+//     S <- S + beta_t k_t u^T
+//     o_t = scale * S^T q_t       (readout from the updated state)
+// The state buffers hold M[j][i] = S[i][j] (value column j, key dim i contiguous).
+//
+// GB300 layout.  Every value column j of S is an independent 128-vector recurrence, so the kernel
+// parallelises over (sequence, head, column) and keeps each column in registers for the whole
+// sequence: 8 lanes own one column, 16 key-dim elements each (i = 4r + 32m + e, r = lane in the
+// group, m, e = 0..3), so both dot products reduce over 8 lanes with 3 butterfly shuffles.  A CTA
+// owns 32 columns of one head (256 threads).  The per-token inputs that every column of the head
+// shares (q, k, g rows: 512 B each) and the CTA's 32 v values are staged by 2-D TMA tensor-map
+// loads into a double-buffered shared-memory ring of kScanTB-token blocks, completion tracked
+// by mbarriers (bounded waits); the next block streams in while the current one is scanned.
+// beta (and the GDN scalar gate) are register-prefetched one block ahead.  Outputs are buffered
+// per block in shared memory and written back as coalesced 128-byte rows.
+//
+// The in-kernel token loop is the chained one-token program: a T-token launch and T one-token
+// launches run the same instruction sequence per token, so their results are bit-identical.
+#include "kda_device.cuh"
+#include "kda_internal.h"
+
+namespace kda {
+
+constexpr int kScanCols = 32;                   // value columns per CTA
+constexpr int kScanThreads = kScanCols * 8;     // 8 lanes per column
+constexpr int kScanTB = 16;                     // tokens per staged block
+constexpr int kColBlocks = kHeadDim / kScanCols;
+
+struct __align__(128) ScanSmem {
+    float q[2][kScanTB][kHeadDim];
+    float k[2][kScanTB][kHeadDim];
+    float g[2][kScanTB][kHeadDim];      // per-channel log-decay (gate mode 0)
+    float v[2][kScanTB][kScanCols];
+    float a[kScanTB][kHeadDim];         // exp(g) of the block being scanned
+    float obuf[kScanTB][kScanCols];
+    float beta[2][kScanTB];
+    float ascal[2][kScanTB];            // exp(g) scalar (gate mode 1)
+    uint64_t bar[2];
+};
+
+template <int GATE_MODE>
+__global__ void __launch_bounds__(kScanThreads)
+kda_scan_seq_kernel(ScanArgs a, const __grid_constant__ CUtensorMap tq,
+                    const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tg,
+                    const __grid_constant__ CUtensorMap tv) {
+    extern __shared__ unsigned char smem_raw[];
+    ScanSmem& sm = *reinterpret_cast<ScanSmem*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+
+    const int tid = threadIdx.x;
+    const int cb = blockIdx.x % kColBlocks;
+    const int h = blockIdx.x / kColBlocks;
+    const int n = a.order ? a.order[blockIdx.y] : (int)blockIdx.y;
+    const int col = tid >> 3, r = tid & 7;
+    const int j = cb * kScanCols + col;
+    const int H = a.H;
+    const long C = (long)H * kHeadDim;
+
+    long begin, end;
+    if (a.seq.cu_seqlens == nullptr) {
+        begin = (long)n * a.seq.T_uniform;
+        end = begin + a.seq.T_uniform;
+    } else {
+        begin = a.seq.cu_seqlens[n];
+        end = a.seq.cu_seqlens[n + 1];
+    }
+    const long L = end - begin;
+    const int nblk = (int)((L + kScanTB - 1) / kScanTB);
+
+    // this lane's 16 elements of column j: S[m][e] = M[j][4r + 32m + e]
+    const long sbase = (((long)n * H + h) * kHeadDim + j) * kHeadDim + 4 * r;
+    float4 S[4];
+#pragma unroll
+    for (int m = 0; m < 4; ++m) S[m] = __ldcs(reinterpret_cast<const float4*>(a.state_in + sbase + 32 * m));
+
+    constexpr uint32_t kTxBytes =
+        (GATE_MODE == 0 ? 3u : 2u) * kScanTB * kHeadDim * 4u + kScanTB * kScanCols * 4u;
+    if (tid == 0) {
+        prefetch_tensormap(&tq);
+        prefetch_tensormap(&tk);
+        if (GATE_MODE == 0) prefetch_tensormap(&tg);
+        prefetch_tensormap(&tv);
+        mbar_init(&sm.bar[0], 1);
+        mbar_init(&sm.bar[1], 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    auto issue = [&](int b, int st) {
+        const int row = (int)(begin + (long)b * kScanTB);
+        fence_proxy_async_smem();
+        mbar_arrive_expect_tx(&sm.bar[st], kTxBytes);
+        tma_load_2d(&sm.q[st][0][0], &tq, h * kHeadDim, row, &sm.bar[st]);
+        tma_load_2d(&sm.k[st][0][0], &tk, h * kHeadDim, row, &sm.bar[st]);
+        if (GATE_MODE == 0) tma_load_2d(&sm.g[st][0][0], &tg, h * kHeadDim, row, &sm.bar[st]);
+        tma_load_2d(&sm.v[st][0][0], &tv, h * kHeadDim + cb * kScanCols, row, &sm.bar[st]);
+    };
+    if (tid == 0 && nblk > 0) issue(0, 0);
+
+    float bpre = 0.0f, gpre = 0.0f;
+    if (tid < kScanTB && tid < L) {
+        bpre = a.beta[(begin + tid) * H + h];
+        if (GATE_MODE == 1) gpre = a.g[(begin + tid) * H + h];
+    }
+
+    for (int b = 0; b < nblk; ++b) {
+        const int st = b & 1;
+        const long row0 = begin + (long)b * kScanTB;
+        const int nt = (int)min((long)kScanTB, L - (long)b * kScanTB);
+        if (tid < kScanTB) {
+            sm.beta[st][tid] = bpre;
+            if (GATE_MODE == 1) sm.ascal[st][tid] = expf(gpre);
+            const long rn = row0 + kScanTB + tid;
+            if (rn < end) {
+                bpre = a.beta[rn * H + h];
+                if (GATE_MODE == 1) gpre = a.g[rn * H + h];
+            }
+        }
+        const bool arrived = mbar_wait_bounded(&sm.bar[st], (uint32_t)((b >> 1) & 1), a.err);
+        if (__syncthreads_or(!arrived)) return;  // device error word already raised
+        if (tid == 0 && b + 1 < nblk) issue(b + 1, st ^ 1);
+        if (GATE_MODE == 0) {
+            for (int e = tid; e < nt * kHeadDim; e += kScanThreads)
+                (&sm.a[0][0])[e] = expf((&sm.g[st][0][0])[e]);
+        }
+        __syncthreads();
+
+        for (int t = 0; t < nt; ++t) {
+            const float* kr = &sm.k[st][t][4 * r];
+            const float* qr = &sm.q[st][t][4 * r];
+            float4 k4[4], a4[4];
+#pragma unroll
+            for (int m = 0; m < 4; ++m) k4[m] = *reinterpret_cast<const float4*>(kr + 32 * m);
+            if (GATE_MODE == 0) {
+#pragma unroll
+                for (int m = 0; m < 4; ++m)
+                    a4[m] = *reinterpret_cast<const float4*>(&sm.a[t][4 * r + 32 * m]);
+            } else {
+                const float as = sm.ascal[st][t];
+#pragma unroll
+                for (int m = 0; m < 4; ++m) a4[m] = make_float4(as, as, as, as);
+            }
+            // decay, then S^T k with the decayed state
+            float d[4];
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                S[m].x = __fmul_rn(a4[m].x, S[m].x);
+                S[m].y = __fmul_rn(a4[m].y, S[m].y);
+                S[m].z = __fmul_rn(a4[m].z, S[m].z);
+                S[m].w = __fmul_rn(a4[m].w, S[m].w);
+                float acc = __fmul_rn(S[m].x, k4[m].x);
+                acc = fmaf(S[m].y, k4[m].y, acc);
+                acc = fmaf(S[m].z, k4[m].z, acc);
+                acc = fmaf(S[m].w, k4[m].w, acc);
+                d[m] = acc;
+            }
+            const float dk = group8_sum((d[0] + d[1]) + (d[2] + d[3]));
+            const float u = sm.v[st][t][col] - dk;
+            const float w = __fmul_rn(sm.beta[st][t], u);
+            // rank-1 update, then S^T q with the updated state
+            float4 q4[4];
+#pragma unroll
+            for (int m = 0; m < 4; ++m) q4[m] = *reinterpret_cast<const float4*>(qr + 32 * m);
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                S[m].x = fmaf(k4[m].x, w, S[m].x);
+                S[m].y = fmaf(k4[m].y, w, S[m].y);
+                S[m].z = fmaf(k4[m].z, w, S[m].z);
+                S[m].w = fmaf(k4[m].w, w, S[m].w);
+                float acc = __fmul_rn(S[m].x, q4[m].x);
+                acc = fmaf(S[m].y, q4[m].y, acc);
+                acc = fmaf(S[m].z, q4[m].z, acc);
+                acc = fmaf(S[m].w, q4[m].w, acc);
+                d[m] = acc;
+            }
+            const float dq = group8_sum((d[0] + d[1]) + (d[2] + d[3]));
+            if (r == 0) sm.obuf[t][col] = __fmul_rn(a.scale, dq);
+        }
+        __syncthreads();
+        for (int e = tid; e < nt * (kScanCols / 4); e += kScanThreads) {
+            const int t = e / (kScanCols / 4), c4 = e % (kScanCols / 4);
+            *reinterpret_cast<float4*>(a.o + (row0 + t) * C + h * kHeadDim + cb * kScanCols + 4 * c4) =
+                *reinterpret_cast<const float4*>(&sm.obuf[t][4 * c4]);
+        }
+    }
+#pragma unroll
+    for (int m = 0; m < 4; ++m) __stcs(reinterpret_cast<float4*>(a.state_out + sbase + 32 * m), S[m]);
+}
+
+// ------------------------------------------------------------------------------------------
+// host side
+// ------------------------------------------------------------------------------------------
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+// 2-D f32 tensor [rows, cols] (row stride = cols), box [box_rows, box_cols], no swizzle.
+static bool make_map(CUtensorMap* m, const float* base, long rows, long cols, int box_cols,
+                     int box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)cols * sizeof(float)};
+    cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
+    cuuint32_t es[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims, strides, box,
+              es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
+template <int GM>
+static cudaError_t launch_t(const ScanArgs& a, cudaStream_t s) {
+    const long C = (long)a.H * kHeadDim;
+    const long rows = a.seq.total_rows;
+    CUtensorMap tq, tk, tg, tv;
+    if (!make_map(&tq, a.q, rows, C, kHeadDim, kScanTB) ||
+        !make_map(&tk, a.k, rows, C, kHeadDim, kScanTB) ||
+        !make_map(&tv, a.v, rows, C, kScanCols, kScanTB))
+        return cudaErrorInvalidValue;
+    if (GM == 0) {
+        if (!make_map(&tg, a.g, rows, C, kHeadDim, kScanTB)) return cudaErrorInvalidValue;
+    } else {
+        tg = tq;  // unused
+    }
+    const size_t smem = sizeof(ScanSmem) + 128;
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(kda_scan_seq_kernel<GM>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    dim3 grid((unsigned)(a.H * kColBlocks), (unsigned)a.seq.N);
+    kda_scan_seq_kernel<GM><<<grid, kScanThreads, smem, s>>>(a, tq, tk, tg, tv);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_scan_seq(const ScanArgs& a, cudaStream_t s) {
+    if (a.seq.N == 0) return cudaSuccess;
+    if (a.seq.total_rows == 0) {
+        // no tokens at all: the state passes through unchanged
+        const size_t bytes = (size_t)a.seq.N * a.H * kHeadDim * kHeadDim * sizeof(float);
+        return cudaMemcpyAsync(a.state_out, a.state_in, bytes, cudaMemcpyDeviceToDevice, s);
+    }
+    return a.gate_mode == 0 ? launch_t<0>(a, s) : launch_t<1>(a, s);
+}
+
+}  // namespace kda

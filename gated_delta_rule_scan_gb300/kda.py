@@ -1,0 +1,189 @@
+"""ctypes binding of libkda (include/kda.h): argument marshalling only.
+
+Each function has the name of the C entry point it calls and takes torch tensors where the C call
+takes device pointers; it passes ``tensor.data_ptr()``, the shape integers and the CUDA stream
+(default: torch's current stream on the tensors' device), and raises ``KdaError`` on a non-zero
+status.  No step of the method runs here: every value is computed by the CUDA kernels behind the
+ABI.  Importing this module loads the library and fails loudly when it is missing.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libkda.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"libkda.so not found at {LIB_PATH}; build it first "
+        "(python -c 'import __graft_entry__ as g; g.build()')")
+_lib = ctypes.CDLL(LIB_PATH)
+
+DTYPE_F32, DTYPE_BF16 = 0, 1
+GATE_PER_CHANNEL, GATE_PER_HEAD = 0, 1
+ALGO_AUTO, ALGO_SEQ, ALGO_CHUNK = 0, 1, 2
+HEAD_DIM = 128
+DECODE_MAX_T = 16
+
+_P, _I, _F, _L, _Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_long, ctypes.c_size_t
+
+_lib.kda_abi_version.restype = _I
+_lib.kda_status_string.restype = ctypes.c_char_p
+_lib.kda_status_string.argtypes = [_I]
+_lib.kda_conv_l2norm_prep.restype = _I
+_lib.kda_conv_l2norm_prep.argtypes = [_P, _P, _P, _I, _P, _P, _P, _P, _P, _P, _I, _F, _P, _P, _P,
+                                      _P, _P, _P, _I, _I, _I, _I, _I, _F, _P]
+_lib.kda_conv_l2norm_prep_varlen.restype = _I
+_lib.kda_conv_l2norm_prep_varlen.argtypes = [_P, _P, _P, _I, _P, _P, _P, _P, _P, _P, _I, _F, _P,
+                                             _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F,
+                                             _P]
+_lib.kda_scan_workspace_bytes.restype = _Z
+_lib.kda_scan_workspace_bytes.argtypes = [_I, _I, _I, _I, _I, _I]
+_lib.kda_scan.restype = _I
+_lib.kda_scan.argtypes = [_P, _P, _P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P, _Z, _P]
+_lib.kda_scan_varlen.restype = _I
+_lib.kda_scan_varlen.argtypes = [_P, _P, _P, _P, _I, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F,
+                                 _I, _P, _Z, _P]
+_lib.kda_gated_rmsnorm_out.restype = _I
+_lib.kda_gated_rmsnorm_out.argtypes = [_P, _P, _P, _P, _L, _I, _F, _P]
+_lib.kda_decode_fused.restype = _I
+_lib.kda_decode_fused.argtypes = [_P, _P, _P, _I, _P, _P, _P, _P, _P, _P, _I, _F, _P, _P, _P, _P,
+                                  _P, _P, _I, _I, _I, _I, _I, _F, _F, _F, _P]
+_lib.kda_device_status.restype = _I
+_lib.kda_device_status.argtypes = [_P]
+
+# every symbol include/kda.h declares
+EXPORTED = ("kda_abi_version", "kda_status_string", "kda_conv_l2norm_prep",
+            "kda_conv_l2norm_prep_varlen", "kda_scan_workspace_bytes", "kda_scan",
+            "kda_scan_varlen", "kda_gated_rmsnorm_out", "kda_decode_fused", "kda_device_status")
+
+
+class KdaError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn} failed: status {status} ({status_string(status)})")
+
+
+def status_string(status: int) -> str:
+    return _lib.kda_status_string(int(status)).decode()
+
+
+def abi_version() -> int:
+    return int(_lib.kda_abi_version())
+
+
+def library():
+    """The ctypes handle (for callers that pass raw pointers, e.g. host-side contract tests)."""
+    return _lib
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream, *tensors) -> int | None:
+    if stream is not None:
+        return stream if isinstance(stream, int) else stream.cuda_stream
+    for t in tensors:
+        if isinstance(t, torch.Tensor) and t.is_cuda:
+            return torch.cuda.current_stream(t.device).cuda_stream
+    return None
+
+
+def _check(fn: str, status: int):
+    if status != 0:
+        raise KdaError(fn, status)
+
+
+def _raw_dtype(t) -> int:
+    return DTYPE_BF16 if t.dtype == torch.bfloat16 else DTYPE_F32
+
+
+def kda_conv_l2norm_prep(q_raw, k_raw, v_raw, conv_w, ring_in, ring_out, f_raw, dt_bias, a_log,
+                         beta_raw, q_hat, k_hat, v_hat, g, beta, *, N, T, H, K=4, gate_mode=0,
+                         gate_lb=-5.0, l2_eps=1e-6, D=HEAD_DIM, stream=None):
+    st = _stream(stream, q_hat)
+    _check("kda_conv_l2norm_prep", _lib.kda_conv_l2norm_prep(
+        _ptr(q_raw), _ptr(k_raw), _ptr(v_raw), _raw_dtype(q_raw), _ptr(conv_w), _ptr(ring_in),
+        _ptr(ring_out), _ptr(f_raw), _ptr(dt_bias), _ptr(a_log), gate_mode, gate_lb,
+        _ptr(beta_raw), _ptr(q_hat), _ptr(k_hat), _ptr(v_hat), _ptr(g), _ptr(beta), N, T, H, D, K,
+        l2_eps, st))
+
+
+def kda_conv_l2norm_prep_varlen(q_raw, k_raw, v_raw, conv_w, ring_in, ring_out, f_raw, dt_bias,
+                                a_log, beta_raw, q_hat, k_hat, v_hat, g, beta, cu_seqlens,
+                                cu_seqlens_host, *, H, K=4, gate_mode=0, gate_lb=-5.0,
+                                l2_eps=1e-6, D=HEAD_DIM, stream=None):
+    """cu_seqlens: int32 device tensor [N+1]; cu_seqlens_host: int32 CPU tensor [N+1]."""
+    N = cu_seqlens_host.numel() - 1
+    total = int(cu_seqlens_host[-1])
+    st = _stream(stream, q_hat)
+    _check("kda_conv_l2norm_prep_varlen", _lib.kda_conv_l2norm_prep_varlen(
+        _ptr(q_raw), _ptr(k_raw), _ptr(v_raw), _raw_dtype(q_raw), _ptr(conv_w), _ptr(ring_in),
+        _ptr(ring_out), _ptr(f_raw), _ptr(dt_bias), _ptr(a_log), gate_mode, gate_lb,
+        _ptr(beta_raw), _ptr(q_hat), _ptr(k_hat), _ptr(v_hat), _ptr(g), _ptr(beta),
+        _ptr(cu_seqlens), _ptr(cu_seqlens_host), N, total, H, D, K, l2_eps, st))
+
+
+def kda_scan_workspace_bytes(N, total_T, H, gate_mode=0, algo=ALGO_AUTO, D=HEAD_DIM) -> int:
+    return int(_lib.kda_scan_workspace_bytes(N, total_T, H, D, gate_mode, algo))
+
+
+def kda_scan(q_hat, k_hat, v_hat, g, beta, state_in, state_out, o, *, N, T, H, gate_mode=0,
+             scale=None, algo=ALGO_AUTO, workspace=None, D=HEAD_DIM, stream=None):
+    scale = D ** -0.5 if scale is None else scale
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = _stream(stream, state_out)
+    _check("kda_scan", _lib.kda_scan(
+        _ptr(q_hat), _ptr(k_hat), _ptr(v_hat), _ptr(g), gate_mode, _ptr(beta), _ptr(state_in),
+        _ptr(state_out), _ptr(o), N, T, H, D, scale, algo, _ptr(workspace), ws_bytes, st))
+
+
+def kda_scan_varlen(q_hat, k_hat, v_hat, g, beta, state_in, state_out, o, cu_seqlens,
+                    cu_seqlens_host, *, H, gate_mode=0, scale=None, algo=ALGO_AUTO,
+                    workspace=None, D=HEAD_DIM, stream=None):
+    N = cu_seqlens_host.numel() - 1
+    total = int(cu_seqlens_host[-1])
+    scale = D ** -0.5 if scale is None else scale
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = _stream(stream, state_out)
+    _check("kda_scan_varlen", _lib.kda_scan_varlen(
+        _ptr(q_hat), _ptr(k_hat), _ptr(v_hat), _ptr(g), gate_mode, _ptr(beta), _ptr(state_in),
+        _ptr(state_out), _ptr(o), _ptr(cu_seqlens), _ptr(cu_seqlens_host), N, total, H, D, scale,
+        algo, _ptr(workspace), ws_bytes, st))
+
+
+def kda_gated_rmsnorm_out(o, norm_w, gate_raw, y, *, rows, eps=1e-6, D=HEAD_DIM, stream=None):
+    st = _stream(stream, y)
+    _check("kda_gated_rmsnorm_out", _lib.kda_gated_rmsnorm_out(
+        _ptr(o), _ptr(norm_w), _ptr(gate_raw), _ptr(y), rows, D, eps, st))
+
+
+def kda_decode_fused(q_raw, k_raw, v_raw, conv_w, ring_in, ring_out, f_raw, dt_bias, a_log,
+                     beta_raw, state_in, state_out, norm_w, gate_raw, y, *, N, T, H, K=4,
+                     gate_mode=0, gate_lb=-5.0, l2_eps=1e-6, scale=None, rms_eps=1e-6,
+                     D=HEAD_DIM, stream=None):
+    scale = D ** -0.5 if scale is None else scale
+    st = _stream(stream, y)
+    _check("kda_decode_fused", _lib.kda_decode_fused(
+        _ptr(q_raw), _ptr(k_raw), _ptr(v_raw), _raw_dtype(q_raw), _ptr(conv_w), _ptr(ring_in),
+        _ptr(ring_out), _ptr(f_raw), _ptr(dt_bias), _ptr(a_log), gate_mode, gate_lb,
+        _ptr(beta_raw), _ptr(state_in), _ptr(state_out), _ptr(norm_w), _ptr(gate_raw), _ptr(y),
+        N, T, H, D, K, l2_eps, scale, rms_eps, st))
+
+
+def kda_device_status(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device error word status."""
+    if stream is None and torch.cuda.is_available():
+        stream = torch.cuda.current_stream().cuda_stream
+    elif stream is not None and not isinstance(stream, int):
+        stream = stream.cuda_stream
+    return int(_lib.kda_device_status(stream))

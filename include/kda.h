@@ -1,0 +1,204 @@
+/*
+ * kda.h -- C ABI of libkda: the Kimi Delta Attention (KDA) gated delta-rule mixer and its
+ * scalar-gate special case, Gated DeltaNet (GDN), on one NVIDIA GB300 (sm_103a).
+ *
+ * The method is the one the docs.rs page "memra_engine/kda.rs" (memra-engine 0.125.0) describes
+ * in its module doc and in kda_core_gated stages 2-6; GDN semantics follow the page
+ * "aprender-serve 0.70.2 src/cuda/executor/gdn_ops.rs".  Conventions follow the C-ABI launcher
+ * pattern of the page "memra_engine/mla_ffi.rs" (memra-engine 0.124.0), module doc:
+ *
+ *   - Every entry returns 0 on success, 10000 + cudaError_t when a CUDA call fails, and
+ *     40000 + n for a contract violation (codes below).  Contract checks run on the host before
+ *     anything is launched; a violating call launches nothing and touches no buffer.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).  Every call
+ *     is asynchronous on that stream; outputs are ready when the stream reaches the call.
+ *   - The caller owns all memory.  The library allocates nothing and keeps no state between calls
+ *     except one device-side error word (see kda_device_status) and cached function attributes.
+ *   - Pointers are device pointers unless the name ends in _host.  Pointers marked [16B] must be
+ *     16-byte aligned (40010 otherwise).
+ *
+ * Notation: N sequences, T tokens per sequence (or total_T packed rows for the varlen entries),
+ * H heads, D = head_dim = 128 (the only width built), C = H*D channels, K conv taps (2..8),
+ * R = K-1 ring slots.  Channel c = h*D + i is the (head, dim) pair ("Geometry" in the module doc),
+ * so every per-token tensor is token-major [rows, C] = [rows, H, D] with no repacking.
+ *   state  [N, H, D, D] f32, element [n][h][j][i] = S[i][j]: S has rows i = key dim and columns
+ *          j = value dim; the buffer stores it transposed, one value column per 512-byte row
+ *          (the "M[col][i]" layout of kda_core's doc).
+ *   ring   [N, 3C, R] f32, planes q, k, v at rows 0, C, 2C; slot 0 is the oldest raw sample.
+ *   conv_w [3C, K] f32, same plane order; tap K-1 multiplies the current token.
+ */
+#ifndef KDA_H
+#define KDA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* status codes */
+#define KDA_OK 0
+#define KDA_ERR_CUDA_BASE 10000       /* 10000 + cudaError_t */
+#define KDA_ERR_HEAD_DIM 40001        /* D != 128 */
+#define KDA_ERR_CONV_K 40002          /* K outside 2..8 while conv_w != NULL */
+#define KDA_ERR_STATE_ALIAS 40003     /* state_in and state_out overlap */
+#define KDA_ERR_NULL 40004            /* a required pointer is NULL */
+#define KDA_ERR_SHAPE 40005           /* negative size, H == 0, N or H > 65535, T too large */
+#define KDA_ERR_CU_SEQLENS 40006      /* cu_seqlens_host[0] != 0, decreasing, or last != total_T */
+#define KDA_ERR_ENUM 40007            /* unknown raw_dtype, gate_mode or algo */
+#define KDA_ERR_TIMEOUT 40008         /* a kernel gave up a bounded device wait (kda_device_status) */
+#define KDA_ERR_WORKSPACE 40009       /* workspace NULL or smaller than kda_scan_workspace_bytes */
+#define KDA_ERR_ALIGN 40010           /* a [16B] pointer is not 16-byte aligned */
+
+/* enums */
+#define KDA_DTYPE_F32 0
+#define KDA_DTYPE_BF16 1
+#define KDA_GATE_PER_CHANNEL 0        /* KDA: g is [rows, C] */
+#define KDA_GATE_PER_HEAD 1           /* GDN: g is [rows, H], broadcast over the key dim */
+#define KDA_ALGO_AUTO 0
+#define KDA_ALGO_SEQ 1
+#define KDA_ALGO_CHUNK 2
+
+#define KDA_HEAD_DIM 128
+#define KDA_DECODE_MAX_T 16
+
+/* ABI revision of this header; bumped on any signature change. */
+int kda_abi_version(void);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* kda_status_string(int status);
+
+/*
+ * kda_conv_l2norm_prep -- stages 2-4 of kda_core_gated: the scan's inputs from projected
+ * channels, for N sequences of T tokens each (rows = N*T, sequence n owns rows n*T .. n*T+T-1).
+ *
+ *   conv (Engine::kda_conv_silu, stage 2): for plane p and channel c, with xt = the ring slots of
+ *     (n, p, c) oldest first followed by the sequence's raw rows,
+ *         x_t = silu( sum_{j<K} conv_w[p*C+c][j] * xt[t+j] ), taps summed j ascending;
+ *   roll (Engine::kda_conv_ring_roll): ring_out = the last R entries of xt (raw values);
+ *   l2   (stage 3, constant KDA_L2_EPS): q_hat, k_hat = x / sqrt(sum_i x_i^2 + l2_eps) per (t, h);
+ *        v_hat = x (no norm);
+ *   gate (stage 4, Engine::kda_gate): gate_mode 0: g[t][c] = gate_lb * sigmoid(exp(a_log[h]) *
+ *        (f_raw[t][c] + dt_bias[c])); gate_mode 1 (gdn_ops.rs gdn_gates_into):
+ *        g[t][h] = -exp(a_log[h]) * softplus(f_raw[t][h] + dt_bias[h]); gate_lb is ignored;
+ *   beta = sigmoid(beta_raw) per (t, h).
+ *
+ * q_raw, k_raw, v_raw  [rows, C] in raw_dtype (KDA_DTYPE_F32 / KDA_DTYPE_BF16), read only.
+ * conv_w               [3C, K] f32, or NULL: no conv and no SiLU (x = raw), rings unused.
+ * ring_in, ring_out    [N, 3C, R] f32 (ignored when conv_w is NULL).  They may be the same
+ *                      buffer (in-place roll); otherwise they must not overlap.
+ * f_raw                [rows, C] (gate_mode 0) or [rows, H] (gate_mode 1) f32.
+ * dt_bias              [C] (gate_mode 0) or [H] (gate_mode 1) f32;  a_log [H] f32.
+ * beta_raw             [rows, H] f32.
+ * q_hat, k_hat, v_hat  [rows, C] f32 outputs [16B];  g: [rows, C] or [rows, H] f32 output [16B];
+ * beta                 [rows, H] f32 output.
+ * Returns 40001/40002/40004/40005/40007/40010 on contract violations.
+ */
+int kda_conv_l2norm_prep(const void* q_raw, const void* k_raw, const void* v_raw, int raw_dtype,
+                         const float* conv_w, const float* ring_in, float* ring_out,
+                         const float* f_raw, const float* dt_bias, const float* a_log,
+                         int gate_mode, float gate_lb, const float* beta_raw, float* q_hat,
+                         float* k_hat, float* v_hat, float* g, float* beta, int N, int T, int H,
+                         int D, int K, float l2_eps, void* stream);
+
+/*
+ * kda_conv_l2norm_prep_varlen -- kda_conv_l2norm_prep over N packed sequences of different
+ * lengths: sequence n owns rows cu_seqlens[n] .. cu_seqlens[n+1]-1 of every [rows, ...] array,
+ * and ring row n.  cu_seqlens is int32 [N+1] on the device (read by the kernels);
+ * cu_seqlens_host is the same array in host memory (validated: starts at 0, non-decreasing, ends
+ * at total_T; 40006 otherwise).  Empty sequences are allowed: their ring rows pass through.
+ */
+int kda_conv_l2norm_prep_varlen(const void* q_raw, const void* k_raw, const void* v_raw,
+                                int raw_dtype, const float* conv_w, const float* ring_in,
+                                float* ring_out, const float* f_raw, const float* dt_bias,
+                                const float* a_log, int gate_mode, float gate_lb,
+                                const float* beta_raw, float* q_hat, float* k_hat, float* v_hat,
+                                float* g, float* beta, const int* cu_seqlens,
+                                const int* cu_seqlens_host, int N, int total_T, int H, int D,
+                                int K, float l2_eps, void* stream);
+
+/*
+ * Workspace bytes kda_scan / kda_scan_varlen need for the given shape and algorithm
+ * (0 for KDA_ALGO_SEQ).  Returns 0 for invalid arguments.
+ */
+size_t kda_scan_workspace_bytes(int N, int total_T, int H, int D, int gate_mode, int algo);
+
+/*
+ * kda_scan -- stage 5 of kda_core_gated (Engine::kda_scan, "the per-channel-decay delta-rule
+ * scan"; module doc): for each sequence n and head h, for t = 0..T-1:
+ *     S <- Diag(exp g_t) S;   u = v_t - S^T k_t;   S <- S + beta_t k_t u^T;   o_t = scale S^T q_t
+ * starting from state_in[n][h] and leaving the final state in state_out[n][h].  With gate_mode 1
+ * the scalar g[t][h] decays every key-dim row alike (Gated DeltaNet).
+ *
+ * q_hat, k_hat, v_hat  [N*T, C] f32 [16B] (q_hat, k_hat normally l2-normalised).
+ * g                    [N*T, C] f32 [16B] (gate_mode 0) or [N*T, H] f32 (gate_mode 1): raw
+ *                      log-decay; the scan applies exp.
+ * beta                 [N*T, H] f32.
+ * state_in, state_out  [N, H, D, D] f32 [16B], distinct, non-overlapping buffers (40003).
+ * o                    [N*T, C] f32 output [16B].
+ * scale                readout scale, normally 1/sqrt(D) (the reference's query scale, applied to
+ *                      the readout only).
+ * algo                 KDA_ALGO_SEQ: register-resident sequential scan; the T-token call equals T
+ *                      chained one-token calls bit for bit.  KDA_ALGO_AUTO picks the faster form
+ *                      for the shape.  KDA_ALGO_CHUNK: chunked form (needs workspace).
+ * workspace            device scratch of at least kda_scan_workspace_bytes(...) bytes [16B], or
+ *                      NULL when that is 0.
+ * T == 0 copies state_in to state_out.
+ */
+int kda_scan(const float* q_hat, const float* k_hat, const float* v_hat, const float* g,
+             int gate_mode, const float* beta, const float* state_in, float* state_out,
+             float* o, int N, int T, int H, int D, float scale, int algo, void* workspace,
+             size_t workspace_bytes, void* stream);
+
+/*
+ * kda_scan_varlen -- kda_scan over N packed sequences (rows cu_seqlens[n] .. cu_seqlens[n+1]-1,
+ * state row n); cu_seqlens / cu_seqlens_host as in kda_conv_l2norm_prep_varlen.  An empty
+ * sequence copies its state through.
+ */
+int kda_scan_varlen(const float* q_hat, const float* k_hat, const float* v_hat, const float* g,
+                    int gate_mode, const float* beta, const float* state_in, float* state_out,
+                    float* o, const int* cu_seqlens, const int* cu_seqlens_host, int N,
+                    int total_T, int H, int D, float scale, int algo, void* workspace,
+                    size_t workspace_bytes, void* stream);
+
+/*
+ * kda_gated_rmsnorm_out -- stage 6 of kda_core_gated (Engine::kda_gated_rmsnorm): per row of D
+ * values, y_i = o_i / sqrt(mean_i o_i^2 + eps) * norm_w[i] * sigmoid(gate_raw_i).  KDA gates with
+ * sigmoid; the gate is not normalised.
+ * o, gate_raw, y   [rows, D] f32 [16B] (rows = tokens * heads);  norm_w [D] f32 [16B], shared by
+ * all heads.  y may alias o.
+ */
+int kda_gated_rmsnorm_out(const float* o, const float* norm_w, const float* gate_raw, float* y,
+                          long rows, int D, float eps, void* stream);
+
+/*
+ * kda_decode_fused -- one decode step (T = 1) or a T-token speculative verify (2 <= T <= 16) of
+ * N sequences in ONE launch: kda_conv_l2norm_prep + kda_scan + kda_gated_rmsnorm_out with the
+ * same arguments, computed without round-tripping the intermediates through memory.  Its outputs
+ * equal those three calls bit for bit, and a T-token call equals T chained one-token calls bit
+ * for bit (the decode == verify identity of the KDA module doc).
+ * Argument meanings and layouts as in the three calls; rows = N*T; conv_w must not be NULL.
+ * ring_in / ring_out may alias; state_in / state_out must not overlap.
+ * norm_w [D] [16B], gate_raw and y [rows, C] f32 [16B].  T outside 1..16 returns 40005.
+ */
+int kda_decode_fused(const void* q_raw, const void* k_raw, const void* v_raw, int raw_dtype,
+                     const float* conv_w, const float* ring_in, float* ring_out,
+                     const float* f_raw, const float* dt_bias, const float* a_log, int gate_mode,
+                     float gate_lb, const float* beta_raw, const float* state_in,
+                     float* state_out, const float* norm_w, const float* gate_raw, float* y,
+                     int N, int T, int H, int D, int K, float l2_eps, float scale, float rms_eps,
+                     void* stream);
+
+/*
+ * kda_device_status -- synchronises `stream`, then reports and clears the device error word on
+ * the current device: 0, or 40008 when a kernel gave up a bounded device wait since the last
+ * check (its outputs are then incomplete), or 10000 + cudaError_t.
+ */
+int kda_device_status(void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H */

@@ -1,0 +1,108 @@
+"""Host-side checks of the C ABI (no GPU): the library loads, exports every entry point that
+include/kda.h declares, and rejects contract violations before touching the device."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def kda():
+    from gated_delta_rule_scan_gb300 import _build
+    _build.build()
+    from gated_delta_rule_scan_gb300 import kda as mod
+    return mod
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "kda.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kda_\w+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(kda):
+    names = _declared()
+    assert len(names) >= 10
+    for n in names:
+        assert hasattr(kda.library(), n), n
+    assert sorted(kda.EXPORTED) == names
+
+
+def test_status_strings(kda):
+    assert kda.abi_version() == 1
+    for code in (0, 40001, 40002, 40003, 40004, 40005, 40006, 40007, 40008, 40009, 40010):
+        assert kda.status_string(code) not in ("unknown status",)
+    assert kda.status_string(10000 + 2) == "CUDA error"
+
+
+# The calls below carry fake (never dereferenced) pointers; every one violates a contract that
+# is checked on the host before any CUDA call, so none reaches the device.
+FAKE = 0x10000  # 16-byte aligned dummy address
+
+
+def test_scan_contract(kda):
+    lib = kda.library()
+    args = [FAKE] * 4 + [0, FAKE, FAKE, FAKE * 2, FAKE * 3]
+
+    def scan(**kw):
+        a = dict(N=1, T=4, H=2, D=128, scale=1.0, algo=1, gate_mode=0)
+        a.update(kw)
+        base = list(args)
+        base[4] = a["gate_mode"]
+        return lib.kda_scan(*base, a["N"], a["T"], a["H"], a["D"], ctypes.c_float(a["scale"]),
+                            a["algo"], None, 0, None)
+    assert scan(D=64) == 40001
+    assert scan(H=0) == 40005
+    assert scan(N=-1) == 40005
+    assert scan(T=-3) == 40005
+    assert scan(gate_mode=2) == 40007
+    assert scan(algo=7) == 40007
+    # state_in == state_out
+    a2 = [FAKE] * 4 + [0, FAKE, FAKE, FAKE, FAKE]
+    assert lib.kda_scan(*a2, 1, 4, 2, 128, ctypes.c_float(1.0), 1, None, 0, None) == 40003
+    # misaligned state
+    a3 = [FAKE] * 4 + [0, FAKE, FAKE + 4, FAKE * 8, FAKE]
+    assert lib.kda_scan(*a3, 1, 4, 2, 128, ctypes.c_float(1.0), 1, None, 0, None) == 40010
+    # null inputs with tokens present
+    a4 = [None] * 4 + [0, None, FAKE, FAKE * 8, None]
+    assert lib.kda_scan(*a4, 1, 4, 2, 128, ctypes.c_float(1.0), 1, None, 0, None) == 40004
+
+
+def test_varlen_cu_seqlens_contract(kda):
+    lib = kda.library()
+    a = [FAKE] * 4 + [0, FAKE, FAKE, FAKE * 8, FAKE]
+    for cu, total in (([1, 3, 5], 5), ([0, 3, 2], 2), ([0, 3, 5], 6)):
+        arr = (ctypes.c_int * len(cu))(*cu)
+        rc = lib.kda_scan_varlen(*a, FAKE, ctypes.cast(arr, ctypes.c_void_p), len(cu) - 1, total,
+                                 2, 128, ctypes.c_float(1.0), 1, None, 0, None)
+        assert rc == 40006, (cu, rc)
+    rc = lib.kda_scan_varlen(*a, None, None, 2, 5, 2, 128, ctypes.c_float(1.0), 1, None, 0, None)
+    assert rc == 40004
+
+
+def test_prep_and_decode_contract(kda):
+    lib = kda.library()
+    F = ctypes.c_float
+    prep = lambda **kw: lib.kda_conv_l2norm_prep(  # noqa: E731
+        FAKE, FAKE, FAKE, kw.get("dtype", 1), FAKE, FAKE, FAKE * 2, FAKE, FAKE, FAKE,
+        kw.get("gm", 0), F(-5.0), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 4, 2, kw.get("D", 128),
+        kw.get("K", 4), F(1e-6), None)
+    assert prep(D=96) == 40001
+    assert prep(K=1) == 40002
+    assert prep(K=9) == 40002
+    assert prep(dtype=5) == 40007
+    assert prep(gm=3) == 40007
+    dec = lambda **kw: lib.kda_decode_fused(  # noqa: E731
+        FAKE, FAKE, FAKE, 1, FAKE, FAKE, FAKE * 2, FAKE, FAKE, FAKE, 0, F(-5.0), FAKE, FAKE,
+        FAKE * 64, FAKE, FAKE, FAKE, 2, kw.get("T", 1), 2, 128, kw.get("K", 4), F(1e-6), F(0.1),
+        F(1e-6), None)
+    assert dec(T=0) == 40005
+    assert dec(T=17) == 40005
+    assert dec(K=12) == 40002
+    norm = lib.kda_gated_rmsnorm_out(FAKE, FAKE + 8, FAKE, FAKE, ctypes.c_long(4), 128, F(1e-6),
+                                     None)
+    assert norm == 40010
