@@ -143,6 +143,44 @@ def _traffic(kernel, files):
     return d.get("dram_bytes_per_launch")
 
 
+def _prefill_e2e(args, d, buf, state_out, ring_out, stream, barrier, max_over_ranks, mixer,
+                 algo, ws, T, H, C):
+    """Prefill through the public API with inputs copied from pinned host memory and y, the final
+    state and the ring read back every step."""
+    import torch
+
+    host = {k: v.cpu().pin_memory() for k, v in d.items() if v is not None}
+    dev_in = {k: torch.empty_like(v) for k, v in d.items() if v is not None}
+    y_host = torch.empty(T, C, dtype=torch.float32).pin_memory()
+    st_host = torch.empty_like(d["state_in"], device="cpu").pin_memory()
+    ring_host = torch.empty_like(d["ring_in"], device="cpu").pin_memory()
+    h2d_bytes = sum(v.numel() * v.element_size() for v in host.values())
+    d2h_bytes = sum(v.numel() * v.element_size() for v in (y_host, st_host, ring_host))
+
+    def e2e_step():
+        for k, v in host.items():
+            dev_in[k].copy_(v, non_blocking=True)
+        out = mixer.kda_forward(H=H, N=1, T=T, algo=algo, out=buf, state_out=state_out,
+                                ring_out=ring_out, **dev_in)
+        y_host.copy_(out["y"], non_blocking=True)
+        st_host.copy_(out["state_out"], non_blocking=True)
+        ring_host.copy_(out["ring_out"], non_blocking=True)
+
+    for _ in range(max(3, args.warmup // 4)):
+        e2e_step()
+    barrier()
+    Ke = max(3, args.steps // 10)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(Ke):
+        e2e_step()
+    e1.record(stream)
+    barrier()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1)) / Ke
+    return {"value": ws * T / (e2e_ms / 1e3), "unit": "tokens/s", "ms_per_step": e2e_ms,
+            "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes}
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -226,35 +264,10 @@ def run_ours(args):
     assert kda.kda_device_status() == 0
 
     # ---------------- prefill end to end from pinned host memory ----------------
-    host = {k: v.cpu().pin_memory() for k, v in d.items() if v is not None}
-    dev_in = {k: torch.empty_like(v) for k, v in d.items() if v is not None}
-    y_host = torch.empty(T, C, dtype=torch.float32).pin_memory()
-    st_host = torch.empty_like(d["state_in"], device="cpu").pin_memory()
-    ring_host = torch.empty_like(d["ring_in"], device="cpu").pin_memory()
-    h2d_bytes = sum(v.numel() * v.element_size() for v in host.values())
-    d2h_bytes = sum(v.numel() * v.element_size() for v in (y_host, st_host, ring_host))
-
-    def e2e_step():
-        for k, v in host.items():
-            dev_in[k].copy_(v, non_blocking=True)
-        out = mixer.kda_forward(H=H, N=1, T=T, algo=algo, out=buf, state_out=state_out,
-                                ring_out=ring_out, **dev_in)
-        y_host.copy_(out["y"], non_blocking=True)
-        st_host.copy_(out["state_out"], non_blocking=True)
-        ring_host.copy_(out["ring_out"], non_blocking=True)
-
-    for _ in range(max(3, args.warmup // 4)):
-        e2e_step()
-    barrier()
-    Ke = max(3, K // 10)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(Ke):
-        e2e_step()
-    e1.record(stream)
-    barrier()
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1)) / Ke
-    del host, dev_in
+    e2e = None
+    if not args.skip_e2e:
+        e2e = _prefill_e2e(args, d, buf, state_out, ring_out, stream, barrier, max_over_ranks,
+                           mixer, algo, ws, T, H, C)
 
     # ---------------- decode step (fused kernel) ----------------
     dec = inputs.decode_step(N=DEC_N, T=1, H=DEC_H)
@@ -294,7 +307,7 @@ def run_ours(args):
     if rank != 0:
         return None
 
-    cpu = cpu_baseline(pre, args.cpu_sample_heads)
+    cpu = None if args.skip_cpu else cpu_baseline(pre, args.cpu_sample_heads)
     return {
         "metric": METRIC, "value": tokens_per_s, "unit": "tokens/s", "n_gpus": ws,
         "steps": K, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
@@ -312,8 +325,7 @@ def run_ours(args):
                                          ["kda_scan_seq.cu", "kda_device.cuh"]),
                      "ms_per_launch": scan_ms, "flop_per_launch": scan_flop,
                      "peak_src": f"152 SMs x 128 FP32 lanes x 2 x {peaks['sm_max_mhz']:.0f} MHz"},
-        "e2e": {"value": ws * T / (e2e_ms / 1e3), "unit": "tokens/s", "ms_per_step": e2e_ms,
-                "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes},
+        "e2e": e2e,
         "decode": {"workload": "64 sequences x 1 token, H=64, fused decode kernel, states "
                                "ping-ponged (512 MiB working set)",
                    "ms_per_step": dec_ms, "seq_per_s": ws * DEC_N / (dec_ms / 1e3),
@@ -405,6 +417,8 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--cpu-sample-heads", type=int, default=16)
     ap.add_argument("--ref-steps", type=int, default=5)
+    ap.add_argument("--skip-e2e", action="store_true", help="profiling runs: no host-copy leg")
+    ap.add_argument("--skip-cpu", action="store_true", help="profiling runs: no oracle timing")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -82,7 +82,9 @@ def gpu_heads(out, inp: KdaInputs, heads):
     """The GPU outputs restricted to the listed heads (same layout as oracle_forward's)."""
     ch = torch.from_numpy(head_channels(heads, inp.D))
     C = inp.H * inp.D
-    res = dict(o=out["o"].cpu()[:, ch], state_out=out["state_out"].cpu()[:, heads])
+    res = dict(state_out=out["state_out"].cpu()[:, heads])
+    if out.get("o") is not None:
+        res["o"] = out["o"].cpu()[:, ch]
     if out.get("y") is not None:
         res["y"] = out["y"].cpu()[:, ch]
     if out.get("ring_out") is not None:
