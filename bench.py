@@ -222,6 +222,7 @@ def run_ours(args):
     state_out = torch.empty_like(d["state_in"])
     ring_out = torch.empty_like(d["ring_in"])
     algo = kda.ALGO_AUTO
+    gate_mode = kda.GATE_PER_CHANNEL | kda.GATE_EXP  # the prep hands decay factors to the scan
 
     ev = {}
 
@@ -229,11 +230,12 @@ def run_ours(args):
         kda.kda_conv_l2norm_prep(d["q_raw"], d["k_raw"], d["v_raw"], d["conv_w"], d["ring_in"],
                                  ring_out, d["f_raw"], d["dt_bias"], d["a_log"], d["beta_raw"],
                                  buf["q_hat"], buf["k_hat"], buf["v_hat"], buf["g"],
-                                 buf["beta"], N=1, T=T, H=H)
+                                 buf["beta"], N=1, T=T, H=H, gate_mode=gate_mode)
         if timed_scan is not None:
             timed_scan[0].record(stream)
         kda.kda_scan(buf["q_hat"], buf["k_hat"], buf["v_hat"], buf["g"], buf["beta"],
-                     d["state_in"], state_out, buf["o"], N=1, T=T, H=H, algo=algo)
+                     d["state_in"], state_out, buf["o"], N=1, T=T, H=H, gate_mode=gate_mode,
+                     algo=algo)
         if timed_scan is not None:
             timed_scan[1].record(stream)
         kda.kda_gated_rmsnorm_out(buf["o"], d["norm_w"], d["gate_raw"], buf["y"], rows=T * H)

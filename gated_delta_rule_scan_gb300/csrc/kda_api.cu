@@ -58,7 +58,7 @@ int prep_impl(const void* q_raw, const void* k_raw, const void* v_raw, int raw_d
     if (seq.N < 0 || seq.N > kMaxGridY || seq.total_rows < 0 || H <= 0 || H > kMaxGridY)
         return KDA_ERR_SHAPE;
     if (raw_dtype != KDA_DTYPE_F32 && raw_dtype != KDA_DTYPE_BF16) return KDA_ERR_ENUM;
-    if (gate_mode != KDA_GATE_PER_CHANNEL && gate_mode != KDA_GATE_PER_HEAD) return KDA_ERR_ENUM;
+    if (gate_mode < 0 || gate_mode > (KDA_GATE_PER_HEAD | KDA_GATE_EXP)) return KDA_ERR_ENUM;
     if (conv_w != nullptr && (K < 2 || K > kMaxConvK)) return KDA_ERR_CONV_K;
     if (seq.N == 0) return KDA_OK;
     if (conv_w != nullptr && (ring_in == nullptr || ring_out == nullptr)) return KDA_ERR_NULL;
@@ -90,7 +90,7 @@ int scan_impl(const float* q, const float* k, const float* v, const float* g, in
     (void)workspace; (void)workspace_bytes;
     if (D != kHeadDim) return KDA_ERR_HEAD_DIM;
     if (seq.N < 0 || seq.N > kMaxGridY || seq.total_rows < 0 || H <= 0) return KDA_ERR_SHAPE;
-    if (gate_mode != KDA_GATE_PER_CHANNEL && gate_mode != KDA_GATE_PER_HEAD) return KDA_ERR_ENUM;
+    if (gate_mode < 0 || gate_mode > (KDA_GATE_PER_HEAD | KDA_GATE_EXP)) return KDA_ERR_ENUM;
     if (algo != KDA_ALGO_AUTO && algo != KDA_ALGO_SEQ) return KDA_ERR_ENUM;
     if (seq.total_rows >= (1L << 31)) return KDA_ERR_SHAPE;
     if (seq.N == 0) return KDA_OK;
@@ -101,7 +101,7 @@ int scan_impl(const float* q, const float* k, const float* v, const float* g, in
     if (seq.total_rows > 0) {
         if (!q || !k || !v || !g || !beta || !o) return KDA_ERR_NULL;
         if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
-            (gate_mode == KDA_GATE_PER_CHANNEL && !aligned16(g)))
+            ((gate_mode & KDA_GATE_PER_HEAD) == 0 && !aligned16(g)))
             return KDA_ERR_ALIGN;
     }
     ScanArgs a{};

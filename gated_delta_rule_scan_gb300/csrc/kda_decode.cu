@@ -9,21 +9,19 @@
 // GB300 layout.  Decode is bound by the 64 KiB state read + write per (sequence, head), so one CTA
 // owns one (sequence, head) and issues its whole state column block as streaming 128-bit loads at
 // entry, before the prologue runs, so the HBM latency overlaps the conv / norm / gate work.  256
-// threads; 8 lanes per value column with 16 key-dim elements each (the same element layout and
-// the same per-token instruction sequence as the sequential prefill scan), 4 columns per lane.
+// threads; 8 lanes share 4 value columns with 16 key-dim elements each, and the per-token step is
+// the sequential prefill scan's (kda_scan_core.cuh), instruction for instruction.
 // The prologue and epilogue use the same device functions as the prep and epilogue kernels, so
 // this kernel's outputs equal prep + scan + gated-RMSNorm launched separately, bit for bit, and a
 // T-token launch equals T one-token launches bit for bit.
-#include "kda_device.cuh"
-#include "kda_internal.h"
+#include "kda_scan_core.cuh"
 
 namespace kda {
 
 constexpr int kDecThreads = 256;
-constexpr int kDecCPL = 4;  // value columns per lane
 
 template <bool BF16, int GATE_MODE>
-__global__ void __launch_bounds__(kDecThreads) kda_decode_fused_kernel(DecodeArgs a) {
+__global__ void __launch_bounds__(kDecThreads, 2) kda_decode_fused_kernel(DecodeArgs a) {
     __shared__ __align__(16) float qh[kDecodeMaxT][kHeadDim];
     __shared__ __align__(16) float kh[kDecodeMaxT][kHeadDim];
     __shared__ __align__(16) float av[kDecodeMaxT][kHeadDim];
@@ -43,16 +41,11 @@ __global__ void __launch_bounds__(kDecThreads) kda_decode_fused_kernel(DecodeArg
     const int grp = lane >> 3, r = lane & 7;
 
     // ---- issue the state loads first: 4 columns x 16 elements per lane -------------------
-    float4 S[kDecCPL][4];
-    const long hbase = ((long)n * H + h) * kHeadDim * kHeadDim;
-#pragma unroll
-    for (int c = 0; c < kDecCPL; ++c) {
-        const int j = warp * 16 + grp * 4 + c;
-#pragma unroll
-        for (int m = 0; m < 4; ++m)
-            S[c][m] = __ldcs(reinterpret_cast<const float4*>(a.state_in + hbase + (long)j * kHeadDim +
-                                                             4 * r + 32 * m));
-    }
+    const int cw = warp * 16 + grp * 4;      // the group's first column
+    const int own = cw + ((r >> 1) & 3);     // the column this lane reduces and writes
+    const long col0 = (((long)n * H + h) * kHeadDim + cw) * kHeadDim;
+    Col4 S;
+    col4_load(S, a.state_in + col0, r);
 
     // ---- prologue, q and k planes: thread = (plane tid/128, channel tid%128) ----------------
     {
@@ -137,76 +130,11 @@ __global__ void __launch_bounds__(kDecThreads) kda_decode_fused_kernel(DecodeArg
 
     // ---- the recurrence, token by token ---------------------------------------------------
     for (int t = 0; t < T; ++t) {
-        float4 k4[4], a4[4], q4[4];
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-            k4[m] = *reinterpret_cast<const float4*>(&kh[t][4 * r + 32 * m]);
-            if (GATE_MODE == 0) {
-                a4[m] = *reinterpret_cast<const float4*>(&av[t][4 * r + 32 * m]);
-            } else {
-                const float as = ascal[t];
-                a4[m] = make_float4(as, as, as, as);
-            }
-        }
-        float dk[kDecCPL];
-#pragma unroll
-        for (int c = 0; c < kDecCPL; ++c) {
-            float d[4];
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                S[c][m].x = __fmul_rn(a4[m].x, S[c][m].x);
-                S[c][m].y = __fmul_rn(a4[m].y, S[c][m].y);
-                S[c][m].z = __fmul_rn(a4[m].z, S[c][m].z);
-                S[c][m].w = __fmul_rn(a4[m].w, S[c][m].w);
-                float acc = __fmul_rn(S[c][m].x, k4[m].x);
-                acc = fmaf(S[c][m].y, k4[m].y, acc);
-                acc = fmaf(S[c][m].z, k4[m].z, acc);
-                acc = fmaf(S[c][m].w, k4[m].w, acc);
-                d[m] = acc;
-            }
-            dk[c] = (d[0] + d[1]) + (d[2] + d[3]);
-        }
-#pragma unroll
-        for (int c = 0; c < kDecCPL; ++c) dk[c] = group8_sum(dk[c]);
-#pragma unroll
-        for (int m = 0; m < 4; ++m) q4[m] = *reinterpret_cast<const float4*>(&qh[t][4 * r + 32 * m]);
-        const float bt = beta_s[t];
-        float dq[kDecCPL];
-#pragma unroll
-        for (int c = 0; c < kDecCPL; ++c) {
-            const int j = warp * 16 + grp * 4 + c;
-            const float u = vh[t][j] - dk[c];
-            const float w = __fmul_rn(bt, u);
-            float d[4];
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                S[c][m].x = fmaf(k4[m].x, w, S[c][m].x);
-                S[c][m].y = fmaf(k4[m].y, w, S[c][m].y);
-                S[c][m].z = fmaf(k4[m].z, w, S[c][m].z);
-                S[c][m].w = fmaf(k4[m].w, w, S[c][m].w);
-                float acc = __fmul_rn(S[c][m].x, q4[m].x);
-                acc = fmaf(S[c][m].y, q4[m].y, acc);
-                acc = fmaf(S[c][m].z, q4[m].z, acc);
-                acc = fmaf(S[c][m].w, q4[m].w, acc);
-                d[m] = acc;
-            }
-            dq[c] = (d[0] + d[1]) + (d[2] + d[3]);
-        }
-#pragma unroll
-        for (int c = 0; c < kDecCPL; ++c) {
-            dq[c] = group8_sum(dq[c]);
-            if (r == 0) os[t][warp * 16 + grp * 4 + c] = __fmul_rn(a.scale, dq[c]);
-        }
+        const float dq = col4_token<GATE_MODE == 0>(S, &kh[t][0], &av[t][0], ascal[t], &qh[t][0],
+                                                    vh[t][own], beta_s[t], r, lane);
+        if ((r & 1) == 0) os[t][own] = __fmul_rn(a.scale, dq);
     }
-    // ---- state out (streaming stores) -------------------------------------------------------
-#pragma unroll
-    for (int c = 0; c < kDecCPL; ++c) {
-        const int j = warp * 16 + grp * 4 + c;
-#pragma unroll
-        for (int m = 0; m < 4; ++m)
-            __stcs(reinterpret_cast<float4*>(a.state_out + hbase + (long)j * kHeadDim + 4 * r + 32 * m),
-                   S[c][m]);
-    }
+    col4_store(S, a.state_out + col0, r);
     __syncthreads();
     // ---- epilogue: gated RMSNorm, one warp per token row -----------------------------------
     for (int t = warp; t < T; t += kDecThreads / 32) {

@@ -84,7 +84,8 @@ __device__ __forceinline__ void window_fill(float (&win)[kMaxConvK], const void*
     }
 }
 
-template <bool BF16, int GATE_MODE, bool CONV>
+// EXP: write the decay factor exp(g) instead of the log-decay g.
+template <bool BF16, int GATE_MODE, bool CONV, bool EXP>
 __global__ void __launch_bounds__(kPrepThreads) kda_prep_kernel(PrepArgs a) {
     __shared__ float xs[2][kTileRows][kHeadDim];   // pre-norm q, k of the tile
     __shared__ float part[2][kPrepThreads / 32][kTileRows];
@@ -153,14 +154,18 @@ __global__ void __launch_bounds__(kPrepThreads) kda_prep_kernel(PrepArgs a) {
         }
         xs[0][t][i] = xq;
         xs[1][t][i] = xk;
-        if constexpr (GATE_MODE == 0)
-            a.g[r * C + c] = kda_gate_f(a.f_raw[r * C + c], a.dt_bias[c], rate, a.gate_lb);
+        if constexpr (GATE_MODE == 0) {
+            const float gl = kda_gate_f(a.f_raw[r * C + c], a.dt_bias[c], rate, a.gate_lb);
+            a.g[r * C + c] = EXP ? expf(gl) : gl;
+        }
     }
     if (i < nt) {
         const long r = r0 + i;
         a.beta[r * H + h] = sigmoid_f(a.beta_raw[r * H + h]);
-        if constexpr (GATE_MODE == 1)
-            a.g[r * H + h] = gdn_gate_f(a.f_raw[r * H + h], a.dt_bias[h], a.a_log[h]);
+        if constexpr (GATE_MODE == 1) {
+            const float gl = gdn_gate_f(a.f_raw[r * H + h], a.dt_bias[h], a.a_log[h]);
+            a.g[r * H + h] = EXP ? expf(gl) : gl;
+        }
     }
 
     // l2 norm of q and k over the head's 128 channels, one reduction per token
@@ -227,12 +232,12 @@ __global__ void __launch_bounds__(256) kda_ring_roll_kernel(PrepArgs a) {
     }
 }
 
-template <bool BF16, int GM, bool CONV>
+template <bool BF16, int GM, bool CONV, bool EXP>
 static cudaError_t launch_prep_t(const PrepArgs& a, cudaStream_t s) {
     const long tiles = (a.seq.total_rows + kTileRows - 1) / kTileRows;
     if (tiles > 0) {
         dim3 grid((unsigned)tiles, (unsigned)a.H);
-        kda_prep_kernel<BF16, GM, CONV><<<grid, kPrepThreads, 0, s>>>(a);
+        kda_prep_kernel<BF16, GM, CONV, EXP><<<grid, kPrepThreads, 0, s>>>(a);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
@@ -245,14 +250,24 @@ static cudaError_t launch_prep_t(const PrepArgs& a, cudaStream_t s) {
     return cudaSuccess;
 }
 
-cudaError_t launch_prep(const PrepArgs& a, cudaStream_t s) {
-    const bool conv = a.conv_w != nullptr;
-    if (a.raw_bf16) {
-        if (a.gate_mode == 0) return conv ? launch_prep_t<true, 0, true>(a, s) : launch_prep_t<true, 0, false>(a, s);
-        return conv ? launch_prep_t<true, 1, true>(a, s) : launch_prep_t<true, 1, false>(a, s);
+template <bool BF16, int GM, bool EXP>
+static cudaError_t launch_prep_c(const PrepArgs& a, cudaStream_t s) {
+    return a.conv_w != nullptr ? launch_prep_t<BF16, GM, true, EXP>(a, s)
+                               : launch_prep_t<BF16, GM, false, EXP>(a, s);
+}
+
+template <bool BF16>
+static cudaError_t launch_prep_b(const PrepArgs& a, cudaStream_t s) {
+    switch (a.gate_mode) {
+        case 0: return launch_prep_c<BF16, 0, false>(a, s);
+        case 1: return launch_prep_c<BF16, 1, false>(a, s);
+        case 2: return launch_prep_c<BF16, 0, true>(a, s);
+        default: return launch_prep_c<BF16, 1, true>(a, s);
     }
-    if (a.gate_mode == 0) return conv ? launch_prep_t<false, 0, true>(a, s) : launch_prep_t<false, 0, false>(a, s);
-    return conv ? launch_prep_t<false, 1, true>(a, s) : launch_prep_t<false, 1, false>(a, s);
+}
+
+cudaError_t launch_prep(const PrepArgs& a, cudaStream_t s) {
+    return a.raw_bf16 ? launch_prep_b<true>(a, s) : launch_prep_b<false>(a, s);
 }
 
 }  // namespace kda

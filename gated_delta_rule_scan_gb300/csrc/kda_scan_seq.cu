@@ -10,40 +10,42 @@
 //
 // GB300 layout.  Every value column j of S is an independent 128-vector recurrence, so the kernel
 // parallelises over (sequence, head, column) and keeps each column in registers for the whole
-// sequence: 8 lanes own one column, 16 key-dim elements each (i = 4r + 32m + e, r = lane in the
-// group, m, e = 0..3), so both dot products reduce over 8 lanes with 3 butterfly shuffles.  A CTA
-// owns 32 columns of one head (256 threads).  The per-token inputs that every column of the head
-// shares (q, k, g rows: 512 B each) and the CTA's 32 v values are staged by 2-D TMA tensor-map
-// loads into a double-buffered shared-memory ring of kScanTB-token blocks, completion tracked
-// by mbarriers (bounded waits); the next block streams in while the current one is scanned.
-// beta (and the GDN scalar gate) are register-prefetched one block ahead.  Outputs are buffered
-// per block in shared memory and written back as coalesced 128-byte rows.
+// sequence.  A CTA (2 warps) owns 32 columns of one head; within a warp, 8 lanes share 4 columns
+// and each lane holds 16 key-dim elements of all 4 (kda_scan_core.cuh), so each k / decay / q
+// value a lane loads from shared memory feeds 4 columns.  The per-token inputs every column of
+// the head shares (q, k, g rows: 512 B each) and the CTA's 32 v values are staged by 2-D TMA
+// tensor-map loads into a double-buffered shared-memory ring of kScanTB-token blocks, completion
+// tracked by mbarriers (bounded waits); the next block streams in while the current one is
+// scanned.  beta (and the GDN scalar gate) are register-prefetched one block ahead.  Outputs are
+// buffered per block in shared memory and written back as coalesced 128-byte rows.
 //
 // The in-kernel token loop is the chained one-token program: a T-token launch and T one-token
 // launches run the same instruction sequence per token, so their results are bit-identical.
-#include "kda_device.cuh"
-#include "kda_internal.h"
+#include "kda_scan_core.cuh"
 
 namespace kda {
 
-constexpr int kScanCols = 32;                   // value columns per CTA
-constexpr int kScanThreads = kScanCols * 8;     // 8 lanes per column
+constexpr int kScanWarps = 2;
+constexpr int kScanThreads = 32 * kScanWarps;
+constexpr int kScanCols = 16 * kScanWarps;      // value columns per CTA
 constexpr int kScanTB = 16;                     // tokens per staged block
 constexpr int kColBlocks = kHeadDim / kScanCols;
 
 struct __align__(128) ScanSmem {
     float q[2][kScanTB][kHeadDim];
     float k[2][kScanTB][kHeadDim];
-    float g[2][kScanTB][kHeadDim];      // per-channel log-decay (gate mode 0)
+    float g[2][kScanTB][kHeadDim];      // per-channel gate (log-decay, or decay factor)
     float v[2][kScanTB][kScanCols];
-    float a[kScanTB][kHeadDim];         // exp(g) of the block being scanned
+    float a[kScanTB][kHeadDim];         // exp(g) of the block being scanned (log-decay input)
     float obuf[kScanTB][kScanCols];
     float beta[2][kScanTB];
-    float ascal[2][kScanTB];            // exp(g) scalar (gate mode 1)
+    float ascal[2][kScanTB];            // per-head decay factor (gate mode 1)
     uint64_t bar[2];
 };
 
-template <int GATE_MODE>
+// GATE_MODE: 0 per-channel g [rows, C], 1 per-head g [rows, H].  EXP_DONE: g already holds the
+// decay factor exp(log-decay), so no exp is taken here.
+template <int GATE_MODE, bool EXP_DONE>
 __global__ void __launch_bounds__(kScanThreads)
 kda_scan_seq_kernel(ScanArgs a, const __grid_constant__ CUtensorMap tq,
                     const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tg,
@@ -53,11 +55,12 @@ kda_scan_seq_kernel(ScanArgs a, const __grid_constant__ CUtensorMap tq,
         (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
 
     const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31, grp = lane >> 3, r = lane & 7;
     const int cb = blockIdx.x % kColBlocks;
     const int h = blockIdx.x / kColBlocks;
     const int n = a.order ? a.order[blockIdx.y] : (int)blockIdx.y;
-    const int col = tid >> 3, r = tid & 7;
-    const int j = cb * kScanCols + col;
+    const int cw = warp * 16 + grp * 4;            // first of the group's 4 columns in the CTA
+    const int own = cw + ((r >> 1) & 3);           // the column this lane reduces and writes
     const int H = a.H;
     const long C = (long)H * kHeadDim;
 
@@ -72,11 +75,9 @@ kda_scan_seq_kernel(ScanArgs a, const __grid_constant__ CUtensorMap tq,
     const long L = end - begin;
     const int nblk = (int)((L + kScanTB - 1) / kScanTB);
 
-    // this lane's 16 elements of column j: S[m][e] = M[j][4r + 32m + e]
-    const long sbase = (((long)n * H + h) * kHeadDim + j) * kHeadDim + 4 * r;
-    float4 S[4];
-#pragma unroll
-    for (int m = 0; m < 4; ++m) S[m] = __ldcs(reinterpret_cast<const float4*>(a.state_in + sbase + 32 * m));
+    Col4 S;
+    const long col0 = (((long)n * H + h) * kHeadDim + cb * kScanCols + cw) * kHeadDim;
+    col4_load(S, a.state_in + col0, r);
 
     constexpr uint32_t kTxBytes =
         (GATE_MODE == 0 ? 3u : 2u) * kScanTB * kHeadDim * 4u + kScanTB * kScanCols * 4u;
@@ -114,7 +115,7 @@ kda_scan_seq_kernel(ScanArgs a, const __grid_constant__ CUtensorMap tq,
         const int nt = (int)min((long)kScanTB, L - (long)b * kScanTB);
         if (tid < kScanTB) {
             sm.beta[st][tid] = bpre;
-            if (GATE_MODE == 1) sm.ascal[st][tid] = expf(gpre);
+            if (GATE_MODE == 1) sm.ascal[st][tid] = EXP_DONE ? gpre : expf(gpre);
             const long rn = row0 + kScanTB + tid;
             if (rn < end) {
                 bpre = a.beta[rn * H + h];
@@ -124,62 +125,18 @@ kda_scan_seq_kernel(ScanArgs a, const __grid_constant__ CUtensorMap tq,
         const bool arrived = mbar_wait_bounded(&sm.bar[st], (uint32_t)((b >> 1) & 1), a.err);
         if (__syncthreads_or(!arrived)) return;  // device error word already raised
         if (tid == 0 && b + 1 < nblk) issue(b + 1, st ^ 1);
-        if (GATE_MODE == 0) {
+        if (GATE_MODE == 0 && !EXP_DONE) {
             for (int e = tid; e < nt * kHeadDim; e += kScanThreads)
                 (&sm.a[0][0])[e] = expf((&sm.g[st][0][0])[e]);
         }
         __syncthreads();
 
         for (int t = 0; t < nt; ++t) {
-            const float* kr = &sm.k[st][t][4 * r];
-            const float* qr = &sm.q[st][t][4 * r];
-            float4 k4[4], a4[4];
-#pragma unroll
-            for (int m = 0; m < 4; ++m) k4[m] = *reinterpret_cast<const float4*>(kr + 32 * m);
-            if (GATE_MODE == 0) {
-#pragma unroll
-                for (int m = 0; m < 4; ++m)
-                    a4[m] = *reinterpret_cast<const float4*>(&sm.a[t][4 * r + 32 * m]);
-            } else {
-                const float as = sm.ascal[st][t];
-#pragma unroll
-                for (int m = 0; m < 4; ++m) a4[m] = make_float4(as, as, as, as);
-            }
-            // decay, then S^T k with the decayed state
-            float d[4];
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                S[m].x = __fmul_rn(a4[m].x, S[m].x);
-                S[m].y = __fmul_rn(a4[m].y, S[m].y);
-                S[m].z = __fmul_rn(a4[m].z, S[m].z);
-                S[m].w = __fmul_rn(a4[m].w, S[m].w);
-                float acc = __fmul_rn(S[m].x, k4[m].x);
-                acc = fmaf(S[m].y, k4[m].y, acc);
-                acc = fmaf(S[m].z, k4[m].z, acc);
-                acc = fmaf(S[m].w, k4[m].w, acc);
-                d[m] = acc;
-            }
-            const float dk = group8_sum((d[0] + d[1]) + (d[2] + d[3]));
-            const float u = sm.v[st][t][col] - dk;
-            const float w = __fmul_rn(sm.beta[st][t], u);
-            // rank-1 update, then S^T q with the updated state
-            float4 q4[4];
-#pragma unroll
-            for (int m = 0; m < 4; ++m) q4[m] = *reinterpret_cast<const float4*>(qr + 32 * m);
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                S[m].x = fmaf(k4[m].x, w, S[m].x);
-                S[m].y = fmaf(k4[m].y, w, S[m].y);
-                S[m].z = fmaf(k4[m].z, w, S[m].z);
-                S[m].w = fmaf(k4[m].w, w, S[m].w);
-                float acc = __fmul_rn(S[m].x, q4[m].x);
-                acc = fmaf(S[m].y, q4[m].y, acc);
-                acc = fmaf(S[m].z, q4[m].z, acc);
-                acc = fmaf(S[m].w, q4[m].w, acc);
-                d[m] = acc;
-            }
-            const float dq = group8_sum((d[0] + d[1]) + (d[2] + d[3]));
-            if (r == 0) sm.obuf[t][col] = __fmul_rn(a.scale, dq);
+            const float* arow = EXP_DONE ? &sm.g[st][t][0] : &sm.a[t][0];
+            const float dq = col4_token<GATE_MODE == 0>(S, &sm.k[st][t][0], arow,
+                                                        sm.ascal[st][t], &sm.q[st][t][0],
+                                                        sm.v[st][t][own], sm.beta[st][t], r, lane);
+            if ((r & 1) == 0) sm.obuf[t][own] = __fmul_rn(a.scale, dq);
         }
         __syncthreads();
         for (int e = tid; e < nt * (kScanCols / 4); e += kScanThreads) {
@@ -188,8 +145,7 @@ kda_scan_seq_kernel(ScanArgs a, const __grid_constant__ CUtensorMap tq,
                 *reinterpret_cast<const float4*>(&sm.obuf[t][4 * c4]);
         }
     }
-#pragma unroll
-    for (int m = 0; m < 4; ++m) __stcs(reinterpret_cast<float4*>(a.state_out + sbase + 32 * m), S[m]);
+    col4_store(S, a.state_out + col0, r);
 }
 
 // ------------------------------------------------------------------------------------------
@@ -229,7 +185,7 @@ static bool make_map(CUtensorMap* m, const float* base, long rows, long cols, in
            CUDA_SUCCESS;
 }
 
-template <int GM>
+template <int GM, bool EXP>
 static cudaError_t launch_t(const ScanArgs& a, cudaStream_t s) {
     const long C = (long)a.H * kHeadDim;
     const long rows = a.seq.total_rows;
@@ -244,15 +200,18 @@ static cudaError_t launch_t(const ScanArgs& a, cudaStream_t s) {
         tg = tq;  // unused
     }
     const size_t smem = sizeof(ScanSmem) + 128;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(kda_scan_seq_kernel<GM>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    static int attr_done[64] = {0};  // per device
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64 || !attr_done[dev]) {
+        e = cudaFuncSetAttribute(kda_scan_seq_kernel<GM, EXP>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        attr_set = true;
+        if (dev >= 0 && dev < 64) attr_done[dev] = 1;
     }
     dim3 grid((unsigned)(a.H * kColBlocks), (unsigned)a.seq.N);
-    kda_scan_seq_kernel<GM><<<grid, kScanThreads, smem, s>>>(a, tq, tk, tg, tv);
+    kda_scan_seq_kernel<GM, EXP><<<grid, kScanThreads, smem, s>>>(a, tq, tk, tg, tv);
     return cudaGetLastError();
 }
 
@@ -263,7 +222,9 @@ cudaError_t launch_scan_seq(const ScanArgs& a, cudaStream_t s) {
         const size_t bytes = (size_t)a.seq.N * a.H * kHeadDim * kHeadDim * sizeof(float);
         return cudaMemcpyAsync(a.state_out, a.state_in, bytes, cudaMemcpyDeviceToDevice, s);
     }
-    return a.gate_mode == 0 ? launch_t<0>(a, s) : launch_t<1>(a, s);
+    const bool exp_done = (a.gate_mode & 2) != 0;
+    if ((a.gate_mode & 1) == 0) return exp_done ? launch_t<0, true>(a, s) : launch_t<0, false>(a, s);
+    return exp_done ? launch_t<1, true>(a, s) : launch_t<1, false>(a, s);
 }
 
 }  // namespace kda

@@ -25,6 +25,7 @@ _lib = ctypes.CDLL(LIB_PATH)
 
 DTYPE_F32, DTYPE_BF16 = 0, 1
 GATE_PER_CHANNEL, GATE_PER_HEAD = 0, 1
+GATE_EXP = 2  # flag: g holds decay factors exp(log-decay)
 ALGO_AUTO, ALGO_SEQ, ALGO_CHUNK = 0, 1, 2
 HEAD_DIM = 128
 DECODE_MAX_T = 16

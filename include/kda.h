@@ -56,6 +56,8 @@ extern "C" {
 #define KDA_DTYPE_BF16 1
 #define KDA_GATE_PER_CHANNEL 0        /* KDA: g is [rows, C] */
 #define KDA_GATE_PER_HEAD 1           /* GDN: g is [rows, H], broadcast over the key dim */
+#define KDA_GATE_EXP 2                /* flag, or-ed into gate_mode: g holds the decay factor
+                                         exp(log-decay) instead of the log-decay itself */
 #define KDA_ALGO_AUTO 0
 #define KDA_ALGO_SEQ 1
 #define KDA_ALGO_CHUNK 2
@@ -83,6 +85,8 @@ const char* kda_status_string(int status);
  *        (f_raw[t][c] + dt_bias[c])); gate_mode 1 (gdn_ops.rs gdn_gates_into):
  *        g[t][h] = -exp(a_log[h]) * softplus(f_raw[t][h] + dt_bias[h]); gate_lb is ignored;
  *   beta = sigmoid(beta_raw) per (t, h).
+ *   With KDA_GATE_EXP or-ed into gate_mode, g receives exp() of the gate above (the per-step
+ *   decay factor in (0, 1]), the form kda_scan consumes without taking exp itself.
  *
  * q_raw, k_raw, v_raw  [rows, C] in raw_dtype (KDA_DTYPE_F32 / KDA_DTYPE_BF16), read only.
  * conv_w               [3C, K] f32, or NULL: no conv and no SiLU (x = raw), rings unused.
@@ -133,7 +137,9 @@ size_t kda_scan_workspace_bytes(int N, int total_T, int H, int D, int gate_mode,
  *
  * q_hat, k_hat, v_hat  [N*T, C] f32 [16B] (q_hat, k_hat normally l2-normalised).
  * g                    [N*T, C] f32 [16B] (gate_mode 0) or [N*T, H] f32 (gate_mode 1): raw
- *                      log-decay; the scan applies exp.
+ *                      log-decay; the scan applies exp.  With KDA_GATE_EXP or-ed into gate_mode,
+ *                      g already holds the decay factors exp(log-decay) (as the prep emits them
+ *                      under the same flag) and the scan uses them as they are.
  * beta                 [N*T, H] f32.
  * state_in, state_out  [N, H, D, D] f32 [16B], distinct, non-overlapping buffers (40003).
  * o                    [N*T, C] f32 output [16B].

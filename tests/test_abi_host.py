@@ -59,7 +59,7 @@ def test_scan_contract(kda):
     assert scan(H=0) == 40005
     assert scan(N=-1) == 40005
     assert scan(T=-3) == 40005
-    assert scan(gate_mode=2) == 40007
+    assert scan(gate_mode=4) == 40007
     assert scan(algo=7) == 40007
     # state_in == state_out
     a2 = [FAKE] * 4 + [0, FAKE, FAKE, FAKE, FAKE]
@@ -95,7 +95,7 @@ def test_prep_and_decode_contract(kda):
     assert prep(K=1) == 40002
     assert prep(K=9) == 40002
     assert prep(dtype=5) == 40007
-    assert prep(gm=3) == 40007
+    assert prep(gm=4) == 40007
     dec = lambda **kw: lib.kda_decode_fused(  # noqa: E731
         FAKE, FAKE, FAKE, 1, FAKE, FAKE, FAKE * 2, FAKE, FAKE, FAKE, 0, F(-5.0), FAKE, FAKE,
         FAKE * 64, FAKE, FAKE, FAKE, 2, kw.get("T", 1), 2, 128, kw.get("K", 4), F(1e-6), F(0.1),

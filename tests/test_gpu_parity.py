@@ -131,9 +131,10 @@ def test_decode_fused_equals_unfused_bitwise():
     """The fused kernel and prep -> scan -> gated RMSNorm compute the same bits."""
     inp = inputs.decode_step(N=16, T=4, H=8, seed=12)
     fused = _decode(inp, 4)
-    unf = gpu_forward(inp, varlen=False, algo=1)
-    for k in ("y", "state_out", "ring_out"):
-        assert torch.equal(fused[k], unf[k]), k
+    for gate_exp in (False, True):
+        unf = gpu_forward(inp, varlen=False, algo=1, gate_exp=gate_exp)
+        for k in ("y", "state_out", "ring_out"):
+            assert torch.equal(fused[k], unf[k]), (k, gate_exp)
 
 
 def test_decode_in_place_ring():
@@ -156,10 +157,15 @@ def test_decode_in_place_ring():
 def test_prefill_small_ragged():
     """T = 4096-shaped workload shrunk to T=203 (ragged against the 16-token blocks), H=6."""
     inp = inputs.prefill(T=203, H=6)
-    out = gpu_forward(inp, algo=1)
+    out = gpu_forward(inp, algo=1, gate_exp=False)
     ref = oracle_forward(inp)
     _assert_close(out, ref, ("y", "o", "state_out", "ring_out"))
     _assert_close(out, ref, ("q_hat", "k_hat", "v_hat", "g", "beta"))
+    # the decay-factor hand-off computes the same bits, and its g is exp of the log-decay
+    out2 = gpu_forward(inp, algo=1, gate_exp=True)
+    for k in ("y", "o", "state_out", "ring_out", "q_hat", "k_hat", "v_hat", "beta"):
+        assert torch.equal(out[k], out2[k]), k
+    assert rel_linf(out2["g"], np.exp(ref["g"])) <= TOL
 
 
 @pytest.mark.slow
@@ -176,7 +182,7 @@ def test_scan_chain_bitwise():
     """kda_scan over T tokens equals T chained one-token kda_scan calls, bit for bit."""
     from gated_delta_rule_scan_gb300 import kda
     inp = inputs.decode_step(N=2, T=37, H=3, seed=14)
-    out = gpu_forward(inp, varlen=False, algo=1)
+    out = gpu_forward(inp, varlen=False, algo=1, gate_exp=False)
     N, T, H = 2, 37, 3
     C = H * 128
     q, k, v, g, b = (out[x].view(N, T, -1) for x in ("q_hat", "k_hat", "v_hat", "g", "beta"))
