@@ -20,7 +20,8 @@ namespace kda {
 
 constexpr int kDecThreads = 256;
 
-template <bool BF16, int GATE_MODE>
+// KW: register window width of the conv (4 when K <= 4, else 8).
+template <bool BF16, int GATE_MODE, int KW>
 __global__ void __launch_bounds__(kDecThreads, 2) kda_decode_fused_kernel(DecodeArgs a) {
     __shared__ __align__(16) float qh[kDecodeMaxT][kHeadDim];
     __shared__ __align__(16) float kh[kDecodeMaxT][kHeadDim];
@@ -29,7 +30,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) kda_decode_fused_kernel(Decode
     __shared__ __align__(16) float os[kDecodeMaxT][kHeadDim];
     __shared__ float beta_s[kDecodeMaxT];
     __shared__ float ascal[kDecodeMaxT];
-    __shared__ float part[2][4][kDecodeMaxT];
+    __shared__ float part[2][2][kDecodeMaxT];
     __shared__ float inv_s[2][kDecodeMaxT];
 
     const int h = blockIdx.x, n = blockIdx.y;
@@ -47,86 +48,81 @@ __global__ void __launch_bounds__(kDecThreads, 2) kda_decode_fused_kernel(Decode
     Col4 S;
     col4_load(S, a.state_in + col0, r);
 
-    // ---- prologue, q and k planes: thread = (plane tid/128, channel tid%128) ----------------
-    {
-        const int p = tid >> 7, i = tid & 127;
-        const int c = h * kHeadDim + i;
-        const void* raw = p == 0 ? a.q_raw : a.k_raw;
-        float wr[kMaxConvK], win[kMaxConvK];
-        const long ring_row = ((long)n * 3 * C + p * C + c) * R;
+    // ---- prologue: 64 threads per task, each on a channel pair (2i, 2i+1) --------------------
+    //      threads 0-63 q plane, 64-127 k plane, 128-191 v plane (+ beta), 192-255 the gate
+    const int task = tid >> 6, i0 = 2 * (tid & 63);
+    const int c = h * kHeadDim + i0;
+    if (task < 3) {
+        const void* raw = task == 0 ? a.q_raw : (task == 1 ? a.k_raw : a.v_raw);
+        float wr[2][KW], win[2][KW];
+        const long ring_row = ((long)n * 3 * C + task * C + c) * R;   // channel c; c+1 is R later
 #pragma unroll
-        for (int m = 0; m < kMaxConvK; ++m) {
-            const int jj = m - (kMaxConvK - K);
-            const int d = kMaxConvK - m;
-            wr[m] = jj >= 0 ? a.conv_w[(p * C + c) * K + jj] : 0.0f;
-            win[m] = d <= R ? a.ring_in[ring_row + (R - d)] : 0.0f;
-        }
-        float (*dst)[kHeadDim] = p == 0 ? qh : kh;
-        for (int t = 0; t < T; ++t) {
-            window_push(win, load_raw<BF16>(raw, (row0 + t) * C + c));
-            dst[t][i] = silu_f(conv_taps_f(wr, win, K));
-        }
+        for (int m = 0; m < KW; ++m) {
+            const int jj = m - (KW - K);
+            const int d = KW - m;
 #pragma unroll
-        for (int m = 0; m < kMaxConvK; ++m) {
-            const int d = kMaxConvK - 1 - m;  // win[m] = sample d steps before the last one
-            if (d < R) a.ring_out[ring_row + (R - 1 - d)] = win[m];
-        }
-    }
-    // ---- v plane (threads 0..127) and the gate (threads 128..255) -------------------------
-    if (tid < kHeadDim) {
-        const int i = tid, c = h * kHeadDim + i;
-        float wr[kMaxConvK], win[kMaxConvK];
-        const long ring_row = ((long)n * 3 * C + 2 * C + c) * R;
-#pragma unroll
-        for (int m = 0; m < kMaxConvK; ++m) {
-            const int jj = m - (kMaxConvK - K);
-            const int d = kMaxConvK - m;
-            wr[m] = jj >= 0 ? a.conv_w[(2 * C + c) * K + jj] : 0.0f;
-            win[m] = d <= R ? a.ring_in[ring_row + (R - d)] : 0.0f;
-        }
-        for (int t = 0; t < T; ++t) {
-            window_push(win, load_raw<BF16>(a.v_raw, (row0 + t) * C + c));
-            vh[t][i] = silu_f(conv_taps_f(wr, win, K));
-        }
-#pragma unroll
-        for (int m = 0; m < kMaxConvK; ++m) {
-            const int d = kMaxConvK - 1 - m;
-            if (d < R) a.ring_out[ring_row + (R - 1 - d)] = win[m];
-        }
-        if (i < T) {
-            beta_s[i] = sigmoid_f(a.beta_raw[(row0 + i) * H + h]);
-            if (GATE_MODE == 1)
-                ascal[i] = expf(gdn_gate_f(a.f_raw[(row0 + i) * H + h], a.dt_bias[h], a.a_log[h]));
-        }
-    } else if (GATE_MODE == 0) {
-        const int i = tid - kHeadDim, c = h * kHeadDim + i;
-        const float rate = expf(a.a_log[h]);
-        const float dt = a.dt_bias[c];
-        for (int t = 0; t < T; ++t)
-            av[t][i] = expf(kda_gate_f(a.f_raw[(row0 + t) * C + c], dt, rate, a.gate_lb));
-    }
-    __syncthreads();
-    // ---- l2 norm of q (warps 0-3) and k (warps 4-7) ----------------------------------------
-    {
-        const int p = tid >> 7, i = tid & 127;
-        float (*x)[kHeadDim] = p == 0 ? qh : kh;
-        for (int t = 0; t < T; ++t) {
-            const float v = x[t][i];
-            const float ssum = warp_sum(__fmul_rn(v, v));
-            if (lane == 0) part[p][warp & 3][t] = ssum;
-        }
-        __syncthreads();
-        if (tid < 2 * kDecodeMaxT) {
-            const int pl = tid / kDecodeMaxT, t = tid % kDecodeMaxT;
-            if (t < T) {
-                const float p4[4] = {part[pl][0][t], part[pl][1][t], part[pl][2][t], part[pl][3][t]};
-                inv_s[pl][t] = l2_inv_f(head_sum4(p4), a.l2_eps);
+            for (int e = 0; e < 2; ++e) {
+                wr[e][m] = jj >= 0 ? a.conv_w[(task * C + c + e) * K + jj] : 0.0f;
+                win[e][m] = d <= R ? a.ring_in[ring_row + e * R + (R - d)] : 0.0f;
             }
         }
-        __syncthreads();
-        for (int t = 0; t < T; ++t) x[t][i] = __fmul_rn(x[t][i], inv_s[p][t]);
-        __syncthreads();
+        float (*dst)[kHeadDim] = task == 0 ? qh : (task == 1 ? kh : vh);
+        for (int t = 0; t < T; ++t) {
+            const float2 x = load_raw2<BF16>(raw, (row0 + t) * C + c);
+            window_push(win[0], x.x);
+            window_push(win[1], x.y);
+            *reinterpret_cast<float2*>(&dst[t][i0]) =
+                make_float2(silu_f(conv_taps_f(wr[0], win[0], K)), silu_f(conv_taps_f(wr[1], win[1], K)));
+        }
+#pragma unroll
+        for (int m = 0; m < KW; ++m) {
+            const int d = KW - 1 - m;  // win[m] = sample d steps before the last one
+            if (d < R) {
+                a.ring_out[ring_row + (R - 1 - d)] = win[0][m];
+                a.ring_out[ring_row + R + (R - 1 - d)] = win[1][m];
+            }
+        }
+        if (task == 2 && (tid & 63) < T) {
+            const int t = tid & 63;
+            beta_s[t] = sigmoid_f(a.beta_raw[(row0 + t) * H + h]);
+            if (GATE_MODE == 1)
+                ascal[t] = expf(gdn_gate_f(a.f_raw[(row0 + t) * H + h], a.dt_bias[h], a.a_log[h]));
+        }
+    } else if (GATE_MODE == 0) {
+        const float rate = expf(a.a_log[h]);
+        const float2 dt = *reinterpret_cast<const float2*>(a.dt_bias + c);
+        for (int t = 0; t < T; ++t) {
+            const float2 f = *reinterpret_cast<const float2*>(a.f_raw + (row0 + t) * C + c);
+            *reinterpret_cast<float2*>(&av[t][i0]) =
+                make_float2(expf(kda_gate_f(f.x, dt.x, rate, a.gate_lb)),
+                            expf(kda_gate_f(f.y, dt.y, rate, a.gate_lb)));
+        }
     }
+    __syncthreads();
+    // ---- l2 norm of q (warps 0-1) and k (warps 2-3) ----------------------------------------
+    if (task < 2) {
+        float (*x)[kHeadDim] = task == 0 ? qh : kh;
+        for (int t = 0; t < T; ++t) {
+            const float2 v = *reinterpret_cast<const float2*>(&x[t][i0]);
+            const float ssum = warp_sum(pair_sumsq(v.x, v.y));
+            if (lane == 0) part[task][warp & 1][t] = ssum;
+        }
+    }
+    __syncthreads();
+    if (tid < 2 * kDecodeMaxT) {
+        const int pl = tid / kDecodeMaxT, t = tid % kDecodeMaxT;
+        if (t < T) inv_s[pl][t] = l2_inv_f(part[pl][0][t] + part[pl][1][t], a.l2_eps);
+    }
+    __syncthreads();
+    if (task < 2) {
+        float (*x)[kHeadDim] = task == 0 ? qh : kh;
+        for (int t = 0; t < T; ++t) {
+            const float2 v = *reinterpret_cast<const float2*>(&x[t][i0]);
+            *reinterpret_cast<float2*>(&x[t][i0]) =
+                make_float2(__fmul_rn(v.x, inv_s[task][t]), __fmul_rn(v.y, inv_s[task][t]));
+        }
+    }
+    __syncthreads();
 
     // ---- the recurrence, token by token ---------------------------------------------------
     for (int t = 0; t < T; ++t) {
@@ -156,15 +152,21 @@ __global__ void __launch_bounds__(kDecThreads, 2) kda_decode_fused_kernel(Decode
     }
 }
 
+template <bool BF16, int GM>
+static void launch_dec_t(const DecodeArgs& a, cudaStream_t s) {
+    dim3 grid((unsigned)a.H, (unsigned)a.N);
+    if (a.K <= 4) kda_decode_fused_kernel<BF16, GM, 4><<<grid, kDecThreads, 0, s>>>(a);
+    else kda_decode_fused_kernel<BF16, GM, kMaxConvK><<<grid, kDecThreads, 0, s>>>(a);
+}
+
 cudaError_t launch_decode_fused(const DecodeArgs& a, cudaStream_t s) {
     if (a.N == 0 || a.T == 0) return cudaSuccess;
-    dim3 grid((unsigned)a.H, (unsigned)a.N);
     if (a.raw_bf16) {
-        if (a.gate_mode == 0) kda_decode_fused_kernel<true, 0><<<grid, kDecThreads, 0, s>>>(a);
-        else kda_decode_fused_kernel<true, 1><<<grid, kDecThreads, 0, s>>>(a);
+        if (a.gate_mode == 0) launch_dec_t<true, 0>(a, s);
+        else launch_dec_t<true, 1>(a, s);
     } else {
-        if (a.gate_mode == 0) kda_decode_fused_kernel<false, 0><<<grid, kDecThreads, 0, s>>>(a);
-        else kda_decode_fused_kernel<false, 1><<<grid, kDecThreads, 0, s>>>(a);
+        if (a.gate_mode == 0) launch_dec_t<false, 0>(a, s);
+        else launch_dec_t<false, 1>(a, s);
     }
     return cudaGetLastError();
 }

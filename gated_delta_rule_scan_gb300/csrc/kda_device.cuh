@@ -58,22 +58,30 @@ __device__ __forceinline__ float gated_norm_f(float o, float inv, float w, float
     return __fmul_rn(__fmul_rn(__fmul_rn(o, inv), w), sigmoid_f(z));
 }
 
-// Causal conv taps over a register window win[0..kMaxConvK-1] whose last K slots hold the K
-// samples oldest first (win[kMaxConvK-1] = current token), weights wr likewise aligned to the
-// end.  Taps are accumulated oldest first, one fmaf each, starting from 0.
-__device__ __forceinline__ float conv_taps_f(const float (&wr)[kMaxConvK],
-                                             const float (&win)[kMaxConvK], int K) {
+// Causal conv taps over a register window win[0..KW-1] whose last K slots hold the K samples
+// oldest first (win[KW-1] = current token), weights wr likewise aligned to the end.  Taps are
+// accumulated oldest first, one fmaf each, starting from 0; the result does not depend on KW.
+template <int KW>
+__device__ __forceinline__ float conv_taps_f(const float (&wr)[KW], const float (&win)[KW], int K) {
     float acc = 0.0f;
 #pragma unroll
-    for (int m = 0; m < kMaxConvK; ++m)
-        if (m >= kMaxConvK - K) acc = fmaf(wr[m], win[m], acc);
+    for (int m = 0; m < KW; ++m)
+        if (m >= KW - K) acc = fmaf(wr[m], win[m], acc);
     return acc;
 }
 
-__device__ __forceinline__ void window_push(float (&win)[kMaxConvK], float x) {
+template <int KW>
+__device__ __forceinline__ void window_push(float (&win)[KW], float x) {
 #pragma unroll
-    for (int m = 0; m < kMaxConvK - 1; ++m) win[m] = win[m + 1];
-    win[kMaxConvK - 1] = x;
+    for (int m = 0; m < KW - 1; ++m) win[m] = win[m + 1];
+    win[KW - 1] = x;
+}
+
+// Sum of squares of a 128-channel head held as channel pairs (2i, 2i+1) by 64 consecutive
+// threads (two warps): each thread adds its pair, each warp reduces by butterfly, and the two
+// warp partials are added.  Both the prep and the fused decode kernel use this grouping.
+__device__ __forceinline__ float pair_sumsq(float x0, float x1) {
+    return __fmul_rn(x0, x0) + __fmul_rn(x1, x1);
 }
 
 // ------------------------------------------------------------------------------------------
@@ -95,9 +103,6 @@ __device__ __forceinline__ float group8_sum(float x) {
     return x;
 }
 
-// Sum of a 128-channel head held one channel per thread across 4 consecutive warps:
-// warp partials are combined in the fixed order ((p0 + p1) + p2) + p3.
-__device__ __forceinline__ float head_sum4(const float* p) { return ((p[0] + p[1]) + p[2]) + p[3]; }
 
 // ------------------------------------------------------------------------------------------
 // loads
@@ -109,6 +114,17 @@ __device__ __forceinline__ float load_raw(const void* base, long idx) {
         return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(base)[idx]);
     } else {
         return reinterpret_cast<const float*>(base)[idx];
+    }
+}
+
+// Two adjacent raw channels (idx even): one 4-byte bf16x2 or 8-byte float2 load.
+template <bool BF16>
+__device__ __forceinline__ float2 load_raw2(const void* base, long idx) {
+    if constexpr (BF16) {
+        return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(
+            reinterpret_cast<const __nv_bfloat16*>(base) + idx));
+    } else {
+        return *reinterpret_cast<const float2*>(reinterpret_cast<const float*>(base) + idx);
     }
 }
 
