@@ -43,7 +43,6 @@ __global__ void __launch_bounds__(kDecThreads, 2) kda_decode_fused_kernel(Decode
 
     // ---- issue the state loads first: 4 columns x 16 elements per lane -------------------
     const int cw = warp * 16 + grp * 4;      // the group's first column
-    const int own = cw + ((r >> 1) & 3);     // the column this lane reduces and writes
     const long col0 = (((long)n * H + h) * kHeadDim + cw) * kHeadDim;
     Col4 S;
     col4_load(S, a.state_in + col0, r);
@@ -86,7 +85,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) kda_decode_fused_kernel(Decode
             const int t = tid & 63;
             beta_s[t] = sigmoid_f(a.beta_raw[(row0 + t) * H + h]);
             if (GATE_MODE == 1)
-                ascal[t] = expf(gdn_gate_f(a.f_raw[(row0 + t) * H + h], a.dt_bias[h], a.a_log[h]));
+                ascal[t] = decay_f(gdn_gate_f(a.f_raw[(row0 + t) * H + h], a.dt_bias[h], a.a_log[h]));
         }
     } else if (GATE_MODE == 0) {
         const float rate = expf(a.a_log[h]);
@@ -94,8 +93,8 @@ __global__ void __launch_bounds__(kDecThreads, 2) kda_decode_fused_kernel(Decode
         for (int t = 0; t < T; ++t) {
             const float2 f = *reinterpret_cast<const float2*>(a.f_raw + (row0 + t) * C + c);
             *reinterpret_cast<float2*>(&av[t][i0]) =
-                make_float2(expf(kda_gate_f(f.x, dt.x, rate, a.gate_lb)),
-                            expf(kda_gate_f(f.y, dt.y, rate, a.gate_lb)));
+                make_float2(decay_f(kda_gate_f(f.x, dt.x, rate, a.gate_lb)),
+                            decay_f(kda_gate_f(f.y, dt.y, rate, a.gate_lb)));
         }
     }
     __syncthreads();
@@ -125,10 +124,21 @@ __global__ void __launch_bounds__(kDecThreads, 2) kda_decode_fused_kernel(Decode
     __syncthreads();
 
     // ---- the recurrence, token by token ---------------------------------------------------
-    for (int t = 0; t < T; ++t) {
-        const float dq = col4_token<GATE_MODE == 0>(S, &kh[t][0], &av[t][0], ascal[t], &qh[t][0],
-                                                    vh[t][own], beta_s[t], r, lane);
-        if ((r & 1) == 0) os[t][own] = __fmul_rn(a.scale, dq);
+    {
+        TokView vw;
+        vw.k = &kh[0][0];
+        vw.a = &av[0][0];
+        vw.q = &qh[0][0];
+        vw.a_scal = ascal;
+        vw.v = &vh[0][0];
+        vw.beta = beta_s;
+        vw.out = &os[0][0];
+        vw.row_stride = kHeadDim;
+        vw.v_stride = kHeadDim;
+        vw.v_col0 = cw;
+        vw.out_stride = kHeadDim;
+        vw.out_col0 = cw;
+        col4_tokens<GATE_MODE == 0, false>(S, T, vw, a.scale, r, lane);
     }
     col4_store(S, a.state_out + col0, r);
     __syncthreads();

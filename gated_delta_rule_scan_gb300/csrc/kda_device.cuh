@@ -22,20 +22,23 @@ constexpr int kWaitSpinLimit = 1 << 22;  // bounded mbarrier wait: ~1 s with the
 constexpr int kDevErrTimeout = 1;
 
 // ------------------------------------------------------------------------------------------
-// scalar maths (f32, IEEE expf / division / sqrt: the library is built without fast-math)
+// scalar maths (f32).  The elementwise prologue / epilogue functions use the hardware
+// exponential and reciprocal intrinsics (a few ulp; far inside the 1e-3 parity bound); the decay
+// factor exp(g) that the recurrence multiplies by uses the full-precision expf.
 // ------------------------------------------------------------------------------------------
 
-__device__ __forceinline__ float sigmoid_f(float x) { return 1.0f / (1.0f + expf(-x)); }
+__device__ __forceinline__ float sigmoid_f(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
 
 __device__ __forceinline__ float silu_f(float x) { return __fmul_rn(x, sigmoid_f(x)); }
 
 // log(1 + e^x) without overflow: max(x, 0) + log1p(e^-|x|)
 __device__ __forceinline__ float softplus_f(float x) {
-    return fmaxf(x, 0.0f) + log1pf(expf(-fabsf(x)));
+    return fmaxf(x, 0.0f) + log1pf(__expf(-fabsf(x)));
 }
 
 // KDA per-channel forget gate as a raw log-decay: lb * sigmoid(rate * (f + dt_bias)),
-// rate = exp(A_log[h]) computed once per head by the caller.
+// rate = exp(A_log[h]) computed once per head by the caller.  decay_f turns it into the factor
+// the recurrence multiplies the state by.
 __device__ __forceinline__ float kda_gate_f(float f, float dt_bias, float rate, float lb) {
     return __fmul_rn(lb, sigmoid_f(__fmul_rn(rate, f + dt_bias)));
 }
@@ -45,12 +48,14 @@ __device__ __forceinline__ float gdn_gate_f(float alpha, float dt_bias, float a_
     return -__fmul_rn(expf(a_log), softplus_f(alpha + dt_bias));
 }
 
+__device__ __forceinline__ float decay_f(float g) { return expf(g); }
+
 // 1 / sqrt(sum of squares + eps): the l2-norm scale (eps inside the sqrt, on the SUM).
-__device__ __forceinline__ float l2_inv_f(float ss, float eps) { return 1.0f / sqrtf(ss + eps); }
+__device__ __forceinline__ float l2_inv_f(float ss, float eps) { return rsqrtf(ss + eps); }
 
 // 1 / sqrt(mean of squares + eps) over 128 values: the RMSNorm scale.
 __device__ __forceinline__ float rms_inv_f(float ss, float eps) {
-    return 1.0f / sqrtf(__fmul_rn(ss, 1.0f / kHeadDim) + eps);
+    return rsqrtf(__fmul_rn(ss, 1.0f / kHeadDim) + eps);
 }
 
 // one gated-RMSNorm output element: ((o * inv) * w) * sigmoid(z)

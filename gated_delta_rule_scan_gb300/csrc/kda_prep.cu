@@ -193,7 +193,7 @@ __global__ void __launch_bounds__(kPrepThreads) kda_prep_kernel(PrepArgs a) {
                 if constexpr (GATE_MODE == 0) {
                     float g0 = kda_gate_f(fr[u].x, dtb.x, rate, a.gate_lb);
                     float g1 = kda_gate_f(fr[u].y, dtb.y, rate, a.gate_lb);
-                    if (EXP) { g0 = expf(g0); g1 = expf(g1); }
+                    if (EXP) { g0 = decay_f(g0); g1 = decay_f(g1); }
                     *reinterpret_cast<float2*>(a.g + r * C + c) = make_float2(g0, g1);
                 }
             }
@@ -204,7 +204,7 @@ __global__ void __launch_bounds__(kPrepThreads) kda_prep_kernel(PrepArgs a) {
         a.beta[r * H + h] = sigmoid_f(a.beta_raw[r * H + h]);
         if constexpr (GATE_MODE == 1) {
             const float gl = gdn_gate_f(a.f_raw[r * H + h], a.dt_bias[h], a.a_log[h]);
-            a.g[r * H + h] = EXP ? expf(gl) : gl;
+            a.g[r * H + h] = EXP ? decay_f(gl) : gl;
         }
     }
     __syncthreads();

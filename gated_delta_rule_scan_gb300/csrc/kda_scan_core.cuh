@@ -15,9 +15,9 @@
 // path below the FP32 pipe (one load per 4 x 4 flops instead of per 4 flops).  The elementwise
 // work uses Blackwell's paired f32x2 FMA/MUL (one instruction, two lanes of arithmetic).
 //
-// The two dot products reduce over the 8 lanes with a transposed butterfly: after exchanging
-// across xor 4 and xor 2 each lane keeps one column's partial sum, and xor 1 completes it, so
-// lanes 2c and 2c+1 of a group hold column c's full sum (4 shuffles instead of 12).
+// The dot products reduce over the 8 lanes with a transposed butterfly (reduce8_group8): one
+// reduction per token completes that token's S^T k for the 4 columns and the previous token's
+// S^T q, so the readout reduction is off the recurrence's critical path.
 #pragma once
 
 #include "kda_device.cuh"
@@ -55,90 +55,152 @@ __device__ __forceinline__ void col4_store(const Col4& S, float* col0, int r) {
         }
 }
 
-// Transposed butterfly over the 8 lanes of a group: d[c] are this lane's partial sums of the 4
-// columns; returns the full sum of column (r >> 1) & 3.
-__device__ __forceinline__ float reduce4_group8(const float (&d)[4], int r) {
-    const bool b2 = (r & 4) != 0, b1 = (r & 2) != 0;
-    const float x0 = b2 ? d[0] : d[2];
-    const float x1 = b2 ? d[1] : d[3];
-    const float y0 = __shfl_xor_sync(0xffffffffu, x0, 4);
-    const float y1 = __shfl_xor_sync(0xffffffffu, x1, 4);
-    const float k0 = (b2 ? d[2] : d[0]) + y0;
-    const float k1 = (b2 ? d[3] : d[1]) + y1;
-    const float x = b1 ? k0 : k1;
-    const float y = __shfl_xor_sync(0xffffffffu, x, 2);
-    float s = (b1 ? k1 : k0) + y;
-    s += __shfl_xor_sync(0xffffffffu, s, 1);
-    return s;
+// Transposed butterfly over the 8 lanes of a group for 8 values per lane: exchanging across
+// xor 4, xor 2 and xor 1 halves the values each lane keeps, so lane r ends with the full sum of
+// value index r.  Each index is summed over the same lanes in the same order whatever the other
+// indices hold.
+__device__ __forceinline__ float reduce8_group8(const float (&v)[8], int r) {
+    const bool b2 = (r & 4) != 0, b1 = (r & 2) != 0, b0 = (r & 1) != 0;
+    float k4[4];
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+        const float y = __shfl_xor_sync(0xffffffffu, b2 ? v[m] : v[4 + m], 4);
+        k4[m] = (b2 ? v[4 + m] : v[m]) + y;
+    }
+    float k2[2];
+#pragma unroll
+    for (int m = 0; m < 2; ++m) {
+        const float y = __shfl_xor_sync(0xffffffffu, b1 ? k4[m] : k4[2 + m], 2);
+        k2[m] = (b1 ? k4[2 + m] : k4[m]) + y;
+    }
+    const float y = __shfl_xor_sync(0xffffffffu, b0 ? k2[0] : k2[1], 1);
+    return (b0 ? k2[1] : k2[0]) + y;
 }
 
 __device__ __forceinline__ float sum4(const float2& a, const float2& b) {
     return (a.x + a.y) + (b.x + b.y);
 }
 
-// One token.  k_row, q_row: the token's 128 key-dim values (shared memory, 16-byte aligned);
-// a_row: its 128 decay factors (PER_CHANNEL) or ignored (a_scalar used instead); v_own: v of the
-// lane's own column (r >> 1) & 3; beta: the token's beta.  Returns S^T q (unscaled) of the own
-// column; lanes 2c and 2c+1 of a group return the same bits for column c.
+// The rows of one token that a lane reads: its 16 key-dim elements of k and of the decay.
+struct TokRows {
+    float4 k[4];
+    float4 a[4];
+};
+
 template <bool PER_CHANNEL>
-__device__ __forceinline__ float col4_token(Col4& S, const float* k_row, const float* a_row,
-                                            float a_scalar, const float* q_row, float v_own,
-                                            float beta, int r, int lane) {
-    float4 k4[4];
-    float2 acc[4][2];
-#pragma unroll
-    for (int c = 0; c < 4; ++c) acc[c][0] = acc[c][1] = make_float2(0.0f, 0.0f);
-    // decay, then S^T k with the decayed state
+__device__ __forceinline__ void load_rows(TokRows& R, const float* k_row, const float* a_row,
+                                          float a_scalar, int r) {
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
-        k4[m] = *reinterpret_cast<const float4*>(k_row + 4 * r + 32 * m);
-        float2 alo, ahi;
-        if (PER_CHANNEL) {
-            const float4 a4 = *reinterpret_cast<const float4*>(a_row + 4 * r + 32 * m);
-            alo = lo2(a4);
-            ahi = hi2(a4);
-        } else {
-            alo = ahi = make_float2(a_scalar, a_scalar);
+        R.k[m] = *reinterpret_cast<const float4*>(k_row + 4 * r + 32 * m);
+        R.a[m] = PER_CHANNEL ? *reinterpret_cast<const float4*>(a_row + 4 * r + 32 * m)
+                             : make_float4(a_scalar, a_scalar, a_scalar, a_scalar);
+    }
+}
+
+// Token-sequence view of shared memory for col4_tokens: row t of k / decay / q is at
+// k + t * row_stride (etc.), v of the group's column c at v + t * v_stride + v_col0 + c,
+// beta at beta[t], scalar decay at a_scal[t] (per-head gate), and the readout of column c goes
+// to out[t * out_stride + out_col0 + c] (already multiplied by scale).
+struct TokView {
+    const float* k;
+    const float* a;
+    const float* q;
+    const float* a_scal;
+    const float* v;
+    const float* beta;
+    float* out;
+    int row_stride, v_stride, v_col0, out_stride, out_col0;
+};
+
+// Runs tokens 0..nt-1 of the view through the recurrence for the 4 columns of this lane's group.
+// Per token: decay and S^T k partial sums; one 8-value reduction that completes this token's
+// S^T k together with the previous token's S^T q; w = beta (v - S^T k) from the lane owning each
+// column, shuffled to the group; rank-1 update and the S^T q partial sums.  The last token's
+// readout is completed by the same reduction with zeros in the key slots, so the bits of every
+// output depend only on the token, not on how a sequence is split into calls.
+// PREFETCH: load the next token's rows during the update (more registers, same values).
+template <bool PER_CHANNEL, bool PREFETCH>
+__device__ __forceinline__ void col4_tokens(Col4& S, int nt, const TokView& vw, float scale,
+                                            int r, int lane) {
+    if (nt <= 0) return;
+    const int c_own = r & 3;
+    const bool key_lane = r < 4;
+    float dqp[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    TokRows cur;
+    load_rows<PER_CHANNEL>(cur, vw.k, vw.a, PER_CHANNEL ? 0.0f : vw.a_scal[0], r);
+    for (int t = 0; t < nt; ++t) {
+        float2 acc[4][2];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc[c][0] = acc[c][1] = make_float2(0.0f, 0.0f);
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            const float2 alo = lo2(cur.a[m]), ahi = hi2(cur.a[m]);
+            const float2 klo = lo2(cur.k[m]), khi = hi2(cur.k[m]);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                S.s[c][2 * m] = __fmul2_rn(alo, S.s[c][2 * m]);
+                S.s[c][2 * m + 1] = __fmul2_rn(ahi, S.s[c][2 * m + 1]);
+                acc[c][0] = __ffma2_rn(S.s[c][2 * m], klo, acc[c][0]);
+                acc[c][1] = __ffma2_rn(S.s[c][2 * m + 1], khi, acc[c][1]);
+            }
         }
-        const float2 klo = lo2(k4[m]), khi = hi2(k4[m]);
+        float v8[8];
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-            S.s[c][2 * m] = __fmul2_rn(alo, S.s[c][2 * m]);
-            S.s[c][2 * m + 1] = __fmul2_rn(ahi, S.s[c][2 * m + 1]);
-            acc[c][0] = __ffma2_rn(S.s[c][2 * m], klo, acc[c][0]);
-            acc[c][1] = __ffma2_rn(S.s[c][2 * m + 1], khi, acc[c][1]);
+            v8[c] = sum4(acc[c][0], acc[c][1]);
+            v8[4 + c] = dqp[c];
+        }
+        const float red = reduce8_group8(v8, r);
+        if (t > 0 && !key_lane)
+            vw.out[(t - 1) * vw.out_stride + vw.out_col0 + c_own] = __fmul_rn(scale, red);
+        const float vt = vw.v[t * vw.v_stride + vw.v_col0 + c_own];
+        const float w = __fmul_rn(vw.beta[t], vt - red);   // meaningful in key lanes 0..3
+        float2 w2[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const float wc = __shfl_sync(0xffffffffu, w, (lane & ~7) | c);
+            w2[c] = make_float2(wc, wc);
+            acc[c][0] = acc[c][1] = make_float2(0.0f, 0.0f);
+        }
+        const float4* qrow = reinterpret_cast<const float4*>(vw.q + t * vw.row_stride + 4 * r);
+        TokRows nxt;
+        if (PREFETCH && t + 1 < nt)
+            load_rows<PER_CHANNEL>(nxt, vw.k + (t + 1) * vw.row_stride,
+                                   vw.a + (t + 1) * vw.row_stride,
+                                   PER_CHANNEL ? 0.0f : vw.a_scal[t + 1], r);
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            const float4 q4 = qrow[8 * m];
+            const float2 klo = lo2(cur.k[m]), khi = hi2(cur.k[m]);
+            const float2 qlo = lo2(q4), qhi = hi2(q4);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                S.s[c][2 * m] = __ffma2_rn(klo, w2[c], S.s[c][2 * m]);
+                S.s[c][2 * m + 1] = __ffma2_rn(khi, w2[c], S.s[c][2 * m + 1]);
+                acc[c][0] = __ffma2_rn(S.s[c][2 * m], qlo, acc[c][0]);
+                acc[c][1] = __ffma2_rn(S.s[c][2 * m + 1], qhi, acc[c][1]);
+            }
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c) dqp[c] = sum4(acc[c][0], acc[c][1]);
+        if (t + 1 < nt) {
+            if (PREFETCH)
+                cur = nxt;
+            else
+                load_rows<PER_CHANNEL>(cur, vw.k + (t + 1) * vw.row_stride,
+                                       vw.a + (t + 1) * vw.row_stride,
+                                       PER_CHANNEL ? 0.0f : vw.a_scal[t + 1], r);
         }
     }
-    float d[4];
-#pragma unroll
-    for (int c = 0; c < 4; ++c) d[c] = sum4(acc[c][0], acc[c][1]);
-    const float dk = reduce4_group8(d, r);
-    const float w = __fmul_rn(beta, v_own - dk);
-    // every lane of the group needs the 4 columns' w: column c's is held by lane 2c of the group
-    float2 w2[4];
+    float v8[8];
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
-        const float wc = __shfl_sync(0xffffffffu, w, (lane & ~7) | (2 * c));
-        w2[c] = make_float2(wc, wc);
-        acc[c][0] = acc[c][1] = make_float2(0.0f, 0.0f);
+        v8[c] = 0.0f;
+        v8[4 + c] = dqp[c];
     }
-    // rank-1 update, then S^T q with the updated state
-#pragma unroll
-    for (int m = 0; m < 4; ++m) {
-        const float4 q4 = *reinterpret_cast<const float4*>(q_row + 4 * r + 32 * m);
-        const float2 klo = lo2(k4[m]), khi = hi2(k4[m]);
-        const float2 qlo = lo2(q4), qhi = hi2(q4);
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            S.s[c][2 * m] = __ffma2_rn(klo, w2[c], S.s[c][2 * m]);
-            S.s[c][2 * m + 1] = __ffma2_rn(khi, w2[c], S.s[c][2 * m + 1]);
-            acc[c][0] = __ffma2_rn(S.s[c][2 * m], qlo, acc[c][0]);
-            acc[c][1] = __ffma2_rn(S.s[c][2 * m + 1], qhi, acc[c][1]);
-        }
-    }
-#pragma unroll
-    for (int c = 0; c < 4; ++c) d[c] = sum4(acc[c][0], acc[c][1]);
-    return reduce4_group8(d, r);
+    const float red = reduce8_group8(v8, r);
+    if (!key_lane) vw.out[(nt - 1) * vw.out_stride + vw.out_col0 + c_own] = __fmul_rn(scale, red);
 }
 
 }  // namespace kda

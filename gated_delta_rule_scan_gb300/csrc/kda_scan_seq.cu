@@ -60,7 +60,6 @@ kda_scan_seq_kernel(ScanArgs a, const __grid_constant__ CUtensorMap tq,
     const int h = blockIdx.x / kColBlocks;
     const int n = a.order ? a.order[blockIdx.y] : (int)blockIdx.y;
     const int cw = warp * 16 + grp * 4;            // first of the group's 4 columns in the CTA
-    const int own = cw + ((r >> 1) & 3);           // the column this lane reduces and writes
     const int H = a.H;
     const long C = (long)H * kHeadDim;
 
@@ -115,7 +114,7 @@ kda_scan_seq_kernel(ScanArgs a, const __grid_constant__ CUtensorMap tq,
         const int nt = (int)min((long)kScanTB, L - (long)b * kScanTB);
         if (tid < kScanTB) {
             sm.beta[st][tid] = bpre;
-            if (GATE_MODE == 1) sm.ascal[st][tid] = EXP_DONE ? gpre : expf(gpre);
+            if (GATE_MODE == 1) sm.ascal[st][tid] = EXP_DONE ? gpre : decay_f(gpre);
             const long rn = row0 + kScanTB + tid;
             if (rn < end) {
                 bpre = a.beta[rn * H + h];
@@ -127,17 +126,24 @@ kda_scan_seq_kernel(ScanArgs a, const __grid_constant__ CUtensorMap tq,
         if (tid == 0 && b + 1 < nblk) issue(b + 1, st ^ 1);
         if (GATE_MODE == 0 && !EXP_DONE) {
             for (int e = tid; e < nt * kHeadDim; e += kScanThreads)
-                (&sm.a[0][0])[e] = expf((&sm.g[st][0][0])[e]);
+                (&sm.a[0][0])[e] = decay_f((&sm.g[st][0][0])[e]);
         }
         __syncthreads();
 
-        for (int t = 0; t < nt; ++t) {
-            const float* arow = EXP_DONE ? &sm.g[st][t][0] : &sm.a[t][0];
-            const float dq = col4_token<GATE_MODE == 0>(S, &sm.k[st][t][0], arow,
-                                                        sm.ascal[st][t], &sm.q[st][t][0],
-                                                        sm.v[st][t][own], sm.beta[st][t], r, lane);
-            if ((r & 1) == 0) sm.obuf[t][own] = __fmul_rn(a.scale, dq);
-        }
+        TokView vw;
+        vw.k = &sm.k[st][0][0];
+        vw.a = EXP_DONE ? &sm.g[st][0][0] : &sm.a[0][0];
+        vw.q = &sm.q[st][0][0];
+        vw.a_scal = &sm.ascal[st][0];
+        vw.v = &sm.v[st][0][0];
+        vw.beta = &sm.beta[st][0];
+        vw.out = &sm.obuf[0][0];
+        vw.row_stride = kHeadDim;
+        vw.v_stride = kScanCols;
+        vw.v_col0 = cw;
+        vw.out_stride = kScanCols;
+        vw.out_col0 = cw;
+        col4_tokens<GATE_MODE == 0, true>(S, nt, vw, a.scale, r, lane);
         __syncthreads();
         for (int e = tid; e < nt * (kScanCols / 4); e += kScanThreads) {
             const int t = e / (kScanCols / 4), c4 = e % (kScanCols / 4);
