@@ -91,7 +91,7 @@ int scan_impl(const float* q, const float* k, const float* v, const float* g, in
     if (D != kHeadDim) return KDA_ERR_HEAD_DIM;
     if (seq.N < 0 || seq.N > kMaxGridY || seq.total_rows < 0 || H <= 0) return KDA_ERR_SHAPE;
     if (gate_mode < 0 || gate_mode > (KDA_GATE_PER_HEAD | KDA_GATE_EXP)) return KDA_ERR_ENUM;
-    if (algo != KDA_ALGO_AUTO && algo != KDA_ALGO_SEQ) return KDA_ERR_ENUM;
+    if (algo != KDA_ALGO_AUTO && algo != KDA_ALGO_SEQ && algo != KDA_ALGO_CHUNK) return KDA_ERR_ENUM;
     if (seq.total_rows >= (1L << 31)) return KDA_ERR_SHAPE;
     if (seq.N == 0) return KDA_OK;
     if (!state_in || !state_out) return KDA_ERR_NULL;
@@ -109,7 +109,9 @@ int scan_impl(const float* q, const float* k, const float* v, const float* g, in
     a.state_in = state_in; a.state_out = state_out; a.o = o;
     a.seq = seq; a.H = H; a.scale = scale; a.order = nullptr;
     a.err = dev_err_ptr();  // null only if the symbol lookup failed: waits then report nothing
-    return cuda_status(launch_scan_seq(a, static_cast<cudaStream_t>(stream)));
+    const bool chunk = algo == KDA_ALGO_CHUNK;
+    return cuda_status(chunk ? launch_scan_chunk(a, static_cast<cudaStream_t>(stream))
+                             : launch_scan_seq(a, static_cast<cudaStream_t>(stream)));
 }
 
 }  // namespace

@@ -3,6 +3,7 @@
 // cudaError_t of its launch(es).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -57,6 +58,11 @@ struct DecodeArgs {
 
 cudaError_t launch_prep(const PrepArgs& a, cudaStream_t s);
 cudaError_t launch_scan_seq(const ScanArgs& a, cudaStream_t s);
+cudaError_t launch_scan_chunk(const ScanArgs& a, cudaStream_t s);
+
+// 2-D f32 tensor map over [rows, cols] (row stride = cols), box [box_rows, box_cols], no swizzle.
+bool make_tensor_map_2d(CUtensorMap* m, const float* base, long rows, long cols, int box_cols,
+                        int box_rows);
 cudaError_t launch_gated_rmsnorm(const NormArgs& a, cudaStream_t s);
 cudaError_t launch_decode_fused(const DecodeArgs& a, cudaStream_t s);
 

@@ -176,9 +176,8 @@ static EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// 2-D f32 tensor [rows, cols] (row stride = cols), box [box_rows, box_cols], no swizzle.
-static bool make_map(CUtensorMap* m, const float* base, long rows, long cols, int box_cols,
-                     int box_rows) {
+bool make_tensor_map_2d(CUtensorMap* m, const float* base, long rows, long cols, int box_cols,
+                        int box_rows) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
@@ -196,12 +195,12 @@ static cudaError_t launch_t(const ScanArgs& a, cudaStream_t s) {
     const long C = (long)a.H * kHeadDim;
     const long rows = a.seq.total_rows;
     CUtensorMap tq, tk, tg, tv;
-    if (!make_map(&tq, a.q, rows, C, kHeadDim, kScanTB) ||
-        !make_map(&tk, a.k, rows, C, kHeadDim, kScanTB) ||
-        !make_map(&tv, a.v, rows, C, kScanCols, kScanTB))
+    if (!make_tensor_map_2d(&tq, a.q, rows, C, kHeadDim, kScanTB) ||
+        !make_tensor_map_2d(&tk, a.k, rows, C, kHeadDim, kScanTB) ||
+        !make_tensor_map_2d(&tv, a.v, rows, C, kScanCols, kScanTB))
         return cudaErrorInvalidValue;
     if (GM == 0) {
-        if (!make_map(&tg, a.g, rows, C, kHeadDim, kScanTB)) return cudaErrorInvalidValue;
+        if (!make_tensor_map_2d(&tg, a.g, rows, C, kHeadDim, kScanTB)) return cudaErrorInvalidValue;
     } else {
         tg = tq;  // unused
     }

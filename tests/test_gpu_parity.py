@@ -42,9 +42,10 @@ def _assert_close(out, ref, keys, tol=TOL, ring_exact=True):
 # tiny KDA scan: 1 x 64 tokens, 4 heads, f32, no conv
 # ------------------------------------------------------------------------------------------
 
-def test_tiny_scan_full_path():
+@pytest.mark.parametrize("algo", [1, 2], ids=["seq", "chunk"])
+def test_tiny_scan_full_path(algo):
     inp = inputs.tiny_scan()
-    out = gpu_forward(inp, algo=1)
+    out = gpu_forward(inp, algo=algo)
     ref = oracle_forward(inp)
     _assert_close(out, ref, ("o", "state_out"))
 
@@ -168,11 +169,25 @@ def test_prefill_small_ragged():
     assert rel_linf(out2["g"], np.exp(ref["g"])) <= TOL
 
 
+@pytest.mark.parametrize("T", [1, 15, 16, 17, 203])
+def test_prefill_chunked_ragged(T):
+    """The chunked tensor-core form against the oracle: T below, at and above one 16-token chunk,
+    and many chunks with a ragged tail; random initial state and ring."""
+    inp = inputs.make_inputs(30 + T, H=3, N=2, T=T, raw_dtype="bf16", conv=True, ring="randn",
+                             state="randn", epilogue=True)
+    out = gpu_forward(inp, algo=2)
+    ref = oracle_forward(inp)
+    _assert_close(out, ref, ("y", "o", "state_out", "ring_out"))
+    out_e = gpu_forward(inp, algo=2, gate_exp=True)
+    _assert_close(out_e, ref, ("y", "o", "state_out"))
+
+
 @pytest.mark.slow
-def test_prefill_full_size():
+@pytest.mark.parametrize("algo", [1, 2], ids=["seq", "chunk"])
+def test_prefill_full_size(algo):
     """T=4096, H=64 (the prefill benchmark workload), every head against the oracle."""
     inp = inputs.prefill()
-    out = gpu_forward(inp, algo=0)
+    out = gpu_forward(inp, algo=algo)
     heads = list(range(0, 64, 4))
     ref = oracle_forward(inp, heads=heads)
     _assert_close(gpu_heads(out, inp, heads), ref, ("y", "o", "state_out", "ring_out"))
@@ -223,20 +238,22 @@ def _varlen_inputs(lengths, seed, H=4):
     return inp
 
 
-def test_varlen_edge_lengths():
+@pytest.mark.parametrize("algo", [1, 2], ids=["seq", "chunk"])
+def test_varlen_edge_lengths(algo):
     """Empty sequences, lengths below the conv window (1, 2), a length equal to it (3), lengths
     straddling the 16-row tiles and blocks."""
     inp = _varlen_inputs([5, 0, 1, 2, 3, 17, 0, 33, 16], seed=21)
-    out = gpu_forward(inp, varlen=True, algo=1)
+    out = gpu_forward(inp, varlen=True, algo=algo)
     ref = oracle_forward(inp)
     _assert_close(out, ref, ("y", "o", "state_out", "ring_out"))
 
 
-def test_varlen_split_resume_state_carry():
+@pytest.mark.parametrize("algo", [1, 2], ids=["seq", "chunk"])
+def test_varlen_split_resume_state_carry(algo):
     """Run each sequence's prefix, then its suffix from the saved (state, ring): the result
     matches the unsplit run (GPU vs GPU) and the oracle."""
     inp = inputs.varlen_prefill(N=6, lo=20, hi=300, H=4, seed=22)
-    full = gpu_forward(inp, varlen=True, algo=1)
+    full = gpu_forward(inp, varlen=True, algo=algo)
     cu = inp.cu_seqlens
     P = inp.split_points
     L = np.diff(cu)
@@ -254,14 +271,14 @@ def test_varlen_split_resume_state_carry():
     for k in ("q_raw", "k_raw", "v_raw", "f_raw", "beta_raw", "gate_raw"):
         setattr(a, k, getattr(inp, k)[sel_a])
     a.cu_seqlens = cu_a
-    out_a = gpu_forward(a, varlen=True, algo=1)
+    out_a = gpu_forward(a, varlen=True, algo=algo)
     b = copy.copy(inp)
     for k in ("q_raw", "k_raw", "v_raw", "f_raw", "beta_raw", "gate_raw"):
         setattr(b, k, getattr(inp, k)[sel_b])
     b.cu_seqlens = cu_b
     b.state_in = out_a["state_out"].cpu()
     b.ring_in = out_a["ring_out"].cpu()
-    out_b = gpu_forward(b, varlen=True, algo=1)
+    out_b = gpu_forward(b, varlen=True, algo=algo)
     y_split = torch.empty_like(full["y"])
     y_split[sel_a.cuda()] = out_a["y"]
     y_split[sel_b.cuda()] = out_b["y"]
@@ -273,10 +290,11 @@ def test_varlen_split_resume_state_carry():
 
 
 @pytest.mark.slow
-def test_varlen_full_size_sampled_heads():
+@pytest.mark.parametrize("algo", [1, 2], ids=["seq", "chunk"])
+def test_varlen_full_size_sampled_heads(algo):
     """16 sequences with lengths U[256, 8192] at H=64, sampled heads against the oracle."""
     inp = inputs.varlen_prefill()
-    out = gpu_forward(inp, varlen=True, algo=0)
+    out = gpu_forward(inp, varlen=True, algo=algo)
     heads = [0, 21, 42, 63]
     ref = oracle_forward(inp, heads=heads)
     _assert_close(gpu_heads(out, inp, heads), ref, ("y", "o", "state_out", "ring_out"))
@@ -286,10 +304,11 @@ def test_varlen_full_size_sampled_heads():
 # Gated DeltaNet special case
 # ------------------------------------------------------------------------------------------
 
+@pytest.mark.parametrize("algo", [1, 2], ids=["seq", "chunk"])
 @pytest.mark.parametrize("T,H", [(300, 4), pytest.param(16384, 32, marks=pytest.mark.slow)])
-def test_gdn_vs_both_oracles(T, H):
+def test_gdn_vs_both_oracles(T, H, algo):
     inp = inputs.gdn_long(T=T, H=H)
-    out = gpu_forward(inp, algo=0)
+    out = gpu_forward(inp, algo=algo)
     heads = list(range(H)) if H <= 4 else [0, 11, 22, 31]
     g = gpu_heads(out, inp, heads)
     ref_kda = oracle_forward(inp, heads=heads)
