@@ -221,8 +221,9 @@ def run_ours(args):
                o=f32(T, C), y=f32(T, C))
     state_out = torch.empty_like(d["state_in"])
     ring_out = torch.empty_like(d["ring_in"])
-    algo = kda.ALGO_AUTO
-    gate_mode = kda.GATE_PER_CHANNEL | kda.GATE_EXP  # the prep hands decay factors to the scan
+    algo = {"auto": kda.ALGO_AUTO, "seq": kda.ALGO_SEQ, "chunk": kda.ALGO_CHUNK}[args.scan_algo]
+    # the sequential form consumes decay factors, the chunked form log-decays
+    gate_mode = kda.GATE_PER_CHANNEL | (kda.GATE_EXP if algo == kda.ALGO_SEQ else 0)
 
     ev = {}
 
@@ -319,7 +320,8 @@ def run_ours(args):
                                " zero state and ring, full fused path",
                    "global_batch": ws, "seq_len": T, "heads": H, "head_dim": D,
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
-                   "scan_algo": "auto", "l2": "inputs larger than L2 (470 MB read per step)"},
+                   "scan_algo": args.scan_algo,
+                   "l2": "inputs larger than L2 (470 MB read per step)"},
         "gpu_launches": launches_per_step * K,
         "roofline": {"bound": "alu", "kernel": "kda_scan_seq_kernel", "achieved": scan_tflops,
                      "peak": fp32_peak, "unit": "TFLOP/s", "frac": scan_tflops / fp32_peak,
@@ -419,6 +421,8 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--cpu-sample-heads", type=int, default=16)
     ap.add_argument("--ref-steps", type=int, default=5)
+    ap.add_argument("--scan-algo", choices=("auto", "seq", "chunk"), default="auto",
+                    help="prefill scan form (auto = the library's choice for the shape)")
     ap.add_argument("--skip-e2e", action="store_true", help="profiling runs: no host-copy leg")
     ap.add_argument("--skip-cpu", action="store_true", help="profiling runs: no oracle timing")
     args = ap.parse_args()
