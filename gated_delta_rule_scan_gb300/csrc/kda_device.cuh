@@ -172,12 +172,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Bounded wait on an mbarrier phase.  Returns false (and raises the device error word) when the
-// phase has not completed after ~1 s; the caller then stops issuing work and returns.
+// Bounded wait on an mbarrier phase.  try_wait itself suspends the thread for a while before it
+// reports "not yet", so the loop does not spin hot; after kWaitSpinLimit tries (seconds) it
+// gives up, raises the device error word and returns false, and the caller stops issuing work.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, int* err) {
     for (int it = 0; it < kWaitSpinLimit; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
-        if (it > 32) __nanosleep(256);
+        if (it > 1024) __nanosleep(64);
     }
     if (err) atomicOr(err, kDevErrTimeout);
     return false;

@@ -80,6 +80,7 @@ struct __align__(1024) ChunkSmem {
     float beta[2][kCc];
     float gs[2][kCc];            // per-head gate of the chunk (GDN), cumulative after phase 1
     float cref[128];             // per-channel reference: half the chunk's total log-decay
+    float ecr[128];              // e^{cref}
     float egc[128];              // e^{G_C}: the chunk's total decay per channel
     float amat[kCc][kCc];        // beta_t A[t][s], strictly lower
     uint64_t bar_tma[2];
@@ -104,24 +105,37 @@ __device__ __forceinline__ void put1(unsigned char (&im)[2][BYTES], uint32_t off
 // store 8 consecutive-k values (one 16-byte core-matrix row) at byte offset off
 template <int BYTES>
 __device__ __forceinline__ void put8(unsigned char (&im)[2][BYTES], uint32_t off, const float (&x)[8]) {
-    __align__(16) __nv_bfloat16 hi[8], lo[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) split_bf16(x[e], hi[e], lo[e]);
-    *reinterpret_cast<uint4*>(&im[0][off]) = *reinterpret_cast<const uint4*>(hi);
-    *reinterpret_cast<uint4*>(&im[1][off]) = *reinterpret_cast<const uint4*>(lo);
+    uint4 hi, lo;
+    split_bf16x2(x[0], x[1], hi.x, lo.x);
+    split_bf16x2(x[2], x[3], hi.y, lo.y);
+    split_bf16x2(x[4], x[5], hi.z, lo.z);
+    split_bf16x2(x[6], x[7], hi.w, lo.w);
+    *reinterpret_cast<uint4*>(&im[0][off]) = hi;
+    *reinterpret_cast<uint4*>(&im[1][off]) = lo;
 }
 
-// D (+)= A * B^T in bf16x3: hi*hi + hi*lo + lo*hi, nks K-steps of 16.
-__device__ __forceinline__ void mma_x3(uint32_t d, uint32_t a_hi, uint32_t a_lo, uint32_t sbo_a,
-                                       uint32_t b_hi, uint32_t b_lo, uint32_t sbo_b, int nks,
+// A pair of descriptors (hi, lo) of one operand image.
+struct DescPair {
+    uint64_t hi, lo;
+};
+
+template <int BYTES>
+__device__ __forceinline__ DescPair desc_pair(unsigned char (&im)[2][BYTES], uint32_t byte_off,
+                                              uint32_t sbo) {
+    return {tc_smem_desc(smem_u32(im[0]) + byte_off, 128, sbo),
+            tc_smem_desc(smem_u32(im[1]) + byte_off, 128, sbo)};
+}
+
+// D (+)= A * B^T in bf16x3: hi*hi + hi*lo + lo*hi, nks K-steps of 16 (256 bytes each).
+__device__ __forceinline__ void mma_x3(uint32_t d, DescPair A, DescPair B, int nks,
                                        uint32_t idesc) {
-    const uint32_t as[3] = {a_hi, a_hi, a_lo};
-    const uint32_t bs[3] = {b_hi, b_lo, b_hi};
+    const uint64_t as[3] = {A.hi, A.hi, A.lo};
+    const uint64_t bs[3] = {B.hi, B.lo, B.hi};
 #pragma unroll
     for (int p = 0; p < 3; ++p)
         for (int ks = 0; ks < nks; ++ks)
-            tc_mma_ss(d, tc_smem_desc(as[p] + ks * 256, 128, sbo_a),
-                      tc_smem_desc(bs[p] + ks * 256, 128, sbo_b), idesc, p > 0 || ks > 0);
+            tc_mma_ss(d, tc_desc_advance(as[p], 256 * ks), tc_desc_advance(bs[p], 256 * ks), idesc,
+                      p > 0 || ks > 0);
 }
 
 // GATE_MODE 0 per-channel, 1 per-head; EXP: g holds decay factors (take log first)
@@ -206,6 +220,12 @@ kda_scan_chunk_kernel(ScanArgs a, const __grid_constant__ CUtensorMap tq,
 
     const uint32_t idA = tc_idesc_bf16(128, 32), idB = tc_idesc_bf16(128, 16);
     const uint32_t id2 = tc_idesc_bf16(128, 144);
+    const DescPair dKB = desc_pair(sm.kb, 0, kSboK128), dBI0 = desc_pair(sm.bi, 0, kSboK128);
+    const DescPair dBI32 = desc_pair(sm.bi, 4 * kSboK128, kSboK128);
+    const DescPair dA1 = desc_pair(sm.a1, 0, kSboK128);
+    const DescPair dKT = desc_pair(sm.kt, 0, kSboK16), dVT = desc_pair(sm.vt, 0, kSboK16);
+    const DescPair dTM = desc_pair(sm.tm, 0, kSboK16), dB2 = desc_pair(sm.b2, 0, kSboK16);
+    const DescPair dA2 = desc_pair(sm.a2, 0, kSboK16);
     uint32_t mma_phase = 0;
     bool failed = false;
     auto mma_wait = [&]() -> bool {
@@ -255,6 +275,7 @@ kda_scan_chunk_kernel(ScanArgs a, const __grid_constant__ CUtensorMap tq,
                 sm.g[st][t][tid] = G;
             }
             sm.cref[tid] = 0.5f * G;
+            sm.ecr[tid] = __expf(0.5f * G);
             sm.egc[tid] = decay_f(G);
             if (G < -170.0f && a.err) atomicOr(a.err, kDevErrRange);
         } else if (tid == 0) {
@@ -269,56 +290,78 @@ kda_scan_chunk_kernel(ScanArgs a, const __grid_constant__ CUtensorMap tq,
         if (GATE_MODE == 1) sm.egc[tid] = decay_f(sm.cref[0]);
 
         // ---- phase 2: operand images --------------------------------------------------------
-        // row images (row = token, 8 consecutive channels per work item)
-        for (int it = tid; it < 64 * 16; it += kChThreads) {
-            const int row = it >> 4, k0 = (it & 15) * 8;   // row 0..63 over 4 images of 16
-            const int img = row >> 4, t = row & 15;
-            float x[8];
-            const bool live = t < nt;
+        // row images: item = (token t, channels k0..k0+7); one exp pair feeds all four images
+        for (int it = tid; it < kCc * 16; it += kChThreads) {
+            const int t = it >> 4, k0 = (it & 15) * 8;
+            float xb[8], xk[8], xq[8], xg[8];
+            if (t < nt) {
+                const float4* K4 = reinterpret_cast<const float4*>(&sm.k[st][t][k0]);
+                const float4* Q4 = reinterpret_cast<const float4*>(&sm.q[st][t][k0]);
+                const float kv[8] = {K4[0].x, K4[0].y, K4[0].z, K4[0].w, K4[1].x, K4[1].y, K4[1].z, K4[1].w};
+                const float qv[8] = {Q4[0].x, Q4[0].y, Q4[0].z, Q4[0].w, Q4[1].x, Q4[1].y, Q4[1].z, Q4[1].w};
+                if (GATE_MODE == 0) {
+                    const float4* G4 = reinterpret_cast<const float4*>(&sm.g[st][t][k0]);
+                    const float4* C4 = reinterpret_cast<const float4*>(&sm.cref[k0]);
+                    const float4* E4 = reinterpret_cast<const float4*>(&sm.ecr[k0]);
+                    const float gv[8] = {G4[0].x, G4[0].y, G4[0].z, G4[0].w, G4[1].x, G4[1].y, G4[1].z, G4[1].w};
+                    const float cv[8] = {C4[0].x, C4[0].y, C4[0].z, C4[0].w, C4[1].x, C4[1].y, C4[1].z, C4[1].w};
+                    const float ev[8] = {E4[0].x, E4[0].y, E4[0].z, E4[0].w, E4[1].x, E4[1].y, E4[1].z, E4[1].w};
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const int kk = k0 + e;
-                float val = 0.0f;
-                if (live) {
-                    const float G = GATE_MODE == 0 ? sm.g[st][t][kk] : sm.gs[st][t];
-                    const float cr = GATE_MODE == 0 ? sm.cref[kk] : 0.0f;
-                    if (img == 0) val = sm.k[st][t][kk] * (GATE_MODE == 0 ? __expf(cr - G) : 1.0f);
-                    else if (img == 1) val = sm.k[st][t][kk] * (GATE_MODE == 0 ? __expf(G - cr) : 1.0f);
-                    else if (img == 2) val = sm.q[st][t][kk] * (GATE_MODE == 0 ? __expf(G - cr) : 1.0f);
-                    else val = sm.q[st][t][kk] * __expf(G);
+                    for (int e = 0; e < 8; ++e) {
+                        const float ef = __expf(gv[e] - cv[e]);   // e^{G-c}
+                        const float eb = __expf(cv[e] - gv[e]);   // e^{c-G}
+                        xb[e] = kv[e] * eb;
+                        xk[e] = kv[e] * ef;
+                        xq[e] = qv[e] * ef;
+                        xg[e] = qv[e] * (ef * ev[e]);             // Q e^{G}
+                    }
+                } else {
+                    const float eg = __expf(sm.gs[st][t]);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        xb[e] = kv[e];
+                        xk[e] = kv[e];
+                        xq[e] = qv[e];
+                        xg[e] = qv[e] * eg;
+                    }
                 }
-                x[e] = val;
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) xb[e] = xk[e] = xq[e] = xg[e] = 0.0f;
             }
-            if (img == 0) put8(sm.kb, img_off(t, k0, kSboK128), x);
-            else put8(sm.bi, img_off(row - 16, k0, kSboK128), x);  // bi rows 0..47
+            put8(sm.kb, img_off(t, k0, kSboK128), xb);
+            put8(sm.bi, img_off(t, k0, kSboK128), xk);
+            put8(sm.bi, img_off(16 + t, k0, kSboK128), xq);
+            put8(sm.bi, img_off(32 + t, k0, kSboK128), xg);
         }
-        // column images (row = channel, 8 consecutive tokens per work item)
-        for (int it = tid; it < 3 * 128 * 2; it += kChThreads) {
-            const int img = it / 256, rem = it % 256, kk = rem >> 1, t0 = (rem & 1) * 8;
-            float x[8];
+        // column images: item = (channel kk, tokens t0..t0+7)
+        for (int it = tid; it < 128 * 2; it += kChThreads) {
+            const int kk = it >> 1, t0 = (it & 1) * 8;
+            float xt[8], xv[8], xc[8];
+            const float GC = GATE_MODE == 0 ? sm.g[st][kCc - 1][kk] : sm.gs[st][kCc - 1];
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 const int t = t0 + e;
-                float val = 0.0f;
                 if (t < nt) {
                     const float G = GATE_MODE == 0 ? sm.g[st][t][kk] : sm.gs[st][t];
-                    const float GC = GATE_MODE == 0 ? sm.g[st][kCc - 1][kk] : sm.gs[st][kCc - 1];
-                    if (img == 0) val = sm.beta[st][t] * sm.k[st][t][kk] * __expf(G);
-                    else if (img == 1) val = sm.beta[st][t] * sm.v[st][t][kk];
-                    else val = sm.k[st][t][kk] * __expf(GC - G);
+                    const float kv = sm.k[st][t][kk];
+                    const float bt = sm.beta[st][t];
+                    xt[e] = bt * kv * __expf(G);          // beta K e^{G}
+                    xv[e] = bt * sm.v[st][t][kk];         // beta V
+                    xc[e] = kv * __expf(GC - G);          // K e^{G_C - G}
+                } else {
+                    xt[e] = xv[e] = xc[e] = 0.0f;
                 }
-                x[e] = val;
             }
-            if (img == 0) put8(sm.kt, img_off(kk, t0, kSboK16), x);
-            else if (img == 1) put8(sm.vt, img_off(kk, t0, kSboK16), x);
-            else put8(sm.b2, img_off(kk, t0, kSboK16), x);
+            put8(sm.kt, img_off(kk, t0, kSboK16), xt);
+            put8(sm.vt, img_off(kk, t0, kSboK16), xv);
+            put8(sm.b2, img_off(kk, t0, kSboK16), xc);
         }
         sync_images();
 
         // ---- MMA-a: [A/beta | Aqk]^T, rows s --------------------------------------------------
         if (tid == 0) {
-            mma_x3(tbase + kTmA, smem_u32(sm.kb[0]), smem_u32(sm.kb[1]), kSboK128,
-                   smem_u32(sm.bi[0]), smem_u32(sm.bi[1]), kSboK128, 8, idA);
+            mma_x3(tbase + kTmA, dKB, dBI0, 8, idA);
             tc_commit(&sm.bar_mma);
         }
         if (__syncthreads_or(!mma_wait())) { failed = true; break; }
@@ -358,10 +401,8 @@ kda_scan_chunk_kernel(ScanArgs a, const __grid_constant__ CUtensorMap tq,
 
         // ---- MMA-b: [W^T | U^T] = (beta K e^G | beta V)^T Tm^T --------------------------------
         if (tid == 0) {
-            mma_x3(tbase + kTmB, smem_u32(sm.kt[0]), smem_u32(sm.kt[1]), kSboK16,
-                   smem_u32(sm.tm[0]), smem_u32(sm.tm[1]), kSboK16, 1, idB);
-            mma_x3(tbase + kTmB + 16, smem_u32(sm.vt[0]), smem_u32(sm.vt[1]), kSboK16,
-                   smem_u32(sm.tm[0]), smem_u32(sm.tm[1]), kSboK16, 1, idB);
+            mma_x3(tbase + kTmB, dKT, dTM, 1, idB);
+            mma_x3(tbase + kTmB + 16, dVT, dTM, 1, idB);
             tc_commit(&sm.bar_mma);
         }
         if (__syncthreads_or(!mma_wait())) { failed = true; break; }
@@ -378,9 +419,7 @@ kda_scan_chunk_kernel(ScanArgs a, const __grid_constant__ CUtensorMap tq,
 
         // ---- MMA-1: [O1^T | X^T] = S^T (Q e^G | W)^T ---------------------------------------
         if (tid == 0) {
-            mma_x3(tbase + kTm1, smem_u32(sm.a1[0]), smem_u32(sm.a1[1]), kSboK128,
-                   smem_u32(sm.bi[0]) + 4 * kSboK128, smem_u32(sm.bi[1]) + 4 * kSboK128,
-                   kSboK128, 8, idA);
+            mma_x3(tbase + kTm1, dA1, dBI32, 8, idA);
             tc_commit(&sm.bar_mma);
         }
         if (__syncthreads_or(!mma_wait())) { failed = true; break; }
@@ -403,8 +442,7 @@ kda_scan_chunk_kernel(ScanArgs a, const __grid_constant__ CUtensorMap tq,
 
         // ---- MMA-2: [dS^T | O2^T] = U'^T (K e^{G_C-G} | Aqk) -------------------------------
         if (tid == 0) {
-            mma_x3(tbase + kTm2, smem_u32(sm.a2[0]), smem_u32(sm.a2[1]), kSboK16,
-                   smem_u32(sm.b2[0]), smem_u32(sm.b2[1]), kSboK16, 1, id2);
+            mma_x3(tbase + kTm2, dA2, dB2, 1, id2);
             tc_commit(&sm.bar_mma);
         }
         if (__syncthreads_or(!mma_wait())) { failed = true; break; }
@@ -414,10 +452,15 @@ kda_scan_chunk_kernel(ScanArgs a, const __grid_constant__ CUtensorMap tq,
                 float d[16];
                 tmem_ld16(tlane + kTm2 + 16 * c16, d);
                 tmem_ld_wait();
+                const float4* E4 = reinterpret_cast<const float4*>(&sm.egc[16 * c16]);
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const int kk = 16 * c16 + e;
-                    srow[kk] = fmaf(srow[kk], sm.egc[kk], d[e]);
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    const float4 e4 = E4[q4];
+                    const int kk = 16 * c16 + 4 * q4;
+                    srow[kk] = fmaf(srow[kk], e4.x, d[4 * q4]);
+                    srow[kk + 1] = fmaf(srow[kk + 1], e4.y, d[4 * q4 + 1]);
+                    srow[kk + 2] = fmaf(srow[kk + 2], e4.z, d[4 * q4 + 2]);
+                    srow[kk + 3] = fmaf(srow[kk + 3], e4.w, d[4 * q4 + 3]);
                 }
             }
             float o2[16];
