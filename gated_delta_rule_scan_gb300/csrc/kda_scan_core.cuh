@@ -203,4 +203,173 @@ __device__ __forceinline__ void col4_tokens(Col4& S, int nt, const TokView& vw, 
     if (!key_lane) vw.out[(nt - 1) * vw.out_stride + vw.out_col0 + c_own] = __fmul_rn(scale, red);
 }
 
+
+// ------------------------------------------------------------------------------------------
+// The same recurrence with G lanes per group (G = 8 or 16): lane = G * grp + r holds key-dim
+// elements i = 4r + 4G m + e (m < 32 / G, e = 0..3) of the group's 4 columns.  G = 16 halves the
+// elements per lane (more warps for the same state) while every shared-memory load still feeds
+// 4 columns.  The 8-value transposed reduction runs over log2(G) butterfly steps and leaves value
+// index r * 8 / G in lane r.
+// ------------------------------------------------------------------------------------------
+
+template <int G>
+struct ColG {
+    float2 s[4][32 / G * 2];
+};
+
+template <int G>
+__device__ __forceinline__ void colg_load(ColG<G>& S, const float* col0, int r) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int m = 0; m < 32 / G; ++m) {
+            const float4 x = __ldcs(reinterpret_cast<const float4*>(col0 + c * kHeadDim + 4 * r + 4 * G * m));
+            S.s[c][2 * m] = lo2(x);
+            S.s[c][2 * m + 1] = hi2(x);
+        }
+}
+
+template <int G>
+__device__ __forceinline__ void colg_store(const ColG<G>& S, float* col0, int r) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int m = 0; m < 32 / G; ++m)
+            __stcs(reinterpret_cast<float4*>(col0 + c * kHeadDim + 4 * r + 4 * G * m),
+                   make_float4(S.s[c][2 * m].x, S.s[c][2 * m].y, S.s[c][2 * m + 1].x,
+                               S.s[c][2 * m + 1].y));
+}
+
+template <int G>
+__device__ __forceinline__ float reduce8_groupG(const float (&v)[8], int r) {
+    if constexpr (G == 8) {
+        return reduce8_group8(v, r);
+    } else {
+        const bool b3 = (r & 8) != 0, b2 = (r & 4) != 0, b1 = (r & 2) != 0;
+        float k4[4];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            const float y = __shfl_xor_sync(0xffffffffu, b3 ? v[m] : v[4 + m], 8);
+            k4[m] = (b3 ? v[4 + m] : v[m]) + y;
+        }
+        float k2[2];
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+            const float y = __shfl_xor_sync(0xffffffffu, b2 ? k4[m] : k4[2 + m], 4);
+            k2[m] = (b2 ? k4[2 + m] : k4[m]) + y;
+        }
+        const float y = __shfl_xor_sync(0xffffffffu, b1 ? k2[0] : k2[1], 2);
+        float s1 = (b1 ? k2[1] : k2[0]) + y;
+        s1 += __shfl_xor_sync(0xffffffffu, s1, 1);
+        return s1;
+    }
+}
+
+template <bool PER_CHANNEL, int G>
+__device__ __forceinline__ void load_rows_g(float4 (&k)[32 / G], float4 (&a)[32 / G],
+                                            const float* k_row, const float* a_row,
+                                            float a_scalar, int r) {
+#pragma unroll
+    for (int m = 0; m < 32 / G; ++m) {
+        k[m] = *reinterpret_cast<const float4*>(k_row + 4 * r + 4 * G * m);
+        a[m] = PER_CHANNEL ? *reinterpret_cast<const float4*>(a_row + 4 * r + 4 * G * m)
+                           : make_float4(a_scalar, a_scalar, a_scalar, a_scalar);
+    }
+}
+
+// col4_tokens with G lanes per group (see above); same contract.
+template <bool PER_CHANNEL, bool PREFETCH, int G>
+__device__ __forceinline__ void colg_tokens(ColG<G>& S, int nt, const TokView& vw, float scale,
+                                            int r, int lane) {
+    if (nt <= 0) return;
+    constexpr int MC = 32 / G;
+    const int idx = r * 8 / G;               // the reduced value this lane ends with
+    const int c_own = idx & 3;
+    const bool key_lane = idx < 4;
+    const bool write_lane = !key_lane && ((r & (G / 8 - 1)) == 0);
+    float dqp[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    float4 ck[MC], ca[MC];
+    load_rows_g<PER_CHANNEL, G>(ck, ca, vw.k, vw.a, PER_CHANNEL ? 0.0f : vw.a_scal[0], r);
+    for (int t = 0; t < nt; ++t) {
+        float2 acc[4][2];
+#pragma unroll
+        for (int m = 0; m < MC; ++m) {
+            const float2 alo = lo2(ca[m]), ahi = hi2(ca[m]);
+            const float2 klo = lo2(ck[m]), khi = hi2(ck[m]);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                S.s[c][2 * m] = __fmul2_rn(alo, S.s[c][2 * m]);
+                S.s[c][2 * m + 1] = __fmul2_rn(ahi, S.s[c][2 * m + 1]);
+                if (m == 0) {
+                    acc[c][0] = __fmul2_rn(S.s[c][0], klo);
+                    acc[c][1] = __fmul2_rn(S.s[c][1], khi);
+                } else {
+                    acc[c][0] = __ffma2_rn(S.s[c][2 * m], klo, acc[c][0]);
+                    acc[c][1] = __ffma2_rn(S.s[c][2 * m + 1], khi, acc[c][1]);
+                }
+            }
+        }
+        float v8[8];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            v8[c] = sum4(acc[c][0], acc[c][1]);
+            v8[4 + c] = dqp[c];
+        }
+        const float red = reduce8_groupG<G>(v8, r);
+        if (t > 0 && write_lane)
+            vw.out[(t - 1) * vw.out_stride + vw.out_col0 + c_own] = __fmul_rn(scale, red);
+        const float vt = vw.v[t * vw.v_stride + vw.v_col0 + c_own];
+        const float w = __fmul_rn(vw.beta[t], vt - red);   // meaningful in key lanes
+        float2 w2[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const float wc = __shfl_sync(0xffffffffu, w, (lane & ~(G - 1)) | (c * G / 8));
+            w2[c] = make_float2(wc, wc);
+        }
+        float4 nk[MC], na[MC];
+        if (PREFETCH && t + 1 < nt)
+            load_rows_g<PER_CHANNEL, G>(nk, na, vw.k + (t + 1) * vw.row_stride,
+                                        vw.a + (t + 1) * vw.row_stride,
+                                        PER_CHANNEL ? 0.0f : vw.a_scal[t + 1], r);
+#pragma unroll
+        for (int m = 0; m < MC; ++m) {
+            const float4 q4 = *reinterpret_cast<const float4*>(vw.q + t * vw.row_stride + 4 * r + 4 * G * m);
+            const float2 klo = lo2(ck[m]), khi = hi2(ck[m]);
+            const float2 qlo = lo2(q4), qhi = hi2(q4);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                S.s[c][2 * m] = __ffma2_rn(klo, w2[c], S.s[c][2 * m]);
+                S.s[c][2 * m + 1] = __ffma2_rn(khi, w2[c], S.s[c][2 * m + 1]);
+                if (m == 0) {
+                    acc[c][0] = __fmul2_rn(S.s[c][0], qlo);
+                    acc[c][1] = __fmul2_rn(S.s[c][1], qhi);
+                } else {
+                    acc[c][0] = __ffma2_rn(S.s[c][2 * m], qlo, acc[c][0]);
+                    acc[c][1] = __ffma2_rn(S.s[c][2 * m + 1], qhi, acc[c][1]);
+                }
+            }
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c) dqp[c] = sum4(acc[c][0], acc[c][1]);
+        if (t + 1 < nt) {
+            if (PREFETCH) {
+#pragma unroll
+                for (int m = 0; m < MC; ++m) { ck[m] = nk[m]; ca[m] = na[m]; }
+            } else {
+                load_rows_g<PER_CHANNEL, G>(ck, ca, vw.k + (t + 1) * vw.row_stride,
+                                            vw.a + (t + 1) * vw.row_stride,
+                                            PER_CHANNEL ? 0.0f : vw.a_scal[t + 1], r);
+            }
+        }
+    }
+    float v8[8];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        v8[c] = 0.0f;
+        v8[4 + c] = dqp[c];
+    }
+    const float red = reduce8_groupG<G>(v8, r);
+    if (write_lane) vw.out[(nt - 1) * vw.out_stride + vw.out_col0 + c_own] = __fmul_rn(scale, red);
+}
+
 }  // namespace kda

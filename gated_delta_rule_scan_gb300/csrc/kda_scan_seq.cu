@@ -10,9 +10,10 @@
 //
 // GB300 layout.  Every value column j of S is an independent 128-vector recurrence, so the kernel
 // parallelises over (sequence, head, column) and keeps each column in registers for the whole
-// sequence.  A CTA (2 warps) owns 32 columns of one head; within a warp, 8 lanes share 4 columns
-// and each lane holds 16 key-dim elements of all 4 (kda_scan_core.cuh), so each k / decay / q
-// value a lane loads from shared memory feeds 4 columns.  The per-token inputs every column of
+// sequence.  A CTA (4 warps) owns 32 columns of one head; within a warp, 16 lanes share 4 columns
+// and each lane holds 8 key-dim elements of all 4 (kda_scan_core.cuh), so each k / decay / q
+// value a lane loads from shared memory feeds 4 columns, and a 4096-token, 64-head prefill runs
+// about two warps per scheduler.  The per-token inputs every column of
 // the head shares (q, k, g rows: 512 B each) and the CTA's 32 v values are staged by 2-D TMA
 // tensor-map loads into a double-buffered shared-memory ring of kScanTB-token blocks, completion
 // tracked by mbarriers (bounded waits); the next block streams in while the current one is
@@ -25,9 +26,10 @@
 
 namespace kda {
 
-constexpr int kScanWarps = 2;
+constexpr int kScanG = 16;                      // lanes per column group (kda_scan_core.cuh)
+constexpr int kScanWarps = 4;
 constexpr int kScanThreads = 32 * kScanWarps;
-constexpr int kScanCols = 16 * kScanWarps;      // value columns per CTA
+constexpr int kScanCols = (32 / kScanG) * 4 * kScanWarps;   // value columns per CTA
 constexpr int kScanTB = 16;                     // tokens per staged block
 constexpr int kColBlocks = kHeadDim / kScanCols;
 
@@ -55,11 +57,11 @@ kda_scan_seq_kernel(ScanArgs a, const __grid_constant__ CUtensorMap tq,
         (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
 
     const int tid = threadIdx.x;
-    const int warp = tid >> 5, lane = tid & 31, grp = lane >> 3, r = lane & 7;
+    const int warp = tid >> 5, lane = tid & 31, grp = lane / kScanG, r = lane % kScanG;
     const int cb = blockIdx.x % kColBlocks;
     const int h = blockIdx.x / kColBlocks;
     const int n = a.order ? a.order[blockIdx.y] : (int)blockIdx.y;
-    const int cw = warp * 16 + grp * 4;            // first of the group's 4 columns in the CTA
+    const int cw = (warp * (32 / kScanG) + grp) * 4;   // first of the group's 4 columns in the CTA
     const int H = a.H;
     const long C = (long)H * kHeadDim;
 
@@ -74,9 +76,9 @@ kda_scan_seq_kernel(ScanArgs a, const __grid_constant__ CUtensorMap tq,
     const long L = end - begin;
     const int nblk = (int)((L + kScanTB - 1) / kScanTB);
 
-    Col4 S;
+    ColG<kScanG> S;
     const long col0 = (((long)n * H + h) * kHeadDim + cb * kScanCols + cw) * kHeadDim;
-    col4_load(S, a.state_in + col0, r);
+    colg_load<kScanG>(S, a.state_in + col0, r);
 
     constexpr uint32_t kTxBytes =
         (GATE_MODE == 0 ? 3u : 2u) * kScanTB * kHeadDim * 4u + kScanTB * kScanCols * 4u;
@@ -143,7 +145,7 @@ kda_scan_seq_kernel(ScanArgs a, const __grid_constant__ CUtensorMap tq,
         vw.v_col0 = cw;
         vw.out_stride = kScanCols;
         vw.out_col0 = cw;
-        col4_tokens<GATE_MODE == 0, true>(S, nt, vw, a.scale, r, lane);
+        colg_tokens<GATE_MODE == 0, true, kScanG>(S, nt, vw, a.scale, r, lane);
         __syncthreads();
         for (int e = tid; e < nt * (kScanCols / 4); e += kScanThreads) {
             const int t = e / (kScanCols / 4), c4 = e % (kScanCols / 4);
@@ -151,7 +153,7 @@ kda_scan_seq_kernel(ScanArgs a, const __grid_constant__ CUtensorMap tq,
                 *reinterpret_cast<const float4*>(&sm.obuf[t][4 * c4]);
         }
     }
-    col4_store(S, a.state_out + col0, r);
+    colg_store<kScanG>(S, a.state_out + col0, r);
 }
 
 // ------------------------------------------------------------------------------------------

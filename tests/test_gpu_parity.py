@@ -128,14 +128,16 @@ def test_verify_equals_chained_decode_bitwise(T):
     _assert_close(gpu_heads(full, inp, heads), ref, ("y", "state_out", "ring_out"))
 
 
-def test_decode_fused_equals_unfused_bitwise():
-    """The fused kernel and prep -> scan -> gated RMSNorm compute the same bits."""
+def test_decode_fused_equals_unfused():
+    """The fused kernel and prep -> scan -> gated RMSNorm agree: the ring bit for bit (pure copies),
+    y and the state to f32 rounding (the two scans reduce over different lane groupings)."""
     inp = inputs.decode_step(N=16, T=4, H=8, seed=12)
     fused = _decode(inp, 4)
     for gate_exp in (False, True):
         unf = gpu_forward(inp, varlen=False, algo=1, gate_exp=gate_exp)
-        for k in ("y", "state_out", "ring_out"):
-            assert torch.equal(fused[k], unf[k]), (k, gate_exp)
+        assert torch.equal(fused["ring_out"], unf["ring_out"])
+        for k in ("y", "state_out"):
+            assert rel_linf(fused[k], unf[k]) <= 1e-5, (k, gate_exp)
 
 
 def test_decode_in_place_ring():
