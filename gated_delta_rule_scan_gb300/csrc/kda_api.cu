@@ -68,6 +68,13 @@ int prep_impl(const void* q_raw, const void* k_raw, const void* v_raw, int raw_d
             return KDA_ERR_NULL;
         if (!aligned16(q_hat) || !aligned16(k_hat) || !aligned16(v_hat) || !aligned16(g))
             return KDA_ERR_ALIGN;
+        // raw rows are read 4 channels at a time: 8-byte bf16x4 or 16-byte f32x4
+        const uintptr_t rmask = raw_dtype == KDA_DTYPE_BF16 ? 7u : 15u;
+        if (((reinterpret_cast<uintptr_t>(q_raw) | reinterpret_cast<uintptr_t>(k_raw) |
+              reinterpret_cast<uintptr_t>(v_raw)) & rmask) != 0)
+            return KDA_ERR_ALIGN;
+        if ((gate_mode & KDA_GATE_PER_HEAD) == 0 && (!aligned16(f_raw) || !aligned16(dt_bias)))
+            return KDA_ERR_ALIGN;
     }
     if (conv_w != nullptr && ring_in != ring_out) {
         const size_t rb = (size_t)seq.N * 3 * H * kHeadDim * (K - 1) * sizeof(float);

@@ -10,12 +10,11 @@
 //            or the GDN per-head g = -exp(A_log[h]) * softplus(alpha + dt_bias[h])
 //            (gdn_ops.rs gdn_gates_into); beta = sigmoid(beta_raw) per (token, head).
 //
-// Layout: one CTA per (tile of kTileRows consecutive packed rows, head); 64 threads, each owning
-// the channel pair (2i, 2i+1) of the head in all three planes, carrying the planes' conv windows
-// in registers while it walks the tile, so each raw sample is read once per tile (plus K-1 halo
-// rows).  Raw rows are read as bf16x2 / float2 pairs and kPrefetch rows of loads are issued
-// before any of them is used, so each thread keeps several loads in flight.  A tile may straddle
-// sequence boundaries (varlen): the windows restart from the next sequence's ring.  The ring is
+// Layout: one warp per (token row, head), 8 consecutive rows of one head per CTA; lane l owns
+// channels 4l..4l+3 of the head in all three planes.  The conv taps read their K-1 older rows
+// directly (the CTA's warps share those rows through L1) or, within K-1 rows of a sequence's
+// start, the ring; the l2 norm is one warp butterfly per row.  Raw rows are read as 8-byte bf16x4
+// (or 16-byte f32x4) vectors and every output row is a 512-byte coalesced store.  The ring is
 // rewritten by a second, tiny kernel launched after this one on the same stream, so ring_in and
 // ring_out may be the same buffer.
 #include "kda_device.cuh"
@@ -23,214 +22,137 @@
 
 namespace kda {
 
-constexpr int kTileRows = 32;
-constexpr int kPrepThreads = kHeadDim / 2;  // one channel pair per thread
-constexpr int kPrefetch = 8;                // rows of loads issued ahead
+constexpr int kRowsPerCta = 8;
+constexpr int kPrepThreads = 32 * kRowsPerCta;
 
-struct SeqCursor {
-    int n;        // sequence index
-    long begin;   // first packed row of the sequence
-    long end;     // one past its last row
-};
-
-// Sequence containing packed row r (rows of empty sequences are skipped).
-__device__ __forceinline__ SeqCursor seq_of_row(const SeqLayout& L, long r) {
-    SeqCursor s;
+// Sequence containing packed row r: its index and first row (rows of empty sequences skipped).
+__device__ __forceinline__ void seq_of_row(const SeqLayout& L, long r, int& n, long& begin) {
     if (L.cu_seqlens == nullptr) {
-        s.n = (int)(r / L.T_uniform);
-        s.begin = (long)s.n * L.T_uniform;
-        s.end = s.begin + L.T_uniform;
-        return s;
+        n = (int)(r / L.T_uniform);
+        begin = (long)n * L.T_uniform;
+        return;
     }
-    // largest n with cu[n] <= r: its sequence is non-empty and contains r
-    int lo = 0, hi = L.N;  // invariant: cu[lo] <= r < cu[hi]
+    int lo = 0, hi = L.N;  // largest n with cu[n] <= r: its sequence is non-empty and holds r
     while (hi - lo > 1) {
-        int mid = (lo + hi) >> 1;
+        const int mid = (lo + hi) >> 1;
         if ((long)L.cu_seqlens[mid] <= r) lo = mid; else hi = mid;
     }
-    s.n = lo;
-    s.begin = L.cu_seqlens[lo];
-    s.end = L.cu_seqlens[lo + 1];
-    return s;
+    n = lo;
+    begin = L.cu_seqlens[lo];
 }
 
-__device__ __forceinline__ SeqCursor seq_next(const SeqLayout& L, SeqCursor s) {
-    SeqCursor t;
-    t.n = s.n + 1;
-    if (L.cu_seqlens == nullptr) {
-        t.begin = s.end;
-        t.end = s.end + L.T_uniform;
+template <bool BF16>
+__device__ __forceinline__ float4 load_raw4(const void* base, long idx) {
+    if constexpr (BF16) {
+        const uint2 u = *reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(base) + idx);
+        const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+        const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+        return make_float4(a.x, a.y, b.x, b.y);
     } else {
-        t.begin = L.cu_seqlens[t.n];
-        t.end = L.cu_seqlens[t.n + 1];
+        return *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(base) + idx);
     }
-    return t;
 }
 
-// Fill the windows of one plane's channel pair with the K-1 samples that precede position p of
-// sequence s: win[KW - d] = sample at position p - d (d = 1..R), from the raw rows when
-// p - d >= 0 and from the ring (oldest slot first) otherwise.  window_push then appends p.
+__device__ __forceinline__ float4 silu4(const float4& x) {
+    return make_float4(silu_f(x.x), silu_f(x.y), silu_f(x.z), silu_f(x.w));
+}
+
+// Conv taps of one plane for 4 channels at position p of its sequence (row r, first row begin):
+// acc = sum_j w[c][j] * xt[p + j] with xt = ring ++ rows, taps summed oldest first (fmaf from 0).
 template <bool BF16, int KW>
-__device__ __forceinline__ void window_fill2(float (&w0)[KW], float (&w1)[KW], const void* raw,
-                                             long C, int c, const float* ring_in, long ring_row0,
-                                             int R, SeqCursor s, long p) {
+__device__ __forceinline__ float4 conv4(const void* raw, long C, int c, const float* ring_in,
+                                        long ring_row0, const float (&w)[4][KW], int K, long r,
+                                        long p) {
+    const int R = K - 1;
+    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
     for (int m = 0; m < KW; ++m) {
-        const int d = KW - m;
-        float2 x = make_float2(0.0f, 0.0f);
-        if (d <= R) {
-            const long pos = p - d;
-            if (pos >= 0) {
-                x = load_raw2<BF16>(raw, (s.begin + pos) * C + c);
-            } else {
-                x.x = ring_in[ring_row0 + (R + pos)];
-                x.y = ring_in[ring_row0 + R + (R + pos)];
-            }
+        const int j = m - (KW - K);            // tap index (0 = oldest)
+        if (j < 0) continue;
+        const long pos = p - R + j;            // position of the sample this tap reads
+        float4 x;
+        if (pos >= 0) {
+            x = load_raw4<BF16>(raw, (r - (p - pos)) * C + c);
+        } else {
+            const long s = R + pos;            // ring slot (0 = oldest)
+            x = make_float4(ring_in[ring_row0 + 0 * R + s], ring_in[ring_row0 + 1 * R + s],
+                            ring_in[ring_row0 + 2 * R + s], ring_in[ring_row0 + 3 * R + s]);
         }
-        w0[m] = x.x;
-        w1[m] = x.y;
+        acc[0] = fmaf(w[0][m], x.x, acc[0]);
+        acc[1] = fmaf(w[1][m], x.y, acc[1]);
+        acc[2] = fmaf(w[2][m], x.z, acc[2]);
+        acc[3] = fmaf(w[3][m], x.w, acc[3]);
     }
+    return make_float4(acc[0], acc[1], acc[2], acc[3]);
 }
 
-// EXP: write the decay factor exp(g) instead of the log-decay g.  KW: register window width
-// (4 when K <= 4, else 8).
+// EXP: write the decay factor exp(g) instead of the log-decay g.  KW: compile-time bound on K.
 template <bool BF16, int GATE_MODE, bool CONV, bool EXP, int KW>
 __global__ void __launch_bounds__(kPrepThreads) kda_prep_kernel(PrepArgs a) {
-    __shared__ __align__(16) float xs[2][kTileRows][kHeadDim];   // pre-norm q, k of the tile
-    __shared__ float part[2][2][kTileRows];
-    __shared__ float inv_s[2][kTileRows];
-
     const int h = blockIdx.y;
-    const int tid = threadIdx.x;
-    const int i0 = 2 * tid;                   // channel pair within the head
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const long r = (long)blockIdx.x * kRowsPerCta + warp;
+    if (r >= a.seq.total_rows) return;
     const int H = a.H;
     const long C = (long)H * kHeadDim;
-    const int c = h * kHeadDim + i0;          // first channel of the pair within a plane
-    const long r0 = (long)blockIdx.x * kTileRows;
-    const int nt = (int)min((long)kTileRows, a.seq.total_rows - r0);
-    const int K = a.K, R = a.K - 1;
-    const int warp = tid >> 5, lane = tid & 31;
+    const int c = h * kHeadDim + 4 * lane;     // first of this lane's 4 channels in a plane
+    const int K = a.K;
 
-    float wq[2][KW], wk[2][KW], wv[2][KW];
-    float winq[2][KW], wink[2][KW], winv[2][KW];
-#pragma unroll
-    for (int m = 0; m < KW; ++m)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            wq[e][m] = wk[e][m] = wv[e][m] = 0.0f;
-            winq[e][m] = wink[e][m] = winv[e][m] = 0.0f;
-        }
-    SeqCursor s = seq_of_row(a.seq, r0);
-    const bool single = s.end >= r0 + nt;     // the whole tile lies in one sequence
-    auto fill = [&](long p) {
-        const long rr = (long)s.n * 3 * C * R;
-        window_fill2<BF16, KW>(winq[0], winq[1], a.q_raw, C, c, a.ring_in, rr + (0 * C + c) * R, R, s, p);
-        window_fill2<BF16, KW>(wink[0], wink[1], a.k_raw, C, c, a.ring_in, rr + (1 * C + c) * R, R, s, p);
-        window_fill2<BF16, KW>(winv[0], winv[1], a.v_raw, C, c, a.ring_in, rr + (2 * C + c) * R, R, s, p);
-    };
+    float4 xq, xk, xv;
     if constexpr (CONV) {
+        int n;
+        long begin;
+        seq_of_row(a.seq, r, n, begin);
+        const long p = r - begin;
+        const int R = K - 1;
+        float wq[4][KW], wk[4][KW], wv[4][KW];
 #pragma unroll
-        for (int m = 0; m < KW; ++m) {
-            const int j = m - (KW - K);
-            if (j >= 0) {
+        for (int e = 0; e < 4; ++e)
 #pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    wq[e][m] = a.conv_w[(0 * C + c + e) * K + j];
-                    wk[e][m] = a.conv_w[(1 * C + c + e) * K + j];
-                    wv[e][m] = a.conv_w[(2 * C + c + e) * K + j];
-                }
+            for (int m = 0; m < KW; ++m) {
+                const int j = m - (KW - K);
+                wq[e][m] = j >= 0 ? a.conv_w[(0 * C + c + e) * K + j] : 0.0f;
+                wk[e][m] = j >= 0 ? a.conv_w[(1 * C + c + e) * K + j] : 0.0f;
+                wv[e][m] = j >= 0 ? a.conv_w[(2 * C + c + e) * K + j] : 0.0f;
             }
-        }
-        fill(r0 - s.begin);
+        const long rr = (long)n * 3 * C * R;
+        xq = silu4(conv4<BF16, KW>(a.q_raw, C, c, a.ring_in, rr + (0 * C + c) * R, wq, K, r, p));
+        xk = silu4(conv4<BF16, KW>(a.k_raw, C, c, a.ring_in, rr + (1 * C + c) * R, wk, K, r, p));
+        xv = silu4(conv4<BF16, KW>(a.v_raw, C, c, a.ring_in, rr + (2 * C + c) * R, wv, K, r, p));
+    } else {
+        xq = load_raw4<BF16>(a.q_raw, r * C + c);
+        xk = load_raw4<BF16>(a.k_raw, r * C + c);
+        xv = load_raw4<BF16>(a.v_raw, r * C + c);
     }
-    float rate = 0.0f;
-    float2 dtb = make_float2(0.0f, 0.0f);
-    if constexpr (GATE_MODE == 0) {
-        rate = expf(a.a_log[h]);
-        dtb = *reinterpret_cast<const float2*>(a.dt_bias + c);
-    }
+    *reinterpret_cast<float4*>(a.v_hat + r * C + c) = xv;
 
-    for (int t0 = 0; t0 < nt; t0 += kPrefetch) {
-        float2 rq[kPrefetch], rk[kPrefetch], rv[kPrefetch], fr[kPrefetch];
-#pragma unroll
-        for (int u = 0; u < kPrefetch; ++u) {
-            if (t0 + u < nt) {
-                const long r = r0 + t0 + u;
-                rq[u] = load_raw2<BF16>(a.q_raw, r * C + c);
-                rk[u] = load_raw2<BF16>(a.k_raw, r * C + c);
-                rv[u] = load_raw2<BF16>(a.v_raw, r * C + c);
-                if (GATE_MODE == 0) fr[u] = *reinterpret_cast<const float2*>(a.f_raw + r * C + c);
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < kPrefetch; ++u) {
-            const int t = t0 + u;
-            if (t < nt) {
-                const long r = r0 + t;
-                float2 xq, xk, xv;
-                if constexpr (CONV) {
-                    if (!single && r >= s.end) {  // next non-empty sequence: restart the windows
-                        do { s = seq_next(a.seq, s); } while (s.end <= r);
-                        fill(0);
-                    }
-                    window_push(winq[0], rq[u].x); window_push(winq[1], rq[u].y);
-                    window_push(wink[0], rk[u].x); window_push(wink[1], rk[u].y);
-                    window_push(winv[0], rv[u].x); window_push(winv[1], rv[u].y);
-                    xq = make_float2(silu_f(conv_taps_f(wq[0], winq[0], K)),
-                                     silu_f(conv_taps_f(wq[1], winq[1], K)));
-                    xk = make_float2(silu_f(conv_taps_f(wk[0], wink[0], K)),
-                                     silu_f(conv_taps_f(wk[1], wink[1], K)));
-                    xv = make_float2(silu_f(conv_taps_f(wv[0], winv[0], K)),
-                                     silu_f(conv_taps_f(wv[1], winv[1], K)));
-                } else {
-                    xq = rq[u];
-                    xk = rk[u];
-                    xv = rv[u];
-                }
-                *reinterpret_cast<float2*>(a.v_hat + r * C + c) = xv;
-                *reinterpret_cast<float2*>(&xs[0][t][i0]) = xq;
-                *reinterpret_cast<float2*>(&xs[1][t][i0]) = xk;
-                if constexpr (GATE_MODE == 0) {
-                    float g0 = kda_gate_f(fr[u].x, dtb.x, rate, a.gate_lb);
-                    float g1 = kda_gate_f(fr[u].y, dtb.y, rate, a.gate_lb);
-                    if (EXP) { g0 = decay_f(g0); g1 = decay_f(g1); }
-                    *reinterpret_cast<float2*>(a.g + r * C + c) = make_float2(g0, g1);
-                }
-            }
-        }
+    // l2 norm over the head's 128 channels: lane partial, then one warp butterfly
+    float sq = __fmul_rn(xq.x, xq.x);
+    sq = fmaf(xq.y, xq.y, sq); sq = fmaf(xq.z, xq.z, sq); sq = fmaf(xq.w, xq.w, sq);
+    float sk = __fmul_rn(xk.x, xk.x);
+    sk = fmaf(xk.y, xk.y, sk); sk = fmaf(xk.z, xk.z, sk); sk = fmaf(xk.w, xk.w, sk);
+    const float iq = l2_inv_f(warp_sum(sq), a.l2_eps);
+    const float ik = l2_inv_f(warp_sum(sk), a.l2_eps);
+    *reinterpret_cast<float4*>(a.q_hat + r * C + c) =
+        make_float4(xq.x * iq, xq.y * iq, xq.z * iq, xq.w * iq);
+    *reinterpret_cast<float4*>(a.k_hat + r * C + c) =
+        make_float4(xk.x * ik, xk.y * ik, xk.z * ik, xk.w * ik);
+
+    if constexpr (GATE_MODE == 0) {
+        const float rate = expf(a.a_log[h]);
+        const float4 f = *reinterpret_cast<const float4*>(a.f_raw + r * C + c);
+        const float4 dt = *reinterpret_cast<const float4*>(a.dt_bias + c);
+        float4 g = make_float4(kda_gate_f(f.x, dt.x, rate, a.gate_lb), kda_gate_f(f.y, dt.y, rate, a.gate_lb),
+                               kda_gate_f(f.z, dt.z, rate, a.gate_lb), kda_gate_f(f.w, dt.w, rate, a.gate_lb));
+        if (EXP) g = make_float4(decay_f(g.x), decay_f(g.y), decay_f(g.z), decay_f(g.w));
+        *reinterpret_cast<float4*>(a.g + r * C + c) = g;
     }
-    if (tid < nt) {
-        const long r = r0 + tid;
+    if (lane == 0) {
         a.beta[r * H + h] = sigmoid_f(a.beta_raw[r * H + h]);
         if constexpr (GATE_MODE == 1) {
             const float gl = gdn_gate_f(a.f_raw[r * H + h], a.dt_bias[h], a.a_log[h]);
             a.g[r * H + h] = EXP ? decay_f(gl) : gl;
         }
-    }
-    __syncthreads();
-
-    // l2 norm of q and k over the head's 128 channels, one reduction per token
-    for (int t = 0; t < nt; ++t) {
-        const float2 xq = *reinterpret_cast<const float2*>(&xs[0][t][i0]);
-        const float2 xk = *reinterpret_cast<const float2*>(&xs[1][t][i0]);
-        const float sq = warp_sum(pair_sumsq(xq.x, xq.y));
-        const float sk = warp_sum(pair_sumsq(xk.x, xk.y));
-        if (lane == 0) { part[0][warp][t] = sq; part[1][warp][t] = sk; }
-    }
-    __syncthreads();
-    {
-        const int pl = tid / kTileRows, t = tid % kTileRows;   // 64 threads = 2 planes x 32 rows
-        if (t < nt) inv_s[pl][t] = l2_inv_f(part[pl][0][t] + part[pl][1][t], a.l2_eps);
-    }
-    __syncthreads();
-    for (int t = 0; t < nt; ++t) {
-        const long r = r0 + t;
-        const float2 xq = *reinterpret_cast<const float2*>(&xs[0][t][i0]);
-        const float2 xk = *reinterpret_cast<const float2*>(&xs[1][t][i0]);
-        *reinterpret_cast<float2*>(a.q_hat + r * C + c) =
-            make_float2(__fmul_rn(xq.x, inv_s[0][t]), __fmul_rn(xq.y, inv_s[0][t]));
-        *reinterpret_cast<float2*>(a.k_hat + r * C + c) =
-            make_float2(__fmul_rn(xk.x, inv_s[1][t]), __fmul_rn(xk.y, inv_s[1][t]));
     }
 }
 
@@ -279,7 +201,7 @@ __global__ void __launch_bounds__(256) kda_ring_roll_kernel(PrepArgs a) {
 
 template <bool BF16, int GM, bool CONV, bool EXP>
 static cudaError_t launch_prep_t(const PrepArgs& a, cudaStream_t s) {
-    const long tiles = (a.seq.total_rows + kTileRows - 1) / kTileRows;
+    const long tiles = (a.seq.total_rows + kRowsPerCta - 1) / kRowsPerCta;
     if (tiles > 0) {
         dim3 grid((unsigned)tiles, (unsigned)a.H);
         if (a.K <= 4) kda_prep_kernel<BF16, GM, CONV, EXP, 4><<<grid, kPrepThreads, 0, s>>>(a);

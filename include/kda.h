@@ -88,12 +88,13 @@ const char* kda_status_string(int status);
  *   With KDA_GATE_EXP or-ed into gate_mode, g receives exp() of the gate above (the per-step
  *   decay factor in (0, 1]), the form kda_scan consumes without taking exp itself.
  *
- * q_raw, k_raw, v_raw  [rows, C] in raw_dtype (KDA_DTYPE_F32 / KDA_DTYPE_BF16), read only.
+ * q_raw, k_raw, v_raw  [rows, C] in raw_dtype (KDA_DTYPE_F32 / KDA_DTYPE_BF16), read only;
+ *                      8-byte aligned (bf16) or 16-byte aligned (f32).
  * conv_w               [3C, K] f32, or NULL: no conv and no SiLU (x = raw), rings unused.
  * ring_in, ring_out    [N, 3C, R] f32 (ignored when conv_w is NULL).  They may be the same
  *                      buffer (in-place roll); otherwise they must not overlap.
- * f_raw                [rows, C] (gate_mode 0) or [rows, H] (gate_mode 1) f32.
- * dt_bias              [C] (gate_mode 0) or [H] (gate_mode 1) f32;  a_log [H] f32.
+ * f_raw                [rows, C] (gate_mode 0, [16B]) or [rows, H] (gate_mode 1) f32.
+ * dt_bias              [C] (gate_mode 0, [16B]) or [H] (gate_mode 1) f32;  a_log [H] f32.
  * beta_raw             [rows, H] f32.
  * q_hat, k_hat, v_hat  [rows, C] f32 outputs [16B];  g: [rows, C] or [rows, H] f32 output [16B];
  * beta                 [rows, H] f32 output.
