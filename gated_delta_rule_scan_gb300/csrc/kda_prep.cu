@@ -10,26 +10,30 @@
 //            or the GDN per-head g = -exp(A_log[h]) * softplus(alpha + dt_bias[h])
 //            (gdn_ops.rs gdn_gates_into); beta = sigmoid(beta_raw) per (token, head).
 //
-// Layout: one warp per (token row, head), 8 consecutive rows of one head per CTA; lane l owns
-// channels 4l..4l+3 of the head in all three planes.  The conv taps read their K-1 older rows
-// directly (the CTA's warps share those rows through L1) or, within K-1 rows of a sequence's
-// start, the ring; the l2 norm is one warp butterfly per row.  Raw rows are read as 8-byte bf16x4
-// (or 16-byte f32x4) vectors and every output row is a 512-byte coalesced store.  The ring is
-// rewritten by a second, tiny kernel launched after this one on the same stream, so ring_in and
-// ring_out may be the same buffer.
+// Layout: one warp walks a run of kRun consecutive packed rows of one head; lane l owns channels
+// 4l..4l+3 of the head in all three planes and keeps their conv weights and a sliding window of
+// the last K raw samples in registers, so every raw sample is read once (plus the K-1 halo rows
+// of the run), as 8-byte bf16x4 (or 16-byte f32x4) vectors, one row ahead of its use.  The l2
+// norm is one warp butterfly per row; every output row is a 512-byte coalesced store.  A run may
+// straddle sequence boundaries (varlen): the window restarts from the next sequence's ring.  The
+// ring is rewritten by a second, tiny kernel launched after this one on the same stream, so
+// ring_in and ring_out may be the same buffer.
 #include "kda_device.cuh"
 #include "kda_internal.h"
 
 namespace kda {
 
-constexpr int kRowsPerCta = 8;
-constexpr int kPrepThreads = 32 * kRowsPerCta;
+constexpr int kRun = 16;               // rows per warp
+constexpr int kPrepWarps = 8;          // warps (runs) per CTA
+constexpr int kPrepThreads = 32 * kPrepWarps;
 
-// Sequence containing packed row r: its index and first row (rows of empty sequences skipped).
-__device__ __forceinline__ void seq_of_row(const SeqLayout& L, long r, int& n, long& begin) {
+// Sequence holding packed row r: index n, first row begin, one-past-last row end.
+__device__ __forceinline__ void seq_of_row(const SeqLayout& L, long r, int& n, long& begin,
+                                           long& end) {
     if (L.cu_seqlens == nullptr) {
         n = (int)(r / L.T_uniform);
         begin = (long)n * L.T_uniform;
+        end = begin + L.T_uniform;
         return;
     }
     int lo = 0, hi = L.N;  // largest n with cu[n] <= r: its sequence is non-empty and holds r
@@ -39,6 +43,7 @@ __device__ __forceinline__ void seq_of_row(const SeqLayout& L, long r, int& n, l
     }
     n = lo;
     begin = L.cu_seqlens[lo];
+    end = L.cu_seqlens[lo + 1];
 }
 
 template <bool BF16>
@@ -53,37 +58,51 @@ __device__ __forceinline__ float4 load_raw4(const void* base, long idx) {
     }
 }
 
-__device__ __forceinline__ float4 silu4(const float4& x) {
-    return make_float4(silu_f(x.x), silu_f(x.y), silu_f(x.z), silu_f(x.w));
+// Register state of one plane for this lane's 4 channels: weights and window, aligned to the end
+// (slot KW-1 = the current sample).
+template <int KW>
+struct PlaneWin {
+    float w[4][KW];
+    float x[4][KW];
+};
+
+template <int KW>
+__device__ __forceinline__ void pw_push(PlaneWin<KW>& P, const float4& v) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+#pragma unroll
+        for (int m = 0; m < KW - 1; ++m) P.x[e][m] = P.x[e][m + 1];
+    P.x[0][KW - 1] = v.x; P.x[1][KW - 1] = v.y; P.x[2][KW - 1] = v.z; P.x[3][KW - 1] = v.w;
 }
 
-// Conv taps of one plane for 4 channels at position p of its sequence (row r, first row begin):
-// acc = sum_j w[c][j] * xt[p + j] with xt = ring ++ rows, taps summed oldest first (fmaf from 0).
+template <int KW>
+__device__ __forceinline__ float4 pw_conv_silu(const PlaneWin<KW>& P, int K) {
+    return make_float4(silu_f(conv_taps_f(P.w[0], P.x[0], K)), silu_f(conv_taps_f(P.w[1], P.x[1], K)),
+                       silu_f(conv_taps_f(P.w[2], P.x[2], K)), silu_f(conv_taps_f(P.w[3], P.x[3], K)));
+}
+
+// Fill the window with the K-1 samples preceding position p of the sequence that starts at row
+// begin: slot KW-d holds the sample at p-d (raw rows when p-d >= 0, else the ring, oldest first).
 template <bool BF16, int KW>
-__device__ __forceinline__ float4 conv4(const void* raw, long C, int c, const float* ring_in,
-                                        long ring_row0, const float (&w)[4][KW], int K, long r,
+__device__ __forceinline__ void pw_fill(PlaneWin<KW>& P, const void* raw, long C, int c,
+                                        const float* ring_in, long ring_row0, int R, long begin,
                                         long p) {
-    const int R = K - 1;
-    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
     for (int m = 0; m < KW; ++m) {
-        const int j = m - (KW - K);            // tap index (0 = oldest)
-        if (j < 0) continue;
-        const long pos = p - R + j;            // position of the sample this tap reads
-        float4 x;
-        if (pos >= 0) {
-            x = load_raw4<BF16>(raw, (r - (p - pos)) * C + c);
-        } else {
-            const long s = R + pos;            // ring slot (0 = oldest)
-            x = make_float4(ring_in[ring_row0 + 0 * R + s], ring_in[ring_row0 + 1 * R + s],
-                            ring_in[ring_row0 + 2 * R + s], ring_in[ring_row0 + 3 * R + s]);
+        const int d = KW - m;
+        float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        if (d <= R) {
+            const long pos = p - d;
+            if (pos >= 0) {
+                v = load_raw4<BF16>(raw, (begin + pos) * C + c);
+            } else {
+                const long s2 = R + pos;
+                v = make_float4(ring_in[ring_row0 + s2], ring_in[ring_row0 + R + s2],
+                                ring_in[ring_row0 + 2 * R + s2], ring_in[ring_row0 + 3 * R + s2]);
+            }
         }
-        acc[0] = fmaf(w[0][m], x.x, acc[0]);
-        acc[1] = fmaf(w[1][m], x.y, acc[1]);
-        acc[2] = fmaf(w[2][m], x.z, acc[2]);
-        acc[3] = fmaf(w[3][m], x.w, acc[3]);
+        P.x[0][m] = v.x; P.x[1][m] = v.y; P.x[2][m] = v.z; P.x[3][m] = v.w;
     }
-    return make_float4(acc[0], acc[1], acc[2], acc[3]);
 }
 
 // EXP: write the decay factor exp(g) instead of the log-decay g.  KW: compile-time bound on K.
@@ -91,63 +110,96 @@ template <bool BF16, int GATE_MODE, bool CONV, bool EXP, int KW>
 __global__ void __launch_bounds__(kPrepThreads) kda_prep_kernel(PrepArgs a) {
     const int h = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const long r = (long)blockIdx.x * kRowsPerCta + warp;
-    if (r >= a.seq.total_rows) return;
+    const long r0 = ((long)blockIdx.x * kPrepWarps + warp) * kRun;
+    const long rows = a.seq.total_rows;
+    if (r0 >= rows) return;
+    const int nr = (int)min((long)kRun, rows - r0);
     const int H = a.H;
     const long C = (long)H * kHeadDim;
     const int c = h * kHeadDim + 4 * lane;     // first of this lane's 4 channels in a plane
-    const int K = a.K;
+    const int K = a.K, R = a.K - 1;
 
-    float4 xq, xk, xv;
+    PlaneWin<KW> pq, pk, pv;
+    int n = 0;
+    long begin = 0, end = 0;
     if constexpr (CONV) {
-        int n;
-        long begin;
-        seq_of_row(a.seq, r, n, begin);
-        const long p = r - begin;
-        const int R = K - 1;
-        float wq[4][KW], wk[4][KW], wv[4][KW];
 #pragma unroll
         for (int e = 0; e < 4; ++e)
 #pragma unroll
             for (int m = 0; m < KW; ++m) {
                 const int j = m - (KW - K);
-                wq[e][m] = j >= 0 ? a.conv_w[(0 * C + c + e) * K + j] : 0.0f;
-                wk[e][m] = j >= 0 ? a.conv_w[(1 * C + c + e) * K + j] : 0.0f;
-                wv[e][m] = j >= 0 ? a.conv_w[(2 * C + c + e) * K + j] : 0.0f;
+                pq.w[e][m] = j >= 0 ? a.conv_w[(0 * C + c + e) * K + j] : 0.0f;
+                pk.w[e][m] = j >= 0 ? a.conv_w[(1 * C + c + e) * K + j] : 0.0f;
+                pv.w[e][m] = j >= 0 ? a.conv_w[(2 * C + c + e) * K + j] : 0.0f;
             }
+        seq_of_row(a.seq, r0, n, begin, end);
         const long rr = (long)n * 3 * C * R;
-        xq = silu4(conv4<BF16, KW>(a.q_raw, C, c, a.ring_in, rr + (0 * C + c) * R, wq, K, r, p));
-        xk = silu4(conv4<BF16, KW>(a.k_raw, C, c, a.ring_in, rr + (1 * C + c) * R, wk, K, r, p));
-        xv = silu4(conv4<BF16, KW>(a.v_raw, C, c, a.ring_in, rr + (2 * C + c) * R, wv, K, r, p));
-    } else {
-        xq = load_raw4<BF16>(a.q_raw, r * C + c);
-        xk = load_raw4<BF16>(a.k_raw, r * C + c);
-        xv = load_raw4<BF16>(a.v_raw, r * C + c);
+        pw_fill<BF16, KW>(pq, a.q_raw, C, c, a.ring_in, rr + (0 * C + c) * R, R, begin, r0 - begin);
+        pw_fill<BF16, KW>(pk, a.k_raw, C, c, a.ring_in, rr + (1 * C + c) * R, R, begin, r0 - begin);
+        pw_fill<BF16, KW>(pv, a.v_raw, C, c, a.ring_in, rr + (2 * C + c) * R, R, begin, r0 - begin);
     }
-    *reinterpret_cast<float4*>(a.v_hat + r * C + c) = xv;
-
-    // l2 norm over the head's 128 channels: lane partial, then one warp butterfly
-    float sq = __fmul_rn(xq.x, xq.x);
-    sq = fmaf(xq.y, xq.y, sq); sq = fmaf(xq.z, xq.z, sq); sq = fmaf(xq.w, xq.w, sq);
-    float sk = __fmul_rn(xk.x, xk.x);
-    sk = fmaf(xk.y, xk.y, sk); sk = fmaf(xk.z, xk.z, sk); sk = fmaf(xk.w, xk.w, sk);
-    const float iq = l2_inv_f(warp_sum(sq), a.l2_eps);
-    const float ik = l2_inv_f(warp_sum(sk), a.l2_eps);
-    *reinterpret_cast<float4*>(a.q_hat + r * C + c) =
-        make_float4(xq.x * iq, xq.y * iq, xq.z * iq, xq.w * iq);
-    *reinterpret_cast<float4*>(a.k_hat + r * C + c) =
-        make_float4(xk.x * ik, xk.y * ik, xk.z * ik, xk.w * ik);
-
+    float rate = 0.0f;
+    float4 dt = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
     if constexpr (GATE_MODE == 0) {
-        const float rate = expf(a.a_log[h]);
-        const float4 f = *reinterpret_cast<const float4*>(a.f_raw + r * C + c);
-        const float4 dt = *reinterpret_cast<const float4*>(a.dt_bias + c);
-        float4 g = make_float4(kda_gate_f(f.x, dt.x, rate, a.gate_lb), kda_gate_f(f.y, dt.y, rate, a.gate_lb),
-                               kda_gate_f(f.z, dt.z, rate, a.gate_lb), kda_gate_f(f.w, dt.w, rate, a.gate_lb));
-        if (EXP) g = make_float4(decay_f(g.x), decay_f(g.y), decay_f(g.z), decay_f(g.w));
-        *reinterpret_cast<float4*>(a.g + r * C + c) = g;
+        rate = expf(a.a_log[h]);
+        dt = *reinterpret_cast<const float4*>(a.dt_bias + c);
     }
-    if (lane == 0) {
+
+    // row-ahead prefetch of the raw samples and f
+    float4 nq = load_raw4<BF16>(a.q_raw, r0 * C + c);
+    float4 nk = load_raw4<BF16>(a.k_raw, r0 * C + c);
+    float4 nv = load_raw4<BF16>(a.v_raw, r0 * C + c);
+    float4 nf = GATE_MODE == 0 ? *reinterpret_cast<const float4*>(a.f_raw + r0 * C + c)
+                               : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    for (int i = 0; i < nr; ++i) {
+        const long r = r0 + i;
+        const float4 cq = nq, ck = nk, cv = nv, cf = nf;
+        if (i + 1 < nr) {
+            nq = load_raw4<BF16>(a.q_raw, (r + 1) * C + c);
+            nk = load_raw4<BF16>(a.k_raw, (r + 1) * C + c);
+            nv = load_raw4<BF16>(a.v_raw, (r + 1) * C + c);
+            if (GATE_MODE == 0) nf = *reinterpret_cast<const float4*>(a.f_raw + (r + 1) * C + c);
+        }
+        float4 xq, xk, xv;
+        if constexpr (CONV) {
+            if (r >= end) {  // entered the next non-empty sequence: restart the windows
+                seq_of_row(a.seq, r, n, begin, end);
+                const long rr = (long)n * 3 * C * R;
+                pw_fill<BF16, KW>(pq, a.q_raw, C, c, a.ring_in, rr + (0 * C + c) * R, R, begin, 0);
+                pw_fill<BF16, KW>(pk, a.k_raw, C, c, a.ring_in, rr + (1 * C + c) * R, R, begin, 0);
+                pw_fill<BF16, KW>(pv, a.v_raw, C, c, a.ring_in, rr + (2 * C + c) * R, R, begin, 0);
+            }
+            pw_push(pq, cq);
+            pw_push(pk, ck);
+            pw_push(pv, cv);
+            xq = pw_conv_silu(pq, K);
+            xk = pw_conv_silu(pk, K);
+            xv = pw_conv_silu(pv, K);
+        } else {
+            xq = cq;
+            xk = ck;
+            xv = cv;
+        }
+        *reinterpret_cast<float4*>(a.v_hat + r * C + c) = xv;
+        float sq = __fmul_rn(xq.x, xq.x);
+        sq = fmaf(xq.y, xq.y, sq); sq = fmaf(xq.z, xq.z, sq); sq = fmaf(xq.w, xq.w, sq);
+        float sk = __fmul_rn(xk.x, xk.x);
+        sk = fmaf(xk.y, xk.y, sk); sk = fmaf(xk.z, xk.z, sk); sk = fmaf(xk.w, xk.w, sk);
+        const float iq = l2_inv_f(warp_sum(sq), a.l2_eps);
+        const float ik = l2_inv_f(warp_sum(sk), a.l2_eps);
+        *reinterpret_cast<float4*>(a.q_hat + r * C + c) =
+            make_float4(xq.x * iq, xq.y * iq, xq.z * iq, xq.w * iq);
+        *reinterpret_cast<float4*>(a.k_hat + r * C + c) =
+            make_float4(xk.x * ik, xk.y * ik, xk.z * ik, xk.w * ik);
+        if constexpr (GATE_MODE == 0) {
+            float4 g = make_float4(kda_gate_f(cf.x, dt.x, rate, a.gate_lb), kda_gate_f(cf.y, dt.y, rate, a.gate_lb),
+                                   kda_gate_f(cf.z, dt.z, rate, a.gate_lb), kda_gate_f(cf.w, dt.w, rate, a.gate_lb));
+            if (EXP) g = make_float4(decay_f(g.x), decay_f(g.y), decay_f(g.z), decay_f(g.w));
+            *reinterpret_cast<float4*>(a.g + r * C + c) = g;
+        }
+    }
+    if (lane < nr) {
+        const long r = r0 + lane;
         a.beta[r * H + h] = sigmoid_f(a.beta_raw[r * H + h]);
         if constexpr (GATE_MODE == 1) {
             const float gl = gdn_gate_f(a.f_raw[r * H + h], a.dt_bias[h], a.a_log[h]);
@@ -201,7 +253,7 @@ __global__ void __launch_bounds__(256) kda_ring_roll_kernel(PrepArgs a) {
 
 template <bool BF16, int GM, bool CONV, bool EXP>
 static cudaError_t launch_prep_t(const PrepArgs& a, cudaStream_t s) {
-    const long tiles = (a.seq.total_rows + kRowsPerCta - 1) / kRowsPerCta;
+    const long tiles = (a.seq.total_rows + (long)kRun * kPrepWarps - 1) / ((long)kRun * kPrepWarps);
     if (tiles > 0) {
         dim3 grid((unsigned)tiles, (unsigned)a.H);
         if (a.K <= 4) kda_prep_kernel<BF16, GM, CONV, EXP, 4><<<grid, kPrepThreads, 0, s>>>(a);
