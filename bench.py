@@ -144,7 +144,7 @@ def _traffic(kernel, files):
 
 
 def _prefill_e2e(args, d, buf, state_out, ring_out, stream, barrier, max_over_ranks, mixer,
-                 algo, ws, T, H, C):
+                 algo, ws, T, H, C, workspace):
     """Prefill through the public API with inputs copied from pinned host memory and y, the final
     state and the ring read back every step."""
     import torch
@@ -161,7 +161,7 @@ def _prefill_e2e(args, d, buf, state_out, ring_out, stream, barrier, max_over_ra
         for k, v in host.items():
             dev_in[k].copy_(v, non_blocking=True)
         out = mixer.kda_forward(H=H, N=1, T=T, algo=algo, out=buf, state_out=state_out,
-                                ring_out=ring_out, **dev_in)
+                                ring_out=ring_out, workspace=workspace, **dev_in)
         y_host.copy_(out["y"], non_blocking=True)
         st_host.copy_(out["state_out"], non_blocking=True)
         ring_host.copy_(out["ring_out"], non_blocking=True)
@@ -224,6 +224,7 @@ def run_ours(args):
     algo = {"auto": kda.ALGO_AUTO, "seq": kda.ALGO_SEQ, "chunk": kda.ALGO_CHUNK}[args.scan_algo]
     # the sequential form consumes decay factors, the chunked form log-decays
     gate_mode = kda.GATE_PER_CHANNEL | (kda.GATE_EXP if algo == kda.ALGO_SEQ else 0)
+    workspace = kda.scan_workspace(1, T, H, dev, algo)   # scratch of the chunked form
 
     ev = {}
 
@@ -236,7 +237,7 @@ def run_ours(args):
             timed_scan[0].record(stream)
         kda.kda_scan(buf["q_hat"], buf["k_hat"], buf["v_hat"], buf["g"], buf["beta"],
                      d["state_in"], state_out, buf["o"], N=1, T=T, H=H, gate_mode=gate_mode,
-                     algo=algo)
+                     algo=algo, workspace=workspace)
         if timed_scan is not None:
             timed_scan[1].record(stream)
         kda.kda_gated_rmsnorm_out(buf["o"], d["norm_w"], d["gate_raw"], buf["y"], rows=T * H)
@@ -270,7 +271,7 @@ def run_ours(args):
     e2e = None
     if not args.skip_e2e:
         e2e = _prefill_e2e(args, d, buf, state_out, ring_out, stream, barrier, max_over_ranks,
-                           mixer, algo, ws, T, H, C)
+                           mixer, algo, ws, T, H, C, workspace)
 
     # ---------------- decode step (fused kernel) ----------------
     dec = inputs.decode_step(N=DEC_N, T=1, H=DEC_H)

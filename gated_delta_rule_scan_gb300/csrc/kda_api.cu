@@ -90,11 +90,20 @@ int prep_impl(const void* q_raw, const void* k_raw, const void* v_raw, int raw_d
     return cuda_status(launch_prep(a, static_cast<cudaStream_t>(stream)));
 }
 
+// Shortest longest-sequence for which AUTO takes the chunked form (measured crossover).
+constexpr long kAutoChunkMinLen = 64;
+
+long max_len(const SeqLayout& seq, const int* cu_host) {
+    if (seq.cu_seqlens == nullptr) return seq.T_uniform;
+    long m = 0;
+    for (int n = 0; n < seq.N; ++n) m = cu_host[n + 1] - cu_host[n] > m ? cu_host[n + 1] - cu_host[n] : m;
+    return m;
+}
+
 int scan_impl(const float* q, const float* k, const float* v, const float* g, int gate_mode,
               const float* beta, const float* state_in, float* state_out, float* o,
-              const SeqLayout& seq, int H, int D, float scale, int algo, void* workspace,
-              size_t workspace_bytes, void* stream) {
-    (void)workspace; (void)workspace_bytes;
+              const SeqLayout& seq, const int* cu_host, int H, int D, float scale, int algo,
+              void* workspace, size_t workspace_bytes, void* stream) {
     if (D != kHeadDim) return KDA_ERR_HEAD_DIM;
     if (seq.N < 0 || seq.N > kMaxGridY || seq.total_rows < 0 || H <= 0) return KDA_ERR_SHAPE;
     if (gate_mode < 0 || gate_mode > (KDA_GATE_PER_HEAD | KDA_GATE_EXP)) return KDA_ERR_ENUM;
@@ -115,9 +124,13 @@ int scan_impl(const float* q, const float* k, const float* v, const float* g, in
     a.q = q; a.k = k; a.v = v; a.g = g; a.gate_mode = gate_mode; a.beta = beta;
     a.state_in = state_in; a.state_out = state_out; a.o = o;
     a.seq = seq; a.H = H; a.scale = scale; a.order = nullptr;
+    const size_t need = chunk_workspace_bytes(seq, cu_host, H);
+    const bool ws_ok = workspace != nullptr && workspace_bytes >= need && aligned16(workspace);
+    bool chunk = algo == KDA_ALGO_CHUNK;
+    if (chunk && !ws_ok) return workspace && !aligned16(workspace) ? KDA_ERR_ALIGN : KDA_ERR_WORKSPACE;
+    if (algo == KDA_ALGO_AUTO) chunk = ws_ok && max_len(seq, cu_host) >= kAutoChunkMinLen;
     a.err = dev_err_ptr();  // null only if the symbol lookup failed: waits then report nothing
-    const bool chunk = algo == KDA_ALGO_CHUNK;
-    return cuda_status(chunk ? launch_scan_chunk(a, static_cast<cudaStream_t>(stream))
+    return cuda_status(chunk ? launch_scan_chunk(a, cu_host, workspace, static_cast<cudaStream_t>(stream))
                              : launch_scan_seq(a, static_cast<cudaStream_t>(stream)));
 }
 
@@ -181,8 +194,14 @@ int kda_conv_l2norm_prep_varlen(const void* q_raw, const void* k_raw, const void
 }
 
 size_t kda_scan_workspace_bytes(int N, int total_T, int H, int D, int gate_mode, int algo) {
-    (void)N; (void)total_T; (void)H; (void)D; (void)gate_mode; (void)algo;
-    return 0;
+    (void)gate_mode;
+    if (N < 0 || total_T < 0 || H <= 0 || D != kHeadDim) return 0;
+    if (algo == KDA_ALGO_SEQ) return 0;
+    // every sequence contributes ceil(L / kChunkTokens) chunks <= L / kChunkTokens + 1, plus the
+    // varlen header of chunk offsets
+    const size_t chunks = (size_t)(total_T + kChunkTokens - 1) / kChunkTokens + (size_t)N;
+    const size_t header = (((size_t)N + 1) * 4 + 255) / 256 * 256;
+    return header + chunks * (size_t)H * kChunkBlockBytes;
 }
 
 int kda_scan(const float* q_hat, const float* k_hat, const float* v_hat, const float* g,
@@ -191,8 +210,8 @@ int kda_scan(const float* q_hat, const float* k_hat, const float* v_hat, const f
              size_t workspace_bytes, void* stream) {
     if (N < 0 || T < 0) return KDA_ERR_SHAPE;
     SeqLayout seq{nullptr, T, N, (long)N * T};
-    return scan_impl(q_hat, k_hat, v_hat, g, gate_mode, beta, state_in, state_out, o, seq, H, D,
-                     scale, algo, workspace, workspace_bytes, stream);
+    return scan_impl(q_hat, k_hat, v_hat, g, gate_mode, beta, state_in, state_out, o, seq, nullptr,
+                     H, D, scale, algo, workspace, workspace_bytes, stream);
 }
 
 int kda_scan_varlen(const float* q_hat, const float* k_hat, const float* v_hat, const float* g,
@@ -207,8 +226,8 @@ int kda_scan_varlen(const float* q_hat, const float* k_hat, const float* v_hat, 
         if (rc) return rc;
     }
     SeqLayout seq{cu_seqlens, 0, N, (long)total_T};
-    return scan_impl(q_hat, k_hat, v_hat, g, gate_mode, beta, state_in, state_out, o, seq, H, D,
-                     scale, algo, workspace, workspace_bytes, stream);
+    return scan_impl(q_hat, k_hat, v_hat, g, gate_mode, beta, state_in, state_out, o, seq,
+                     cu_seqlens_host, H, D, scale, algo, workspace, workspace_bytes, stream);
 }
 
 int kda_gated_rmsnorm_out(const float* o, const float* norm_w, const float* gate_raw, float* y,

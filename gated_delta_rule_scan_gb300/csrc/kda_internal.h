@@ -58,7 +58,12 @@ struct DecodeArgs {
 
 cudaError_t launch_prep(const PrepArgs& a, cudaStream_t s);
 cudaError_t launch_scan_seq(const ScanArgs& a, cudaStream_t s);
-cudaError_t launch_scan_chunk(const ScanArgs& a, cudaStream_t s);
+cudaError_t launch_scan_chunk(const ScanArgs& a, const int* cu_host, void* workspace,
+                              cudaStream_t s);
+// exact workspace the chunked scan needs for this layout (cu_host: host copy of cu_seqlens)
+size_t chunk_workspace_bytes(const SeqLayout& s, const int* cu_host, int H);
+constexpr int kChunkTokens = 32;        // tokens per chunk of the chunked scan
+constexpr size_t kChunkBlockBytes = 70144;  // workspace bytes per (chunk, head)
 
 // 2-D f32 tensor map over [rows, cols] (row stride = cols), box [box_rows, box_cols], no swizzle.
 bool make_tensor_map_2d(CUtensorMap* m, const float* base, long rows, long cols, int box_cols,

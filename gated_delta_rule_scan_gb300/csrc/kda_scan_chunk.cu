@@ -1,5 +1,5 @@
 // kda_scan_chunk.cu -- the chunked (UT / WY) form of the per-channel gated delta rule on the
-// tcgen05 tensor cores.
+// tcgen05 tensor cores: a parallel intra-chunk kernel and a sequential inter-chunk kernel.
 //
 // Method: "memra_engine/kda.rs" (memra-engine 0.125.0) module doc, the chunked twin: KDA's decay
 // is per channel, so the chunk form carries a per-channel cumulative log gate Gcum[t][i] with k
@@ -17,120 +17,75 @@
 //     S_C       = Diag(Gamma_C) S0 + (K * Gamma_C / Gamma)^T U'
 // (the algebra is pinned against the sequential oracle at every chunk size by the test suite).
 //
-// GB300 design.  One CTA (128 threads) owns one (sequence, head) and walks its chunks of kCc = 16
-// tokens; thread i is TMEM lane i and, depending on the phase, key channel k = i or value row
-// v = i.  The state is kept transposed (S^T, value rows) in that thread's registers, f32, for the
-// whole sequence.  Every contraction runs on tcgen05 (M = 128, f32 accumulators in TMEM) with
-// bf16 operands written by the threads into shared memory in the K-major core-matrix layout;
-// each operand is split x = hi + lo (bf16 each) and every product is hi*hi + hi*lo + lo*hi, which
-// keeps ~16 significant bits (relative error ~1e-5, far inside the 1e-3 parity bound; one bf16
-// pass is ~4e-3).  Per chunk:
-//   MMA-a   [A/beta | Aqk]^T  = (K e^{c-G}) (K e^{G-c} | Q e^{G-c})^T      M=128 (16 used), N=32
-//           (c = half the chunk's total gate per channel, so every exponent stays inside f32)
-//   Tm      forward substitution on 16 lanes
-//   MMA-b   [W^T | U^T]       = (beta K e^G | beta V)^T Tm^T                  M=128, N=16+16, K=16
-//   MMA-1   [O1^T | X^T]      = S^T (Q e^G | W)^T                             M=128, N=32, K=128
-//   U'^T = U^T - X^T                                                         (registers)
-//   MMA-2   [dS^T | O2^T]     = U'^T (K e^{G_C-G} | Aqk)                      M=128, N=144, K=16
-//   S^T <- S^T Diag(e^{G_C}) + dS^T,  o = scale (O1 + O2)                    (registers)
-// The per-token q, k, v, g rows stream in by 2-D TMA, double-buffered, with bounded mbarrier
-// waits; MMA completion is tracked by tcgen05.commit on an mbarrier.  For the per-head (GDN) gate
-// the decay factors are scalars per token, so A and Aqk are formed from unscaled k, q and scaled
-// after the MMA, which removes any range limit on the gate.  For the per-channel gate the chunk's
-// total log-decay must stay above -170 on every channel (the KDA gate is bounded below by -5 per
-// token, so 16 tokens stay above -80); otherwise the kernel raises the device error word.
+// GB300 design.  Chunks are kCc = 32 tokens.  Everything that does not depend on the state -- A,
+// Aqk, Tm, W, U and the decayed k / q -- is computed by kda_chunk_intra_kernel for every
+// (chunk, head) at once, in parallel over the whole GPU, and written to the caller's workspace as
+// ready-to-use tensor-core operand images.  kda_chunk_inter_kernel then walks each (sequence,
+// head)'s chunks in order with only two dependent MMA stages per chunk:
+//     [O1^T | X^T]  = S^T   (Q e^G | W)^T          M=128 (value rows), N=64,  K=128
+//     U'^T          = U^T - X^T
+//     [dS^T | O2^T] = U'^T  (K e^{G_C-G} | Aqk)    M=128,              N=160, K=32
+//     S^T <- S^T Diag(e^{G_C}) + dS^T,   o = scale (O1 + O2)
+// with S^T and U'^T held in tensor memory as the MMAs' A operands and the state row kept in f32
+// registers.  All operands are bf16 split as x = hi + lo and every product is
+// hi*hi + hi*lo + lo*hi (about 16 significant bits; relative error ~1e-5, inside the 1e-3 parity
+// bound, where one bf16 pass gives ~4e-3).  Shared-memory operands are K-major, no swizzle,
+// 8-row x 16-byte core matrices (kda_tc.cuh).
+//
+// Range.  The intra-chunk products pair k_t e^{G_t - c} with k_s e^{c - G_s}, c = half the
+// chunk's total gate per channel, so each factor stays below e^{|G_C|/2}.  For the per-channel
+// gate the chunk's total log-decay must stay above -170 on every channel (the KDA gate's lower
+// bound of -5 per token gives -160 over 32 tokens); beyond that the kernel raises the device error
+// word.  The per-head (GDN) gate forms A and Aqk from unscaled k and q and applies the scalar
+// e^{G_t - G_s} <= 1 after the MMA, so it has no range limit.
 #include "kda_tc.cuh"
 
 namespace kda {
 
-constexpr int kCc = 16;
-constexpr int kChThreads = 128;
-constexpr uint32_t kSboK128 = 2048;  // 8-row group stride of a K = 128 bf16 image
-constexpr uint32_t kSboK16 = 256;    // 8-row group stride of a K = 16 bf16 image
-constexpr int kDevErrRange = 2;      // device error word bit: chunk gate outside the f32 range
+constexpr int kCc = 32;                  // tokens per chunk
+constexpr int kThr = 128;                // both kernels: thread = TMEM lane
+constexpr uint32_t kSbo128 = 2048;       // 8-row group stride, K = 128 bf16 image
+constexpr uint32_t kSbo32 = 512;         // 8-row group stride, K = 32 bf16 image
+constexpr int kDevErrRange = 2;          // device error word bit: chunk gate outside f32 range
 
-constexpr int kImgA1 = 128 * 128 * 2;  // S^T            [128 v  x 128 k]
-constexpr int kImgKB = kCc * 128 * 2;  // K e^{c-G}      [16 s   x 128 k]  (descriptor spans 32 KB)
-constexpr int kImgBI = 64 * 128 * 2;   // K e^{G-c} ; Q e^{G-c} ; Q e^G ; W   [64 x 128 k]
-constexpr int kImgKT = 128 * kCc * 2;  // (beta K e^G)^T [128 k  x 16 s]
-constexpr int kImgVT = 128 * kCc * 2;  // (beta V)^T     [128 v  x 16 s]
-constexpr int kImgTM = kCc * kCc * 2;  // Tm             [16 t   x 16 s]
-constexpr int kImgB2 = 144 * kCc * 2;  // (K e^{G_C-G})^T ; Aqk  [144 x 16]
-constexpr int kImgA2 = 128 * kCc * 2;  // U'^T           [128 v  x 16 t]
+// ---- workspace block of one (chunk, head) ----------------------------------------------------
+constexpr int kQWBytes = 64 * 128 * 2;             // [Q e^G (32 rows) ; W (32 rows)] x 128 k
+constexpr int kB2Bytes = (128 + kCc) * kCc * 2;    // [(K e^{G_C-G})^T (128 rows) ; Aqk (32)] x 32
+constexpr int kUTBytes = 128 * kCc * 4;            // U^T f32 [128 v][32 t]
+constexpr int kEGBytes = 128 * 4;                  // e^{G_C} f32 [128]
+constexpr int kOffQW = 0;                          // hi, then lo at + kQWBytes
+constexpr int kOffB2 = 2 * kQWBytes;               // hi, then lo at + kB2Bytes
+constexpr int kOffUT = kOffB2 + 2 * kB2Bytes;
+constexpr int kOffEG = kOffUT + kUTBytes;
+constexpr int kBlkBytes = kOffEG + kEGBytes;       // 70144
+static_assert(kBlkBytes % 128 == 0, "workspace blocks stay 128-byte aligned");
+constexpr int kHeaderAlign = 256;
 
-// TMEM columns of the four accumulators (256 allocated)
-constexpr uint32_t kTmA = 0, kTmB = 32, kTm1 = 64, kTm2 = 96;
-
-struct __align__(1024) ChunkSmem {
-    // operand images, [0] = hi, [1] = lo; kb is followed by a1 so that kb's 128-row descriptor
-    // (only its first 16 rows are used) stays inside this allocation
-    unsigned char kb[2][kImgKB];
-    unsigned char a1[2][kImgA1];
-    unsigned char bi[2][kImgBI];
-    unsigned char kt[2][kImgKT];
-    unsigned char vt[2][kImgVT];
-    unsigned char tm[2][kImgTM];
-    unsigned char b2[2][kImgB2];
-    unsigned char a2[2][kImgA2];
-    // staged chunk rows (TMA, double-buffered); g is turned into the cumulative gate in place
-    float q[2][kCc][128];
-    float k[2][kCc][128];
-    float v[2][kCc][128];
-    float g[2][kCc][128];
-    float beta[2][kCc];
-    float gs[2][kCc];            // per-head gate of the chunk (GDN), cumulative after phase 1
-    float cref[128];             // per-channel reference: half the chunk's total log-decay
-    float ecr[128];              // e^{cref}
-    float egc[128];              // e^{G_C}: the chunk's total decay per channel
-    float amat[kCc][kCc];        // beta_t A[t][s], strictly lower
-    uint64_t bar_tma[2];
-    uint64_t bar_mma;
-    uint32_t tmem_base;
-};
-
-// byte offset of element (row, col) in a bf16 image with 8-row group stride sbo
-__device__ __forceinline__ uint32_t img_off(int row, int col, uint32_t sbo) {
-    return tc_offset(row, col, sbo);
-}
-
-// store x at byte offset off of an image pair (hi, lo)
-template <int BYTES>
-__device__ __forceinline__ void put1(unsigned char (&im)[2][BYTES], uint32_t off, float x) {
-    __nv_bfloat16 hi, lo;
-    split_bf16(x, hi, lo);
-    *reinterpret_cast<__nv_bfloat16*>(&im[0][off]) = hi;
-    *reinterpret_cast<__nv_bfloat16*>(&im[1][off]) = lo;
-}
-
-// store 8 consecutive-k values (one 16-byte core-matrix row) at byte offset off
-template <int BYTES>
-__device__ __forceinline__ void put8(unsigned char (&im)[2][BYTES], uint32_t off, const float (&x)[8]) {
+// store 8 values (one 16-byte core-matrix row) as bf16 hi / lo at byte offset off of two images
+__device__ __forceinline__ void put8x(unsigned char* hi_img, unsigned char* lo_img, uint32_t off,
+                                      const float (&x)[8]) {
     uint4 hi, lo;
     split_bf16x2(x[0], x[1], hi.x, lo.x);
     split_bf16x2(x[2], x[3], hi.y, lo.y);
     split_bf16x2(x[4], x[5], hi.z, lo.z);
     split_bf16x2(x[6], x[7], hi.w, lo.w);
-    *reinterpret_cast<uint4*>(&im[0][off]) = hi;
-    *reinterpret_cast<uint4*>(&im[1][off]) = lo;
+    *reinterpret_cast<uint4*>(hi_img + off) = hi;
+    *reinterpret_cast<uint4*>(lo_img + off) = lo;
 }
 
-// A pair of descriptors (hi, lo) of one operand image.
-struct DescPair {
-    uint64_t hi, lo;
-};
-
-template <int BYTES>
-__device__ __forceinline__ DescPair desc_pair(unsigned char (&im)[2][BYTES], uint32_t byte_off,
-                                              uint32_t sbo) {
-    return {tc_smem_desc(smem_u32(im[0]) + byte_off, 128, sbo),
-            tc_smem_desc(smem_u32(im[1]) + byte_off, 128, sbo)};
+__device__ __forceinline__ void put1x(unsigned char* hi_img, unsigned char* lo_img, uint32_t off,
+                                      float x) {
+    __nv_bfloat16 h, l;
+    split_bf16(x, h, l);
+    *reinterpret_cast<__nv_bfloat16*>(hi_img + off) = h;
+    *reinterpret_cast<__nv_bfloat16*>(lo_img + off) = l;
 }
 
-// D (+)= A * B^T in bf16x3: hi*hi + hi*lo + lo*hi, nks K-steps of 16 (256 bytes each).
-__device__ __forceinline__ void mma_x3(uint32_t d, DescPair A, DescPair B, int nks,
-                                       uint32_t idesc) {
-    const uint64_t as[3] = {A.hi, A.hi, A.lo};
-    const uint64_t bs[3] = {B.hi, B.lo, B.hi};
+// D (+)= A * B^T, bf16x3, both operands in shared memory
+__device__ __forceinline__ void mma3_ss(uint32_t d, uint64_t a_hi, uint64_t a_lo, uint64_t b_hi,
+                                        uint64_t b_lo, int nks, uint32_t idesc) {
+    const uint64_t as[3] = {a_hi, a_hi, a_lo};
+    const uint64_t bs[3] = {b_hi, b_lo, b_hi};
 #pragma unroll
     for (int p = 0; p < 3; ++p)
         for (int ks = 0; ks < nks; ++ks)
@@ -138,398 +93,627 @@ __device__ __forceinline__ void mma_x3(uint32_t d, DescPair A, DescPair B, int n
                       p > 0 || ks > 0);
 }
 
-// GATE_MODE 0 per-channel, 1 per-head; EXP: g holds decay factors (take log first)
+// D[tmem] (+)= A[tmem] * B[smem desc]^T, issued by one thread
+__device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                         uint32_t idesc, bool accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"((uint32_t)accumulate)
+        : "memory");
+}
+
+// D (+)= A * B^T, bf16x3, A in tensor memory (hi at a_hi, lo at a_lo; 8 columns per K-step of
+// 16), B in shared memory
+__device__ __forceinline__ void mma3_ts(uint32_t d, uint32_t a_hi, uint32_t a_lo, uint64_t b_hi,
+                                        uint64_t b_lo, int nks, uint32_t idesc) {
+    const uint32_t as[3] = {a_hi, a_hi, a_lo};
+    const uint64_t bs[3] = {b_hi, b_lo, b_hi};
+#pragma unroll
+    for (int p = 0; p < 3; ++p)
+        for (int ks = 0; ks < nks; ++ks)
+            tc_mma_ts(d, as[p] + 8 * ks, tc_desc_advance(bs[p], 256 * ks), idesc, p > 0 || ks > 0);
+}
+
+__device__ __forceinline__ void seq_range(const SeqLayout& L, int n, long& begin, long& end) {
+    if (L.cu_seqlens == nullptr) {
+        begin = (long)n * L.T_uniform;
+        end = begin + L.T_uniform;
+    } else {
+        begin = L.cu_seqlens[n];
+        end = L.cu_seqlens[n + 1];
+    }
+}
+
+// first global chunk index of sequence n
+__device__ __forceinline__ long chunk_base(const SeqLayout& L, const int* chunk_off, int n) {
+    if (L.cu_seqlens == nullptr) return (long)n * ((L.T_uniform + kCc - 1) / kCc);
+    return chunk_off[n];
+}
+
+// ============================================================================================
+// kernel 0: per-sequence chunk offsets (varlen): chunk_off[n] = sum_{m<n} ceil(L_m / kCc)
+// ============================================================================================
+__global__ void __launch_bounds__(1024) kda_chunk_offsets_kernel(const int* cu, int N, int* out) {
+    __shared__ long part[1024];
+    const int tid = threadIdx.x;
+    const int per = (N + 1023) / 1024;
+    const int b = min(N, tid * per), e = min(N, b + per);
+    long sum = 0;
+    for (int n = b; n < e; ++n) sum += (cu[n + 1] - cu[n] + kCc - 1) / kCc;
+    part[tid] = sum;
+    __syncthreads();
+    if (tid == 0) {
+        long acc = 0;
+        for (int i = 0; i < 1024; ++i) { const long x = part[i]; part[i] = acc; acc += x; }
+        out[N] = (int)acc;
+    }
+    __syncthreads();
+    long acc = part[tid];
+    for (int n = b; n < e; ++n) {
+        out[n] = (int)acc;
+        acc += (cu[n + 1] - cu[n] + kCc - 1) / kCc;
+    }
+}
+
+// ============================================================================================
+// kernel 1: intra-chunk quantities, one CTA per (chunk, head)
+// ============================================================================================
+
+struct __align__(1024) IntraSmem {
+    // kb is followed by bia so that kb's 128-row descriptor (32 rows used) stays inside
+    unsigned char kb[2][kCc * 128 * 2];          // K e^{c-G}           [32 s x 128 k]
+    unsigned char bia[2][64 * 128 * 2];          // [K e^{G-c} ; Q e^{G-c}]  [64 x 128 k]
+    unsigned char kt[2][128 * kCc * 2];          // (beta K e^G)^T      [128 k x 32 s]
+    unsigned char vt[2][128 * kCc * 2];          // (beta V)^T          [128 v x 32 s]
+    unsigned char tm[2][kCc * kCc * 2];          // Tm                  [32 t x 32 s]
+    float G[kCc][128];                           // cumulative log-decay
+    float amat[kCc][kCc + 1];                    // beta_t A[t][s], strictly lower
+    float tinv[kCc][kCc + 1];                    // Tm (f32) while it is assembled
+    float beta[kCc];
+    float gs[kCc];                               // per-head cumulative gate (GDN)
+    float cref[128];
+    float ecr[128];
+    uint64_t bar;
+    uint32_t tmem_base;
+};
+
 template <int GATE_MODE, bool EXP>
-__global__ void __launch_bounds__(kChThreads, 1)
-kda_scan_chunk_kernel(ScanArgs a, const __grid_constant__ CUtensorMap tq,
-                      const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
-                      const __grid_constant__ CUtensorMap tg) {
+__global__ void __launch_bounds__(kThr, 2)
+kda_chunk_intra_kernel(ScanArgs a, const int* chunk_off, unsigned char* ws) {
     extern __shared__ unsigned char smem_raw[];
-    ChunkSmem& sm = *reinterpret_cast<ChunkSmem*>(
+    IntraSmem& sm = *reinterpret_cast<IntraSmem*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int h = blockIdx.x;
-    const int n = a.order ? a.order[blockIdx.y] : (int)blockIdx.y;
+    const int h = blockIdx.y;
+    const long gid = blockIdx.x;                 // global chunk index
     const int H = a.H;
     const long C = (long)H * kHeadDim;
-    long begin, end;
+
+    // chunk -> (sequence n, chunk c within it)
+    int n;
     if (a.seq.cu_seqlens == nullptr) {
-        begin = (long)n * a.seq.T_uniform;
-        end = begin + a.seq.T_uniform;
+        const long per = (a.seq.T_uniform + kCc - 1) / kCc;
+        n = (int)(gid / per);
     } else {
-        begin = a.seq.cu_seqlens[n];
-        end = a.seq.cu_seqlens[n + 1];
+        int lo = 0, hi = a.seq.N;                // largest n with chunk_off[n] <= gid
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if ((long)chunk_off[mid] <= gid) lo = mid; else hi = mid;
+        }
+        n = lo;
     }
-    const long L = end - begin;
-    const int nch = (int)((L + kCc - 1) / kCc);
+    long begin, end;
+    seq_range(a.seq, n, begin, end);
+    const long c = gid - chunk_base(a.seq, chunk_off, n);
+    const long row0 = begin + c * kCc;
+    const int nt = (int)min((long)kCc, end - row0);
+    unsigned char* blk = ws + ((long)gid * H + h) * kBlkBytes;
 
     if (warp == 0) {
-        tmem_alloc(&sm.tmem_base, 256);
+        tmem_alloc(&sm.tmem_base, 128);
         tmem_relinquish();
     }
     if (tid == 0) {
-        prefetch_tensormap(&tq);
-        prefetch_tensormap(&tk);
-        prefetch_tensormap(&tv);
-        if (GATE_MODE == 0) prefetch_tensormap(&tg);
-        mbar_init(&sm.bar_tma[0], 1);
-        mbar_init(&sm.bar_tma[1], 1);
-        mbar_init(&sm.bar_mma, 1);
+        mbar_init(&sm.bar, 1);
         fence_mbar_init();
     }
-    // this thread's state row S^T[v = tid][0..127]
-    float srow[128];
-    const float* sin = a.state_in + (((long)n * H + h) * kHeadDim + tid) * kHeadDim;
+
+    // ---- cumulative gate, beta ---------------------------------------------------------------
+    if (GATE_MODE == 0) {
+        float gv[kCc];
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-        const float4 x = __ldcs(reinterpret_cast<const float4*>(sin) + j);
-        srow[4 * j] = x.x; srow[4 * j + 1] = x.y; srow[4 * j + 2] = x.z; srow[4 * j + 3] = x.w;
-    }
-    auto write_a1 = [&]() {
+        for (int t = 0; t < kCc; ++t)
+            gv[t] = t < nt ? a.g[(row0 + t) * C + h * kHeadDim + tid] : (EXP ? 1.0f : 0.0f);
+        float G = 0.0f;
 #pragma unroll
-        for (int c8 = 0; c8 < 16; ++c8) {
-            float x[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) x[e] = srow[8 * c8 + e];
-            put8(sm.a1, img_off(tid, 8 * c8, kSboK128), x);
+        for (int t = 0; t < kCc; ++t) {
+            G += EXP ? logf(gv[t]) : gv[t];
+            sm.G[t][tid] = G;
         }
-    };
-    write_a1();
+        sm.cref[tid] = 0.5f * G;
+        sm.ecr[tid] = __expf(0.5f * G);
+        reinterpret_cast<float*>(blk + kOffEG)[tid] = decay_f(G);
+        if (G < -170.0f && a.err) atomicOr(a.err, kDevErrRange);
+    }
+    if (tid < kCc) {
+        const bool live = tid < nt;
+        sm.beta[tid] = live ? a.beta[(row0 + tid) * H + h] : 0.0f;
+        if (GATE_MODE == 1) {
+            const float x = live ? a.g[(row0 + tid) * H + h] : (EXP ? 1.0f : 0.0f);
+            sm.gs[tid] = EXP ? logf(x) : x;
+        }
+    }
+    __syncthreads();
+    if (GATE_MODE == 1) {
+        if (tid == 0) {
+            float G = 0.0f;
+            for (int t = 0; t < kCc; ++t) { G += sm.gs[t]; sm.gs[t] = G; }
+        }
+        __syncthreads();
+        reinterpret_cast<float*>(blk + kOffEG)[tid] = decay_f(sm.gs[kCc - 1]);
+    }
+
+    // ---- row images: item = (token t, channels k0..k0+7) --------------------------------------
+    for (int it = tid; it < kCc * 16; it += kThr) {
+        const int t = it >> 4, k0 = (it & 15) * 8;
+        float xb[8], xk[8], xq[8], xg[8];
+        if (t < nt) {
+            const float* kp = a.k + (row0 + t) * C + h * kHeadDim + k0;
+            const float* qp = a.q + (row0 + t) * C + h * kHeadDim + k0;
+            const float4 k4a = *reinterpret_cast<const float4*>(kp);
+            const float4 k4b = *reinterpret_cast<const float4*>(kp + 4);
+            const float4 q4a = *reinterpret_cast<const float4*>(qp);
+            const float4 q4b = *reinterpret_cast<const float4*>(qp + 4);
+            const float kv[8] = {k4a.x, k4a.y, k4a.z, k4a.w, k4b.x, k4b.y, k4b.z, k4b.w};
+            const float qv[8] = {q4a.x, q4a.y, q4a.z, q4a.w, q4b.x, q4b.y, q4b.z, q4b.w};
+            if (GATE_MODE == 0) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float gt = sm.G[t][k0 + e], cr = sm.cref[k0 + e];
+                    const float ef = __expf(gt - cr), eb = __expf(cr - gt);
+                    xb[e] = kv[e] * eb;
+                    xk[e] = kv[e] * ef;
+                    xq[e] = qv[e] * ef;
+                    xg[e] = qv[e] * (ef * sm.ecr[k0 + e]);
+                }
+            } else {
+                const float eg = __expf(sm.gs[t]);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    xb[e] = kv[e];
+                    xk[e] = kv[e];
+                    xq[e] = qv[e];
+                    xg[e] = qv[e] * eg;
+                }
+            }
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) xb[e] = xk[e] = xq[e] = xg[e] = 0.0f;
+        }
+        put8x(sm.kb[0], sm.kb[1], tc_offset(t, k0, kSbo128), xb);
+        put8x(sm.bia[0], sm.bia[1], tc_offset(t, k0, kSbo128), xk);
+        put8x(sm.bia[0], sm.bia[1], tc_offset(kCc + t, k0, kSbo128), xq);
+        put8x(blk + kOffQW, blk + kOffQW + kQWBytes, tc_offset(t, k0, kSbo128), xg);
+    }
+    // ---- column images: item = (channel kk, tokens t0..t0+7) ----------------------------------
+    for (int it = tid; it < 128 * (kCc / 8); it += kThr) {
+        const int kk = it & 127, t0 = (it >> 7) * 8;
+        float xt[8], xv[8], xc[8];
+        const float GC = GATE_MODE == 0 ? sm.G[kCc - 1][kk] : sm.gs[kCc - 1];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const int t = t0 + e;
+            if (t < nt) {
+                const float G = GATE_MODE == 0 ? sm.G[t][kk] : sm.gs[t];
+                const float kv = a.k[(row0 + t) * C + h * kHeadDim + kk];
+                const float bt = sm.beta[t];
+                xt[e] = bt * kv * __expf(G);
+                xv[e] = bt * a.v[(row0 + t) * C + h * kHeadDim + kk];
+                xc[e] = kv * __expf(GC - G);
+            } else {
+                xt[e] = xv[e] = xc[e] = 0.0f;
+            }
+        }
+        put8x(sm.kt[0], sm.kt[1], tc_offset(kk, t0, kSbo32), xt);
+        put8x(sm.vt[0], sm.vt[1], tc_offset(kk, t0, kSbo32), xv);
+        put8x(blk + kOffB2, blk + kOffB2 + kB2Bytes, tc_offset(kk, t0, kSbo32), xc);
+    }
+    fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tbase = sm.tmem_base;
     const uint32_t tlane = tbase + ((uint32_t)(32 * warp) << 16);
+    uint32_t phase = 0;
+    bool ok = true;
 
-    constexpr uint32_t kTx = (GATE_MODE == 0 ? 4u : 3u) * kCc * 128 * 4;
-    auto issue = [&](int c, int st) {
-        const int row = (int)(begin + (long)c * kCc);
-        fence_proxy_async_smem();
-        mbar_arrive_expect_tx(&sm.bar_tma[st], kTx);
-        tma_load_2d(&sm.q[st][0][0], &tq, h * kHeadDim, row, &sm.bar_tma[st]);
-        tma_load_2d(&sm.k[st][0][0], &tk, h * kHeadDim, row, &sm.bar_tma[st]);
-        tma_load_2d(&sm.v[st][0][0], &tv, h * kHeadDim, row, &sm.bar_tma[st]);
-        if (GATE_MODE == 0) tma_load_2d(&sm.g[st][0][0], &tg, h * kHeadDim, row, &sm.bar_tma[st]);
-    };
-    if (tid == 0 && nch > 0) issue(0, 0);
-    float bpre = 0.0f, gpre = 0.0f;
-    if (tid < kCc && tid < L) {
-        bpre = a.beta[(begin + tid) * H + h];
-        if (GATE_MODE == 1) gpre = a.g[(begin + tid) * H + h];
+    // ---- MMA-a: D[s][n] = (K e^{c-G})_s . (K e^{G-c} | Q e^{G-c})_n ----------------------------
+    if (tid == 0) {
+        mma3_ss(tbase, tc_smem_desc(smem_u32(sm.kb[0]), 128, kSbo128),
+                tc_smem_desc(smem_u32(sm.kb[1]), 128, kSbo128),
+                tc_smem_desc(smem_u32(sm.bia[0]), 128, kSbo128),
+                tc_smem_desc(smem_u32(sm.bia[1]), 128, kSbo128), 8, tc_idesc_bf16(128, 64));
+        tc_commit(&sm.bar);
     }
+    ok = mbar_wait_bounded(&sm.bar, phase, a.err);
+    phase ^= 1u;
+    tc_fence_after();
+    if (__syncthreads_or(!ok)) goto done;
 
-    const uint32_t idA = tc_idesc_bf16(128, 32), idB = tc_idesc_bf16(128, 16);
-    const uint32_t id2 = tc_idesc_bf16(128, 144);
-    const DescPair dKB = desc_pair(sm.kb, 0, kSboK128), dBI0 = desc_pair(sm.bi, 0, kSboK128);
-    const DescPair dBI32 = desc_pair(sm.bi, 4 * kSboK128, kSboK128);
-    const DescPair dA1 = desc_pair(sm.a1, 0, kSboK128);
-    const DescPair dKT = desc_pair(sm.kt, 0, kSboK16), dVT = desc_pair(sm.vt, 0, kSboK16);
-    const DescPair dTM = desc_pair(sm.tm, 0, kSboK16), dB2 = desc_pair(sm.b2, 0, kSboK16);
-    const DescPair dA2 = desc_pair(sm.a2, 0, kSboK16);
-    uint32_t mma_phase = 0;
+    // ---- A, Aqk, Tm (warp 0; lane s = key token s) --------------------------------------------
+    if (warp == 0) {
+        float d[64];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) tmem_ld16(tlane + 16 * q, *reinterpret_cast<float(*)[16]>(&d[16 * q]));
+        tmem_ld_wait();
+        const int s = lane;
+        const float Gs = GATE_MODE == 1 ? sm.gs[s] : 0.0f;
+        unsigned char* b2h = blk + kOffB2;
+        unsigned char* b2l = blk + kOffB2 + kB2Bytes;
+#pragma unroll
+        for (int t = 0; t < kCc; ++t) {
+            float fac = 1.0f;
+            if (GATE_MODE == 1) fac = __expf(fminf(sm.gs[t] - Gs, 0.0f));
+            sm.amat[t][s] = t > s ? sm.beta[t] * d[t] * fac : 0.0f;
+            put1x(b2h, b2l, tc_offset(128 + t, s, kSbo32), t >= s ? d[kCc + t] * fac : 0.0f);
+        }
+        __syncwarp();
+        // diagonal 16x16 blocks by forward substitution: lane s solves column s of its block
+        {
+            const int b0 = s < 16 ? 0 : 16;
+            float x[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                float acc = (b0 + i == s) ? 1.0f : 0.0f;
+#pragma unroll
+                for (int j = 0; j < i; ++j) acc = fmaf(-sm.amat[b0 + i][b0 + j], x[j], acc);
+                x[i] = acc;
+                sm.tinv[b0 + i][s] = acc;
+            }
+            if (s < 16) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) sm.tinv[i][16 + s] = 0.0f;  // upper-right block
+            }
+        }
+        __syncwarp();
+        // lower-left block: T21 = -T22 A21 T11 (lane s < 16 owns column s)
+        if (s < 16) {
+            float m1[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {     // (A21 T11)[i][s]
+                float acc = 0.0f;
+#pragma unroll
+                for (int j = 0; j < 16; ++j) acc = fmaf(sm.amat[16 + i][j], sm.tinv[j][s], acc);
+                m1[i] = acc;
+            }
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {     // -(T22 m1)[i]
+                float acc = 0.0f;
+#pragma unroll
+                for (int j = 0; j < 16; ++j) acc = fmaf(sm.tinv[16 + i][16 + j], m1[j], acc);
+                sm.tinv[16 + i][s] = -acc;
+            }
+        }
+        __syncwarp();
+#pragma unroll
+        for (int t = 0; t < kCc; ++t) put1x(sm.tm[0], sm.tm[1], tc_offset(t, s, kSbo32), sm.tinv[t][s]);
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    // ---- MMA-b: [W^T | U^T] = (beta K e^G | beta V)^T Tm^T -----------------------------------
+    if (tid == 0) {
+        const uint64_t tmh = tc_smem_desc(smem_u32(sm.tm[0]), 128, kSbo32);
+        const uint64_t tml = tc_smem_desc(smem_u32(sm.tm[1]), 128, kSbo32);
+        mma3_ss(tbase + 64, tc_smem_desc(smem_u32(sm.kt[0]), 128, kSbo32),
+                tc_smem_desc(smem_u32(sm.kt[1]), 128, kSbo32), tmh, tml, 2, tc_idesc_bf16(128, 32));
+        mma3_ss(tbase + 96, tc_smem_desc(smem_u32(sm.vt[0]), 128, kSbo32),
+                tc_smem_desc(smem_u32(sm.vt[1]), 128, kSbo32), tmh, tml, 2, tc_idesc_bf16(128, 32));
+        tc_commit(&sm.bar);
+    }
+    ok = mbar_wait_bounded(&sm.bar, phase, a.err);
+    phase ^= 1u;
+    tc_fence_after();
+    if (__syncthreads_or(!ok)) goto done;
+    {
+        float w[32], u[32];
+        tmem_ld16(tlane + 64, *reinterpret_cast<float(*)[16]>(&w[0]));
+        tmem_ld16(tlane + 80, *reinterpret_cast<float(*)[16]>(&w[16]));
+        tmem_ld16(tlane + 96, *reinterpret_cast<float(*)[16]>(&u[0]));
+        tmem_ld16(tlane + 112, *reinterpret_cast<float(*)[16]>(&u[16]));
+        tmem_ld_wait();
+        // W[t][k = tid] into QW rows 32 + t; U^T[v = tid][t] into the f32 block
+        unsigned char* qwh = blk + kOffQW;
+        unsigned char* qwl = blk + kOffQW + kQWBytes;
+#pragma unroll
+        for (int t = 0; t < kCc; ++t) put1x(qwh, qwl, tc_offset(kCc + t, tid, kSbo128), w[t]);
+        float4* ut = reinterpret_cast<float4*>(blk + kOffUT + tid * kCc * 4);
+#pragma unroll
+        for (int q = 0; q < kCc / 4; ++q) ut[q] = make_float4(u[4 * q], u[4 * q + 1], u[4 * q + 2], u[4 * q + 3]);
+    }
+done:
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tbase, 128);
+}
+
+// ============================================================================================
+// kernel 2: the state recurrence over chunks, one CTA per (sequence, head)
+// ============================================================================================
+
+struct __align__(1024) InterSmem {
+    unsigned char blk[2][kBlkBytes];             // double-buffered workspace blocks
+    uint64_t bar_ld[2];
+    uint64_t bar_mma;
+    uint32_t tmem_base;
+};
+
+// TMEM columns
+constexpr uint32_t kTA1 = 0;      // S^T hi (64) then lo (64)
+constexpr uint32_t kTA2 = 128;    // U'^T hi (16) then lo (16)
+constexpr uint32_t kTD1 = 160;    // [O1^T | X^T]  64
+constexpr uint32_t kTD2 = 224;    // [dS^T | O2^T] 160
+
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// write NV f32 values (NV multiple of 32) as packed bf16 hi words at col_hi and lo words at col_lo
+template <int NV>
+__device__ __forceinline__ void tmem_put_split(uint32_t col_hi, uint32_t col_lo, const float* v) {
+#pragma unroll
+    for (int b = 0; b < NV / 32; ++b) {
+        float hw[16], lw[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            uint32_t hu, lu;
+            split_bf16x2(v[32 * b + 2 * i], v[32 * b + 2 * i + 1], hu, lu);
+            hw[i] = __uint_as_float(hu);
+            lw[i] = __uint_as_float(lu);
+        }
+        tmem_st16(col_hi + 16 * b, hw);
+        tmem_st16(col_lo + 16 * b, lw);
+    }
+}
+
+template <int GATE_MODE>
+__global__ void __launch_bounds__(kThr, 1)
+kda_chunk_inter_kernel(ScanArgs a, const int* chunk_off, const unsigned char* ws) {
+    extern __shared__ unsigned char smem_raw[];
+    InterSmem& sm = *reinterpret_cast<InterSmem*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int h = blockIdx.x;
+    const int n = a.order ? a.order[blockIdx.y] : (int)blockIdx.y;
+    const int H = a.H;
+    const long C = (long)H * kHeadDim;
+    long begin, end;
+    seq_range(a.seq, n, begin, end);
+    const long L = end - begin;
+    const int nch = (int)((L + kCc - 1) / kCc);
+    const long gbase = chunk_base(a.seq, chunk_off, n);
+
+    if (warp == 0) {
+        tmem_alloc(&sm.tmem_base, 512);
+        tmem_relinquish();
+    }
+    if (tid == 0) {
+        mbar_init(&sm.bar_ld[0], 1);
+        mbar_init(&sm.bar_ld[1], 1);
+        mbar_init(&sm.bar_mma, 1);
+        fence_mbar_init();
+    }
+    float srow[128];
+    {
+        const float4* sin = reinterpret_cast<const float4*>(
+            a.state_in + (((long)n * H + h) * kHeadDim + tid) * kHeadDim);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            const float4 x = __ldcs(sin + j);
+            srow[4 * j] = x.x; srow[4 * j + 1] = x.y; srow[4 * j + 2] = x.z; srow[4 * j + 3] = x.w;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = sm.tmem_base;
+    const uint32_t tlane = tbase + ((uint32_t)(32 * warp) << 16);
+    tmem_put_split<128>(tlane + kTA1, tlane + kTA1 + 64, srow);
+    tmem_st_wait();
+
+    auto issue = [&](int c, int st) {
+        const unsigned char* src = ws + ((gbase + c) * H + h) * (long)kBlkBytes;
+        mbar_arrive_expect_tx(&sm.bar_ld[st], kBlkBytes);
+        bulk_load(&sm.blk[st][kOffQW], src + kOffQW, 2 * kQWBytes, &sm.bar_ld[st]);
+        bulk_load(&sm.blk[st][kOffB2], src + kOffB2, 2 * kB2Bytes, &sm.bar_ld[st]);
+        bulk_load(&sm.blk[st][kOffUT], src + kOffUT, kUTBytes + kEGBytes, &sm.bar_ld[st]);
+    };
+    if (tid == 0) {
+        if (nch > 0) issue(0, 0);
+        if (nch > 1) issue(1, 1);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    const uint32_t id1 = tc_idesc_bf16(128, 64), id2 = tc_idesc_bf16(128, 160);
+    uint32_t mph = 0;
     bool failed = false;
-    auto mma_wait = [&]() -> bool {
-        const bool ok = mbar_wait_bounded(&sm.bar_mma, mma_phase, a.err);
-        if (ok) mma_phase ^= 1u;
-        tc_fence_after();
-        return ok;
-    };
-    auto sync_images = [&]() {  // thread-written operand images -> visible to the tensor cores
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
-    };
-
-    for (int c = 0; c < nch && !failed; ++c) {
+    for (int c = 0; c < nch; ++c) {
         const int st = c & 1;
         const long row0 = begin + (long)c * kCc;
         const int nt = (int)min((long)kCc, L - (long)c * kCc);
-        if (tid < kCc) {
-            sm.beta[st][tid] = tid < nt ? bpre : 0.0f;
-            if (GATE_MODE == 1) {
-                float gl = tid < nt ? gpre : 0.0f;
-                if (EXP && tid < nt) gl = logf(gpre);
-                sm.gs[st][tid] = gl;
-            }
-            const long rn = row0 + kCc + tid;
-            if (rn < end) {
-                bpre = a.beta[rn * H + h];
-                if (GATE_MODE == 1) gpre = a.g[rn * H + h];
-            }
-        }
-        const bool arrived = mbar_wait_bounded(&sm.bar_tma[st], (uint32_t)((c >> 1) & 1), a.err);
-        if (__syncthreads_or(!arrived)) { failed = true; break; }
-        if (tid == 0 && c + 1 < nch) issue(c + 1, st ^ 1);
-
-        // ---- phase 1: cumulative gate over the chunk ------------------------------------------
-        if (GATE_MODE == 0) {
-            float G = 0.0f;
-            for (int t = 0; t < kCc; ++t) {
-                float x = 0.0f;
-                if (t < nt) {
-                    x = sm.g[st][t][tid];
-                    if (EXP) x = logf(x);
-                }
-                G += x;
-                sm.g[st][t][tid] = G;
-            }
-            sm.cref[tid] = 0.5f * G;
-            sm.ecr[tid] = __expf(0.5f * G);
-            sm.egc[tid] = decay_f(G);
-            if (G < -170.0f && a.err) atomicOr(a.err, kDevErrRange);
-        } else if (tid == 0) {
-            float G = 0.0f;
-            for (int t = 0; t < kCc; ++t) {
-                G += sm.gs[st][t];
-                sm.gs[st][t] = G;
-            }
-            sm.cref[0] = G;
-        }
-        __syncthreads();
-        if (GATE_MODE == 1) sm.egc[tid] = decay_f(sm.cref[0]);
-
-        // ---- phase 2: operand images --------------------------------------------------------
-        // row images: item = (token t, channels k0..k0+7); one exp pair feeds all four images
-        for (int it = tid; it < kCc * 16; it += kChThreads) {
-            const int t = it >> 4, k0 = (it & 15) * 8;
-            float xb[8], xk[8], xq[8], xg[8];
-            if (t < nt) {
-                const float4* K4 = reinterpret_cast<const float4*>(&sm.k[st][t][k0]);
-                const float4* Q4 = reinterpret_cast<const float4*>(&sm.q[st][t][k0]);
-                const float kv[8] = {K4[0].x, K4[0].y, K4[0].z, K4[0].w, K4[1].x, K4[1].y, K4[1].z, K4[1].w};
-                const float qv[8] = {Q4[0].x, Q4[0].y, Q4[0].z, Q4[0].w, Q4[1].x, Q4[1].y, Q4[1].z, Q4[1].w};
-                if (GATE_MODE == 0) {
-                    const float4* G4 = reinterpret_cast<const float4*>(&sm.g[st][t][k0]);
-                    const float4* C4 = reinterpret_cast<const float4*>(&sm.cref[k0]);
-                    const float4* E4 = reinterpret_cast<const float4*>(&sm.ecr[k0]);
-                    const float gv[8] = {G4[0].x, G4[0].y, G4[0].z, G4[0].w, G4[1].x, G4[1].y, G4[1].z, G4[1].w};
-                    const float cv[8] = {C4[0].x, C4[0].y, C4[0].z, C4[0].w, C4[1].x, C4[1].y, C4[1].z, C4[1].w};
-                    const float ev[8] = {E4[0].x, E4[0].y, E4[0].z, E4[0].w, E4[1].x, E4[1].y, E4[1].z, E4[1].w};
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const float ef = __expf(gv[e] - cv[e]);   // e^{G-c}
-                        const float eb = __expf(cv[e] - gv[e]);   // e^{c-G}
-                        xb[e] = kv[e] * eb;
-                        xk[e] = kv[e] * ef;
-                        xq[e] = qv[e] * ef;
-                        xg[e] = qv[e] * (ef * ev[e]);             // Q e^{G}
-                    }
-                } else {
-                    const float eg = __expf(sm.gs[st][t]);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        xb[e] = kv[e];
-                        xk[e] = kv[e];
-                        xq[e] = qv[e];
-                        xg[e] = qv[e] * eg;
-                    }
-                }
-            } else {
-#pragma unroll
-                for (int e = 0; e < 8; ++e) xb[e] = xk[e] = xq[e] = xg[e] = 0.0f;
-            }
-            put8(sm.kb, img_off(t, k0, kSboK128), xb);
-            put8(sm.bi, img_off(t, k0, kSboK128), xk);
-            put8(sm.bi, img_off(16 + t, k0, kSboK128), xq);
-            put8(sm.bi, img_off(32 + t, k0, kSboK128), xg);
-        }
-        // column images: item = (channel kk, tokens t0..t0+7)
-        for (int it = tid; it < 128 * 2; it += kChThreads) {
-            const int kk = it >> 1, t0 = (it & 1) * 8;
-            float xt[8], xv[8], xc[8];
-            const float GC = GATE_MODE == 0 ? sm.g[st][kCc - 1][kk] : sm.gs[st][kCc - 1];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const int t = t0 + e;
-                if (t < nt) {
-                    const float G = GATE_MODE == 0 ? sm.g[st][t][kk] : sm.gs[st][t];
-                    const float kv = sm.k[st][t][kk];
-                    const float bt = sm.beta[st][t];
-                    xt[e] = bt * kv * __expf(G);          // beta K e^{G}
-                    xv[e] = bt * sm.v[st][t][kk];         // beta V
-                    xc[e] = kv * __expf(GC - G);          // K e^{G_C - G}
-                } else {
-                    xt[e] = xv[e] = xc[e] = 0.0f;
-                }
-            }
-            put8(sm.kt, img_off(kk, t0, kSboK16), xt);
-            put8(sm.vt, img_off(kk, t0, kSboK16), xv);
-            put8(sm.b2, img_off(kk, t0, kSboK16), xc);
-        }
-        sync_images();
-
-        // ---- MMA-a: [A/beta | Aqk]^T, rows s --------------------------------------------------
+        const bool got = mbar_wait_bounded(&sm.bar_ld[st], (uint32_t)((c >> 1) & 1), a.err);
+        if (__syncthreads_or(!got)) { failed = true; break; }
+        unsigned char* B = sm.blk[st];
+        // MMA-1: [O1^T | X^T] = S^T (Q e^G | W)^T
         if (tid == 0) {
-            mma_x3(tbase + kTmA, dKB, dBI0, 8, idA);
+            mma3_ts(tbase + kTD1, tbase + kTA1, tbase + kTA1 + 64,
+                    tc_smem_desc(smem_u32(B + kOffQW), 128, kSbo128),
+                    tc_smem_desc(smem_u32(B + kOffQW + kQWBytes), 128, kSbo128), 8, id1);
             tc_commit(&sm.bar_mma);
         }
-        if (__syncthreads_or(!mma_wait())) { failed = true; break; }
-
-        // ---- phase 4: A, Aqk, Tm on warp 0 ---------------------------------------------------
-        if (warp == 0) {
-            float d[32];
-            tmem_ld16(tlane + kTmA, *reinterpret_cast<float(*)[16]>(&d[0]));
-            tmem_ld16(tlane + kTmA + 16, *reinterpret_cast<float(*)[16]>(&d[16]));  // rows s
-            tmem_ld_wait();
-            const int s = lane;
-            if (s < kCc) {
-                const float Gs = GATE_MODE == 1 ? sm.gs[st][s] : 0.0f;
-#pragma unroll
-                for (int t = 0; t < kCc; ++t) {
-                    float fac = 1.0f;
-                    if (GATE_MODE == 1) fac = __expf(fminf(sm.gs[st][t] - Gs, 0.0f));
-                    sm.amat[t][s] = t > s ? sm.beta[st][t] * d[t] * fac : 0.0f;
-                    const float aqk = t >= s ? d[16 + t] * fac : 0.0f;
-                    put1(sm.b2, img_off(128 + t, s, kSboK16), aqk);
-                }
-            }
-            __syncwarp();
-            if (s < kCc) {
-                float x[kCc];
-#pragma unroll
-                for (int t = 0; t < kCc; ++t) {
-                    float acc = t == s ? 1.0f : 0.0f;
-#pragma unroll
-                    for (int j = 0; j < t; ++j) acc = fmaf(-sm.amat[t][j], x[j], acc);
-                    x[t] = acc;
-                    put1(sm.tm, img_off(t, s, kSboK16), acc);
-                }
-            }
-        }
-        sync_images();
-
-        // ---- MMA-b: [W^T | U^T] = (beta K e^G | beta V)^T Tm^T --------------------------------
-        if (tid == 0) {
-            mma_x3(tbase + kTmB, dKT, dTM, 1, idB);
-            mma_x3(tbase + kTmB + 16, dVT, dTM, 1, idB);
-            tc_commit(&sm.bar_mma);
-        }
-        if (__syncthreads_or(!mma_wait())) { failed = true; break; }
-        float urow[kCc];
-        {
-            float d[16];
-            tmem_ld16(tlane + kTmB, d);              // W[t][k = tid]
-            tmem_ld16(tlane + kTmB + 16, urow);      // U^T[v = tid][t]
-            tmem_ld_wait();
-#pragma unroll
-            for (int t = 0; t < kCc; ++t) put1(sm.bi, img_off(48 + t, tid, kSboK128), d[t]);
-        }
-        sync_images();
-
-        // ---- MMA-1: [O1^T | X^T] = S^T (Q e^G | W)^T ---------------------------------------
-        if (tid == 0) {
-            mma_x3(tbase + kTm1, dA1, dBI32, 8, idA);
-            tc_commit(&sm.bar_mma);
-        }
-        if (__syncthreads_or(!mma_wait())) { failed = true; break; }
+        bool ok = mbar_wait_bounded(&sm.bar_mma, mph, a.err);
+        if (ok) mph ^= 1u;
+        tc_fence_after();
+        if (__syncthreads_or(!ok)) { failed = true; break; }
         float o1[kCc];
         {
-            float xr[16];
-            tmem_ld16(tlane + kTm1, o1);
-            tmem_ld16(tlane + kTm1 + 16, xr);
+            float x[kCc];
+            tmem_ld16(tlane + kTD1, *reinterpret_cast<float(*)[16]>(&o1[0]));
+            tmem_ld16(tlane + kTD1 + 16, *reinterpret_cast<float(*)[16]>(&o1[16]));
+            tmem_ld16(tlane + kTD1 + 32, *reinterpret_cast<float(*)[16]>(&x[0]));
+            tmem_ld16(tlane + kTD1 + 48, *reinterpret_cast<float(*)[16]>(&x[16]));
             tmem_ld_wait();
-            float up[16];
+            const float4* ut = reinterpret_cast<const float4*>(B + kOffUT + tid * kCc * 4);
+            float up[kCc];
 #pragma unroll
-            for (int t = 0; t < kCc; ++t) up[t] = urow[t] - xr[t];
-            float lo8[8], hi8[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) { lo8[e] = up[e]; hi8[e] = up[8 + e]; }
-            put8(sm.a2, img_off(tid, 0, kSboK16), lo8);
-            put8(sm.a2, img_off(tid, 8, kSboK16), hi8);
+            for (int q = 0; q < kCc / 4; ++q) {
+                const float4 u4 = ut[q];
+                up[4 * q] = u4.x - x[4 * q];
+                up[4 * q + 1] = u4.y - x[4 * q + 1];
+                up[4 * q + 2] = u4.z - x[4 * q + 2];
+                up[4 * q + 3] = u4.w - x[4 * q + 3];
+            }
+            tmem_put_split<kCc>(tlane + kTA2, tlane + kTA2 + 16, up);
+            tmem_st_wait();
         }
-        sync_images();
-
-        // ---- MMA-2: [dS^T | O2^T] = U'^T (K e^{G_C-G} | Aqk) -------------------------------
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        // MMA-2: [dS^T | O2^T] = U'^T (K e^{G_C-G} | Aqk)
         if (tid == 0) {
-            mma_x3(tbase + kTm2, dA2, dB2, 1, id2);
+            mma3_ts(tbase + kTD2, tbase + kTA2, tbase + kTA2 + 16,
+                    tc_smem_desc(smem_u32(B + kOffB2), 128, kSbo32),
+                    tc_smem_desc(smem_u32(B + kOffB2 + kB2Bytes), 128, kSbo32), 2, id2);
             tc_commit(&sm.bar_mma);
         }
-        if (__syncthreads_or(!mma_wait())) { failed = true; break; }
+        ok = mbar_wait_bounded(&sm.bar_mma, mph, a.err);
+        if (ok) mph ^= 1u;
+        tc_fence_after();
+        if (__syncthreads_or(!ok)) { failed = true; break; }
         {
+            const float* eg = reinterpret_cast<const float*>(B + kOffEG);
 #pragma unroll
-            for (int c16 = 0; c16 < 8; ++c16) {
+            for (int q16 = 0; q16 < 8; ++q16) {
                 float d[16];
-                tmem_ld16(tlane + kTm2 + 16 * c16, d);
+                tmem_ld16(tlane + kTD2 + 16 * q16, d);
                 tmem_ld_wait();
-                const float4* E4 = reinterpret_cast<const float4*>(&sm.egc[16 * c16]);
 #pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) {
-                    const float4 e4 = E4[q4];
-                    const int kk = 16 * c16 + 4 * q4;
-                    srow[kk] = fmaf(srow[kk], e4.x, d[4 * q4]);
-                    srow[kk + 1] = fmaf(srow[kk + 1], e4.y, d[4 * q4 + 1]);
-                    srow[kk + 2] = fmaf(srow[kk + 2], e4.z, d[4 * q4 + 2]);
-                    srow[kk + 3] = fmaf(srow[kk + 3], e4.w, d[4 * q4 + 3]);
+                for (int e = 0; e < 16; ++e) {
+                    const int kk = 16 * q16 + e;
+                    srow[kk] = fmaf(srow[kk], eg[kk], d[e]);
                 }
             }
-            float o2[16];
-            tmem_ld16(tlane + kTm2 + 128, o2);
+            float o2[kCc];
+            tmem_ld16(tlane + kTD2 + 128, *reinterpret_cast<float(*)[16]>(&o2[0]));
+            tmem_ld16(tlane + kTD2 + 144, *reinterpret_cast<float(*)[16]>(&o2[16]));
             tmem_ld_wait();
             float* orow = a.o + row0 * C + h * kHeadDim + tid;
 #pragma unroll
             for (int t = 0; t < kCc; ++t)
                 if (t < nt) orow[(long)t * C] = __fmul_rn(a.scale, o1[t] + o2[t]);
+            tmem_put_split<128>(tlane + kTA1, tlane + kTA1 + 64, srow);
+            tmem_st_wait();
         }
-        write_a1();
-        sync_images();
+        tc_fence_before();
+        __syncthreads();   // this stage's block is consumed; S^T is in place for the next MMA-1
+        tc_fence_after();
+        if (tid == 0 && c + 2 < nch) issue(c + 2, st);
     }
     if (!failed) {
-        float* sout = a.state_out + (((long)n * H + h) * kHeadDim + tid) * kHeadDim;
+        float4* sout = reinterpret_cast<float4*>(a.state_out + (((long)n * H + h) * kHeadDim + tid) * kHeadDim);
 #pragma unroll
         for (int j = 0; j < 32; ++j)
-            __stcs(reinterpret_cast<float4*>(sout) + j,
-                   make_float4(srow[4 * j], srow[4 * j + 1], srow[4 * j + 2], srow[4 * j + 3]));
+            __stcs(sout + j, make_float4(srow[4 * j], srow[4 * j + 1], srow[4 * j + 2], srow[4 * j + 3]));
     } else {
-        // let in-flight MMAs finish (bounded) before the tensor memory is released
-        mbar_wait_bounded(&sm.bar_mma, mma_phase, nullptr);
+        mbar_wait_bounded(&sm.bar_mma, mph, nullptr);   // let in-flight MMAs drain (bounded)
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tbase, 256);
+    if (warp == 0) tmem_dealloc(tbase, 512);
 }
 
-template <int GM, bool EXP>
-static cudaError_t launch_chunk_t(const ScanArgs& a, cudaStream_t s) {
-    const long C = (long)a.H * kHeadDim;
-    const long rows = a.seq.total_rows;
-    CUtensorMap tq, tk, tv, tg;
-    if (!make_tensor_map_2d(&tq, a.q, rows, C, kHeadDim, kCc) ||
-        !make_tensor_map_2d(&tk, a.k, rows, C, kHeadDim, kCc) ||
-        !make_tensor_map_2d(&tv, a.v, rows, C, kHeadDim, kCc))
-        return cudaErrorInvalidValue;
-    if (GM == 0) {
-        if (!make_tensor_map_2d(&tg, a.g, rows, C, kHeadDim, kCc)) return cudaErrorInvalidValue;
-    } else {
-        tg = tq;
-    }
-    const size_t smem = sizeof(ChunkSmem) + 1024;
-    static int attr_done[64] = {0};
+// ============================================================================================
+// host side
+// ============================================================================================
+
+long chunk_count(const SeqLayout& s, const int* cu_host) {
+    if (s.cu_seqlens == nullptr) return (long)s.N * ((s.T_uniform + kCc - 1) / kCc);
+    long total = 0;
+    for (int n = 0; n < s.N; ++n) total += (cu_host[n + 1] - cu_host[n] + kCc - 1) / kCc;
+    return total;
+}
+
+size_t chunk_workspace_bytes(const SeqLayout& s, const int* cu_host, int H) {
+    const size_t header =
+        s.cu_seqlens ? (((size_t)(s.N + 1) * 4 + kHeaderAlign - 1) / kHeaderAlign) * kHeaderAlign : 0;
+    return header + (size_t)chunk_count(s, cu_host) * H * kBlkBytes;
+}
+
+template <typename K>
+static cudaError_t set_smem(K kernel, size_t bytes) {
+    static int done[64] = {0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64 || !attr_done[dev]) {
-        e = cudaFuncSetAttribute(kda_scan_chunk_kernel<GM, EXP>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = 1;
+    return e;
+}
+
+template <int GM, bool EXP>
+static cudaError_t launch_chunk_t(const ScanArgs& a, const int* cu_host, void* workspace,
+                                  cudaStream_t s) {
+    const long nchunks = chunk_count(a.seq, cu_host);
+    int* chunk_off = nullptr;
+    unsigned char* ws = static_cast<unsigned char*>(workspace);
+    if (a.seq.cu_seqlens != nullptr) {
+        chunk_off = reinterpret_cast<int*>(ws);
+        ws += ((size_t)(a.seq.N + 1) * 4 + kHeaderAlign - 1) / kHeaderAlign * kHeaderAlign;
+        kda_chunk_offsets_kernel<<<1, 1024, 0, s>>>(a.seq.cu_seqlens, a.seq.N, chunk_off);
+        cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
-        if (dev >= 0 && dev < 64) attr_done[dev] = 1;
     }
-    dim3 grid((unsigned)a.H, (unsigned)a.seq.N);
-    kda_scan_chunk_kernel<GM, EXP><<<grid, kChThreads, smem, s>>>(a, tq, tk, tv, tg);
+    if (nchunks > 0) {
+        const size_t smem1 = sizeof(IntraSmem) + 1024;
+        cudaError_t e = set_smem(kda_chunk_intra_kernel<GM, EXP>, smem1);
+        if (e != cudaSuccess) return e;
+        dim3 g1((unsigned)nchunks, (unsigned)a.H);
+        kda_chunk_intra_kernel<GM, EXP><<<g1, kThr, smem1, s>>>(a, chunk_off, ws);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    const size_t smem2 = sizeof(InterSmem) + 1024;
+    cudaError_t e = set_smem(kda_chunk_inter_kernel<GM>, smem2);
+    if (e != cudaSuccess) return e;
+    dim3 g2((unsigned)a.H, (unsigned)a.seq.N);
+    kda_chunk_inter_kernel<GM><<<g2, kThr, smem2, s>>>(a, chunk_off, ws);
     return cudaGetLastError();
 }
 
-size_t chunk_smem_bytes() { return sizeof(ChunkSmem) + 1024; }
-
-cudaError_t launch_scan_chunk(const ScanArgs& a, cudaStream_t s) {
+cudaError_t launch_scan_chunk(const ScanArgs& a, const int* cu_host, void* workspace,
+                              cudaStream_t s) {
     if (a.seq.N == 0) return cudaSuccess;
     if (a.seq.total_rows == 0) {
         const size_t bytes = (size_t)a.seq.N * a.H * kHeadDim * kHeadDim * sizeof(float);
         return cudaMemcpyAsync(a.state_out, a.state_in, bytes, cudaMemcpyDeviceToDevice, s);
     }
     const bool exp_done = (a.gate_mode & 2) != 0;
-    if ((a.gate_mode & 1) == 0) return exp_done ? launch_chunk_t<0, true>(a, s) : launch_chunk_t<0, false>(a, s);
-    return exp_done ? launch_chunk_t<1, true>(a, s) : launch_chunk_t<1, false>(a, s);
+    if ((a.gate_mode & 1) == 0)
+        return exp_done ? launch_chunk_t<0, true>(a, cu_host, workspace, s)
+                        : launch_chunk_t<0, false>(a, cu_host, workspace, s);
+    return exp_done ? launch_chunk_t<1, true>(a, cu_host, workspace, s)
+                    : launch_chunk_t<1, false>(a, cu_host, workspace, s);
 }
 
 }  // namespace kda

@@ -138,6 +138,13 @@ def kda_scan_workspace_bytes(N, total_T, H, gate_mode=0, algo=ALGO_AUTO, D=HEAD_
     return int(_lib.kda_scan_workspace_bytes(N, total_T, H, D, gate_mode, algo))
 
 
+def scan_workspace(N, total_T, H, device, algo=ALGO_AUTO):
+    """A device byte buffer large enough for kda_scan / kda_scan_varlen (None when none is
+    needed)."""
+    nbytes = kda_scan_workspace_bytes(N, total_T, H, algo=algo)
+    return None if nbytes == 0 else torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+
 def kda_scan(q_hat, k_hat, v_hat, g, beta, state_in, state_out, o, *, N, T, H, gate_mode=0,
              scale=None, algo=ALGO_AUTO, workspace=None, D=HEAD_DIM, stream=None):
     scale = D ** -0.5 if scale is None else scale

@@ -19,12 +19,15 @@ def kda_forward(*, q_raw, k_raw, v_raw, f_raw, dt_bias, a_log, beta_raw, state_i
                 conv_w=None, ring_in=None, norm_w=None, gate_raw=None, cu_seqlens=None,
                 cu_seqlens_host=None, N=None, T=None, K=4, gate_mode=0, gate_lb=-5.0,
                 l2_eps=1e-6, rms_eps=1e-6, scale=None, algo=kda.ALGO_AUTO, state_out=None,
-                ring_out=None, out=None, gate_exp=True, stream=None):
+                ring_out=None, out=None, gate_exp=None, workspace=None, stream=None):
     """Run the mixer on device tensors.  Either (N, T) for N sequences of T tokens, or
     cu_seqlens (int32 device) + cu_seqlens_host (int32 CPU) for packed sequences.
     gate_exp: hand the gate from the prep to the scan as decay factors exp(log-decay) (the
-    prep takes the exp once per element instead of every scan CTA taking it); the returned g then
-    holds decay factors.  Both forms compute the same bits.
+    prep takes the exp once per element instead of every sequential-scan CTA taking it); the
+    returned g then holds decay factors.  Default: on for the sequential form, off otherwise (the
+    chunked form consumes log-decays).
+    workspace: scratch for the chunked form; allocated here when algo is AUTO or CHUNK and none
+    is given.
     Returns a dict with q_hat, k_hat, v_hat, g, beta, o, y (None without an epilogue),
     state_out and ring_out."""
     D = kda.HEAD_DIM
@@ -49,6 +52,10 @@ def kda_forward(*, q_raw, k_raw, v_raw, f_raw, dt_bias, a_log, beta_raw, state_i
         state_out = torch.empty_like(state_in)
     if conv_w is not None and ring_out is None:
         ring_out = torch.empty_like(ring_in)
+    if workspace is None and algo != kda.ALGO_SEQ:
+        workspace = kda.scan_workspace(n_seq, rows, H, q_raw.device, algo)
+    if gate_exp is None:
+        gate_exp = algo == kda.ALGO_SEQ
     gm = gate_mode | (kda.GATE_EXP if gate_exp else 0)
     common = dict(H=H, K=K, gate_mode=gm, gate_lb=gate_lb, l2_eps=l2_eps, stream=stream)
     if varlen:
@@ -57,13 +64,13 @@ def kda_forward(*, q_raw, k_raw, v_raw, f_raw, dt_bias, a_log, beta_raw, state_i
                                         cu_seqlens, cu_seqlens_host, **common)
         kda.kda_scan_varlen(q_hat, k_hat, v_hat, g, beta, state_in, state_out, o, cu_seqlens,
                             cu_seqlens_host, H=H, gate_mode=gm, scale=scale, algo=algo,
-                            stream=stream)
+                            workspace=workspace, stream=stream)
     else:
         kda.kda_conv_l2norm_prep(q_raw, k_raw, v_raw, conv_w, ring_in, ring_out, f_raw, dt_bias,
                                  a_log, beta_raw, q_hat, k_hat, v_hat, g, beta, N=N, T=T,
                                  **common)
         kda.kda_scan(q_hat, k_hat, v_hat, g, beta, state_in, state_out, o, N=N, T=T, H=H,
-                     gate_mode=gm, scale=scale, algo=algo, stream=stream)
+                     gate_mode=gm, scale=scale, algo=algo, workspace=workspace, stream=stream)
     y = None
     if norm_w is not None:
         y = take("y", (rows, C))

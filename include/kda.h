@@ -124,8 +124,10 @@ int kda_conv_l2norm_prep_varlen(const void* q_raw, const void* k_raw, const void
                                 int K, float l2_eps, void* stream);
 
 /*
- * Workspace bytes kda_scan / kda_scan_varlen need for the given shape and algorithm
- * (0 for KDA_ALGO_SEQ).  Returns 0 for invalid arguments.
+ * Workspace bytes that suffice for kda_scan / kda_scan_varlen over N sequences holding total_T
+ * tokens in all (an upper bound for any split of total_T into N lengths): 0 for KDA_ALGO_SEQ,
+ * else the chunked form's scratch, about 2.1 KB per (token, head).  Returns 0 for invalid
+ * arguments.
  */
 size_t kda_scan_workspace_bytes(int N, int total_T, int H, int D, int gate_mode, int algo);
 
@@ -147,10 +149,16 @@ size_t kda_scan_workspace_bytes(int N, int total_T, int H, int D, int gate_mode,
  * scale                readout scale, normally 1/sqrt(D) (the reference's query scale, applied to
  *                      the readout only).
  * algo                 KDA_ALGO_SEQ: register-resident sequential scan; the T-token call equals T
- *                      chained one-token calls bit for bit.  KDA_ALGO_AUTO picks the faster form
- *                      for the shape.  KDA_ALGO_CHUNK: chunked form (needs workspace).
- * workspace            device scratch of at least kda_scan_workspace_bytes(...) bytes [16B], or
- *                      NULL when that is 0.
+ *                      chained one-token calls bit for bit.  KDA_ALGO_CHUNK: the chunked (UT/WY)
+ *                      form on the tensor cores (module doc's chunked twin); needs workspace;
+ *                      for the per-channel gate every 32-token chunk's total log-decay must stay
+ *                      above -170 per channel (a bounded gate such as KDA's >= -5 per token
+ *                      satisfies it), otherwise kda_device_status reports 40008.
+ *                      KDA_ALGO_AUTO takes the chunked form when a large-enough workspace is given
+ *                      and the longest sequence has at least 64 tokens, else the sequential one.
+ * workspace            device scratch [16B], at least kda_scan_workspace_bytes(...) bytes for
+ *                      KDA_ALGO_CHUNK (40009 otherwise), or NULL.  Its contents are overwritten;
+ *                      calls that share a workspace must not overlap on the GPU.
  * T == 0 copies state_in to state_out.
  */
 int kda_scan(const float* q_hat, const float* k_hat, const float* v_hat, const float* g,
