@@ -659,9 +659,10 @@ size_t chunk_workspace_bytes(const SeqLayout& s, const int* cu_host, int H) {
     return header + (size_t)chunk_count(s, cu_host) * H * kBlkBytes;
 }
 
+// Opt a kernel into `bytes` of dynamic shared memory once per device; `done` is the caller's own
+// per-kernel flag array (one per template instantiation).
 template <typename K>
-static cudaError_t set_smem(K kernel, size_t bytes) {
-    static int done[64] = {0};
+static cudaError_t set_smem(K kernel, size_t bytes, int (&done)[64]) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -686,7 +687,8 @@ static cudaError_t launch_chunk_t(const ScanArgs& a, const int* cu_host, void* w
     }
     if (nchunks > 0) {
         const size_t smem1 = sizeof(IntraSmem) + 1024;
-        cudaError_t e = set_smem(kda_chunk_intra_kernel<GM, EXP>, smem1);
+        static int done1[64] = {0};
+        cudaError_t e = set_smem(kda_chunk_intra_kernel<GM, EXP>, smem1, done1);
         if (e != cudaSuccess) return e;
         dim3 g1((unsigned)nchunks, (unsigned)a.H);
         kda_chunk_intra_kernel<GM, EXP><<<g1, kThr, smem1, s>>>(a, chunk_off, ws);
@@ -694,7 +696,8 @@ static cudaError_t launch_chunk_t(const ScanArgs& a, const int* cu_host, void* w
         if (e != cudaSuccess) return e;
     }
     const size_t smem2 = sizeof(InterSmem) + 1024;
-    cudaError_t e = set_smem(kda_chunk_inter_kernel<GM>, smem2);
+    static int done2[64] = {0};
+    cudaError_t e = set_smem(kda_chunk_inter_kernel<GM>, smem2, done2);
     if (e != cudaSuccess) return e;
     dim3 g2((unsigned)a.H, (unsigned)a.seq.N);
     kda_chunk_inter_kernel<GM><<<g2, kThr, smem2, s>>>(a, chunk_off, ws);
