@@ -153,6 +153,8 @@ const char* kda_status_string(int s) {
         case KDA_ERR_TIMEOUT: return "a kernel gave up a bounded device wait";
         case KDA_ERR_WORKSPACE: return "workspace missing or too small";
         case KDA_ERR_ALIGN: return "a pointer that must be 16-byte aligned is not";
+        case KDA_ERR_SCRATCH_LIMIT:
+            return "the chunked scratch this call needs exceeds KDA_STATIC_SCRATCH_BYTES";
         default:
             if (s >= KDA_ERR_CUDA_BASE && s < KDA_ERR_CUDA_BASE + 10000) return "CUDA error";
             return "unknown status";
@@ -293,6 +295,29 @@ int kda_device_status(void* stream) {
         return KDA_ERR_TIMEOUT;
     }
     return KDA_OK;
+}
+
+int kda_scan_varlen_static(const float* q_hat, const float* k_hat, const float* v_hat,
+                           const float* g, int gate_mode, const float* beta,
+                           const float* state_in, float* state_out, float* o,
+                           const int* cu_seqlens, const int* cu_seqlens_host, int N, int total_T,
+                           int H, int D, float scale, void* stream) {
+    // every contract check that does not need the device comes before the scratch setup
+    if (D != kHeadDim) return KDA_ERR_HEAD_DIM;
+    if (N < 0 || total_T < 0 || N > kMaxGridY || H <= 0) return KDA_ERR_SHAPE;
+    if (N == 0) return KDA_OK;
+    if (cu_seqlens == nullptr) return KDA_ERR_NULL;
+    const int rc = check_cu(cu_seqlens_host, N, total_T);
+    if (rc) return rc;
+    const SeqLayout seq{cu_seqlens, 0, N, (long)total_T};
+    if (chunk_workspace_bytes(seq, cu_seqlens_host, H) > kStaticScratchBytes)
+        return KDA_ERR_SCRATCH_LIMIT;
+    void* scratch = nullptr;
+    const cudaError_t e = static_scratch(&scratch);
+    if (e != cudaSuccess) return cuda_status(e);
+    return scan_impl(q_hat, k_hat, v_hat, g, gate_mode, beta, state_in, state_out, o, seq,
+                     cu_seqlens_host, H, D, scale, KDA_ALGO_CHUNK, scratch, kStaticScratchBytes,
+                     stream);
 }
 
 }  // extern "C"

@@ -62,6 +62,11 @@ cudaError_t launch_scan_chunk(const ScanArgs& a, const int* cu_host, void* works
                               cudaStream_t s);
 // exact workspace the chunked scan needs for this layout (cu_host: host copy of cu_seqlens)
 size_t chunk_workspace_bytes(const SeqLayout& s, const int* cu_host, int H);
+
+// Fixed device scratch for kda_scan_varlen_static (kda_scan_static.cu): its byte size, and the
+// address of this device's copy (looked up once per device, on the first call with it current).
+constexpr size_t kStaticScratchBytes = (size_t)32 << 20;
+cudaError_t static_scratch(void** ptr);
 constexpr int kChunkTokens = 32;        // tokens per chunk of the chunked scan
 constexpr size_t kChunkBlockBytes = 70144;  // workspace bytes per (chunk, head)
 

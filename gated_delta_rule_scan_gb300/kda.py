@@ -29,6 +29,7 @@ GATE_EXP = 2  # flag: g holds decay factors exp(log-decay)
 ALGO_AUTO, ALGO_SEQ, ALGO_CHUNK = 0, 1, 2
 HEAD_DIM = 128
 DECODE_MAX_T = 16
+STATIC_SCRATCH_BYTES = 32 << 20  # kda_scan_varlen_static's fixed device scratch
 
 _P, _I, _F, _L, _Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_long, ctypes.c_size_t
 
@@ -50,6 +51,9 @@ _lib.kda_scan_varlen.restype = _I
 _lib.kda_scan_varlen.argtypes = [_P, _P, _P, _P, _I, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F,
                                  _I, _P, _Z, _P]
 _lib.kda_gated_rmsnorm_out.restype = _I
+_lib.kda_scan_varlen_static.restype = _I
+_lib.kda_scan_varlen_static.argtypes = [_P, _P, _P, _P, _I, _P, _P, _P, _P, _P, _P, _I, _I, _I,
+                                        _I, _F, _P]
 _lib.kda_gated_rmsnorm_out.argtypes = [_P, _P, _P, _P, _L, _I, _F, _P]
 _lib.kda_decode_fused.restype = _I
 _lib.kda_decode_fused.argtypes = [_P, _P, _P, _I, _P, _P, _P, _P, _P, _P, _I, _F, _P, _P, _P, _P,
@@ -60,7 +64,8 @@ _lib.kda_device_status.argtypes = [_P]
 # every symbol include/kda.h declares
 EXPORTED = ("kda_abi_version", "kda_status_string", "kda_conv_l2norm_prep",
             "kda_conv_l2norm_prep_varlen", "kda_scan_workspace_bytes", "kda_scan",
-            "kda_scan_varlen", "kda_gated_rmsnorm_out", "kda_decode_fused", "kda_device_status")
+            "kda_scan_varlen", "kda_gated_rmsnorm_out", "kda_decode_fused", "kda_device_status",
+            "kda_scan_varlen_static")
 
 
 class KdaError(RuntimeError):
@@ -167,6 +172,20 @@ def kda_scan_varlen(q_hat, k_hat, v_hat, g, beta, state_in, state_out, o, cu_seq
         _ptr(q_hat), _ptr(k_hat), _ptr(v_hat), _ptr(g), gate_mode, _ptr(beta), _ptr(state_in),
         _ptr(state_out), _ptr(o), _ptr(cu_seqlens), _ptr(cu_seqlens_host), N, total, H, D, scale,
         algo, _ptr(workspace), ws_bytes, st))
+
+
+def kda_scan_varlen_static(q_hat, k_hat, v_hat, g, beta, state_in, state_out, o, cu_seqlens,
+                           cu_seqlens_host, *, H, gate_mode=0, scale=None, D=HEAD_DIM,
+                           stream=None):
+    """kda_scan_varlen's chunked form on the library's fixed device scratch (no allocation)."""
+    N = cu_seqlens_host.numel() - 1
+    total = int(cu_seqlens_host[-1])
+    scale = D ** -0.5 if scale is None else scale
+    st = _stream(stream, state_out)
+    _check("kda_scan_varlen_static", _lib.kda_scan_varlen_static(
+        _ptr(q_hat), _ptr(k_hat), _ptr(v_hat), _ptr(g), gate_mode, _ptr(beta), _ptr(state_in),
+        _ptr(state_out), _ptr(o), _ptr(cu_seqlens), _ptr(cu_seqlens_host), N, total, H, D, scale,
+        st))
 
 
 def kda_gated_rmsnorm_out(o, norm_w, gate_raw, y, *, rows, eps=1e-6, D=HEAD_DIM, stream=None):

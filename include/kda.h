@@ -50,6 +50,8 @@ extern "C" {
 #define KDA_ERR_TIMEOUT 40008         /* a kernel gave up a bounded device wait (kda_device_status) */
 #define KDA_ERR_WORKSPACE 40009       /* workspace NULL or smaller than kda_scan_workspace_bytes */
 #define KDA_ERR_ALIGN 40010           /* a [16B] pointer is not 16-byte aligned */
+#define KDA_ERR_SCRATCH_LIMIT 40011   /* kda_scan_varlen_static: problem needs more scratch than
+                                         KDA_STATIC_SCRATCH_BYTES */
 
 /* enums */
 #define KDA_DTYPE_F32 0
@@ -63,6 +65,7 @@ extern "C" {
 #define KDA_ALGO_CHUNK 2
 
 #define KDA_HEAD_DIM 128
+#define KDA_STATIC_SCRATCH_BYTES 33554432u  /* kda_scan_varlen_static's fixed scratch (32 MiB) */
 #define KDA_DECODE_MAX_T 16
 
 /* ABI revision of this header; bumped on any signature change. */
@@ -176,6 +179,34 @@ int kda_scan_varlen(const float* q_hat, const float* k_hat, const float* v_hat, 
                     float* o, const int* cu_seqlens, const int* cu_seqlens_host, int N,
                     int total_T, int H, int D, float scale, int algo, void* workspace,
                     size_t workspace_bytes, void* stream);
+
+/*
+ * kda_scan_varlen_static -- kda_scan_varlen with algo KDA_ALGO_CHUNK, except that the chunked
+ * form's scratch is a fixed array of KDA_STATIC_SCRATCH_BYTES (32 MiB) inside the library rather
+ * than a caller workspace: the call allocates no device or host memory (no cudaMalloc, no
+ * allocating library routine).  The KDA pages have no counterpart to this entry point; it serves
+ * callers that may not allocate device memory on their call path.
+ *
+ * Arguments, layouts, results and errors as in kda_scan_varlen (algo and workspace are implied).
+ * The results equal kda_scan_varlen with KDA_ALGO_CHUNK bit for bit.
+ * Size limit: the problem's chunked scratch -- kda_scan_workspace_bytes for its exact lengths,
+ * a 256-byte header plus 70,144 bytes per (32-token chunk, head), about
+ * H * sum_n ceil(len_n / 32) <= 478 -- must fit KDA_STATIC_SCRATCH_BYTES; a larger problem
+ * returns 40011 and launches nothing.
+ * Setup: the first call on each device looks up the array's address once, with that device
+ * current (a failure returns 10000 + its cudaError_t).  Make that first call before any stream
+ * capture begins.
+ * Zeroing: nothing in the scratch has to start at zero; every byte the call reads it has first
+ * written itself, so no clearing happens between calls.
+ * Concurrency: the array is one per device and shared by every call on it.  Calls that may run
+ * at the same time on the GPU (different streams, or several host threads) race on it and
+ * corrupt one another's results; serialise them on one stream.
+ */
+int kda_scan_varlen_static(const float* q_hat, const float* k_hat, const float* v_hat,
+                           const float* g, int gate_mode, const float* beta,
+                           const float* state_in, float* state_out, float* o,
+                           const int* cu_seqlens, const int* cu_seqlens_host, int N, int total_T,
+                           int H, int D, float scale, void* stream);
 
 /*
  * kda_gated_rmsnorm_out -- stage 6 of kda_core_gated (Engine::kda_gated_rmsnorm): per row of D

@@ -34,7 +34,7 @@ def test_every_declared_symbol_is_exported(kda):
 
 def test_status_strings(kda):
     assert kda.abi_version() == 1
-    for code in (0, 40001, 40002, 40003, 40004, 40005, 40006, 40007, 40008, 40009, 40010):
+    for code in (0, 40001, 40002, 40003, 40004, 40005, 40006, 40007, 40008, 40009, 40010, 40011):
         assert kda.status_string(code) not in ("unknown status",)
     assert kda.status_string(10000 + 2) == "CUDA error"
 
@@ -106,3 +106,23 @@ def test_prep_and_decode_contract(kda):
     norm = lib.kda_gated_rmsnorm_out(FAKE, FAKE + 8, FAKE, FAKE, ctypes.c_long(4), 128, F(1e-6),
                                      None)
     assert norm == 40010
+
+
+def test_static_scan_contract(kda):
+    """kda_scan_varlen_static refuses, before any device call, a problem whose chunked scratch
+    exceeds KDA_STATIC_SCRATCH_BYTES, besides kda_scan_varlen's own contract."""
+    lib = kda.library()
+    a = [FAKE] * 4 + [0, FAKE, FAKE, FAKE * 8, FAKE]
+    per_block = 70144
+    cap_blocks = (kda.STATIC_SCRATCH_BYTES - 256) // per_block
+
+    def call(cu, H, D=128):
+        arr = (ctypes.c_int * len(cu))(*cu)
+        return lib.kda_scan_varlen_static(*a, FAKE, ctypes.cast(arr, ctypes.c_void_p),
+                                          len(cu) - 1, cu[-1], H, D, ctypes.c_float(1.0), None)
+    assert call([0, 32 * (cap_blocks + 1)], 1) == 40011
+    assert call([0, 32 * (cap_blocks // 2 + 1) - 5, 32 * (cap_blocks + 2) - 10], 2) == 40011
+    assert call([0, 3, 2], 1) == 40006
+    assert call([0, 64], 1, D=64) == 40001
+    assert call([0, 64], 0) == 40005
+    assert kda.status_string(40011) != "unknown status"
