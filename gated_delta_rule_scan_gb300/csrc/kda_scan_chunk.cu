@@ -51,7 +51,7 @@ constexpr int kDevErrRange = 2;          // device error word bit: chunk gate ou
 // ---- workspace block of one (chunk, head) ----------------------------------------------------
 constexpr int kQWBytes = 64 * 128 * 2;             // [Q e^G (32 rows) ; W (32 rows)] x 128 k
 constexpr int kB2Bytes = (128 + kCc) * kCc * 2;    // [(K e^{G_C-G})^T (128 rows) ; Aqk (32)] x 32
-constexpr int kUTBytes = 128 * kCc * 4;            // U^T f32 [128 v][32 t]
+constexpr int kUTBytes = 128 * kCc * 4;            // U f32 [32 t][128 v]
 constexpr int kEGBytes = 128 * 4;                  // e^{G_C} f32 [128]
 constexpr int kOffQW = 0;                          // hi, then lo at + kQWBytes
 constexpr int kOffB2 = 2 * kQWBytes;               // hi, then lo at + kB2Bytes
@@ -161,30 +161,34 @@ __global__ void __launch_bounds__(1024) kda_chunk_offsets_kernel(const int* cu, 
 // kernel 1: intra-chunk quantities, one CTA per (chunk, head)
 // ============================================================================================
 
-struct __align__(1024) IntraSmem {
-    // kb is followed by bia so that kb's 128-row descriptor (32 rows used) stays inside
-    unsigned char kb[2][kCc * 128 * 2];          // K e^{c-G}           [32 s x 128 k]
-    unsigned char bia[2][64 * 128 * 2];          // [K e^{G-c} ; Q e^{G-c}]  [64 x 128 k]
-    unsigned char kt[2][128 * kCc * 2];          // (beta K e^G)^T      [128 k x 32 s]
-    unsigned char vt[2][128 * kCc * 2];          // (beta V)^T          [128 v x 32 s]
-    unsigned char tm[2][kCc * kCc * 2];          // Tm                  [32 t x 32 s]
-    float G[kCc][128];                           // cumulative log-decay
-    float amat[kCc][kCc + 1];                    // beta_t A[t][s], strictly lower
-    float tinv[kCc][kCc + 1];                    // Tm (f32) while it is assembled
+struct __align__(128) IntraSmem {
+    // MMA-a A operand [K e^{G-c} ; Q e^{G-c}] (64 rows, K = 128 channels).  Its 128-row
+    // descriptor reads rows 64..127 from the 16 KB that follow (bia[1] after bia[0], kb after
+    // bia[1]); those accumulator rows are discarded.
+    // After MMA-a its first 16 KB hold the MMA-b A operand: Tm in four copies [4 x 32 t x 32 s],
+    // hi then lo (8 KB each).
+    unsigned char bia[2][64 * 128 * 2];
+    unsigned char kb[2][kCc * 128 * 2];          // K e^{c-G}            [32 s x 128 k]  MMA-a B
+    unsigned char ktv[2][256 * kCc * 2];         // [(beta K e^G)^T ; (beta V)^T] [256 x 32 s]  MMA-b B
+    float scr[kCc * 128];                        // G [32 t][128 k]; after MMA-a: A, Tm, products
     float beta[kCc];
-    float gs[kCc];                               // per-head cumulative gate (GDN)
+    float gs[kCc];                               // per-head log-gate per token (GDN)
+    float gsc[kCc];                              // its running sum (GDN)
     float cref[128];
     float ecr[128];
     uint64_t bar;
     uint32_t tmem_base;
 };
+constexpr int kLd = kCc + 1;                     // row stride of the 32 x 32 f32 matrices in scr
+constexpr int kTmBytes = 128 * kCc * 2;          // one (hi or lo) four-copy Tm image
+static_assert(2 * kTmBytes <= 64 * 128 * 2, "Tm fits in bia[0]");
 
 template <int GATE_MODE, bool EXP>
 __global__ void __launch_bounds__(kThr, 2)
 kda_chunk_intra_kernel(ScanArgs a, const int* chunk_off, unsigned char* ws) {
     extern __shared__ unsigned char smem_raw[];
     IntraSmem& sm = *reinterpret_cast<IntraSmem*>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+        (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int h = blockIdx.y;
     const long gid = blockIdx.x;                 // global chunk index
@@ -210,32 +214,32 @@ kda_chunk_intra_kernel(ScanArgs a, const int* chunk_off, unsigned char* ws) {
     const long row0 = begin + c * kCc;
     const int nt = (int)min((long)kCc, end - row0);
     unsigned char* blk = ws + ((long)gid * H + h) * kBlkBytes;
+    const long hoff = row0 * C + (long)h * kHeadDim;
 
-    if (warp == 0) {
-        tmem_alloc(&sm.tmem_base, 128);
-        tmem_relinquish();
-    }
-    if (tid == 0) {
-        mbar_init(&sm.bar, 1);
-        fence_mbar_init();
-    }
-
-    // ---- cumulative gate, beta ---------------------------------------------------------------
-    if (GATE_MODE == 0) {
-        float gv[kCc];
+    // ---- every global load of the chunk is issued before any store ---------------------------
+    // column role: channel tid over the chunk's 32 tokens
+    float kc[kCc], vc[kCc], gc[kCc];
 #pragma unroll
-        for (int t = 0; t < kCc; ++t)
-            gv[t] = t < nt ? a.g[(row0 + t) * C + h * kHeadDim + tid] : (EXP ? 1.0f : 0.0f);
-        float G = 0.0f;
+    for (int t = 0; t < kCc; ++t) {
+        const bool live = t < nt;
+        kc[t] = live ? __ldg(a.k + hoff + t * C + tid) : 0.0f;
+        vc[t] = live ? __ldg(a.v + hoff + t * C + tid) : 0.0f;
+        if (GATE_MODE == 0) gc[t] = live ? __ldg(a.g + hoff + t * C + tid) : (EXP ? 1.0f : 0.0f);
+    }
+    // row role: tokens tr + 8j (j = 0..3), channels k0 .. k0+7
+    const int tr = tid >> 4, k0 = (tid & 15) * 8;
+    float4 kr[4][2], qr[4][2];
 #pragma unroll
-        for (int t = 0; t < kCc; ++t) {
-            G += EXP ? logf(gv[t]) : gv[t];
-            sm.G[t][tid] = G;
+    for (int j = 0; j < 4; ++j) {
+        const int t = tr + 8 * j;
+        if (t < nt) {
+            const float4* kp = reinterpret_cast<const float4*>(a.k + hoff + t * C + k0);
+            const float4* qp = reinterpret_cast<const float4*>(a.q + hoff + t * C + k0);
+            kr[j][0] = __ldg(kp); kr[j][1] = __ldg(kp + 1);
+            qr[j][0] = __ldg(qp); qr[j][1] = __ldg(qp + 1);
+        } else {
+            kr[j][0] = kr[j][1] = qr[j][0] = qr[j][1] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
-        sm.cref[tid] = 0.5f * G;
-        sm.ecr[tid] = __expf(0.5f * G);
-        reinterpret_cast<float*>(blk + kOffEG)[tid] = decay_f(G);
-        if (G < -170.0f && a.err) atomicOr(a.err, kDevErrRange);
     }
     if (tid < kCc) {
         const bool live = tid < nt;
@@ -245,80 +249,100 @@ kda_chunk_intra_kernel(ScanArgs a, const int* chunk_off, unsigned char* ws) {
             sm.gs[tid] = EXP ? logf(x) : x;
         }
     }
-    __syncthreads();
-    if (GATE_MODE == 1) {
-        if (tid == 0) {
-            float G = 0.0f;
-            for (int t = 0; t < kCc; ++t) { G += sm.gs[t]; sm.gs[t] = G; }
-        }
-        __syncthreads();
-        reinterpret_cast<float*>(blk + kOffEG)[tid] = decay_f(sm.gs[kCc - 1]);
+
+    if (warp == 0) {
+        tmem_alloc(&sm.tmem_base, 256);
+        tmem_relinquish();
+    }
+    if (tid == 0) {
+        mbar_init(&sm.bar, 1);
+        fence_mbar_init();
     }
 
-    // ---- row images: item = (token t, channels k0..k0+7) --------------------------------------
-    for (int it = tid; it < kCc * 16; it += kThr) {
-        const int t = it >> 4, k0 = (it & 15) * 8;
+    // ---- cumulative gate: gc[t] = G_t of channel tid (KDA) or of the head (GDN) ---------------
+    if (GATE_MODE == 0) {
+        float G = 0.0f;
+#pragma unroll
+        for (int t = 0; t < kCc; ++t) {
+            G += EXP ? logf(gc[t]) : gc[t];
+            gc[t] = G;
+            sm.scr[t * 128 + tid] = G;
+        }
+        sm.cref[tid] = 0.5f * G;
+        sm.ecr[tid] = __expf(0.5f * G);
+        reinterpret_cast<float*>(blk + kOffEG)[tid] = decay_f(G);
+        if (G < -170.0f && a.err) atomicOr(a.err, kDevErrRange);
+    }
+    __syncthreads();
+    if (GATE_MODE == 1) {
+        float G = 0.0f;
+#pragma unroll
+        for (int t = 0; t < kCc; ++t) {
+            G += sm.gs[t];
+            gc[t] = G;
+        }
+        if (tid < kCc) {
+            float Gt = 0.0f;
+            for (int t = 0; t <= tid; ++t) Gt += sm.gs[t];   // same summation order as gc
+            sm.gsc[tid] = Gt;
+        }
+        reinterpret_cast<float*>(blk + kOffEG)[tid] = decay_f(G);
+    }
+
+    // ---- column images: channel tid, tokens 8j .. 8j+7 ----------------------------------------
+    {
+        const float GC = gc[kCc - 1];
+#pragma unroll
+        for (int j = 0; j < kCc / 8; ++j) {
+            float xt[8], xv[8], xc[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int t = 8 * j + e;
+                const float bt = sm.beta[t];
+                xt[e] = bt * kc[t] * __expf(gc[t]);
+                xv[e] = bt * vc[t];
+                xc[e] = kc[t] * __expf(GC - gc[t]);
+            }
+            put8x(sm.ktv[0], sm.ktv[1], tc_offset(tid, 8 * j, kSbo32), xt);
+            put8x(sm.ktv[0], sm.ktv[1], tc_offset(128 + tid, 8 * j, kSbo32), xv);
+            put8x(blk + kOffB2, blk + kOffB2 + kB2Bytes, tc_offset(tid, 8 * j, kSbo32), xc);
+        }
+    }
+    if (GATE_MODE == 1) __syncthreads();          // gsc
+
+    // ---- row images: token t = tr + 8j, channels k0 .. k0+7 -----------------------------------
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int t = tr + 8 * j;
+        const float kv[8] = {kr[j][0].x, kr[j][0].y, kr[j][0].z, kr[j][0].w,
+                             kr[j][1].x, kr[j][1].y, kr[j][1].z, kr[j][1].w};
+        const float qv[8] = {qr[j][0].x, qr[j][0].y, qr[j][0].z, qr[j][0].w,
+                             qr[j][1].x, qr[j][1].y, qr[j][1].z, qr[j][1].w};
         float xb[8], xk[8], xq[8], xg[8];
-        if (t < nt) {
-            const float* kp = a.k + (row0 + t) * C + h * kHeadDim + k0;
-            const float* qp = a.q + (row0 + t) * C + h * kHeadDim + k0;
-            const float4 k4a = *reinterpret_cast<const float4*>(kp);
-            const float4 k4b = *reinterpret_cast<const float4*>(kp + 4);
-            const float4 q4a = *reinterpret_cast<const float4*>(qp);
-            const float4 q4b = *reinterpret_cast<const float4*>(qp + 4);
-            const float kv[8] = {k4a.x, k4a.y, k4a.z, k4a.w, k4b.x, k4b.y, k4b.z, k4b.w};
-            const float qv[8] = {q4a.x, q4a.y, q4a.z, q4a.w, q4b.x, q4b.y, q4b.z, q4b.w};
-            if (GATE_MODE == 0) {
+        if (GATE_MODE == 0) {
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const float gt = sm.G[t][k0 + e], cr = sm.cref[k0 + e];
-                    const float ef = __expf(gt - cr), eb = __expf(cr - gt);
-                    xb[e] = kv[e] * eb;
-                    xk[e] = kv[e] * ef;
-                    xq[e] = qv[e] * ef;
-                    xg[e] = qv[e] * (ef * sm.ecr[k0 + e]);
-                }
-            } else {
-                const float eg = __expf(sm.gs[t]);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    xb[e] = kv[e];
-                    xk[e] = kv[e];
-                    xq[e] = qv[e];
-                    xg[e] = qv[e] * eg;
-                }
+            for (int e = 0; e < 8; ++e) {
+                const float gt = sm.scr[t * 128 + k0 + e], cr = sm.cref[k0 + e];
+                const float ef = __expf(gt - cr), eb = __expf(cr - gt);
+                xb[e] = kv[e] * eb;
+                xk[e] = kv[e] * ef;
+                xq[e] = qv[e] * ef;
+                xg[e] = qv[e] * (ef * sm.ecr[k0 + e]);
             }
         } else {
+            const float eg = __expf(sm.gsc[t]);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) xb[e] = xk[e] = xq[e] = xg[e] = 0.0f;
+            for (int e = 0; e < 8; ++e) {
+                xb[e] = kv[e];
+                xk[e] = kv[e];
+                xq[e] = qv[e];
+                xg[e] = qv[e] * eg;
+            }
         }
         put8x(sm.kb[0], sm.kb[1], tc_offset(t, k0, kSbo128), xb);
         put8x(sm.bia[0], sm.bia[1], tc_offset(t, k0, kSbo128), xk);
         put8x(sm.bia[0], sm.bia[1], tc_offset(kCc + t, k0, kSbo128), xq);
         put8x(blk + kOffQW, blk + kOffQW + kQWBytes, tc_offset(t, k0, kSbo128), xg);
-    }
-    // ---- column images: item = (channel kk, tokens t0..t0+7) ----------------------------------
-    for (int it = tid; it < 128 * (kCc / 8); it += kThr) {
-        const int kk = it & 127, t0 = (it >> 7) * 8;
-        float xt[8], xv[8], xc[8];
-        const float GC = GATE_MODE == 0 ? sm.G[kCc - 1][kk] : sm.gs[kCc - 1];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const int t = t0 + e;
-            if (t < nt) {
-                const float G = GATE_MODE == 0 ? sm.G[t][kk] : sm.gs[t];
-                const float kv = a.k[(row0 + t) * C + h * kHeadDim + kk];
-                const float bt = sm.beta[t];
-                xt[e] = bt * kv * __expf(G);
-                xv[e] = bt * a.v[(row0 + t) * C + h * kHeadDim + kk];
-                xc[e] = kv * __expf(GC - G);
-            } else {
-                xt[e] = xv[e] = xc[e] = 0.0f;
-            }
-        }
-        put8x(sm.kt[0], sm.kt[1], tc_offset(kk, t0, kSbo32), xt);
-        put8x(sm.vt[0], sm.vt[1], tc_offset(kk, t0, kSbo32), xv);
-        put8x(blk + kOffB2, blk + kOffB2 + kB2Bytes, tc_offset(kk, t0, kSbo32), xc);
     }
     fence_proxy_async_smem();
     tc_fence_before();
@@ -328,91 +352,124 @@ kda_chunk_intra_kernel(ScanArgs a, const int* chunk_off, unsigned char* ws) {
     const uint32_t tlane = tbase + ((uint32_t)(32 * warp) << 16);
     uint32_t phase = 0;
     bool ok = true;
+    float* am = sm.scr;                          // A (strictly lower), f32 [32][kLd]
+    float* ti = sm.scr + kCc * kLd;              // Tm
+    float* pb = sm.scr + 2 * kCc * kLd;          // block products
+    unsigned char* tmh = sm.bia[0];              // Tm image, written once MMA-a has completed
+    unsigned char* tml = sm.bia[0] + kTmBytes;
 
-    // ---- MMA-a: D[s][n] = (K e^{c-G})_s . (K e^{G-c} | Q e^{G-c})_n ----------------------------
+    // ---- MMA-a: D[r][s] = (K e^{G-c} ; Q e^{G-c})_r . (K e^{c-G})_s ---------------------------
     if (tid == 0) {
-        mma3_ss(tbase, tc_smem_desc(smem_u32(sm.kb[0]), 128, kSbo128),
-                tc_smem_desc(smem_u32(sm.kb[1]), 128, kSbo128),
-                tc_smem_desc(smem_u32(sm.bia[0]), 128, kSbo128),
-                tc_smem_desc(smem_u32(sm.bia[1]), 128, kSbo128), 8, tc_idesc_bf16(128, 64));
+        mma3_ss(tbase, tc_smem_desc(smem_u32(sm.bia[0]), 128, kSbo128),
+                tc_smem_desc(smem_u32(sm.bia[1]), 128, kSbo128),
+                tc_smem_desc(smem_u32(sm.kb[0]), 128, kSbo128),
+                tc_smem_desc(smem_u32(sm.kb[1]), 128, kSbo128), 8, tc_idesc_bf16(128, kCc));
         tc_commit(&sm.bar);
     }
+    for (int i = tid; i < kCc * kLd; i += kThr) ti[i] = 0.0f;   // G is dead: scr is free
     ok = mbar_wait_bounded(&sm.bar, phase, a.err);
     phase ^= 1u;
     tc_fence_after();
     if (__syncthreads_or(!ok)) goto done;
 
-    // ---- A, Aqk, Tm (warp 0; lane s = key token s) --------------------------------------------
-    if (warp == 0) {
-        float d[64];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) tmem_ld16(tlane + 16 * q, *reinterpret_cast<float(*)[16]>(&d[16 * q]));
+    // ---- A (warp 0, lane t = row t) and Aqk (warp 1, lane t) -----------------------------------
+    if (warp < 2) {
+        float d[kCc];
+        tmem_ld16(tlane, *reinterpret_cast<float(*)[16]>(&d[0]));
+        tmem_ld16(tlane + 16, *reinterpret_cast<float(*)[16]>(&d[16]));
         tmem_ld_wait();
-        const int s = lane;
-        const float Gs = GATE_MODE == 1 ? sm.gs[s] : 0.0f;
-        unsigned char* b2h = blk + kOffB2;
-        unsigned char* b2l = blk + kOffB2 + kB2Bytes;
+        const int t = lane;
+        const float Gt = GATE_MODE == 1 ? sm.gsc[t] : 0.0f;
+        if (warp == 0) {
+            const float bt = sm.beta[t];
 #pragma unroll
-        for (int t = 0; t < kCc; ++t) {
-            float fac = 1.0f;
-            if (GATE_MODE == 1) fac = __expf(fminf(sm.gs[t] - Gs, 0.0f));
-            sm.amat[t][s] = t > s ? sm.beta[t] * d[t] * fac : 0.0f;
-            put1x(b2h, b2l, tc_offset(128 + t, s, kSbo32), t >= s ? d[kCc + t] * fac : 0.0f);
-        }
-        __syncwarp();
-        // diagonal 16x16 blocks by forward substitution: lane s solves column s of its block
-        {
-            const int b0 = s < 16 ? 0 : 16;
-            float x[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                float acc = (b0 + i == s) ? 1.0f : 0.0f;
-#pragma unroll
-                for (int j = 0; j < i; ++j) acc = fmaf(-sm.amat[b0 + i][b0 + j], x[j], acc);
-                x[i] = acc;
-                sm.tinv[b0 + i][s] = acc;
+            for (int s = 0; s < kCc; ++s) {
+                const float fac = GATE_MODE == 1 ? __expf(fminf(Gt - gc[s], 0.0f)) : 1.0f;
+                am[t * kLd + s] = s < t ? bt * d[s] * fac : 0.0f;
             }
-            if (s < 16) {
+        } else {
+            unsigned char* b2h = blk + kOffB2;
+            unsigned char* b2l = blk + kOffB2 + kB2Bytes;
 #pragma unroll
-                for (int i = 0; i < 16; ++i) sm.tinv[i][16 + s] = 0.0f;  // upper-right block
+            for (int sb = 0; sb < kCc / 8; ++sb) {
+                float x[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int s = 8 * sb + e;
+                    const float fac = GATE_MODE == 1 ? __expf(fminf(Gt - gc[s], 0.0f)) : 1.0f;
+                    x[e] = s <= t ? d[s] * fac : 0.0f;
+                }
+                put8x(b2h, b2l, tc_offset(128 + t, 8 * sb, kSbo32), x);
             }
         }
-        __syncwarp();
-        // lower-left block: T21 = -T22 A21 T11 (lane s < 16 owns column s)
-        if (s < 16) {
-            float m1[16];
+    }
+    __syncthreads();
+
+    // ---- Tm = (I + A)^{-1}: 8x8 diagonal blocks by substitution, then two doubling steps of
+    //      [T11 0; T21 T22] with T21 = -T22 A21 T11 ------------------------------------------
+    if (tid < kCc) {
+        const int b8 = (tid >> 3) * 8, j = tid & 7;
+        float x[8];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {     // (A21 T11)[i][s]
-                float acc = 0.0f;
+        for (int r = 0; r < 8; ++r) {
+            float acc = r == j ? 1.0f : 0.0f;
 #pragma unroll
-                for (int j = 0; j < 16; ++j) acc = fmaf(sm.amat[16 + i][j], sm.tinv[j][s], acc);
-                m1[i] = acc;
-            }
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {     // -(T22 m1)[i]
-                float acc = 0.0f;
-#pragma unroll
-                for (int j = 0; j < 16; ++j) acc = fmaf(sm.tinv[16 + i][16 + j], m1[j], acc);
-                sm.tinv[16 + i][s] = -acc;
-            }
+            for (int m = 0; m < r; ++m) acc = fmaf(-am[(b8 + r) * kLd + b8 + m], x[m], acc);
+            x[r] = acc;
+            ti[(b8 + r) * kLd + b8 + j] = acc;
         }
-        __syncwarp();
+    }
+    __syncthreads();
+    {
+        const int p = tid >> 6, r = (tid & 63) >> 3, cc = tid & 7;
+        const int r0 = 16 * p + 8, c0 = 16 * p;
+        float acc = 0.0f;
 #pragma unroll
-        for (int t = 0; t < kCc; ++t) put1x(sm.tm[0], sm.tm[1], tc_offset(t, s, kSbo32), sm.tinv[t][s]);
+        for (int m = 0; m < 8; ++m) acc = fmaf(am[(r0 + r) * kLd + c0 + m], ti[(c0 + m) * kLd + c0 + cc], acc);
+        pb[(r0 + r) * kLd + c0 + cc] = acc;
+        __syncthreads();
+        acc = 0.0f;
+#pragma unroll
+        for (int m = 0; m < 8; ++m) acc = fmaf(ti[(r0 + r) * kLd + r0 + m], pb[(r0 + m) * kLd + c0 + cc], acc);
+        ti[(r0 + r) * kLd + c0 + cc] = -acc;
+        __syncthreads();
+    }
+#pragma unroll
+    for (int e = tid; e < 256; e += kThr) {
+        const int r = e >> 4, cc = e & 15;
+        float acc = 0.0f;
+#pragma unroll
+        for (int m = 0; m < 16; ++m) acc = fmaf(am[(16 + r) * kLd + m], ti[m * kLd + cc], acc);
+        pb[(16 + r) * kLd + cc] = acc;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int e = tid; e < 256; e += kThr) {
+        const int r = e >> 4, cc = e & 15;
+        float acc = 0.0f;
+#pragma unroll
+        for (int m = 0; m < 16; ++m) acc = fmaf(ti[(16 + r) * kLd + 16 + m], pb[(16 + m) * kLd + cc], acc);
+        ti[(16 + r) * kLd + cc] = -acc;
+    }
+    __syncthreads();
+    {   // Tm image, four copies (rows t, 32+t, 64+t, 96+t) so that each warp reads its own
+        const int t = tid >> 2, s0 = (tid & 3) * 8;
+        float x[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] = ti[t * kLd + s0 + e];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) put8x(tmh, tml, tc_offset(32 * r + t, s0, kSbo32), x);
     }
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
 
-    // ---- MMA-b: [W^T | U^T] = (beta K e^G | beta V)^T Tm^T -----------------------------------
+    // ---- MMA-b: [W | U] = Tm [(beta K e^G) | (beta V)], every warp's 32 lanes = tokens --------
     if (tid == 0) {
-        const uint64_t tmh = tc_smem_desc(smem_u32(sm.tm[0]), 128, kSbo32);
-        const uint64_t tml = tc_smem_desc(smem_u32(sm.tm[1]), 128, kSbo32);
-        mma3_ss(tbase + 64, tc_smem_desc(smem_u32(sm.kt[0]), 128, kSbo32),
-                tc_smem_desc(smem_u32(sm.kt[1]), 128, kSbo32), tmh, tml, 2, tc_idesc_bf16(128, 32));
-        mma3_ss(tbase + 96, tc_smem_desc(smem_u32(sm.vt[0]), 128, kSbo32),
-                tc_smem_desc(smem_u32(sm.vt[1]), 128, kSbo32), tmh, tml, 2, tc_idesc_bf16(128, 32));
+        mma3_ss(tbase, tc_smem_desc(smem_u32(tmh), 128, kSbo32), tc_smem_desc(smem_u32(tml), 128, kSbo32),
+                tc_smem_desc(smem_u32(sm.ktv[0]), 128, kSbo32),
+                tc_smem_desc(smem_u32(sm.ktv[1]), 128, kSbo32), 2, tc_idesc_bf16(128, 256));
         tc_commit(&sm.bar);
     }
     ok = mbar_wait_bounded(&sm.bar, phase, a.err);
@@ -420,25 +477,30 @@ kda_chunk_intra_kernel(ScanArgs a, const int* chunk_off, unsigned char* ws) {
     tc_fence_after();
     if (__syncthreads_or(!ok)) goto done;
     {
-        float w[32], u[32];
-        tmem_ld16(tlane + 64, *reinterpret_cast<float(*)[16]>(&w[0]));
-        tmem_ld16(tlane + 80, *reinterpret_cast<float(*)[16]>(&w[16]));
-        tmem_ld16(tlane + 96, *reinterpret_cast<float(*)[16]>(&u[0]));
-        tmem_ld16(tlane + 112, *reinterpret_cast<float(*)[16]>(&u[16]));
+        // warp w: columns 64w .. 64w+63 of [W | U] for token t = lane
+        const int t = lane;
+        float x[64];
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            tmem_ld16(tlane + 64 * warp + 16 * q, *reinterpret_cast<float(*)[16]>(&x[16 * q]));
         tmem_ld_wait();
-        // W[t][k = tid] into QW rows 32 + t; U^T[v = tid][t] into the f32 block
-        unsigned char* qwh = blk + kOffQW;
-        unsigned char* qwl = blk + kOffQW + kQWBytes;
+        if (warp < 2) {     // W row t, channels 64w .. : QW image rows 32 + t
+            unsigned char* qwh = blk + kOffQW;
+            unsigned char* qwl = blk + kOffQW + kQWBytes;
 #pragma unroll
-        for (int t = 0; t < kCc; ++t) put1x(qwh, qwl, tc_offset(kCc + t, tid, kSbo128), w[t]);
-        float4* ut = reinterpret_cast<float4*>(blk + kOffUT + tid * kCc * 4);
+            for (int cb = 0; cb < 8; ++cb)
+                put8x(qwh, qwl, tc_offset(kCc + t, 64 * warp + 8 * cb, kSbo128),
+                      *reinterpret_cast<const float(*)[8]>(&x[8 * cb]));
+        } else {            // U row t, values 64(w-2) .. : f32 [32 t][128 v]
+            float4* ut = reinterpret_cast<float4*>(blk + kOffUT) + t * 32 + 16 * (warp - 2);
 #pragma unroll
-        for (int q = 0; q < kCc / 4; ++q) ut[q] = make_float4(u[4 * q], u[4 * q + 1], u[4 * q + 2], u[4 * q + 3]);
+            for (int q = 0; q < 16; ++q) ut[q] = make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
+        }
     }
 done:
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tbase, 128);
+    if (warp == 0) tmem_dealloc(tbase, 256);
 }
 
 // ============================================================================================
@@ -573,16 +635,10 @@ kda_chunk_inter_kernel(ScanArgs a, const int* chunk_off, const unsigned char* ws
             tmem_ld16(tlane + kTD1 + 32, *reinterpret_cast<float(*)[16]>(&x[0]));
             tmem_ld16(tlane + kTD1 + 48, *reinterpret_cast<float(*)[16]>(&x[16]));
             tmem_ld_wait();
-            const float4* ut = reinterpret_cast<const float4*>(B + kOffUT + tid * kCc * 4);
+            const float* ut = reinterpret_cast<const float*>(B + kOffUT) + tid;
             float up[kCc];
 #pragma unroll
-            for (int q = 0; q < kCc / 4; ++q) {
-                const float4 u4 = ut[q];
-                up[4 * q] = u4.x - x[4 * q];
-                up[4 * q + 1] = u4.y - x[4 * q + 1];
-                up[4 * q + 2] = u4.z - x[4 * q + 2];
-                up[4 * q + 3] = u4.w - x[4 * q + 3];
-            }
+            for (int t = 0; t < kCc; ++t) up[t] = ut[t * 128] - x[t];
             tmem_put_split<kCc>(tlane + kTA2, tlane + kTA2 + 16, up);
             tmem_st_wait();
         }
@@ -686,7 +742,7 @@ static cudaError_t launch_chunk_t(const ScanArgs& a, const int* cu_host, void* w
         if (e != cudaSuccess) return e;
     }
     if (nchunks > 0) {
-        const size_t smem1 = sizeof(IntraSmem) + 1024;
+        const size_t smem1 = sizeof(IntraSmem) + 128;
         static int done1[64] = {0};
         cudaError_t e = set_smem(kda_chunk_intra_kernel<GM, EXP>, smem1, done1);
         if (e != cudaSuccess) return e;
