@@ -184,8 +184,11 @@ int kda_scan_varlen(const float* q_hat, const float* k_hat, const float* v_hat, 
  * kda_scan_varlen_static -- kda_scan_varlen with algo KDA_ALGO_CHUNK, except that the chunked
  * form's scratch is a fixed array of KDA_STATIC_SCRATCH_BYTES (32 MiB) inside the library rather
  * than a caller workspace: the call allocates no device or host memory (no cudaMalloc, no
- * allocating library routine).  The KDA pages have no counterpart to this entry point; it serves
- * callers that may not allocate device memory on their call path.
+ * allocating library routine).  The KDA pages have no counterpart to this entry point.  It is for
+ * callers that must not allocate device memory while they run: a serving process that reserves its
+ * whole HBM budget at start-up and turns allocation off afterwards (an allocation then fails, or
+ * stalls the device in the middle of a step), or plain C code with no allocator at hand.  The
+ * array is held on every GPU where the library's scratch module is loaded, until the process exits.
  *
  * Arguments, layouts, results and errors as in kda_scan_varlen (algo and workspace are implied).
  * The results equal kda_scan_varlen with KDA_ALGO_CHUNK bit for bit.

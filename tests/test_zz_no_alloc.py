@@ -1,6 +1,10 @@
 """kda_scan_varlen_static (the chunked scan on the library's fixed device scratch) against
 kda_scan_varlen's chunked form with a caller workspace, through the C ABI.
 
+The static form exists for callers that may not allocate device memory during a call -- a server
+that has reserved its whole HBM budget up front, or C code without an allocator -- so the test
+also checks that a call claims no device memory.
+
 Two static calls in a row -- different sequence lengths, head counts and gate kinds, so the second
 reuses scratch the first left full -- must each equal the workspace path bit for bit.  The file
 name sorts last so the test also runs after every other GPU test; it passes alone as well."""
