@@ -507,10 +507,13 @@ done:
 // kernel 2: the state recurrence over chunks, one CTA per (sequence, head)
 // ============================================================================================
 
-struct __align__(1024) InterSmem {
-    unsigned char blk[2][kBlkBytes];             // double-buffered workspace blocks
-    uint64_t bar_ld[2];
-    uint64_t bar_mma;
+constexpr int kInterStages = 2;                  // workspace blocks in flight per CTA
+
+struct __align__(128) InterSmem {
+    unsigned char blk[kInterStages][kBlkBytes];
+    float otile[2][kCc][128];                    // a chunk's o rows on their way to global memory
+    uint64_t bar_ld[kInterStages];
+    uint64_t bar_mma;                            // MMA-1, then MMA-2
     uint32_t tmem_base;
 };
 
@@ -527,6 +530,14 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
         "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
         : "memory");
 }
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// wait until at most one committed group still reads its shared-memory source
+__device__ __forceinline__ void bulk_wait_read1() {
+    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+// wait until every committed group has completed its writes
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // write NV f32 values (NV multiple of 32) as packed bf16 hi words at col_hi and lo words at col_lo
 template <int NV>
@@ -546,13 +557,30 @@ __device__ __forceinline__ void tmem_put_split(uint32_t col_hi, uint32_t col_lo,
     }
 }
 
+// write 16 f32 values as 8 packed bf16 hi words at col_hi and 8 lo words at col_lo
+__device__ __forceinline__ void tmem_put_split16(uint32_t col_hi, uint32_t col_lo, const float* v) {
+    uint32_t hw[8], lw[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) split_bf16x2(v[2 * i], v[2 * i + 1], hw[i], lw[i]);
+    tmem_st8(col_hi, hw);
+    tmem_st8(col_lo, lw);
+}
+
+// Threads: 256.  Thread (half hf = tid / 128, value row v = tid % 128) owns TMEM lane v; it keeps
+// key columns 64 hf .. 64 hf + 63 of state row v in registers and handles tokens 16 hf .. 16 hf + 15
+// of each chunk's U' and o.  Thread 0 issues the MMAs, thread 32 the workspace loads, and the
+// lanes of warp 2 the o rows' bulk stores (lane t: token t of the chunk).
+constexpr int kThrInter = 256;
+
 template <int GATE_MODE>
-__global__ void __launch_bounds__(kThr, 1)
-kda_chunk_inter_kernel(ScanArgs a, const int* chunk_off, const unsigned char* ws) {
+__global__ void __launch_bounds__(kThrInter, 1)
+kda_chunk_inter_kernel(ScanArgs a, const int* chunk_off, const unsigned char* ws,
+                       const __grid_constant__ CUtensorMap tmo) {
     extern __shared__ unsigned char smem_raw[];
     InterSmem& sm = *reinterpret_cast<InterSmem*>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+        (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
     const int tid = threadIdx.x, warp = tid >> 5;
+    const int v = tid & 127, hf = tid >> 7;
     const int h = blockIdx.x;
     const int n = a.order ? a.order[blockIdx.y] : (int)blockIdx.y;
     const int H = a.H;
@@ -568,17 +596,16 @@ kda_chunk_inter_kernel(ScanArgs a, const int* chunk_off, const unsigned char* ws
         tmem_relinquish();
     }
     if (tid == 0) {
-        mbar_init(&sm.bar_ld[0], 1);
-        mbar_init(&sm.bar_ld[1], 1);
+        for (int i = 0; i < kInterStages; ++i) mbar_init(&sm.bar_ld[i], 1);
         mbar_init(&sm.bar_mma, 1);
         fence_mbar_init();
     }
-    float srow[128];
+    float srow[64];
     {
         const float4* sin = reinterpret_cast<const float4*>(
-            a.state_in + (((long)n * H + h) * kHeadDim + tid) * kHeadDim);
+            a.state_in + (((long)n * H + h) * kHeadDim + v) * kHeadDim + 64 * hf);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
+        for (int j = 0; j < 16; ++j) {
             const float4 x = __ldcs(sin + j);
             srow[4 * j] = x.x; srow[4 * j + 1] = x.y; srow[4 * j + 2] = x.z; srow[4 * j + 3] = x.w;
         }
@@ -587,8 +614,8 @@ kda_chunk_inter_kernel(ScanArgs a, const int* chunk_off, const unsigned char* ws
     __syncthreads();
     tc_fence_after();
     const uint32_t tbase = sm.tmem_base;
-    const uint32_t tlane = tbase + ((uint32_t)(32 * warp) << 16);
-    tmem_put_split<128>(tlane + kTA1, tlane + kTA1 + 64, srow);
+    const uint32_t tl = tbase + ((uint32_t)(32 * (warp & 3)) << 16);
+    tmem_put_split<64>(tl + kTA1 + 32 * hf, tl + kTA1 + 64 + 32 * hf, srow);
     tmem_st_wait();
 
     auto issue = [&](int c, int st) {
@@ -598,48 +625,74 @@ kda_chunk_inter_kernel(ScanArgs a, const int* chunk_off, const unsigned char* ws
         bulk_load(&sm.blk[st][kOffB2], src + kOffB2, 2 * kB2Bytes, &sm.bar_ld[st]);
         bulk_load(&sm.blk[st][kOffUT], src + kOffUT, kUTBytes + kEGBytes, &sm.bar_ld[st]);
     };
-    if (tid == 0) {
-        if (nch > 0) issue(0, 0);
-        if (nch > 1) issue(1, 1);
+    const uint32_t id1 = tc_idesc_bf16(128, 2 * kCc), id2 = tc_idesc_bf16(128, 160);
+    // MMA-1: [O1^T | X^T] = S^T (Q e^G | W)^T for the chunk in stage st.  (One N = 64 group: the
+    // tensor pipe's cost here follows the instruction count, so two N = 32 groups are slower.)
+    auto mma1 = [&](int st) {
+        const unsigned char* B = sm.blk[st];
+        mma3_ts(tbase + kTD1, tbase + kTA1, tbase + kTA1 + 64,
+                tc_smem_desc(smem_u32(B + kOffQW), 128, kSbo128),
+                tc_smem_desc(smem_u32(B + kOffQW + kQWBytes), 128, kSbo128), 8, id1);
+        tc_commit(&sm.bar_mma);
+    };
+    // the state is in TMEM; the first chunk's MMA-1 goes out as soon as its block lands
+    if (tid == 0 && nch > 0) {
+        for (int i = 0; i < kInterStages && i < nch; ++i) issue(i, i);
+        tc_fence_before();
+        if (mbar_wait_bounded(&sm.bar_ld[0], 0, a.err)) {
+            tc_fence_after();
+            mma1(0);
+        }
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
 
-    const uint32_t id1 = tc_idesc_bf16(128, 64), id2 = tc_idesc_bf16(128, 160);
     uint32_t mph = 0;
     bool failed = false;
+    const float scale = a.scale;
+    const bool ostore_lane = warp == 2;
+    const int olane = tid & 31;
+    // store the o rows of chunk cp (staged in otile[cp & 1]) -- warp 2 only.  A full chunk (or
+    // one whose overhang lies past the last row of the tensor) goes out as one TMA tile store;
+    // the ragged last chunk of a sequence followed by another is copied row by row.
+    auto flush_o = [&](int cp) {
+        const long r0 = begin + (long)cp * kCc;
+        const int ntp = (int)min((long)kCc, L - (long)cp * kCc);
+        if (ntp == kCc || end == a.seq.total_rows) {
+            if (olane == 0) tma_store_2d(&tmo, sm.otile[cp & 1], h * kHeadDim, (int)r0);
+        } else {
+            for (int t = 0; t < ntp; ++t)
+                reinterpret_cast<float4*>(a.o + (r0 + t) * C + h * kHeadDim)[olane] =
+                    reinterpret_cast<const float4*>(sm.otile[cp & 1][t])[olane];
+        }
+        bulk_commit();
+    };
     for (int c = 0; c < nch; ++c) {
-        const int st = c & 1;
-        const long row0 = begin + (long)c * kCc;
-        const int nt = (int)min((long)kCc, L - (long)c * kCc);
-        const bool got = mbar_wait_bounded(&sm.bar_ld[st], (uint32_t)((c >> 1) & 1), a.err);
+        const int st = c % kInterStages;
+        const unsigned char* B = sm.blk[st];
+        const bool got = mbar_wait_bounded(&sm.bar_ld[st], (uint32_t)((c / kInterStages) & 1), a.err);
         if (__syncthreads_or(!got)) { failed = true; break; }
-        unsigned char* B = sm.blk[st];
-        // MMA-1: [O1^T | X^T] = S^T (Q e^G | W)^T
-        if (tid == 0) {
-            mma3_ts(tbase + kTD1, tbase + kTA1, tbase + kTA1 + 64,
-                    tc_smem_desc(smem_u32(B + kOffQW), 128, kSbo128),
-                    tc_smem_desc(smem_u32(B + kOffQW + kQWBytes), 128, kSbo128), 8, id1);
-            tc_commit(&sm.bar_mma);
+        if (ostore_lane && c > 0) {      // the previous chunk's o tile is complete (barrier above)
+            flush_o(c - 1);
+            bulk_wait_read1();           // the tile written next iteration is free again
         }
         bool ok = mbar_wait_bounded(&sm.bar_mma, mph, a.err);
         if (ok) mph ^= 1u;
         tc_fence_after();
         if (__syncthreads_or(!ok)) { failed = true; break; }
-        float o1[kCc];
+        // O1 and X for tokens 16 hf ..; U' = U - X into TMEM as MMA-2's A operand
+        float o1[16];
         {
-            float x[kCc];
-            tmem_ld16(tlane + kTD1, *reinterpret_cast<float(*)[16]>(&o1[0]));
-            tmem_ld16(tlane + kTD1 + 16, *reinterpret_cast<float(*)[16]>(&o1[16]));
-            tmem_ld16(tlane + kTD1 + 32, *reinterpret_cast<float(*)[16]>(&x[0]));
-            tmem_ld16(tlane + kTD1 + 48, *reinterpret_cast<float(*)[16]>(&x[16]));
+            float x[16];
+            tmem_ld16(tl + kTD1 + 16 * hf, o1);
+            tmem_ld16(tl + kTD1 + 32 + 16 * hf, x);
             tmem_ld_wait();
-            const float* ut = reinterpret_cast<const float*>(B + kOffUT) + tid;
-            float up[kCc];
+            const float* ut = reinterpret_cast<const float*>(B + kOffUT) + (16 * hf) * 128 + v;
+            float up[16];
 #pragma unroll
-            for (int t = 0; t < kCc; ++t) up[t] = ut[t * 128] - x[t];
-            tmem_put_split<kCc>(tlane + kTA2, tlane + kTA2 + 16, up);
+            for (int t = 0; t < 16; ++t) up[t] = ut[t * 128] - x[t];
+            tmem_put_split16(tl + kTA2 + 8 * hf, tl + kTA2 + 16 + 8 * hf, up);
             tmem_st_wait();
         }
         tc_fence_before();
@@ -656,39 +709,56 @@ kda_chunk_inter_kernel(ScanArgs a, const int* chunk_off, const unsigned char* ws
         if (ok) mph ^= 1u;
         tc_fence_after();
         if (__syncthreads_or(!ok)) { failed = true; break; }
+        float o2[16];
         {
-            const float* eg = reinterpret_cast<const float*>(B + kOffEG);
+            const float4* eg4 = reinterpret_cast<const float4*>(B + kOffEG) + 16 * hf;
 #pragma unroll
-            for (int q16 = 0; q16 < 8; ++q16) {
-                float d[16];
-                tmem_ld16(tlane + kTD2 + 16 * q16, d);
+            for (int half = 0; half < 2; ++half) {
+                float d[32];
+                tmem_ld16(tl + kTD2 + 64 * hf + 32 * half, *reinterpret_cast<float(*)[16]>(&d[0]));
+                tmem_ld16(tl + kTD2 + 64 * hf + 32 * half + 16, *reinterpret_cast<float(*)[16]>(&d[16]));
+                if (half == 1) tmem_ld16(tl + kTD2 + 128 + 16 * hf, o2);
                 tmem_ld_wait();
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const int kk = 16 * q16 + e;
-                    srow[kk] = fmaf(srow[kk], eg[kk], d[e]);
+                for (int q = 0; q < 8; ++q) {
+                    const float4 e4 = eg4[8 * half + q];
+                    const int kk = 32 * half + 4 * q;
+                    srow[kk] = fmaf(srow[kk], e4.x, d[4 * q]);
+                    srow[kk + 1] = fmaf(srow[kk + 1], e4.y, d[4 * q + 1]);
+                    srow[kk + 2] = fmaf(srow[kk + 2], e4.z, d[4 * q + 2]);
+                    srow[kk + 3] = fmaf(srow[kk + 3], e4.w, d[4 * q + 3]);
                 }
             }
-            float o2[kCc];
-            tmem_ld16(tlane + kTD2 + 128, *reinterpret_cast<float(*)[16]>(&o2[0]));
-            tmem_ld16(tlane + kTD2 + 144, *reinterpret_cast<float(*)[16]>(&o2[16]));
-            tmem_ld_wait();
-            float* orow = a.o + row0 * C + h * kHeadDim + tid;
-#pragma unroll
-            for (int t = 0; t < kCc; ++t)
-                if (t < nt) orow[(long)t * C] = __fmul_rn(a.scale, o1[t] + o2[t]);
-            tmem_put_split<128>(tlane + kTA1, tlane + kTA1 + 64, srow);
+            tmem_put_split<64>(tl + kTA1 + 32 * hf, tl + kTA1 + 64 + 32 * hf, srow);
             tmem_st_wait();
         }
         tc_fence_before();
-        __syncthreads();   // this stage's block is consumed; S^T is in place for the next MMA-1
+        __syncthreads();   // block st consumed; S^T in place for the next MMA-1
         tc_fence_after();
-        if (tid == 0 && c + 2 < nch) issue(c + 2, st);
+        if (tid == 0 && c + 1 < nch) {
+            const int s1 = (c + 1) % kInterStages;
+            if (mbar_wait_bounded(&sm.bar_ld[s1], (uint32_t)(((c + 1) / kInterStages) & 1), a.err)) {
+                tc_fence_after();
+                mma1(s1);
+            }
+        }
+        if (tid == 32 && c + kInterStages < nch) issue(c + kInterStages, st);
+        // the chunk's o rows into the staging tile while the next MMA-1 runs
+        float* ot = &sm.otile[c & 1][16 * hf][v];
+#pragma unroll
+        for (int t = 0; t < 16; ++t) ot[t * 128] = __fmul_rn(scale, o1[t] + o2[t]);
+        fence_proxy_async_smem();
+    }
+    __syncthreads();
+    if (ostore_lane) {
+        if (!failed && nch > 0) flush_o(nch - 1);
+        bulk_wait_all();
     }
     if (!failed) {
-        float4* sout = reinterpret_cast<float4*>(a.state_out + (((long)n * H + h) * kHeadDim + tid) * kHeadDim);
+        float4* sout = reinterpret_cast<float4*>(
+            a.state_out + (((long)n * H + h) * kHeadDim + v) * kHeadDim + 64 * hf);
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
+        for (int j = 0; j < 16; ++j)
             __stcs(sout + j, make_float4(srow[4 * j], srow[4 * j + 1], srow[4 * j + 2], srow[4 * j + 3]));
     } else {
         mbar_wait_bounded(&sm.bar_mma, mph, nullptr);   // let in-flight MMAs drain (bounded)
@@ -751,12 +821,15 @@ static cudaError_t launch_chunk_t(const ScanArgs& a, const int* cu_host, void* w
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    const size_t smem2 = sizeof(InterSmem) + 1024;
+    const size_t smem2 = sizeof(InterSmem) + 128;
     static int done2[64] = {0};
     cudaError_t e = set_smem(kda_chunk_inter_kernel<GM>, smem2, done2);
     if (e != cudaSuccess) return e;
     dim3 g2((unsigned)a.H, (unsigned)a.seq.N);
-    kda_chunk_inter_kernel<GM><<<g2, kThr, smem2, s>>>(a, chunk_off, ws);
+    CUtensorMap tmo;
+    if (!make_tensor_map_2d(&tmo, a.o, a.seq.total_rows, (long)a.H * kHeadDim, kHeadDim, kCc))
+        return cudaErrorInvalidValue;
+    kda_chunk_inter_kernel<GM><<<g2, kThrInter, smem2, s>>>(a, chunk_off, ws, tmo);
     return cudaGetLastError();
 }
 
