@@ -10,7 +10,10 @@ Printed JSON line (rank 0):
   value       prefill tokens/s, all ranks, inputs resident in HBM, CUDA events
   e2e         the same through the public API with inputs copied from pinned host memory and the
               result (y, final state, ring) read back every step
-  roofline    the scan kernel (dominant) against the FP32-pipe peak (bound "alu")
+  roofline    the step's dominant kernel (by device time, from the library's per-kernel CUDA-event
+              timer over the timed region) against measured HBM bandwidth, with its
+              algorithmic bytes per launch; "kernels" lists every kernel the same way.  With
+              --scan-algo seq (the staged sequential path) the scan against the FP32-pipe peak.
   decode      decode state GB/s, total GB/s and its roofline against measured HBM bandwidth
   cpu_baseline  the f64 oracle on a bounded sample of the prefill workload, host cores
 --impl reference times that oracle alone as the reference arm.
@@ -143,8 +146,30 @@ def _traffic(kernel, files):
     return d.get("dram_bytes_per_launch")
 
 
+def _kernel_bytes(T, H, blk_bytes, chunks):
+    """Algorithmic HBM bytes per launch of each kernel of the prefill step (T tokens, H heads, one
+    sequence, conv K=4, bf16 raw q/k/v): what the kernel must read and write, once each."""
+    C = H * D
+    f32, bf16 = 4, 2
+    plane = T * C * f32
+    ws = chunks * H * blk_bytes
+    return {
+        # raw q, k, v (bf16), gate input, beta input, conv weights + ring -> q, k, v, g, beta
+        "kda_prep_kernel": 3 * T * C * bf16 + plane + T * H * f32 + 3 * C * 4 * f32
+                           + 3 * C * 3 * f32 + 4 * plane + T * H * f32,
+        "kda_ring_roll_kernel": 3 * C * 3 * (bf16 + f32),
+        # q, k, v, g, beta -> the workspace of operand images
+        "kda_chunk_intra_kernel": 4 * plane + T * H * f32 + ws,
+        # workspace + state in -> o + state out
+        "kda_chunk_inter_kernel": ws + 2 * H * D * D * f32 + plane,
+        "kda_chunk_offsets_kernel": 0,
+        # o + RMSNorm gate + weight -> y
+        "kda_gated_rmsnorm_kernel": 3 * plane + D * f32,
+    }
+
+
 def _prefill_e2e(args, d, buf, state_out, ring_out, stream, barrier, max_over_ranks, mixer,
-                 algo, ws, T, H, C, workspace):
+                 algo, ws, T, H, C, workspace, fused):
     """Prefill through the public API with inputs copied from pinned host memory and y, the final
     state and the ring read back every step."""
     import torch
@@ -160,8 +185,12 @@ def _prefill_e2e(args, d, buf, state_out, ring_out, stream, barrier, max_over_ra
     def e2e_step():
         for k, v in host.items():
             dev_in[k].copy_(v, non_blocking=True)
-        out = mixer.kda_forward(H=H, N=1, T=T, algo=algo, out=buf, state_out=state_out,
-                                ring_out=ring_out, workspace=workspace, **dev_in)
+        if fused:
+            out = mixer.kda_prefill(H=H, N=1, T=T, state_out=state_out, ring_out=ring_out,
+                                    y=buf["y"], workspace=workspace, **dev_in)
+        else:
+            out = mixer.kda_forward(H=H, N=1, T=T, algo=algo, out=buf, state_out=state_out,
+                                    ring_out=ring_out, workspace=workspace, **dev_in)
         y_host.copy_(out["y"], non_blocking=True)
         st_host.copy_(out["state_out"], non_blocking=True)
         ring_host.copy_(out["ring_out"], non_blocking=True)
@@ -222,13 +251,25 @@ def run_ours(args):
     state_out = torch.empty_like(d["state_in"])
     ring_out = torch.empty_like(d["ring_in"])
     algo = {"auto": kda.ALGO_AUTO, "seq": kda.ALGO_SEQ, "chunk": kda.ALGO_CHUNK}[args.scan_algo]
+    # auto / chunk: one kda_prefill_fused call per step (prep, chunked scan with the RMSNorm
+    # epilogue); seq: the staged calls with the sequential scan
+    fused = algo != kda.ALGO_SEQ
     # the sequential form consumes decay factors, the chunked form log-decays
     gate_mode = kda.GATE_PER_CHANNEL | (kda.GATE_EXP if algo == kda.ALGO_SEQ else 0)
-    workspace = kda.scan_workspace(1, T, H, dev, algo)   # scratch of the chunked form
-
-    ev = {}
+    if fused:
+        workspace = kda.prefill_workspace(1, T, H, dev)
+    else:
+        workspace = kda.scan_workspace(1, T, H, dev, algo)
+    chunks = (T + 31) // 32
+    blk_bytes = (kda.kda_scan_workspace_bytes(1, T, H, algo=kda.ALGO_CHUNK) - 256) // ((chunks + 1) * H)
 
     def prefill_step(timed_scan=None):
+        if fused:
+            kda.kda_prefill_fused(d["q_raw"], d["k_raw"], d["v_raw"], d["conv_w"], d["ring_in"],
+                                  ring_out, d["f_raw"], d["dt_bias"], d["a_log"], d["beta_raw"],
+                                  d["state_in"], state_out, d["norm_w"], d["gate_raw"], buf["y"],
+                                  workspace, N=1, T=T, H=H)
+            return
         kda.kda_conv_l2norm_prep(d["q_raw"], d["k_raw"], d["v_raw"], d["conv_w"], d["ring_in"],
                                  ring_out, d["f_raw"], d["dt_bias"], d["a_log"], d["beta_raw"],
                                  buf["q_hat"], buf["k_hat"], buf["v_hat"], buf["g"],
@@ -242,10 +283,11 @@ def run_ours(args):
             timed_scan[1].record(stream)
         kda.kda_gated_rmsnorm_out(buf["o"], d["norm_w"], d["gate_raw"], buf["y"], rows=T * H)
 
-    launches_per_step = 4  # prep, ring roll, scan, gated RMSNorm
+    kda.kernel_timing(True)     # CUDA events around every library launch
     for _ in range(args.warmup):
         prefill_step()
     barrier()
+    kda.kernel_times()          # drop the warm-up launches
     K = args.steps
     scan_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(K)]
@@ -254,14 +296,20 @@ def run_ours(args):
         barrier()
         t0.record(stream)
         for i in range(K):
-            prefill_step(scan_ev[i])
+            prefill_step(None if fused else scan_ev[i])
         t1.record(stream)
         barrier()
     clocks = clk.summary()
+    ktimes = kda.kernel_times()
+    kda.kernel_timing(False)
     ms = max_over_ranks(t0.elapsed_time(t1))
     ms_step = ms / K
     tokens_per_s = ws * T / (ms_step / 1e3)
-    scan_ms = statistics.mean(a.elapsed_time(b) for a, b in scan_ev)
+    if fused:
+        scan_ms = sum(ktimes[k][1] for k in ("kda_chunk_intra_kernel", "kda_chunk_inter_kernel",
+                                             "kda_chunk_offsets_kernel") if k in ktimes) / K
+    else:
+        scan_ms = statistics.mean(a.elapsed_time(b) for a, b in scan_ev)
     scan_flop = FLOP_PER_TOKEN_HEAD * T * H
     fp32_peak = _fp32_peak_tflops(peaks["sm_max_mhz"])
     scan_tflops = scan_flop / (scan_ms / 1e3) / 1e12
@@ -271,7 +319,7 @@ def run_ours(args):
     e2e = None
     if not args.skip_e2e:
         e2e = _prefill_e2e(args, d, buf, state_out, ring_out, stream, barrier, max_over_ranks,
-                           mixer, algo, ws, T, H, C, workspace)
+                           mixer, algo, ws, T, H, C, workspace, fused)
 
     # ---------------- decode step (fused kernel) ----------------
     dec = inputs.decode_step(N=DEC_N, T=1, H=DEC_H)
@@ -312,24 +360,54 @@ def run_ours(args):
         return None
 
     cpu = None if args.skip_cpu else cpu_baseline(pre, args.cpu_sample_heads)
+    kbytes = _kernel_bytes(T, H, blk_bytes, chunks)
+    total_kms = sum(v[1] for v in ktimes.values())
+    kernels = []
+    for name, (n, kms) in sorted(ktimes.items(), key=lambda kv: -kv[1][1]):
+        per = kms / n
+        b = kbytes.get(name)
+        ent = {"kernel": name, "launches": n, "ms_per_launch": per, "share": kms / total_kms}
+        if b:
+            gbs = b / (per / 1e3) / 1e9
+            ent.update(bytes_per_launch=b, gbs=gbs, frac_hbm=gbs / peaks["hbm_gbs"])
+        kernels.append(ent)
+    if fused:
+        top = kernels[0]
+        src_files = {"kda_chunk_intra_kernel": ["kda_scan_chunk.cu", "kda_tc.cuh", "kda_device.cuh"],
+                     "kda_gated_rmsnorm_kernel": ["kda_epilogue.cu", "kda_device.cuh"],
+                     "kda_chunk_inter_kernel": ["kda_scan_chunk.cu", "kda_tc.cuh", "kda_device.cuh"],
+                     "kda_prep_kernel": ["kda_prep.cu", "kda_device.cuh"]}
+        roofline = {"bound": "hbm", "kernel": top["kernel"], "achieved": top.get("gbs"),
+                    "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": top.get("frac_hbm"),
+                    "traffic": _traffic(top["kernel"], src_files.get(top["kernel"], [])),
+                    "bytes_per_launch": top.get("bytes_per_launch"),
+                    "ms_per_launch": top["ms_per_launch"],
+                    "peak_src": f"{peaks['src']} hbm_gbs (copy bandwidth)",
+                    "timing": "library CUDA-event timer around each launch, timed region"}
+    else:
+        roofline = {"bound": "alu", "kernel": "kda_scan_seq_kernel", "achieved": scan_tflops,
+                    "peak": fp32_peak, "unit": "TFLOP/s", "frac": scan_tflops / fp32_peak,
+                    "traffic": _traffic("kda_scan_seq_kernel",
+                                        ["kda_scan_seq.cu", "kda_device.cuh"]),
+                    "ms_per_launch": scan_ms, "flop_per_launch": scan_flop,
+                    "peak_src": f"152 SMs x 128 FP32 lanes x 2 x {peaks['sm_max_mhz']:.0f} MHz"}
     return {
         "metric": METRIC, "value": tokens_per_s, "unit": "tokens/s", "n_gpus": ws,
         "steps": K, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded numpy default_rng; bf16 raw q/k/v, f32 gates, state, norm)",
         "config": {"workload": "prefill: 1 sequence x 4096 tokens, H=64, head_dim=128, conv K=4,"
-                               " zero state and ring, full fused path",
+                               " zero state and ring, whole mixer per step",
+                   "path": "kda_prefill_fused (prep, chunked scan, gated RMSNorm)" if fused
+                           else "staged calls, sequential scan",
                    "global_batch": ws, "seq_len": T, "heads": H, "head_dim": D,
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
                    "scan_algo": args.scan_algo,
                    "l2": "inputs larger than L2 (470 MB read per step)"},
-        "gpu_launches": launches_per_step * K,
-        "roofline": {"bound": "alu", "kernel": "kda_scan_seq_kernel", "achieved": scan_tflops,
-                     "peak": fp32_peak, "unit": "TFLOP/s", "frac": scan_tflops / fp32_peak,
-                     "traffic": _traffic("kda_scan_seq_kernel",
-                                         ["kda_scan_seq.cu", "kda_device.cuh"]),
-                     "ms_per_launch": scan_ms, "flop_per_launch": scan_flop,
-                     "peak_src": f"152 SMs x 128 FP32 lanes x 2 x {peaks['sm_max_mhz']:.0f} MHz"},
+        "gpu_launches": sum(v[0] for v in ktimes.values()),
+        "roofline": roofline,
+        "kernels": kernels,
+        "scan_ms_per_step": scan_ms,
         "e2e": e2e,
         "decode": {"workload": "64 sequences x 1 token, H=64, fused decode kernel, states "
                                "ping-ponged (512 MiB working set)",

@@ -134,6 +134,64 @@ int scan_impl(const float* q, const float* k, const float* v, const float* g, in
                              : launch_scan_seq(a, static_cast<cudaStream_t>(stream)));
 }
 
+// Byte offsets of the pieces of kda_prefill_fused's workspace: the prep outputs (q, k, v, g,
+// beta), the scan's readout o, then the chunked scan's scratch.
+struct PrefillLayout {
+    size_t q, k, v, g, beta, o, chunk;
+};
+
+inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+PrefillLayout prefill_layout(long rows, int H, int gate_mode) {
+    const size_t plane = align256((size_t)rows * H * kHeadDim * sizeof(float));
+    const size_t gsz = (gate_mode & KDA_GATE_PER_HEAD) ? (size_t)rows * H * sizeof(float) : plane;
+    PrefillLayout L;
+    L.q = 0; L.k = plane; L.v = 2 * plane; L.g = 3 * plane;
+    L.beta = L.g + align256(gsz);
+    L.o = L.beta + align256((size_t)rows * H * sizeof(float));
+    L.chunk = L.o + plane;
+    return L;
+}
+
+int prefill_impl(const void* q_raw, const void* k_raw, const void* v_raw, int raw_dtype,
+                 const float* conv_w, const float* ring_in, float* ring_out, const float* f_raw,
+                 const float* dt_bias, const float* a_log, int gate_mode, float gate_lb,
+                 const float* beta_raw, const float* state_in, float* state_out,
+                 const float* norm_w, const float* gate_raw, float* y, const SeqLayout& seq,
+                 const int* cu_host, int H, int D, int K, float l2_eps, float scale,
+                 float norm_eps, void* workspace, size_t workspace_bytes, void* stream) {
+    if (D != kHeadDim) return KDA_ERR_HEAD_DIM;
+    if (seq.N < 0 || seq.N > kMaxGridY || seq.total_rows < 0 || H <= 0 || H > kMaxGridY)
+        return KDA_ERR_SHAPE;
+    if (seq.total_rows >= (1L << 31)) return KDA_ERR_SHAPE;
+    if (gate_mode != KDA_GATE_PER_CHANNEL && gate_mode != KDA_GATE_PER_HEAD) return KDA_ERR_ENUM;
+    if (seq.N == 0) return KDA_OK;
+    if (seq.total_rows > 0) {
+        if (!norm_w || !gate_raw || !y) return KDA_ERR_NULL;
+        if (!aligned16(norm_w) || !aligned16(gate_raw) || !aligned16(y)) return KDA_ERR_ALIGN;
+    }
+    const PrefillLayout L = prefill_layout(seq.total_rows, H, gate_mode);
+    const size_t need = L.chunk + chunk_workspace_bytes(seq, cu_host, H);
+    if (workspace == nullptr || workspace_bytes < need) return KDA_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return KDA_ERR_ALIGN;
+    unsigned char* w = static_cast<unsigned char*>(workspace);
+    float* qh = reinterpret_cast<float*>(w + L.q);
+    float* kh = reinterpret_cast<float*>(w + L.k);
+    float* vh = reinterpret_cast<float*>(w + L.v);
+    float* gh = reinterpret_cast<float*>(w + L.g);
+    float* bh = reinterpret_cast<float*>(w + L.beta);
+    float* oh = reinterpret_cast<float*>(w + L.o);
+    int rc = prep_impl(q_raw, k_raw, v_raw, raw_dtype, conv_w, ring_in, ring_out, f_raw, dt_bias,
+                       a_log, gate_mode, gate_lb, beta_raw, qh, kh, vh, gh, bh, seq, H, D, K,
+                       l2_eps, stream);
+    if (rc != KDA_OK) return rc;
+    rc = scan_impl(qh, kh, vh, gh, gate_mode, bh, state_in, state_out, oh, seq, cu_host, H, D,
+                   scale, KDA_ALGO_CHUNK, w + L.chunk, workspace_bytes - L.chunk, stream);
+    if (rc != KDA_OK || seq.total_rows == 0) return rc;
+    NormArgs na{oh, norm_w, gate_raw, y, seq.total_rows * H, norm_eps};
+    return cuda_status(launch_gated_rmsnorm(na, static_cast<cudaStream_t>(stream)));
+}
+
 }  // namespace
 
 extern "C" {
@@ -204,6 +262,51 @@ size_t kda_scan_workspace_bytes(int N, int total_T, int H, int D, int gate_mode,
     const size_t chunks = (size_t)(total_T + kChunkTokens - 1) / kChunkTokens + (size_t)N;
     const size_t header = (((size_t)N + 1) * 4 + 255) / 256 * 256;
     return header + chunks * (size_t)H * kChunkBlockBytes;
+}
+
+size_t kda_prefill_workspace_bytes(int N, int total_T, int H, int D, int gate_mode) {
+    if (N < 0 || total_T < 0 || H <= 0 || D != kHeadDim) return 0;
+    if (gate_mode != KDA_GATE_PER_CHANNEL && gate_mode != KDA_GATE_PER_HEAD) return 0;
+    return prefill_layout(total_T, H, gate_mode).chunk +
+           kda_scan_workspace_bytes(N, total_T, H, D, gate_mode, KDA_ALGO_CHUNK);
+}
+
+int kda_prefill_fused(const void* q_raw, const void* k_raw, const void* v_raw, int raw_dtype,
+                      const float* conv_w, const float* ring_in, float* ring_out,
+                      const float* f_raw, const float* dt_bias, const float* a_log, int gate_mode,
+                      float gate_lb, const float* beta_raw, const float* state_in,
+                      float* state_out, const float* norm_w, const float* gate_raw, float* y,
+                      int N, int T, int H, int D, int K, float l2_eps, float scale,
+                      float rms_eps, void* workspace, size_t workspace_bytes, void* stream) {
+    if (N < 0 || T < 0) return KDA_ERR_SHAPE;
+    SeqLayout seq{nullptr, T, N, (long)N * T};
+    return prefill_impl(q_raw, k_raw, v_raw, raw_dtype, conv_w, ring_in, ring_out, f_raw, dt_bias,
+                        a_log, gate_mode, gate_lb, beta_raw, state_in, state_out, norm_w, gate_raw,
+                        y, seq, nullptr, H, D, K, l2_eps, scale, rms_eps, workspace,
+                        workspace_bytes, stream);
+}
+
+int kda_prefill_fused_varlen(const void* q_raw, const void* k_raw, const void* v_raw,
+                             int raw_dtype, const float* conv_w, const float* ring_in,
+                             float* ring_out, const float* f_raw, const float* dt_bias,
+                             const float* a_log, int gate_mode, float gate_lb,
+                             const float* beta_raw, const float* state_in, float* state_out,
+                             const float* norm_w, const float* gate_raw, float* y,
+                             const int* cu_seqlens, const int* cu_seqlens_host, int N,
+                             int total_T, int H, int D, int K, float l2_eps, float scale,
+                             float rms_eps, void* workspace, size_t workspace_bytes,
+                             void* stream) {
+    if (N < 0 || total_T < 0) return KDA_ERR_SHAPE;
+    if (N > 0) {
+        if (cu_seqlens == nullptr) return KDA_ERR_NULL;
+        const int rc = check_cu(cu_seqlens_host, N, total_T);
+        if (rc) return rc;
+    }
+    SeqLayout seq{cu_seqlens, 0, N, (long)total_T};
+    return prefill_impl(q_raw, k_raw, v_raw, raw_dtype, conv_w, ring_in, ring_out, f_raw, dt_bias,
+                        a_log, gate_mode, gate_lb, beta_raw, state_in, state_out, norm_w, gate_raw,
+                        y, seq, cu_seqlens_host, H, D, K, l2_eps, scale, rms_eps, workspace,
+                        workspace_bytes, stream);
 }
 
 int kda_scan(const float* q_hat, const float* k_hat, const float* v_hat, const float* g,

@@ -165,6 +165,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) kda_decode_fused_kernel(Decode
 template <bool BF16, int GM>
 static void launch_dec_t(const DecodeArgs& a, cudaStream_t s) {
     dim3 grid((unsigned)a.H, (unsigned)a.N);
+    KernelTimer kt(kKDecode, s);
     if (a.K <= 4) kda_decode_fused_kernel<BF16, GM, 4><<<grid, kDecThreads, 0, s>>>(a);
     else kda_decode_fused_kernel<BF16, GM, kMaxConvK><<<grid, kDecThreads, 0, s>>>(a);
 }

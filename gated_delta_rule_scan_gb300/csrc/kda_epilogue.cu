@@ -37,6 +37,7 @@ __global__ void __launch_bounds__(256) kda_gated_rmsnorm_kernel(NormArgs a) {
 cudaError_t launch_gated_rmsnorm(const NormArgs& a, cudaStream_t s) {
     if (a.rows == 0) return cudaSuccess;
     const long blocks = (a.rows + 7) / 8;
+    KernelTimer kt(kKRmsNorm, s);
     kda_gated_rmsnorm_kernel<<<(unsigned)blocks, 256, 0, s>>>(a);
     return cudaGetLastError();
 }

@@ -78,4 +78,20 @@ cudaError_t launch_decode_fused(const DecodeArgs& a, cudaStream_t s);
 
 constexpr int kDecodeMaxT = 16;   // tokens one fused decode/verify call may carry
 
+// ---- optional per-kernel timing (kda_timer.cu): a KernelTimer scoped around a launch records a
+// CUDA event before and after it on the launch stream while timing is enabled.
+enum KernelId {
+    kKPrep, kKRingRoll, kKScanSeq, kKChunkOffsets, kKChunkIntra, kKChunkInter, kKRmsNorm,
+    kKDecode, kKernelCount
+};
+class KernelTimer {
+public:
+    KernelTimer(int id, cudaStream_t s);
+    ~KernelTimer();
+    KernelTimer(const KernelTimer&) = delete;
+    KernelTimer& operator=(const KernelTimer&) = delete;
+private:
+    int id_; cudaStream_t s_; bool on_;
+};
+
 }  // namespace kda

@@ -256,6 +256,7 @@ static cudaError_t launch_prep_t(const PrepArgs& a, cudaStream_t s) {
     const long tiles = (a.seq.total_rows + (long)kRun * kPrepWarps - 1) / ((long)kRun * kPrepWarps);
     if (tiles > 0) {
         dim3 grid((unsigned)tiles, (unsigned)a.H);
+        KernelTimer kt(kKPrep, s);
         if (a.K <= 4) kda_prep_kernel<BF16, GM, CONV, EXP, 4><<<grid, kPrepThreads, 0, s>>>(a);
         else kda_prep_kernel<BF16, GM, CONV, EXP, kMaxConvK><<<grid, kPrepThreads, 0, s>>>(a);
         cudaError_t e = cudaGetLastError();
@@ -264,6 +265,7 @@ static cudaError_t launch_prep_t(const PrepArgs& a, cudaStream_t s) {
     if (CONV && a.seq.N > 0) {
         const long C3 = 3L * a.H * kHeadDim;
         dim3 grid((unsigned)((C3 + 255) / 256), (unsigned)a.seq.N);
+        KernelTimer kt(kKRingRoll, s);
         kda_ring_roll_kernel<BF16><<<grid, 256, 0, s>>>(a);
         return cudaGetLastError();
     }

@@ -292,13 +292,19 @@ kda_chunk_intra_kernel(ScanArgs a, const int* chunk_off, unsigned char* ws) {
     // ---- column images: channel tid, tokens 8j .. 8j+7 ----------------------------------------
     {
         const float GC = gc[kCc - 1];
+        float bv[kCc];                           // loaded before the image stores (see below)
+#pragma unroll
+        for (int q = 0; q < kCc / 4; ++q) {
+            const float4 b4 = *reinterpret_cast<const float4*>(&sm.beta[4 * q]);
+            bv[4 * q] = b4.x; bv[4 * q + 1] = b4.y; bv[4 * q + 2] = b4.z; bv[4 * q + 3] = b4.w;
+        }
 #pragma unroll
         for (int j = 0; j < kCc / 8; ++j) {
             float xt[8], xv[8], xc[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 const int t = 8 * j + e;
-                const float bt = sm.beta[t];
+                const float bt = bv[t];
                 xt[e] = bt * kc[t] * __expf(gc[t]);
                 xv[e] = bt * vc[t];
                 xc[e] = kc[t] * __expf(GC - gc[t]);
@@ -311,6 +317,23 @@ kda_chunk_intra_kernel(ScanArgs a, const int* chunk_off, unsigned char* ws) {
     if (GATE_MODE == 1) __syncthreads();          // gsc
 
     // ---- row images: token t = tr + 8j, channels k0 .. k0+7 -----------------------------------
+    // the shared-memory operands of all four items first (the image stores below are byte
+    // stores that could alias them, so loads after a store would wait for it)
+    float gtv[4][8], crv[8], ecv[8];
+    if (GATE_MODE == 0) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float4 a0 = *reinterpret_cast<const float4*>(&sm.scr[(tr + 8 * j) * 128 + k0]);
+            const float4 a1 = *reinterpret_cast<const float4*>(&sm.scr[(tr + 8 * j) * 128 + k0 + 4]);
+            gtv[j][0] = a0.x; gtv[j][1] = a0.y; gtv[j][2] = a0.z; gtv[j][3] = a0.w;
+            gtv[j][4] = a1.x; gtv[j][5] = a1.y; gtv[j][6] = a1.z; gtv[j][7] = a1.w;
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) { crv[e] = sm.cref[k0 + e]; ecv[e] = sm.ecr[k0 + e]; }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) gtv[j][0] = sm.gsc[tr + 8 * j];
+    }
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         const int t = tr + 8 * j;
@@ -322,15 +345,15 @@ kda_chunk_intra_kernel(ScanArgs a, const int* chunk_off, unsigned char* ws) {
         if (GATE_MODE == 0) {
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-                const float gt = sm.scr[t * 128 + k0 + e], cr = sm.cref[k0 + e];
+                const float gt = gtv[j][e], cr = crv[e];
                 const float ef = __expf(gt - cr), eb = __expf(cr - gt);
                 xb[e] = kv[e] * eb;
                 xk[e] = kv[e] * ef;
                 xq[e] = qv[e] * ef;
-                xg[e] = qv[e] * (ef * sm.ecr[k0 + e]);
+                xg[e] = qv[e] * (ef * ecv[e]);
             }
         } else {
-            const float eg = __expf(sm.gsc[t]);
+            const float eg = __expf(gtv[j][0]);
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 xb[e] = kv[e];
@@ -511,7 +534,7 @@ constexpr int kInterStages = 2;                  // workspace blocks in flight p
 
 struct __align__(128) InterSmem {
     unsigned char blk[kInterStages][kBlkBytes];
-    float otile[2][kCc][128];                    // a chunk's o rows on their way to global memory
+    float otile[2][kCc][128];                    // a chunk's o rows on their way out
     uint64_t bar_ld[kInterStages];
     uint64_t bar_mma;                            // MMA-1, then MMA-2
     uint32_t tmem_base;
@@ -681,13 +704,17 @@ kda_chunk_inter_kernel(ScanArgs a, const int* chunk_off, const unsigned char* ws
         if (ok) mph ^= 1u;
         tc_fence_after();
         if (__syncthreads_or(!ok)) { failed = true; break; }
-        // O1 and X for tokens 16 hf ..; U' = U - X into TMEM as MMA-2's A operand
-        float o1[16];
+        // O1 and X for tokens 16 hf ..; O1 waits in the output tile (its buffer's previous bulk
+        // store has been read: warp 2 waited for it before the barrier above); U' = U - X into
+        // TMEM as MMA-2's A operand
+        float* ot = &sm.otile[c & 1][16 * hf][v];
         {
-            float x[16];
+            float x[16], o1[16];
             tmem_ld16(tl + kTD1 + 16 * hf, o1);
             tmem_ld16(tl + kTD1 + 32 + 16 * hf, x);
             tmem_ld_wait();
+#pragma unroll
+            for (int t = 0; t < 16; ++t) ot[t * 128] = o1[t];
             const float* ut = reinterpret_cast<const float*>(B + kOffUT) + (16 * hf) * 128 + v;
             float up[16];
 #pragma unroll
@@ -744,9 +771,11 @@ kda_chunk_inter_kernel(ScanArgs a, const int* chunk_off, const unsigned char* ws
         }
         if (tid == 32 && c + kInterStages < nch) issue(c + kInterStages, st);
         // the chunk's o rows into the staging tile while the next MMA-1 runs
-        float* ot = &sm.otile[c & 1][16 * hf][v];
+        float ov[16];
 #pragma unroll
-        for (int t = 0; t < 16; ++t) ot[t * 128] = __fmul_rn(scale, o1[t] + o2[t]);
+        for (int t = 0; t < 16; ++t) ov[t] = __fmul_rn(scale, ot[t * 128] + o2[t]);
+#pragma unroll
+        for (int t = 0; t < 16; ++t) ot[t * 128] = ov[t];
         fence_proxy_async_smem();
     }
     __syncthreads();
@@ -807,6 +836,7 @@ static cudaError_t launch_chunk_t(const ScanArgs& a, const int* cu_host, void* w
     if (a.seq.cu_seqlens != nullptr) {
         chunk_off = reinterpret_cast<int*>(ws);
         ws += ((size_t)(a.seq.N + 1) * 4 + kHeaderAlign - 1) / kHeaderAlign * kHeaderAlign;
+        KernelTimer kt(kKChunkOffsets, s);
         kda_chunk_offsets_kernel<<<1, 1024, 0, s>>>(a.seq.cu_seqlens, a.seq.N, chunk_off);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
@@ -817,6 +847,7 @@ static cudaError_t launch_chunk_t(const ScanArgs& a, const int* cu_host, void* w
         cudaError_t e = set_smem(kda_chunk_intra_kernel<GM, EXP>, smem1, done1);
         if (e != cudaSuccess) return e;
         dim3 g1((unsigned)nchunks, (unsigned)a.H);
+        KernelTimer kt(kKChunkIntra, s);
         kda_chunk_intra_kernel<GM, EXP><<<g1, kThr, smem1, s>>>(a, chunk_off, ws);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
@@ -829,6 +860,7 @@ static cudaError_t launch_chunk_t(const ScanArgs& a, const int* cu_host, void* w
     CUtensorMap tmo;
     if (!make_tensor_map_2d(&tmo, a.o, a.seq.total_rows, (long)a.H * kHeadDim, kHeadDim, kCc))
         return cudaErrorInvalidValue;
+    KernelTimer kt(kKChunkInter, s);
     kda_chunk_inter_kernel<GM><<<g2, kThrInter, smem2, s>>>(a, chunk_off, ws, tmo);
     return cudaGetLastError();
 }

@@ -218,6 +218,7 @@ static cudaError_t launch_t(const ScanArgs& a, cudaStream_t s) {
         if (dev >= 0 && dev < 64) attr_done[dev] = 1;
     }
     dim3 grid((unsigned)(a.H * kColBlocks), (unsigned)a.seq.N);
+    KernelTimer kt(kKScanSeq, s);
     kda_scan_seq_kernel<GM, EXP><<<grid, kScanThreads, smem, s>>>(a, tq, tk, tg, tv);
     return cudaGetLastError();
 }

@@ -56,6 +56,21 @@ _lib.kda_scan_varlen_static.argtypes = [_P, _P, _P, _P, _I, _P, _P, _P, _P, _P, 
                                         _I, _F, _P]
 _lib.kda_gated_rmsnorm_out.argtypes = [_P, _P, _P, _P, _L, _I, _F, _P]
 _lib.kda_decode_fused.restype = _I
+_lib.kda_prefill_workspace_bytes.restype = _Z
+_lib.kda_prefill_workspace_bytes.argtypes = [_I, _I, _I, _I, _I]
+_lib.kda_prefill_fused.restype = _I
+_lib.kda_prefill_fused.argtypes = [_P, _P, _P, _I, _P, _P, _P, _P, _P, _P, _I, _F, _P, _P, _P, _P,
+                                   _P, _P, _I, _I, _I, _I, _I, _F, _F, _F, _P, _Z, _P]
+_lib.kda_prefill_fused_varlen.restype = _I
+_lib.kda_prefill_fused_varlen.argtypes = [_P, _P, _P, _I, _P, _P, _P, _P, _P, _P, _I, _F, _P, _P,
+                                          _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _F, _F,
+                                          _P, _Z, _P]
+_lib.kda_kernel_timing.restype = _I
+_lib.kda_kernel_timing.argtypes = [_I]
+_lib.kda_kernel_times.restype = _I
+_lib.kda_kernel_times.argtypes = [_I, _P, _P]
+_lib.kda_kernel_name.restype = ctypes.c_char_p
+_lib.kda_kernel_name.argtypes = [_I]
 _lib.kda_decode_fused.argtypes = [_P, _P, _P, _I, _P, _P, _P, _P, _P, _P, _I, _F, _P, _P, _P, _P,
                                   _P, _P, _I, _I, _I, _I, _I, _F, _F, _F, _P]
 _lib.kda_device_status.restype = _I
@@ -65,7 +80,9 @@ _lib.kda_device_status.argtypes = [_P]
 EXPORTED = ("kda_abi_version", "kda_status_string", "kda_conv_l2norm_prep",
             "kda_conv_l2norm_prep_varlen", "kda_scan_workspace_bytes", "kda_scan",
             "kda_scan_varlen", "kda_gated_rmsnorm_out", "kda_decode_fused", "kda_device_status",
-            "kda_scan_varlen_static")
+            "kda_scan_varlen_static", "kda_prefill_workspace_bytes", "kda_prefill_fused",
+            "kda_prefill_fused_varlen", "kda_kernel_timing", "kda_kernel_times",
+            "kda_kernel_name")
 
 
 class KdaError(RuntimeError):
@@ -205,6 +222,71 @@ def kda_decode_fused(q_raw, k_raw, v_raw, conv_w, ring_in, ring_out, f_raw, dt_b
         _ptr(ring_out), _ptr(f_raw), _ptr(dt_bias), _ptr(a_log), gate_mode, gate_lb,
         _ptr(beta_raw), _ptr(state_in), _ptr(state_out), _ptr(norm_w), _ptr(gate_raw), _ptr(y),
         N, T, H, D, K, l2_eps, scale, rms_eps, st))
+
+
+def kda_prefill_workspace_bytes(N, total_T, H, gate_mode=0, D=HEAD_DIM) -> int:
+    return int(_lib.kda_prefill_workspace_bytes(N, total_T, H, D, gate_mode))
+
+
+def prefill_workspace(N, total_T, H, device, gate_mode=0):
+    """A device byte buffer large enough for kda_prefill_fused / kda_prefill_fused_varlen."""
+    nbytes = kda_prefill_workspace_bytes(N, total_T, H, gate_mode)
+    return torch.empty(max(nbytes, 16), dtype=torch.uint8, device=device)
+
+
+def _ws_bytes(workspace):
+    return 0 if workspace is None else workspace.numel() * workspace.element_size()
+
+
+def kda_prefill_fused(q_raw, k_raw, v_raw, conv_w, ring_in, ring_out, f_raw, dt_bias, a_log,
+                      beta_raw, state_in, state_out, norm_w, gate_raw, y, workspace, *, N, T, H,
+                      K=4, gate_mode=0, gate_lb=-5.0, l2_eps=1e-6, scale=None, rms_eps=1e-6,
+                      D=HEAD_DIM, stream=None):
+    scale = D ** -0.5 if scale is None else scale
+    st = _stream(stream, y)
+    _check("kda_prefill_fused", _lib.kda_prefill_fused(
+        _ptr(q_raw), _ptr(k_raw), _ptr(v_raw), _raw_dtype(q_raw), _ptr(conv_w), _ptr(ring_in),
+        _ptr(ring_out), _ptr(f_raw), _ptr(dt_bias), _ptr(a_log), gate_mode, gate_lb,
+        _ptr(beta_raw), _ptr(state_in), _ptr(state_out), _ptr(norm_w), _ptr(gate_raw), _ptr(y),
+        N, T, H, D, K, l2_eps, scale, rms_eps, _ptr(workspace), _ws_bytes(workspace), st))
+
+
+def kda_prefill_fused_varlen(q_raw, k_raw, v_raw, conv_w, ring_in, ring_out, f_raw, dt_bias,
+                             a_log, beta_raw, state_in, state_out, norm_w, gate_raw, y,
+                             workspace, cu_seqlens, cu_seqlens_host, *, H, K=4, gate_mode=0,
+                             gate_lb=-5.0, l2_eps=1e-6, scale=None, rms_eps=1e-6, D=HEAD_DIM,
+                             stream=None):
+    N = cu_seqlens_host.numel() - 1
+    total = int(cu_seqlens_host[-1])
+    scale = D ** -0.5 if scale is None else scale
+    st = _stream(stream, y)
+    _check("kda_prefill_fused_varlen", _lib.kda_prefill_fused_varlen(
+        _ptr(q_raw), _ptr(k_raw), _ptr(v_raw), _raw_dtype(q_raw), _ptr(conv_w), _ptr(ring_in),
+        _ptr(ring_out), _ptr(f_raw), _ptr(dt_bias), _ptr(a_log), gate_mode, gate_lb,
+        _ptr(beta_raw), _ptr(state_in), _ptr(state_out), _ptr(norm_w), _ptr(gate_raw), _ptr(y),
+        _ptr(cu_seqlens), _ptr(cu_seqlens_host), N, total, H, D, K, l2_eps, scale, rms_eps,
+        _ptr(workspace), _ws_bytes(workspace), st))
+
+
+def kernel_timing(enable: bool) -> bool:
+    """Turn per-kernel event timing on (clearing the totals) or off; returns the old setting."""
+    return bool(_lib.kda_kernel_timing(1 if enable else 0))
+
+
+def kernel_times() -> dict:
+    """{kernel name: (launches, total ms)} since the last read, for kernels launched at least once
+    (waits for the recorded launches)."""
+    n = 16
+    launches = (ctypes.c_long * n)()
+    ms = (ctypes.c_double * n)()
+    k = _lib.kda_kernel_times(n, launches, ms)
+    if k < 0:
+        raise KdaError("kda_kernel_times", -k)
+    out = {}
+    for i in range(min(k, n)):
+        if launches[i]:
+            out[_lib.kda_kernel_name(i).decode()] = (int(launches[i]), float(ms[i]))
+    return out
 
 
 def kda_device_status(stream=None) -> int:

@@ -80,6 +80,40 @@ def kda_forward(*, q_raw, k_raw, v_raw, f_raw, dt_bias, a_log, beta_raw, state_i
                 state_out=state_out, ring_out=ring_out, n_seq=n_seq)
 
 
+def kda_prefill(*, q_raw, k_raw, v_raw, f_raw, dt_bias, a_log, beta_raw, state_in, H, conv_w,
+                ring_in, norm_w, gate_raw, cu_seqlens=None, cu_seqlens_host=None, N=None, T=None,
+                K=4, gate_mode=0, gate_lb=-5.0, l2_eps=1e-6, rms_eps=1e-6, scale=None,
+                state_out=None, ring_out=None, y=None, workspace=None, stream=None):
+    """The whole mixer for a prefill in one library call (kda_prefill_fused[_varlen]): conv +
+    SiLU, l2 norm, gates, the chunked scan and the gated RMSNorm, the intermediates kept in the
+    workspace.  Either (N, T) or cu_seqlens (int32 device) + cu_seqlens_host (int32
+    CPU).  workspace: from kda.prefill_workspace (allocated here when None).
+    Returns a dict with y, state_out and ring_out."""
+    C = H * kda.HEAD_DIM
+    rows = q_raw.shape[0]
+    varlen = cu_seqlens is not None
+    if not varlen:
+        assert N is not None and T is not None and N * T == rows
+    n_seq = (cu_seqlens_host.numel() - 1) if varlen else N
+    if y is None:
+        y = _empty((rows, C), q_raw)
+    if state_out is None:
+        state_out = torch.empty_like(state_in)
+    if ring_out is None and conv_w is not None:
+        ring_out = torch.empty_like(ring_in)
+    if workspace is None:
+        workspace = kda.prefill_workspace(n_seq, rows, H, q_raw.device, gate_mode)
+    args = (q_raw, k_raw, v_raw, conv_w, ring_in, ring_out, f_raw, dt_bias, a_log, beta_raw,
+            state_in, state_out, norm_w, gate_raw, y, workspace)
+    common = dict(H=H, K=K, gate_mode=gate_mode, gate_lb=gate_lb, l2_eps=l2_eps, scale=scale,
+                  rms_eps=rms_eps, stream=stream)
+    if varlen:
+        kda.kda_prefill_fused_varlen(*args, cu_seqlens, cu_seqlens_host, **common)
+    else:
+        kda.kda_prefill_fused(*args, N=N, T=T, **common)
+    return dict(y=y, state_out=state_out, ring_out=ring_out, n_seq=n_seq)
+
+
 def kda_decode(*, q_raw, k_raw, v_raw, conv_w, ring_in, f_raw, dt_bias, a_log, beta_raw,
                state_in, norm_w, gate_raw, N, T, H, K=4, gate_mode=0, gate_lb=-5.0,
                l2_eps=1e-6, rms_eps=1e-6, scale=None, state_out=None, ring_out=None, y=None,

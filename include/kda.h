@@ -222,6 +222,66 @@ int kda_gated_rmsnorm_out(const float* o, const float* norm_w, const float* gate
                           long rows, int D, float eps, void* stream);
 
 /*
+ * kda_prefill_workspace_bytes -- device scratch that suffices for kda_prefill_fused /
+ * kda_prefill_fused_varlen over N sequences holding total_T tokens in all: the intermediate
+ * q, k, v, gate, beta and readout planes (about 20 bytes per (token, channel)) plus the chunked
+ * scan's scratch (kda_scan_workspace_bytes with KDA_ALGO_CHUNK).  Returns 0 for invalid
+ * arguments.
+ */
+size_t kda_prefill_workspace_bytes(int N, int total_T, int H, int D, int gate_mode);
+
+/*
+ * kda_prefill_fused -- a prefill of N sequences of T tokens in one call: stages 2-6 of
+ * kda_core_gated (conv + SiLU, l2 norm, gates and beta, the chunked scan, gated RMSNorm), the
+ * same computation as kda_conv_l2norm_prep + kda_scan with KDA_ALGO_CHUNK +
+ * kda_gated_rmsnorm_out with the same arguments, the intermediates kept in the workspace.
+ * Arguments and layouts as in those three calls; gate_mode is KDA_GATE_PER_CHANNEL or
+ * KDA_GATE_PER_HEAD (the KDA_GATE_EXP flag is not accepted, 40007); norm_w [D] f32 [16B];
+ * gate_raw and y [N*T, C] f32 [16B].  The chunked form's range condition applies (every
+ * 32-token chunk's total log-decay above -170 per channel, else kda_device_status reports 40008).
+ * workspace   device scratch [16B] of at least kda_prefill_workspace_bytes(...) bytes (40009
+ *             otherwise); its contents are overwritten, so calls sharing it must not overlap.
+ * y, state_out and ring_out equal those of the three calls bit for bit.
+ */
+int kda_prefill_fused(const void* q_raw, const void* k_raw, const void* v_raw, int raw_dtype,
+                      const float* conv_w, const float* ring_in, float* ring_out,
+                      const float* f_raw, const float* dt_bias, const float* a_log, int gate_mode,
+                      float gate_lb, const float* beta_raw, const float* state_in,
+                      float* state_out, const float* norm_w, const float* gate_raw, float* y,
+                      int N, int T, int H, int D, int K, float l2_eps, float scale,
+                      float rms_eps, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * kda_prefill_fused_varlen -- kda_prefill_fused over N packed sequences (rows cu_seqlens[n] ..
+ * cu_seqlens[n+1]-1, state and ring row n); cu_seqlens / cu_seqlens_host as in
+ * kda_conv_l2norm_prep_varlen.
+ */
+int kda_prefill_fused_varlen(const void* q_raw, const void* k_raw, const void* v_raw,
+                             int raw_dtype, const float* conv_w, const float* ring_in,
+                             float* ring_out, const float* f_raw, const float* dt_bias,
+                             const float* a_log, int gate_mode, float gate_lb,
+                             const float* beta_raw, const float* state_in, float* state_out,
+                             const float* norm_w, const float* gate_raw, float* y,
+                             const int* cu_seqlens, const int* cu_seqlens_host, int N,
+                             int total_T, int H, int D, int K, float l2_eps, float scale,
+                             float rms_eps, void* workspace, size_t workspace_bytes,
+                             void* stream);
+
+/*
+ * Per-kernel timing (support, for measurement; not part of the method).
+ * kda_kernel_timing(1) makes every kernel launch of the library record a CUDA event before and
+ * after it on its stream, and clears the totals; kda_kernel_timing(0) stops.  Returns the previous
+ * setting.  Off by default, when it costs nothing measurable.
+ * kda_kernel_times waits for the recorded launches, writes for kernel ids 0 .. max_kernels-1 the
+ * number of launches and their summed device time in milliseconds since the last read (either
+ * array may be NULL), clears them, and returns the number of kernel ids, or -(10000 + cudaError_t)
+ * on a CUDA error.  kda_kernel_name(id) is that kernel's name, NULL outside the range.
+ */
+int kda_kernel_timing(int enable);
+int kda_kernel_times(int max_kernels, long* launches, double* total_ms);
+const char* kda_kernel_name(int id);
+
+/*
  * kda_decode_fused -- one decode step (T = 1) or a T-token speculative verify (2 <= T <= 16) of
  * N sequences in ONE launch: kda_conv_l2norm_prep + kda_scan + kda_gated_rmsnorm_out with the
  * same arguments, computed without round-tripping the intermediates through memory.  Its outputs

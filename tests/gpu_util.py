@@ -47,6 +47,23 @@ def gpu_forward(inp: KdaInputs, *, varlen=None, algo=0, **kw):
     return out
 
 
+def gpu_prefill(inp: KdaInputs, *, varlen=None, **kw):
+    """The fused prefill entry point (kda_prefill_fused[_varlen]) on the workload."""
+    from gated_delta_rule_scan_gb300 import mixer
+    d = to_dev(inp)
+    T = inp.uniform_T
+    if varlen is None:
+        varlen = T is None
+    if varlen:
+        cu_h = torch.from_numpy(inp.cu_seqlens.astype(np.int32))
+        extra = dict(cu_seqlens=cu_h.to("cuda"), cu_seqlens_host=cu_h)
+    else:
+        extra = dict(N=inp.N, T=T)
+    out = mixer.kda_prefill(H=inp.H, K=inp.K, gate_mode=inp.gate_mode, **d, **extra, **kw)
+    torch.cuda.synchronize()
+    return out
+
+
 def head_channels(heads, D=128):
     return np.concatenate([np.arange(h * D, (h + 1) * D) for h in heads])
 

@@ -126,3 +126,16 @@ def test_static_scan_contract(kda):
     assert call([0, 64], 1, D=64) == 40001
     assert call([0, 64], 0) == 40005
     assert kda.status_string(40011) != "unknown status"
+
+
+def test_kernel_timer_host(kda):
+    """The timing switch and the read work without a device: nothing pending reads as zeros."""
+    lib = kda.library()
+    assert kda.kernel_timing(True) in (False, True)
+    assert kda.kernel_times() == {}
+    assert kda.kernel_timing(False) is True
+    n = lib.kda_kernel_times(0, None, None)
+    assert n >= 8
+    names = [lib.kda_kernel_name(i).decode() for i in range(n)]
+    assert "kda_chunk_inter_kernel" in names and "kda_prep_kernel" in names
+    assert lib.kda_kernel_name(n) is None and lib.kda_kernel_name(-1) is None

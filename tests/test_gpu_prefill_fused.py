@@ -1,0 +1,140 @@
+"""GPU parity of the fused prefill (kda_prefill_fused[_varlen]): conv + SiLU, l2 norm, gates,
+chunked scan and gated RMSNorm in one call, with the readout fed straight into the norm.
+
+Against the f64 oracle: relative L-inf <= 1e-3 on y and the state, the ring bit-equal.  Against
+the stage-by-stage path with the chunked scan (the same kernels in the same order): y, state and
+ring bit-equal.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from gated_delta_rule_scan_gb300 import inputs
+from tests.gpu_util import TOL, gpu_forward, gpu_heads, gpu_prefill, oracle_forward, rel_linf
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+    yield
+    from gated_delta_rule_scan_gb300 import kda
+    assert kda.kda_device_status() == 0
+
+
+def _check(fused, inp, varlen=None, heads=None):
+    if heads is None:
+        ref = oracle_forward(inp)
+        got = fused
+    else:
+        ref = oracle_forward(inp, heads=heads)
+        got = gpu_heads(fused, inp, heads)
+    errs = {k: rel_linf(got[k], ref[k]) for k in ("y", "state_out")}
+    assert max(errs.values()) <= TOL, errs
+    if got.get("ring_out") is not None:
+        assert np.array_equal(got["ring_out"].cpu().double().numpy(), ref["ring_out"])
+    unf = gpu_forward(inp, varlen=varlen, algo=2)
+    assert torch.equal(fused["state_out"], unf["state_out"])
+    if fused.get("ring_out") is not None:
+        assert torch.equal(fused["ring_out"], unf["ring_out"])
+    assert torch.equal(fused["y"], unf["y"])
+
+
+@pytest.mark.parametrize("T", [1, 17, 32, 203])
+def test_prefill_fused_ragged(T):
+    """One chunk or less, exactly one chunk, and many chunks with a ragged tail; two sequences,
+    random state and ring (the uniform layout's ragged chunk is followed by the next sequence)."""
+    inp = inputs.make_inputs(60 + T, H=3, N=2, T=T, raw_dtype="bf16", conv=True, ring="randn",
+                             state="randn", epilogue=True)
+    _check(gpu_prefill(inp), inp)
+
+
+def test_prefill_fused_varlen_edges():
+    """Packed sequences with empty ones, lengths below the conv window and around the chunk."""
+    lengths = [5, 0, 1, 2, 3, 17, 0, 33, 64, 70]
+    inp = inputs.make_inputs(71, H=4, N=len(lengths), lengths=(0, 1), raw_dtype="bf16",
+                             conv=True, ring="randn", state="randn", epilogue=True)
+    cu = np.concatenate([[0], np.cumsum(lengths)])
+    rows = int(cu[-1])
+    rng = np.random.default_rng(1071)
+    C = inp.H * 128
+    for k in ("q_raw", "k_raw", "v_raw"):
+        setattr(inp, k, torch.from_numpy(rng.standard_normal((rows, C)).astype(np.float32))
+                .to(torch.bfloat16))
+    inp.f_raw = torch.from_numpy(rng.standard_normal((rows, C)).astype(np.float32))
+    inp.beta_raw = torch.from_numpy(rng.standard_normal((rows, inp.H)).astype(np.float32))
+    inp.gate_raw = torch.from_numpy(rng.standard_normal((rows, C)).astype(np.float32))
+    inp.cu_seqlens = cu
+    _check(gpu_prefill(inp, varlen=True), inp, varlen=True)
+
+
+def test_prefill_fused_gdn():
+    """The per-head (Gated DeltaNet) gate through the fused path."""
+    inp = inputs.make_inputs(72, H=4, N=1, T=300, raw_dtype="f32", conv=True, ring="randn",
+                             gate_mode=1, state="randn", epilogue=True)
+    _check(gpu_prefill(inp), inp)
+
+
+@pytest.mark.slow
+def test_prefill_fused_full_size():
+    """T=4096, H=64 (the prefill benchmark workload), sampled heads against the oracle."""
+    inp = inputs.prefill()
+    _check(gpu_prefill(inp), inp, heads=list(range(0, 64, 8)))
+
+
+@pytest.mark.slow
+def test_prefill_fused_varlen_full_size():
+    """16 sequences with lengths U[256, 8192] at H=64, sampled heads against the oracle."""
+    inp = inputs.varlen_prefill()
+    _check(gpu_prefill(inp, varlen=True), inp, varlen=True, heads=[0, 21, 42, 63])
+
+
+def test_prefill_fused_contract():
+    """Contract errors through the C ABI: the decay-factor flag, a short workspace, no output."""
+    from gated_delta_rule_scan_gb300 import kda
+    inp = inputs.make_inputs(73, H=2, N=1, T=40, raw_dtype="bf16", conv=True, ring="randn",
+                             state="randn", epilogue=True)
+    from tests.gpu_util import to_dev
+    d = to_dev(inp)
+    y = torch.empty(40, 256, device="cuda")
+    s_out = torch.empty_like(d["state_in"])
+    r_out = torch.empty_like(d["ring_in"])
+    ws = kda.prefill_workspace(1, 40, 2, "cuda")
+    args = [d["q_raw"], d["k_raw"], d["v_raw"], d["conv_w"], d["ring_in"], r_out, d["f_raw"],
+            d["dt_bias"], d["a_log"], d["beta_raw"], d["state_in"], s_out, d["norm_w"],
+            d["gate_raw"], y, ws]
+    with pytest.raises(kda.KdaError) as e:
+        kda.kda_prefill_fused(*args, N=1, T=40, H=2, gate_mode=kda.GATE_EXP)
+    assert e.value.status == 40007
+    short = args.copy()
+    short[-1] = ws[: ws.numel() // 4]   # the query is an upper bound: cut well below the need
+    with pytest.raises(kda.KdaError) as e:
+        kda.kda_prefill_fused(*short, N=1, T=40, H=2)
+    assert e.value.status == 40009
+    none_y = args.copy()
+    none_y[-2] = None
+    with pytest.raises(kda.KdaError) as e:
+        kda.kda_prefill_fused(*none_y, N=1, T=40, H=2)
+    assert e.value.status == 40004
+
+
+def test_kernel_timer_counts_fused_launches():
+    """With timing on, one fused prefill of two packed sequences records exactly its kernels:
+    prep, ring roll, chunk offsets, intra, inter and the RMSNorm, once each."""
+    from gated_delta_rule_scan_gb300 import kda
+    inp = inputs.make_inputs(74, H=2, N=2, lengths=(40, 90), raw_dtype="bf16", conv=True,
+                             ring="randn", state="randn", epilogue=True)
+    kda.kernel_timing(True)
+    try:
+        gpu_prefill(inp, varlen=True)
+        times = kda.kernel_times()
+    finally:
+        kda.kernel_timing(False)
+    assert set(times) == {"kda_prep_kernel", "kda_ring_roll_kernel", "kda_chunk_offsets_kernel",
+                          "kda_chunk_intra_kernel", "kda_chunk_inter_kernel",
+                          "kda_gated_rmsnorm_kernel"}, times
+    assert all(n == 1 and ms > 0 for n, ms in times.values()), times
