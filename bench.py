@@ -160,6 +160,9 @@ def _kernel_bytes(T, H, blk_bytes, chunks):
         "kda_ring_roll_kernel": 3 * C * 3 * (bf16 + f32),
         # q, k, v, g, beta -> the workspace of operand images
         "kda_chunk_intra_kernel": 4 * plane + T * H * f32 + ws,
+        # raw q, k, v (bf16), gate input, beta input, conv weights + ring -> the workspace
+        "kda_chunk_prep_intra_kernel": 3 * T * C * bf16 + plane + T * H * f32 + 3 * C * 4 * f32
+                                       + 3 * C * 3 * f32 + ws,
         # workspace + state in -> o + state out
         "kda_chunk_inter_kernel": ws + 2 * H * D * D * f32 + plane,
         "kda_chunk_offsets_kernel": 0,
@@ -239,8 +242,8 @@ def run_ours(args):
         return float(t.item())
 
     # ---------------- prefill workload (resident) ----------------
-    pre = inputs.prefill(T=PREFILL_T, H=PREFILL_H)
-    H, T = PREFILL_H, PREFILL_T
+    H, T = args.heads, PREFILL_T
+    pre = inputs.prefill(T=T, H=H)
     C = H * D
     d = {k: (None if getattr(pre, k) is None else getattr(pre, k).to(dev)) for k in
          ("q_raw", "k_raw", "v_raw", "conv_w", "ring_in", "f_raw", "dt_bias", "a_log",
@@ -306,8 +309,9 @@ def run_ours(args):
     ms_step = ms / K
     tokens_per_s = ws * T / (ms_step / 1e3)
     if fused:
-        scan_ms = sum(ktimes[k][1] for k in ("kda_chunk_intra_kernel", "kda_chunk_inter_kernel",
-                                             "kda_chunk_offsets_kernel") if k in ktimes) / K
+        scan_ms = sum(ktimes[k][1] for k in ("kda_chunk_prep_intra_kernel", "kda_chunk_intra_kernel",
+                                             "kda_chunk_inter_kernel", "kda_chunk_offsets_kernel")
+                      if k in ktimes) / K
     else:
         scan_ms = statistics.mean(a.elapsed_time(b) for a, b in scan_ev)
     scan_flop = FLOP_PER_TOKEN_HEAD * T * H
@@ -373,9 +377,13 @@ def run_ours(args):
         kernels.append(ent)
     if fused:
         top = kernels[0]
-        src_files = {"kda_chunk_intra_kernel": ["kda_scan_chunk.cu", "kda_tc.cuh", "kda_device.cuh"],
+        src_files = {"kda_chunk_intra_kernel": ["kda_scan_chunk.cu", "kda_chunk_common.cuh", "kda_tc.cuh",
+                                                "kda_device.cuh"],
+                     "kda_chunk_prep_intra_kernel": ["kda_chunk_prep.cu", "kda_chunk_common.cuh",
+                                                     "kda_tc.cuh", "kda_device.cuh"],
                      "kda_gated_rmsnorm_kernel": ["kda_epilogue.cu", "kda_device.cuh"],
-                     "kda_chunk_inter_kernel": ["kda_scan_chunk.cu", "kda_tc.cuh", "kda_device.cuh"],
+                     "kda_chunk_inter_kernel": ["kda_scan_chunk.cu", "kda_chunk_common.cuh", "kda_tc.cuh",
+                                                "kda_device.cuh"],
                      "kda_prep_kernel": ["kda_prep.cu", "kda_device.cuh"]}
         roofline = {"bound": "hbm", "kernel": top["kernel"], "achieved": top.get("gbs"),
                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": top.get("frac_hbm"),
@@ -396,7 +404,7 @@ def run_ours(args):
         "steps": K, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded numpy default_rng; bf16 raw q/k/v, f32 gates, state, norm)",
-        "config": {"workload": "prefill: 1 sequence x 4096 tokens, H=64, head_dim=128, conv K=4,"
+        "config": {"workload": f"prefill: 1 sequence x 4096 tokens, H={H}, head_dim=128, conv K=4,"
                                " zero state and ring, whole mixer per step",
                    "path": "kda_prefill_fused (prep, chunked scan, gated RMSNorm)" if fused
                            else "staged calls, sequential scan",
@@ -448,16 +456,22 @@ def _oracle_sample(pre, heads):
     return time.perf_counter() - t
 
 
-def cpu_baseline(pre, n_heads):
+def cpu_baseline(pre, n_heads, min_secs=10.0):
+    """The oracle as it stands on the host cores: the prefill workload restricted to n_heads heads
+    (all 64 by default, i.e. the whole workload), repeated until at least min_secs have passed."""
     from oracle import oracle as orc
     orc.build()
     heads = list(range(n_heads))
-    secs = _oracle_sample(pre, heads)
-    frac = n_heads / pre.H
-    return {"value": PREFILL_T * frac / secs, "unit": "tokens/s",
+    secs = []
+    while sum(secs) < min_secs and len(secs) < 100:
+        secs.append(_oracle_sample(pre, heads))
+    total = sum(secs)
+    tokens = PREFILL_T * (n_heads / pre.H) * len(secs)
+    return {"value": tokens / total, "unit": "tokens/s",
             "cores": min(orc.num_threads(), n_heads), "kind": "oracle",
             "sample": f"prefill workload, heads 0..{n_heads - 1} of {pre.H} (all {PREFILL_T} "
-                      f"tokens, full mixer), {secs:.1f} s, scaled to 64 heads",
+                      f"tokens, full mixer) x {len(secs)} runs, {total:.1f} s"
+                      + ("" if n_heads == pre.H else ", scaled to all heads"),
             "host_cpus": os.cpu_count()}
 
 
@@ -498,12 +512,14 @@ def main():
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--cpu-sample-heads", type=int, default=16)
+    ap.add_argument("--cpu-sample-heads", type=int, default=64)
     ap.add_argument("--ref-steps", type=int, default=5)
     ap.add_argument("--scan-algo", choices=("auto", "seq", "chunk"), default="auto",
                     help="prefill scan form (auto = the library's choice for the shape)")
     ap.add_argument("--skip-e2e", action="store_true", help="profiling runs: no host-copy leg")
     ap.add_argument("--skip-cpu", action="store_true", help="profiling runs: no oracle timing")
+    ap.add_argument("--heads", type=int, default=PREFILL_H,
+                    help="profiling runs: a smaller prefill of the same kernels (default 64)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -48,12 +48,16 @@ int check_cu(const int* cu_host, int N, long total) {
     return KDA_OK;
 }
 
-int prep_impl(const void* q_raw, const void* k_raw, const void* v_raw, int raw_dtype,
-              const float* conv_w, const float* ring_in, float* ring_out, const float* f_raw,
-              const float* dt_bias, const float* a_log, int gate_mode, float gate_lb,
-              const float* beta_raw, float* q_hat, float* k_hat, float* v_hat, float* g,
-              float* beta, const SeqLayout& seq, int H, int D, int K, float l2_eps,
-              void* stream) {
+// Contract checks of the prep stages and their argument block.  planes: the call writes the
+// q, k, v, g, beta planes (the fused prefill does not, and passes them as NULL).
+int prep_build(const void* q_raw, const void* k_raw, const void* v_raw, int raw_dtype,
+               const float* conv_w, const float* ring_in, float* ring_out, const float* f_raw,
+               const float* dt_bias, const float* a_log, int gate_mode, float gate_lb,
+               const float* beta_raw, float* q_hat, float* k_hat, float* v_hat, float* g,
+               float* beta, const SeqLayout& seq, int H, int D, int K, float l2_eps,
+               bool planes, PrepArgs& a) {
+    a = PrepArgs{};
+    a.seq = seq;
     if (D != kHeadDim) return KDA_ERR_HEAD_DIM;
     if (seq.N < 0 || seq.N > kMaxGridY || seq.total_rows < 0 || H <= 0 || H > kMaxGridY)
         return KDA_ERR_SHAPE;
@@ -63,10 +67,10 @@ int prep_impl(const void* q_raw, const void* k_raw, const void* v_raw, int raw_d
     if (seq.N == 0) return KDA_OK;
     if (conv_w != nullptr && (ring_in == nullptr || ring_out == nullptr)) return KDA_ERR_NULL;
     if (seq.total_rows > 0) {
-        if (!q_raw || !k_raw || !v_raw || !f_raw || !dt_bias || !a_log || !beta_raw || !q_hat ||
-            !k_hat || !v_hat || !g || !beta)
+        if (!q_raw || !k_raw || !v_raw || !f_raw || !dt_bias || !a_log || !beta_raw)
             return KDA_ERR_NULL;
-        if (!aligned16(q_hat) || !aligned16(k_hat) || !aligned16(v_hat) || !aligned16(g))
+        if (planes && (!q_hat || !k_hat || !v_hat || !g || !beta)) return KDA_ERR_NULL;
+        if (planes && (!aligned16(q_hat) || !aligned16(k_hat) || !aligned16(v_hat) || !aligned16(g)))
             return KDA_ERR_ALIGN;
         // raw rows are read 4 channels at a time: 8-byte bf16x4 or 16-byte f32x4
         const uintptr_t rmask = raw_dtype == KDA_DTYPE_BF16 ? 7u : 15u;
@@ -80,13 +84,26 @@ int prep_impl(const void* q_raw, const void* k_raw, const void* v_raw, int raw_d
         const size_t rb = (size_t)seq.N * 3 * H * kHeadDim * (K - 1) * sizeof(float);
         if (overlap(ring_in, ring_out, rb)) return KDA_ERR_STATE_ALIAS;
     }
-    PrepArgs a{};
     a.q_raw = q_raw; a.k_raw = k_raw; a.v_raw = v_raw; a.raw_bf16 = raw_dtype == KDA_DTYPE_BF16;
     a.conv_w = conv_w; a.ring_in = ring_in; a.ring_out = ring_out;
     a.f_raw = f_raw; a.dt_bias = dt_bias; a.a_log = a_log; a.gate_mode = gate_mode;
     a.gate_lb = gate_lb; a.beta_raw = beta_raw;
     a.q_hat = q_hat; a.k_hat = k_hat; a.v_hat = v_hat; a.g = g; a.beta = beta;
     a.seq = seq; a.H = H; a.K = conv_w ? K : 1; a.l2_eps = l2_eps;
+    return KDA_OK;
+}
+
+int prep_impl(const void* q_raw, const void* k_raw, const void* v_raw, int raw_dtype,
+              const float* conv_w, const float* ring_in, float* ring_out, const float* f_raw,
+              const float* dt_bias, const float* a_log, int gate_mode, float gate_lb,
+              const float* beta_raw, float* q_hat, float* k_hat, float* v_hat, float* g,
+              float* beta, const SeqLayout& seq, int H, int D, int K, float l2_eps,
+              void* stream) {
+    PrepArgs a;
+    const int rc = prep_build(q_raw, k_raw, v_raw, raw_dtype, conv_w, ring_in, ring_out, f_raw,
+                              dt_bias, a_log, gate_mode, gate_lb, beta_raw, q_hat, k_hat, v_hat,
+                              g, beta, seq, H, D, K, l2_eps, true, a);
+    if (rc != KDA_OK || seq.N == 0) return rc;
     return cuda_status(launch_prep(a, static_cast<cudaStream_t>(stream)));
 }
 
@@ -134,22 +151,18 @@ int scan_impl(const float* q, const float* k, const float* v, const float* g, in
                              : launch_scan_seq(a, static_cast<cudaStream_t>(stream)));
 }
 
-// Byte offsets of the pieces of kda_prefill_fused's workspace: the prep outputs (q, k, v, g,
-// beta), the scan's readout o, then the chunked scan's scratch.
+// Byte offsets of the pieces of kda_prefill_fused's workspace: the scan's readout o, then the
+// chunked scan's scratch (the prepared q, k, v, g never leave the chunk kernel).
 struct PrefillLayout {
-    size_t q, k, v, g, beta, o, chunk;
+    size_t o, chunk;
 };
 
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-PrefillLayout prefill_layout(long rows, int H, int gate_mode) {
-    const size_t plane = align256((size_t)rows * H * kHeadDim * sizeof(float));
-    const size_t gsz = (gate_mode & KDA_GATE_PER_HEAD) ? (size_t)rows * H * sizeof(float) : plane;
+PrefillLayout prefill_layout(long rows, int H) {
     PrefillLayout L;
-    L.q = 0; L.k = plane; L.v = 2 * plane; L.g = 3 * plane;
-    L.beta = L.g + align256(gsz);
-    L.o = L.beta + align256((size_t)rows * H * sizeof(float));
-    L.chunk = L.o + plane;
+    L.o = 0;
+    L.chunk = align256((size_t)rows * H * kHeadDim * sizeof(float));
     return L;
 }
 
@@ -170,23 +183,26 @@ int prefill_impl(const void* q_raw, const void* k_raw, const void* v_raw, int ra
         if (!norm_w || !gate_raw || !y) return KDA_ERR_NULL;
         if (!aligned16(norm_w) || !aligned16(gate_raw) || !aligned16(y)) return KDA_ERR_ALIGN;
     }
-    const PrefillLayout L = prefill_layout(seq.total_rows, H, gate_mode);
+    PrepArgs pa;
+    int rc = prep_build(q_raw, k_raw, v_raw, raw_dtype, conv_w, ring_in, ring_out, f_raw, dt_bias,
+                        a_log, gate_mode, gate_lb, beta_raw, nullptr, nullptr, nullptr, nullptr,
+                        nullptr, seq, H, D, K, l2_eps, false, pa);
+    if (rc != KDA_OK) return rc;
+    if (!state_in || !state_out) return KDA_ERR_NULL;
+    if (!aligned16(state_in) || !aligned16(state_out)) return KDA_ERR_ALIGN;
+    if (overlap(state_in, state_out, (size_t)seq.N * H * kHeadDim * kHeadDim * sizeof(float)))
+        return KDA_ERR_STATE_ALIAS;
+    const PrefillLayout L = prefill_layout(seq.total_rows, H);
     const size_t need = L.chunk + chunk_workspace_bytes(seq, cu_host, H);
     if (workspace == nullptr || workspace_bytes < need) return KDA_ERR_WORKSPACE;
     if (!aligned16(workspace)) return KDA_ERR_ALIGN;
     unsigned char* w = static_cast<unsigned char*>(workspace);
-    float* qh = reinterpret_cast<float*>(w + L.q);
-    float* kh = reinterpret_cast<float*>(w + L.k);
-    float* vh = reinterpret_cast<float*>(w + L.v);
-    float* gh = reinterpret_cast<float*>(w + L.g);
-    float* bh = reinterpret_cast<float*>(w + L.beta);
     float* oh = reinterpret_cast<float*>(w + L.o);
-    int rc = prep_impl(q_raw, k_raw, v_raw, raw_dtype, conv_w, ring_in, ring_out, f_raw, dt_bias,
-                       a_log, gate_mode, gate_lb, beta_raw, qh, kh, vh, gh, bh, seq, H, D, K,
-                       l2_eps, stream);
-    if (rc != KDA_OK) return rc;
-    rc = scan_impl(qh, kh, vh, gh, gate_mode, bh, state_in, state_out, oh, seq, cu_host, H, D,
-                   scale, KDA_ALGO_CHUNK, w + L.chunk, workspace_bytes - L.chunk, stream);
+    ScanArgs a{};
+    a.gate_mode = gate_mode; a.state_in = state_in; a.state_out = state_out; a.o = oh;
+    a.seq = seq; a.H = H; a.scale = scale; a.order = nullptr; a.err = dev_err_ptr();
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    rc = cuda_status(launch_prefill_chunk(pa, a, cu_host, w + L.chunk, st));
     if (rc != KDA_OK || seq.total_rows == 0) return rc;
     NormArgs na{oh, norm_w, gate_raw, y, seq.total_rows * H, norm_eps};
     return cuda_status(launch_gated_rmsnorm(na, static_cast<cudaStream_t>(stream)));
@@ -267,7 +283,7 @@ size_t kda_scan_workspace_bytes(int N, int total_T, int H, int D, int gate_mode,
 size_t kda_prefill_workspace_bytes(int N, int total_T, int H, int D, int gate_mode) {
     if (N < 0 || total_T < 0 || H <= 0 || D != kHeadDim) return 0;
     if (gate_mode != KDA_GATE_PER_CHANNEL && gate_mode != KDA_GATE_PER_HEAD) return 0;
-    return prefill_layout(total_T, H, gate_mode).chunk +
+    return prefill_layout(total_T, H).chunk +
            kda_scan_workspace_bytes(N, total_T, H, D, gate_mode, KDA_ALGO_CHUNK);
 }
 

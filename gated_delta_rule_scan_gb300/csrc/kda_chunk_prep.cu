@@ -1,0 +1,467 @@
+// kda_chunk_prep.cu -- the fused prefill's first kernel: stages 2-4 of kda_core_gated (conv +
+// SiLU, l2 norm, gates, beta; "memra_engine/kda.rs", memra-engine 0.125.0) computed straight
+// into the chunked form's intra-chunk operand images, one CTA per (32-token chunk, head), so the
+// prepared q, k, v and gate planes never reach memory.  From the images on, the CTA runs the same
+// MMA tail as the chunked scan's intra kernel (kda_chunk_common.cuh).
+//
+// Layout: warp w takes tokens 8w .. 8w+7 of the chunk and lane l channels 4l .. 4l+3 of the head,
+// the prep kernel's lane-to-channel map, so every per-token quantity is computed with the prep's
+// arithmetic: conv taps oldest first over a window that starts K-1 samples back (from the ring
+// for the first chunk of a sequence), SiLU, the l2 sum of squares reduced over the warp (a
+// transposed butterfly that adds the same pairs as the prep's per-row butterfly), gates and beta.
+// The column images (8 consecutive tokens of one channel per 16-byte row) come straight from a
+// thread's registers; the row images (8 consecutive channels of one token) pair lane l with l^1
+// by shuffles.  The per-channel running sum of the gate passes from warp to warp through shared
+// memory in token order, the order of the chunked scan's own intra kernel.  The output blocks
+// therefore equal those of the prep kernel followed by the intra kernel bit for bit.
+#include "kda_chunk_common.cuh"
+
+namespace kda {
+
+constexpr int kTokW = 8;   // tokens per warp: 4 warps cover one 32-token chunk
+
+template <bool BF16>
+struct RawVec;
+template <>
+struct RawVec<true> { using T = uint2; };     // 4 bf16 channels
+template <>
+struct RawVec<false> { using T = float4; };   // 4 f32 channels
+
+template <bool BF16>
+__device__ __forceinline__ typename RawVec<BF16>::T raw_ld(const void* base, long idx) {
+    if constexpr (BF16) {
+        return __ldg(reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(base) + idx));
+    } else {
+        return __ldg(reinterpret_cast<const float4*>(reinterpret_cast<const float*>(base) + idx));
+    }
+}
+
+template <bool BF16>
+__device__ __forceinline__ typename RawVec<BF16>::T raw_zero() {
+    if constexpr (BF16) return make_uint2(0u, 0u);
+    else return make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+}
+
+template <bool BF16>
+__device__ __forceinline__ float4 raw_unpack(const typename RawVec<BF16>::T& u) {
+    if constexpr (BF16) {
+        const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+        const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+        return make_float4(a.x, a.y, b.x, b.y);
+    } else {
+        return u;
+    }
+}
+
+__device__ __forceinline__ float f4c(const float4& v, int e) {
+    return e == 0 ? v.x : (e == 1 ? v.y : (e == 2 ? v.z : v.w));
+}
+
+// One plane's raw samples for this lane's 4 channels: the KW-1 samples before the warp's first
+// token (halo, f32) and the warp's 8 tokens (raw, packed).
+template <bool BF16, int KW>
+struct PlaneRaw {
+    float4 halo[KW - 1];
+    typename RawVec<BF16>::T cur[kTokW];
+};
+
+// Issue the loads of one plane.  pos0 = position of the warp's first token in its sequence;
+// ring_base = this plane's ring row of channel c4 (channel e at + e*R).
+template <bool BF16, bool CONV, int KW>
+__device__ __forceinline__ void plane_load(PlaneRaw<BF16, KW>& P, const void* raw, long C, long c4,
+                                           long begin, long pos0, int ntok, const float* ring_in,
+                                           long ring_base, int R) {
+#pragma unroll
+    for (int i = 0; i < kTokW; ++i)
+        P.cur[i] = i < ntok ? raw_ld<BF16>(raw, (begin + pos0 + i) * C + c4) : raw_zero<BF16>();
+    if (CONV && ntok > 0) {                       // (a warp past the sequence end loads nothing)
+#pragma unroll
+        for (int m = 0; m < KW - 1; ++m) {
+            const int d = KW - 1 - m;                 // samples back from the first token
+            const long pos = pos0 - d;
+            float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            if (d <= R) {
+                if (pos >= 0) {
+                    v = raw_unpack<BF16>(raw_ld<BF16>(raw, (begin + pos) * C + c4));
+                } else {
+                    const long s2 = R + pos;
+                    v = make_float4(ring_in[ring_base + s2], ring_in[ring_base + R + s2],
+                                    ring_in[ring_base + 2 * R + s2], ring_in[ring_base + 3 * R + s2]);
+                }
+            }
+            P.halo[m] = v;
+        }
+    }
+}
+
+// conv + SiLU of one plane for the warp's 8 tokens (or the raw samples without a conv).
+template <bool BF16, bool CONV, int KW>
+__device__ __forceinline__ void plane_conv(const PlaneRaw<BF16, KW>& P, const float (&w)[4][KW],
+                                           int K, float (&y)[kTokW][4]) {
+    float4 cur[kTokW];
+#pragma unroll
+    for (int i = 0; i < kTokW; ++i) cur[i] = raw_unpack<BF16>(P.cur[i]);
+#pragma unroll
+    for (int i = 0; i < kTokW; ++i) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            if constexpr (CONV) {
+                float win[KW];
+#pragma unroll
+                for (int m = 0; m < KW; ++m) {
+                    const int idx = i + m;            // window slot m = sample at token i-(KW-1)+m
+                    win[m] = idx < KW - 1 ? f4c(P.halo[idx], e) : f4c(cur[idx - (KW - 1)], e);
+                }
+                y[i][e] = silu_f(conv_taps_f(w[e], win, K));
+            } else {
+                y[i][e] = f4c(cur[i], e);
+            }
+        }
+    }
+}
+
+template <int KW>
+__device__ __forceinline__ void plane_weights(const float* conv_w, long row, int K, float (&w)[4][KW]) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+#pragma unroll
+        for (int m = 0; m < KW; ++m) {
+            const int j = m - (KW - K);
+            w[e][m] = j >= 0 ? conv_w[(row + e) * K + j] : 0.0f;
+        }
+}
+
+// Sum 16 per-lane values over the warp with 16 shuffles: on return lanes 2j and 2j+1 hold the
+// total of value j.  Each step adds a lane's own partial and its partner's, the pairs of a
+// per-value butterfly (xor 16, 8, 4, 2, 1), so the totals equal warp_sum's bit for bit.
+__device__ __forceinline__ float warp_sum16(float (&x)[16]) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int w = 8; w >= 1; w >>= 1) {
+        const int off = 2 * w;
+        const bool upper = (lane & off) != 0;
+#pragma unroll
+        for (int i = 0; i < w; ++i) {
+            const float send = upper ? x[i] : x[i + w];
+            const float keep = upper ? x[i + w] : x[i];
+            x[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+        }
+    }
+    return x[0] + __shfl_xor_sync(0xffffffffu, x[0], 1);
+}
+
+// The 8-channel row of token j of this lane's half of the warp's tokens (even lane: tokens 0-3,
+// odd lane: tokens 4-7): own 4 channels plus the partner lane's 4, in channel order.
+__device__ __forceinline__ void pair_rows(const float (&x)[kTokW][4], float (&row)[4][8]) {
+    const bool odd = (threadIdx.x & 1) != 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float send = odd ? x[j][e] : x[4 + j][e];
+            const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
+            row[j][e] = odd ? recv : x[j][e];
+            row[j][4 + e] = odd ? x[4 + j][e] : recv;
+        }
+}
+
+template <bool BF16, int GATE_MODE, bool CONV, int KW>
+__global__ void __launch_bounds__(kThr, 2)
+kda_chunk_prep_intra_kernel(PrepArgs p, ScanArgs a, const int* chunk_off, unsigned char* ws) {
+    extern __shared__ unsigned char smem_raw[];
+    IntraSmem& sm = *reinterpret_cast<IntraSmem*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int h = blockIdx.y;
+    const long gid = blockIdx.x;                 // global chunk index
+    const int H = a.H;
+    const long C = (long)H * kHeadDim;
+
+    int n;
+    if (a.seq.cu_seqlens == nullptr) {
+        n = (int)(gid / ((a.seq.T_uniform + kCc - 1) / kCc));
+    } else {
+        int lo = 0, hi = a.seq.N;                // largest n with chunk_off[n] <= gid
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if ((long)chunk_off[mid] <= gid) lo = mid; else hi = mid;
+        }
+        n = lo;
+    }
+    long begin, end;
+    seq_range(a.seq, n, begin, end);
+    const long c = gid - chunk_base(a.seq, chunk_off, n);
+    const long row0 = begin + c * kCc;
+    const int nt = (int)min((long)kCc, end - row0);
+    unsigned char* blk = ws + ((long)gid * H + h) * kBlkBytes;
+    const int kq = 4 * lane;                     // first of this lane's channels within the head
+    const long c4 = (long)h * kHeadDim + kq;     // ... within the plane
+    const int t0 = kTokW * warp;                 // the warp's first token within the chunk
+    const int ntok = max(0, min(kTokW, nt - t0));
+    const int K = p.K, R = p.K - 1;
+
+    // ---- loads: raw q, k, v with the conv halo, the gate input, beta ---------------------------
+    PlaneRaw<BF16, KW> rq, rk, rv;
+    {
+        const long pos0 = c * kCc + t0;
+        const long rr = (long)n * 3 * C * R;
+        plane_load<BF16, CONV, KW>(rq, p.q_raw, C, c4, begin, pos0, ntok, p.ring_in, rr + (0 * C + c4) * R, R);
+        plane_load<BF16, CONV, KW>(rk, p.k_raw, C, c4, begin, pos0, ntok, p.ring_in, rr + (1 * C + c4) * R, R);
+        plane_load<BF16, CONV, KW>(rv, p.v_raw, C, c4, begin, pos0, ntok, p.ring_in, rr + (2 * C + c4) * R, R);
+    }
+    float4 fr[kTokW];
+    if (GATE_MODE == 0) {
+#pragma unroll
+        for (int i = 0; i < kTokW; ++i)
+            fr[i] = i < ntok ? __ldg(reinterpret_cast<const float4*>(p.f_raw + (row0 + t0 + i) * C + c4))
+                             : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    }
+    if (tid < kCc) {
+        const bool live = tid < nt;
+        sm.beta[tid] = live ? sigmoid_f(p.beta_raw[(row0 + tid) * H + h]) : 0.0f;
+        if (GATE_MODE == 1)
+            sm.gs[tid] = live ? gdn_gate_f(p.f_raw[(row0 + tid) * H + h], p.dt_bias[h], p.a_log[h]) : 0.0f;
+    }
+    if (warp == 0) {
+        tmem_alloc(&sm.tmem_base, 256);
+        tmem_relinquish();
+    }
+    if (tid == 0) {
+        mbar_init(&sm.bar, 1);
+        fence_mbar_init();
+    }
+
+    // ---- conv + SiLU; l2 norm of q and k over the head (one warp = one token group) ------------
+    float v[kTokW][4], k[kTokW][4], q[kTokW][4];
+    {
+        float w[4][KW];
+        if constexpr (CONV) plane_weights<KW>(p.conv_w, 2 * C + c4, K, w);
+        plane_conv<BF16, CONV, KW>(rv, w, K, v);
+        if constexpr (CONV) plane_weights<KW>(p.conv_w, 1 * C + c4, K, w);
+        plane_conv<BF16, CONV, KW>(rk, w, K, k);
+        if constexpr (CONV) plane_weights<KW>(p.conv_w, 0 * C + c4, K, w);
+        plane_conv<BF16, CONV, KW>(rq, w, K, q);
+    }
+    {
+        float ss[16];
+#pragma unroll
+        for (int i = 0; i < kTokW; ++i) {
+            float s = __fmul_rn(q[i][0], q[i][0]);
+            s = fmaf(q[i][1], q[i][1], s); s = fmaf(q[i][2], q[i][2], s); s = fmaf(q[i][3], q[i][3], s);
+            ss[i] = s;
+            s = __fmul_rn(k[i][0], k[i][0]);
+            s = fmaf(k[i][1], k[i][1], s); s = fmaf(k[i][2], k[i][2], s); s = fmaf(k[i][3], k[i][3], s);
+            ss[kTokW + i] = s;
+        }
+        const float part = warp_sum16(ss);
+#pragma unroll
+        for (int i = 0; i < kTokW; ++i) {
+            const float iq = l2_inv_f(__shfl_sync(0xffffffffu, part, 2 * i), p.l2_eps);
+            const float ik = l2_inv_f(__shfl_sync(0xffffffffu, part, 2 * (kTokW + i)), p.l2_eps);
+            const bool live = i < ntok;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                q[i][e] = live ? q[i][e] * iq : 0.0f;
+                k[i][e] = live ? k[i][e] * ik : 0.0f;
+                v[i][e] = live ? v[i][e] : 0.0f;
+            }
+        }
+    }
+
+    // ---- running gate sum G (per channel, KDA) in token order, warp to warp --------------------
+    float G[kTokW][4];
+    float GCh = 0.0f;                            // per-head gate: the chunk's total
+    if (GATE_MODE == 0) {
+        const float rate = expf(p.a_log[h]);
+        const float4 dt = *reinterpret_cast<const float4*>(p.dt_bias + c4);
+        const float dtv[4] = {dt.x, dt.y, dt.z, dt.w};
+        float g[kTokW][4];
+#pragma unroll
+        for (int i = 0; i < kTokW; ++i)
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                g[i][e] = i < ntok ? kda_gate_f(f4c(fr[i], e), dtv[e], rate, p.gate_lb) : 0.0f;
+        float* carry = sm.cref;                  // the running sums handed on (reused below)
+#pragma unroll
+        for (int s = 0; s < 4; ++s) {
+            if (warp == s) {
+                float run[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) run[e] = s == 0 ? 0.0f : carry[kq + e];
+#pragma unroll
+                for (int i = 0; i < kTokW; ++i)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        run[e] += g[i][e];
+                        G[i][e] = run[e];
+                    }
+                if (s < 3) {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) carry[kq + e] = run[e];
+                } else {                         // G over the whole chunk: references, decay, range
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        sm.gcs[kq + e] = run[e];
+                        sm.cref[kq + e] = 0.5f * run[e];
+                        sm.ecr[kq + e] = __expf(0.5f * run[e]);
+                        reinterpret_cast<float*>(blk + kOffEG)[kq + e] = decay_f(run[e]);
+                        if (run[e] < -170.0f && a.err) atomicOr(a.err, kDevErrRange);
+                    }
+                }
+            }
+            __syncthreads();
+        }
+#pragma unroll
+        for (int i = 0; i < kTokW; ++i)
+            *reinterpret_cast<float4*>(&sm.scr[(t0 + i) * 128 + kq]) =
+                make_float4(G[i][0], G[i][1], G[i][2], G[i][3]);
+    } else {
+        __syncthreads();                         // sm.gs
+        float run = 0.0f;                        // the running sum in token order
+        for (int t = 0; t < t0; ++t) run += sm.gs[t];
+#pragma unroll
+        for (int i = 0; i < kTokW; ++i) {
+            run += sm.gs[t0 + i];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) G[i][e] = run;
+        }
+        for (int t = t0 + kTokW; t < kCc; ++t) run += sm.gs[t];
+        GCh = run;
+        if (tid < kCc) {
+            float Gt = 0.0f;
+            for (int t = 0; t <= tid; ++t) Gt += sm.gs[t];    // same summation order as G
+            sm.gsc[tid] = Gt;
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) reinterpret_cast<float*>(blk + kOffEG)[kq + e] = decay_f(GCh);
+    }
+    __syncthreads();                             // G tile, references, beta, gsc
+
+    // ---- column images: channel kq+e, tokens t0 .. t0+7 ----------------------------------------
+    {
+        float bv[kTokW];
+#pragma unroll
+        for (int i = 0; i < kTokW; ++i) bv[i] = sm.beta[t0 + i];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            float xt[8], xv[8], xc[8];
+            const float GCe = GATE_MODE == 0 ? sm.gcs[kq + e] : GCh;
+#pragma unroll
+            for (int i = 0; i < kTokW; ++i) {
+                const float Gi = G[i][e];
+                xt[i] = bv[i] * k[i][e] * __expf(Gi);
+                xv[i] = bv[i] * v[i][e];
+                xc[i] = k[i][e] * __expf(GCe - Gi);
+            }
+            put8x(sm.ktv[0], sm.ktv[1], tc_offset(kq + e, t0, kSbo32), xt);
+            put8x(sm.ktv[0], sm.ktv[1], tc_offset(128 + kq + e, t0, kSbo32), xv);
+            put8x(blk + kOffB2, blk + kOffB2 + kB2Bytes, tc_offset(kq + e, t0, kSbo32), xc);
+        }
+    }
+
+    // ---- row images: tokens t0 + 4*(lane&1) + j, channels k0 .. k0+7 ---------------------------
+    {
+        float kr[4][8], qr[4][8];
+        pair_rows(k, kr);
+        pair_rows(q, qr);
+        const int k0 = 8 * (lane >> 1);
+        const int tb = t0 + 4 * (lane & 1);
+        float crv[8], ecv[8], gtv[4][8];
+        if (GATE_MODE == 0) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) { crv[e] = sm.cref[k0 + e]; ecv[e] = sm.ecr[k0 + e]; }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float4 a0 = *reinterpret_cast<const float4*>(&sm.scr[(tb + j) * 128 + k0]);
+                const float4 a1 = *reinterpret_cast<const float4*>(&sm.scr[(tb + j) * 128 + k0 + 4]);
+                gtv[j][0] = a0.x; gtv[j][1] = a0.y; gtv[j][2] = a0.z; gtv[j][3] = a0.w;
+                gtv[j][4] = a1.x; gtv[j][5] = a1.y; gtv[j][6] = a1.z; gtv[j][7] = a1.w;
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) gtv[j][0] = sm.gsc[tb + j];
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int t = tb + j;
+            float xb[8], xk[8], xq[8], xg[8];
+            if (GATE_MODE == 0) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float gt = gtv[j][e], cr = crv[e];
+                    const float ef = __expf(gt - cr), eb = __expf(cr - gt);
+                    xb[e] = kr[j][e] * eb;
+                    xk[e] = kr[j][e] * ef;
+                    xq[e] = qr[j][e] * ef;
+                    xg[e] = qr[j][e] * (ef * ecv[e]);
+                }
+            } else {
+                const float eg = __expf(gtv[j][0]);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    xb[e] = kr[j][e];
+                    xk[e] = kr[j][e];
+                    xq[e] = qr[j][e];
+                    xg[e] = qr[j][e] * eg;
+                }
+            }
+            put8x(sm.kb[0], sm.kb[1], tc_offset(t, k0, kSbo128), xb);
+            put8x(sm.bia[0], sm.bia[1], tc_offset(t, k0, kSbo128), xk);
+            put8x(sm.bia[0], sm.bia[1], tc_offset(kCc + t, k0, kSbo128), xq);
+            put8x(blk + kOffQW, blk + kOffQW + kQWBytes, tc_offset(t, k0, kSbo128), xg);
+        }
+    }
+    intra_mma_tail<GATE_MODE>(sm, a.err, blk);
+}
+
+template <bool BF16, int GM, bool CONV, int KW>
+static cudaError_t launch_prep_intra_t(const PrepArgs& p, const ScanArgs& a, const int* chunk_off,
+                                       unsigned char* blocks, long nchunks, cudaStream_t s) {
+    const size_t smem = sizeof(IntraSmem) + 128;
+    static int done[64] = {0};
+    cudaError_t e = set_smem(kda_chunk_prep_intra_kernel<BF16, GM, CONV, KW>, smem, done);
+    if (e != cudaSuccess) return e;
+    dim3 grid((unsigned)nchunks, (unsigned)a.H);
+    KernelTimer kt(kKPrepIntra, s);
+    kda_chunk_prep_intra_kernel<BF16, GM, CONV, KW><<<grid, kThr, smem, s>>>(p, a, chunk_off, blocks);
+    return cudaGetLastError();
+}
+
+template <bool BF16, int GM>
+static cudaError_t launch_prep_intra_c(const PrepArgs& p, const ScanArgs& a, const int* chunk_off,
+                                       unsigned char* blocks, long nchunks, cudaStream_t s) {
+    if (p.conv_w == nullptr)
+        return launch_prep_intra_t<BF16, GM, false, 4>(p, a, chunk_off, blocks, nchunks, s);
+    if (p.K <= 4) return launch_prep_intra_t<BF16, GM, true, 4>(p, a, chunk_off, blocks, nchunks, s);
+    return launch_prep_intra_t<BF16, GM, true, kMaxConvK>(p, a, chunk_off, blocks, nchunks, s);
+}
+
+cudaError_t launch_prefill_chunk(const PrepArgs& p, const ScanArgs& a, const int* cu_host,
+                                 void* workspace, cudaStream_t s) {
+    if (a.seq.N == 0) return cudaSuccess;
+    cudaError_t e;
+    if (a.seq.total_rows == 0) {
+        const size_t bytes = (size_t)a.seq.N * a.H * kHeadDim * kHeadDim * sizeof(float);
+        e = cudaMemcpyAsync(a.state_out, a.state_in, bytes, cudaMemcpyDeviceToDevice, s);
+        if (e != cudaSuccess) return e;
+        return launch_ring_roll(p, s);
+    }
+    int* chunk_off = nullptr;
+    unsigned char* blocks = nullptr;
+    e = launch_chunk_offsets(a.seq, workspace, &chunk_off, &blocks, s);
+    if (e != cudaSuccess) return e;
+    const long nchunks = chunk_count(a.seq, cu_host);
+    if (nchunks > 0) {
+        const bool gm1 = (a.gate_mode & 1) != 0;
+        if (p.raw_bf16) e = gm1 ? launch_prep_intra_c<true, 1>(p, a, chunk_off, blocks, nchunks, s)
+                                : launch_prep_intra_c<true, 0>(p, a, chunk_off, blocks, nchunks, s);
+        else e = gm1 ? launch_prep_intra_c<false, 1>(p, a, chunk_off, blocks, nchunks, s)
+                     : launch_prep_intra_c<false, 0>(p, a, chunk_off, blocks, nchunks, s);
+        if (e != cudaSuccess) return e;
+    }
+    e = launch_ring_roll(p, s);                  // after the kernel above has read ring_in
+    if (e != cudaSuccess) return e;
+    return launch_chunk_inter(a, chunk_off, blocks, s);
+}
+
+}  // namespace kda

@@ -62,6 +62,19 @@ cudaError_t launch_scan_chunk(const ScanArgs& a, const int* cu_host, void* works
                               cudaStream_t s);
 // exact workspace the chunked scan needs for this layout (cu_host: host copy of cu_seqlens)
 size_t chunk_workspace_bytes(const SeqLayout& s, const int* cu_host, int H);
+long chunk_count(const SeqLayout& s, const int* cu_host);
+// pieces of the chunked form for the fused prefill (kda_scan_chunk.cu): the varlen chunk offsets
+// at the head of the workspace (blocks = where the per-(chunk, head) blocks start), and the
+// inter-chunk kernel over filled blocks
+cudaError_t launch_chunk_offsets(const SeqLayout& seq, void* workspace, int** chunk_off,
+                                 unsigned char** blocks, cudaStream_t s);
+cudaError_t launch_chunk_inter(const ScanArgs& a, const int* chunk_off,
+                               const unsigned char* blocks, cudaStream_t s);
+// the fused prefill's prep + intra-chunk kernel, then the ring roll (kda_chunk_prep.cu)
+cudaError_t launch_prefill_chunk(const PrepArgs& p, const ScanArgs& a, const int* cu_host,
+                                 void* workspace, cudaStream_t s);
+// the conv ring roll alone (kda_prep.cu)
+cudaError_t launch_ring_roll(const PrepArgs& a, cudaStream_t s);
 
 // Fixed device scratch for kda_scan_varlen_static (kda_scan_static.cu): its byte size, and the
 // address of this device's copy (looked up once per device, on the first call with it current).
@@ -82,7 +95,7 @@ constexpr int kDecodeMaxT = 16;   // tokens one fused decode/verify call may car
 // CUDA event before and after it on the launch stream while timing is enabled.
 enum KernelId {
     kKPrep, kKRingRoll, kKScanSeq, kKChunkOffsets, kKChunkIntra, kKChunkInter, kKRmsNorm,
-    kKDecode, kKernelCount
+    kKDecode, kKPrepIntra, kKernelCount
 };
 class KernelTimer {
 public:

@@ -251,6 +251,16 @@ __global__ void __launch_bounds__(256) kda_ring_roll_kernel(PrepArgs a) {
     }
 }
 
+cudaError_t launch_ring_roll(const PrepArgs& a, cudaStream_t s) {
+    if (a.conv_w == nullptr || a.seq.N == 0) return cudaSuccess;
+    const long C3 = 3L * a.H * kHeadDim;
+    dim3 grid((unsigned)((C3 + 255) / 256), (unsigned)a.seq.N);
+    KernelTimer kt(kKRingRoll, s);
+    if (a.raw_bf16) kda_ring_roll_kernel<true><<<grid, 256, 0, s>>>(a);
+    else kda_ring_roll_kernel<false><<<grid, 256, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
 template <bool BF16, int GM, bool CONV, bool EXP>
 static cudaError_t launch_prep_t(const PrepArgs& a, cudaStream_t s) {
     const long tiles = (a.seq.total_rows + (long)kRun * kPrepWarps - 1) / ((long)kRun * kPrepWarps);
@@ -262,13 +272,7 @@ static cudaError_t launch_prep_t(const PrepArgs& a, cudaStream_t s) {
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    if (CONV && a.seq.N > 0) {
-        const long C3 = 3L * a.H * kHeadDim;
-        dim3 grid((unsigned)((C3 + 255) / 256), (unsigned)a.seq.N);
-        KernelTimer kt(kKRingRoll, s);
-        kda_ring_roll_kernel<BF16><<<grid, 256, 0, s>>>(a);
-        return cudaGetLastError();
-    }
+    if (CONV) return launch_ring_roll(a, s);
     return cudaSuccess;
 }
 

@@ -223,10 +223,9 @@ int kda_gated_rmsnorm_out(const float* o, const float* norm_w, const float* gate
 
 /*
  * kda_prefill_workspace_bytes -- device scratch that suffices for kda_prefill_fused /
- * kda_prefill_fused_varlen over N sequences holding total_T tokens in all: the intermediate
- * q, k, v, gate, beta and readout planes (about 20 bytes per (token, channel)) plus the chunked
- * scan's scratch (kda_scan_workspace_bytes with KDA_ALGO_CHUNK).  Returns 0 for invalid
- * arguments.
+ * kda_prefill_fused_varlen over N sequences holding total_T tokens in all: the scan's readout
+ * plane (4 bytes per (token, channel)) plus the chunked scan's scratch (kda_scan_workspace_bytes
+ * with KDA_ALGO_CHUNK).  Returns 0 for invalid arguments.
  */
 size_t kda_prefill_workspace_bytes(int N, int total_T, int H, int D, int gate_mode);
 
@@ -234,7 +233,9 @@ size_t kda_prefill_workspace_bytes(int N, int total_T, int H, int D, int gate_mo
  * kda_prefill_fused -- a prefill of N sequences of T tokens in one call: stages 2-6 of
  * kda_core_gated (conv + SiLU, l2 norm, gates and beta, the chunked scan, gated RMSNorm), the
  * same computation as kda_conv_l2norm_prep + kda_scan with KDA_ALGO_CHUNK +
- * kda_gated_rmsnorm_out with the same arguments, the intermediates kept in the workspace.
+ * kda_gated_rmsnorm_out with the same arguments.  The prepared q, k, v and gates are computed
+ * inside the chunked scan's first kernel and never reach memory; the readout passes through the
+ * workspace on its way to the RMSNorm.
  * Arguments and layouts as in those three calls; gate_mode is KDA_GATE_PER_CHANNEL or
  * KDA_GATE_PER_HEAD (the KDA_GATE_EXP flag is not accepted, 40007); norm_w [D] f32 [16B];
  * gate_raw and y [N*T, C] f32 [16B].  The chunked form's range condition applies (every
