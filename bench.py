@@ -506,6 +506,57 @@ def run_reference(args):
                     "d2h_bytes_per_step": 0}}
 
 
+def run_crossover(args):
+    """The sequential and the chunked scan (kda_scan, q/k/v/g resident) over a grid of sequence
+    counts and lengths at H = 64: one JSON line per point with both times.  The library's AUTO
+    rule is set from this table."""
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    from gated_delta_rule_scan_gb300 import kda
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    gen = torch.Generator(device=dev).manual_seed(5)
+
+    def timed(N, T, H, algo):
+        C, rows = H * D, N * T
+        unit = lambda: torch.nn.functional.normalize(  # noqa: E731
+            torch.randn(rows, H, D, device=dev, generator=gen), dim=-1).reshape(rows, C)
+        q, k = unit(), unit()
+        v = torch.randn(rows, C, device=dev, generator=gen)
+        gl = -5.0 * torch.sigmoid(torch.randn(rows, C, device=dev, generator=gen))
+        seq = algo == kda.ALGO_SEQ
+        g = torch.exp(gl) if seq else gl
+        beta = torch.sigmoid(torch.randn(rows, H, device=dev, generator=gen))
+        s0 = torch.zeros(N, H, D, D, device=dev)
+        s1, o = torch.empty_like(s0), torch.empty(rows, C, device=dev)
+        ws = kda.scan_workspace(N, rows, H, dev, algo)
+        gm = kda.GATE_EXP if seq else 0
+
+        def f():
+            kda.kda_scan(q, k, v, g, beta, s0, s1, o, N=N, T=T, H=H, gate_mode=gm, algo=algo,
+                         workspace=ws)
+        for _ in range(3):
+            f()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.steps):
+            f()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / args.steps * 1e3
+
+    for N in (1, 16, 64):
+        for T in (16, 32, 48, 64, 96, 128, 256, 512, 1024):
+            s_us = timed(N, T, PREFILL_H, kda.ALGO_SEQ)
+            c_us = timed(N, T, PREFILL_H, kda.ALGO_CHUNK)
+            print(json.dumps({"N": N, "T": T, "H": PREFILL_H, "seq_us": round(s_us, 1),
+                              "chunk_us": round(c_us, 1),
+                              "faster": "chunk" if c_us < s_us else "seq"}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -518,11 +569,16 @@ def main():
                     help="prefill scan form (auto = the library's choice for the shape)")
     ap.add_argument("--skip-e2e", action="store_true", help="profiling runs: no host-copy leg")
     ap.add_argument("--skip-cpu", action="store_true", help="profiling runs: no oracle timing")
+    ap.add_argument("--crossover", action="store_true",
+                    help="time the sequential vs the chunked scan over lengths and exit")
     ap.add_argument("--heads", type=int, default=PREFILL_H,
                     help="profiling runs: a smaller prefill of the same kernels (default 64)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.crossover:
+        run_crossover(args)
+        return
     res = run_reference(args) if args.impl == "reference" else run_ours(args)
     if res is not None:
         print(json.dumps(res), flush=True)

@@ -107,8 +107,13 @@ int prep_impl(const void* q_raw, const void* k_raw, const void* v_raw, int raw_d
     return cuda_status(launch_prep(a, static_cast<cudaStream_t>(stream)));
 }
 
-// Shortest longest-sequence for which AUTO takes the chunked form (measured crossover).
-constexpr long kAutoChunkMinLen = 64;
+// AUTO takes the chunked form when the longest sequence has at least kAutoChunkMinLen tokens, or
+// at least kAutoChunkMinLenWide when there are kAutoWidePairs or more (sequence, head) pairs.
+// Measured on GB300 (H = 64): one sequence crosses over between 96 and 128 tokens, 16 or more
+// sequences between 48 and 64.
+constexpr long kAutoChunkMinLen = 128;
+constexpr long kAutoChunkMinLenWide = 64;
+constexpr long kAutoWidePairs = 512;
 
 long max_len(const SeqLayout& seq, const int* cu_host) {
     if (seq.cu_seqlens == nullptr) return seq.T_uniform;
@@ -145,7 +150,11 @@ int scan_impl(const float* q, const float* k, const float* v, const float* g, in
     const bool ws_ok = workspace != nullptr && workspace_bytes >= need && aligned16(workspace);
     bool chunk = algo == KDA_ALGO_CHUNK;
     if (chunk && !ws_ok) return workspace && !aligned16(workspace) ? KDA_ERR_ALIGN : KDA_ERR_WORKSPACE;
-    if (algo == KDA_ALGO_AUTO) chunk = ws_ok && max_len(seq, cu_host) >= kAutoChunkMinLen;
+    if (algo == KDA_ALGO_AUTO) {
+        const long ml = max_len(seq, cu_host);
+        const bool wide = (long)seq.N * H >= kAutoWidePairs;
+        chunk = ws_ok && (ml >= kAutoChunkMinLen || (wide && ml >= kAutoChunkMinLenWide));
+    }
     a.err = dev_err_ptr();  // null only if the symbol lookup failed: waits then report nothing
     return cuda_status(chunk ? launch_scan_chunk(a, cu_host, workspace, static_cast<cudaStream_t>(stream))
                              : launch_scan_seq(a, static_cast<cudaStream_t>(stream)));

@@ -162,16 +162,18 @@ static_assert(2 * kTmBytes <= 64 * 128 * 2, "Tm fits in bia[0]");
 // inverse Tm = (I + A)^{-1}, MMA-b (W and U) and the workspace epilogue.  On entry every thread
 // has written its share of sm.bia, sm.kb, sm.ktv, the QG and K^T images in blk and blk's EG row;
 // sm.beta (and for GDN sm.gsc, the running per-head gate) are set; warp 0 holds sm.tmem_base
-// (256 columns) and sm.bar is initialised.  Ends with the TMEM deallocated.
-template <int GATE_MODE>
+// (256 columns) and sm.bar is initialised.  Ends with the TMEM deallocated.  NT = threads of the
+// CTA, 128 or 256 (warps w and w+4 share TMEM lane quarter w and split the epilogue's columns).
+template <int GATE_MODE, int NT>
 __device__ __forceinline__ void intra_mma_tail(IntraSmem& sm, int* err, unsigned char* blk) {
+    static_assert(NT == 128 || NT == 256, "128 or 256 threads");
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tbase = sm.tmem_base;
-    const uint32_t tlane = tbase + ((uint32_t)(32 * warp) << 16);
+    const uint32_t tlane = tbase + ((uint32_t)(32 * (warp & 3)) << 16);
     uint32_t phase = 0;
     bool ok = true;
     float* am = sm.scr;                          // A (strictly lower), f32 [32][kLd]
@@ -188,7 +190,7 @@ __device__ __forceinline__ void intra_mma_tail(IntraSmem& sm, int* err, unsigned
                 tc_smem_desc(smem_u32(sm.kb[1]), 128, kSbo128), 8, tc_idesc_bf16(128, kCc));
         tc_commit(&sm.bar);
     }
-    for (int i = tid; i < kCc * kLd; i += kThr) ti[i] = 0.0f;   // G is dead: scr is free
+    for (int i = tid; i < kCc * kLd; i += NT) ti[i] = 0.0f;     // G is dead: scr is free
     ok = mbar_wait_bounded(&sm.bar, phase, err);
     phase ^= 1u;
     tc_fence_after();
@@ -243,21 +245,25 @@ __device__ __forceinline__ void intra_mma_tail(IntraSmem& sm, int* err, unsigned
     }
     __syncthreads();
     {
-        const int p = tid >> 6, r = (tid & 63) >> 3, cc = tid & 7;
+        const int p = (tid >> 6) & 1, r = (tid & 63) >> 3, cc = tid & 7;   // threads 0..127
         const int r0 = 16 * p + 8, c0 = 16 * p;
-        float acc = 0.0f;
+        if (tid < 128) {
+            float acc = 0.0f;
 #pragma unroll
-        for (int m = 0; m < 8; ++m) acc = fmaf(am[(r0 + r) * kLd + c0 + m], ti[(c0 + m) * kLd + c0 + cc], acc);
-        pb[(r0 + r) * kLd + c0 + cc] = acc;
+            for (int m = 0; m < 8; ++m) acc = fmaf(am[(r0 + r) * kLd + c0 + m], ti[(c0 + m) * kLd + c0 + cc], acc);
+            pb[(r0 + r) * kLd + c0 + cc] = acc;
+        }
         __syncthreads();
-        acc = 0.0f;
+        if (tid < 128) {
+            float acc = 0.0f;
 #pragma unroll
-        for (int m = 0; m < 8; ++m) acc = fmaf(ti[(r0 + r) * kLd + r0 + m], pb[(r0 + m) * kLd + c0 + cc], acc);
-        ti[(r0 + r) * kLd + c0 + cc] = -acc;
+            for (int m = 0; m < 8; ++m) acc = fmaf(ti[(r0 + r) * kLd + r0 + m], pb[(r0 + m) * kLd + c0 + cc], acc);
+            ti[(r0 + r) * kLd + c0 + cc] = -acc;
+        }
         __syncthreads();
     }
 #pragma unroll
-    for (int e = tid; e < 256; e += kThr) {
+    for (int e = tid; e < 256; e += NT) {
         const int r = e >> 4, cc = e & 15;
         float acc = 0.0f;
 #pragma unroll
@@ -266,7 +272,7 @@ __device__ __forceinline__ void intra_mma_tail(IntraSmem& sm, int* err, unsigned
     }
     __syncthreads();
 #pragma unroll
-    for (int e = tid; e < 256; e += kThr) {
+    for (int e = tid; e < 256; e += NT) {
         const int r = e >> 4, cc = e & 15;
         float acc = 0.0f;
 #pragma unroll
@@ -274,7 +280,7 @@ __device__ __forceinline__ void intra_mma_tail(IntraSmem& sm, int* err, unsigned
         ti[(16 + r) * kLd + cc] = -acc;
     }
     __syncthreads();
-    {   // Tm image, four copies (rows t, 32+t, 64+t, 96+t) so that each warp reads its own
+    if (tid < 128) {   // Tm image, four copies (rows t, 32+t, 64+t, 96+t): one per lane quarter
         const int t = tid >> 2, s0 = (tid & 3) * 8;
         float x[8];
 #pragma unroll
@@ -299,24 +305,25 @@ __device__ __forceinline__ void intra_mma_tail(IntraSmem& sm, int* err, unsigned
     tc_fence_after();
     if (__syncthreads_or(!ok)) goto done;
     {
-        // warp w: columns 64w .. 64w+63 of [W | U] for token t = lane
-        const int t = lane;
-        float x[64];
+        // warp w: columns CW*w .. CW*w+CW-1 of [W | U] (W: 0..127, U: 128..255) for token t = lane
+        constexpr int CW = 256 / (NT / 32);
+        const int t = lane, col0 = CW * warp;
+        float x[CW];
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-            tmem_ld16(tlane + 64 * warp + 16 * q, *reinterpret_cast<float(*)[16]>(&x[16 * q]));
+        for (int q = 0; q < CW / 16; ++q)
+            tmem_ld16(tlane + col0 + 16 * q, *reinterpret_cast<float(*)[16]>(&x[16 * q]));
         tmem_ld_wait();
-        if (warp < 2) {     // W row t, channels 64w .. : QW image rows 32 + t
+        if (col0 < 128) {   // W row t, channels col0 .. : QW image rows 32 + t
             unsigned char* qwh = blk + kOffQW;
             unsigned char* qwl = blk + kOffQW + kQWBytes;
 #pragma unroll
-            for (int cb = 0; cb < 8; ++cb)
-                put8x(qwh, qwl, tc_offset(kCc + t, 64 * warp + 8 * cb, kSbo128),
+            for (int cb = 0; cb < CW / 8; ++cb)
+                put8x(qwh, qwl, tc_offset(kCc + t, col0 + 8 * cb, kSbo128),
                       *reinterpret_cast<const float(*)[8]>(&x[8 * cb]));
-        } else {            // U row t, values 64(w-2) .. : f32 [32 t][128 v]
-            float4* ut = reinterpret_cast<float4*>(blk + kOffUT) + t * 32 + 16 * (warp - 2);
+        } else {            // U row t, values col0 - 128 .. : f32 [32 t][128 v]
+            float4* ut = reinterpret_cast<float4*>(blk + kOffUT) + t * 32 + (col0 - 128) / 4;
 #pragma unroll
-            for (int q = 0; q < 16; ++q) ut[q] = make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
+            for (int q = 0; q < CW / 4; ++q) ut[q] = make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
         }
     }
 done:

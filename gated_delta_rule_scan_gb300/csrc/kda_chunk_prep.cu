@@ -4,21 +4,22 @@
 // prepared q, k, v and gate planes never reach memory.  From the images on, the CTA runs the same
 // MMA tail as the chunked scan's intra kernel (kda_chunk_common.cuh).
 //
-// Layout: warp w takes tokens 8w .. 8w+7 of the chunk and lane l channels 4l .. 4l+3 of the head,
+// Layout: 256 threads; warp w takes tokens 4w .. 4w+3 of the chunk and lane l channels 4l .. 4l+3 of the head,
 // the prep kernel's lane-to-channel map, so every per-token quantity is computed with the prep's
 // arithmetic: conv taps oldest first over a window that starts K-1 samples back (from the ring
 // for the first chunk of a sequence), SiLU, the l2 sum of squares reduced over the warp (a
 // transposed butterfly that adds the same pairs as the prep's per-row butterfly), gates and beta.
-// The column images (8 consecutive tokens of one channel per 16-byte row) come straight from a
-// thread's registers; the row images (8 consecutive channels of one token) pair lane l with l^1
-// by shuffles.  The per-channel running sum of the gate passes from warp to warp through shared
+// The column images (consecutive tokens of one channel) are written from a thread's registers
+// as 8-byte half rows of their 16-byte core-matrix rows; the row images (8 consecutive channels
+// of one token) pair lane l with l^1 by shuffles.  The per-channel running sum of the gate passes from warp to warp through shared
 // memory in token order, the order of the chunked scan's own intra kernel.  The output blocks
 // therefore equal those of the prep kernel followed by the intra kernel bit for bit.
 #include "kda_chunk_common.cuh"
 
 namespace kda {
 
-constexpr int kTokW = 8;   // tokens per warp: 4 warps cover one 32-token chunk
+constexpr int kTokW = 4;      // tokens per warp: 8 warps cover one 32-token chunk
+constexpr int kThrF = 256;    // threads of the fused kernel
 
 template <bool BF16>
 struct RawVec;
@@ -131,14 +132,14 @@ __device__ __forceinline__ void plane_weights(const float* conv_w, long row, int
         }
 }
 
-// Sum 16 per-lane values over the warp with 16 shuffles: on return lanes 2j and 2j+1 hold the
-// total of value j.  Each step adds a lane's own partial and its partner's, the pairs of a
-// per-value butterfly (xor 16, 8, 4, 2, 1), so the totals equal warp_sum's bit for bit.
-__device__ __forceinline__ float warp_sum16(float (&x)[16]) {
+// Sum 8 per-lane values over the warp with 9 shuffles: on return lanes 4j .. 4j+3 hold the total
+// of value j.  Each step adds a lane's own partial and its partner's, the pairs of a per-value
+// butterfly (xor 16, 8, 4, 2, 1), so the totals equal warp_sum's bit for bit.
+__device__ __forceinline__ float warp_sum8(float (&x)[8]) {
     const int lane = threadIdx.x & 31;
 #pragma unroll
-    for (int w = 8; w >= 1; w >>= 1) {
-        const int off = 2 * w;
+    for (int w = 4; w >= 1; w >>= 1) {
+        const int off = 4 * w;
         const bool upper = (lane & off) != 0;
 #pragma unroll
         for (int i = 0; i < w; ++i) {
@@ -147,26 +148,38 @@ __device__ __forceinline__ float warp_sum16(float (&x)[16]) {
             x[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
         }
     }
-    return x[0] + __shfl_xor_sync(0xffffffffu, x[0], 1);
+    float t = x[0] + __shfl_xor_sync(0xffffffffu, x[0], 2);
+    return t + __shfl_xor_sync(0xffffffffu, t, 1);
 }
 
-// The 8-channel row of token j of this lane's half of the warp's tokens (even lane: tokens 0-3,
-// odd lane: tokens 4-7): own 4 channels plus the partner lane's 4, in channel order.
-__device__ __forceinline__ void pair_rows(const float (&x)[kTokW][4], float (&row)[4][8]) {
+// 4 f32 values as bf16 hi / lo at byte offset off (8-byte aligned) of two images: half of a
+// 16-byte core-matrix row.
+__device__ __forceinline__ void put4x(unsigned char* hi_img, unsigned char* lo_img, uint32_t off,
+                                      const float (&x)[4]) {
+    uint2 hi, lo;
+    split_bf16x2(x[0], x[1], hi.x, lo.x);
+    split_bf16x2(x[2], x[3], hi.y, lo.y);
+    *reinterpret_cast<uint2*>(hi_img + off) = hi;
+    *reinterpret_cast<uint2*>(lo_img + off) = lo;
+}
+
+// The 8-channel rows of this lane's half of the warp's tokens (even lane: tokens 0-1, odd lane:
+// tokens 2-3): own 4 channels plus the partner lane's 4, in channel order.
+__device__ __forceinline__ void pair_rows(const float (&x)[kTokW][4], float (&row)[2][8]) {
     const bool odd = (threadIdx.x & 1) != 0;
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
+    for (int j = 0; j < 2; ++j)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-            const float send = odd ? x[j][e] : x[4 + j][e];
+            const float send = odd ? x[j][e] : x[2 + j][e];
             const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
             row[j][e] = odd ? recv : x[j][e];
-            row[j][4 + e] = odd ? x[4 + j][e] : recv;
+            row[j][4 + e] = odd ? x[2 + j][e] : recv;
         }
 }
 
 template <bool BF16, int GATE_MODE, bool CONV, int KW>
-__global__ void __launch_bounds__(kThr, 2)
+__global__ void __launch_bounds__(kThrF, 2)
 kda_chunk_prep_intra_kernel(PrepArgs p, ScanArgs a, const int* chunk_off, unsigned char* ws) {
     extern __shared__ unsigned char smem_raw[];
     IntraSmem& sm = *reinterpret_cast<IntraSmem*>(
@@ -243,7 +256,7 @@ kda_chunk_prep_intra_kernel(PrepArgs p, ScanArgs a, const int* chunk_off, unsign
         plane_conv<BF16, CONV, KW>(rq, w, K, q);
     }
     {
-        float ss[16];
+        float ss[2 * kTokW];
 #pragma unroll
         for (int i = 0; i < kTokW; ++i) {
             float s = __fmul_rn(q[i][0], q[i][0]);
@@ -253,11 +266,11 @@ kda_chunk_prep_intra_kernel(PrepArgs p, ScanArgs a, const int* chunk_off, unsign
             s = fmaf(k[i][1], k[i][1], s); s = fmaf(k[i][2], k[i][2], s); s = fmaf(k[i][3], k[i][3], s);
             ss[kTokW + i] = s;
         }
-        const float part = warp_sum16(ss);
+        const float part = warp_sum8(ss);
 #pragma unroll
         for (int i = 0; i < kTokW; ++i) {
-            const float iq = l2_inv_f(__shfl_sync(0xffffffffu, part, 2 * i), p.l2_eps);
-            const float ik = l2_inv_f(__shfl_sync(0xffffffffu, part, 2 * (kTokW + i)), p.l2_eps);
+            const float iq = l2_inv_f(__shfl_sync(0xffffffffu, part, 4 * i), p.l2_eps);
+            const float ik = l2_inv_f(__shfl_sync(0xffffffffu, part, 4 * (kTokW + i)), p.l2_eps);
             const bool live = i < ntok;
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
@@ -283,7 +296,7 @@ kda_chunk_prep_intra_kernel(PrepArgs p, ScanArgs a, const int* chunk_off, unsign
                 g[i][e] = i < ntok ? kda_gate_f(f4c(fr[i], e), dtv[e], rate, p.gate_lb) : 0.0f;
         float* carry = sm.cref;                  // the running sums handed on (reused below)
 #pragma unroll
-        for (int s = 0; s < 4; ++s) {
+        for (int s = 0; s < kThrF / 32; ++s) {
             if (warp == s) {
                 float run[4];
 #pragma unroll
@@ -295,7 +308,7 @@ kda_chunk_prep_intra_kernel(PrepArgs p, ScanArgs a, const int* chunk_off, unsign
                         run[e] += g[i][e];
                         G[i][e] = run[e];
                     }
-                if (s < 3) {
+                if (s < kThrF / 32 - 1) {
 #pragma unroll
                     for (int e = 0; e < 4; ++e) carry[kq + e] = run[e];
                 } else {                         // G over the whole chunk: references, decay, range
@@ -344,7 +357,7 @@ kda_chunk_prep_intra_kernel(PrepArgs p, ScanArgs a, const int* chunk_off, unsign
         for (int i = 0; i < kTokW; ++i) bv[i] = sm.beta[t0 + i];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-            float xt[8], xv[8], xc[8];
+            float xt[kTokW], xv[kTokW], xc[kTokW];
             const float GCe = GATE_MODE == 0 ? sm.gcs[kq + e] : GCh;
 #pragma unroll
             for (int i = 0; i < kTokW; ++i) {
@@ -353,25 +366,25 @@ kda_chunk_prep_intra_kernel(PrepArgs p, ScanArgs a, const int* chunk_off, unsign
                 xv[i] = bv[i] * v[i][e];
                 xc[i] = k[i][e] * __expf(GCe - Gi);
             }
-            put8x(sm.ktv[0], sm.ktv[1], tc_offset(kq + e, t0, kSbo32), xt);
-            put8x(sm.ktv[0], sm.ktv[1], tc_offset(128 + kq + e, t0, kSbo32), xv);
-            put8x(blk + kOffB2, blk + kOffB2 + kB2Bytes, tc_offset(kq + e, t0, kSbo32), xc);
+            put4x(sm.ktv[0], sm.ktv[1], tc_offset(kq + e, t0, kSbo32), xt);
+            put4x(sm.ktv[0], sm.ktv[1], tc_offset(128 + kq + e, t0, kSbo32), xv);
+            put4x(blk + kOffB2, blk + kOffB2 + kB2Bytes, tc_offset(kq + e, t0, kSbo32), xc);
         }
     }
 
-    // ---- row images: tokens t0 + 4*(lane&1) + j, channels k0 .. k0+7 ---------------------------
+    // ---- row images: tokens t0 + 2*(lane&1) + j, channels k0 .. k0+7 ---------------------------
     {
-        float kr[4][8], qr[4][8];
+        float kr[2][8], qr[2][8];
         pair_rows(k, kr);
         pair_rows(q, qr);
         const int k0 = 8 * (lane >> 1);
-        const int tb = t0 + 4 * (lane & 1);
-        float crv[8], ecv[8], gtv[4][8];
+        const int tb = t0 + 2 * (lane & 1);
+        float crv[8], ecv[8], gtv[2][8];
         if (GATE_MODE == 0) {
 #pragma unroll
             for (int e = 0; e < 8; ++e) { crv[e] = sm.cref[k0 + e]; ecv[e] = sm.ecr[k0 + e]; }
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
+            for (int j = 0; j < 2; ++j) {
                 const float4 a0 = *reinterpret_cast<const float4*>(&sm.scr[(tb + j) * 128 + k0]);
                 const float4 a1 = *reinterpret_cast<const float4*>(&sm.scr[(tb + j) * 128 + k0 + 4]);
                 gtv[j][0] = a0.x; gtv[j][1] = a0.y; gtv[j][2] = a0.z; gtv[j][3] = a0.w;
@@ -379,10 +392,10 @@ kda_chunk_prep_intra_kernel(PrepArgs p, ScanArgs a, const int* chunk_off, unsign
             }
         } else {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) gtv[j][0] = sm.gsc[tb + j];
+            for (int j = 0; j < 2; ++j) gtv[j][0] = sm.gsc[tb + j];
         }
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
+        for (int j = 0; j < 2; ++j) {
             const int t = tb + j;
             float xb[8], xk[8], xq[8], xg[8];
             if (GATE_MODE == 0) {
@@ -411,7 +424,7 @@ kda_chunk_prep_intra_kernel(PrepArgs p, ScanArgs a, const int* chunk_off, unsign
             put8x(blk + kOffQW, blk + kOffQW + kQWBytes, tc_offset(t, k0, kSbo128), xg);
         }
     }
-    intra_mma_tail<GATE_MODE>(sm, a.err, blk);
+    intra_mma_tail<GATE_MODE, kThrF>(sm, a.err, blk);
 }
 
 template <bool BF16, int GM, bool CONV, int KW>
@@ -423,7 +436,7 @@ static cudaError_t launch_prep_intra_t(const PrepArgs& p, const ScanArgs& a, con
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)nchunks, (unsigned)a.H);
     KernelTimer kt(kKPrepIntra, s);
-    kda_chunk_prep_intra_kernel<BF16, GM, CONV, KW><<<grid, kThr, smem, s>>>(p, a, chunk_off, blocks);
+    kda_chunk_prep_intra_kernel<BF16, GM, CONV, KW><<<grid, kThrF, smem, s>>>(p, a, chunk_off, blocks);
     return cudaGetLastError();
 }
 

@@ -158,7 +158,8 @@ size_t kda_scan_workspace_bytes(int N, int total_T, int H, int D, int gate_mode,
  *                      above -170 per channel (a bounded gate such as KDA's >= -5 per token
  *                      satisfies it), otherwise kda_device_status reports 40008.
  *                      KDA_ALGO_AUTO takes the chunked form when a large-enough workspace is given
- *                      and the longest sequence has at least 64 tokens, else the sequential one.
+ *                      and the longest sequence has at least 128 tokens (64 when N * H >= 512),
+ *                      else the sequential one: the measured crossover on GB300.
  * workspace            device scratch [16B], at least kda_scan_workspace_bytes(...) bytes for
  *                      KDA_ALGO_CHUNK (40009 otherwise), or NULL.  Its contents are overwritten;
  *                      calls that share a workspace must not overlap on the GPU.
