@@ -162,10 +162,19 @@ static_assert(2 * kTmBytes <= 64 * 128 * 2, "Tm fits in bia[0]");
 // inverse Tm = (I + A)^{-1}, MMA-b (W and U) and the workspace epilogue.  On entry every thread
 // has written its share of sm.bia, sm.kb, sm.ktv, the QG and K^T images in blk and blk's EG row;
 // sm.beta (and for GDN sm.gsc, the running per-head gate) are set; warp 0 holds sm.tmem_base
-// (256 columns) and sm.bar is initialised.  Ends with the TMEM deallocated.  NT = threads of the
-// CTA, 128 or 256 (warps w and w+4 share TMEM lane quarter w and split the epilogue's columns).
-template <int GATE_MODE, int NT>
-__device__ __forceinline__ void intra_mma_tail(IntraSmem& sm, int* err, unsigned char* blk) {
+// (256 columns) and sm.bar is initialised; phase is sm.bar's current parity (updated).  Once
+// MMA-a has completed (sm.bia[1] and sm.kb are then free for the rest of the tail), every thread
+// calls after_a(); once the Tm image is written (sm.scr is then free), after_tm().  Ends after a barrier, the TMEM still allocated; returns false if a bounded
+// wait gave up.  NT = threads of the CTA, 128 or 256 (warps w and w+4 share TMEM lane quarter w
+// and split the epilogue's columns).
+struct NoHook {
+    __device__ void operator()() const {}
+};
+
+template <int GATE_MODE, int NT, typename AfterA = NoHook, typename AfterTm = NoHook>
+__device__ __forceinline__ bool intra_mma_tail(IntraSmem& sm, int* err, unsigned char* blk,
+                                               uint32_t& phase, AfterA after_a = AfterA(),
+                                               AfterTm after_tm = AfterTm()) {
     static_assert(NT == 128 || NT == 256, "128 or 256 threads");
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     fence_proxy_async_smem();
@@ -174,7 +183,6 @@ __device__ __forceinline__ void intra_mma_tail(IntraSmem& sm, int* err, unsigned
     tc_fence_after();
     const uint32_t tbase = sm.tmem_base;
     const uint32_t tlane = tbase + ((uint32_t)(32 * (warp & 3)) << 16);
-    uint32_t phase = 0;
     bool ok = true;
     float* am = sm.scr;                          // A (strictly lower), f32 [32][kLd]
     float* ti = sm.scr + kCc * kLd;              // Tm
@@ -195,6 +203,7 @@ __device__ __forceinline__ void intra_mma_tail(IntraSmem& sm, int* err, unsigned
     phase ^= 1u;
     tc_fence_after();
     if (__syncthreads_or(!ok)) goto done;
+    after_a();
 
     // ---- A (warp 0, lane t = row t) and Aqk (warp 1, lane t) -----------------------------------
     if (warp < 2) {
@@ -292,6 +301,7 @@ __device__ __forceinline__ void intra_mma_tail(IntraSmem& sm, int* err, unsigned
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    after_tm();
 
     // ---- MMA-b: [W | U] = Tm [(beta K e^G) | (beta V)], every warp's 32 lanes = tokens --------
     if (tid == 0) {
@@ -329,7 +339,7 @@ __device__ __forceinline__ void intra_mma_tail(IntraSmem& sm, int* err, unsigned
 done:
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tbase, 256);
+    return ok;
 }
 
 // Opt a kernel into `bytes` of dynamic shared memory once per device; `done` is the caller's own

@@ -152,6 +152,41 @@ __device__ __forceinline__ float warp_sum8(float (&x)[8]) {
     return t + __shfl_xor_sync(0xffffffffu, t, 1);
 }
 
+// the chunk of global index gid: its sequence n and rows, the chunk's first row and its tokens
+__device__ __forceinline__ void chunk_task(const SeqLayout& L, const int* chunk_off, long gid,
+                                           int& n, long& begin, long& end, long& row0, int& nt) {
+    if (L.cu_seqlens == nullptr) {
+        n = (int)(gid / ((L.T_uniform + kCc - 1) / kCc));
+    } else {
+        int lo = 0, hi = L.N;                    // largest n with chunk_off[n] <= gid
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if ((long)chunk_off[mid] <= gid) lo = mid; else hi = mid;
+        }
+        n = lo;
+    }
+    seq_range(L, n, begin, end);
+    row0 = begin + (gid - chunk_base(L, chunk_off, n)) * kCc;
+    nt = (int)min((long)kCc, end - row0);
+}
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)),
+                 "l"(reinterpret_cast<uint64_t>(src))
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// Staged bf16 raw rows of one task: [plane][row][128 channels], row r = chunk token r - (KW-1)
+// (the conv halo first).  Lives in sm.bia[1] + sm.kb (32 KB), free from the end of one task's
+// MMA-a to the next task's conv.
+template <int KW>
+struct RawStage {
+    static constexpr int kRows = kCc + KW - 1;
+    __nv_bfloat16 v[3][kRows][kHeadDim];
+};
+
 // 4 f32 values as bf16 hi / lo at byte offset off (8-byte aligned) of two images: half of a
 // 16-byte core-matrix row.
 __device__ __forceinline__ void put4x(unsigned char* hi_img, unsigned char* lo_img, uint32_t off,
@@ -178,52 +213,127 @@ __device__ __forceinline__ void pair_rows(const float (&x)[kTokW][4], float (&ro
         }
 }
 
+// Issue the cp.async copies of task `task`'s raw q, k, v rows (the chunk's tokens and its conv
+// halo inside the sequence) into the stage; every thread takes a share of the 16-byte pieces.
+template <int KW>
+__device__ __forceinline__ void stage_raw(RawStage<KW>& st, const PrepArgs& p, const ScanArgs& a,
+                                          const int* chunk_off, long task, long nchunks) {
+    const long gid = task % nchunks;
+    const int h = (int)(task / nchunks);
+    int n, nt;
+    long begin, end, row0;
+    chunk_task(a.seq, chunk_off, gid, n, begin, end, row0, nt);
+    const long C = (long)a.H * kHeadDim;
+    const long pos_c = row0 - begin;             // position of the chunk's first token
+    constexpr int kPieces = 3 * RawStage<KW>::kRows * (kHeadDim / 8);
+    for (int idx = threadIdx.x; idx < kPieces; idx += kThrF) {
+        const int pl = idx / (RawStage<KW>::kRows * 16);
+        const int r = (idx / 16) % RawStage<KW>::kRows;
+        const int j = idx % 16;
+        const int t = r - (KW - 1);
+        if (t < nt && pos_c + t >= 0) {
+            const void* raw = pl == 0 ? p.q_raw : (pl == 1 ? p.k_raw : p.v_raw);
+            cp_async16(&st.v[pl][r][8 * j],
+                       reinterpret_cast<const __nv_bfloat16*>(raw) + (row0 + t) * C + (long)h * kHeadDim + 8 * j);
+        }
+    }
+    cp_async_commit();
+}
+
+// Issue the cp.async copies of task `task`'s gate-input rows (KDA: [32 tokens][128] f32) into
+// sm.scr, free from the end of one task's Tm image to the next task's gate step.
+__device__ __forceinline__ void stage_f(float* dst, const PrepArgs& p, const ScanArgs& a,
+                                        const int* chunk_off, long task, long nchunks) {
+    const long gid = task % nchunks;
+    const int h = (int)(task / nchunks);
+    int n, nt;
+    long begin, end, row0;
+    chunk_task(a.seq, chunk_off, gid, n, begin, end, row0, nt);
+    const long C = (long)a.H * kHeadDim;
+    for (int idx = threadIdx.x; idx < kCc * (kHeadDim / 4); idx += kThrF) {
+        const int t = idx / (kHeadDim / 4), j = idx % (kHeadDim / 4);
+        if (t < nt) cp_async16(dst + t * kHeadDim + 4 * j, p.f_raw + (row0 + t) * C + (long)h * kHeadDim + 4 * j);
+    }
+    cp_async_commit();
+}
+
+// The staged samples of one plane for this lane's 4 channels: the halo (from the stage, or the
+// ring before the sequence start) and the warp's tokens, in the PlaneRaw form the conv reads.
+template <int KW>
+__device__ __forceinline__ void plane_from_stage(PlaneRaw<true, KW>& P, const RawStage<KW>& st,
+                                                 int pl, int t0, int kq, long pos0, int R,
+                                                 const float* ring_in, long ring_base) {
+#pragma unroll
+    for (int i = 0; i < kTokW; ++i)
+        P.cur[i] = *reinterpret_cast<const uint2*>(&st.v[pl][t0 + i + KW - 1][kq]);
+#pragma unroll
+    for (int m = 0; m < KW - 1; ++m) {
+        const int d = KW - 1 - m;
+        const long pos = pos0 - d;
+        float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        if (d <= R) {
+            if (pos >= 0) {
+                v = raw_unpack<true>(*reinterpret_cast<const uint2*>(&st.v[pl][t0 + m][kq]));
+            } else {
+                const long s2 = R + pos;
+                v = make_float4(ring_in[ring_base + s2], ring_in[ring_base + R + s2],
+                                ring_in[ring_base + 2 * R + s2], ring_in[ring_base + 3 * R + s2]);
+            }
+        }
+        P.halo[m] = v;
+    }
+}
+
+// Persistent: CTA b takes tasks b, b + gridDim.x, ... (task = head * nchunks + chunk).  With bf16
+// raw input the next task's raw rows are copied into shared memory while this task's MMA tail
+// runs (PF); f32 raw rows do not fit the free space and are loaded directly.
 template <bool BF16, int GATE_MODE, bool CONV, int KW>
 __global__ void __launch_bounds__(kThrF, 2)
-kda_chunk_prep_intra_kernel(PrepArgs p, ScanArgs a, const int* chunk_off, unsigned char* ws) {
+kda_chunk_prep_intra_kernel(PrepArgs p, ScanArgs a, const int* chunk_off, unsigned char* ws,
+                            long nchunks) {
+    constexpr bool PF = BF16;
     extern __shared__ unsigned char smem_raw[];
     IntraSmem& sm = *reinterpret_cast<IntraSmem*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+    RawStage<KW>& stage = *reinterpret_cast<RawStage<KW>*>(sm.bia[1]);
+    static_assert(sizeof(RawStage<KW>) <= sizeof(sm.bia[1]) + sizeof(sm.kb), "stage fits");
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int h = blockIdx.y;
-    const long gid = blockIdx.x;                 // global chunk index
     const int H = a.H;
     const long C = (long)H * kHeadDim;
-
-    int n;
-    if (a.seq.cu_seqlens == nullptr) {
-        n = (int)(gid / ((a.seq.T_uniform + kCc - 1) / kCc));
-    } else {
-        int lo = 0, hi = a.seq.N;                // largest n with chunk_off[n] <= gid
-        while (hi - lo > 1) {
-            const int mid = (lo + hi) >> 1;
-            if ((long)chunk_off[mid] <= gid) lo = mid; else hi = mid;
-        }
-        n = lo;
-    }
-    long begin, end;
-    seq_range(a.seq, n, begin, end);
-    const long c = gid - chunk_base(a.seq, chunk_off, n);
-    const long row0 = begin + c * kCc;
-    const int nt = (int)min((long)kCc, end - row0);
-    unsigned char* blk = ws + ((long)gid * H + h) * kBlkBytes;
+    const long ntasks = nchunks * H;
     const int kq = 4 * lane;                     // first of this lane's channels within the head
-    const long c4 = (long)h * kHeadDim + kq;     // ... within the plane
     const int t0 = kTokW * warp;                 // the warp's first token within the chunk
-    const int ntok = max(0, min(kTokW, nt - t0));
     const int K = p.K, R = p.K - 1;
 
-    // ---- loads: raw q, k, v with the conv halo, the gate input, beta ---------------------------
-    PlaneRaw<BF16, KW> rq, rk, rv;
-    {
-        const long pos0 = c * kCc + t0;
-        const long rr = (long)n * 3 * C * R;
-        plane_load<BF16, CONV, KW>(rq, p.q_raw, C, c4, begin, pos0, ntok, p.ring_in, rr + (0 * C + c4) * R, R);
-        plane_load<BF16, CONV, KW>(rk, p.k_raw, C, c4, begin, pos0, ntok, p.ring_in, rr + (1 * C + c4) * R, R);
-        plane_load<BF16, CONV, KW>(rv, p.v_raw, C, c4, begin, pos0, ntok, p.ring_in, rr + (2 * C + c4) * R, R);
+    if (warp == 0) {
+        tmem_alloc(&sm.tmem_base, 256);
+        tmem_relinquish();
     }
+    if (tid == 0) {
+        mbar_init(&sm.bar, 1);
+        fence_mbar_init();
+    }
+    uint32_t phase = 0;
+    if (PF && (long)blockIdx.x < ntasks) {
+        stage_raw<KW>(stage, p, a, chunk_off, blockIdx.x, nchunks);
+        if (GATE_MODE == 0) stage_f(sm.scr, p, a, chunk_off, blockIdx.x, nchunks);
+    }
+    __syncthreads();
+
+    for (long task = blockIdx.x; task < ntasks; task += gridDim.x) {
+    const long gid = task % nchunks;             // global chunk index
+    const int h = (int)(task / nchunks);
+    int n, nt;
+    long begin, end, row0;
+    chunk_task(a.seq, chunk_off, gid, n, begin, end, row0, nt);
+    const long c = (row0 - begin) / kCc;
+    unsigned char* blk = ws + ((long)gid * H + h) * kBlkBytes;
+    const long c4 = (long)h * kHeadDim + kq;     // this lane's first channel within the plane
+    const int ntok = max(0, min(kTokW, nt - t0));
+
+    // ---- loads: the gate input and beta; raw q, k, v (staged, or direct) -----------------------
     float4 fr[kTokW];
-    if (GATE_MODE == 0) {
+    if (GATE_MODE == 0 && !PF) {
 #pragma unroll
         for (int i = 0; i < kTokW; ++i)
             fr[i] = i < ntok ? __ldg(reinterpret_cast<const float4*>(p.f_raw + (row0 + t0 + i) * C + c4))
@@ -235,25 +345,45 @@ kda_chunk_prep_intra_kernel(PrepArgs p, ScanArgs a, const int* chunk_off, unsign
         if (GATE_MODE == 1)
             sm.gs[tid] = live ? gdn_gate_f(p.f_raw[(row0 + tid) * H + h], p.dt_bias[h], p.a_log[h]) : 0.0f;
     }
-    if (warp == 0) {
-        tmem_alloc(&sm.tmem_base, 256);
-        tmem_relinquish();
-    }
-    if (tid == 0) {
-        mbar_init(&sm.bar, 1);
-        fence_mbar_init();
+    const long pos0 = c * kCc + t0;
+    const long rr = (long)n * 3 * C * R;
+    PlaneRaw<BF16, KW> rq, rk, rv;               // direct loads (no staging)
+    if constexpr (PF) {
+        cp_async_wait_all();
+        __syncthreads();                         // every thread's pieces of the stage have landed
+        if (GATE_MODE == 0) {
+#pragma unroll
+            for (int i = 0; i < kTokW; ++i)
+                fr[i] = i < ntok ? *reinterpret_cast<const float4*>(&sm.scr[(t0 + i) * kHeadDim + kq])
+                                 : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        }
+    } else {
+        plane_load<BF16, CONV, KW>(rq, p.q_raw, C, c4, begin, pos0, ntok, p.ring_in, rr + (0 * C + c4) * R, R);
+        plane_load<BF16, CONV, KW>(rk, p.k_raw, C, c4, begin, pos0, ntok, p.ring_in, rr + (1 * C + c4) * R, R);
+        plane_load<BF16, CONV, KW>(rv, p.v_raw, C, c4, begin, pos0, ntok, p.ring_in, rr + (2 * C + c4) * R, R);
     }
 
     // ---- conv + SiLU; l2 norm of q and k over the head (one warp = one token group) ------------
     float v[kTokW][4], k[kTokW][4], q[kTokW][4];
     {
         float w[4][KW];
-        if constexpr (CONV) plane_weights<KW>(p.conv_w, 2 * C + c4, K, w);
-        plane_conv<BF16, CONV, KW>(rv, w, K, v);
-        if constexpr (CONV) plane_weights<KW>(p.conv_w, 1 * C + c4, K, w);
-        plane_conv<BF16, CONV, KW>(rk, w, K, k);
-        if constexpr (CONV) plane_weights<KW>(p.conv_w, 0 * C + c4, K, w);
-        plane_conv<BF16, CONV, KW>(rq, w, K, q);
+        if constexpr (PF) {                      // one plane's samples live at a time
+            const int Rr = CONV ? R : 0;
+#pragma unroll
+            for (int pl = 2; pl >= 0; --pl) {
+                PlaneRaw<true, KW> pr;
+                plane_from_stage<KW>(pr, stage, pl, t0, kq, pos0, Rr, p.ring_in, rr + (pl * C + c4) * R);
+                if constexpr (CONV) plane_weights<KW>(p.conv_w, pl * C + c4, K, w);
+                plane_conv<true, CONV, KW>(pr, w, K, pl == 2 ? v : (pl == 1 ? k : q));
+            }
+        } else {
+            if constexpr (CONV) plane_weights<KW>(p.conv_w, 2 * C + c4, K, w);
+            plane_conv<BF16, CONV, KW>(rv, w, K, v);
+            if constexpr (CONV) plane_weights<KW>(p.conv_w, 1 * C + c4, K, w);
+            plane_conv<BF16, CONV, KW>(rk, w, K, k);
+            if constexpr (CONV) plane_weights<KW>(p.conv_w, 0 * C + c4, K, w);
+            plane_conv<BF16, CONV, KW>(rq, w, K, q);
+        }
     }
     {
         float ss[2 * kTokW];
@@ -424,7 +554,18 @@ kda_chunk_prep_intra_kernel(PrepArgs p, ScanArgs a, const int* chunk_off, unsign
             put8x(blk + kOffQW, blk + kOffQW + kQWBytes, tc_offset(t, k0, kSbo128), xg);
         }
     }
-    intra_mma_tail<GATE_MODE, kThrF>(sm, a.err, blk);
+    const long next = task + gridDim.x;
+    const bool ok = intra_mma_tail<GATE_MODE, kThrF>(sm, a.err, blk, phase, [&]() {
+        if (PF && next < ntasks) stage_raw<KW>(stage, p, a, chunk_off, next, nchunks);
+    }, [&]() {
+        if (PF && GATE_MODE == 0 && next < ntasks) stage_f(sm.scr, p, a, chunk_off, next, nchunks);
+    });
+    if (!ok) break;
+    }   // task loop
+    if (PF) cp_async_wait_all();                 // no copy may land after the CTA has left
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(sm.tmem_base, 256);
 }
 
 template <bool BF16, int GM, bool CONV, int KW>
@@ -434,9 +575,15 @@ static cudaError_t launch_prep_intra_t(const PrepArgs& p, const ScanArgs& a, con
     static int done[64] = {0};
     cudaError_t e = set_smem(kda_chunk_prep_intra_kernel<BF16, GM, CONV, KW>, smem, done);
     if (e != cudaSuccess) return e;
-    dim3 grid((unsigned)nchunks, (unsigned)a.H);
+    int dev = 0, sms = 0;
+    e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    const long ntasks = nchunks * a.H;
+    const long ctas = min(ntasks, 2L * sms);     // two resident CTAs per SM, persistent
     KernelTimer kt(kKPrepIntra, s);
-    kda_chunk_prep_intra_kernel<BF16, GM, CONV, KW><<<grid, kThrF, smem, s>>>(p, a, chunk_off, blocks);
+    kda_chunk_prep_intra_kernel<BF16, GM, CONV, KW><<<(unsigned)ctas, kThrF, smem, s>>>(p, a, chunk_off, blocks,
+                                                                                      nchunks);
     return cudaGetLastError();
 }
 

@@ -219,7 +219,9 @@ kda_chunk_intra_kernel(ScanArgs a, const int* chunk_off, unsigned char* ws) {
         put8x(sm.bia[0], sm.bia[1], tc_offset(kCc + t, k0, kSbo128), xq);
         put8x(blk + kOffQW, blk + kOffQW + kQWBytes, tc_offset(t, k0, kSbo128), xg);
     }
-    intra_mma_tail<GATE_MODE, kThr>(sm, a.err, blk);
+    uint32_t phase = 0;
+    intra_mma_tail<GATE_MODE, kThr>(sm, a.err, blk, phase);
+    if (warp == 0) tmem_dealloc(sm.tmem_base, 256);
 }
 
 // ============================================================================================
