@@ -172,45 +172,69 @@ def _kernel_bytes(T, H, blk_bytes, chunks):
 
 
 def _prefill_e2e(args, d, buf, state_out, ring_out, stream, barrier, max_over_ranks, mixer,
-                 algo, ws, T, H, C, workspace, fused):
-    """Prefill through the public API with inputs copied from pinned host memory and y, the final
-    state and the ring read back every step."""
+                 algo, ws, T, H, C, workspace, fused, gate_mode):
+    """Prefill through the public API with every step's inputs copied from pinned host memory and
+    its y, final state and ring read back.  Fused path: mixer.HostPrefillStream, which overlaps
+    one step's host->device copy, the previous step's prefill and the device->host copy of the
+    one before on three streams (weights resident).  Sequential path: one stream, in order."""
     import torch
 
-    host = {k: v.cpu().pin_memory() for k, v in d.items() if v is not None}
-    dev_in = {k: torch.empty_like(v) for k, v in d.items() if v is not None}
-    y_host = torch.empty(T, C, dtype=torch.float32).pin_memory()
-    st_host = torch.empty_like(d["state_in"], device="cpu").pin_memory()
-    ring_host = torch.empty_like(d["ring_in"], device="cpu").pin_memory()
-    h2d_bytes = sum(v.numel() * v.element_size() for v in host.values())
-    d2h_bytes = sum(v.numel() * v.element_size() for v in (y_host, st_host, ring_host))
+    if fused:
+        host_in = {k: d[k].cpu().pin_memory() for k in mixer.HostPrefillStream.BATCH_KEYS}
+        host_out = dict(y=torch.empty(T, C, dtype=torch.float32).pin_memory(),
+                        state_out=torch.empty_like(host_in["state_in"]).pin_memory(),
+                        ring_out=torch.empty_like(host_in["ring_in"]).pin_memory())
+        pipe = mixer.HostPrefillStream(like=host_in, conv_w=d["conv_w"], dt_bias=d["dt_bias"],
+                                       a_log=d["a_log"], norm_w=d["norm_w"], H=H, N=1, T=T,
+                                       gate_mode=gate_mode)
+        h2d_bytes, d2h_bytes = pipe.h2d_bytes_per_batch, pipe.d2h_bytes_per_batch
 
-    def e2e_step():
-        for k, v in host.items():
-            dev_in[k].copy_(v, non_blocking=True)
-        if fused:
-            out = mixer.kda_prefill(H=H, N=1, T=T, state_out=state_out, ring_out=ring_out,
-                                    y=buf["y"], workspace=workspace, **dev_in)
-        else:
+        def e2e_step():
+            pipe.submit(host_in, host_out)
+
+        def e2e_start(ev):
+            ev.record(pipe.copy_in)
+
+        def e2e_stop(ev):
+            pipe.record_done(ev)
+    else:
+        host = {k: v.cpu().pin_memory() for k, v in d.items() if v is not None}
+        dev_in = {k: torch.empty_like(v) for k, v in d.items() if v is not None}
+        y_host = torch.empty(T, C, dtype=torch.float32).pin_memory()
+        st_host = torch.empty_like(d["state_in"], device="cpu").pin_memory()
+        ring_host = torch.empty_like(d["ring_in"], device="cpu").pin_memory()
+        h2d_bytes = sum(v.numel() * v.element_size() for v in host.values())
+        d2h_bytes = sum(v.numel() * v.element_size() for v in (y_host, st_host, ring_host))
+
+        def e2e_step():
+            for k, v in host.items():
+                dev_in[k].copy_(v, non_blocking=True)
             out = mixer.kda_forward(H=H, N=1, T=T, algo=algo, out=buf, state_out=state_out,
                                     ring_out=ring_out, workspace=workspace, **dev_in)
-        y_host.copy_(out["y"], non_blocking=True)
-        st_host.copy_(out["state_out"], non_blocking=True)
-        ring_host.copy_(out["ring_out"], non_blocking=True)
+            y_host.copy_(out["y"], non_blocking=True)
+            st_host.copy_(out["state_out"], non_blocking=True)
+            ring_host.copy_(out["ring_out"], non_blocking=True)
+
+        def e2e_start(ev):
+            ev.record(stream)
+
+        def e2e_stop(ev):
+            ev.record(stream)
 
     for _ in range(max(3, args.warmup // 4)):
         e2e_step()
     barrier()
     Ke = max(3, args.steps // 10)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
+    e2e_start(e0)
     for _ in range(Ke):
         e2e_step()
-    e1.record(stream)
+    e2e_stop(e1)
     barrier()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1)) / Ke
     return {"value": ws * T / (e2e_ms / 1e3), "unit": "tokens/s", "ms_per_step": e2e_ms,
-            "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes}
+            "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes,
+            "pipeline": ("three streams: copy-in, prefill, copy-out" if fused else "one stream")}
 
 
 def run_ours(args):
@@ -323,7 +347,7 @@ def run_ours(args):
     e2e = None
     if not args.skip_e2e:
         e2e = _prefill_e2e(args, d, buf, state_out, ring_out, stream, barrier, max_over_ranks,
-                           mixer, algo, ws, T, H, C, workspace, fused)
+                           mixer, algo, ws, T, H, C, workspace, fused, gate_mode)
 
     # ---------------- decode step (fused kernel) ----------------
     dec = inputs.decode_step(N=DEC_N, T=1, H=DEC_H)

@@ -130,3 +130,97 @@ def kda_decode(*, q_raw, k_raw, v_raw, conv_w, ring_in, f_raw, dt_bias, a_log, b
                          gate_mode=gate_mode, gate_lb=gate_lb, l2_eps=l2_eps, scale=scale,
                          rms_eps=rms_eps, stream=stream)
     return dict(y=y, state_out=state_out, ring_out=ring_out)
+
+
+class HostPrefillStream:
+    """Prefill over batches that live in pinned host memory, pipelined over three CUDA streams:
+    while batch i runs kda_prefill on the device, batch i+1 is copied in and the results of
+    batch i-1 are copied out (the host<->device link is full duplex, so the two copies overlap
+    each other as well as the kernels).  Every batch moves its own inputs and results; nothing is
+    cached between batches.
+
+    Layout: `slots` (default 2) device copies of the per-batch inputs and outputs, used in turn;
+    one prefill workspace, since the prefills run in order on one stream.  The weights (conv_w,
+    dt_bias, a_log, norm_w) are model parameters and stay resident on the device.
+    Fixed-length batches only: every batch has the N, T, H given here.
+
+    submit(host_in, host_out) queues one batch and returns at once.  host_in maps BATCH_KEYS to
+    pinned CPU tensors (ring_in only when the mixer has a conv); host_out maps y, state_out and
+    (with a conv) ring_out to pinned CPU tensors that receive the results.  Neither may be
+    touched by the host until synchronize() returns.  Ordering: a slot's inputs are overwritten
+    only after the prefill that read them finished, and its outputs only after they were copied
+    out (CUDA events on the streams; the host never blocks in submit)."""
+
+    BATCH_KEYS = ("q_raw", "k_raw", "v_raw", "f_raw", "beta_raw", "gate_raw", "state_in",
+                  "ring_in")
+
+    def __init__(self, *, like, conv_w, dt_bias, a_log, norm_w, H, N, T, K=4, gate_mode=0,
+                 gate_lb=-5.0, l2_eps=1e-6, rms_eps=1e-6, scale=None, slots=2):
+        dev = dt_bias.device
+        if dev.type != "cuda":
+            raise ValueError("HostPrefillStream: the weights must be CUDA tensors")
+        self.keys = tuple(k for k in self.BATCH_KEYS
+                          if not (k == "ring_in" and conv_w is None))
+        self.weights = dict(conv_w=conv_w, dt_bias=dt_bias, a_log=a_log, norm_w=norm_w)
+        self.params = dict(H=H, N=N, T=T, K=K, gate_mode=gate_mode, gate_lb=gate_lb,
+                           l2_eps=l2_eps, rms_eps=rms_eps, scale=scale)
+        rows, C = N * T, H * kda.HEAD_DIM
+        self.slots = []
+        for _ in range(slots):
+            din = {k: torch.empty(like[k].shape, dtype=like[k].dtype, device=dev)
+                   for k in self.keys}
+            dout = dict(y=torch.empty(rows, C, dtype=torch.float32, device=dev),
+                        state_out=torch.empty_like(din["state_in"]))
+            if conv_w is not None:
+                dout["ring_out"] = torch.empty_like(din["ring_in"])
+            self.slots.append((din, dout, dict(copied=torch.cuda.Event(),
+                                               ran=torch.cuda.Event(),
+                                               drained=torch.cuda.Event())))
+        self.workspace = kda.prefill_workspace(N, rows, H, dev, gate_mode)
+        self.copy_in = torch.cuda.Stream(dev)
+        self.run = torch.cuda.Stream(dev)
+        self.copy_out = torch.cuda.Stream(dev)
+        self.submitted = 0
+
+    @property
+    def h2d_bytes_per_batch(self) -> int:
+        din = self.slots[0][0]
+        return sum(t.numel() * t.element_size() for t in din.values())
+
+    @property
+    def d2h_bytes_per_batch(self) -> int:
+        dout = self.slots[0][1]
+        return sum(t.numel() * t.element_size() for t in dout.values())
+
+    def submit(self, host_in, host_out):
+        din, dout, ev = self.slots[self.submitted % len(self.slots)]
+        reused = self.submitted >= len(self.slots)
+        if reused:                          # the slot's previous prefill has read its inputs
+            self.copy_in.wait_event(ev["ran"])
+        with torch.cuda.stream(self.copy_in):
+            for k in self.keys:
+                din[k].copy_(host_in[k], non_blocking=True)
+        ev["copied"].record(self.copy_in)
+        self.run.wait_event(ev["copied"])
+        if reused:                          # the slot's previous results have been copied out
+            self.run.wait_event(ev["drained"])
+        kda_prefill(**{"ring_in": None, **din}, **self.weights, **self.params, y=dout["y"],
+                    state_out=dout["state_out"], ring_out=dout.get("ring_out"),
+                    workspace=self.workspace, stream=self.run)
+        ev["ran"].record(self.run)
+        self.copy_out.wait_event(ev["ran"])
+        with torch.cuda.stream(self.copy_out):
+            for k, t in dout.items():
+                host_out[k].copy_(t, non_blocking=True)
+        ev["drained"].record(self.copy_out)
+        self.submitted += 1
+
+    def record_done(self, event):
+        """Record `event` on the copy-out stream: it completes once every batch submitted so far
+        has been copied in, run and copied out."""
+        event.record(self.copy_out)
+
+    def synchronize(self):
+        self.copy_out.synchronize()
+        self.run.synchronize()
+        self.copy_in.synchronize()
