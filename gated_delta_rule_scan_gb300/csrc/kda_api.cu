@@ -197,6 +197,10 @@ int prefill_impl(const void* q_raw, const void* k_raw, const void* v_raw, int ra
                         a_log, gate_mode, gate_lb, beta_raw, nullptr, nullptr, nullptr, nullptr,
                         nullptr, seq, H, D, K, l2_eps, false, pa);
     if (rc != KDA_OK) return rc;
+    // the fused kernel copies bf16 raw rows into shared memory 16 bytes at a time
+    if (seq.total_rows > 0 && pa.raw_bf16 &&
+        (!aligned16(q_raw) || !aligned16(k_raw) || !aligned16(v_raw)))
+        return KDA_ERR_ALIGN;
     if (!state_in || !state_out) return KDA_ERR_NULL;
     if (!aligned16(state_in) || !aligned16(state_out)) return KDA_ERR_ALIGN;
     if (overlap(state_in, state_out, (size_t)seq.N * H * kHeadDim * kHeadDim * sizeof(float)))

@@ -1,19 +1,23 @@
 // kda_chunk_prep.cu -- the fused prefill's first kernel: stages 2-4 of kda_core_gated (conv +
 // SiLU, l2 norm, gates, beta; "memra_engine/kda.rs", memra-engine 0.125.0) computed straight
-// into the chunked form's intra-chunk operand images, one CTA per (32-token chunk, head), so the
-// prepared q, k, v and gate planes never reach memory.  From the images on, the CTA runs the same
-// MMA tail as the chunked scan's intra kernel (kda_chunk_common.cuh).
+// into the chunked form's intra-chunk operand images, so the prepared q, k, v and gate planes never
+// reach memory.  Persistent CTAs (two per SM) loop over (32-token chunk, head) tasks; from the
+// images on, a task runs the same MMA tail as the chunked scan's intra kernel
+// (kda_chunk_common.cuh), and while it runs the next task's inputs are copied into shared memory.
 //
-// Layout: 256 threads; warp w takes tokens 4w .. 4w+3 of the chunk and lane l channels 4l .. 4l+3 of the head,
-// the prep kernel's lane-to-channel map, so every per-token quantity is computed with the prep's
-// arithmetic: conv taps oldest first over a window that starts K-1 samples back (from the ring
-// for the first chunk of a sequence), SiLU, the l2 sum of squares reduced over the warp (a
-// transposed butterfly that adds the same pairs as the prep's per-row butterfly), gates and beta.
-// The column images (consecutive tokens of one channel) are written from a thread's registers
-// as 8-byte half rows of their 16-byte core-matrix rows; the row images (8 consecutive channels
-// of one token) pair lane l with l^1 by shuffles.  The per-channel running sum of the gate passes from warp to warp through shared
-// memory in token order, the order of the chunked scan's own intra kernel.  The output blocks
-// therefore equal those of the prep kernel followed by the intra kernel bit for bit.
+// Layout: 256 threads; warp w takes tokens 4w .. 4w+3 of the chunk and lane l channels 4l .. 4l+3
+// of the head, the prep kernel's lane-to-channel map, so every per-token quantity is computed
+// with the prep's arithmetic: conv taps oldest first over a window that starts K-1 samples back
+// (from the ring for the first chunk of a sequence), SiLU, the l2 sum of squares reduced over the
+// warp (a transposed butterfly that adds the same pairs as the prep's per-row butterfly), gates
+// and beta.  The column images (consecutive tokens of one channel) are written from a thread's
+// registers as 8-byte half rows of their 16-byte core-matrix rows; the row images (8 consecutive
+// channels of one token) pair lane l with l^1 by shuffles.  The per-channel running sum of the
+// gate passes from warp to warp through shared memory in token order, the order of the chunked
+// scan's own intra kernel.  The output blocks therefore equal those of the prep kernel followed
+// by the intra kernel bit for bit.
+#include <cstring>
+
 #include "kda_chunk_common.cuh"
 
 namespace kda {
@@ -59,7 +63,7 @@ __device__ __forceinline__ float f4c(const float4& v, int e) {
 }
 
 // One plane's raw samples for this lane's 4 channels: the KW-1 samples before the warp's first
-// token (halo, f32) and the warp's 8 tokens (raw, packed).
+// token (halo, f32) and the warp's 4 tokens (raw, packed).
 template <bool BF16, int KW>
 struct PlaneRaw {
     float4 halo[KW - 1];
@@ -95,7 +99,7 @@ __device__ __forceinline__ void plane_load(PlaneRaw<BF16, KW>& P, const void* ra
     }
 }
 
-// conv + SiLU of one plane for the warp's 8 tokens (or the raw samples without a conv).
+// conv + SiLU of one plane for the warp's 4 tokens (or the raw samples without a conv).
 template <bool BF16, bool CONV, int KW>
 __device__ __forceinline__ void plane_conv(const PlaneRaw<BF16, KW>& P, const float (&w)[4][KW],
                                            int K, float (&y)[kTokW][4]) {
@@ -118,6 +122,18 @@ __device__ __forceinline__ void plane_conv(const PlaneRaw<BF16, KW>& P, const fl
                 y[i][e] = f4c(cur[i], e);
             }
         }
+    }
+}
+
+// The staged (transposed) weights of channels kq .. kq+3: one 16-byte load per tap.
+template <int KW>
+__device__ __forceinline__ void plane_weights_t(const float* wt, int kq, int K, float (&w)[4][KW]) {
+#pragma unroll
+    for (int m = 0; m < KW; ++m) {
+        const int j = m - (KW - K);
+        const float4 x = j >= 0 ? *reinterpret_cast<const float4*>(wt + j * kHeadDim + kq)
+                                : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        w[0][m] = x.x; w[1][m] = x.y; w[2][m] = x.z; w[3][m] = x.w;
     }
 }
 
@@ -155,8 +171,8 @@ __device__ __forceinline__ float warp_sum8(float (&x)[8]) {
 // the chunk of global index gid: its sequence n and rows, the chunk's first row and its tokens
 __device__ __forceinline__ void chunk_task(const SeqLayout& L, const int* chunk_off, long gid,
                                            int& n, long& begin, long& end, long& row0, int& nt) {
-    if (L.cu_seqlens == nullptr) {
-        n = (int)(gid / ((L.T_uniform + kCc - 1) / kCc));
+    if (L.cu_seqlens == nullptr) {          // gid < 2^31 (host check)
+        n = (int)((unsigned)gid / (unsigned)((L.T_uniform + kCc - 1) / kCc));
     } else {
         int lo = 0, hi = L.N;                    // largest n with chunk_off[n] <= gid
         while (hi - lo > 1) {
@@ -168,6 +184,23 @@ __device__ __forceinline__ void chunk_task(const SeqLayout& L, const int* chunk_
     seq_range(L, n, begin, end);
     row0 = begin + (gid - chunk_base(L, chunk_off, n)) * kCc;
     nt = (int)min((long)kCc, end - row0);
+}
+
+// A task of the persistent kernel: (global chunk gid, head h), task = h * nchunks + gid, and the
+// chunk's sequence n, rows and token count.  The host keeps h * nchunks + gid below 2^31.
+struct TaskPos {
+    long begin, end, row0, gid;
+    int n, h, nt;
+};
+
+__device__ __forceinline__ TaskPos task_pos(const SeqLayout& L, const int* chunk_off, long task,
+                                            long nchunks) {
+    TaskPos t;
+    const unsigned tk = (unsigned)task, nc = (unsigned)nchunks;
+    t.h = (int)(tk / nc);
+    t.gid = (long)(tk - (unsigned)t.h * nc);
+    chunk_task(L, chunk_off, t.gid, t.n, t.begin, t.end, t.row0, t.nt);
+    return t;
 }
 
 __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
@@ -213,46 +246,84 @@ __device__ __forceinline__ void pair_rows(const float (&x)[kTokW][4], float (&ro
         }
 }
 
-// Issue the cp.async copies of task `task`'s raw q, k, v rows (the chunk's tokens and its conv
-// halo inside the sequence) into the stage; every thread takes a share of the 16-byte pieces.
+// Tensor maps of the raw rows: q, k, v [rows, C] bf16 with a [kRows, 128] box, and (KDA) the
+// gate input f [rows, C] f32 with a [32, 128] box.
+struct RawMaps {
+    CUtensorMap q, k, v, f;
+};
+
+// Issued by one thread: TMA tile loads of task tp's raw q, k, v rows (the chunk's tokens and the
+// KW-1 rows before them) into the stage, counted on bar.  Rows before the tensor or past its end
+// read as zeros; rows of a neighbouring sequence are loaded but never read (the conv takes the
+// halo from the ring before the sequence start, and tokens past the chunk end are masked).
 template <int KW>
-__device__ __forceinline__ void stage_raw(RawStage<KW>& st, const PrepArgs& p, const ScanArgs& a,
-                                          const int* chunk_off, long task, long nchunks) {
-    const long gid = task % nchunks;
-    const int h = (int)(task / nchunks);
-    int n, nt;
-    long begin, end, row0;
-    chunk_task(a.seq, chunk_off, gid, n, begin, end, row0, nt);
-    const long C = (long)a.H * kHeadDim;
-    const long pos_c = row0 - begin;             // position of the chunk's first token
-    constexpr int kPieces = 3 * RawStage<KW>::kRows * (kHeadDim / 8);
-    for (int idx = threadIdx.x; idx < kPieces; idx += kThrF) {
-        const int pl = idx / (RawStage<KW>::kRows * 16);
-        const int r = (idx / 16) % RawStage<KW>::kRows;
-        const int j = idx % 16;
-        const int t = r - (KW - 1);
-        if (t < nt && pos_c + t >= 0) {
-            const void* raw = pl == 0 ? p.q_raw : (pl == 1 ? p.k_raw : p.v_raw);
-            cp_async16(&st.v[pl][r][8 * j],
-                       reinterpret_cast<const __nv_bfloat16*>(raw) + (row0 + t) * C + (long)h * kHeadDim + 8 * j);
-        }
-    }
-    cp_async_commit();
+__device__ __forceinline__ void stage_raw(RawStage<KW>& st, const RawMaps& m, const TaskPos& tp,
+                                          uint64_t* bar) {
+    mbar_arrive_expect_tx(bar, 3u * RawStage<KW>::kRows * kHeadDim * sizeof(__nv_bfloat16));
+    const int x = tp.h * kHeadDim, y = (int)tp.row0 - (KW - 1);
+    tma_load_2d(&st.v[0][0][0], &m.q, x, y, bar);
+    tma_load_2d(&st.v[1][0][0], &m.k, x, y, bar);
+    tma_load_2d(&st.v[2][0][0], &m.v, x, y, bar);
 }
 
-// Issue the cp.async copies of task `task`'s gate-input rows (KDA: [32 tokens][128] f32) into
-// sm.scr, free from the end of one task's Tm image to the next task's gate step.
-__device__ __forceinline__ void stage_f(float* dst, const PrepArgs& p, const ScanArgs& a,
-                                        const int* chunk_off, long task, long nchunks) {
-    const long gid = task % nchunks;
-    const int h = (int)(task / nchunks);
-    int n, nt;
-    long begin, end, row0;
-    chunk_task(a.seq, chunk_off, gid, n, begin, end, row0, nt);
-    const long C = (long)a.H * kHeadDim;
-    for (int idx = threadIdx.x; idx < kCc * (kHeadDim / 4); idx += kThrF) {
-        const int t = idx / (kHeadDim / 4), j = idx % (kHeadDim / 4);
-        if (t < nt) cp_async16(dst + t * kHeadDim + 4 * j, p.f_raw + (row0 + t) * C + (long)h * kHeadDim + 4 * j);
+// Issued by one thread: the TMA tile load of task tp's gate-input rows (KDA: [32 tokens][128]
+// f32) into sm.scr, free from the end of one task's Tm image to the next task's gate step.
+__device__ __forceinline__ void stage_f(float* dst, const RawMaps& m, const TaskPos& tp,
+                                        uint64_t* bar) {
+    mbar_arrive_expect_tx(bar, kCc * kHeadDim * sizeof(float));
+    tma_load_2d(dst, &m.f, tp.h * kHeadDim, (int)tp.row0, bar);
+}
+
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)),
+                 "l"(reinterpret_cast<uint64_t>(src))
+                 : "memory");
+}
+
+// Staged small inputs of one task: the head's conv weights (K <= 4 taps, transposed to
+// [plane][tap][channel] so a lane reads its 4 channels' tap as one conflict-free 16-byte load),
+// dt_bias (KDA: the head's 128 channels; GDN: one value), A_log of the head, and the chunk's raw
+// beta and (GDN) gate inputs.  Filled during the previous task's MMA tail, so that the front half
+// waits on no global load; a region of its own, read only by the front half.
+struct ParamStage {
+    float w[3][4 * kHeadDim];
+    float dt[kHeadDim];
+    float braw[kCc];
+    float fraw[kCc];
+    float alog;
+};
+
+struct __align__(128) PrepIntraSmem {
+    IntraSmem in;
+    ParamStage ps;
+    uint64_t bar_raw, bar_f;                     // TMA completion of the raw rows, the gate input
+};
+// two resident CTAs per SM: 228 KB of shared memory per SM, 1 KB of it reserved per CTA
+static_assert(2 * (sizeof(PrepIntraSmem) + 128 + 1024) <= 228 * 1024, "two CTAs per SM");
+
+// Issue the cp.async copies of task tp's small inputs into the parameter stage.
+template <int GATE_MODE, bool CONV>
+__device__ __forceinline__ void stage_params(ParamStage& ps, const PrepArgs& p, int H, long C,
+                                             const TaskPos& tp) {
+    const int tid = threadIdx.x, h = tp.h, nt = tp.nt;
+    const long row0 = tp.row0;
+    if constexpr (CONV) {
+        const int K = p.K, per = kHeadDim * K;   // one plane's rows of this head, contiguous
+        for (int idx = tid; idx < 3 * per; idx += kThrF) {
+            const int pl = idx / per, r = idx - pl * per;
+            const int ch = K == 4 ? r >> 2 : r / K, j = r - ch * K;
+            cp_async4(&ps.w[pl][j * kHeadDim + ch], p.conv_w + (pl * C + (long)h * kHeadDim) * K + r);
+        }
+    }
+    if (GATE_MODE == 0) {
+        if (tid < kHeadDim / 4) cp_async16(&ps.dt[4 * tid], p.dt_bias + (long)h * kHeadDim + 4 * tid);
+    } else if (tid == kThrF - 1) {
+        cp_async4(&ps.dt[0], p.dt_bias + h);
+    }
+    if (tid == kThrF - 2) cp_async4(&ps.alog, p.a_log + h);
+    if (tid < nt) {
+        cp_async4(&ps.braw[tid], p.beta_raw + (row0 + tid) * H + h);
+        if (GATE_MODE == 1) cp_async4(&ps.fraw[tid], p.f_raw + (row0 + tid) * H + h);
     }
     cp_async_commit();
 }
@@ -285,16 +356,20 @@ __device__ __forceinline__ void plane_from_stage(PlaneRaw<true, KW>& P, const Ra
 }
 
 // Persistent: CTA b takes tasks b, b + gridDim.x, ... (task = head * nchunks + chunk).  With bf16
-// raw input the next task's raw rows are copied into shared memory while this task's MMA tail
-// runs (PF); f32 raw rows do not fit the free space and are loaded directly.
+// raw input the next task's raw rows, gate input and small inputs are copied into shared memory
+// while this task's MMA tail runs (PF); f32 raw rows do not fit the free space and are loaded
+// directly, as are conv weights of more than 4 taps.
 template <bool BF16, int GATE_MODE, bool CONV, int KW>
 __global__ void __launch_bounds__(kThrF, 2)
 kda_chunk_prep_intra_kernel(PrepArgs p, ScanArgs a, const int* chunk_off, unsigned char* ws,
-                            long nchunks) {
+                            long nchunks, const __grid_constant__ RawMaps maps) {
     constexpr bool PF = BF16;
+    constexpr bool PW = PF && CONV && KW <= 4;   // conv weights from the parameter stage
     extern __shared__ unsigned char smem_raw[];
-    IntraSmem& sm = *reinterpret_cast<IntraSmem*>(
+    PrepIntraSmem& smf = *reinterpret_cast<PrepIntraSmem*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+    IntraSmem& sm = smf.in;
+    ParamStage& ps = smf.ps;
     RawStage<KW>& stage = *reinterpret_cast<RawStage<KW>*>(sm.bia[1]);
     static_assert(sizeof(RawStage<KW>) <= sizeof(sm.bia[1]) + sizeof(sm.kb), "stage fits");
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -311,21 +386,30 @@ kda_chunk_prep_intra_kernel(PrepArgs p, ScanArgs a, const int* chunk_off, unsign
     }
     if (tid == 0) {
         mbar_init(&sm.bar, 1);
+        mbar_init(&smf.bar_raw, 1);
+        mbar_init(&smf.bar_f, 1);
         fence_mbar_init();
     }
-    uint32_t phase = 0;
+    uint32_t phase = 0, ph_ld = 0;               // MMA commits; staged loads (one per task)
+    bool ld_pending = false;                     // a task's loads issued and not yet waited on
     if (PF && (long)blockIdx.x < ntasks) {
-        stage_raw<KW>(stage, p, a, chunk_off, blockIdx.x, nchunks);
-        if (GATE_MODE == 0) stage_f(sm.scr, p, a, chunk_off, blockIdx.x, nchunks);
+        const TaskPos tp = task_pos(a.seq, chunk_off, blockIdx.x, nchunks);
+        if (tid == 0) {
+            prefetch_tensormap(&maps.q);
+            prefetch_tensormap(&maps.k);
+            prefetch_tensormap(&maps.v);
+            stage_raw<KW>(stage, maps, tp, &smf.bar_raw);
+            if (GATE_MODE == 0) stage_f(sm.scr, maps, tp, &smf.bar_f);
+        }
+        stage_params<GATE_MODE, PW>(ps, p, H, C, tp);
     }
     __syncthreads();
 
     for (long task = blockIdx.x; task < ntasks; task += gridDim.x) {
-    const long gid = task % nchunks;             // global chunk index
-    const int h = (int)(task / nchunks);
-    int n, nt;
-    long begin, end, row0;
-    chunk_task(a.seq, chunk_off, gid, n, begin, end, row0, nt);
+    const TaskPos tp = task_pos(a.seq, chunk_off, task, nchunks);
+    const long gid = tp.gid;                     // global chunk index
+    const int h = tp.h, n = tp.n, nt = tp.nt;
+    const long begin = tp.begin, row0 = tp.row0;
     const long c = (row0 - begin) / kCc;
     unsigned char* blk = ws + ((long)gid * H + h) * kBlkBytes;
     const long c4 = (long)h * kHeadDim + kq;     // this lane's first channel within the plane
@@ -339,7 +423,7 @@ kda_chunk_prep_intra_kernel(PrepArgs p, ScanArgs a, const int* chunk_off, unsign
             fr[i] = i < ntok ? __ldg(reinterpret_cast<const float4*>(p.f_raw + (row0 + t0 + i) * C + c4))
                              : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
     }
-    if (tid < kCc) {
+    if (!PF && tid < kCc) {
         const bool live = tid < nt;
         sm.beta[tid] = live ? sigmoid_f(p.beta_raw[(row0 + tid) * H + h]) : 0.0f;
         if (GATE_MODE == 1)
@@ -349,8 +433,18 @@ kda_chunk_prep_intra_kernel(PrepArgs p, ScanArgs a, const int* chunk_off, unsign
     const long rr = (long)n * 3 * C * R;
     PlaneRaw<BF16, KW> rq, rk, rv;               // direct loads (no staging)
     if constexpr (PF) {
+        bool ld_ok = mbar_wait_bounded(&smf.bar_raw, ph_ld, a.err);
+        if (GATE_MODE == 0) ld_ok = mbar_wait_bounded(&smf.bar_f, ph_ld, a.err) && ld_ok;
+        ph_ld ^= 1u;
+        ld_pending = false;
         cp_async_wait_all();
-        __syncthreads();                         // every thread's pieces of the stage have landed
+        if (__syncthreads_or(!ld_ok)) break;     // every piece of the stage has landed
+        if (tid < kCc) {
+            const bool live = tid < nt;
+            sm.beta[tid] = live ? sigmoid_f(ps.braw[tid]) : 0.0f;
+            if (GATE_MODE == 1)
+                sm.gs[tid] = live ? gdn_gate_f(ps.fraw[tid], ps.dt[0], ps.alog) : 0.0f;
+        }
         if (GATE_MODE == 0) {
 #pragma unroll
             for (int i = 0; i < kTokW; ++i)
@@ -373,7 +467,8 @@ kda_chunk_prep_intra_kernel(PrepArgs p, ScanArgs a, const int* chunk_off, unsign
             for (int pl = 2; pl >= 0; --pl) {
                 PlaneRaw<true, KW> pr;
                 plane_from_stage<KW>(pr, stage, pl, t0, kq, pos0, Rr, p.ring_in, rr + (pl * C + c4) * R);
-                if constexpr (CONV) plane_weights<KW>(p.conv_w, pl * C + c4, K, w);
+                if constexpr (PW) plane_weights_t<KW>(ps.w[pl], kq, K, w);
+                else if constexpr (CONV) plane_weights<KW>(p.conv_w, pl * C + c4, K, w);
                 plane_conv<true, CONV, KW>(pr, w, K, pl == 2 ? v : (pl == 1 ? k : q));
             }
         } else {
@@ -415,8 +510,9 @@ kda_chunk_prep_intra_kernel(PrepArgs p, ScanArgs a, const int* chunk_off, unsign
     float G[kTokW][4];
     float GCh = 0.0f;                            // per-head gate: the chunk's total
     if (GATE_MODE == 0) {
-        const float rate = expf(p.a_log[h]);
-        const float4 dt = *reinterpret_cast<const float4*>(p.dt_bias + c4);
+        const float rate = expf(PF ? ps.alog : p.a_log[h]);
+        const float4 dt = PF ? *reinterpret_cast<const float4*>(&ps.dt[kq])
+                             : *reinterpret_cast<const float4*>(p.dt_bias + c4);
         const float dtv[4] = {dt.x, dt.y, dt.z, dt.w};
         float g[kTokW][4];
 #pragma unroll
@@ -556,12 +652,22 @@ kda_chunk_prep_intra_kernel(PrepArgs p, ScanArgs a, const int* chunk_off, unsign
     }
     const long next = task + gridDim.x;
     const bool ok = intra_mma_tail<GATE_MODE, kThrF>(sm, a.err, blk, phase, [&]() {
-        if (PF && next < ntasks) stage_raw<KW>(stage, p, a, chunk_off, next, nchunks);
+        if (PF && next < ntasks) {
+            const TaskPos np = task_pos(a.seq, chunk_off, next, nchunks);
+            ld_pending = true;
+            if (tid == 0) stage_raw<KW>(stage, maps, np, &smf.bar_raw);
+            stage_params<GATE_MODE, PW>(ps, p, H, C, np);
+        }
     }, [&]() {
-        if (PF && GATE_MODE == 0 && next < ntasks) stage_f(sm.scr, p, a, chunk_off, next, nchunks);
+        if (PF && GATE_MODE == 0 && next < ntasks && tid == 0)
+            stage_f(sm.scr, maps, task_pos(a.seq, chunk_off, next, nchunks), &smf.bar_f);
     });
     if (!ok) break;
     }   // task loop
+    if (PF && ld_pending) {                      // left early: let the next task's loads land
+        mbar_wait_bounded(&smf.bar_raw, ph_ld, a.err);
+        if (GATE_MODE == 0) mbar_wait_bounded(&smf.bar_f, ph_ld, a.err);
+    }
     if (PF) cp_async_wait_all();                 // no copy may land after the CTA has left
     tc_fence_before();
     __syncthreads();
@@ -571,7 +677,7 @@ kda_chunk_prep_intra_kernel(PrepArgs p, ScanArgs a, const int* chunk_off, unsign
 template <bool BF16, int GM, bool CONV, int KW>
 static cudaError_t launch_prep_intra_t(const PrepArgs& p, const ScanArgs& a, const int* chunk_off,
                                        unsigned char* blocks, long nchunks, cudaStream_t s) {
-    const size_t smem = sizeof(IntraSmem) + 128;
+    const size_t smem = sizeof(PrepIntraSmem) + 128;
     static int done[64] = {0};
     cudaError_t e = set_smem(kda_chunk_prep_intra_kernel<BF16, GM, CONV, KW>, smem, done);
     if (e != cudaSuccess) return e;
@@ -580,10 +686,22 @@ static cudaError_t launch_prep_intra_t(const PrepArgs& p, const ScanArgs& a, con
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
     const long ntasks = nchunks * a.H;
+    if (ntasks >= (1L << 31)) return cudaErrorInvalidValue;   // tasks split with 32-bit division
     const long ctas = min(ntasks, 2L * sms);     // two resident CTAs per SM, persistent
+    RawMaps maps;
+    std::memset(&maps, 0, sizeof(maps));
+    if (BF16) {                                  // the staged form reads through tensor maps
+        const long rows = a.seq.total_rows, C = (long)a.H * kHeadDim;
+        constexpr int kRows = RawStage<KW>::kRows;
+        if (!make_tensor_map_2d_any(&maps.q, p.q_raw, true, rows, C, kHeadDim, kRows) ||
+            !make_tensor_map_2d_any(&maps.k, p.k_raw, true, rows, C, kHeadDim, kRows) ||
+            !make_tensor_map_2d_any(&maps.v, p.v_raw, true, rows, C, kHeadDim, kRows) ||
+            (GM == 0 && !make_tensor_map_2d_any(&maps.f, p.f_raw, false, rows, C, kHeadDim, kCc)))
+            return cudaErrorInvalidValue;
+    }
     KernelTimer kt(kKPrepIntra, s);
-    kda_chunk_prep_intra_kernel<BF16, GM, CONV, KW><<<(unsigned)ctas, kThrF, smem, s>>>(p, a, chunk_off, blocks,
-                                                                                      nchunks);
+    kda_chunk_prep_intra_kernel<BF16, GM, CONV, KW><<<(unsigned)ctas, kThrF, smem, s>>>(
+        p, a, chunk_off, blocks, nchunks, maps);
     return cudaGetLastError();
 }
 

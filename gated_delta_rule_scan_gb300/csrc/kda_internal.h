@@ -86,6 +86,9 @@ constexpr size_t kChunkBlockBytes = 70144;  // workspace bytes per (chunk, head)
 // 2-D f32 tensor map over [rows, cols] (row stride = cols), box [box_rows, box_cols], no swizzle.
 bool make_tensor_map_2d(CUtensorMap* m, const float* base, long rows, long cols, int box_cols,
                         int box_rows);
+// The same over bf16 (bf16 = true) or f32 elements.
+bool make_tensor_map_2d_any(CUtensorMap* m, const void* base, bool bf16, long rows, long cols,
+                            int box_cols, int box_rows);
 cudaError_t launch_gated_rmsnorm(const NormArgs& a, cudaStream_t s);
 cudaError_t launch_decode_fused(const DecodeArgs& a, cudaStream_t s);
 

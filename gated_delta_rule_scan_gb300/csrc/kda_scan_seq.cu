@@ -178,18 +178,24 @@ static EncodeTiledFn encode_fn() {
     return fn;
 }
 
-bool make_tensor_map_2d(CUtensorMap* m, const float* base, long rows, long cols, int box_cols,
-                        int box_rows) {
+bool make_tensor_map_2d_any(CUtensorMap* m, const void* base, bool bf16, long rows, long cols,
+                            int box_cols, int box_rows) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
+    const size_t es_bytes = bf16 ? 2 : 4;
     cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)cols * sizeof(float)};
+    cuuint64_t strides[1] = {(cuuint64_t)cols * es_bytes};
     cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
     cuuint32_t es[2] = {1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims, strides, box,
-              es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
-           CUDA_SUCCESS;
+    return fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
+              const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool make_tensor_map_2d(CUtensorMap* m, const float* base, long rows, long cols, int box_cols,
+                        int box_rows) {
+    return make_tensor_map_2d_any(m, base, false, rows, cols, box_cols, box_rows);
 }
 
 template <int GM, bool EXP>

@@ -237,8 +237,9 @@ size_t kda_prefill_workspace_bytes(int N, int total_T, int H, int D, int gate_mo
  * kda_gated_rmsnorm_out with the same arguments.  The prepared q, k, v and gates are computed
  * inside the chunked scan's first kernel and never reach memory; the readout passes through the
  * workspace on its way to the RMSNorm.
- * Arguments and layouts as in those three calls; gate_mode is KDA_GATE_PER_CHANNEL or
- * KDA_GATE_PER_HEAD (the KDA_GATE_EXP flag is not accepted, 40007); norm_w [D] f32 [16B];
+ * Arguments and layouts as in those three calls, except that bf16 q_raw, k_raw and v_raw must be
+ * [16B] here (40010 otherwise; the staged prep needs 8 bytes); gate_mode is KDA_GATE_PER_CHANNEL
+ * or KDA_GATE_PER_HEAD (the KDA_GATE_EXP flag is not accepted, 40007); norm_w [D] f32 [16B];
  * gate_raw and y [N*T, C] f32 [16B].  The chunked form's range condition applies (every
  * 32-token chunk's total log-decay above -170 per channel, else kda_device_status reports 40008).
  * workspace   device scratch [16B] of at least kda_prefill_workspace_bytes(...) bytes (40009

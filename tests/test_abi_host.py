@@ -108,6 +108,22 @@ def test_prep_and_decode_contract(kda):
     assert norm == 40010
 
 
+def test_prefill_contract(kda):
+    """kda_prefill_fused takes bf16 raw rows only at 16-byte alignment (the staged prep accepts
+    8), and refuses the decay-factor gate flag, before any device call."""
+    lib = kda.library()
+    F = ctypes.c_float
+
+    def call(q=FAKE, gm=0, dtype=1):
+        return lib.kda_prefill_fused(q, FAKE, FAKE, dtype, FAKE, FAKE, FAKE * 2, FAKE, FAKE, FAKE,
+                                     gm, F(-5.0), FAKE, FAKE, FAKE * 4, FAKE, FAKE, FAKE, 1, 64, 2,
+                                     128, 4, F(1e-6), F(0.1), F(1e-6), FAKE, 0, None)
+    assert call(q=FAKE + 8) == 40010
+    assert call(q=FAKE + 8, dtype=0) == 40010
+    assert call(gm=2) == 40007
+    assert call() == 40009          # aligned and valid up to the (zero-byte) workspace
+
+
 def test_static_scan_contract(kda):
     """kda_scan_varlen_static refuses, before any device call, a problem whose chunked scratch
     exceeds KDA_STATIC_SCRATCH_BYTES, besides kda_scan_varlen's own contract."""

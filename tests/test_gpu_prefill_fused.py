@@ -79,6 +79,19 @@ def test_prefill_fused_gdn():
     _check(gpu_prefill(inp), inp)
 
 
+@pytest.mark.parametrize("raw,gate_mode,conv,K", [("bf16", 1, True, 4), ("bf16", 0, True, 6),
+                                                  ("bf16", 1, False, 4), ("f32", 0, True, 4),
+                                                  ("bf16", 0, True, 2)])
+def test_prefill_fused_variants(raw, gate_mode, conv, K):
+    """Each kernel variant: bf16 raw rows staged in shared memory (with the conv weights for up
+    to 4 taps, loaded directly for more) or f32 rows loaded directly; per-channel or per-head
+    gate; with or without the conv.  Many chunks per sequence, so every persistent CTA runs
+    several tasks and stages the next one's inputs."""
+    inp = inputs.make_inputs(90 + K, H=5, N=3, T=333, K=K, raw_dtype=raw, conv=conv,
+                             ring="randn", gate_mode=gate_mode, state="randn", epilogue=True)
+    _check(gpu_prefill(inp), inp)
+
+
 @pytest.mark.slow
 def test_prefill_fused_full_size():
     """T=4096, H=64 (the prefill benchmark workload), sampled heads against the oracle."""
