@@ -171,16 +171,36 @@ struct NoHook {
     __device__ void operator()() const {}
 };
 
-template <int GATE_MODE, int NT, typename AfterA = NoHook, typename AfterTm = NoHook>
+// MMA-a, issued by one thread once sm.bia and sm.kb hold the row images (and a proxy fence and a
+// barrier have made them visible): D[r][s] = (K e^{G-c} ; Q e^{G-c})_r . (K e^{c-G})_s, committed
+// to sm.bar.
+__device__ __forceinline__ void intra_mma_a_issue(IntraSmem& sm) {
+    mma3_ss(sm.tmem_base, tc_smem_desc(smem_u32(sm.bia[0]), 128, kSbo128),
+            tc_smem_desc(smem_u32(sm.bia[1]), 128, kSbo128),
+            tc_smem_desc(smem_u32(sm.kb[0]), 128, kSbo128),
+            tc_smem_desc(smem_u32(sm.kb[1]), 128, kSbo128), 8, tc_idesc_bf16(128, kCc));
+    tc_commit(&sm.bar);
+}
+
+// PRE_A: the caller has issued MMA-a already (intra_mma_a_issue after the row images) and wrote
+// the column images while it ran; the tail starts by waiting for it.  The caller may have thread 0
+// bulk-store from sm.scr meanwhile: in this mode the tail lets those copies read sm.scr before it
+// writes there.
+template <int GATE_MODE, int NT, bool PRE_A = false, typename AfterA = NoHook,
+          typename AfterTm = NoHook>
 __device__ __forceinline__ bool intra_mma_tail(IntraSmem& sm, int* err, unsigned char* blk,
                                                uint32_t& phase, AfterA after_a = AfterA(),
-                                               AfterTm after_tm = AfterTm()) {
+                                               AfterTm after_tm = AfterTm(),
+                                               const CUtensorMap* umap = nullptr, int ublock = 0) {
     static_assert(NT == 128 || NT == 256, "128 or 256 threads");
+    static_assert(!PRE_A || NT == 256, "the staged epilogue takes 32 columns per warp");
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
+    if (!PRE_A) {
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+    }
     const uint32_t tbase = sm.tmem_base;
     const uint32_t tlane = tbase + ((uint32_t)(32 * (warp & 3)) << 16);
     bool ok = true;
@@ -191,18 +211,16 @@ __device__ __forceinline__ bool intra_mma_tail(IntraSmem& sm, int* err, unsigned
     unsigned char* tml = sm.bia[0] + kTmBytes;
 
     // ---- MMA-a: D[r][s] = (K e^{G-c} ; Q e^{G-c})_r . (K e^{c-G})_s ---------------------------
-    if (tid == 0) {
-        mma3_ss(tbase, tc_smem_desc(smem_u32(sm.bia[0]), 128, kSbo128),
-                tc_smem_desc(smem_u32(sm.bia[1]), 128, kSbo128),
-                tc_smem_desc(smem_u32(sm.kb[0]), 128, kSbo128),
-                tc_smem_desc(smem_u32(sm.kb[1]), 128, kSbo128), 8, tc_idesc_bf16(128, kCc));
-        tc_commit(&sm.bar);
-    }
-    for (int i = tid; i < kCc * kLd; i += NT) ti[i] = 0.0f;     // G is dead: scr is free
+    if (!PRE_A && tid == 0) intra_mma_a_issue(sm);
+    if (!PRE_A)
+        for (int i = tid; i < kCc * kLd; i += NT) ti[i] = 0.0f;   // G is dead: scr is free
     ok = mbar_wait_bounded(&sm.bar, phase, err);
     phase ^= 1u;
     tc_fence_after();
+    if (PRE_A && tid == 0) bulk_wait_read0();   // the caller's copies out of sm.scr have read it
     if (__syncthreads_or(!ok)) goto done;
+    if (PRE_A)
+        for (int i = tid; i < kCc * kLd; i += NT) ti[i] = 0.0f;
     after_a();
 
     // ---- A (warp 0, lane t = row t) and Aqk (warp 1, lane t) -----------------------------------
@@ -323,7 +341,20 @@ __device__ __forceinline__ bool intra_mma_tail(IntraSmem& sm, int* err, unsigned
         for (int q = 0; q < CW / 16; ++q)
             tmem_ld16(tlane + col0 + 16 * q, *reinterpret_cast<float(*)[16]>(&x[16 * q]));
         tmem_ld_wait();
-        if (col0 < 128) {   // W row t, channels col0 .. : QW image rows 32 + t
+        if (PRE_A) {        // staged in sm.ktv (free once MMA-b has completed), copied out in bulk
+            if (col0 < 128) {   // W row t: rows 0..31 of an image of 32 rows (hi, lo at +8 KB)
+#pragma unroll
+                for (int cb = 0; cb < CW / 8; ++cb)
+                    put8x(sm.ktv[0], sm.ktv[0] + kCc * kSbo128 / 8, tc_offset(t, col0 + 8 * cb, kSbo128),
+                          *reinterpret_cast<const float(*)[8]>(&x[8 * cb]));
+            } else {            // U row t: a [32 t][32 v] f32 tile, 16-byte pieces 128B-swizzled
+                unsigned char* tile = sm.ktv[1] + (col0 - 128) * 128;
+#pragma unroll
+                for (int q = 0; q < CW / 4; ++q)
+                    *reinterpret_cast<float4*>(tile + t * 128 + ((q ^ (t & 7)) << 4)) =
+                        make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
+            }
+        } else if (col0 < 128) {   // W row t, channels col0 .. : QW image rows 32 + t
             unsigned char* qwh = blk + kOffQW;
             unsigned char* qwl = blk + kOffQW + kQWBytes;
 #pragma unroll
@@ -338,7 +369,16 @@ __device__ __forceinline__ bool intra_mma_tail(IntraSmem& sm, int* err, unsigned
     }
 done:
     tc_fence_before();
+    if (PRE_A) fence_proxy_async_smem();
     __syncthreads();
+    if (PRE_A && ok && tid == 0) {   // W: QW rows 32..63 (hi, lo); U: four [32 t][32 v] tiles
+        constexpr uint32_t kW = kCc * kSbo128 / 8;   // 8 KB: 4 groups of 8 rows
+        bulk_store(blk + kOffQW + kW, sm.ktv[0], kW);
+        bulk_store(blk + kOffQW + kQWBytes + kW, sm.ktv[0] + kW, kW);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) tma_store_3d(umap, sm.ktv[1] + 4096 * j, 32 * j, 0, ublock);
+        bulk_commit();
+    }
     return ok;
 }
 

@@ -250,6 +250,7 @@ __device__ __forceinline__ void pair_rows(const float (&x)[kTokW][4], float (&ro
 // gate input f [rows, C] f32 with a [32, 128] box.
 struct RawMaps {
     CUtensorMap q, k, v, f;
+    CUtensorMap ut;              // the workspace blocks' U rows (the MMA tail's epilogue)
 };
 
 // Issued by one thread: TMA tile loads of task tp's raw q, k, v rows (the chunk's tokens and the
@@ -298,8 +299,10 @@ struct __align__(128) PrepIntraSmem {
     ParamStage ps;
     uint64_t bar_raw, bar_f;                     // TMA completion of the raw rows, the gate input
 };
+// the dynamic allocation: the layout plus room to align it to 1024 bytes (128-byte swizzled tiles)
+constexpr size_t kPrepIntraSmemBytes = sizeof(PrepIntraSmem) + 1024;
 // two resident CTAs per SM: 228 KB of shared memory per SM, 1 KB of it reserved per CTA
-static_assert(2 * (sizeof(PrepIntraSmem) + 128 + 1024) <= 228 * 1024, "two CTAs per SM");
+static_assert(2 * (kPrepIntraSmemBytes + 1024) <= 228 * 1024, "two CTAs per SM");
 
 // Issue the cp.async copies of task tp's small inputs into the parameter stage.
 template <int GATE_MODE, bool CONV>
@@ -367,7 +370,7 @@ kda_chunk_prep_intra_kernel(PrepArgs p, ScanArgs a, const int* chunk_off, unsign
     constexpr bool PW = PF && CONV && KW <= 4;   // conv weights from the parameter stage
     extern __shared__ unsigned char smem_raw[];
     PrepIntraSmem& smf = *reinterpret_cast<PrepIntraSmem*>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     IntraSmem& sm = smf.in;
     ParamStage& ps = smf.ps;
     RawStage<KW>& stage = *reinterpret_cast<RawStage<KW>*>(sm.bia[1]);
@@ -576,28 +579,6 @@ kda_chunk_prep_intra_kernel(PrepArgs p, ScanArgs a, const int* chunk_off, unsign
     }
     __syncthreads();                             // G tile, references, beta, gsc
 
-    // ---- column images: channel kq+e, tokens t0 .. t0+7 ----------------------------------------
-    {
-        float bv[kTokW];
-#pragma unroll
-        for (int i = 0; i < kTokW; ++i) bv[i] = sm.beta[t0 + i];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            float xt[kTokW], xv[kTokW], xc[kTokW];
-            const float GCe = GATE_MODE == 0 ? sm.gcs[kq + e] : GCh;
-#pragma unroll
-            for (int i = 0; i < kTokW; ++i) {
-                const float Gi = G[i][e];
-                xt[i] = bv[i] * k[i][e] * __expf(Gi);
-                xv[i] = bv[i] * v[i][e];
-                xc[i] = k[i][e] * __expf(GCe - Gi);
-            }
-            put4x(sm.ktv[0], sm.ktv[1], tc_offset(kq + e, t0, kSbo32), xt);
-            put4x(sm.ktv[0], sm.ktv[1], tc_offset(128 + kq + e, t0, kSbo32), xv);
-            put4x(blk + kOffB2, blk + kOffB2 + kB2Bytes, tc_offset(kq + e, t0, kSbo32), xc);
-        }
-    }
-
     // ---- row images: tokens t0 + 2*(lane&1) + j, channels k0 .. k0+7 ---------------------------
     {
         float kr[2][8], qr[2][8];
@@ -650,8 +631,50 @@ kda_chunk_prep_intra_kernel(PrepArgs p, ScanArgs a, const int* chunk_off, unsign
             put8x(blk + kOffQW, blk + kOffQW + kQWBytes, tc_offset(t, k0, kSbo128), xg);
         }
     }
+    // ---- MMA-a on the row images ---------------------------------------------------------------
+    if (tid == 0) bulk_wait_read0();             // the last epilogue's copies have read sm.ktv
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (tid == 0) intra_mma_a_issue(sm);
+
+    // ---- column images (while MMA-a runs): channel kq+e, tokens t0 .. t0+3 ----------------------
+    // K e^{G} beta and V beta into sm.ktv (MMA-b's B operand); K e^{G_C-G} staged in sm.scr (the G
+    // tile is dead once the row images are written) and copied to the workspace in bulk.
+    unsigned char* b2s = reinterpret_cast<unsigned char*>(sm.scr);
+    constexpr uint32_t kB2KBytes = kHeadDim * kCc * 2;
+    {
+        float bv[kTokW];
+#pragma unroll
+        for (int i = 0; i < kTokW; ++i) bv[i] = sm.beta[t0 + i];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            float xt[kTokW], xv[kTokW], xc[kTokW];
+            const float GCe = GATE_MODE == 0 ? sm.gcs[kq + e] : GCh;
+#pragma unroll
+            for (int i = 0; i < kTokW; ++i) {
+                const float Gi = G[i][e];
+                xt[i] = bv[i] * k[i][e] * __expf(Gi);
+                xv[i] = bv[i] * v[i][e];
+                xc[i] = k[i][e] * __expf(GCe - Gi);
+            }
+            put4x(sm.ktv[0], sm.ktv[1], tc_offset(kq + e, t0, kSbo32), xt);
+            put4x(sm.ktv[0], sm.ktv[1], tc_offset(128 + kq + e, t0, kSbo32), xv);
+            put4x(b2s, b2s + kB2KBytes, tc_offset(kq + e, t0, kSbo32), xc);
+        }
+    }
+    // the first 128 rows of the B2 images (K e^{G_C-G}, hi and lo) leave in two bulk copies
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (tid == 0) {
+        bulk_store(blk + kOffB2, b2s, kB2KBytes);
+        bulk_store(blk + kOffB2 + kB2Bytes, b2s + kB2KBytes, kB2KBytes);
+        bulk_commit();
+    }
+
     const long next = task + gridDim.x;
-    const bool ok = intra_mma_tail<GATE_MODE, kThrF>(sm, a.err, blk, phase, [&]() {
+    const bool ok = intra_mma_tail<GATE_MODE, kThrF, true>(sm, a.err, blk, phase, [&]() {
         if (PF && next < ntasks) {
             const TaskPos np = task_pos(a.seq, chunk_off, next, nchunks);
             ld_pending = true;
@@ -661,7 +684,7 @@ kda_chunk_prep_intra_kernel(PrepArgs p, ScanArgs a, const int* chunk_off, unsign
     }, [&]() {
         if (PF && GATE_MODE == 0 && next < ntasks && tid == 0)
             stage_f(sm.scr, maps, task_pos(a.seq, chunk_off, next, nchunks), &smf.bar_f);
-    });
+    }, &maps.ut, (int)(gid * H + h));
     if (!ok) break;
     }   // task loop
     if (PF && ld_pending) {                      // left early: let the next task's loads land
@@ -669,6 +692,7 @@ kda_chunk_prep_intra_kernel(PrepArgs p, ScanArgs a, const int* chunk_off, unsign
         if (GATE_MODE == 0) mbar_wait_bounded(&smf.bar_f, ph_ld, a.err);
     }
     if (PF) cp_async_wait_all();                 // no copy may land after the CTA has left
+    if (tid == 0) bulk_wait_all();               // nor leave unfinished
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(sm.tmem_base, 256);
@@ -677,7 +701,7 @@ kda_chunk_prep_intra_kernel(PrepArgs p, ScanArgs a, const int* chunk_off, unsign
 template <bool BF16, int GM, bool CONV, int KW>
 static cudaError_t launch_prep_intra_t(const PrepArgs& p, const ScanArgs& a, const int* chunk_off,
                                        unsigned char* blocks, long nchunks, cudaStream_t s) {
-    const size_t smem = sizeof(PrepIntraSmem) + 128;
+    const size_t smem = kPrepIntraSmemBytes;
     static int done[64] = {0};
     cudaError_t e = set_smem(kda_chunk_prep_intra_kernel<BF16, GM, CONV, KW>, smem, done);
     if (e != cudaSuccess) return e;
@@ -690,6 +714,8 @@ static cudaError_t launch_prep_intra_t(const PrepArgs& p, const ScanArgs& a, con
     const long ctas = min(ntasks, 2L * sms);     // two resident CTAs per SM, persistent
     RawMaps maps;
     std::memset(&maps, 0, sizeof(maps));
+    if (!make_tensor_map_blocks_ut(&maps.ut, blocks + kOffUT, ntasks, kBlkBytes))
+        return cudaErrorInvalidValue;
     if (BF16) {                                  // the staged form reads through tensor maps
         const long rows = a.seq.total_rows, C = (long)a.H * kHeadDim;
         constexpr int kRows = RawStage<KW>::kRows;

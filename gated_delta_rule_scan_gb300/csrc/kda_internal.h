@@ -89,6 +89,9 @@ bool make_tensor_map_2d(CUtensorMap* m, const float* base, long rows, long cols,
 // The same over bf16 (bf16 = true) or f32 elements.
 bool make_tensor_map_2d_any(CUtensorMap* m, const void* base, bool bf16, long rows, long cols,
                             int box_cols, int box_rows);
+// The U rows of the chunked scan's workspace blocks: f32 [nblocks][32 tokens][128 values] at
+// `base` (the first block's U region), block stride block_bytes; box [1][32][32], 128-byte swizzle.
+bool make_tensor_map_blocks_ut(CUtensorMap* m, void* base, long nblocks, size_t block_bytes);
 cudaError_t launch_gated_rmsnorm(const NormArgs& a, cudaStream_t s);
 cudaError_t launch_decode_fused(const DecodeArgs& a, cudaStream_t s);
 

@@ -244,22 +244,6 @@ constexpr uint32_t kTA2 = 128;    // U'^T hi (16) then lo (16)
 constexpr uint32_t kTD1 = 160;    // [O1^T | X^T]  64
 constexpr uint32_t kTD2 = 224;    // [dS^T | O2^T] 160
 
-__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-            smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
-        : "memory");
-}
-
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-// wait until at most one committed group still reads its shared-memory source
-__device__ __forceinline__ void bulk_wait_read1() {
-    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-}
-// wait until every committed group has completed its writes
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-
 // write NV f32 values (NV multiple of 32) as packed bf16 hi words at col_hi and lo words at col_lo
 template <int NV>
 __device__ __forceinline__ void tmem_put_split(uint32_t col_hi, uint32_t col_lo, const float* v) {

@@ -193,6 +193,18 @@ bool make_tensor_map_2d_any(CUtensorMap* m, const void* base, bool bf16, long ro
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool make_tensor_map_blocks_ut(CUtensorMap* m, void* base, long nblocks, size_t block_bytes) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {128, 32, (cuuint64_t)nblocks};
+    cuuint64_t strides[2] = {128 * sizeof(float), (cuuint64_t)block_bytes};
+    cuuint32_t box[3] = {32, 32, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool make_tensor_map_2d(CUtensorMap* m, const float* base, long rows, long cols, int box_cols,
                         int box_rows) {
     return make_tensor_map_2d_any(m, base, false, rows, cols, box_cols, box_rows);
