@@ -48,6 +48,9 @@ constexpr int kCc = 32;                  // tokens per chunk
 constexpr int kThr = 128;                // both kernels: thread = TMEM lane
 constexpr uint32_t kSbo128 = 2048;       // 8-row group stride, K = 128 bf16 image
 constexpr uint32_t kSbo32 = 512;         // 8-row group stride, K = 32 bf16 image
+// The same for MMA-b's B operand in shared memory, padded by 16 bytes so that the column images'
+// 8-byte stores from 32 lanes (rows 4 apart) spread over the banks instead of landing on two.
+constexpr uint32_t kSboKt = 528;
 constexpr int kDevErrRange = 2;          // device error word bit: chunk gate outside f32 range
 
 // ---- workspace block of one (chunk, head) ----------------------------------------------------
@@ -142,7 +145,7 @@ struct __align__(128) IntraSmem {
     // hi then lo (8 KB each).
     unsigned char bia[2][64 * 128 * 2];
     unsigned char kb[2][kCc * 128 * 2];          // K e^{c-G}            [32 s x 128 k]  MMA-a B
-    unsigned char ktv[2][256 * kCc * 2];         // [(beta K e^G)^T ; (beta V)^T] [256 x 32 s]  MMA-b B
+    unsigned char ktv[2][256 / 8 * kSboKt];      // [(beta K e^G)^T ; (beta V)^T] [256 x 32 s]  MMA-b B
     float scr[kCc * 128];                        // G [32 t][128 k]; after MMA-a: A, Tm, products
     float beta[kCc];
     float gs[kCc];                               // per-head log-gate per token (GDN)
@@ -324,8 +327,8 @@ __device__ __forceinline__ bool intra_mma_tail(IntraSmem& sm, int* err, unsigned
     // ---- MMA-b: [W | U] = Tm [(beta K e^G) | (beta V)], every warp's 32 lanes = tokens --------
     if (tid == 0) {
         mma3_ss(tbase, tc_smem_desc(smem_u32(tmh), 128, kSbo32), tc_smem_desc(smem_u32(tml), 128, kSbo32),
-                tc_smem_desc(smem_u32(sm.ktv[0]), 128, kSbo32),
-                tc_smem_desc(smem_u32(sm.ktv[1]), 128, kSbo32), 2, tc_idesc_bf16(128, 256));
+                tc_smem_desc(smem_u32(sm.ktv[0]), 128, kSboKt),
+                tc_smem_desc(smem_u32(sm.ktv[1]), 128, kSboKt), 2, tc_idesc_bf16(128, 256));
         tc_commit(&sm.bar);
     }
     ok = mbar_wait_bounded(&sm.bar, phase, err);
@@ -345,10 +348,10 @@ __device__ __forceinline__ bool intra_mma_tail(IntraSmem& sm, int* err, unsigned
             if (col0 < 128) {   // W row t: rows 0..31 of an image of 32 rows (hi, lo at +8 KB)
 #pragma unroll
                 for (int cb = 0; cb < CW / 8; ++cb)
-                    put8x(sm.ktv[0], sm.ktv[0] + kCc * kSbo128 / 8, tc_offset(t, col0 + 8 * cb, kSbo128),
+                    put8x(sm.ktv[1], sm.ktv[1] + kCc * kSbo128 / 8, tc_offset(t, col0 + 8 * cb, kSbo128),
                           *reinterpret_cast<const float(*)[8]>(&x[8 * cb]));
             } else {            // U row t: a [32 t][32 v] f32 tile, 16-byte pieces 128B-swizzled
-                unsigned char* tile = sm.ktv[1] + (col0 - 128) * 128;
+                unsigned char* tile = sm.ktv[0] + (col0 - 128) * 128;   // 1024-byte aligned
 #pragma unroll
                 for (int q = 0; q < CW / 4; ++q)
                     *reinterpret_cast<float4*>(tile + t * 128 + ((q ^ (t & 7)) << 4)) =
@@ -373,10 +376,10 @@ done:
     __syncthreads();
     if (PRE_A && ok && tid == 0) {   // W: QW rows 32..63 (hi, lo); U: four [32 t][32 v] tiles
         constexpr uint32_t kW = kCc * kSbo128 / 8;   // 8 KB: 4 groups of 8 rows
-        bulk_store(blk + kOffQW + kW, sm.ktv[0], kW);
-        bulk_store(blk + kOffQW + kQWBytes + kW, sm.ktv[0] + kW, kW);
+        bulk_store(blk + kOffQW + kW, sm.ktv[1], kW);
+        bulk_store(blk + kOffQW + kQWBytes + kW, sm.ktv[1] + kW, kW);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) tma_store_3d(umap, sm.ktv[1] + 4096 * j, 32 * j, 0, ublock);
+        for (int j = 0; j < 4; ++j) tma_store_3d(umap, sm.ktv[0] + 4096 * j, 32 * j, 0, ublock);
         bulk_commit();
     }
     return ok;

@@ -16,6 +16,7 @@
 // gate passes from warp to warp through shared memory in token order, the order of the chunked
 // scan's own intra kernel.  The output blocks therefore equal those of the prep kernel followed
 // by the intra kernel bit for bit.
+#include <cstddef>
 #include <cstring>
 
 #include "kda_chunk_common.cuh"
@@ -232,17 +233,22 @@ __device__ __forceinline__ void put4x(unsigned char* hi_img, unsigned char* lo_i
 }
 
 // The 8-channel rows of this lane's half of the warp's tokens (even lane: tokens 0-1, odd lane:
-// tokens 2-3): own 4 channels plus the partner lane's 4, in channel order.
-__device__ __forceinline__ void pair_rows(const float (&x)[kTokW][4], float (&row)[2][8]) {
+// tokens 2-3): own 4 channels plus the partner lane's 4, in channel order.  row[j] is token
+// j ^ sw of the half (sw is the same for both lanes of a pair), so that lanes with sw set write
+// their two rows in the other order and a 16-byte store of the warp touches four row slots of the
+// core matrices instead of two.
+__device__ __forceinline__ void pair_rows(const float (&x)[kTokW][4], float (&row)[2][8], bool sw) {
     const bool odd = (threadIdx.x & 1) != 0;
 #pragma unroll
     for (int j = 0; j < 2; ++j)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-            const float send = odd ? x[j][e] : x[2 + j][e];
+            const float lo_t = sw ? x[1 - j][e] : x[j][e];          // token j ^ sw
+            const float hi_t = sw ? x[3 - j][e] : x[2 + j][e];      // token 2 + (j ^ sw)
+            const float send = odd ? lo_t : hi_t;
             const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
-            row[j][e] = odd ? recv : x[j][e];
-            row[j][4 + e] = odd ? x[2 + j][e] : recv;
+            row[j][e] = odd ? recv : lo_t;
+            row[j][4 + e] = odd ? hi_t : recv;
         }
 }
 
@@ -299,6 +305,12 @@ struct __align__(128) PrepIntraSmem {
     ParamStage ps;
     uint64_t bar_raw, bar_f;                     // TMA completion of the raw rows, the gate input
 };
+// TMA destinations and sources inside the layout (its base aligned to 1024 bytes): the raw-row
+// stage at sm.bia[1] and the gate input at sm.scr (128-byte aligned), the epilogue's swizzled U
+// tiles at sm.ktv[0] (1024-byte aligned).
+static_assert(offsetof(IntraSmem, bia) + sizeof(IntraSmem::bia[0]) == 16384, "stage at 16 KB");
+static_assert(offsetof(IntraSmem, ktv) % 1024 == 0, "U tiles 1024-byte aligned");
+static_assert(offsetof(IntraSmem, scr) % 128 == 0, "gate input 128-byte aligned");
 // the dynamic allocation: the layout plus room to align it to 1024 bytes (128-byte swizzled tiles)
 constexpr size_t kPrepIntraSmemBytes = sizeof(PrepIntraSmem) + 1024;
 // two resident CTAs per SM: 228 KB of shared memory per SM, 1 KB of it reserved per CTA
@@ -579,31 +591,33 @@ kda_chunk_prep_intra_kernel(PrepArgs p, ScanArgs a, const int* chunk_off, unsign
     }
     __syncthreads();                             // G tile, references, beta, gsc
 
-    // ---- row images: tokens t0 + 2*(lane&1) + j, channels k0 .. k0+7 ---------------------------
+    // ---- row images: tokens t0 + 2*(lane&1) + (j ^ sw), channels k0 .. k0+7 --------------------
     {
+        const bool sw = ((lane >> 1) & 1) != 0;
         float kr[2][8], qr[2][8];
-        pair_rows(k, kr);
-        pair_rows(q, qr);
+        pair_rows(k, kr, sw);
+        pair_rows(q, qr, sw);
         const int k0 = 8 * (lane >> 1);
         const int tb = t0 + 2 * (lane & 1);
+        const int tj[2] = {tb + (sw ? 1 : 0), tb + (sw ? 0 : 1)};
         float crv[8], ecv[8], gtv[2][8];
         if (GATE_MODE == 0) {
 #pragma unroll
             for (int e = 0; e < 8; ++e) { crv[e] = sm.cref[k0 + e]; ecv[e] = sm.ecr[k0 + e]; }
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
-                const float4 a0 = *reinterpret_cast<const float4*>(&sm.scr[(tb + j) * 128 + k0]);
-                const float4 a1 = *reinterpret_cast<const float4*>(&sm.scr[(tb + j) * 128 + k0 + 4]);
+                const float4 a0 = *reinterpret_cast<const float4*>(&sm.scr[tj[j] * 128 + k0]);
+                const float4 a1 = *reinterpret_cast<const float4*>(&sm.scr[tj[j] * 128 + k0 + 4]);
                 gtv[j][0] = a0.x; gtv[j][1] = a0.y; gtv[j][2] = a0.z; gtv[j][3] = a0.w;
                 gtv[j][4] = a1.x; gtv[j][5] = a1.y; gtv[j][6] = a1.z; gtv[j][7] = a1.w;
             }
         } else {
 #pragma unroll
-            for (int j = 0; j < 2; ++j) gtv[j][0] = sm.gsc[tb + j];
+            for (int j = 0; j < 2; ++j) gtv[j][0] = sm.gsc[tj[j]];
         }
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
-            const int t = tb + j;
+            const int t = tj[j];
             float xb[8], xk[8], xq[8], xg[8];
             if (GATE_MODE == 0) {
 #pragma unroll
@@ -659,8 +673,8 @@ kda_chunk_prep_intra_kernel(PrepArgs p, ScanArgs a, const int* chunk_off, unsign
                 xv[i] = bv[i] * v[i][e];
                 xc[i] = k[i][e] * __expf(GCe - Gi);
             }
-            put4x(sm.ktv[0], sm.ktv[1], tc_offset(kq + e, t0, kSbo32), xt);
-            put4x(sm.ktv[0], sm.ktv[1], tc_offset(128 + kq + e, t0, kSbo32), xv);
+            put4x(sm.ktv[0], sm.ktv[1], tc_offset(kq + e, t0, kSboKt), xt);
+            put4x(sm.ktv[0], sm.ktv[1], tc_offset(128 + kq + e, t0, kSboKt), xv);
             put4x(b2s, b2s + kB2KBytes, tc_offset(kq + e, t0, kSbo32), xc);
         }
     }

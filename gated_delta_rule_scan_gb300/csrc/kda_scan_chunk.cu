@@ -161,8 +161,8 @@ kda_chunk_intra_kernel(ScanArgs a, const int* chunk_off, unsigned char* ws) {
                 xv[e] = bt * vc[t];
                 xc[e] = kc[t] * __expf(GC - gc[t]);
             }
-            put8x(sm.ktv[0], sm.ktv[1], tc_offset(tid, 8 * j, kSbo32), xt);
-            put8x(sm.ktv[0], sm.ktv[1], tc_offset(128 + tid, 8 * j, kSbo32), xv);
+            put8x(sm.ktv[0], sm.ktv[1], tc_offset(tid, 8 * j, kSboKt), xt);
+            put8x(sm.ktv[0], sm.ktv[1], tc_offset(128 + tid, 8 * j, kSboKt), xv);
             put8x(blk + kOffB2, blk + kOffB2 + kB2Bytes, tc_offset(tid, 8 * j, kSbo32), xc);
         }
     }
