@@ -272,8 +272,10 @@ __device__ __forceinline__ void tmem_put_split16(uint32_t col_hi, uint32_t col_l
 }
 
 // Threads: 256.  Thread (half hf = tid / 128, value row v = tid % 128) owns TMEM lane v; it keeps
-// key columns 64 hf .. 64 hf + 63 of state row v in registers and handles tokens 16 hf .. 16 hf + 15
-// of each chunk's U' and o.  Thread 0 issues the MMAs, thread 32 the workspace loads, and the
+// key columns 32 hf .. 32 hf + 31 and 64 + 32 hf .. 64 + 32 hf + 31 of state row v in registers
+// (srow[0..31], srow[32..63]) and handles tokens 16 hf .. 16 hf + 15 of each chunk's U' and o.
+// The state update runs in two passes, keys 0..63 then 64..127, so that the next chunk's MMA-1
+// takes its first four K-steps while the second pass runs.  Thread 0 issues the MMAs, thread 32 the workspace loads, and the
 // lanes of warp 2 the o rows' bulk stores (lane t: token t of the chunk).
 constexpr int kThrInter = 256;
 
@@ -307,11 +309,11 @@ kda_chunk_inter_kernel(ScanArgs a, const int* chunk_off, const unsigned char* ws
     }
     float srow[64];
     {
-        const float4* sin = reinterpret_cast<const float4*>(
-            a.state_in + (((long)n * H + h) * kHeadDim + v) * kHeadDim + 64 * hf);
+        const float* srow_in = a.state_in + (((long)n * H + h) * kHeadDim + v) * kHeadDim;
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
-            const float4 x = __ldcs(sin + j);
+            const float4 x = __ldcs(reinterpret_cast<const float4*>(
+                srow_in + (j < 8 ? 32 * hf : 64 + 32 * hf - 32) + 4 * j));
             srow[4 * j] = x.x; srow[4 * j + 1] = x.y; srow[4 * j + 2] = x.z; srow[4 * j + 3] = x.w;
         }
     }
@@ -320,7 +322,8 @@ kda_chunk_inter_kernel(ScanArgs a, const int* chunk_off, const unsigned char* ws
     tc_fence_after();
     const uint32_t tbase = sm.tmem_base;
     const uint32_t tl = tbase + ((uint32_t)(32 * (warp & 3)) << 16);
-    tmem_put_split<64>(tl + kTA1 + 32 * hf, tl + kTA1 + 64 + 32 * hf, srow);
+    tmem_put_split<32>(tl + kTA1 + 16 * hf, tl + kTA1 + 64 + 16 * hf, srow);
+    tmem_put_split<32>(tl + kTA1 + 32 + 16 * hf, tl + kTA1 + 96 + 16 * hf, srow + 32);
     tmem_st_wait();
 
     auto issue = [&](int c, int st) {
@@ -331,13 +334,25 @@ kda_chunk_inter_kernel(ScanArgs a, const int* chunk_off, const unsigned char* ws
         bulk_load(&sm.blk[st][kOffUT], src + kOffUT, kUTBytes + kEGBytes, &sm.bar_ld[st]);
     };
     const uint32_t id1 = tc_idesc_bf16(128, 2 * kCc), id2 = tc_idesc_bf16(128, 160);
-    // MMA-1: [O1^T | X^T] = S^T (Q e^G | W)^T for the chunk in stage st.  (One N = 64 group: the
-    // tensor pipe's cost here follows the instruction count, so two N = 32 groups are slower.)
-    auto mma1 = [&](int st) {
+    // MMA-1: [O1^T | X^T] = S^T (Q e^G | W)^T for the chunk in stage st, K-steps ks0 .. ks0+3
+    // (keys 16 ks0 ..), bf16x3 per K-step; the first product of K-step 0 starts the sum.  (One
+    // N = 64 group: the tensor pipe's cost here follows the instruction count, so two N = 32
+    // groups are slower.)
+    auto mma1_half = [&](int st, int ks0) {
         const unsigned char* B = sm.blk[st];
-        mma3_ts(tbase + kTD1, tbase + kTA1, tbase + kTA1 + 64,
-                tc_smem_desc(smem_u32(B + kOffQW), 128, kSbo128),
-                tc_smem_desc(smem_u32(B + kOffQW + kQWBytes), 128, kSbo128), 8, id1);
+        const uint64_t bh = tc_smem_desc(smem_u32(B + kOffQW), 128, kSbo128);
+        const uint64_t bl = tc_smem_desc(smem_u32(B + kOffQW + kQWBytes), 128, kSbo128);
+#pragma unroll
+        for (int ks = ks0; ks < ks0 + 4; ++ks) {
+            const uint32_t ah = tbase + kTA1 + 8 * ks, al = tbase + kTA1 + 64 + 8 * ks;
+            tc_mma_ts(tbase + kTD1, ah, tc_desc_advance(bh, 256 * ks), id1, ks > 0);
+            tc_mma_ts(tbase + kTD1, ah, tc_desc_advance(bl, 256 * ks), id1, true);
+            tc_mma_ts(tbase + kTD1, al, tc_desc_advance(bh, 256 * ks), id1, true);
+        }
+    };
+    auto mma1 = [&](int st) {
+        mma1_half(st, 0);
+        mma1_half(st, 4);
         tc_commit(&sm.bar_mma);
     };
     // the state is in TMEM; the first chunk's MMA-1 goes out as soon as its block lands
@@ -419,36 +434,42 @@ kda_chunk_inter_kernel(ScanArgs a, const int* chunk_off, const unsigned char* ws
         tc_fence_after();
         if (__syncthreads_or(!ok)) { failed = true; break; }
         float o2[16];
-        {
-            const float4* eg4 = reinterpret_cast<const float4*>(B + kOffEG) + 16 * hf;
+        bool next_ok = false;            // thread 0: the next chunk's block landed, MMA-1 going
+        // S <- S e^{G_C} + dS, keys 0..63 (srow[0..31]) then 64..127 (srow[32..63]); after the
+        // first pass thread 0 starts the next chunk's MMA-1 on keys 0..63
+        const float4* eg4 = reinterpret_cast<const float4*>(B + kOffEG);
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                float d[32];
-                tmem_ld16(tl + kTD2 + 64 * hf + 32 * half, *reinterpret_cast<float(*)[16]>(&d[0]));
-                tmem_ld16(tl + kTD2 + 64 * hf + 32 * half + 16, *reinterpret_cast<float(*)[16]>(&d[16]));
-                if (half == 1) tmem_ld16(tl + kTD2 + 128 + 16 * hf, o2);
-                tmem_ld_wait();
+        for (int pass = 0; pass < 2; ++pass) {
+            const int k0 = 64 * pass + 32 * hf;      // this thread's first key of the pass
+            float d[32];
+            tmem_ld16(tl + kTD2 + k0, *reinterpret_cast<float(*)[16]>(&d[0]));
+            tmem_ld16(tl + kTD2 + k0 + 16, *reinterpret_cast<float(*)[16]>(&d[16]));
+            if (pass == 1) tmem_ld16(tl + kTD2 + 128 + 16 * hf, o2);
+            tmem_ld_wait();
+            float* sr = srow + 32 * pass;
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const float4 e4 = eg4[8 * half + q];
-                    const int kk = 32 * half + 4 * q;
-                    srow[kk] = fmaf(srow[kk], e4.x, d[4 * q]);
-                    srow[kk + 1] = fmaf(srow[kk + 1], e4.y, d[4 * q + 1]);
-                    srow[kk + 2] = fmaf(srow[kk + 2], e4.z, d[4 * q + 2]);
-                    srow[kk + 3] = fmaf(srow[kk + 3], e4.w, d[4 * q + 3]);
-                }
+            for (int q = 0; q < 8; ++q) {
+                const float4 e4 = eg4[k0 / 4 + q];
+                sr[4 * q] = fmaf(sr[4 * q], e4.x, d[4 * q]);
+                sr[4 * q + 1] = fmaf(sr[4 * q + 1], e4.y, d[4 * q + 1]);
+                sr[4 * q + 2] = fmaf(sr[4 * q + 2], e4.z, d[4 * q + 2]);
+                sr[4 * q + 3] = fmaf(sr[4 * q + 3], e4.w, d[4 * q + 3]);
             }
-            tmem_put_split<64>(tl + kTA1 + 32 * hf, tl + kTA1 + 64 + 32 * hf, srow);
+            tmem_put_split<32>(tl + kTA1 + k0 / 2, tl + kTA1 + 64 + k0 / 2, sr);
             tmem_st_wait();
-        }
-        tc_fence_before();
-        __syncthreads();   // block st consumed; S^T in place for the next MMA-1
-        tc_fence_after();
-        if (tid == 0 && c + 1 < nch) {
-            const int s1 = (c + 1) % kInterStages;
-            if (mbar_wait_bounded(&sm.bar_ld[s1], (uint32_t)(((c + 1) / kInterStages) & 1), a.err)) {
-                tc_fence_after();
-                mma1(s1);
+            tc_fence_before();
+            __syncthreads();   // pass 1: block st consumed; S^T in place for the next MMA-1
+            tc_fence_after();
+            if (tid == 0 && c + 1 < nch) {
+                const int s1 = (c + 1) % kInterStages;
+                if (pass == 0)
+                    next_ok = mbar_wait_bounded(&sm.bar_ld[s1], (uint32_t)(((c + 1) / kInterStages) & 1),
+                                                a.err);
+                if (next_ok) {
+                    tc_fence_after();
+                    mma1_half(s1, 4 * pass);
+                    if (pass == 1) tc_commit(&sm.bar_mma);
+                }
             }
         }
         if (tid == 32 && c + kInterStages < nch) issue(c + kInterStages, st);
@@ -466,11 +487,11 @@ kda_chunk_inter_kernel(ScanArgs a, const int* chunk_off, const unsigned char* ws
         bulk_wait_all();
     }
     if (!failed) {
-        float4* sout = reinterpret_cast<float4*>(
-            a.state_out + (((long)n * H + h) * kHeadDim + v) * kHeadDim + 64 * hf);
+        float* srow_out = a.state_out + (((long)n * H + h) * kHeadDim + v) * kHeadDim;
 #pragma unroll
         for (int j = 0; j < 16; ++j)
-            __stcs(sout + j, make_float4(srow[4 * j], srow[4 * j + 1], srow[4 * j + 2], srow[4 * j + 3]));
+            __stcs(reinterpret_cast<float4*>(srow_out + (j < 8 ? 32 * hf : 64 + 32 * hf - 32) + 4 * j),
+                   make_float4(srow[4 * j], srow[4 * j + 1], srow[4 * j + 2], srow[4 * j + 3]));
     } else {
         mbar_wait_bounded(&sm.bar_mma, mph, nullptr);   // let in-flight MMAs drain (bounded)
     }
