@@ -163,8 +163,8 @@ def _kernel_bytes(T, H, blk_bytes, chunks):
         # raw q, k, v (bf16), gate input, beta input, conv weights + ring -> the workspace
         "kda_chunk_prep_intra_kernel": 3 * T * C * bf16 + plane + T * H * f32 + 3 * C * 4 * f32
                                        + 3 * C * 3 * f32 + ws,
-        # workspace + state in -> o + state out
-        "kda_chunk_inter_kernel": ws + 2 * H * D * D * f32 + plane,
+        # workspace + state in -> o + state out; in the fused prefill also the conv ring roll
+        "kda_chunk_inter_kernel": ws + 2 * H * D * D * f32 + plane + 3 * C * 3 * (bf16 + 2 * f32),
         "kda_chunk_offsets_kernel": 0,
         # o + RMSNorm gate + weight -> y
         "kda_gated_rmsnorm_kernel": 3 * plane + D * f32,

@@ -777,9 +777,8 @@ cudaError_t launch_prefill_chunk(const PrepArgs& p, const ScanArgs& a, const int
                      : launch_prep_intra_c<false, 0>(p, a, chunk_off, blocks, nchunks, s);
         if (e != cudaSuccess) return e;
     }
-    e = launch_ring_roll(p, s);                  // after the kernel above has read ring_in
-    if (e != cudaSuccess) return e;
-    return launch_chunk_inter(a, chunk_off, blocks, s);
+    // the inter kernel also rolls the conv ring (after the kernel above has read ring_in)
+    return launch_chunk_inter(a, chunk_off, blocks, s, p.conv_w != nullptr ? &p : nullptr);
 }
 
 }  // namespace kda

@@ -69,7 +69,8 @@ long chunk_count(const SeqLayout& s, const int* cu_host);
 cudaError_t launch_chunk_offsets(const SeqLayout& seq, void* workspace, int** chunk_off,
                                  unsigned char** blocks, cudaStream_t s);
 cudaError_t launch_chunk_inter(const ScanArgs& a, const int* chunk_off,
-                               const unsigned char* blocks, cudaStream_t s);
+                               const unsigned char* blocks, cudaStream_t s,
+                               const PrepArgs* ring = nullptr);
 // the fused prefill's prep + intra-chunk kernel, then the ring roll (kda_chunk_prep.cu)
 cudaError_t launch_prefill_chunk(const PrepArgs& p, const ScanArgs& a, const int* cu_host,
                                  void* workspace, cudaStream_t s);

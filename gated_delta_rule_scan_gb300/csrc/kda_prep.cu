@@ -20,6 +20,7 @@
 // ring_in and ring_out may be the same buffer.
 #include "kda_device.cuh"
 #include "kda_internal.h"
+#include "kda_ring.cuh"
 
 namespace kda {
 
@@ -208,47 +209,13 @@ __global__ void __launch_bounds__(kPrepThreads) kda_prep_kernel(PrepArgs a) {
     }
 }
 
-// Ring roll: ring_out[n][pc][s] = xt[L_n + s], xt = (ring_in[n][pc][0..R-1], raw rows of n).
-// One thread per (sequence, fused channel); each reads all its old slots before writing, so the
-// roll is safe in place.
+// Ring roll, one thread per (sequence, fused channel) (kda_ring.cuh).
 template <bool BF16>
 __global__ void __launch_bounds__(256) kda_ring_roll_kernel(PrepArgs a) {
     const long C = (long)a.H * kHeadDim;
     const long idx = (long)blockIdx.x * blockDim.x + threadIdx.x;
-    const int n = blockIdx.y;
     if (idx >= 3 * C) return;
-    const int p = (int)(idx / C);
-    const long c = idx % C;
-    const int R = a.K - 1;
-    long begin, end;
-    if (a.seq.cu_seqlens == nullptr) {
-        begin = (long)n * a.seq.T_uniform;
-        end = begin + a.seq.T_uniform;
-    } else {
-        begin = a.seq.cu_seqlens[n];
-        end = a.seq.cu_seqlens[n + 1];
-    }
-    const long Ln = end - begin;
-    const void* raw = p == 0 ? a.q_raw : (p == 1 ? a.k_raw : a.v_raw);
-    const long base = ((long)n * 3 * C + idx) * R;
-    float old[kMaxConvK - 1];
-#pragma unroll
-    for (int s2 = 0; s2 < kMaxConvK - 1; ++s2) old[s2] = s2 < R ? a.ring_in[base + s2] : 0.0f;
-#pragma unroll
-    for (int s2 = 0; s2 < kMaxConvK - 1; ++s2) {
-        if (s2 < R) {
-            const long pos = Ln + s2;  // index into xt
-            float x;
-            if (pos < R) {
-                x = 0.0f;
-#pragma unroll
-                for (int m = 0; m < kMaxConvK - 1; ++m) if (m == pos) x = old[m];
-            } else {
-                x = load_raw<BF16>(raw, (begin + pos - R) * C + c);
-            }
-            a.ring_out[base + s2] = x;
-        }
-    }
+    ring_roll_one<BF16>(a, blockIdx.y, (int)(idx / C), idx % C);
 }
 
 cudaError_t launch_ring_roll(const PrepArgs& a, cudaStream_t s) {

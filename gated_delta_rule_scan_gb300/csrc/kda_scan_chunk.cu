@@ -2,7 +2,10 @@
 // tcgen05 tensor cores: the per-sequence chunk offsets, the intra-chunk kernel over the prepared
 // q, k, v, g planes and the sequential inter-chunk kernel, with their launchers.  The method,
 // the workspace layout and the shared device code are in kda_chunk_common.cuh.
+#include <cstring>
+
 #include "kda_chunk_common.cuh"
+#include "kda_ring.cuh"
 
 namespace kda {
 
@@ -232,7 +235,7 @@ constexpr int kInterStages = 2;                  // workspace blocks in flight p
 
 struct __align__(128) InterSmem {
     unsigned char blk[kInterStages][kBlkBytes];
-    float otile[2][kCc][128];                    // a chunk's o rows on their way out
+    float otile[3][kCc][128];                    // chunks' o rows on their way out (c % 3)
     uint64_t bar_ld[kInterStages];
     uint64_t bar_mma;                            // MMA-1, then MMA-2
     uint32_t tmem_base;
@@ -282,7 +285,7 @@ constexpr int kThrInter = 256;
 template <int GATE_MODE>
 __global__ void __launch_bounds__(kThrInter, 1)
 kda_chunk_inter_kernel(ScanArgs a, const int* chunk_off, const unsigned char* ws,
-                       const __grid_constant__ CUtensorMap tmo) {
+                       const __grid_constant__ CUtensorMap tmo, const __grid_constant__ PrepArgs ring) {
     extern __shared__ unsigned char smem_raw[];
     InterSmem& sm = *reinterpret_cast<InterSmem*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
@@ -367,44 +370,53 @@ kda_chunk_inter_kernel(ScanArgs a, const int* chunk_off, const unsigned char* ws
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // the fused prefill's conv ring roll of this (sequence, head) while the first MMA-1 runs (the
+    // prep kernel that read ring_in has finished)
+    if (ring.conv_w != nullptr) {
+        for (int i = tid; i < 3 * kHeadDim; i += kThrInter) {
+            const int p = i / kHeadDim;
+            const long c = (long)h * kHeadDim + i % kHeadDim;
+            if (ring.raw_bf16) ring_roll_one<true>(ring, n, p, c);
+            else ring_roll_one<false>(ring, n, p, c);
+        }
+    }
 
     uint32_t mph = 0;
     bool failed = false;
     const float scale = a.scale;
     const bool ostore_lane = warp == 2;
     const int olane = tid & 31;
-    // store the o rows of chunk cp (staged in otile[cp & 1]) -- warp 2 only.  A full chunk (or
+    // store the o rows of chunk cp (staged in otile[cp % 3]) -- warp 2 only.  A full chunk (or
     // one whose overhang lies past the last row of the tensor) goes out as one TMA tile store;
     // the ragged last chunk of a sequence followed by another is copied row by row.
     auto flush_o = [&](int cp) {
         const long r0 = begin + (long)cp * kCc;
         const int ntp = (int)min((long)kCc, L - (long)cp * kCc);
         if (ntp == kCc || end == a.seq.total_rows) {
-            if (olane == 0) tma_store_2d(&tmo, sm.otile[cp & 1], h * kHeadDim, (int)r0);
+            if (olane == 0) tma_store_2d(&tmo, sm.otile[cp % 3], h * kHeadDim, (int)r0);
         } else {
             for (int t = 0; t < ntp; ++t)
                 reinterpret_cast<float4*>(a.o + (r0 + t) * C + h * kHeadDim)[olane] =
-                    reinterpret_cast<const float4*>(sm.otile[cp & 1][t])[olane];
+                    reinterpret_cast<const float4*>(sm.otile[cp % 3][t])[olane];
         }
         bulk_commit();
     };
     for (int c = 0; c < nch; ++c) {
         const int st = c % kInterStages;
         const unsigned char* B = sm.blk[st];
-        const bool got = mbar_wait_bounded(&sm.bar_ld[st], (uint32_t)((c / kInterStages) & 1), a.err);
-        if (__syncthreads_or(!got)) { failed = true; break; }
-        if (ostore_lane && c > 0) {      // the previous chunk's o tile is complete (barrier above)
-            flush_o(c - 1);
-            bulk_wait_read1();           // the tile written next iteration is free again
-        }
-        bool ok = mbar_wait_bounded(&sm.bar_mma, mph, a.err);
+        // the block landed before thread 0 issued this chunk's MMA-1; each thread still observes
+        // its barrier before reading it
+        bool ok = mbar_wait_bounded(&sm.bar_ld[st], (uint32_t)((c / kInterStages) & 1), a.err);
+        if (ostore_lane) bulk_wait_read1();   // only the last o store may still read its tile:
+                                              // the one of chunk c-3 (tile c % 3) is free
+        ok = ok && mbar_wait_bounded(&sm.bar_mma, mph, a.err);
         if (ok) mph ^= 1u;
         tc_fence_after();
         if (__syncthreads_or(!ok)) { failed = true; break; }
-        // O1 and X for tokens 16 hf ..; O1 waits in the output tile (its buffer's previous bulk
-        // store has been read: warp 2 waited for it before the barrier above); U' = U - X into
-        // TMEM as MMA-2's A operand
-        float* ot = &sm.otile[c & 1][16 * hf][v];
+        if (ostore_lane && c > 0) flush_o(c - 1);   // its o rows were written before the barrier
+        // O1 and X for tokens 16 hf ..; O1 waits in the output tile; U' = U - X into TMEM as
+        // MMA-2's A operand
+        float* ot = &sm.otile[c % 3][16 * hf][v];
         {
             float x[16], o1[16];
             tmem_ld16(tl + kTD1 + 16 * hf, o1);
@@ -531,7 +543,7 @@ cudaError_t launch_chunk_offsets(const SeqLayout& seq, void* workspace, int** ch
 
 template <int GM>
 static cudaError_t launch_inter_t(const ScanArgs& a, const int* chunk_off,
-                                  const unsigned char* blocks, cudaStream_t s) {
+                                  const unsigned char* blocks, const PrepArgs& ring, cudaStream_t s) {
     const size_t smem2 = sizeof(InterSmem) + 128;
     static int done2[64] = {0};
     cudaError_t e = set_smem(kda_chunk_inter_kernel<GM>, smem2, done2);
@@ -541,14 +553,17 @@ static cudaError_t launch_inter_t(const ScanArgs& a, const int* chunk_off,
     if (!make_tensor_map_2d(&tmo, a.o, a.seq.total_rows, (long)a.H * kHeadDim, kHeadDim, kCc))
         return cudaErrorInvalidValue;
     KernelTimer kt(kKChunkInter, s);
-    kda_chunk_inter_kernel<GM><<<g2, kThrInter, smem2, s>>>(a, chunk_off, blocks, tmo);
+    kda_chunk_inter_kernel<GM><<<g2, kThrInter, smem2, s>>>(a, chunk_off, blocks, tmo, ring);
     return cudaGetLastError();
 }
 
 cudaError_t launch_chunk_inter(const ScanArgs& a, const int* chunk_off,
-                               const unsigned char* blocks, cudaStream_t s) {
-    return (a.gate_mode & 1) == 0 ? launch_inter_t<0>(a, chunk_off, blocks, s)
-                                  : launch_inter_t<1>(a, chunk_off, blocks, s);
+                               const unsigned char* blocks, cudaStream_t s, const PrepArgs* ring) {
+    PrepArgs none;
+    std::memset(&none, 0, sizeof(none));
+    const PrepArgs& r = ring != nullptr ? *ring : none;
+    return (a.gate_mode & 1) == 0 ? launch_inter_t<0>(a, chunk_off, blocks, r, s)
+                                  : launch_inter_t<1>(a, chunk_off, blocks, r, s);
 }
 
 template <int GM, bool EXP>

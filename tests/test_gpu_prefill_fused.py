@@ -137,8 +137,8 @@ def test_prefill_fused_contract():
 
 def test_kernel_timer_counts_fused_launches():
     """With timing on, one fused prefill of two packed sequences records exactly its kernels:
-    chunk offsets, the fused prep + intra-chunk kernel, ring roll, inter and the RMSNorm, once
-    each (no separate prep kernel)."""
+    chunk offsets, the fused prep + intra-chunk kernel, inter (which also rolls the conv ring)
+    and the RMSNorm, once each (no separate prep or ring-roll kernel)."""
     from gated_delta_rule_scan_gb300 import kda
     inp = inputs.make_inputs(74, H=2, N=2, lengths=(40, 90), raw_dtype="bf16", conv=True,
                              ring="randn", state="randn", epilogue=True)
@@ -148,7 +148,6 @@ def test_kernel_timer_counts_fused_launches():
         times = kda.kernel_times()
     finally:
         kda.kernel_timing(False)
-    assert set(times) == {"kda_ring_roll_kernel", "kda_chunk_offsets_kernel",
-                          "kda_chunk_prep_intra_kernel", "kda_chunk_inter_kernel",
-                          "kda_gated_rmsnorm_kernel"}, times
+    assert set(times) == {"kda_chunk_offsets_kernel", "kda_chunk_prep_intra_kernel",
+                          "kda_chunk_inter_kernel", "kda_gated_rmsnorm_kernel"}, times
     assert all(n == 1 and ms > 0 for n, ms in times.values()), times
