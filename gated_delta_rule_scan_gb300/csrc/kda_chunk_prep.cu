@@ -535,35 +535,39 @@ kda_chunk_prep_intra_kernel(PrepArgs p, ScanArgs a, const int* chunk_off, unsign
 #pragma unroll
             for (int e = 0; e < 4; ++e)
                 g[i][e] = i < ntok ? kda_gate_f(f4c(fr[i], e), dtv[e], rate, p.gate_lb) : 0.0f;
-        float* carry = sm.cref;                  // the running sums handed on (reused below)
+        // blocked running sum (the chunked intra kernel's order): each warp sums its 4 tokens in
+        // order from 0, the warps' totals go through shared memory (sm.bia[0], free until the row
+        // images), and warp w adds the totals of warps 0 .. w-1 in order, starting from 0
+        float run[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-        for (int s = 0; s < kThrF / 32; ++s) {
-            if (warp == s) {
-                float run[4];
+        for (int i = 0; i < kTokW; ++i)
 #pragma unroll
-                for (int e = 0; e < 4; ++e) run[e] = s == 0 ? 0.0f : carry[kq + e];
-#pragma unroll
-                for (int i = 0; i < kTokW; ++i)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        run[e] += g[i][e];
-                        G[i][e] = run[e];
-                    }
-                if (s < kThrF / 32 - 1) {
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) carry[kq + e] = run[e];
-                } else {                         // G over the whole chunk: references, decay, range
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        sm.gcs[kq + e] = run[e];
-                        sm.cref[kq + e] = 0.5f * run[e];
-                        sm.ecr[kq + e] = __expf(0.5f * run[e]);
-                        reinterpret_cast<float*>(blk + kOffEG)[kq + e] = decay_f(run[e]);
-                        if (run[e] < -170.0f && a.err) atomicOr(a.err, kDevErrRange);
-                    }
-                }
+            for (int e = 0; e < 4; ++e) {
+                run[e] += g[i][e];
+                G[i][e] = run[e];
             }
-            __syncthreads();
+        float* gtot = reinterpret_cast<float*>(sm.bia[0]);   // [8 warps][128 channels]
+        *reinterpret_cast<float4*>(&gtot[warp * kHeadDim + kq]) = make_float4(run[0], run[1], run[2], run[3]);
+        __syncthreads();
+        float pre[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        for (int w2 = 0; w2 < warp; ++w2) {
+            const float4 t4 = *reinterpret_cast<const float4*>(&gtot[w2 * kHeadDim + kq]);
+            pre[0] += t4.x; pre[1] += t4.y; pre[2] += t4.z; pre[3] += t4.w;
+        }
+#pragma unroll
+        for (int i = 0; i < kTokW; ++i)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) G[i][e] = pre[e] + G[i][e];
+        if (warp == kThrF / 32 - 1) {            // G over the whole chunk: references, decay, range
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float tot = G[kTokW - 1][e];
+                sm.gcs[kq + e] = tot;
+                sm.cref[kq + e] = 0.5f * tot;
+                sm.ecr[kq + e] = __expf(0.5f * tot);
+                reinterpret_cast<float*>(blk + kOffEG)[kq + e] = decay_f(tot);
+                if (tot < -170.0f && a.err) atomicOr(a.err, kDevErrRange);
+            }
         }
 #pragma unroll
         for (int i = 0; i < kTokW; ++i)

@@ -115,13 +115,26 @@ kda_chunk_intra_kernel(ScanArgs a, const int* chunk_off, unsigned char* ws) {
     }
 
     // ---- cumulative gate: gc[t] = G_t of channel tid (KDA) or of the head (GDN) ---------------
+    // KDA, blocked: tokens in blocks of 4, each block summed in order from 0; the running total
+    // of the blocks before (in order, from 0) is added to every token of the block
     if (GATE_MODE == 0) {
-        float G = 0.0f;
+        float G = 0.0f;                          // total of the blocks so far
 #pragma unroll
-        for (int t = 0; t < kCc; ++t) {
-            G += EXP ? logf(gc[t]) : gc[t];
-            gc[t] = G;
-            sm.scr[t * 128 + tid] = G;
+        for (int b = 0; b < kCc / 4; ++b) {
+            float run = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int t = 4 * b + i;
+                run += EXP ? logf(gc[t]) : gc[t];
+                gc[t] = run;
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int t = 4 * b + i;
+                gc[t] = G + gc[t];
+                sm.scr[t * 128 + tid] = gc[t];
+            }
+            G = G + run;
         }
         sm.cref[tid] = 0.5f * G;
         sm.ecr[tid] = __expf(0.5f * G);
