@@ -62,6 +62,45 @@ def _dist():
     return ws, rank, local
 
 
+class Replicas:
+    """The N > 1 plumbing: one process per GPU, each running an independent replica of the
+    workload (the (sequence, head) units shard with no exchange step, so there is no data-path
+    collective).  barrier() brackets the timed region (and synchronises the device);
+    max_over_ranks() takes the slowest rank's time; whole_job() turns it into throughput over the
+    units all ranks processed.  World size 1 needs no process group."""
+
+    def __init__(self, ws, rank, device, backend="nccl"):
+        import torch
+        import torch.distributed as dist
+        self.ws, self.rank, self.device = ws, rank, torch.device(device)
+        self._dist = dist
+        if ws > 1 and not dist.is_initialized():
+            dist.init_process_group(backend)
+
+    def barrier(self):
+        import torch
+        if self.ws > 1:
+            self._dist.barrier()
+        if self.device.type == "cuda":
+            torch.cuda.synchronize(self.device)
+
+    def max_over_ranks(self, x):
+        import torch
+        if self.ws == 1:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=self.device)
+        self._dist.all_reduce(t, op=self._dist.ReduceOp.MAX)
+        return float(t.item())
+
+    def whole_job(self, units_per_rank, ms):
+        """Units per second over all ranks: every rank processed units_per_rank in at most ms."""
+        return self.ws * units_per_rank / (ms / 1e3)
+
+    def close(self):
+        if self.ws > 1 and self._dist.is_initialized():
+            self._dist.destroy_process_group()
+
+
 # ------------------------------------------------------------------------------------------
 # clocks
 # ------------------------------------------------------------------------------------------
@@ -232,20 +271,18 @@ def _prefill_e2e(args, d, buf, state_out, ring_out, stream, barrier, max_over_ra
     e2e_stop(e1)
     barrier()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1)) / Ke
-    return {"value": ws * T / (e2e_ms / 1e3), "unit": "tokens/s", "ms_per_step": e2e_ms,
+    return {"value": ws * T / (e2e_ms / 1e3), "unit": "tokens/s", "ms_per_step": e2e_ms,  # all ranks
             "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes,
             "pipeline": ("three streams: copy-in, prefill, copy-out" if fused else "one stream")}
 
 
 def run_ours(args):
     import torch
-    import torch.distributed as dist
 
     ws, rank, local = _dist()
-    if ws > 1:
-        dist.init_process_group("nccl")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
+    rep = Replicas(ws, rank, dev)
     import __graft_entry__
     __graft_entry__.build()
     from gated_delta_rule_scan_gb300 import inputs, kda, mixer
@@ -253,17 +290,7 @@ def run_ours(args):
     peaks = _peaks()
     stream = torch.cuda.current_stream()
 
-    def barrier():
-        if ws > 1:
-            dist.barrier()
-        torch.cuda.synchronize()
-
-    def max_over_ranks(x):
-        if ws == 1:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+    barrier, max_over_ranks = rep.barrier, rep.max_over_ranks
 
     # ---------------- prefill workload (resident) ----------------
     H, T = args.heads, PREFILL_T
@@ -331,7 +358,7 @@ def run_ours(args):
     kda.kernel_timing(False)
     ms = max_over_ranks(t0.elapsed_time(t1))
     ms_step = ms / K
-    tokens_per_s = ws * T / (ms_step / 1e3)
+    tokens_per_s = rep.whole_job(T, ms_step)
     if fused:
         scan_ms = sum(ktimes[k][1] for k in ("kda_chunk_prep_intra_kernel", "kda_chunk_intra_kernel",
                                              "kda_chunk_inter_kernel", "kda_chunk_offsets_kernel")
@@ -382,8 +409,7 @@ def run_ours(args):
     dec_gbs = dec_bytes / (dec_ms / 1e3) / 1e9
     assert kda.kda_device_status() == 0
 
-    if ws > 1:
-        dist.destroy_process_group()
+    rep.close()
     if rank != 0:
         return None
 
