@@ -37,6 +37,7 @@ sys.path.insert(0, ROOT)
 METRIC = "KDA prefill tokens/s (H=64,d=128); decode state HBM GB/s vs peak"
 D = 128
 PREFILL_T, PREFILL_H = 4096, 64
+RB_T = 4                         # verify width of the rollback workload
 DEC_N, DEC_H = 64, 64
 FLOP_PER_TOKEN_HEAD = 7 * D * D   # decay D^2 + S^T k 2D^2 + rank-1 update 2D^2 + S^T q 2D^2
 SMS, FP32_LANES, SM_MAX_MHZ = 152, 128, 2070.0
@@ -409,6 +410,41 @@ def run_ours(args):
     dec_gbs = dec_bytes / (dec_ms / 1e3) / 1e9
     assert kda.kda_device_status() == 0
 
+    # ---------------- verify rollback (the decode kernel on accepted prefixes) ----------------
+    import numpy as np
+    ver = inputs.decode_step(N=DEC_N, T=RB_T, H=DEC_H, seed=5)
+    dv = {k: getattr(ver, k).to(dev) for k in
+          ("q_raw", "k_raw", "v_raw", "conv_w", "ring_in", "f_raw", "dt_bias", "a_log",
+           "beta_raw", "state_in", "norm_w", "gate_raw")}
+    keep_h = np.random.default_rng(6).integers(1, RB_T, size=DEC_N, endpoint=False)
+    keep_d = torch.from_numpy(keep_h.astype(np.int32)).to(dev)
+    rb_state = torch.empty_like(dv["state_in"])
+    rb_ring = torch.empty_like(dv["ring_in"])
+    y_rb = torch.empty(DEC_N * RB_T, DEC_H * D, device=dev)
+
+    def rollback():
+        kda.kda_verify_rollback(dv["q_raw"], dv["k_raw"], dv["v_raw"], dv["conv_w"], dv["ring_in"],
+                                rb_ring, dv["f_raw"], dv["dt_bias"], dv["a_log"], dv["beta_raw"],
+                                dv["state_in"], rb_state, dv["norm_w"], dv["gate_raw"], y_rb,
+                                keep_d, N=DEC_N, T=RB_T, H=DEC_H)
+
+    for _ in range(max(args.warmup, 3)):
+        rollback()
+    barrier()
+    r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    r0.record(stream)
+    for _ in range(Kd):
+        rollback()
+    r1.record(stream)
+    barrier()
+    rb_ms = max_over_ranks(r0.elapsed_time(r1)) / Kd
+    kept = int(keep_h.sum())
+    # state and ring read + written once per sequence; raw q/k/v, f, beta, z read and y written
+    # for the kept rows only
+    rb_bytes = (DEC_N * (DEC_H * D * D * 4 * 2 + 3 * C1 * 3 * 4 * 2)
+                + kept * (3 * C1 * 2 + C1 * 4 * 3 + DEC_H * 4) + 3 * C1 * 4 * 4 + C1 * 4 + D * 4)
+    assert kda.kda_device_status() == 0
+
     rep.close()
     if rank != 0:
         return None
@@ -478,6 +514,15 @@ def run_ours(args):
                                 "traffic": _traffic("kda_decode_fused_kernel",
                                                     ["kda_decode.cu", "kda_device.cuh"]),
                                 "bytes_per_launch": dec_bytes}},
+        "rollback": {"workload": f"{DEC_N} sequences, verify width {RB_T}, H={DEC_H}, accepted "
+                                 f"prefixes U[1, {RB_T - 1}] ({kept} rows kept), one "
+                                 "kda_verify_rollback launch",
+                     "ms_per_step": rb_ms,
+                     "roofline": {"bound": "hbm", "kernel": "kda_decode_fused_kernel",
+                                  "achieved": rb_bytes / (rb_ms / 1e3) / 1e9,
+                                  "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                  "frac": rb_bytes / (rb_ms / 1e3) / 1e9 / peaks["hbm_gbs"],
+                                  "bytes_per_launch": rb_bytes}},
         "clocks": clocks,
         "cpu_baseline": cpu,
     }

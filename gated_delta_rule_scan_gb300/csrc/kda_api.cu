@@ -221,6 +221,45 @@ int prefill_impl(const void* q_raw, const void* k_raw, const void* v_raw, int ra
     return cuda_status(launch_gated_rmsnorm(na, static_cast<cudaStream_t>(stream)));
 }
 
+int decode_impl(const void* q_raw, const void* k_raw, const void* v_raw, int raw_dtype,
+                const float* conv_w, const float* ring_in, float* ring_out, const float* f_raw,
+                const float* dt_bias, const float* a_log, int gate_mode, float gate_lb,
+                const float* beta_raw, const float* state_in, float* state_out,
+                const float* norm_w, const float* gate_raw, float* y, int N, int T, int H, int D,
+                int K, float l2_eps, float scale, float rms_eps, const int* keep, bool rollback,
+                void* stream) {
+    if (D != kHeadDim) return KDA_ERR_HEAD_DIM;
+    if (N < 0 || N > kMaxGridY || H <= 0 || H > kMaxGridY || T < 1 || T > kDecodeMaxT)
+        return KDA_ERR_SHAPE;
+    if (raw_dtype != KDA_DTYPE_F32 && raw_dtype != KDA_DTYPE_BF16) return KDA_ERR_ENUM;
+    if (gate_mode != KDA_GATE_PER_CHANNEL && gate_mode != KDA_GATE_PER_HEAD) return KDA_ERR_ENUM;
+    if (K < 2 || K > kMaxConvK) return KDA_ERR_CONV_K;
+    if (N == 0) return KDA_OK;
+    if (!q_raw || !k_raw || !v_raw || !conv_w || !ring_in || !ring_out || !f_raw || !dt_bias ||
+        !a_log || !beta_raw || !state_in || !state_out || !norm_w || !gate_raw || !y)
+        return KDA_ERR_NULL;
+    if (!aligned16(state_in) || !aligned16(state_out) || !aligned16(norm_w) ||
+        !aligned16(gate_raw) || !aligned16(y))
+        return KDA_ERR_ALIGN;
+    const size_t sb = (size_t)N * H * kHeadDim * kHeadDim * sizeof(float);
+    if (overlap(state_in, state_out, sb)) return KDA_ERR_STATE_ALIAS;
+    if (ring_in != ring_out) {
+        const size_t rb = (size_t)N * 3 * H * kHeadDim * (K - 1) * sizeof(float);
+        if (overlap(ring_in, ring_out, rb)) return KDA_ERR_STATE_ALIAS;
+    }
+    DecodeArgs a{};
+    a.q_raw = q_raw; a.k_raw = k_raw; a.v_raw = v_raw; a.raw_bf16 = raw_dtype == KDA_DTYPE_BF16;
+    a.conv_w = conv_w; a.ring_in = ring_in; a.ring_out = ring_out;
+    a.f_raw = f_raw; a.dt_bias = dt_bias; a.a_log = a_log; a.gate_mode = gate_mode;
+    a.gate_lb = gate_lb; a.beta_raw = beta_raw; a.state_in = state_in; a.state_out = state_out;
+    a.norm_w = norm_w; a.gate_raw = gate_raw; a.y = y;
+    a.N = N; a.T = T; a.H = H; a.K = K; a.l2_eps = l2_eps; a.scale = scale; a.rms_eps = rms_eps;
+    if (rollback && keep == nullptr) return KDA_ERR_NULL;
+    a.keep = keep;
+    return cuda_status(launch_decode_fused(a, static_cast<cudaStream_t>(stream)));
+}
+
+
 }  // namespace
 
 extern "C" {
@@ -376,6 +415,7 @@ int kda_gated_rmsnorm_out(const float* o, const float* norm_w, const float* gate
     return cuda_status(launch_gated_rmsnorm(a, static_cast<cudaStream_t>(stream)));
 }
 
+
 int kda_decode_fused(const void* q_raw, const void* k_raw, const void* v_raw, int raw_dtype,
                      const float* conv_w, const float* ring_in, float* ring_out,
                      const float* f_raw, const float* dt_bias, const float* a_log, int gate_mode,
@@ -383,33 +423,21 @@ int kda_decode_fused(const void* q_raw, const void* k_raw, const void* v_raw, in
                      float* state_out, const float* norm_w, const float* gate_raw, float* y,
                      int N, int T, int H, int D, int K, float l2_eps, float scale, float rms_eps,
                      void* stream) {
-    if (D != kHeadDim) return KDA_ERR_HEAD_DIM;
-    if (N < 0 || N > kMaxGridY || H <= 0 || H > kMaxGridY || T < 1 || T > kDecodeMaxT)
-        return KDA_ERR_SHAPE;
-    if (raw_dtype != KDA_DTYPE_F32 && raw_dtype != KDA_DTYPE_BF16) return KDA_ERR_ENUM;
-    if (gate_mode != KDA_GATE_PER_CHANNEL && gate_mode != KDA_GATE_PER_HEAD) return KDA_ERR_ENUM;
-    if (K < 2 || K > kMaxConvK) return KDA_ERR_CONV_K;
-    if (N == 0) return KDA_OK;
-    if (!q_raw || !k_raw || !v_raw || !conv_w || !ring_in || !ring_out || !f_raw || !dt_bias ||
-        !a_log || !beta_raw || !state_in || !state_out || !norm_w || !gate_raw || !y)
-        return KDA_ERR_NULL;
-    if (!aligned16(state_in) || !aligned16(state_out) || !aligned16(norm_w) ||
-        !aligned16(gate_raw) || !aligned16(y))
-        return KDA_ERR_ALIGN;
-    const size_t sb = (size_t)N * H * kHeadDim * kHeadDim * sizeof(float);
-    if (overlap(state_in, state_out, sb)) return KDA_ERR_STATE_ALIAS;
-    if (ring_in != ring_out) {
-        const size_t rb = (size_t)N * 3 * H * kHeadDim * (K - 1) * sizeof(float);
-        if (overlap(ring_in, ring_out, rb)) return KDA_ERR_STATE_ALIAS;
-    }
-    DecodeArgs a{};
-    a.q_raw = q_raw; a.k_raw = k_raw; a.v_raw = v_raw; a.raw_bf16 = raw_dtype == KDA_DTYPE_BF16;
-    a.conv_w = conv_w; a.ring_in = ring_in; a.ring_out = ring_out;
-    a.f_raw = f_raw; a.dt_bias = dt_bias; a.a_log = a_log; a.gate_mode = gate_mode;
-    a.gate_lb = gate_lb; a.beta_raw = beta_raw; a.state_in = state_in; a.state_out = state_out;
-    a.norm_w = norm_w; a.gate_raw = gate_raw; a.y = y;
-    a.N = N; a.T = T; a.H = H; a.K = K; a.l2_eps = l2_eps; a.scale = scale; a.rms_eps = rms_eps;
-    return cuda_status(launch_decode_fused(a, static_cast<cudaStream_t>(stream)));
+    return decode_impl(q_raw, k_raw, v_raw, raw_dtype, conv_w, ring_in, ring_out, f_raw, dt_bias,
+                       a_log, gate_mode, gate_lb, beta_raw, state_in, state_out, norm_w, gate_raw,
+                       y, N, T, H, D, K, l2_eps, scale, rms_eps, nullptr, false, stream);
+}
+
+int kda_verify_rollback(const void* q_raw, const void* k_raw, const void* v_raw, int raw_dtype,
+                        const float* conv_w, const float* ring_in, float* ring_out,
+                        const float* f_raw, const float* dt_bias, const float* a_log,
+                        int gate_mode, float gate_lb, const float* beta_raw,
+                        const float* state_in, float* state_out, const float* norm_w,
+                        const float* gate_raw, float* y, const int* keep, int N, int T, int H,
+                        int D, int K, float l2_eps, float scale, float rms_eps, void* stream) {
+    return decode_impl(q_raw, k_raw, v_raw, raw_dtype, conv_w, ring_in, ring_out, f_raw, dt_bias,
+                       a_log, gate_mode, gate_lb, beta_raw, state_in, state_out, norm_w, gate_raw,
+                       y, N, T, H, D, K, l2_eps, scale, rms_eps, keep, true, stream);
 }
 
 int kda_device_status(void* stream) {

@@ -35,9 +35,11 @@ __global__ void __launch_bounds__(kDecThreads, 2) kda_decode_fused_kernel(Decode
 
     const int h = blockIdx.x, n = blockIdx.y;
     const int tid = threadIdx.x;
-    const int H = a.H, T = a.T, K = a.K, R = a.K - 1;
+    const int H = a.H, K = a.K, R = a.K - 1;
     const long C = (long)H * kHeadDim;
-    const long row0 = (long)n * T;
+    const long row0 = (long)n * a.T;             // rows of sequence n: stride T in every mode
+    // tokens taken: all T, or (rollback) the first keep[n]
+    const int T = a.keep != nullptr ? min(max(a.keep[n], 0), a.T) : a.T;
     const int warp = tid >> 5, lane = tid & 31;
     const int grp = lane >> 3, r = lane & 7;
 

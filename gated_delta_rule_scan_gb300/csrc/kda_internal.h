@@ -54,6 +54,8 @@ struct DecodeArgs {
     const float* state_in; float* state_out;
     const float* norm_w; const float* gate_raw; float* y;
     int N; int T; int H; int K; float l2_eps; float scale; float rms_eps;
+    const int* keep;         // rollback: tokens of sequence n to take (device [N], clamped to
+                             // 0..T; rows keep their stride T), or null for all T
 };
 
 cudaError_t launch_prep(const PrepArgs& a, cudaStream_t s);

@@ -73,6 +73,9 @@ _lib.kda_kernel_name.restype = ctypes.c_char_p
 _lib.kda_kernel_name.argtypes = [_I]
 _lib.kda_decode_fused.argtypes = [_P, _P, _P, _I, _P, _P, _P, _P, _P, _P, _I, _F, _P, _P, _P, _P,
                                   _P, _P, _I, _I, _I, _I, _I, _F, _F, _F, _P]
+_lib.kda_verify_rollback.restype = _I
+_lib.kda_verify_rollback.argtypes = [_P, _P, _P, _I, _P, _P, _P, _P, _P, _P, _I, _F, _P, _P, _P,
+                                     _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _F, _F, _P]
 _lib.kda_device_status.restype = _I
 _lib.kda_device_status.argtypes = [_P]
 
@@ -82,7 +85,7 @@ EXPORTED = ("kda_abi_version", "kda_status_string", "kda_conv_l2norm_prep",
             "kda_scan_varlen", "kda_gated_rmsnorm_out", "kda_decode_fused", "kda_device_status",
             "kda_scan_varlen_static", "kda_prefill_workspace_bytes", "kda_prefill_fused",
             "kda_prefill_fused_varlen", "kda_kernel_timing", "kda_kernel_times",
-            "kda_kernel_name")
+            "kda_kernel_name", "kda_verify_rollback")
 
 
 class KdaError(RuntimeError):
@@ -222,6 +225,20 @@ def kda_decode_fused(q_raw, k_raw, v_raw, conv_w, ring_in, ring_out, f_raw, dt_b
         _ptr(ring_out), _ptr(f_raw), _ptr(dt_bias), _ptr(a_log), gate_mode, gate_lb,
         _ptr(beta_raw), _ptr(state_in), _ptr(state_out), _ptr(norm_w), _ptr(gate_raw), _ptr(y),
         N, T, H, D, K, l2_eps, scale, rms_eps, st))
+
+
+def kda_verify_rollback(q_raw, k_raw, v_raw, conv_w, ring_in, ring_out, f_raw, dt_bias, a_log,
+                        beta_raw, state_in, state_out, norm_w, gate_raw, y, keep, *, N, T, H, K=4,
+                        gate_mode=0, gate_lb=-5.0, l2_eps=1e-6, scale=None, rms_eps=1e-6,
+                        D=HEAD_DIM, stream=None):
+    """keep: int32 device tensor [N], tokens accepted per sequence of the T-token verify batch."""
+    scale = D ** -0.5 if scale is None else scale
+    st = _stream(stream, y)
+    _check("kda_verify_rollback", _lib.kda_verify_rollback(
+        _ptr(q_raw), _ptr(k_raw), _ptr(v_raw), _raw_dtype(q_raw), _ptr(conv_w), _ptr(ring_in),
+        _ptr(ring_out), _ptr(f_raw), _ptr(dt_bias), _ptr(a_log), gate_mode, gate_lb,
+        _ptr(beta_raw), _ptr(state_in), _ptr(state_out), _ptr(norm_w), _ptr(gate_raw), _ptr(y),
+        _ptr(keep), N, T, H, D, K, l2_eps, scale, rms_eps, st))
 
 
 def kda_prefill_workspace_bytes(N, total_T, H, gate_mode=0, D=HEAD_DIM) -> int:

@@ -132,6 +132,26 @@ def kda_decode(*, q_raw, k_raw, v_raw, conv_w, ring_in, f_raw, dt_bias, a_log, b
     return dict(y=y, state_out=state_out, ring_out=ring_out)
 
 
+def kda_verify_rollback(*, q_raw, k_raw, v_raw, conv_w, ring_in, f_raw, dt_bias, a_log,
+                        beta_raw, state_in, norm_w, gate_raw, keep, N, T, H, K=4, gate_mode=0,
+                        gate_lb=-5.0, l2_eps=1e-6, rms_eps=1e-6, scale=None, state_out=None,
+                        ring_out=None, y=None, stream=None):
+    """Roll a T-token verify round back to the accepted prefixes: keep (int32 device [N]) tokens
+    of each sequence, from the pre-round state_in and ring_in.  ring_out may be ring_in."""
+    if state_out is None:
+        state_out = torch.empty_like(state_in)
+    if ring_out is None:
+        ring_out = torch.empty_like(ring_in)
+    if y is None:
+        y = torch.zeros((q_raw.shape[0], H * kda.HEAD_DIM), dtype=torch.float32,
+                        device=q_raw.device)
+    kda.kda_verify_rollback(q_raw, k_raw, v_raw, conv_w, ring_in, ring_out, f_raw, dt_bias,
+                            a_log, beta_raw, state_in, state_out, norm_w, gate_raw, y, keep,
+                            N=N, T=T, H=H, K=K, gate_mode=gate_mode, gate_lb=gate_lb,
+                            l2_eps=l2_eps, scale=scale, rms_eps=rms_eps, stream=stream)
+    return dict(y=y, state_out=state_out, ring_out=ring_out)
+
+
 class HostPrefillStream:
     """Prefill over batches that live in pinned host memory, pipelined over three CUDA streams:
     while batch i runs kda_prefill on the device, batch i+1 is copied in and the results of

@@ -303,6 +303,30 @@ int kda_decode_fused(const void* q_raw, const void* k_raw, const void* v_raw, in
                      void* stream);
 
 /*
+ * kda_verify_rollback -- the rollback of a speculative verify round (kda_verify_rollback_rows,
+ * memra_engine/kda.rs, memra-engine 0.125.0: restore the pre-round conv ring, re-roll the kept
+ * raw rows, replay the scan at T = keep from the pre-round state): from the state and ring BEFORE
+ * a T-token verify, take only the first keep[n] rows of each sequence n of the same verify batch
+ * and produce the state, ring and y rows that keep[n] chained one-token kda_decode_fused calls
+ * would, bit for bit (the decode == verify identity applied to the accepted prefix).  One launch;
+ * the prep of the kept rows is recomputed from the raw rows with the verify's own arithmetic.
+ * Arguments as in kda_decode_fused, plus
+ * keep        device int32 [N]: tokens accepted per sequence, clamped to 0..T on the device
+ *             (keep[n] = 0 leaves state and ring of sequence n as they were).  NULL returns 40004.
+ * The raw rows, f, beta and gate_raw keep the verify batch's layout: row n*T + t.  ring_in must
+ * hold the ring from before the round (the verify call may not have rolled it in place, or the
+ * caller keeps a copy); state_in the state from before the round (a verify never writes it,
+ * since its state_out is another buffer).  y rows n*T + t are written for t < keep[n] only.
+ */
+int kda_verify_rollback(const void* q_raw, const void* k_raw, const void* v_raw, int raw_dtype,
+                        const float* conv_w, const float* ring_in, float* ring_out,
+                        const float* f_raw, const float* dt_bias, const float* a_log,
+                        int gate_mode, float gate_lb, const float* beta_raw,
+                        const float* state_in, float* state_out, const float* norm_w,
+                        const float* gate_raw, float* y, const int* keep, int N, int T, int H,
+                        int D, int K, float l2_eps, float scale, float rms_eps, void* stream);
+
+/*
  * kda_device_status -- synchronises `stream`, then reports and clears the device error word on
  * the current device: 0, or 40008 when a kernel gave up a bounded device wait since the last
  * check (its outputs are then incomplete), or 10000 + cudaError_t.
