@@ -287,22 +287,25 @@ void orc_scan_gdn(const double* q, const double* k, const double* v, const doubl
 }
 
 /* ------------------------------------------------------------------------------------------ */
-/* a6: sigmoid-gated RMSNorm over head_dim                                                      */
+/* a6: gated RMSNorm over head_dim                                                              */
 /* ------------------------------------------------------------------------------------------ */
 
 /*
- * [KDA] stage 6 and `Engine::kda_gated_rmsnorm` (KDA gates with sigmoid; the gate itself is not
- * normalised, [GDN] `gdn_gated_rmsnorm_into` doc), per row of length D:
- *     y_i = o_i / sqrt( (1/D) sum_i o_i^2 + eps ) * w_i * sigmoid(z_i)
- * w is [D], shared by all heads.
+ * [KDA] stage 6 and `Engine::kda_gated_rmsnorm` (the gate itself is not normalised, [GDN]
+ * `gdn_gated_rmsnorm_into` doc), per row of length D:
+ *     y_i = o_i / sqrt( (1/D) sum_i o_i^2 + eps ) * w_i * gate(z_i)
+ * w is [D], shared by all heads.  gate = sigmoid (KDA, silu_gate = 0) or SiLU, z * sigmoid(z)
+ * (GDN's `gated_rmsnorm`, silu_gate = 1; the `Engine::kda_gated_rmsnorm` doc contrasts the two).
  */
 void orc_gated_rmsnorm(const double* o, const double* w, const double* z, double* y, long rows,
-                       int D, double eps) {
+                       int D, double eps, int silu_gate) {
     for (long r = 0; r < rows; ++r) {
         double ss = 0.0;
         for (int i = 0; i < D; ++i) ss += o[r * D + i] * o[r * D + i];
         const double inv = 1.0 / sqrt(ss / D + eps);
-        for (int i = 0; i < D; ++i)
-            y[r * D + i] = o[r * D + i] * inv * w[i] * sigmoid(z[r * D + i]);
+        for (int i = 0; i < D; ++i) {
+            const double zi = z[r * D + i];
+            y[r * D + i] = o[r * D + i] * inv * w[i] * (silu_gate ? silu(zi) : sigmoid(zi));
+        }
     }
 }

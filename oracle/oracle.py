@@ -67,7 +67,7 @@ def _bind(path: str):
     lib.orc_sigmoid.argtypes = [dp, dp, L]
     for fn in (lib.orc_scan_kda, lib.orc_scan_gdn):
         fn.argtypes = [dp, dp, dp, dp, dp, lp, I, I, I, dp, dp, dp, D]
-    lib.orc_gated_rmsnorm.argtypes = [dp, dp, dp, dp, L, I, D]
+    lib.orc_gated_rmsnorm.argtypes = [dp, dp, dp, dp, L, I, D, I]
     for name in ("orc_conv_silu", "orc_l2norm", "orc_gate_kda", "orc_gate_gdn",
                  "orc_sigmoid", "orc_scan_kda", "orc_scan_gdn", "orc_gated_rmsnorm"):
         getattr(lib, name).restype = None
@@ -198,12 +198,16 @@ def scan_gdn(q, k, v, g, beta, state_in, cu_seqlens=None, scale=None):
     return o, st
 
 
-def gated_rmsnorm(o, w, z, eps: float = 1e-6):
-    """a6 over rows of length D = w.size."""
+def gated_rmsnorm(o, w, z, eps: float = 1e-6, gate: str = "sigmoid"):
+    """a6 over rows of length D = w.size; gate "sigmoid" (KDA) or "silu" (GDN's
+    gated_rmsnorm)."""
+    if gate not in ("sigmoid", "silu"):
+        raise ValueError(gate)
     o, w, z = _f64(o), _f64(w), _f64(z)
     D = w.size
     y = np.empty_like(o)
-    _load().orc_gated_rmsnorm(_p(o), _p(w), _p(z), _p(y), o.size // D, D, eps)
+    _load().orc_gated_rmsnorm(_p(o), _p(w), _p(z), _p(y), o.size // D, D, eps,
+                              1 if gate == "silu" else 0)
     return y
 
 
@@ -214,7 +218,7 @@ def gated_rmsnorm(o, w, z, eps: float = 1e-6):
 def forward(*, q_raw, k_raw, v_raw, f_raw, dt_bias, a_log, beta_raw, state_in, H, D,
             conv_w=None, ring_in=None, cu_seqlens=None, gate_mode=0, gate_lb=-5.0,
             norm_w=None, gate_raw=None, l2_eps=1e-6, rms_eps=1e-6, scale=None,
-            scalar_scan=False):
+            scalar_scan=False, norm_gate="sigmoid"):
     """The mixer from projected channels to the gated output, in the pages' stage order
     (conv+SiLU -> ring roll -> l2 norm -> gates -> scan -> gated RMSNorm).
 
@@ -226,6 +230,7 @@ def forward(*, q_raw, k_raw, v_raw, f_raw, dt_bias, a_log, beta_raw, state_in, H
     state_in: [N, H, D, D] (M[j][i] layout).
     norm_w: [D] and gate_raw: [rows, C], or None for no epilogue.
     scalar_scan: run the separate scalar-gate routine (gate_mode 1 only).
+    norm_gate: the RMSNorm's gate, "sigmoid" (KDA) or "silu" (GDN's gated_rmsnorm).
     Returns a dict with q_hat, k_hat, v_hat, g, beta, o, y (or None), state_out, ring_out.
     """
     C = H * D
@@ -272,7 +277,8 @@ def forward(*, q_raw, k_raw, v_raw, f_raw, dt_bias, a_log, beta_raw, state_in, H
                          state_in, cu, scale)
     y = None
     if norm_w is not None:
-        y = gated_rmsnorm(o.reshape(rows, C), norm_w, gate_raw, rms_eps).reshape(rows, C)
+        y = gated_rmsnorm(o.reshape(rows, C), norm_w, gate_raw, rms_eps,
+                          norm_gate).reshape(rows, C)
     return dict(q_hat=q_hat.reshape(rows, C), k_hat=k_hat.reshape(rows, C),
                 v_hat=v_hat.reshape(rows, C), g=g, beta=beta, o=o.reshape(rows, C), y=y,
                 state_out=st, ring_out=ring_out)

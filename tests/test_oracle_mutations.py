@@ -52,8 +52,10 @@ MUTATIONS = [
      "sq += (col[i] - b * k[row + i] * uj) * q[row + i];"),
     ("rmsnorm_sum_not_mean", "const double inv = 1.0 / sqrt(ss / D + eps);",
      "const double inv = 1.0 / sqrt(ss + eps);"),
-    ("rmsnorm_gate_silu", "y[r * D + i] = o[r * D + i] * inv * w[i] * sigmoid(z[r * D + i]);",
-     "y[r * D + i] = o[r * D + i] * inv * w[i] * silu(z[r * D + i]);"),
+    ("rmsnorm_gate_silu", "(silu_gate ? silu(zi) : sigmoid(zi))",
+     "(silu_gate ? silu(zi) : silu(zi))"),
+    ("rmsnorm_silu_gate_is_sigmoid", "(silu_gate ? silu(zi) : sigmoid(zi))",
+     "(silu_gate ? sigmoid(zi) : sigmoid(zi))"),
 ]
 
 

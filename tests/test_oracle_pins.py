@@ -12,6 +12,7 @@ Which pin covers which oracle routine:
   gate_gdn        alpha + dt_bias = 0 gives -exp(A_log) ln 2; large-argument limit.
   sigmoid         closed values.
   gated_rmsnorm   w = 1, z -> +inf reduces to a plain RMSNorm closed form; gate factor.
+  gated_rmsnorm_silu   the SiLU-gated mode at hand values (sigmoid(ln 3) = 3/4) and z -> +inf.
   forward         split-at-every-point state carry (bit-equal); T-token call equals T chained
                   one-token calls (bit-equal).
 Every check is a plain function so test_oracle_mutations.py can run it against mutated oracle
@@ -304,6 +305,24 @@ def check_gated_rmsnorm():
     np.testing.assert_allclose(y2, want * w / (1 + np.exp(-z)), rtol=1e-13)
 
 
+def check_gated_rmsnorm_silu():
+    """The SiLU-gated mode (GDN's gated_rmsnorm): hand values, D = 2, o = (3, 4), w = 1, eps = 0,
+    so o / rms = (3, 4) / sqrt(12.5); silu(0) = 0 and silu(ln 3) = (3/4) ln 3 exactly
+    (sigmoid(ln 3) = 3/4).  And z -> +inf: silu(z) = z, a plain RMSNorm times z."""
+    o = np.array([[3.0, 4.0], [3.0, 4.0]])
+    z = np.array([[0.0, np.log(3.0)], [np.log(3.0), 0.0]])
+    y = orc.gated_rmsnorm(o, np.ones(2), z, 0.0, gate="silu")
+    r = np.sqrt(12.5)
+    np.testing.assert_allclose(y, [[0.0, 4.0 / r * 0.75 * np.log(3.0)],
+                                   [3.0 / r * 0.75 * np.log(3.0), 0.0]], rtol=1e-15, atol=0)
+    rng = _rng(12)
+    D = 32
+    o = rng.standard_normal((4, D))
+    y = orc.gated_rmsnorm(o, np.ones(D), np.full((4, D), 1e3), 1e-6, gate="silu")
+    want = o / np.sqrt((o ** 2).mean(1, keepdims=True) + 1e-6) * 1e3
+    np.testing.assert_allclose(y, want, rtol=1e-14)
+
+
 # ------------------------------------------------------------------------------------------
 # whole-mixer state carry
 # ------------------------------------------------------------------------------------------
@@ -390,6 +409,7 @@ ALL_CHECKS = [
     check_orthonormal_recall, check_dense_product_form, check_chunked_form_every_chunk_size,
     check_default_scale, check_gdn_equals_broadcast_kda, check_conv_one_hot_shift,
     check_conv_taps_general, check_l2norm, check_gates, check_gated_rmsnorm,
+    check_gated_rmsnorm_silu,
     check_split_state_carry, check_chained_single_tokens_equal_multi_token,
     check_varlen_equals_separate_calls,
 ]
