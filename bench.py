@@ -410,6 +410,32 @@ def run_ours(args):
     dec_gbs = dec_bytes / (dec_ms / 1e3) / 1e9
     assert kda.kda_device_status() == 0
 
+    # the same step in place (state and ring), captured once in a CUDA graph and replayed
+    g_state, g_ring = dd["state_in"].clone(), dd["ring_in"].clone()
+    g_y = torch.empty_like(y_dec)
+
+    def decode_in_place():
+        kda.kda_decode_fused(dd["q_raw"], dd["k_raw"], dd["v_raw"], dd["conv_w"], g_ring, g_ring,
+                             dd["f_raw"], dd["dt_bias"], dd["a_log"], dd["beta_raw"], g_state,
+                             g_state, dd["norm_w"], dd["gate_raw"], g_y, N=DEC_N, T=1, H=DEC_H)
+
+    decode_in_place()
+    barrier()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        decode_in_place()
+    for _ in range(max(args.warmup, 3)):
+        graph.replay()
+    barrier()
+    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    g0.record(stream)
+    for _ in range(Kd):
+        graph.replay()
+    g1.record(stream)
+    barrier()
+    dec_graph_ms = max_over_ranks(g0.elapsed_time(g1)) / Kd
+    assert kda.kda_device_status() == 0
+
     # ---------------- verify rollback (the decode kernel on accepted prefixes) ----------------
     import numpy as np
     ver = inputs.decode_step(N=DEC_N, T=RB_T, H=DEC_H, seed=5)
@@ -514,6 +540,14 @@ def run_ours(args):
                                 "traffic": _traffic("kda_decode_fused_kernel",
                                                     ["kda_decode.cu", "kda_device.cuh"]),
                                 "bytes_per_launch": dec_bytes}},
+        "decode_graph": {"workload": "the decode step in place (state and ring), captured once "
+                                     "in a CUDA graph and replayed",
+                         "ms_per_step": dec_graph_ms,
+                         "roofline": {"bound": "hbm", "kernel": "kda_decode_fused_kernel",
+                                      "achieved": dec_bytes / (dec_graph_ms / 1e3) / 1e9,
+                                      "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                      "frac": dec_bytes / (dec_graph_ms / 1e3) / 1e9
+                                      / peaks["hbm_gbs"], "bytes_per_launch": dec_bytes}},
         "rollback": {"workload": f"{DEC_N} sequences, verify width {RB_T}, H={DEC_H}, accepted "
                                  f"prefixes U[1, {RB_T - 1}] ({kept} rows kept), one "
                                  "kda_verify_rollback launch",

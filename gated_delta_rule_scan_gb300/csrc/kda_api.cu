@@ -186,6 +186,8 @@ int prefill_impl(const void* q_raw, const void* k_raw, const void* v_raw, int ra
     if (seq.N < 0 || seq.N > kMaxGridY || seq.total_rows < 0 || H <= 0 || H > kMaxGridY)
         return KDA_ERR_SHAPE;
     if (seq.total_rows >= (1L << 31)) return KDA_ERR_SHAPE;
+    const bool norm_silu = (gate_mode & KDA_NORM_SILU) != 0;
+    gate_mode &= ~KDA_NORM_SILU;
     if (gate_mode != KDA_GATE_PER_CHANNEL && gate_mode != KDA_GATE_PER_HEAD) return KDA_ERR_ENUM;
     if (seq.N == 0) return KDA_OK;
     if (seq.total_rows > 0) {
@@ -217,8 +219,20 @@ int prefill_impl(const void* q_raw, const void* k_raw, const void* v_raw, int ra
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
     rc = cuda_status(launch_prefill_chunk(pa, a, cu_host, w + L.chunk, st));
     if (rc != KDA_OK || seq.total_rows == 0) return rc;
-    NormArgs na{oh, norm_w, gate_raw, y, seq.total_rows * H, norm_eps};
+    NormArgs na{oh, norm_w, gate_raw, y, seq.total_rows * H, norm_eps, norm_silu ? 1 : 0};
     return cuda_status(launch_gated_rmsnorm(na, static_cast<cudaStream_t>(stream)));
+}
+
+int norm_impl(const float* o, const float* norm_w, const float* gate_raw, float* y, long rows,
+              int D, float eps, bool silu, void* stream) {
+    if (D != kHeadDim) return KDA_ERR_HEAD_DIM;
+    if (rows < 0) return KDA_ERR_SHAPE;
+    if (rows == 0) return KDA_OK;
+    if (!o || !norm_w || !gate_raw || !y) return KDA_ERR_NULL;
+    if (!aligned16(o) || !aligned16(norm_w) || !aligned16(gate_raw) || !aligned16(y))
+        return KDA_ERR_ALIGN;
+    NormArgs a{o, norm_w, gate_raw, y, rows, eps, silu ? 1 : 0};
+    return cuda_status(launch_gated_rmsnorm(a, static_cast<cudaStream_t>(stream)));
 }
 
 int decode_impl(const void* q_raw, const void* k_raw, const void* v_raw, int raw_dtype,
@@ -232,6 +246,8 @@ int decode_impl(const void* q_raw, const void* k_raw, const void* v_raw, int raw
     if (N < 0 || N > kMaxGridY || H <= 0 || H > kMaxGridY || T < 1 || T > kDecodeMaxT)
         return KDA_ERR_SHAPE;
     if (raw_dtype != KDA_DTYPE_F32 && raw_dtype != KDA_DTYPE_BF16) return KDA_ERR_ENUM;
+    const bool norm_silu = (gate_mode & KDA_NORM_SILU) != 0;
+    gate_mode &= ~KDA_NORM_SILU;
     if (gate_mode != KDA_GATE_PER_CHANNEL && gate_mode != KDA_GATE_PER_HEAD) return KDA_ERR_ENUM;
     if (K < 2 || K > kMaxConvK) return KDA_ERR_CONV_K;
     if (N == 0) return KDA_OK;
@@ -242,7 +258,9 @@ int decode_impl(const void* q_raw, const void* k_raw, const void* v_raw, int raw
         !aligned16(gate_raw) || !aligned16(y))
         return KDA_ERR_ALIGN;
     const size_t sb = (size_t)N * H * kHeadDim * kHeadDim * sizeof(float);
-    if (overlap(state_in, state_out, sb)) return KDA_ERR_STATE_ALIAS;
+    // in place (state_out == state_in) is allowed: every thread loads its part of its (sequence,
+    // head) block before it stores the same elements; a partial overlap is not
+    if (state_in != state_out && overlap(state_in, state_out, sb)) return KDA_ERR_STATE_ALIAS;
     if (ring_in != ring_out) {
         const size_t rb = (size_t)N * 3 * H * kHeadDim * (K - 1) * sizeof(float);
         if (overlap(ring_in, ring_out, rb)) return KDA_ERR_STATE_ALIAS;
@@ -256,6 +274,7 @@ int decode_impl(const void* q_raw, const void* k_raw, const void* v_raw, int raw
     a.N = N; a.T = T; a.H = H; a.K = K; a.l2_eps = l2_eps; a.scale = scale; a.rms_eps = rms_eps;
     if (rollback && keep == nullptr) return KDA_ERR_NULL;
     a.keep = keep;
+    a.norm_silu = norm_silu ? 1 : 0;
     return cuda_status(launch_decode_fused(a, static_cast<cudaStream_t>(stream)));
 }
 
@@ -334,6 +353,7 @@ size_t kda_scan_workspace_bytes(int N, int total_T, int H, int D, int gate_mode,
 
 size_t kda_prefill_workspace_bytes(int N, int total_T, int H, int D, int gate_mode) {
     if (N < 0 || total_T < 0 || H <= 0 || D != kHeadDim) return 0;
+    gate_mode &= ~KDA_NORM_SILU;
     if (gate_mode != KDA_GATE_PER_CHANNEL && gate_mode != KDA_GATE_PER_HEAD) return 0;
     return prefill_layout(total_T, H).chunk +
            kda_scan_workspace_bytes(N, total_T, H, D, gate_mode, KDA_ALGO_CHUNK);
@@ -405,14 +425,12 @@ int kda_scan_varlen(const float* q_hat, const float* k_hat, const float* v_hat, 
 
 int kda_gated_rmsnorm_out(const float* o, const float* norm_w, const float* gate_raw, float* y,
                           long rows, int D, float eps, void* stream) {
-    if (D != kHeadDim) return KDA_ERR_HEAD_DIM;
-    if (rows < 0) return KDA_ERR_SHAPE;
-    if (rows == 0) return KDA_OK;
-    if (!o || !norm_w || !gate_raw || !y) return KDA_ERR_NULL;
-    if (!aligned16(o) || !aligned16(norm_w) || !aligned16(gate_raw) || !aligned16(y))
-        return KDA_ERR_ALIGN;
-    NormArgs a{o, norm_w, gate_raw, y, rows, eps};
-    return cuda_status(launch_gated_rmsnorm(a, static_cast<cudaStream_t>(stream)));
+    return norm_impl(o, norm_w, gate_raw, y, rows, D, eps, false, stream);
+}
+
+int kda_gated_rmsnorm_silu_out(const float* o, const float* norm_w, const float* gate_raw,
+                               float* y, long rows, int D, float eps, void* stream) {
+    return norm_impl(o, norm_w, gate_raw, y, rows, D, eps, true, stream);
 }
 
 

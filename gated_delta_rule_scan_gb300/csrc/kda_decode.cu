@@ -156,10 +156,17 @@ __global__ void __launch_bounds__(kDecThreads, 2) kda_decode_fused_kernel(Decode
         const float4 w4 = *reinterpret_cast<const float4*>(a.norm_w + 4 * lane);
         const float4 z4 = *reinterpret_cast<const float4*>(a.gate_raw + base);
         float4 y4;
-        y4.x = gated_norm_f(o4.x, inv, w4.x, z4.x);
-        y4.y = gated_norm_f(o4.y, inv, w4.y, z4.y);
-        y4.z = gated_norm_f(o4.z, inv, w4.z, z4.z);
-        y4.w = gated_norm_f(o4.w, inv, w4.w, z4.w);
+        if (a.norm_silu) {
+            y4.x = gated_norm_f<true>(o4.x, inv, w4.x, z4.x);
+            y4.y = gated_norm_f<true>(o4.y, inv, w4.y, z4.y);
+            y4.z = gated_norm_f<true>(o4.z, inv, w4.z, z4.z);
+            y4.w = gated_norm_f<true>(o4.w, inv, w4.w, z4.w);
+        } else {
+            y4.x = gated_norm_f(o4.x, inv, w4.x, z4.x);
+            y4.y = gated_norm_f(o4.y, inv, w4.y, z4.y);
+            y4.z = gated_norm_f(o4.z, inv, w4.z, z4.z);
+            y4.w = gated_norm_f(o4.w, inv, w4.w, z4.w);
+        }
         *reinterpret_cast<float4*>(a.y + base) = y4;
     }
 }

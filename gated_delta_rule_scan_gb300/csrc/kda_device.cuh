@@ -58,9 +58,11 @@ __device__ __forceinline__ float rms_inv_f(float ss, float eps) {
     return rsqrtf(__fmul_rn(ss, 1.0f / kHeadDim) + eps);
 }
 
-// one gated-RMSNorm output element: ((o * inv) * w) * sigmoid(z)
+// one gated-RMSNorm output element: ((o * inv) * w) * gate(z), gate = sigmoid (KDA) or SiLU
+// (GDN's gated_rmsnorm)
+template <bool SILU = false>
 __device__ __forceinline__ float gated_norm_f(float o, float inv, float w, float z) {
-    return __fmul_rn(__fmul_rn(__fmul_rn(o, inv), w), sigmoid_f(z));
+    return __fmul_rn(__fmul_rn(__fmul_rn(o, inv), w), SILU ? silu_f(z) : sigmoid_f(z));
 }
 
 // Causal conv taps over a register window win[0..KW-1] whose last K slots hold the K samples

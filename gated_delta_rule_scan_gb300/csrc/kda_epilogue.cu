@@ -13,6 +13,7 @@
 
 namespace kda {
 
+template <bool SILU>
 __global__ void __launch_bounds__(256) kda_gated_rmsnorm_kernel(NormArgs a) {
     const long row = (long)blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
@@ -27,10 +28,10 @@ __global__ void __launch_bounds__(256) kda_gated_rmsnorm_kernel(NormArgs a) {
     const float4 w4 = *reinterpret_cast<const float4*>(a.w + 4 * lane);
     const float4 z4 = __ldcs(reinterpret_cast<const float4*>(a.z + base));
     float4 y4;
-    y4.x = gated_norm_f(o4.x, inv, w4.x, z4.x);
-    y4.y = gated_norm_f(o4.y, inv, w4.y, z4.y);
-    y4.z = gated_norm_f(o4.z, inv, w4.z, z4.z);
-    y4.w = gated_norm_f(o4.w, inv, w4.w, z4.w);
+    y4.x = gated_norm_f<SILU>(o4.x, inv, w4.x, z4.x);
+    y4.y = gated_norm_f<SILU>(o4.y, inv, w4.y, z4.y);
+    y4.z = gated_norm_f<SILU>(o4.z, inv, w4.z, z4.z);
+    y4.w = gated_norm_f<SILU>(o4.w, inv, w4.w, z4.w);
     __stcs(reinterpret_cast<float4*>(a.y + base), y4);
 }
 
@@ -38,7 +39,8 @@ cudaError_t launch_gated_rmsnorm(const NormArgs& a, cudaStream_t s) {
     if (a.rows == 0) return cudaSuccess;
     const long blocks = (a.rows + 7) / 8;
     KernelTimer kt(kKRmsNorm, s);
-    kda_gated_rmsnorm_kernel<<<(unsigned)blocks, 256, 0, s>>>(a);
+    if (a.silu) kda_gated_rmsnorm_kernel<true><<<(unsigned)blocks, 256, 0, s>>>(a);
+    else kda_gated_rmsnorm_kernel<false><<<(unsigned)blocks, 256, 0, s>>>(a);
     return cudaGetLastError();
 }
 

@@ -44,6 +44,7 @@ struct ScanArgs {
 
 struct NormArgs {
     const float* o; const float* w; const float* z; float* y; long rows; float eps;
+    int silu;                // gate: 0 sigmoid (KDA), 1 SiLU (GDN's gated_rmsnorm)
 };
 
 struct DecodeArgs {
@@ -56,6 +57,7 @@ struct DecodeArgs {
     int N; int T; int H; int K; float l2_eps; float scale; float rms_eps;
     const int* keep;         // rollback: tokens of sequence n to take (device [N], clamped to
                              // 0..T; rows keep their stride T), or null for all T
+    int norm_silu;           // RMSNorm gate: 0 sigmoid (KDA), 1 SiLU (GDN's gated_rmsnorm)
 };
 
 cudaError_t launch_prep(const PrepArgs& a, cudaStream_t s);

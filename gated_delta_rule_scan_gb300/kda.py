@@ -26,6 +26,7 @@ _lib = ctypes.CDLL(LIB_PATH)
 DTYPE_F32, DTYPE_BF16 = 0, 1
 GATE_PER_CHANNEL, GATE_PER_HEAD = 0, 1
 GATE_EXP = 2  # flag: g holds decay factors exp(log-decay)
+NORM_SILU = 4  # flag (fused entries): the RMSNorm gates with SiLU(z) instead of sigmoid(z)
 ALGO_AUTO, ALGO_SEQ, ALGO_CHUNK = 0, 1, 2
 HEAD_DIM = 128
 DECODE_MAX_T = 16
@@ -55,6 +56,8 @@ _lib.kda_scan_varlen_static.restype = _I
 _lib.kda_scan_varlen_static.argtypes = [_P, _P, _P, _P, _I, _P, _P, _P, _P, _P, _P, _I, _I, _I,
                                         _I, _F, _P]
 _lib.kda_gated_rmsnorm_out.argtypes = [_P, _P, _P, _P, _L, _I, _F, _P]
+_lib.kda_gated_rmsnorm_silu_out.restype = _I
+_lib.kda_gated_rmsnorm_silu_out.argtypes = [_P, _P, _P, _P, _L, _I, _F, _P]
 _lib.kda_decode_fused.restype = _I
 _lib.kda_prefill_workspace_bytes.restype = _Z
 _lib.kda_prefill_workspace_bytes.argtypes = [_I, _I, _I, _I, _I]
@@ -85,7 +88,7 @@ EXPORTED = ("kda_abi_version", "kda_status_string", "kda_conv_l2norm_prep",
             "kda_scan_varlen", "kda_gated_rmsnorm_out", "kda_decode_fused", "kda_device_status",
             "kda_scan_varlen_static", "kda_prefill_workspace_bytes", "kda_prefill_fused",
             "kda_prefill_fused_varlen", "kda_kernel_timing", "kda_kernel_times",
-            "kda_kernel_name", "kda_verify_rollback")
+            "kda_kernel_name", "kda_verify_rollback", "kda_gated_rmsnorm_silu_out")
 
 
 class KdaError(RuntimeError):
@@ -211,6 +214,13 @@ def kda_scan_varlen_static(q_hat, k_hat, v_hat, g, beta, state_in, state_out, o,
 def kda_gated_rmsnorm_out(o, norm_w, gate_raw, y, *, rows, eps=1e-6, D=HEAD_DIM, stream=None):
     st = _stream(stream, y)
     _check("kda_gated_rmsnorm_out", _lib.kda_gated_rmsnorm_out(
+        _ptr(o), _ptr(norm_w), _ptr(gate_raw), _ptr(y), rows, D, eps, st))
+
+
+def kda_gated_rmsnorm_silu_out(o, norm_w, gate_raw, y, *, rows, eps=1e-6, D=HEAD_DIM,
+                               stream=None):
+    st = _stream(stream, y)
+    _check("kda_gated_rmsnorm_silu_out", _lib.kda_gated_rmsnorm_silu_out(
         _ptr(o), _ptr(norm_w), _ptr(gate_raw), _ptr(y), rows, D, eps, st))
 
 

@@ -11,6 +11,12 @@ import torch
 from . import kda
 
 
+def _norm_flag(norm_gate):
+    if norm_gate not in ("sigmoid", "silu"):
+        raise ValueError(norm_gate)
+    return kda.NORM_SILU if norm_gate == "silu" else 0
+
+
 def _empty(shape, like):
     return torch.empty(shape, dtype=torch.float32, device=like.device)
 
@@ -19,7 +25,8 @@ def kda_forward(*, q_raw, k_raw, v_raw, f_raw, dt_bias, a_log, beta_raw, state_i
                 conv_w=None, ring_in=None, norm_w=None, gate_raw=None, cu_seqlens=None,
                 cu_seqlens_host=None, N=None, T=None, K=4, gate_mode=0, gate_lb=-5.0,
                 l2_eps=1e-6, rms_eps=1e-6, scale=None, algo=kda.ALGO_AUTO, state_out=None,
-                ring_out=None, out=None, gate_exp=None, workspace=None, stream=None):
+                ring_out=None, out=None, gate_exp=None, workspace=None, stream=None,
+                norm_gate="sigmoid"):
     """Run the mixer on device tensors.  Either (N, T) for N sequences of T tokens, or
     cu_seqlens (int32 device) + cu_seqlens_host (int32 CPU) for packed sequences.
     gate_exp: hand the gate from the prep to the scan as decay factors exp(log-decay) (the
@@ -28,6 +35,7 @@ def kda_forward(*, q_raw, k_raw, v_raw, f_raw, dt_bias, a_log, beta_raw, state_i
     chunked form consumes log-decays).
     workspace: scratch for the chunked form; allocated here when algo is AUTO or CHUNK and none
     is given.
+    norm_gate: the RMSNorm's gate, "sigmoid" (KDA) or "silu" (GDN's gated_rmsnorm).
     Returns a dict with q_hat, k_hat, v_hat, g, beta, o, y (None without an epilogue),
     state_out and ring_out."""
     D = kda.HEAD_DIM
@@ -74,8 +82,9 @@ def kda_forward(*, q_raw, k_raw, v_raw, f_raw, dt_bias, a_log, beta_raw, state_i
     y = None
     if norm_w is not None:
         y = take("y", (rows, C))
-        kda.kda_gated_rmsnorm_out(o, norm_w, gate_raw, y, rows=rows * H, eps=rms_eps,
-                                  stream=stream)
+        _norm_flag(norm_gate)
+        norm = kda.kda_gated_rmsnorm_silu_out if norm_gate == "silu" else kda.kda_gated_rmsnorm_out
+        norm(o, norm_w, gate_raw, y, rows=rows * H, eps=rms_eps, stream=stream)
     return dict(q_hat=q_hat, k_hat=k_hat, v_hat=v_hat, g=g, beta=beta, o=o, y=y,
                 state_out=state_out, ring_out=ring_out, n_seq=n_seq)
 
@@ -83,11 +92,13 @@ def kda_forward(*, q_raw, k_raw, v_raw, f_raw, dt_bias, a_log, beta_raw, state_i
 def kda_prefill(*, q_raw, k_raw, v_raw, f_raw, dt_bias, a_log, beta_raw, state_in, H, conv_w,
                 ring_in, norm_w, gate_raw, cu_seqlens=None, cu_seqlens_host=None, N=None, T=None,
                 K=4, gate_mode=0, gate_lb=-5.0, l2_eps=1e-6, rms_eps=1e-6, scale=None,
-                state_out=None, ring_out=None, y=None, workspace=None, stream=None):
+                state_out=None, ring_out=None, y=None, workspace=None, stream=None,
+                norm_gate="sigmoid"):
     """The whole mixer for a prefill in one library call (kda_prefill_fused[_varlen]): conv +
     SiLU, l2 norm, gates, the chunked scan and the gated RMSNorm, the intermediates kept in the
     workspace.  Either (N, T) or cu_seqlens (int32 device) + cu_seqlens_host (int32
     CPU).  workspace: from kda.prefill_workspace (allocated here when None).
+    norm_gate: the RMSNorm's gate, "sigmoid" (KDA) or "silu" (GDN's gated_rmsnorm).
     Returns a dict with y, state_out and ring_out."""
     C = H * kda.HEAD_DIM
     rows = q_raw.shape[0]
@@ -105,8 +116,8 @@ def kda_prefill(*, q_raw, k_raw, v_raw, f_raw, dt_bias, a_log, beta_raw, state_i
         workspace = kda.prefill_workspace(n_seq, rows, H, q_raw.device, gate_mode)
     args = (q_raw, k_raw, v_raw, conv_w, ring_in, ring_out, f_raw, dt_bias, a_log, beta_raw,
             state_in, state_out, norm_w, gate_raw, y, workspace)
-    common = dict(H=H, K=K, gate_mode=gate_mode, gate_lb=gate_lb, l2_eps=l2_eps, scale=scale,
-                  rms_eps=rms_eps, stream=stream)
+    common = dict(H=H, K=K, gate_mode=gate_mode | _norm_flag(norm_gate), gate_lb=gate_lb,
+                  l2_eps=l2_eps, scale=scale, rms_eps=rms_eps, stream=stream)
     if varlen:
         kda.kda_prefill_fused_varlen(*args, cu_seqlens, cu_seqlens_host, **common)
     else:
@@ -117,8 +128,9 @@ def kda_prefill(*, q_raw, k_raw, v_raw, f_raw, dt_bias, a_log, beta_raw, state_i
 def kda_decode(*, q_raw, k_raw, v_raw, conv_w, ring_in, f_raw, dt_bias, a_log, beta_raw,
                state_in, norm_w, gate_raw, N, T, H, K=4, gate_mode=0, gate_lb=-5.0,
                l2_eps=1e-6, rms_eps=1e-6, scale=None, state_out=None, ring_out=None, y=None,
-               stream=None):
-    """One fused decode (T=1) or T-token verify launch.  ring_out may be ring_in (in place)."""
+               stream=None, norm_gate="sigmoid"):
+    """One fused decode (T=1) or T-token verify launch.  ring_out may be ring_in and state_out
+    state_in (in place).  norm_gate: "sigmoid" (KDA) or "silu" (GDN's gated_rmsnorm)."""
     if state_out is None:
         state_out = torch.empty_like(state_in)
     if ring_out is None:
@@ -127,7 +139,8 @@ def kda_decode(*, q_raw, k_raw, v_raw, conv_w, ring_in, f_raw, dt_bias, a_log, b
         y = _empty((q_raw.shape[0], H * kda.HEAD_DIM), q_raw)
     kda.kda_decode_fused(q_raw, k_raw, v_raw, conv_w, ring_in, ring_out, f_raw, dt_bias, a_log,
                          beta_raw, state_in, state_out, norm_w, gate_raw, y, N=N, T=T, H=H, K=K,
-                         gate_mode=gate_mode, gate_lb=gate_lb, l2_eps=l2_eps, scale=scale,
+                         gate_mode=gate_mode | _norm_flag(norm_gate), gate_lb=gate_lb,
+                         l2_eps=l2_eps, scale=scale,
                          rms_eps=rms_eps, stream=stream)
     return dict(y=y, state_out=state_out, ring_out=ring_out)
 
@@ -135,7 +148,7 @@ def kda_decode(*, q_raw, k_raw, v_raw, conv_w, ring_in, f_raw, dt_bias, a_log, b
 def kda_verify_rollback(*, q_raw, k_raw, v_raw, conv_w, ring_in, f_raw, dt_bias, a_log,
                         beta_raw, state_in, norm_w, gate_raw, keep, N, T, H, K=4, gate_mode=0,
                         gate_lb=-5.0, l2_eps=1e-6, rms_eps=1e-6, scale=None, state_out=None,
-                        ring_out=None, y=None, stream=None):
+                        ring_out=None, y=None, stream=None, norm_gate="sigmoid"):
     """Roll a T-token verify round back to the accepted prefixes: keep (int32 device [N]) tokens
     of each sequence, from the pre-round state_in and ring_in.  ring_out may be ring_in."""
     if state_out is None:
@@ -147,8 +160,9 @@ def kda_verify_rollback(*, q_raw, k_raw, v_raw, conv_w, ring_in, f_raw, dt_bias,
                         device=q_raw.device)
     kda.kda_verify_rollback(q_raw, k_raw, v_raw, conv_w, ring_in, ring_out, f_raw, dt_bias,
                             a_log, beta_raw, state_in, state_out, norm_w, gate_raw, y, keep,
-                            N=N, T=T, H=H, K=K, gate_mode=gate_mode, gate_lb=gate_lb,
-                            l2_eps=l2_eps, scale=scale, rms_eps=rms_eps, stream=stream)
+                            N=N, T=T, H=H, K=K, gate_mode=gate_mode | _norm_flag(norm_gate),
+                            gate_lb=gate_lb, l2_eps=l2_eps, scale=scale, rms_eps=rms_eps,
+                            stream=stream)
     return dict(y=y, state_out=state_out, ring_out=ring_out)
 
 

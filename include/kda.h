@@ -42,7 +42,8 @@ extern "C" {
 #define KDA_ERR_CUDA_BASE 10000       /* 10000 + cudaError_t */
 #define KDA_ERR_HEAD_DIM 40001        /* D != 128 */
 #define KDA_ERR_CONV_K 40002          /* K outside 2..8 while conv_w != NULL */
-#define KDA_ERR_STATE_ALIAS 40003     /* state_in and state_out overlap */
+#define KDA_ERR_STATE_ALIAS 40003     /* state (or ring) buffers overlap; decode and rollback
+                                         accept the very same buffer (in place) */
 #define KDA_ERR_NULL 40004            /* a required pointer is NULL */
 #define KDA_ERR_SHAPE 40005           /* negative size, H == 0, N or H > 65535, T too large */
 #define KDA_ERR_CU_SEQLENS 40006      /* cu_seqlens_host[0] != 0, decreasing, or last != total_T */
@@ -60,6 +61,12 @@ extern "C" {
 #define KDA_GATE_PER_HEAD 1           /* GDN: g is [rows, H], broadcast over the key dim */
 #define KDA_GATE_EXP 2                /* flag, or-ed into gate_mode: g holds the decay factor
                                          exp(log-decay) instead of the log-decay itself */
+#define KDA_NORM_SILU 4               /* flag, or-ed into gate_mode of the fused entries
+                                         (kda_prefill_fused[_varlen], kda_decode_fused,
+                                         kda_verify_rollback): the RMSNorm gates with
+                                         SiLU(z) = z * sigmoid(z), the GDN form, instead of
+                                         sigmoid(z) (Engine::kda_gated_rmsnorm doc).  The
+                                         prep and scan entries have no norm: 40007 there */
 #define KDA_ALGO_AUTO 0
 #define KDA_ALGO_SEQ 1
 #define KDA_ALGO_CHUNK 2
@@ -223,6 +230,15 @@ int kda_gated_rmsnorm_out(const float* o, const float* norm_w, const float* gate
                           long rows, int D, float eps, void* stream);
 
 /*
+ * kda_gated_rmsnorm_silu_out -- the same with the SiLU gate of GDN's gated_rmsnorm
+ * (Engine::kda_gated_rmsnorm doc: GDN gates with SiLU, KDA with sigmoid):
+ * y_i = o_i / sqrt(mean_i o_i^2 + eps) * norm_w[i] * gate_raw_i * sigmoid(gate_raw_i).
+ * Arguments as in kda_gated_rmsnorm_out.
+ */
+int kda_gated_rmsnorm_silu_out(const float* o, const float* norm_w, const float* gate_raw,
+                               float* y, long rows, int D, float eps, void* stream);
+
+/*
  * kda_prefill_workspace_bytes -- device scratch that suffices for kda_prefill_fused /
  * kda_prefill_fused_varlen over N sequences holding total_T tokens in all: the scan's readout
  * plane (4 bytes per (token, channel)) plus the chunked scan's scratch (kda_scan_workspace_bytes
@@ -291,7 +307,9 @@ const char* kda_kernel_name(int id);
  * equal those three calls bit for bit, and a T-token call equals T chained one-token calls bit
  * for bit (the decode == verify identity of the KDA module doc).
  * Argument meanings and layouts as in the three calls; rows = N*T; conv_w must not be NULL.
- * ring_in / ring_out may alias; state_in / state_out must not overlap.
+ * ring_in / ring_out may be the same buffer, and so may state_in / state_out (an in-place step:
+ * with stable pointers a decode step can be captured once in a CUDA graph and replayed); buffers
+ * that overlap without being the same return 40003.
  * norm_w [D] [16B], gate_raw and y [rows, C] f32 [16B].  T outside 1..16 returns 40005.
  */
 int kda_decode_fused(const void* q_raw, const void* k_raw, const void* v_raw, int raw_dtype,
@@ -315,8 +333,8 @@ int kda_decode_fused(const void* q_raw, const void* k_raw, const void* v_raw, in
  *             (keep[n] = 0 leaves state and ring of sequence n as they were).  NULL returns 40004.
  * The raw rows, f, beta and gate_raw keep the verify batch's layout: row n*T + t.  ring_in must
  * hold the ring from before the round (the verify call may not have rolled it in place, or the
- * caller keeps a copy); state_in the state from before the round (a verify never writes it,
- * since its state_out is another buffer).  y rows n*T + t are written for t < keep[n] only.
+ * caller keeps a copy); state_in the state from before the round (the verify ran out of place,
+ * or the caller keeps a copy).  y rows n*T + t are written for t < keep[n] only.
  */
 int kda_verify_rollback(const void* q_raw, const void* k_raw, const void* v_raw, int raw_dtype,
                         const float* conv_w, const float* ring_in, float* ring_out,

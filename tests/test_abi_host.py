@@ -108,6 +108,11 @@ def test_prep_and_decode_contract(kda):
         FAKE * 64, FAKE, FAKE, FAKE, keep, 2, kw.get("T", 4), 2, 128, 4, F(1e-6), F(0.1),
         F(1e-6), None)
     assert rb(None) == 40004                 # keep is required
+    # in place is fine for decode (it launches, so only a partial overlap is checked here)
+    partial = lib.kda_decode_fused(
+        FAKE, FAKE, FAKE, 1, FAKE, FAKE, FAKE * 2, FAKE, FAKE, FAKE, 0, F(-5.0), FAKE, FAKE * 64,
+        FAKE * 64 + 16, FAKE, FAKE, FAKE, 2, 1, 2, 128, 4, F(1e-6), F(0.1), F(1e-6), None)
+    assert partial == 40003
     assert rb(FAKE, T=17) == 40005
     assert rb(FAKE, T=0) == 40005
     norm = lib.kda_gated_rmsnorm_out(FAKE, FAKE + 8, FAKE, FAKE, ctypes.c_long(4), 128, F(1e-6),
