@@ -303,6 +303,8 @@ struct ParamStage {
 struct __align__(128) PrepIntraSmem {
     IntraSmem in;
     ParamStage ps;
+    alignas(128) float gtot[kThrF / 32][kHeadDim];   // the warps' 4-token gate totals (KDA),
+                                                     // read and written as float4
     uint64_t bar_raw, bar_f;                     // TMA completion of the raw rows, the gate input
 };
 // TMA destinations and sources inside the layout (its base aligned to 1024 bytes): the raw-row
@@ -311,6 +313,10 @@ struct __align__(128) PrepIntraSmem {
 static_assert(offsetof(IntraSmem, bia) + sizeof(IntraSmem::bia[0]) == 16384, "stage at 16 KB");
 static_assert(offsetof(IntraSmem, ktv) % 1024 == 0, "U tiles 1024-byte aligned");
 static_assert(offsetof(IntraSmem, scr) % 128 == 0, "gate input 128-byte aligned");
+// 16-byte vector accesses into the parameter stage and the gate totals
+static_assert(offsetof(PrepIntraSmem, ps) % 16 == 0 && offsetof(ParamStage, dt) % 16 == 0,
+              "dt_bias stage 16-byte aligned");
+static_assert(offsetof(PrepIntraSmem, gtot) % 16 == 0, "gate totals 16-byte aligned");
 // the dynamic allocation: the layout plus room to align it to 1024 bytes (128-byte swizzled tiles)
 constexpr size_t kPrepIntraSmemBytes = sizeof(PrepIntraSmem) + 1024;
 // two resident CTAs per SM: 228 KB of shared memory per SM, 1 KB of it reserved per CTA
@@ -524,6 +530,7 @@ kda_chunk_prep_intra_kernel(PrepArgs p, ScanArgs a, const int* chunk_off, unsign
     // ---- running gate sum G (per channel, KDA) in token order, warp to warp --------------------
     float G[kTokW][4];
     float GCh = 0.0f;                            // per-head gate: the chunk's total
+    float cref_l[4], ecr_l[4];                   // KDA: c = G_C / 2 and e^c of this lane's channels
     if (GATE_MODE == 0) {
         const float rate = expf(PF ? ps.alog : p.a_log[h]);
         const float4 dt = PF ? *reinterpret_cast<const float4*>(&ps.dt[kq])
@@ -536,8 +543,8 @@ kda_chunk_prep_intra_kernel(PrepArgs p, ScanArgs a, const int* chunk_off, unsign
             for (int e = 0; e < 4; ++e)
                 g[i][e] = i < ntok ? kda_gate_f(f4c(fr[i], e), dtv[e], rate, p.gate_lb) : 0.0f;
         // blocked running sum (the chunked intra kernel's order): each warp sums its 4 tokens in
-        // order from 0, the warps' totals go through shared memory (sm.bia[0], free until the row
-        // images), and warp w adds the totals of warps 0 .. w-1 in order, starting from 0
+        // order from 0, the warps' totals go through shared memory, and warp w adds the totals
+        // of warps 0 .. w-1 in order, starting from 0
         float run[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
         for (int i = 0; i < kTokW; ++i)
@@ -546,7 +553,7 @@ kda_chunk_prep_intra_kernel(PrepArgs p, ScanArgs a, const int* chunk_off, unsign
                 run[e] += g[i][e];
                 G[i][e] = run[e];
             }
-        float* gtot = reinterpret_cast<float*>(sm.bia[0]);   // [8 warps][128 channels]
+        float* gtot = &smf.gtot[0][0];
         *reinterpret_cast<float4*>(&gtot[warp * kHeadDim + kq]) = make_float4(run[0], run[1], run[2], run[3]);
         __syncthreads();
         float pre[4] = {0.0f, 0.0f, 0.0f, 0.0f};
@@ -558,21 +565,32 @@ kda_chunk_prep_intra_kernel(PrepArgs p, ScanArgs a, const int* chunk_off, unsign
         for (int i = 0; i < kTokW; ++i)
 #pragma unroll
             for (int e = 0; e < 4; ++e) G[i][e] = pre[e] + G[i][e];
-        if (warp == kThrF / 32 - 1) {            // G over the whole chunk: references, decay, range
+        // G over the whole chunk, in every warp from the same additions as warp 7's last token
+        // (so the same bits): the reference c = G_C / 2 and e^c of this lane's channels, for the
+        // row images without another barrier
+        float tot[4] = {pre[0], pre[1], pre[2], pre[3]};
+        for (int w2 = warp; w2 < kThrF / 32; ++w2) {
+            const float4 t4 = *reinterpret_cast<const float4*>(&gtot[w2 * kHeadDim + kq]);
+            tot[0] += t4.x; tot[1] += t4.y; tot[2] += t4.z; tot[3] += t4.w;
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            cref_l[e] = 0.5f * tot[e];
+            ecr_l[e] = __expf(0.5f * tot[e]);
+        }
+        if (warp == kThrF / 32 - 1) {            // published for the column images and the block
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const float tot = G[kTokW - 1][e];
-                sm.gcs[kq + e] = tot;
-                sm.cref[kq + e] = 0.5f * tot;
-                sm.ecr[kq + e] = __expf(0.5f * tot);
-                reinterpret_cast<float*>(blk + kOffEG)[kq + e] = decay_f(tot);
-                if (tot < -170.0f && a.err) atomicOr(a.err, kDevErrRange);
+                sm.gcs[kq + e] = tot[e];
+                reinterpret_cast<float*>(blk + kOffEG)[kq + e] = decay_f(tot[e]);
+                if (tot[e] < -170.0f && a.err) atomicOr(a.err, kDevErrRange);
             }
         }
 #pragma unroll
         for (int i = 0; i < kTokW; ++i)
             *reinterpret_cast<float4*>(&sm.scr[(t0 + i) * 128 + kq]) =
                 make_float4(G[i][0], G[i][1], G[i][2], G[i][3]);
+        __syncwarp();                            // the row images read this warp's own G rows
     } else {
         __syncthreads();                         // sm.gs
         float run = 0.0f;                        // the running sum in token order
@@ -592,8 +610,8 @@ kda_chunk_prep_intra_kernel(PrepArgs p, ScanArgs a, const int* chunk_off, unsign
         }
 #pragma unroll
         for (int e = 0; e < 4; ++e) reinterpret_cast<float*>(blk + kOffEG)[kq + e] = decay_f(GCh);
+        __syncthreads();                         // gsc
     }
-    __syncthreads();                             // G tile, references, beta, gsc
 
     // ---- row images: tokens t0 + 2*(lane&1) + (j ^ sw), channels k0 .. k0+7 --------------------
     {
@@ -606,8 +624,17 @@ kda_chunk_prep_intra_kernel(PrepArgs p, ScanArgs a, const int* chunk_off, unsign
         const int tj[2] = {tb + (sw ? 1 : 0), tb + (sw ? 0 : 1)};
         float crv[8], ecv[8], gtv[2][8];
         if (GATE_MODE == 0) {
+            // channels k0 .. k0+7 = this lane pair's: the even lane's 4 then the odd lane's 4
+            const bool odd = (lane & 1) != 0;
 #pragma unroll
-            for (int e = 0; e < 8; ++e) { crv[e] = sm.cref[k0 + e]; ecv[e] = sm.ecr[k0 + e]; }
+            for (int e = 0; e < 4; ++e) {
+                const float oc = __shfl_xor_sync(0xffffffffu, cref_l[e], 1);
+                const float oe = __shfl_xor_sync(0xffffffffu, ecr_l[e], 1);
+                crv[e] = odd ? oc : cref_l[e];
+                crv[4 + e] = odd ? cref_l[e] : oc;
+                ecv[e] = odd ? oe : ecr_l[e];
+                ecv[4 + e] = odd ? ecr_l[e] : oe;
+            }
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
                 const float4 a0 = *reinterpret_cast<const float4*>(&sm.scr[tj[j] * 128 + k0]);
