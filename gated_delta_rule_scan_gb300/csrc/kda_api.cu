@@ -458,6 +458,12 @@ int kda_verify_rollback(const void* q_raw, const void* k_raw, const void* v_raw,
                        y, N, T, H, D, K, l2_eps, scale, rms_eps, keep, true, stream);
 }
 
+int kda_selftest_wait_timeout(void* stream) {
+    int* p = dev_err_ptr();
+    if (p == nullptr) return cuda_status(cudaErrorUnknown);
+    return cuda_status(launch_wait_selftest(p, static_cast<cudaStream_t>(stream)));
+}
+
 int kda_device_status(void* stream) {
     cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_status(e);

@@ -61,6 +61,7 @@ struct DecodeArgs {
 };
 
 cudaError_t launch_prep(const PrepArgs& a, cudaStream_t s);
+cudaError_t launch_wait_selftest(int* err, cudaStream_t s);
 cudaError_t launch_scan_seq(const ScanArgs& a, cudaStream_t s);
 cudaError_t launch_scan_chunk(const ScanArgs& a, const int* cu_host, void* workspace,
                               cudaStream_t s);

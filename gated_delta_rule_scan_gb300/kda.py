@@ -81,6 +81,8 @@ _lib.kda_verify_rollback.argtypes = [_P, _P, _P, _I, _P, _P, _P, _P, _P, _P, _I,
                                      _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _F, _F, _P]
 _lib.kda_device_status.restype = _I
 _lib.kda_device_status.argtypes = [_P]
+_lib.kda_selftest_wait_timeout.restype = _I
+_lib.kda_selftest_wait_timeout.argtypes = [_P]
 
 # every symbol include/kda.h declares
 EXPORTED = ("kda_abi_version", "kda_status_string", "kda_conv_l2norm_prep",
@@ -88,7 +90,8 @@ EXPORTED = ("kda_abi_version", "kda_status_string", "kda_conv_l2norm_prep",
             "kda_scan_varlen", "kda_gated_rmsnorm_out", "kda_decode_fused", "kda_device_status",
             "kda_scan_varlen_static", "kda_prefill_workspace_bytes", "kda_prefill_fused",
             "kda_prefill_fused_varlen", "kda_kernel_timing", "kda_kernel_times",
-            "kda_kernel_name", "kda_verify_rollback", "kda_gated_rmsnorm_silu_out")
+            "kda_kernel_name", "kda_verify_rollback", "kda_gated_rmsnorm_silu_out",
+            "kda_selftest_wait_timeout")
 
 
 class KdaError(RuntimeError):
@@ -323,3 +326,13 @@ def kda_device_status(stream=None) -> int:
     elif stream is not None and not isinstance(stream, int):
         stream = stream.cuda_stream
     return int(_lib.kda_device_status(stream))
+
+
+def kda_selftest_wait_timeout(stream=None):
+    """Launch the bounded-wait self-test (a wait that nothing completes gives up after about a
+    second); a following kda_device_status() returns 40008."""
+    if stream is None and torch.cuda.is_available():
+        stream = torch.cuda.current_stream().cuda_stream
+    elif stream is not None and not isinstance(stream, int):
+        stream = stream.cuda_stream
+    _check("kda_selftest_wait_timeout", _lib.kda_selftest_wait_timeout(stream))

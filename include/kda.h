@@ -345,6 +345,16 @@ int kda_verify_rollback(const void* q_raw, const void* k_raw, const void* v_raw,
                         int D, int K, float l2_eps, float scale, float rms_eps, void* stream);
 
 /*
+ * kda_selftest_wait_timeout -- a self-test of failure detection (no counterpart in the pages):
+ * launches one kernel whose single thread waits, with the bounded wait every kernel here uses,
+ * on a barrier that nothing completes.  The wait gives up after about a second, raises the device
+ * error word and the kernel ends; a following kda_device_status(stream) returns 40008 (and
+ * clears the word).  Nothing faults or hangs; the context stays usable.  Returns 0, or
+ * 10000 + cudaError_t if the launch fails.
+ */
+int kda_selftest_wait_timeout(void* stream);
+
+/*
  * kda_device_status -- synchronises `stream`, then reports and clears the device error word on
  * the current device: 0, or 40008 when a kernel gave up a bounded device wait since the last
  * check (its outputs are then incomplete), or 10000 + cudaError_t.
