@@ -175,6 +175,24 @@ def _kernel_hash(files):
     return h.hexdigest()[:16]
 
 
+# the sources each kernel is built from: profiles/traffic.json holds DRAM traffic keyed by their
+# hash, reported only while they are unchanged
+KERNEL_SOURCES = {
+    "kda_chunk_intra_kernel": ["kda_scan_chunk.cu", "kda_chunk_common.cuh", "kda_tc.cuh",
+                               "kda_device.cuh", "kda_internal.h", "kda_ring.cuh"],
+    "kda_chunk_prep_intra_kernel": ["kda_chunk_prep.cu", "kda_chunk_common.cuh", "kda_tc.cuh",
+                                    "kda_device.cuh", "kda_internal.h"],
+    "kda_chunk_inter_kernel": ["kda_scan_chunk.cu", "kda_chunk_common.cuh", "kda_tc.cuh",
+                               "kda_device.cuh", "kda_internal.h", "kda_ring.cuh"],
+    "kda_gated_rmsnorm_kernel": ["kda_epilogue.cu", "kda_device.cuh", "kda_internal.h"],
+    "kda_prep_kernel": ["kda_prep.cu", "kda_device.cuh", "kda_internal.h", "kda_ring.cuh"],
+    "kda_decode_fused_kernel": ["kda_decode.cu", "kda_scan_core.cuh", "kda_device.cuh",
+                                "kda_internal.h"],
+    "kda_scan_seq_kernel": ["kda_scan_seq.cu", "kda_scan_core.cuh", "kda_device.cuh",
+                            "kda_internal.h"],
+}
+
+
 def _traffic(kernel, files):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on this source."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
@@ -501,21 +519,15 @@ def run_ours(args):
     for name, (n, kms) in sorted(ktimes.items(), key=lambda kv: -kv[1][1]):
         per = kms / n
         b = kbytes.get(name)
-        ent = {"kernel": name, "launches": n, "ms_per_launch": per, "share": kms / total_kms}
+        ent = {"kernel": name, "launches": n, "ms_per_launch": per, "share": kms / total_kms,
+               "traffic": _traffic(name, KERNEL_SOURCES.get(name, []))}
         if b:
             gbs = b / (per / 1e3) / 1e9
             ent.update(bytes_per_launch=b, gbs=gbs, frac_hbm=gbs / peaks["hbm_gbs"])
         kernels.append(ent)
     if fused:
         top = kernels[0]
-        src_files = {"kda_chunk_intra_kernel": ["kda_scan_chunk.cu", "kda_chunk_common.cuh", "kda_tc.cuh",
-                                                "kda_device.cuh"],
-                     "kda_chunk_prep_intra_kernel": ["kda_chunk_prep.cu", "kda_chunk_common.cuh",
-                                                     "kda_tc.cuh", "kda_device.cuh"],
-                     "kda_gated_rmsnorm_kernel": ["kda_epilogue.cu", "kda_device.cuh"],
-                     "kda_chunk_inter_kernel": ["kda_scan_chunk.cu", "kda_chunk_common.cuh", "kda_tc.cuh",
-                                                "kda_device.cuh"],
-                     "kda_prep_kernel": ["kda_prep.cu", "kda_device.cuh"]}
+        src_files = KERNEL_SOURCES
         roofline = {"bound": "hbm", "kernel": top["kernel"], "achieved": top.get("gbs"),
                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": top.get("frac_hbm"),
                     "traffic": _traffic(top["kernel"], src_files.get(top["kernel"], [])),
@@ -527,7 +539,7 @@ def run_ours(args):
         roofline = {"bound": "alu", "kernel": "kda_scan_seq_kernel", "achieved": scan_tflops,
                     "peak": fp32_peak, "unit": "TFLOP/s", "frac": scan_tflops / fp32_peak,
                     "traffic": _traffic("kda_scan_seq_kernel",
-                                        ["kda_scan_seq.cu", "kda_device.cuh"]),
+                                        KERNEL_SOURCES["kda_scan_seq_kernel"]),
                     "ms_per_launch": scan_ms, "flop_per_launch": scan_flop,
                     "peak_src": f"152 SMs x 128 FP32 lanes x 2 x {peaks['sm_max_mhz']:.0f} MHz"}
     return {
@@ -557,7 +569,7 @@ def run_ours(args):
                                 "frac": dec_gbs / peaks["hbm_gbs"],
                                 "peak_src": f"{peaks['src']} hbm_gbs",
                                 "traffic": _traffic("kda_decode_fused_kernel",
-                                                    ["kda_decode.cu", "kda_device.cuh"]),
+                                                    KERNEL_SOURCES["kda_decode_fused_kernel"]),
                                 "bytes_per_launch": dec_bytes}},
         "decode_graph": {"workload": "the decode step in place (state and ring), captured once "
                                      "in a CUDA graph and replayed",

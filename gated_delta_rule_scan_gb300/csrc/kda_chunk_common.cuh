@@ -331,10 +331,11 @@ __device__ __forceinline__ bool intra_mma_tail(IntraSmem& sm, int* err, unsigned
                 tc_smem_desc(smem_u32(sm.ktv[1]), 128, kSboKt), 2, tc_idesc_bf16(128, 256));
         tc_commit(&sm.bar);
     }
+    // every thread observes MMA-b's completion itself; whether every wait succeeded is agreed at
+    // the final barrier below (the epilogue runs either way, its bulk copies only on success)
     ok = mbar_wait_bounded(&sm.bar, phase, err);
     phase ^= 1u;
     tc_fence_after();
-    if (__syncthreads_or(!ok)) goto done;
     {
         // warp w: columns CW*w .. CW*w+CW-1 of [W | U] (W: 0..127, U: 128..255) for token t = lane
         constexpr int CW = 256 / (NT / 32);
@@ -373,7 +374,7 @@ __device__ __forceinline__ bool intra_mma_tail(IntraSmem& sm, int* err, unsigned
 done:
     tc_fence_before();
     if (PRE_A) fence_proxy_async_smem();
-    __syncthreads();
+    ok = __syncthreads_or(!ok) == 0;
     if (PRE_A && ok && tid == 0) {   // W: QW rows 32..63 (hi, lo); U: four [32 t][32 v] tiles
         constexpr uint32_t kW = kCc * kSbo128 / 8;   // 8 KB: 4 groups of 8 rows
         bulk_store(blk + kOffQW + kW, sm.ktv[1], kW);

@@ -396,6 +396,7 @@ kda_chunk_inter_kernel(ScanArgs a, const int* chunk_off, const unsigned char* ws
 
     uint32_t mph = 0;
     bool failed = false;
+    bool late_fail = false;          // an MMA-2 wait gave up: ends the loop at its next barrier
     const float scale = a.scale;
     const bool ostore_lane = warp == 2;
     const int olane = tid & 31;
@@ -425,7 +426,7 @@ kda_chunk_inter_kernel(ScanArgs a, const int* chunk_off, const unsigned char* ws
         ok = ok && mbar_wait_bounded(&sm.bar_mma, mph, a.err);
         if (ok) mph ^= 1u;
         tc_fence_after();
-        if (__syncthreads_or(!ok)) { failed = true; break; }
+        if (__syncthreads_or(!ok || late_fail)) { failed = true; break; }
         if (ostore_lane && c > 0) flush_o(c - 1);   // its o rows were written before the barrier
         // O1 and X for tokens 16 hf ..; O1 waits in the output tile; U' = U - X into TMEM as
         // MMA-2's A operand
@@ -454,10 +455,14 @@ kda_chunk_inter_kernel(ScanArgs a, const int* chunk_off, const unsigned char* ws
                     tc_smem_desc(smem_u32(B + kOffB2 + kB2Bytes), 128, kSbo32), 2, id2);
             tc_commit(&sm.bar_mma);
         }
-        ok = mbar_wait_bounded(&sm.bar_mma, mph, a.err);
-        if (ok) mph ^= 1u;
+        // every thread observes MMA-2's completion itself (no barrier needed for the TMEM reads
+        // below); a wait that gave up is carried to the next barrier that can end the loop
+        {
+            const bool ok2 = mbar_wait_bounded(&sm.bar_mma, mph, a.err);
+            if (ok2) mph ^= 1u;
+            late_fail = late_fail || !ok2;
+        }
         tc_fence_after();
-        if (__syncthreads_or(!ok)) { failed = true; break; }
         float o2[16];
         bool next_ok = false;            // thread 0: the next chunk's block landed, MMA-1 going
         // S <- S e^{G_C} + dS, keys 0..63 (srow[0..31]) then 64..127 (srow[32..63]); after the
@@ -506,7 +511,7 @@ kda_chunk_inter_kernel(ScanArgs a, const int* chunk_off, const unsigned char* ws
         for (int t = 0; t < 16; ++t) ot[t * 128] = ov[t];
         fence_proxy_async_smem();
     }
-    __syncthreads();
+    failed = __syncthreads_or(failed || late_fail) != 0;
     if (ostore_lane) {
         if (!failed && nch > 0) flush_o(nch - 1);
         bulk_wait_all();
