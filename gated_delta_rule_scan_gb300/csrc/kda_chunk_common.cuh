@@ -150,8 +150,8 @@ struct __align__(128) IntraSmem {
     float beta[kCc];
     float gs[kCc];                               // per-head log-gate per token (GDN)
     float gsc[kCc];                              // its running sum (GDN)
-    float cref[128];
-    float ecr[128];
+    float cref[128];                             // intra kernel: c = G_C / 2 per channel
+    float ecr[128];                              // intra kernel: e^c
     float gcs[128];                              // the chunk's total gate per channel (fused prep)
     uint64_t bar;
     uint32_t tmem_base;
@@ -163,13 +163,15 @@ static_assert(2 * kTmBytes <= 64 * 128 * 2, "Tm fits in bia[0]");
 // The part of the intra-chunk computation that follows the operand images, shared by the
 // chunked scan's intra kernel and the fused prefill kernel: MMA-a (A and Aqk), the blocked
 // inverse Tm = (I + A)^{-1}, MMA-b (W and U) and the workspace epilogue.  On entry every thread
-// has written its share of sm.bia, sm.kb, sm.ktv, the QG and K^T images in blk and blk's EG row;
-// sm.beta (and for GDN sm.gsc, the running per-head gate) are set; warp 0 holds sm.tmem_base
-// (256 columns) and sm.bar is initialised; phase is sm.bar's current parity (updated).  Once
-// MMA-a has completed (sm.bia[1] and sm.kb are then free for the rest of the tail), every thread
-// calls after_a(); once the Tm image is written (sm.scr is then free), after_tm().  Ends after a barrier, the TMEM still allocated; returns false if a bounded
-// wait gave up.  NT = threads of the CTA, 128 or 256 (warps w and w+4 share TMEM lane quarter w
-// and split the epilogue's columns).
+// has written its share of sm.bia, sm.kb, sm.ktv, the QG and K^T images in blk and blk's EG row
+// (the fused kernel: the column images may still be on their way, see PRE_A below); sm.beta (and
+// for GDN sm.gsc, the running per-head gate) are set; warp 0 holds sm.tmem_base (256 columns) and
+// sm.bar is initialised; phase is sm.bar's current parity (updated).  Once MMA-a has completed
+// (sm.bia[1] and sm.kb are then free for the rest of the tail), every thread calls after_a();
+// once the Tm image is written (sm.scr is then free), after_tm().  Ends after a barrier that
+// also agrees on the result, the TMEM still allocated; returns false (in every thread) if a
+// bounded wait gave up.  NT = threads of the CTA, 128 or 256 (warps w and w+4 share TMEM lane
+// quarter w and split the epilogue's columns).
 struct NoHook {
     __device__ void operator()() const {}
 };
