@@ -215,6 +215,14 @@ class HostPrefillStream:
         self.run = torch.cuda.Stream(dev)
         self.copy_out = torch.cuda.Stream(dev)
         self.submitted = 0
+        # the buffers live on the default stream's pool but are used on the three streams: the
+        # allocator keeps their memory until work queued there has finished, even if this
+        # object is dropped early
+        for din, dout, _ in self.slots:
+            for t in (*din.values(), *dout.values()):
+                for st in (self.copy_in, self.run, self.copy_out):
+                    t.record_stream(st)
+        self.workspace.record_stream(self.run)
 
     @property
     def h2d_bytes_per_batch(self) -> int:
@@ -258,3 +266,7 @@ class HostPrefillStream:
         self.copy_out.synchronize()
         self.run.synchronize()
         self.copy_in.synchronize()
+
+    def close(self):
+        """Wait for every submitted batch; the host buffers given to submit() are then free."""
+        self.synchronize()
