@@ -125,9 +125,11 @@ long max_len(const SeqLayout& seq, const int* cu_host) {
 int scan_impl(const float* q, const float* k, const float* v, const float* g, int gate_mode,
               const float* beta, const float* state_in, float* state_out, float* o,
               const SeqLayout& seq, const int* cu_host, int H, int D, float scale, int algo,
-              void* workspace, size_t workspace_bytes, void* stream) {
+              void* workspace, size_t workspace_bytes, void* stream, int Hk = 0) {
     if (D != kHeadDim) return KDA_ERR_HEAD_DIM;
     if (seq.N < 0 || seq.N > kMaxGridY || seq.total_rows < 0 || H <= 0) return KDA_ERR_SHAPE;
+    if (Hk == 0) Hk = H;
+    if (Hk < 1 || Hk > kMaxGridY) return KDA_ERR_SHAPE;
     if (gate_mode < 0 || gate_mode > (KDA_GATE_PER_HEAD | KDA_GATE_EXP)) return KDA_ERR_ENUM;
     if (algo != KDA_ALGO_AUTO && algo != KDA_ALGO_SEQ && algo != KDA_ALGO_CHUNK) return KDA_ERR_ENUM;
     if (seq.total_rows >= (1L << 31)) return KDA_ERR_SHAPE;
@@ -143,6 +145,7 @@ int scan_impl(const float* q, const float* k, const float* v, const float* g, in
             return KDA_ERR_ALIGN;
     }
     ScanArgs a{};
+    a.Hk = Hk;
     a.q = q; a.k = k; a.v = v; a.g = g; a.gate_mode = gate_mode; a.beta = beta;
     a.state_in = state_in; a.state_out = state_out; a.o = o;
     a.seq = seq; a.H = H; a.scale = scale; a.order = nullptr;
@@ -421,6 +424,33 @@ int kda_scan_varlen(const float* q_hat, const float* k_hat, const float* v_hat, 
     SeqLayout seq{cu_seqlens, 0, N, (long)total_T};
     return scan_impl(q_hat, k_hat, v_hat, g, gate_mode, beta, state_in, state_out, o, seq,
                      cu_seqlens_host, H, D, scale, algo, workspace, workspace_bytes, stream);
+}
+
+int kda_scan_gqa(const float* q_hat, const float* k_hat, const float* v_hat, const float* g,
+                 int gate_mode, const float* beta, const float* state_in, float* state_out,
+                 float* o, int N, int T, int H, int Hk, int D, float scale, int algo,
+                 void* workspace, size_t workspace_bytes, void* stream) {
+    if (N < 0 || T < 0 || Hk <= 0) return KDA_ERR_SHAPE;
+    SeqLayout seq{nullptr, T, N, (long)N * T};
+    return scan_impl(q_hat, k_hat, v_hat, g, gate_mode, beta, state_in, state_out, o, seq, nullptr,
+                     H, D, scale, algo, workspace, workspace_bytes, stream, Hk);
+}
+
+int kda_scan_varlen_gqa(const float* q_hat, const float* k_hat, const float* v_hat,
+                        const float* g, int gate_mode, const float* beta, const float* state_in,
+                        float* state_out, float* o, const int* cu_seqlens,
+                        const int* cu_seqlens_host, int N, int total_T, int H, int Hk, int D,
+                        float scale, int algo, void* workspace, size_t workspace_bytes,
+                        void* stream) {
+    if (N < 0 || total_T < 0 || Hk <= 0) return KDA_ERR_SHAPE;
+    if (N > 0) {
+        if (cu_seqlens == nullptr) return KDA_ERR_NULL;
+        const int rc = check_cu(cu_seqlens_host, N, total_T);
+        if (rc) return rc;
+    }
+    SeqLayout seq{cu_seqlens, 0, N, (long)total_T};
+    return scan_impl(q_hat, k_hat, v_hat, g, gate_mode, beta, state_in, state_out, o, seq,
+                     cu_seqlens_host, H, D, scale, algo, workspace, workspace_bytes, stream, Hk);
 }
 
 int kda_gated_rmsnorm_out(const float* o, const float* norm_w, const float* gate_raw, float* y,

@@ -40,7 +40,12 @@ struct ScanArgs {
     int H; float scale;
     const int* order;        // device-side order of sequences (longest first) or null
     int* err;                // device error word
+    int Hk;                  // heads of q and k (grouped queries: value head h reads q/k head
+                             // h % Hk; rows of q and k are Hk * D wide); 0 means H
 };
+
+// the heads of q and k, and the one value head h reads
+__host__ __device__ inline int qk_heads(const ScanArgs& a) { return a.Hk > 0 ? a.Hk : a.H; }
 
 struct NormArgs {
     const float* o; const float* w; const float* z; float* y; long rows; float eps;

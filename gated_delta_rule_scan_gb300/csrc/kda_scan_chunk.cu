@@ -70,6 +70,8 @@ kda_chunk_intra_kernel(ScanArgs a, const int* chunk_off, unsigned char* ws) {
     const int nt = (int)min((long)kCc, end - row0);
     unsigned char* blk = ws + ((long)gid * H + h) * kBlkBytes;
     const long hoff = row0 * C + (long)h * kHeadDim;
+    const long Ck = (long)qk_heads(a) * kHeadDim;     // q and k rows: the head h % Hk
+    const long qkoff = row0 * Ck + (long)(h % qk_heads(a)) * kHeadDim;
 
     // ---- every global load of the chunk is issued before any store ---------------------------
     // column role: channel tid over the chunk's 32 tokens
@@ -77,7 +79,7 @@ kda_chunk_intra_kernel(ScanArgs a, const int* chunk_off, unsigned char* ws) {
 #pragma unroll
     for (int t = 0; t < kCc; ++t) {
         const bool live = t < nt;
-        kc[t] = live ? __ldg(a.k + hoff + t * C + tid) : 0.0f;
+        kc[t] = live ? __ldg(a.k + qkoff + t * Ck + tid) : 0.0f;
         vc[t] = live ? __ldg(a.v + hoff + t * C + tid) : 0.0f;
         if (GATE_MODE == 0) gc[t] = live ? __ldg(a.g + hoff + t * C + tid) : (EXP ? 1.0f : 0.0f);
     }
@@ -88,8 +90,8 @@ kda_chunk_intra_kernel(ScanArgs a, const int* chunk_off, unsigned char* ws) {
     for (int j = 0; j < 4; ++j) {
         const int t = tr + 8 * j;
         if (t < nt) {
-            const float4* kp = reinterpret_cast<const float4*>(a.k + hoff + t * C + k0);
-            const float4* qp = reinterpret_cast<const float4*>(a.q + hoff + t * C + k0);
+            const float4* kp = reinterpret_cast<const float4*>(a.k + qkoff + t * Ck + k0);
+            const float4* qp = reinterpret_cast<const float4*>(a.q + qkoff + t * Ck + k0);
             kr[j][0] = __ldg(kp); kr[j][1] = __ldg(kp + 1);
             qr[j][0] = __ldg(qp); qr[j][1] = __ldg(qp + 1);
         } else {

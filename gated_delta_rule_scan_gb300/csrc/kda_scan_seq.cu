@@ -64,6 +64,7 @@ kda_scan_seq_kernel(ScanArgs a, const __grid_constant__ CUtensorMap tq,
     const int cw = (warp * (32 / kScanG) + grp) * 4;   // first of the group's 4 columns in the CTA
     const int H = a.H;
     const long C = (long)H * kHeadDim;
+    const int kh = h % qk_heads(a);             // the q / k head this value head reads
 
     long begin, end;
     if (a.seq.cu_seqlens == nullptr) {
@@ -97,8 +98,8 @@ kda_scan_seq_kernel(ScanArgs a, const __grid_constant__ CUtensorMap tq,
         const int row = (int)(begin + (long)b * kScanTB);
         fence_proxy_async_smem();
         mbar_arrive_expect_tx(&sm.bar[st], kTxBytes);
-        tma_load_2d(&sm.q[st][0][0], &tq, h * kHeadDim, row, &sm.bar[st]);
-        tma_load_2d(&sm.k[st][0][0], &tk, h * kHeadDim, row, &sm.bar[st]);
+        tma_load_2d(&sm.q[st][0][0], &tq, kh * kHeadDim, row, &sm.bar[st]);
+        tma_load_2d(&sm.k[st][0][0], &tk, kh * kHeadDim, row, &sm.bar[st]);
         if (GATE_MODE == 0) tma_load_2d(&sm.g[st][0][0], &tg, h * kHeadDim, row, &sm.bar[st]);
         tma_load_2d(&sm.v[st][0][0], &tv, h * kHeadDim + cb * kScanCols, row, &sm.bar[st]);
     };
@@ -213,10 +214,11 @@ bool make_tensor_map_2d(CUtensorMap* m, const float* base, long rows, long cols,
 template <int GM, bool EXP>
 static cudaError_t launch_t(const ScanArgs& a, cudaStream_t s) {
     const long C = (long)a.H * kHeadDim;
+    const long Ck = (long)qk_heads(a) * kHeadDim;
     const long rows = a.seq.total_rows;
     CUtensorMap tq, tk, tg, tv;
-    if (!make_tensor_map_2d(&tq, a.q, rows, C, kHeadDim, kScanTB) ||
-        !make_tensor_map_2d(&tk, a.k, rows, C, kHeadDim, kScanTB) ||
+    if (!make_tensor_map_2d(&tq, a.q, rows, Ck, kHeadDim, kScanTB) ||
+        !make_tensor_map_2d(&tk, a.k, rows, Ck, kHeadDim, kScanTB) ||
         !make_tensor_map_2d(&tv, a.v, rows, C, kScanCols, kScanTB))
         return cudaErrorInvalidValue;
     if (GM == 0) {

@@ -81,6 +81,12 @@ _lib.kda_verify_rollback.argtypes = [_P, _P, _P, _I, _P, _P, _P, _P, _P, _P, _I,
                                      _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _F, _F, _P]
 _lib.kda_device_status.restype = _I
 _lib.kda_device_status.argtypes = [_P]
+_lib.kda_scan_gqa.restype = _I
+_lib.kda_scan_gqa.argtypes = [_P, _P, _P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P,
+                              _Z, _P]
+_lib.kda_scan_varlen_gqa.restype = _I
+_lib.kda_scan_varlen_gqa.argtypes = [_P, _P, _P, _P, _I, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I,
+                                     _I, _F, _I, _P, _Z, _P]
 _lib.kda_selftest_wait_timeout.restype = _I
 _lib.kda_selftest_wait_timeout.argtypes = [_P]
 
@@ -91,7 +97,7 @@ EXPORTED = ("kda_abi_version", "kda_status_string", "kda_conv_l2norm_prep",
             "kda_scan_varlen_static", "kda_prefill_workspace_bytes", "kda_prefill_fused",
             "kda_prefill_fused_varlen", "kda_kernel_timing", "kda_kernel_times",
             "kda_kernel_name", "kda_verify_rollback", "kda_gated_rmsnorm_silu_out",
-            "kda_selftest_wait_timeout")
+            "kda_selftest_wait_timeout", "kda_scan_gqa", "kda_scan_varlen_gqa")
 
 
 class KdaError(RuntimeError):
@@ -184,6 +190,32 @@ def kda_scan(q_hat, k_hat, v_hat, g, beta, state_in, state_out, o, *, N, T, H, g
     _check("kda_scan", _lib.kda_scan(
         _ptr(q_hat), _ptr(k_hat), _ptr(v_hat), _ptr(g), gate_mode, _ptr(beta), _ptr(state_in),
         _ptr(state_out), _ptr(o), N, T, H, D, scale, algo, _ptr(workspace), ws_bytes, st))
+
+
+def kda_scan_gqa(q_hat, k_hat, v_hat, g, beta, state_in, state_out, o, *, N, T, H, Hk,
+                 gate_mode=0, scale=None, algo=ALGO_AUTO, workspace=None, D=HEAD_DIM, stream=None):
+    """kda_scan with grouped queries: q_hat / k_hat have Hk heads, value head h reads h % Hk."""
+    scale = D ** -0.5 if scale is None else scale
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = _stream(stream, state_out)
+    _check("kda_scan_gqa", _lib.kda_scan_gqa(
+        _ptr(q_hat), _ptr(k_hat), _ptr(v_hat), _ptr(g), gate_mode, _ptr(beta), _ptr(state_in),
+        _ptr(state_out), _ptr(o), N, T, H, Hk, D, scale, algo, _ptr(workspace), ws_bytes, st))
+
+
+def kda_scan_varlen_gqa(q_hat, k_hat, v_hat, g, beta, state_in, state_out, o, cu_seqlens,
+                        cu_seqlens_host, *, H, Hk, gate_mode=0, scale=None, algo=ALGO_AUTO,
+                        workspace=None, D=HEAD_DIM, stream=None):
+    """kda_scan_varlen with grouped queries (see kda_scan_gqa)."""
+    N = cu_seqlens_host.numel() - 1
+    total = int(cu_seqlens_host[-1])
+    scale = D ** -0.5 if scale is None else scale
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = _stream(stream, state_out)
+    _check("kda_scan_varlen_gqa", _lib.kda_scan_varlen_gqa(
+        _ptr(q_hat), _ptr(k_hat), _ptr(v_hat), _ptr(g), gate_mode, _ptr(beta), _ptr(state_in),
+        _ptr(state_out), _ptr(o), _ptr(cu_seqlens), _ptr(cu_seqlens_host), N, total, H, Hk, D,
+        scale, algo, _ptr(workspace), ws_bytes, st))
 
 
 def kda_scan_varlen(q_hat, k_hat, v_hat, g, beta, state_in, state_out, o, cu_seqlens,

@@ -189,6 +189,24 @@ int kda_scan_varlen(const float* q_hat, const float* k_hat, const float* v_hat, 
                     size_t workspace_bytes, void* stream);
 
 /*
+ * kda_scan_gqa, kda_scan_varlen_gqa -- kda_scan / kda_scan_varlen with grouped queries: q_hat
+ * and k_hat hold Hk heads ([rows, Hk*D] f32 [16B]) and value head h reads q/k head h % Hk (the
+ * tiled order of `gdn_delta_rule_into` / delta_rule_recurrence_gqa, aprender-serve gdn_ops.rs);
+ * v_hat, g, beta, the state and o keep H heads.  Hk >= 1 (40005 otherwise); Hk == H is kda_scan
+ * itself.  Same workspace as kda_scan_workspace_bytes(N, total_T, H, ...).
+ */
+int kda_scan_gqa(const float* q_hat, const float* k_hat, const float* v_hat, const float* g,
+                 int gate_mode, const float* beta, const float* state_in, float* state_out,
+                 float* o, int N, int T, int H, int Hk, int D, float scale, int algo,
+                 void* workspace, size_t workspace_bytes, void* stream);
+int kda_scan_varlen_gqa(const float* q_hat, const float* k_hat, const float* v_hat,
+                        const float* g, int gate_mode, const float* beta, const float* state_in,
+                        float* state_out, float* o, const int* cu_seqlens,
+                        const int* cu_seqlens_host, int N, int total_T, int H, int Hk, int D,
+                        float scale, int algo, void* workspace, size_t workspace_bytes,
+                        void* stream);
+
+/*
  * kda_scan_varlen_static -- kda_scan_varlen with algo KDA_ALGO_CHUNK, except that the chunked
  * form's scratch is a fixed array of KDA_STATIC_SCRATCH_BYTES (32 MiB) inside the library rather
  * than a caller workspace: the call allocates no device or host memory (no cudaMalloc, no
