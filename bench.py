@@ -666,6 +666,90 @@ def run_reference(args):
                     "d2h_bytes_per_step": 0}}
 
 
+def run_configs(args):
+    """The other configurations of the workload table (the headline is the prefill): the 4-token
+    verify, the packed varlen prefill and the long GDN scan, each through the public API on
+    resident inputs larger than L2, one JSON line each (mean of --steps calls after 3 warm-up
+    calls)."""
+    import numpy as np
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    from gated_delta_rule_scan_gb300 import inputs, kda, mixer
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    peaks = _peaks()
+    K = max(args.steps, 5)
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(K):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        assert kda.kda_device_status() == 0
+        return e0.elapsed_time(e1) / K
+
+    def to_dev(inp):
+        return {k: (None if getattr(inp, k) is None else getattr(inp, k).to(dev)) for k in
+                ("q_raw", "k_raw", "v_raw", "conv_w", "ring_in", "f_raw", "dt_bias", "a_log",
+                 "beta_raw", "state_in", "norm_w", "gate_raw")}
+
+    # 1' verify: 64 sequences x 4 tokens, one fused launch
+    ver = inputs.decode_step(N=DEC_N, T=4, H=DEC_H)
+    dv = to_dev(ver)
+    vout = dict(state_out=torch.empty_like(dv["state_in"]), ring_out=torch.empty_like(dv["ring_in"]),
+                y=torch.empty(DEC_N * 4, DEC_H * D, device=dev))
+    ms = timed(lambda: mixer.kda_decode(N=DEC_N, T=4, H=DEC_H, **dv, **vout))
+    C1 = DEC_H * D
+    vbytes = DEC_N * (DEC_H * D * D * 4 * 2 + 3 * C1 * 3 * 4 * 2 + 4 * (3 * C1 * 2 + C1 * 4 * 3
+                                                                      + DEC_H * 4))
+    print(json.dumps({"config": "verify: 64 sequences x 4 tokens, H=64, fused decode kernel",
+                      "ms_per_call": ms, "tokens_per_s": DEC_N * 4 / (ms / 1e3),
+                      "hbm_gbs": vbytes / (ms / 1e3) / 1e9,
+                      "frac_hbm": vbytes / (ms / 1e3) / 1e9 / peaks["hbm_gbs"]}), flush=True)
+    del dv, vout
+
+    # 3 varlen: 16 packed sequences, lengths U[256, 8192], fused prefill
+    var = inputs.varlen_prefill()
+    dvl = to_dev(var)
+    cu_h = torch.from_numpy(var.cu_seqlens.astype(np.int32))
+    cu_d = cu_h.to(dev)
+    total = int(cu_h[-1])
+    ws = kda.prefill_workspace(var.N, total, var.H, dev)
+    vout = dict(state_out=torch.empty_like(dvl["state_in"]), ring_out=torch.empty_like(dvl["ring_in"]),
+                y=torch.empty(total, var.H * D, device=dev))
+    ms = timed(lambda: mixer.kda_prefill(H=var.H, cu_seqlens=cu_d, cu_seqlens_host=cu_h,
+                                         workspace=ws, **dvl, **vout))
+    print(json.dumps({"config": f"varlen: {var.N} sequences, lengths U[256, 8192] "
+                                f"({total} tokens), H={var.H}, fused prefill",
+                      "ms_per_call": ms, "tokens_per_s": total / (ms / 1e3)}), flush=True)
+    del dvl, vout, ws
+
+    # 4 GDN long: 1 x 16384 tokens, H=32, per-head gate, f32, prep + scan (no conv, no norm)
+    gdn = inputs.gdn_long()
+    dg = to_dev(gdn)
+    rows = gdn.rows
+    ws = kda.scan_workspace(1, rows, gdn.H, dev, kda.ALGO_AUTO)
+    f32 = lambda *sh: torch.empty(*sh, device=dev)  # noqa: E731
+    C4 = gdn.H * D
+    gbuf = dict(q_hat=f32(rows, C4), k_hat=f32(rows, C4), v_hat=f32(rows, C4), g=f32(rows, gdn.H),
+                beta=f32(rows, gdn.H), o=f32(rows, C4))
+    st = torch.empty_like(dg["state_in"])
+    ms = timed(lambda: mixer.kda_forward(H=gdn.H, N=1, T=rows, gate_mode=1, out=gbuf,
+                                         state_out=st, workspace=ws,
+                                         **{k: v for k, v in dg.items()
+                                            if k not in ("norm_w", "gate_raw")}))
+    print(json.dumps({"config": f"GDN long: 1 x {rows} tokens, H={gdn.H}, per-head gate, f32, "
+                                "prep + scan (AUTO: chunked)",
+                      "ms_per_call": ms, "tokens_per_s": rows / (ms / 1e3)}), flush=True)
+
+
 def run_crossover(args):
     """The sequential and the chunked scan (kda_scan, q/k/v/g resident) over a grid of sequence
     counts and lengths at H = 64: one JSON line per point with both times.  The library's AUTO
@@ -729,6 +813,8 @@ def main():
                     help="prefill scan form (auto = the library's choice for the shape)")
     ap.add_argument("--skip-e2e", action="store_true", help="profiling runs: no host-copy leg")
     ap.add_argument("--skip-cpu", action="store_true", help="profiling runs: no oracle timing")
+    ap.add_argument("--configs", action="store_true",
+                    help="time the verify, varlen and GDN-long configurations, one JSON line each")
     ap.add_argument("--crossover", action="store_true",
                     help="time the sequential vs the chunked scan over lengths and exit")
     ap.add_argument("--heads", type=int, default=PREFILL_H,
@@ -736,6 +822,9 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.configs:
+        run_configs(args)
+        return
     if args.crossover:
         run_crossover(args)
         return
