@@ -38,22 +38,29 @@ METRIC = "KDA prefill tokens/s (H=64,d=128); decode state HBM GB/s vs peak"
 D = 128
 PREFILL_T, PREFILL_H = 4096, 64
 RB_T = 4                         # verify width of the rollback workload
+VER_T = 4                        # tokens per sequence of the verify leg
 DEC_N, DEC_H = 64, 64
 FLOP_PER_TOKEN_HEAD = 7 * D * D   # decay D^2 + S^T k 2D^2 + rank-1 update 2D^2 + S^T q 2D^2
-SMS, FP32_LANES, SM_MAX_MHZ = 152, 128, 2070.0
+FP32_LANES, SM_MAX_MHZ = 128, 2070.0
 
 
 def _peaks():
+    """Roofline denominators: the measured copy bandwidth and bf16 GEMM rates of this machine's
+    GB300s when MEASURED_PEAKS.json is present, else the recipe's fallback figures."""
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         d = json.load(open(p))
-        return dict(hbm_gbs=float(d["hbm_gbs"]), src="measured", sm_max_mhz=float(
-            d.get("sm_max_mhz", SM_MAX_MHZ)))
-    return dict(hbm_gbs=6800.0, src="fallback", sm_max_mhz=SM_MAX_MHZ)
+        return dict(hbm_gbs=float(d["hbm_gbs"]), src="measured",
+                    bf16_tflops=float(d.get("bf16_tflops", 1900.0)),
+                    bf16_tflops_sustained=float(d.get("bf16_tflops_sustained", 1700.0)),
+                    sm_max_mhz=float(d.get("sm_max_mhz", SM_MAX_MHZ)))
+    return dict(hbm_gbs=6800.0, src="fallback", bf16_tflops=1900.0,
+                bf16_tflops_sustained=1700.0, sm_max_mhz=SM_MAX_MHZ)
 
 
-def _fp32_peak_tflops(mhz):
-    return SMS * FP32_LANES * 2 * mhz * 1e6 / 1e12
+def _fp32_peak_tflops(sms, mhz):
+    """FP32 FMA peak: SMs x 128 lanes x 2 flop x clock."""
+    return sms * FP32_LANES * 2 * mhz * 1e6 / 1e12
 
 
 def _dist():
@@ -204,29 +211,70 @@ def _traffic(kernel, files):
     return d.get("dram_bytes_per_launch")
 
 
-def _kernel_bytes(T, H, blk_bytes, chunks):
-    """Algorithmic HBM bytes per launch of each kernel of the prefill step (T tokens, H heads, one
-    sequence, conv K=4, bf16 raw q/k/v): what the kernel must read and write, once each."""
+def _method_bytes(T, H, K=4):
+    """The method's own HBM bytes per prefill step (T tokens, H heads, one sequence, conv K taps,
+    bf16 raw q/k/v), split by the kernel that moves them: every input read once, every output
+    written once, no intermediate.  What the library writes and reads back between its own
+    kernels (the chunk workspace, the readout plane o, the staged path's prepared planes) is
+    implementation traffic, reported apart by _impl_bytes."""
     C = H * D
     f32, bf16 = 4, 2
     plane = T * C * f32
-    ws = chunks * H * blk_bytes
+    raw = 3 * T * C * bf16
+    small = C * f32 + H * f32                       # dt_bias, A_log
+    conv = 3 * C * K * f32
+    ring = 3 * C * (K - 1) * f32                    # one direction
+    state = H * D * D * f32                         # one direction
+    beta = T * H * f32
+    norm = plane + D * f32                          # z read (y written: plane below)
     return {
-        # raw q, k, v (bf16), gate input, beta input, conv weights + ring -> q, k, v, g, beta
-        "kda_prep_kernel": 3 * T * C * bf16 + plane + T * H * f32 + 3 * C * 4 * f32
-                           + 3 * C * 3 * f32 + 4 * plane + T * H * f32,
-        "kda_ring_roll_kernel": 3 * C * 3 * (bf16 + f32),
-        # q, k, v, g, beta -> the workspace of operand images
-        "kda_chunk_intra_kernel": 4 * plane + T * H * f32 + ws,
-        # raw q, k, v (bf16), gate input, beta input, conv weights + ring -> the workspace
-        "kda_chunk_prep_intra_kernel": 3 * T * C * bf16 + plane + T * H * f32 + 3 * C * 4 * f32
-                                       + 3 * C * 3 * f32 + ws,
-        # workspace + state in -> o + state out; in the fused prefill also the conv ring roll
-        "kda_chunk_inter_kernel": ws + 2 * H * D * D * f32 + plane + 3 * C * 3 * (bf16 + 2 * f32),
+        # fused path: raw q, k, v, f, beta, conv weights, ring in, gate parameters
+        "kda_chunk_prep_intra_kernel": raw + plane + beta + conv + ring + small,
+        # state in and out, the rolled ring out
+        "kda_chunk_inter_kernel": 2 * state + ring,
+        # z and the norm weight in, y out
+        "kda_gated_rmsnorm_kernel": norm + plane,
+        # staged path: prep reads what the fused prep reads and writes the ring; the scan moves
+        # the state (its q, k, v, g, beta in and o out are intermediates)
+        "kda_prep_kernel": raw + plane + beta + conv + 2 * ring + small,
+        "kda_ring_roll_kernel": 0,
+        "kda_chunk_intra_kernel": 0,
+        "kda_scan_seq_kernel": 2 * state,
         "kda_chunk_offsets_kernel": 0,
-        # o + RMSNorm gate + weight -> y
-        "kda_gated_rmsnorm_kernel": 3 * plane + D * f32,
     }
+
+
+def _impl_bytes(T, H, blk_bytes, chunks, K=4):
+    """Intermediate bytes each kernel of the prefill step writes or reads back (not the method's
+    I/O): the chunk workspace (one block per (chunk, head)), the readout plane o between the scan
+    and the RMSNorm, and the staged path's prepared q, k, v, g, beta planes."""
+    C = H * D
+    plane = T * C * 4
+    ws = chunks * H * blk_bytes
+    prepared = 4 * plane + T * H * 4
+    return {
+        "kda_chunk_prep_intra_kernel": ws,
+        "kda_chunk_inter_kernel": ws + plane,
+        "kda_gated_rmsnorm_kernel": plane,
+        "kda_prep_kernel": prepared,
+        "kda_ring_roll_kernel": 3 * C * (K - 1) * (2 + 4 + 4),
+        "kda_chunk_intra_kernel": prepared + ws,
+        "kda_scan_seq_kernel": prepared + plane,
+        "kda_chunk_offsets_kernel": 0,
+    }
+
+
+def _chunk_flops(T, H):
+    """Products the chunked form's tensor cores compute per launch (one pass, i.e. before the
+    bf16 x3 split that triples the MMA instructions), for 32-token chunks: intra = A and Aqk
+    ([K;Q] (64 x 128) times K^T) plus [W | U] = Tm times [beta K e^G | beta V] (32 x 32 x 256);
+    inter = MMA-1 (S^T, 128 x 128, times 64 rows) plus MMA-2 (U'^T, 128 x 32, times 160 rows)."""
+    chunks_h = (T + 31) // 32 * H
+    intra = 2 * 64 * 128 * 32 + 2 * 32 * 32 * 256
+    inter = 2 * 128 * 128 * 64 + 2 * 128 * 32 * 160
+    return {"kda_chunk_prep_intra_kernel": chunks_h * intra,
+            "kda_chunk_intra_kernel": chunks_h * intra,
+            "kda_chunk_inter_kernel": chunks_h * inter}
 
 
 def _prefill_e2e(args, d, buf, state_out, ring_out, stream, barrier, max_over_ranks, mixer,
@@ -282,7 +330,15 @@ def _prefill_e2e(args, d, buf, state_out, ring_out, stream, barrier, max_over_ra
     for _ in range(max(3, args.warmup // 4)):
         e2e_step()
     barrier()
-    Ke = max(3, args.steps // 10)
+    # at least 20 steps and at least a second of timed work (the warm-up sets the estimate)
+    w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_start(w0)
+    for _ in range(3):
+        e2e_step()
+    e2e_stop(w1)
+    barrier()
+    est_ms = max(w0.elapsed_time(w1) / 3, 1e-3)
+    Ke = max(20, args.steps // 10, int(1000.0 / est_ms) + 1)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e2e_start(e0)
     for _ in range(Ke):
@@ -404,7 +460,8 @@ def run_ours(args):
     else:
         scan_ms = statistics.mean(a.elapsed_time(b) for a, b in scan_ev)
     scan_flop = FLOP_PER_TOKEN_HEAD * T * H
-    fp32_peak = _fp32_peak_tflops(peaks["sm_max_mhz"])
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    fp32_peak = _fp32_peak_tflops(sms, peaks["sm_max_mhz"])
     scan_tflops = scan_flop / (scan_ms / 1e3) / 1e12
     assert kda.kda_device_status() == 0
 
@@ -473,6 +530,38 @@ def run_ours(args):
     dec_graph_ms = max_over_ranks(g0.elapsed_time(g1)) / Kd
     assert kda.kda_device_status() == 0
 
+    # ---------------- 4-token verify of the decode batch (the same kernel, T = 4) -------------
+    ver4 = inputs.decode_step(N=DEC_N, T=VER_T, H=DEC_H)
+    dv4 = {k: getattr(ver4, k).to(dev) for k in
+           ("q_raw", "k_raw", "v_raw", "conv_w", "ring_in", "f_raw", "dt_bias", "a_log",
+            "beta_raw", "state_in", "norm_w", "gate_raw")}
+    v_states = [dv4["state_in"], torch.empty_like(dv4["state_in"])]
+    v_ring = dv4["ring_in"]
+    y_ver = torch.empty(DEC_N * VER_T, DEC_H * D, device=dev)
+
+    def verify_step(i):
+        kda.kda_decode_fused(dv4["q_raw"], dv4["k_raw"], dv4["v_raw"], dv4["conv_w"], v_ring,
+                             v_ring, dv4["f_raw"], dv4["dt_bias"], dv4["a_log"],
+                             dv4["beta_raw"], v_states[i & 1], v_states[(i + 1) & 1],
+                             dv4["norm_w"], dv4["gate_raw"], y_ver, N=DEC_N, T=VER_T, H=DEC_H)
+
+    for i in range(max(args.warmup, 3)):
+        verify_step(i)
+    barrier()
+    v0, v1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    v0.record(stream)
+    for i in range(Kd):
+        verify_step(i)
+    v1.record(stream)
+    barrier()
+    ver_ms = max_over_ranks(v0.elapsed_time(v1)) / Kd
+    # state and ring read + written once per call; per token raw q/k/v in, f, beta, z in, y out
+    ver_bytes = (DEC_N * (DEC_H * D * D * 4 * 2 + 3 * C1 * 3 * 4 * 2)
+                 + DEC_N * VER_T * (3 * C1 * 2 + C1 * 4 * 3 + DEC_H * 4)
+                 + 3 * C1 * 4 * 4 + C1 * 4 + DEC_H * 4 + D * 4)
+    assert kda.kda_device_status() == 0
+    del dv4, v_states, y_ver
+
     # ---------------- verify rollback (the decode kernel on accepted prefixes) ----------------
     import numpy as np
     ver = inputs.decode_step(N=DEC_N, T=RB_T, H=DEC_H, seed=5)
@@ -513,39 +602,70 @@ def run_ours(args):
         return None
 
     cpu = None if args.skip_cpu else cpu_baseline(pre, args.cpu_sample_heads)
-    kbytes = _kernel_bytes(T, H, blk_bytes, chunks)
+    mbytes = _method_bytes(T, H)
+    ibytes = _impl_bytes(T, H, blk_bytes, chunks)
+    cflops = _chunk_flops(T, H)
+    tensor_peak = peaks["bf16_tflops_sustained"]
     total_kms = sum(v[1] for v in ktimes.values())
     kernels = []
     for name, (n, kms) in sorted(ktimes.items(), key=lambda kv: -kv[1][1]):
         per = kms / n
-        b = kbytes.get(name)
         ent = {"kernel": name, "launches": n, "ms_per_launch": per, "share": kms / total_kms,
                "traffic": _traffic(name, KERNEL_SOURCES.get(name, []))}
-        if b:
-            gbs = b / (per / 1e3) / 1e9
-            ent.update(bytes_per_launch=b, gbs=gbs, frac_hbm=gbs / peaks["hbm_gbs"])
+        if name in mbytes:
+            gbs = mbytes[name] / (per / 1e3) / 1e9
+            ent.update(bytes_per_launch=mbytes[name], gbs=gbs, frac_hbm=gbs / peaks["hbm_gbs"],
+                       impl_bytes_per_launch=ibytes[name],
+                       impl_gbs=ibytes[name] / (per / 1e3) / 1e9)
+        if name in cflops:
+            tf = cflops[name] / (per / 1e3) / 1e12
+            ent.update(tensor_flop_per_launch=cflops[name], tensor_tflops=tf,
+                       frac_tensor=tf / tensor_peak)
         kernels.append(ent)
+    step_bytes = sum(mbytes[k] for k in ("kda_chunk_prep_intra_kernel", "kda_chunk_inter_kernel",
+                                         "kda_gated_rmsnorm_kernel"))
+    method_tflops = scan_flop / (ms_step / 1e3) / 1e12
+    step = {"method_bytes": step_bytes, "method_gbs": step_bytes / (ms_step / 1e3) / 1e9,
+            "frac_hbm": step_bytes / (ms_step / 1e3) / 1e9 / peaks["hbm_gbs"],
+            "method_flop": scan_flop, "method_tflops": method_tflops,
+            "note": "the whole step: the method's I/O (raw q/k/v, f, beta, z, conv weights, ring "
+                    "and state in and out, y) and its 7*D^2 flop per token-head over the step "
+                    "time"}
     if fused:
         top = kernels[0]
-        src_files = KERNEL_SOURCES
         roofline = {"bound": "hbm", "kernel": top["kernel"], "achieved": top.get("gbs"),
                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": top.get("frac_hbm"),
-                    "traffic": _traffic(top["kernel"], src_files.get(top["kernel"], [])),
+                    "traffic": _traffic(top["kernel"], KERNEL_SOURCES.get(top["kernel"], [])),
                     "bytes_per_launch": top.get("bytes_per_launch"),
+                    "impl_bytes_per_launch": top.get("impl_bytes_per_launch"),
                     "ms_per_launch": top["ms_per_launch"],
                     "peak_src": f"{peaks['src']} hbm_gbs (copy bandwidth)",
+                    "bytes": "the method's I/O this kernel moves (raw q/k/v, f, beta, conv "
+                             "weights, ring in); its workspace writes are impl_bytes_per_launch",
                     "timing": "library CUDA-event timer around each launch, timed region"}
+        # the prefill's fraction of the tensor-pipe roofline: the method's flop over the step
+        roofline_tensor = {"bound": "tensor", "kernel": "whole step (prep + intra, inter, "
+                                                        "RMSNorm)",
+                           "achieved": method_tflops, "peak": tensor_peak, "unit": "TFLOP/s",
+                           "frac": method_tflops / tensor_peak,
+                           "flop_per_step": scan_flop,
+                           "peak_src": f"{peaks['src']} bf16_tflops_sustained (cuBLAS bf16 GEMM "
+                                       "over seconds)"}
     else:
         roofline = {"bound": "alu", "kernel": "kda_scan_seq_kernel", "achieved": scan_tflops,
                     "peak": fp32_peak, "unit": "TFLOP/s", "frac": scan_tflops / fp32_peak,
                     "traffic": _traffic("kda_scan_seq_kernel",
                                         KERNEL_SOURCES["kda_scan_seq_kernel"]),
                     "ms_per_launch": scan_ms, "flop_per_launch": scan_flop,
-                    "peak_src": f"152 SMs x 128 FP32 lanes x 2 x {peaks['sm_max_mhz']:.0f} MHz"}
+                    "peak_src": f"{sms} SMs x 128 FP32 lanes x 2 x {peaks['sm_max_mhz']:.0f} MHz"}
+        roofline_tensor = None
     return {
         "metric": METRIC, "value": tokens_per_s, "unit": "tokens/s", "n_gpus": ws,
         "steps": K, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": ("f32 state and elementwise; tensor-core products bf16 x3 "
+                  "(hi*hi + hi*lo + lo*hi, f32 accumulate); bf16 raw q/k/v" if fused
+                  else "f32 (FP32 FMA scan); bf16 raw q/k/v"),
         "data": "synthetic (seeded numpy default_rng; bf16 raw q/k/v, f32 gates, state, norm)",
         "config": {"workload": f"prefill: 1 sequence x 4096 tokens, H={H}, head_dim=128, conv K=4,"
                                " zero state and ring, whole mixer per step",
@@ -557,6 +677,8 @@ def run_ours(args):
                    "l2": "inputs larger than L2 (470 MB read per step)"},
         "gpu_launches": sum(v[0] for v in ktimes.values()),
         "roofline": roofline,
+        "roofline_tensor": roofline_tensor,
+        "step": step,
         "kernels": kernels,
         "scan_ms_per_step": scan_ms,
         "e2e": e2e,
@@ -579,6 +701,15 @@ def run_ours(args):
                                       "peak": peaks["hbm_gbs"], "unit": "GB/s",
                                       "frac": dec_bytes / (dec_graph_ms / 1e3) / 1e9
                                       / peaks["hbm_gbs"], "bytes_per_launch": dec_bytes}},
+        "verify": {"workload": f"{DEC_N} sequences x {VER_T} tokens, H={DEC_H}, one "
+                               "kda_decode_fused launch (the decode kernel at T = 4), states "
+                               "ping-ponged",
+                   "ms_per_step": ver_ms, "tokens_per_s": ws * DEC_N * VER_T / (ver_ms / 1e3),
+                   "roofline": {"bound": "hbm", "kernel": "kda_decode_fused_kernel",
+                                "achieved": ver_bytes / (ver_ms / 1e3) / 1e9,
+                                "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                "frac": ver_bytes / (ver_ms / 1e3) / 1e9 / peaks["hbm_gbs"],
+                                "bytes_per_launch": ver_bytes}},
         "rollback": {"workload": f"{DEC_N} sequences, verify width {RB_T}, H={DEC_H}, accepted "
                                  f"prefixes U[1, {RB_T - 1}] ({kept} rows kept), one "
                                  "kda_verify_rollback launch",

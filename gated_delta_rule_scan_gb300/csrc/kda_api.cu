@@ -15,22 +15,39 @@ using namespace kda;
 // one device error word per device, raised by kernels that give up a bounded wait
 __device__ int g_kda_dev_err;
 
-constexpr int kMaxDevices = 64;
 constexpr int kMaxGridY = 65535;  // sequences (and heads) map to gridDim.y
 
+// the current device's error word (its address is looked up once per device)
 int* dev_err_ptr() {
-    static int* ptrs[kMaxDevices] = {nullptr};
+    static PerDevice<int*> ptrs;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-    if (!ptrs[dev]) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_kda_dev_err) != cudaSuccess) return nullptr;
-        ptrs[dev] = static_cast<int*>(p);
+    int* p = ptrs[dev].load(std::memory_order_acquire);
+    if (p == nullptr) {
+        void* q = nullptr;
+        if (cudaGetSymbolAddress(&q, g_kda_dev_err) != cudaSuccess) return nullptr;
+        p = static_cast<int*>(q);
+        ptrs[dev].store(p, std::memory_order_release);
     }
-    return ptrs[dev];
+    return p;
 }
 
 inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA_BASE + (int)e; }
+
+// The kernels run on the stream's device, while the per-device lookups (the error word, the fixed
+// scratch, function attributes) follow the current device: a stream of another device is a
+// contract violation (40012).  The legacy and per-thread default streams always belong to the
+// current device.  Only host-side queries; nothing is launched.
+int check_stream_device(void* stream) {
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (s == nullptr || s == cudaStreamLegacy || s == cudaStreamPerThread) return KDA_OK;
+    int sdev = -1, cur = -1;
+    cudaError_t e = cudaStreamGetDevice(s, &sdev);
+    if (e != cudaSuccess) return cuda_status(e);
+    e = cudaGetDevice(&cur);
+    if (e != cudaSuccess) return cuda_status(e);
+    return sdev == cur ? KDA_OK : KDA_ERR_STREAM_DEVICE;
+}
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -104,6 +121,7 @@ int prep_impl(const void* q_raw, const void* k_raw, const void* v_raw, int raw_d
                               dt_bias, a_log, gate_mode, gate_lb, beta_raw, q_hat, k_hat, v_hat,
                               g, beta, seq, H, D, K, l2_eps, true, a);
     if (rc != KDA_OK || seq.N == 0) return rc;
+    if (const int sd = check_stream_device(stream)) return sd;
     return cuda_status(launch_prep(a, static_cast<cudaStream_t>(stream)));
 }
 
@@ -158,6 +176,7 @@ int scan_impl(const float* q, const float* k, const float* v, const float* g, in
         const bool wide = (long)seq.N * H >= kAutoWidePairs;
         chunk = ws_ok && (ml >= kAutoChunkMinLen || (wide && ml >= kAutoChunkMinLenWide));
     }
+    if (const int sd = check_stream_device(stream)) return sd;
     a.err = dev_err_ptr();  // null only if the symbol lookup failed: waits then report nothing
     return cuda_status(chunk ? launch_scan_chunk(a, cu_host, workspace, static_cast<cudaStream_t>(stream))
                              : launch_scan_seq(a, static_cast<cudaStream_t>(stream)));
@@ -214,6 +233,7 @@ int prefill_impl(const void* q_raw, const void* k_raw, const void* v_raw, int ra
     const size_t need = L.chunk + chunk_workspace_bytes(seq, cu_host, H);
     if (workspace == nullptr || workspace_bytes < need) return KDA_ERR_WORKSPACE;
     if (!aligned16(workspace)) return KDA_ERR_ALIGN;
+    if (const int sd = check_stream_device(stream)) return sd;
     unsigned char* w = static_cast<unsigned char*>(workspace);
     float* oh = reinterpret_cast<float*>(w + L.o);
     ScanArgs a{};
@@ -234,6 +254,7 @@ int norm_impl(const float* o, const float* norm_w, const float* gate_raw, float*
     if (!o || !norm_w || !gate_raw || !y) return KDA_ERR_NULL;
     if (!aligned16(o) || !aligned16(norm_w) || !aligned16(gate_raw) || !aligned16(y))
         return KDA_ERR_ALIGN;
+    if (const int sd = check_stream_device(stream)) return sd;
     NormArgs a{o, norm_w, gate_raw, y, rows, eps, silu ? 1 : 0};
     return cuda_status(launch_gated_rmsnorm(a, static_cast<cudaStream_t>(stream)));
 }
@@ -278,6 +299,7 @@ int decode_impl(const void* q_raw, const void* k_raw, const void* v_raw, int raw
     if (rollback && keep == nullptr) return KDA_ERR_NULL;
     a.keep = keep;
     a.norm_silu = norm_silu ? 1 : 0;
+    if (const int sd = check_stream_device(stream)) return sd;
     return cuda_status(launch_decode_fused(a, static_cast<cudaStream_t>(stream)));
 }
 
@@ -303,6 +325,8 @@ const char* kda_status_string(int s) {
         case KDA_ERR_ALIGN: return "a pointer that must be 16-byte aligned is not";
         case KDA_ERR_SCRATCH_LIMIT:
             return "the chunked scratch this call needs exceeds KDA_STATIC_SCRATCH_BYTES";
+        case KDA_ERR_STREAM_DEVICE:
+            return "the stream belongs to a device other than the current one";
         default:
             if (s >= KDA_ERR_CUDA_BASE && s < KDA_ERR_CUDA_BASE + 10000) return "CUDA error";
             return "unknown status";
@@ -489,12 +513,14 @@ int kda_verify_rollback(const void* q_raw, const void* k_raw, const void* v_raw,
 }
 
 int kda_selftest_wait_timeout(void* stream) {
+    if (const int sd = check_stream_device(stream)) return sd;
     int* p = dev_err_ptr();
     if (p == nullptr) return cuda_status(cudaErrorUnknown);
     return cuda_status(launch_wait_selftest(p, static_cast<cudaStream_t>(stream)));
 }
 
 int kda_device_status(void* stream) {
+    if (const int sd = check_stream_device(stream)) return sd;
     cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_status(e);
     int* p = dev_err_ptr();
@@ -526,6 +552,7 @@ int kda_scan_varlen_static(const float* q_hat, const float* k_hat, const float* 
     const SeqLayout seq{cu_seqlens, 0, N, (long)total_T};
     if (chunk_workspace_bytes(seq, cu_seqlens_host, H) > kStaticScratchBytes)
         return KDA_ERR_SCRATCH_LIMIT;
+    if (const int sd = check_stream_device(stream)) return sd;
     void* scratch = nullptr;
     const cudaError_t e = static_scratch(&scratch);
     if (e != cudaSuccess) return cuda_status(e);

@@ -389,15 +389,16 @@ done:
 }
 
 // Opt a kernel into `bytes` of dynamic shared memory once per device; `done` is the caller's own
-// per-kernel flag array (one per template instantiation).
+// per-device flag array (one per template instantiation).
 template <typename K>
-inline cudaError_t set_smem(K kernel, size_t bytes, int (&done)[64]) {
+inline cudaError_t set_smem(K kernel, size_t bytes, PerDevice<int>& done) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
+    const bool cached = dev >= 0 && dev < kMaxDevices;
+    if (cached && done[dev].load(std::memory_order_acquire)) return cudaSuccess;
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
-    if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = 1;
+    if (e == cudaSuccess && cached) done[dev].store(1, std::memory_order_release);
     return e;
 }
 

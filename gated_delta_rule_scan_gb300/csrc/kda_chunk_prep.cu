@@ -747,7 +747,7 @@ template <bool BF16, int GM, bool CONV, int KW>
 static cudaError_t launch_prep_intra_t(const PrepArgs& p, const ScanArgs& a, const int* chunk_off,
                                        unsigned char* blocks, long nchunks, cudaStream_t s) {
     const size_t smem = kPrepIntraSmemBytes;
-    static int done[64] = {0};
+    static PerDevice<int> done;
     cudaError_t e = set_smem(kda_chunk_prep_intra_kernel<BF16, GM, CONV, KW>, smem, done);
     if (e != cudaSuccess) return e;
     int dev = 0, sms = 0;

@@ -7,10 +7,20 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace kda {
 
 constexpr int kHeadDim = 128;      // the only head width the kernels are built for
 constexpr int kMaxConvK = 8;       // conv window held in registers (taps 2..8)
+constexpr int kMaxDevices = 64;    // per-device caches (symbol addresses, function attributes)
+
+// A value looked up once per device (a symbol address, an attribute that was set).  Every slot
+// is an atomic, so host threads that make their first call on one device at the same time each
+// look the value up and store the same result: no data race.  The cache is not invalidated by
+// cudaDeviceReset; a process that resets a device must not call the library on it afterwards.
+template <typename T>
+using PerDevice = std::atomic<T>[kMaxDevices];
 
 // Row ranges of the packed token-major arrays.  When cu_seqlens is null every sequence has
 // T_uniform tokens and sequence n owns rows [n*T, (n+1)*T).

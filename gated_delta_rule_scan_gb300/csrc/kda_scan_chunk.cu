@@ -565,7 +565,7 @@ template <int GM>
 static cudaError_t launch_inter_t(const ScanArgs& a, const int* chunk_off,
                                   const unsigned char* blocks, const PrepArgs& ring, cudaStream_t s) {
     const size_t smem2 = sizeof(InterSmem) + 128;
-    static int done2[64] = {0};
+    static PerDevice<int> done2;
     cudaError_t e = set_smem(kda_chunk_inter_kernel<GM>, smem2, done2);
     if (e != cudaSuccess) return e;
     dim3 g2((unsigned)a.H, (unsigned)a.seq.N);
@@ -596,7 +596,7 @@ static cudaError_t launch_chunk_t(const ScanArgs& a, const int* cu_host, void* w
     if (e != cudaSuccess) return e;
     if (nchunks > 0) {
         const size_t smem1 = sizeof(IntraSmem) + 128;
-        static int done1[64] = {0};
+        static PerDevice<int> done1;
         e = set_smem(kda_chunk_intra_kernel<GM, EXP>, smem1, done1);
         if (e != cudaSuccess) return e;
         dim3 g1((unsigned)nchunks, (unsigned)a.H);

@@ -227,15 +227,16 @@ static cudaError_t launch_t(const ScanArgs& a, cudaStream_t s) {
         tg = tq;  // unused
     }
     const size_t smem = sizeof(ScanSmem) + 128;
-    static int attr_done[64] = {0};  // per device
+    static PerDevice<int> attr_done;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64 || !attr_done[dev]) {
+    const bool cached = dev >= 0 && dev < kMaxDevices;
+    if (!cached || !attr_done[dev].load(std::memory_order_acquire)) {
         e = cudaFuncSetAttribute(kda_scan_seq_kernel<GM, EXP>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        if (dev >= 0 && dev < 64) attr_done[dev] = 1;
+        if (cached) attr_done[dev].store(1, std::memory_order_release);
     }
     dim3 grid((unsigned)(a.H * kColBlocks), (unsigned)a.seq.N);
     KernelTimer kt(kKScanSeq, s);

@@ -11,19 +11,20 @@ namespace kda {
 static __device__ __align__(256) unsigned char g_kda_static_scratch[kStaticScratchBytes];
 
 cudaError_t static_scratch(void** ptr) {
-    static void* ptrs[64] = {nullptr};
+    static PerDevice<void*> ptrs;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (ptrs[dev] == nullptr) {
-        // one-time setup on this device (the caller has made it current)
-        void* p = nullptr;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    void* p = ptrs[dev].load(std::memory_order_acquire);
+    if (p == nullptr) {
+        // one-time setup on this device (the caller has made it current and checked that the
+        // stream belongs to it)
         e = cudaGetSymbolAddress(&p, g_kda_static_scratch);
         if (e != cudaSuccess) return e;
-        ptrs[dev] = p;
+        ptrs[dev].store(p, std::memory_order_release);
     }
-    *ptr = ptrs[dev];
+    *ptr = p;
     return cudaSuccess;
 }
 

@@ -141,6 +141,17 @@ def _check(fn: str, status: int):
         raise KdaError(fn, status)
 
 
+def _call(fn: str, like, *args):
+    """Call C entry ``fn`` with the device of tensor ``like`` current: the library keys its
+    per-device lookups by the current device and requires the stream to belong to it (40012)."""
+    if isinstance(like, torch.Tensor) and like.is_cuda:
+        with torch.cuda.device(like.device):
+            status = getattr(_lib, fn)(*args)
+    else:
+        status = getattr(_lib, fn)(*args)
+    _check(fn, status)
+
+
 def _raw_dtype(t) -> int:
     return DTYPE_BF16 if t.dtype == torch.bfloat16 else DTYPE_F32
 
@@ -149,11 +160,11 @@ def kda_conv_l2norm_prep(q_raw, k_raw, v_raw, conv_w, ring_in, ring_out, f_raw, 
                          beta_raw, q_hat, k_hat, v_hat, g, beta, *, N, T, H, K=4, gate_mode=0,
                          gate_lb=-5.0, l2_eps=1e-6, D=HEAD_DIM, stream=None):
     st = _stream(stream, q_hat)
-    _check("kda_conv_l2norm_prep", _lib.kda_conv_l2norm_prep(
+    _call("kda_conv_l2norm_prep", q_hat,
         _ptr(q_raw), _ptr(k_raw), _ptr(v_raw), _raw_dtype(q_raw), _ptr(conv_w), _ptr(ring_in),
         _ptr(ring_out), _ptr(f_raw), _ptr(dt_bias), _ptr(a_log), gate_mode, gate_lb,
         _ptr(beta_raw), _ptr(q_hat), _ptr(k_hat), _ptr(v_hat), _ptr(g), _ptr(beta), N, T, H, D, K,
-        l2_eps, st))
+        l2_eps, st)
 
 
 def kda_conv_l2norm_prep_varlen(q_raw, k_raw, v_raw, conv_w, ring_in, ring_out, f_raw, dt_bias,
@@ -164,11 +175,11 @@ def kda_conv_l2norm_prep_varlen(q_raw, k_raw, v_raw, conv_w, ring_in, ring_out, 
     N = cu_seqlens_host.numel() - 1
     total = int(cu_seqlens_host[-1])
     st = _stream(stream, q_hat)
-    _check("kda_conv_l2norm_prep_varlen", _lib.kda_conv_l2norm_prep_varlen(
+    _call("kda_conv_l2norm_prep_varlen", q_hat,
         _ptr(q_raw), _ptr(k_raw), _ptr(v_raw), _raw_dtype(q_raw), _ptr(conv_w), _ptr(ring_in),
         _ptr(ring_out), _ptr(f_raw), _ptr(dt_bias), _ptr(a_log), gate_mode, gate_lb,
         _ptr(beta_raw), _ptr(q_hat), _ptr(k_hat), _ptr(v_hat), _ptr(g), _ptr(beta),
-        _ptr(cu_seqlens), _ptr(cu_seqlens_host), N, total, H, D, K, l2_eps, st))
+        _ptr(cu_seqlens), _ptr(cu_seqlens_host), N, total, H, D, K, l2_eps, st)
 
 
 def kda_scan_workspace_bytes(N, total_T, H, gate_mode=0, algo=ALGO_AUTO, D=HEAD_DIM) -> int:
@@ -187,9 +198,9 @@ def kda_scan(q_hat, k_hat, v_hat, g, beta, state_in, state_out, o, *, N, T, H, g
     scale = D ** -0.5 if scale is None else scale
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     st = _stream(stream, state_out)
-    _check("kda_scan", _lib.kda_scan(
+    _call("kda_scan", state_out,
         _ptr(q_hat), _ptr(k_hat), _ptr(v_hat), _ptr(g), gate_mode, _ptr(beta), _ptr(state_in),
-        _ptr(state_out), _ptr(o), N, T, H, D, scale, algo, _ptr(workspace), ws_bytes, st))
+        _ptr(state_out), _ptr(o), N, T, H, D, scale, algo, _ptr(workspace), ws_bytes, st)
 
 
 def kda_scan_gqa(q_hat, k_hat, v_hat, g, beta, state_in, state_out, o, *, N, T, H, Hk,
@@ -198,9 +209,9 @@ def kda_scan_gqa(q_hat, k_hat, v_hat, g, beta, state_in, state_out, o, *, N, T, 
     scale = D ** -0.5 if scale is None else scale
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     st = _stream(stream, state_out)
-    _check("kda_scan_gqa", _lib.kda_scan_gqa(
+    _call("kda_scan_gqa", state_out,
         _ptr(q_hat), _ptr(k_hat), _ptr(v_hat), _ptr(g), gate_mode, _ptr(beta), _ptr(state_in),
-        _ptr(state_out), _ptr(o), N, T, H, Hk, D, scale, algo, _ptr(workspace), ws_bytes, st))
+        _ptr(state_out), _ptr(o), N, T, H, Hk, D, scale, algo, _ptr(workspace), ws_bytes, st)
 
 
 def kda_scan_varlen_gqa(q_hat, k_hat, v_hat, g, beta, state_in, state_out, o, cu_seqlens,
@@ -212,10 +223,10 @@ def kda_scan_varlen_gqa(q_hat, k_hat, v_hat, g, beta, state_in, state_out, o, cu
     scale = D ** -0.5 if scale is None else scale
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     st = _stream(stream, state_out)
-    _check("kda_scan_varlen_gqa", _lib.kda_scan_varlen_gqa(
+    _call("kda_scan_varlen_gqa", state_out,
         _ptr(q_hat), _ptr(k_hat), _ptr(v_hat), _ptr(g), gate_mode, _ptr(beta), _ptr(state_in),
         _ptr(state_out), _ptr(o), _ptr(cu_seqlens), _ptr(cu_seqlens_host), N, total, H, Hk, D,
-        scale, algo, _ptr(workspace), ws_bytes, st))
+        scale, algo, _ptr(workspace), ws_bytes, st)
 
 
 def kda_scan_varlen(q_hat, k_hat, v_hat, g, beta, state_in, state_out, o, cu_seqlens,
@@ -226,10 +237,10 @@ def kda_scan_varlen(q_hat, k_hat, v_hat, g, beta, state_in, state_out, o, cu_seq
     scale = D ** -0.5 if scale is None else scale
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     st = _stream(stream, state_out)
-    _check("kda_scan_varlen", _lib.kda_scan_varlen(
+    _call("kda_scan_varlen", state_out,
         _ptr(q_hat), _ptr(k_hat), _ptr(v_hat), _ptr(g), gate_mode, _ptr(beta), _ptr(state_in),
         _ptr(state_out), _ptr(o), _ptr(cu_seqlens), _ptr(cu_seqlens_host), N, total, H, D, scale,
-        algo, _ptr(workspace), ws_bytes, st))
+        algo, _ptr(workspace), ws_bytes, st)
 
 
 def kda_scan_varlen_static(q_hat, k_hat, v_hat, g, beta, state_in, state_out, o, cu_seqlens,
@@ -240,23 +251,23 @@ def kda_scan_varlen_static(q_hat, k_hat, v_hat, g, beta, state_in, state_out, o,
     total = int(cu_seqlens_host[-1])
     scale = D ** -0.5 if scale is None else scale
     st = _stream(stream, state_out)
-    _check("kda_scan_varlen_static", _lib.kda_scan_varlen_static(
+    _call("kda_scan_varlen_static", state_out,
         _ptr(q_hat), _ptr(k_hat), _ptr(v_hat), _ptr(g), gate_mode, _ptr(beta), _ptr(state_in),
         _ptr(state_out), _ptr(o), _ptr(cu_seqlens), _ptr(cu_seqlens_host), N, total, H, D, scale,
-        st))
+        st)
 
 
 def kda_gated_rmsnorm_out(o, norm_w, gate_raw, y, *, rows, eps=1e-6, D=HEAD_DIM, stream=None):
     st = _stream(stream, y)
-    _check("kda_gated_rmsnorm_out", _lib.kda_gated_rmsnorm_out(
-        _ptr(o), _ptr(norm_w), _ptr(gate_raw), _ptr(y), rows, D, eps, st))
+    _call("kda_gated_rmsnorm_out", y,
+        _ptr(o), _ptr(norm_w), _ptr(gate_raw), _ptr(y), rows, D, eps, st)
 
 
 def kda_gated_rmsnorm_silu_out(o, norm_w, gate_raw, y, *, rows, eps=1e-6, D=HEAD_DIM,
                                stream=None):
     st = _stream(stream, y)
-    _check("kda_gated_rmsnorm_silu_out", _lib.kda_gated_rmsnorm_silu_out(
-        _ptr(o), _ptr(norm_w), _ptr(gate_raw), _ptr(y), rows, D, eps, st))
+    _call("kda_gated_rmsnorm_silu_out", y,
+        _ptr(o), _ptr(norm_w), _ptr(gate_raw), _ptr(y), rows, D, eps, st)
 
 
 def kda_decode_fused(q_raw, k_raw, v_raw, conv_w, ring_in, ring_out, f_raw, dt_bias, a_log,
@@ -265,11 +276,11 @@ def kda_decode_fused(q_raw, k_raw, v_raw, conv_w, ring_in, ring_out, f_raw, dt_b
                      D=HEAD_DIM, stream=None):
     scale = D ** -0.5 if scale is None else scale
     st = _stream(stream, y)
-    _check("kda_decode_fused", _lib.kda_decode_fused(
+    _call("kda_decode_fused", y,
         _ptr(q_raw), _ptr(k_raw), _ptr(v_raw), _raw_dtype(q_raw), _ptr(conv_w), _ptr(ring_in),
         _ptr(ring_out), _ptr(f_raw), _ptr(dt_bias), _ptr(a_log), gate_mode, gate_lb,
         _ptr(beta_raw), _ptr(state_in), _ptr(state_out), _ptr(norm_w), _ptr(gate_raw), _ptr(y),
-        N, T, H, D, K, l2_eps, scale, rms_eps, st))
+        N, T, H, D, K, l2_eps, scale, rms_eps, st)
 
 
 def kda_verify_rollback(q_raw, k_raw, v_raw, conv_w, ring_in, ring_out, f_raw, dt_bias, a_log,
@@ -279,11 +290,11 @@ def kda_verify_rollback(q_raw, k_raw, v_raw, conv_w, ring_in, ring_out, f_raw, d
     """keep: int32 device tensor [N], tokens accepted per sequence of the T-token verify batch."""
     scale = D ** -0.5 if scale is None else scale
     st = _stream(stream, y)
-    _check("kda_verify_rollback", _lib.kda_verify_rollback(
+    _call("kda_verify_rollback", y,
         _ptr(q_raw), _ptr(k_raw), _ptr(v_raw), _raw_dtype(q_raw), _ptr(conv_w), _ptr(ring_in),
         _ptr(ring_out), _ptr(f_raw), _ptr(dt_bias), _ptr(a_log), gate_mode, gate_lb,
         _ptr(beta_raw), _ptr(state_in), _ptr(state_out), _ptr(norm_w), _ptr(gate_raw), _ptr(y),
-        _ptr(keep), N, T, H, D, K, l2_eps, scale, rms_eps, st))
+        _ptr(keep), N, T, H, D, K, l2_eps, scale, rms_eps, st)
 
 
 def kda_prefill_workspace_bytes(N, total_T, H, gate_mode=0, D=HEAD_DIM) -> int:
@@ -306,11 +317,11 @@ def kda_prefill_fused(q_raw, k_raw, v_raw, conv_w, ring_in, ring_out, f_raw, dt_
                       D=HEAD_DIM, stream=None):
     scale = D ** -0.5 if scale is None else scale
     st = _stream(stream, y)
-    _check("kda_prefill_fused", _lib.kda_prefill_fused(
+    _call("kda_prefill_fused", y,
         _ptr(q_raw), _ptr(k_raw), _ptr(v_raw), _raw_dtype(q_raw), _ptr(conv_w), _ptr(ring_in),
         _ptr(ring_out), _ptr(f_raw), _ptr(dt_bias), _ptr(a_log), gate_mode, gate_lb,
         _ptr(beta_raw), _ptr(state_in), _ptr(state_out), _ptr(norm_w), _ptr(gate_raw), _ptr(y),
-        N, T, H, D, K, l2_eps, scale, rms_eps, _ptr(workspace), _ws_bytes(workspace), st))
+        N, T, H, D, K, l2_eps, scale, rms_eps, _ptr(workspace), _ws_bytes(workspace), st)
 
 
 def kda_prefill_fused_varlen(q_raw, k_raw, v_raw, conv_w, ring_in, ring_out, f_raw, dt_bias,
@@ -322,12 +333,12 @@ def kda_prefill_fused_varlen(q_raw, k_raw, v_raw, conv_w, ring_in, ring_out, f_r
     total = int(cu_seqlens_host[-1])
     scale = D ** -0.5 if scale is None else scale
     st = _stream(stream, y)
-    _check("kda_prefill_fused_varlen", _lib.kda_prefill_fused_varlen(
+    _call("kda_prefill_fused_varlen", y,
         _ptr(q_raw), _ptr(k_raw), _ptr(v_raw), _raw_dtype(q_raw), _ptr(conv_w), _ptr(ring_in),
         _ptr(ring_out), _ptr(f_raw), _ptr(dt_bias), _ptr(a_log), gate_mode, gate_lb,
         _ptr(beta_raw), _ptr(state_in), _ptr(state_out), _ptr(norm_w), _ptr(gate_raw), _ptr(y),
         _ptr(cu_seqlens), _ptr(cu_seqlens_host), N, total, H, D, K, l2_eps, scale, rms_eps,
-        _ptr(workspace), _ws_bytes(workspace), st))
+        _ptr(workspace), _ws_bytes(workspace), st)
 
 
 def kernel_timing(enable: bool) -> bool:

@@ -11,9 +11,17 @@
  *     40000 + n for a contract violation (codes below).  Contract checks run on the host before
  *     anything is launched; a violating call launches nothing and touches no buffer.
  *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).  Every call
- *     is asynchronous on that stream; outputs are ready when the stream reaches the call.
- *   - The caller owns all memory.  The library allocates nothing and keeps no state between calls
- *     except one device-side error word (see kda_device_status) and cached function attributes.
+ *     is asynchronous on that stream; outputs are ready when the stream reaches the call.  The
+ *     stream must belong to the CURRENT device (cudaSetDevice), whose memory the pointers refer
+ *     to: the library keys its per-device lookups by the current device, so a stream of another
+ *     device returns 40012 and launches nothing.
+ *   - The caller owns all memory.  The library allocates no device memory.  It keeps no state
+ *     between calls except one device-side error word (see kda_device_status) and, per device,
+ *     cached symbol addresses and function attributes.  The first call on a device may load the
+ *     library's module there and set function attributes; after that, with kernel timing off,
+ *     calls allocate no host memory either (kernel timing, kda_kernel_timing, creates CUDA events
+ *     and grows host-side lists while it is on).  The per-device caches are filled thread-safely;
+ *     a device that the process resets (cudaDeviceReset) must not be used with the library again.
  *   - Pointers are device pointers unless the name ends in _host.  Pointers marked [16B] must be
  *     16-byte aligned (40010 otherwise).
  *
@@ -53,6 +61,7 @@ extern "C" {
 #define KDA_ERR_ALIGN 40010           /* a [16B] pointer is not 16-byte aligned */
 #define KDA_ERR_SCRATCH_LIMIT 40011   /* kda_scan_varlen_static: problem needs more scratch than
                                          KDA_STATIC_SCRATCH_BYTES */
+#define KDA_ERR_STREAM_DEVICE 40012   /* the stream belongs to a device other than the current one */
 
 /* enums */
 #define KDA_DTYPE_F32 0
@@ -209,8 +218,8 @@ int kda_scan_varlen_gqa(const float* q_hat, const float* k_hat, const float* v_h
 /*
  * kda_scan_varlen_static -- kda_scan_varlen with algo KDA_ALGO_CHUNK, except that the chunked
  * form's scratch is a fixed array of KDA_STATIC_SCRATCH_BYTES (32 MiB) inside the library rather
- * than a caller workspace: the call allocates no device or host memory (no cudaMalloc, no
- * allocating library routine).  The KDA pages have no counterpart to this entry point.  It is for
+ * than a caller workspace: the call allocates no device memory (no cudaMalloc, no allocating
+ * library routine), and after its first call on a device, with kernel timing off, no host memory.  The KDA pages have no counterpart to this entry point.  It is for
  * callers that must not allocate device memory while they run: a serving process that reserves its
  * whole HBM budget at start-up and turns allocation off afterwards (an allocation then fails, or
  * stalls the device in the middle of a step), or plain C code with no allocator at hand.  The
@@ -223,8 +232,9 @@ int kda_scan_varlen_gqa(const float* q_hat, const float* k_hat, const float* v_h
  * H * sum_n ceil(len_n / 32) <= 478 -- must fit KDA_STATIC_SCRATCH_BYTES; a larger problem
  * returns 40011 and launches nothing.
  * Setup: the first call on each device looks up the array's address once, with that device
- * current (a failure returns 10000 + its cudaError_t).  Make that first call before any stream
- * capture begins.
+ * current (a failure returns 10000 + its cudaError_t); the stream must belong to that device
+ * (40012 otherwise), so the kernels never see another device's array.  Make that first call
+ * before any stream capture begins.
  * Zeroing: nothing in the scratch has to start at zero; every byte the call reads it has first
  * written itself, so no clearing happens between calls.
  * Concurrency: the array is one per device and shared by every call on it.  Calls that may run

@@ -34,7 +34,8 @@ def test_every_declared_symbol_is_exported(kda):
 
 def test_status_strings(kda):
     assert kda.abi_version() == 1
-    for code in (0, 40001, 40002, 40003, 40004, 40005, 40006, 40007, 40008, 40009, 40010, 40011):
+    for code in (0, 40001, 40002, 40003, 40004, 40005, 40006, 40007, 40008, 40009, 40010, 40011,
+                 40012):
         assert kda.status_string(code) not in ("unknown status",)
     assert kda.status_string(10000 + 2) == "CUDA error"
 
@@ -149,6 +150,9 @@ def test_static_scan_contract(kda):
         return lib.kda_scan_varlen_static(*a, FAKE, ctypes.cast(arr, ctypes.c_void_p),
                                           len(cu) - 1, cu[-1], H, D, ctypes.c_float(1.0), None)
     assert call([0, 32 * (cap_blocks + 1)], 1) == 40011
+    # exactly the cap (ragged tail) passes the size check; with no device the call then stops
+    # at its first CUDA query, never with the limit's code
+    assert call([0, 32 * cap_blocks - 5], 1) not in (0, 40011)
     assert call([0, 32 * (cap_blocks // 2 + 1) - 5, 32 * (cap_blocks + 2) - 10], 2) == 40011
     assert call([0, 3, 2], 1) == 40006
     assert call([0, 64], 1, D=64) == 40001

@@ -1,7 +1,8 @@
-"""Host checks of the benchmark's bookkeeping (no GPU): the algorithmic bytes behind each
-roofline fraction equal the per-unit figures of the prefill workload worked out by hand (T = 4096
-tokens, H = 64 heads, D = 128, conv K = 4, 128 chunks of 32 tokens, 70,144-byte workspace
-blocks), and every kernel the benchmark reports has its source list on disk."""
+"""Host checks of the benchmark's bookkeeping (no GPU): the method bytes behind each roofline
+fraction equal the per-unit figures of the prefill workload worked out by hand (T = 4096 tokens,
+H = 64 heads, D = 128, conv K = 4), the library's intermediate traffic (128 chunks of 32 tokens,
+70,144-byte workspace blocks) is counted apart from them, and every kernel the benchmark reports
+has its source list on disk."""
 
 import importlib.util
 import os
@@ -21,18 +22,45 @@ def bench():
     return mod
 
 
-def test_prefill_kernel_bytes(bench):
-    kb = bench._kernel_bytes(4096, 64, 70144, 128)
+def test_prefill_method_bytes(bench):
+    """The method's own I/O per prefill step, attributed to the fused kernels, adds up to the
+    step's inputs read once and outputs written once; no workspace byte is counted in it."""
+    mb = bench._method_bytes(4096, 64)
     MB = 1 << 20
     raw = 3 * 4096 * 8192 * 2               # 192 MiB of bf16 q, k, v
-    plane = 4096 * 8192 * 4                 # 128 MiB per f32 [T, C] plane
-    blocks = 128 * 64 * 70144               # the workspace: one block per (chunk, head)
-    assert raw == 192 * MB and plane == 128 * MB and blocks == 574_619_648
-    small = 4096 * 64 * 4 + 3 * 8192 * 4 * 4 + 3 * 8192 * 3 * 4   # beta in, conv weights, ring in
-    assert kb["kda_chunk_prep_intra_kernel"] == raw + plane + small + blocks == 911_900_672
-    ring = 3 * 8192 * 3 * (2 + 4 + 4)       # raw tail rows in, ring in, ring out
-    assert kb["kda_chunk_inter_kernel"] == blocks + 2 * 64 * 128 * 128 * 4 + plane + ring
-    assert kb["kda_gated_rmsnorm_kernel"] == 3 * plane + 128 * 4        # o, z in; y out; weight
+    plane = 4096 * 8192 * 4                 # 128 MiB per f32 [T, C] plane (f, z, y)
+    assert raw == 192 * MB and plane == 128 * MB
+    beta = 4096 * 64 * 4
+    conv = 3 * 8192 * 4 * 4
+    ring = 3 * 8192 * 3 * 4                 # one direction
+    state = 64 * 128 * 128 * 4              # one direction
+    params = 8192 * 4 + 64 * 4 + 128 * 4    # dt_bias, A_log, norm weight
+    assert mb["kda_chunk_prep_intra_kernel"] == raw + plane + beta + conv + ring + 8192 * 4 + 64 * 4
+    assert mb["kda_chunk_inter_kernel"] == 2 * state + ring
+    assert mb["kda_gated_rmsnorm_kernel"] == 2 * plane + 128 * 4
+    step = sum(mb[k] for k in ("kda_chunk_prep_intra_kernel", "kda_chunk_inter_kernel",
+                               "kda_gated_rmsnorm_kernel"))
+    assert step == raw + 3 * plane + beta + conv + 2 * ring + 2 * state + params == 614_433_536
+
+
+def test_prefill_impl_bytes(bench):
+    """The library's own intermediates, reported apart: the chunk workspace (one 70,144-byte
+    block per (32-token chunk, head)) and the readout plane o."""
+    ib = bench._impl_bytes(4096, 64, 70144, 128)
+    blocks = 128 * 64 * 70144
+    plane = 4096 * 8192 * 4
+    assert blocks == 574_619_648
+    assert ib["kda_chunk_prep_intra_kernel"] == blocks
+    assert ib["kda_chunk_inter_kernel"] == blocks + plane
+    assert ib["kda_gated_rmsnorm_kernel"] == plane
+
+
+def test_chunk_flops(bench):
+    """The chunked form's tensor-core products per (32-token chunk, head), one pass each."""
+    f = bench._chunk_flops(4096, 64)
+    per = 128 * 64
+    assert f["kda_chunk_prep_intra_kernel"] == per * (2 * 64 * 128 * 32 + 2 * 32 * 32 * 256)
+    assert f["kda_chunk_inter_kernel"] == per * (2 * 128 * 128 * 64 + 2 * 128 * 32 * 160)
 
 
 def test_kernel_sources_exist(bench):

@@ -11,7 +11,7 @@ import pytest
 import torch
 
 from gated_delta_rule_scan_gb300 import inputs
-from tests.gpu_util import TOL, gpu_forward, gpu_heads, gpu_prefill, oracle_forward, rel_linf
+from tests.gpu_util import TOL, check_all_heads, gpu_forward, gpu_prefill, rel_linf
 
 pytestmark = pytest.mark.gpu
 
@@ -26,17 +26,9 @@ def _lib():
     assert kda.kda_device_status() == 0
 
 
-def _check(fused, inp, varlen=None, heads=None):
-    if heads is None:
-        ref = oracle_forward(inp)
-        got = fused
-    else:
-        ref = oracle_forward(inp, heads=heads)
-        got = gpu_heads(fused, inp, heads)
-    errs = {k: rel_linf(got[k], ref[k]) for k in ("y", "state_out")}
-    assert max(errs.values()) <= TOL, errs
-    if got.get("ring_out") is not None:
-        assert np.array_equal(got["ring_out"].cpu().double().numpy(), ref["ring_out"])
+def _check(fused, inp, varlen=None):
+    keys = ("y", "state_out") + (("ring_out",) if fused.get("ring_out") is not None else ())
+    check_all_heads(fused, inp, keys)
     unf = gpu_forward(inp, varlen=varlen, algo=2)
     assert torch.equal(fused["state_out"], unf["state_out"])
     if fused.get("ring_out") is not None:
@@ -94,16 +86,51 @@ def test_prefill_fused_variants(raw, gate_mode, conv, K):
 
 @pytest.mark.slow
 def test_prefill_fused_full_size():
-    """T=4096, H=64 (the prefill benchmark workload), sampled heads against the oracle."""
+    """T=4096, H=64 (the prefill benchmark workload), every head against the oracle."""
     inp = inputs.prefill()
-    _check(gpu_prefill(inp), inp, heads=list(range(0, 64, 8)))
+    _check(gpu_prefill(inp), inp)
+
+
+def _split_rows(inp, first):
+    """The workload cut at each sequence's split point: the first parts (first=True) or the rest,
+    as packed inputs of their own, and the rows of the original they came from."""
+    import copy
+    cu, P = inp.cu_seqlens, inp.split_points
+    parts = [np.arange(cu[n], cu[n] + P[n]) if first else np.arange(cu[n] + P[n], cu[n + 1])
+             for n in range(inp.N)]
+    sel = torch.from_numpy(np.concatenate(parts))
+    sub = copy.copy(inp)
+    for k in ("q_raw", "k_raw", "v_raw", "f_raw", "beta_raw", "gate_raw"):
+        setattr(sub, k, getattr(inp, k)[sel])
+    sub.cu_seqlens = np.concatenate([[0], np.cumsum([len(p) for p in parts])])
+    return sub, sel
 
 
 @pytest.mark.slow
-def test_prefill_fused_varlen_full_size():
-    """16 sequences with lengths U[256, 8192] at H=64, sampled heads against the oracle."""
+def test_prefill_varlen_full_size_split_resume():
+    """The packed varlen workload at its stated size (16 sequences, lengths U[256, 8192], H=64,
+    random states and rings): the fused prefill against the oracle on every head and bit-equal to
+    the staged chunked path; then each sequence cut at its seeded split point, the prefix run,
+    and the suffix resumed from the saved (state, ring) -- through the fused prefill and through
+    the staged chunked path -- matches the unsplit run within the tolerance, the ring bit for
+    bit."""
     inp = inputs.varlen_prefill()
-    _check(gpu_prefill(inp, varlen=True), inp, varlen=True, heads=[0, 21, 42, 63])
+    full = gpu_prefill(inp, varlen=True)
+    _check(full, inp, varlen=True)
+    a, sel_a = _split_rows(inp, True)
+    b, sel_b = _split_rows(inp, False)
+    for run in (lambda x: gpu_prefill(x, varlen=True), lambda x: gpu_forward(x, varlen=True, algo=2)):
+        out_a = run(a)
+        b.state_in = out_a["state_out"].cpu()
+        b.ring_in = out_a["ring_out"].cpu()
+        out_b = run(b)
+        y = torch.empty_like(full["y"])
+        y[sel_a.cuda()] = out_a["y"]
+        y[sel_b.cuda()] = out_b["y"]
+        assert rel_linf(y, full["y"]) <= TOL
+        assert rel_linf(out_b["state_out"], full["state_out"]) <= TOL
+        assert torch.equal(out_b["ring_out"], full["ring_out"])
+        del out_a, out_b, y
 
 
 def test_prefill_fused_contract():

@@ -91,3 +91,22 @@ def test_static_scratch_limit():
         _static(c)
     assert err.value.status == 40011
     assert torch.isnan(c["o_static"]).all()          # nothing launched
+
+
+def test_static_scratch_exactly_at_limit():
+    """A problem that needs exactly the largest number of (32-token chunk, head) blocks the fixed
+    array holds -- one head, one sequence whose last chunk is ragged -- is accepted and equals the
+    workspace path bit for bit (an off-by-one in the size check, or a write past the array's end,
+    would show here)."""
+    dev = torch.device("cuda:0")
+    cap_blocks = (kda.STATIC_SCRATCH_BYTES - 256) // 70144
+    c = _case(24, [32 * cap_blocks - 5], 1, kda.GATE_PER_CHANNEL, dev)
+    _static(c)
+    kda.kda_scan_varlen(c["q"], c["k"], c["v"], c["g"], c["beta"], c["s0"], c["s_ws"], c["o_ws"],
+                        c["cu"], c["cu_host"], H=1, gate_mode=kda.GATE_PER_CHANNEL,
+                        algo=kda.ALGO_CHUNK, workspace=c["ws"])
+    torch.cuda.synchronize()
+    assert kda.kda_device_status() == 0
+    assert torch.isfinite(c["o_static"]).all()
+    assert torch.equal(c["o_static"], c["o_ws"])
+    assert torch.equal(c["s_static"], c["s_ws"])
