@@ -309,3 +309,29 @@ void orc_gated_rmsnorm(const double* o, const double* w, const double* z, double
         }
     }
 }
+
+/* ------------------------------------------------------------------------------------------ */
+/* stage 1: the projections that read the layer input x                                        */
+/* ------------------------------------------------------------------------------------------ */
+
+/*
+ * One projection of t token rows: out[s][r] = sum_{k=0}^{in_f-1} w[r][k] * x[s][k], the terms
+ * added k ascending from 0, in f64.  w is [rows][in_f] (the layer's `[out, hidden]` weight
+ * layout), x is [t][in_f], out is [t][rows].
+ * [KDA] `kda_core_gated` stage 1: the six projections q, k, v, forget-down, gate-down and beta
+ * each read x this way (`KdaAttnLayer` field docs give the shapes: wq/wk/wv [qkv, hidden],
+ * f_a/g_a [head_dim, hidden], b_proj [heads, hidden]); `Engine::kda_proj_fused6` computes the six
+ * in one launch with the same result per row.
+ */
+void orc_matvec_rows(const double* w, const double* x, double* out, long rows, long in_f, int t) {
+    for (int s = 0; s < t; ++s) {
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static)
+#endif
+        for (long r = 0; r < rows; ++r) {
+            double acc = 0.0;
+            for (long k = 0; k < in_f; ++k) acc += w[r * in_f + k] * x[(long)s * in_f + k];
+            out[(long)s * rows + r] = acc;
+        }
+    }
+}

@@ -68,8 +68,10 @@ def _bind(path: str):
     for fn in (lib.orc_scan_kda, lib.orc_scan_gdn):
         fn.argtypes = [dp, dp, dp, dp, dp, lp, I, I, I, dp, dp, dp, D]
     lib.orc_gated_rmsnorm.argtypes = [dp, dp, dp, dp, L, I, D, I]
+    lib.orc_matvec_rows.argtypes = [dp, dp, dp, L, L, I]
     for name in ("orc_conv_silu", "orc_l2norm", "orc_gate_kda", "orc_gate_gdn",
-                 "orc_sigmoid", "orc_scan_kda", "orc_scan_gdn", "orc_gated_rmsnorm"):
+                 "orc_sigmoid", "orc_scan_kda", "orc_scan_gdn", "orc_gated_rmsnorm",
+                 "orc_matvec_rows"):
         getattr(lib, name).restype = None
     return lib
 
@@ -209,6 +211,25 @@ def gated_rmsnorm(o, w, z, eps: float = 1e-6, gate: str = "sigmoid"):
     _load().orc_gated_rmsnorm(_p(o), _p(w), _p(z), _p(y), o.size // D, D, eps,
                               1 if gate == "silu" else 0)
     return y
+
+
+def matvec_rows(w, x):
+    """One projection of token rows: out[s][r] = sum_k w[r][k] x[s][k] (terms k ascending, f64).
+    w: [rows, in_f] (bf16 weights are upcast exactly), x: [t, in_f].  Returns [t, rows]."""
+    w, x = _f64(w), _f64(x)
+    rows, in_f = w.shape
+    x = x.reshape(-1, in_f)
+    t = x.shape[0]
+    out = np.empty((t, rows))
+    if t and rows:
+        _load().orc_matvec_rows(_p(w), _p(x), _p(out), rows, in_f, t)
+    return out
+
+
+def proj6(x, w_q, w_k, w_v, w_fa, w_ga, w_b):
+    """Stage 1 of the mixer: the six projections of the layer input x [t, hidden], in the pages'
+    output order [q, k, v, forget_down, gate_down, beta_raw]."""
+    return [matvec_rows(w, x) for w in (w_q, w_k, w_v, w_fa, w_ga, w_b)]
 
 
 # ------------------------------------------------------------------------------------------

@@ -56,6 +56,11 @@ MUTATIONS = [
      "(silu_gate ? silu(zi) : silu(zi))"),
     ("rmsnorm_silu_gate_is_sigmoid", "(silu_gate ? silu(zi) : sigmoid(zi))",
      "(silu_gate ? sigmoid(zi) : sigmoid(zi))"),
+    ("matvec_last_term_dropped", "for (long k = 0; k < in_f; ++k) acc += w[r * in_f + k]",
+     "for (long k = 0; k + 1 < in_f; ++k) acc += w[r * in_f + k]"),
+    ("matvec_first_token_only", "* x[(long)s * in_f + k];", "* x[k];"),
+    ("matvec_weight_column_shifted", "acc += w[r * in_f + k] * x",
+     "acc += w[r * in_f + (k + 1) % in_f] * x"),
 ]
 
 

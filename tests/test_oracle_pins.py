@@ -15,6 +15,8 @@ Which pin covers which oracle routine:
   gated_rmsnorm_silu   the SiLU-gated mode at hand values (sigmoid(ln 3) = 3/4) and z -> +inf.
   forward         split-at-every-point state carry (bit-equal); T-token call equals T chained
                   one-token calls (bit-equal).
+  matvec_rows     one-hot weight rows select inputs exactly; small-integer case equals exact
+  (proj6)         integer dot products; a band matrix's closed form; the six outputs' order.
 Every check is a plain function so test_oracle_mutations.py can run it against mutated oracle
 builds and show that each planted mistake is caught.
 """
@@ -404,6 +406,63 @@ def check_varlen_equals_separate_calls():
     np.testing.assert_array_equal(packed["ring_out"][1], cat["ring_in"][1])
 
 
+# ------------------------------------------------------------------------------------------
+# stage 1: the projections that read x
+# ------------------------------------------------------------------------------------------
+
+def check_matvec_one_hot_rows():
+    """Weight rows that are one-hot pick one input entry each: out[s][r] = x[s][p(r)] exactly."""
+    rng = _rng(40)
+    rows, in_f, t = 7, 19, 3
+    p = rng.permutation(in_f)[:rows]
+    w = np.zeros((rows, in_f))
+    w[np.arange(rows), p] = 1.0
+    x = rng.standard_normal((t, in_f))
+    np.testing.assert_array_equal(orc.matvec_rows(w, x), x[:, p])
+
+
+def check_matvec_exact_integers():
+    """Small integer weights and inputs: every partial sum is an exact integer in f64, so the
+    result equals the exact integer dot products computed here with Python ints, row by row and
+    token by token (a non-square shape, so a transposed operand or a swapped stride cannot
+    pass)."""
+    rng = _rng(41)
+    rows, in_f, t = 5, 11, 4
+    w = rng.integers(-9, 10, size=(rows, in_f))
+    x = rng.integers(-9, 10, size=(t, in_f))
+    want = np.array([[sum(int(w[r, k]) * int(x[s, k]) for k in range(in_f)) for r in range(rows)]
+                     for s in range(t)], dtype=float)
+    np.testing.assert_array_equal(orc.matvec_rows(w.astype(float), x.astype(float)), want)
+
+
+def check_matvec_band():
+    """w[r][r] = r + 1 and w[r][r+1] = 2 (a band): out[s][r] = (r+1) x[s][r] + 2 x[s][r+1]."""
+    rng = _rng(42)
+    rows, in_f, t = 6, 9, 2
+    w = np.zeros((rows, in_f))
+    for r in range(rows):
+        w[r, r] = r + 1.0
+        w[r, r + 1] = 2.0
+    x = rng.standard_normal((t, in_f))
+    want = np.stack([(np.arange(rows) + 1.0) * x[s, :rows] + 2.0 * x[s, 1:rows + 1]
+                     for s in range(t)])
+    np.testing.assert_allclose(orc.matvec_rows(w, x), want, rtol=0, atol=1e-14)
+
+
+def check_proj6_order_and_shapes():
+    """The six projections come back in the pages' order [q, k, v, forget-down, gate-down,
+    beta] with shapes [t, rows of each weight]; each weight tagged by a distinct constant row
+    sum shows which output it produced."""
+    t, in_f = 2, 8
+    dims = (6, 6, 6, 3, 3, 2)
+    ws = [np.full((d, in_f), float(i + 1)) for i, d in enumerate(dims)]
+    x = np.ones((t, in_f))
+    outs = orc.proj6(x, *ws)
+    assert [o.shape for o in outs] == [(t, d) for d in dims]
+    for i, o in enumerate(outs):
+        np.testing.assert_array_equal(o, np.full_like(o, (i + 1) * in_f))
+
+
 ALL_CHECKS = [
     check_three_token_golden, check_three_token_embedded, check_beta_zero_closed_form,
     check_orthonormal_recall, check_dense_product_form, check_chunked_form_every_chunk_size,
@@ -411,7 +470,8 @@ ALL_CHECKS = [
     check_conv_taps_general, check_l2norm, check_gates, check_gated_rmsnorm,
     check_gated_rmsnorm_silu,
     check_split_state_carry, check_chained_single_tokens_equal_multi_token,
-    check_varlen_equals_separate_calls,
+    check_varlen_equals_separate_calls, check_matvec_one_hot_rows, check_matvec_exact_integers,
+    check_matvec_band, check_proj6_order_and_shapes,
 ]
 
 
