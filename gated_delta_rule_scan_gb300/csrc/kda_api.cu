@@ -37,12 +37,18 @@ inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? KDA_OK : KDA_E
 // The kernels run on the stream's device, while the per-device lookups (the error word, the fixed
 // scratch, function attributes) follow the current device: a stream of another device is a
 // contract violation (40012).  The legacy and per-thread default streams always belong to the
-// current device.  Only host-side queries; nothing is launched.
+// current device.  Only host-side queries; nothing is launched.  The runtime refuses the stream's
+// device query while the stream is being captured into a graph (error 900), so a capturing stream
+// is not checked: the caller then answers for the match itself.
 int check_stream_device(void* stream) {
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (s == nullptr || s == cudaStreamLegacy || s == cudaStreamPerThread) return KDA_OK;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(s, &cs);
+    if (e != cudaSuccess) return cuda_status(e);
+    if (cs != cudaStreamCaptureStatusNone) return KDA_OK;
     int sdev = -1, cur = -1;
-    cudaError_t e = cudaStreamGetDevice(s, &sdev);
+    e = cudaStreamGetDevice(s, &sdev);
     if (e != cudaSuccess) return cuda_status(e);
     e = cudaGetDevice(&cur);
     if (e != cudaSuccess) return cuda_status(e);

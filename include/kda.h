@@ -14,7 +14,9 @@
  *     is asynchronous on that stream; outputs are ready when the stream reaches the call.  The
  *     stream must belong to the CURRENT device (cudaSetDevice), whose memory the pointers refer
  *     to: the library keys its per-device lookups by the current device, so a stream of another
- *     device returns 40012 and launches nothing.
+ *     device returns 40012 and launches nothing.  (While a stream is being captured into a CUDA
+ *     graph the runtime refuses that query, and the call cannot check: the caller must keep the
+ *     capturing stream's device current.)
  *   - The caller owns all memory.  The library allocates no device memory.  It keeps no state
  *     between calls except one device-side error word (see kda_device_status) and, per device,
  *     cached symbol addresses and function attributes.  The first call on a device may load the
