@@ -39,6 +39,8 @@ D = 128
 PREFILL_T, PREFILL_H = 4096, 64
 RB_T = 4                         # verify width of the rollback workload
 VER_T = 4                        # tokens per sequence of the verify leg
+PROJ_HIDDEN = 6144               # layer width of the projection leg (synthetic weights; the pages
+                                 # do not state it, 6144 is a multiple of 128 as they require)
 DEC_N, DEC_H = 64, 64
 FLOP_PER_TOKEN_HEAD = 7 * D * D   # decay D^2 + S^T k 2D^2 + rank-1 update 2D^2 + S^T q 2D^2
 FP32_LANES, SM_MAX_MHZ = 128, 2070.0
@@ -197,6 +199,7 @@ KERNEL_SOURCES = {
                                 "kda_internal.h"],
     "kda_scan_seq_kernel": ["kda_scan_seq.cu", "kda_scan_core.cuh", "kda_device.cuh",
                             "kda_internal.h"],
+    "kda_proj6_kernel": ["kda_proj.cu", "kda_tc.cuh", "kda_device.cuh", "kda_internal.h"],
 }
 
 
@@ -597,6 +600,38 @@ def run_ours(args):
                 + kept * (3 * C1 * 2 + C1 * 4 * 3 + DEC_H * 4) + 3 * C1 * 4 * 4 + C1 * 4 + D * 4)
     assert kda.kda_device_status() == 0
 
+    # ---------------- stage 1: the six projections of the decode batch's layer input ----------
+    import numpy as np_
+    prng = np_.random.default_rng(7)
+    pdims = (DEC_H * D, DEC_H * D, DEC_H * D, D, D, DEC_H)
+    pw = [torch.from_numpy((prng.standard_normal((r, PROJ_HIDDEN), dtype=np_.float32)
+                            / np_.float32(np_.sqrt(PROJ_HIDDEN)))).to(torch.bfloat16).to(dev)
+          for r in pdims]
+    px = torch.from_numpy(prng.standard_normal((DEC_N, PROJ_HIDDEN), dtype=np_.float32)).to(dev)
+    pouts = [torch.empty(DEC_N, r, device=dev) for r in pdims]
+    pws = kda.proj6_workspace(DEC_N, PROJ_HIDDEN, dev)
+
+    def proj_step():
+        kda.kda_proj6(px, *pw, *pouts, pws, H=DEC_H)
+
+    for _ in range(max(args.warmup, 3)):
+        proj_step()
+    barrier()
+    kda.kernel_timing(True)
+    p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    p0.record(stream)
+    for _ in range(Kd):
+        proj_step()
+    p1.record(stream)
+    barrier()
+    proj_kt = kda.kernel_times()
+    kda.kernel_timing(False)
+    proj_ms = max_over_ranks(p0.elapsed_time(p1)) / Kd
+    proj_w_bytes = sum(r * PROJ_HIDDEN * 2 for r in pdims)
+    proj_bytes = proj_w_bytes + DEC_N * PROJ_HIDDEN * 4 + DEC_N * sum(pdims) * 4
+    assert kda.kda_device_status() == 0
+    del pw, px, pouts, pws
+
     rep.close()
     if rank != 0:
         return None
@@ -719,6 +754,21 @@ def run_ours(args):
                                   "peak": peaks["hbm_gbs"], "unit": "GB/s",
                                   "frac": rb_bytes / (rb_ms / 1e3) / 1e9 / peaks["hbm_gbs"],
                                   "bytes_per_launch": rb_bytes}},
+        "proj6": {"workload": f"the six projections of a {DEC_N}-row decode batch: hidden "
+                              f"{PROJ_HIDDEN} -> q, k, v ({DEC_H * D} each), forget/gate down "
+                              f"({D} each), beta ({DEC_H}); bf16 weights, f32 x and outputs; "
+                              "kda_proj6 (x split + one tcgen05 launch)",
+                  "ms_per_step": proj_ms,
+                  "kernels": {k: {"launches": v[0], "ms_per_launch": v[1] / v[0]}
+                              for k, v in proj_kt.items()},
+                  "roofline": {"bound": "hbm", "kernel": "kda_proj6_kernel + kda_proj_split_kernel",
+                               "achieved": proj_bytes / (proj_ms / 1e3) / 1e9,
+                               "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                               "frac": proj_bytes / (proj_ms / 1e3) / 1e9 / peaks["hbm_gbs"],
+                               "bytes_per_launch": proj_bytes,
+                               "weight_bytes": proj_w_bytes,
+                               "bytes": "bf16 weights read once, x read and the six outputs "
+                                        "written once (the x hi/lo images are intermediates)"}},
         "clocks": clocks,
         "cpu_baseline": cpu,
     }

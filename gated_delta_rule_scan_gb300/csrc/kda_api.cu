@@ -543,6 +543,46 @@ int kda_device_status(void* stream) {
     return KDA_OK;
 }
 
+size_t kda_proj6_workspace_bytes(int t, int in_f) {
+    if (t < 1 || t > kProjMaxT || in_f <= 0 || in_f % kProjKAlign != 0) return 0;
+    return proj_workspace_bytes(t, in_f);
+}
+
+int kda_proj6(const float* x, int t, int in_f, const void* w_q, const void* w_k, const void* w_v,
+              const void* w_fa, const void* w_ga, const void* w_b, float* q_raw, float* k_raw,
+              float* v_raw, float* f_down, float* g_down, float* beta_raw, int H, int D,
+              void* workspace, size_t workspace_bytes, void* stream) {
+    if (D != kHeadDim) return KDA_ERR_HEAD_DIM;
+    if (t < 1 || t > kProjMaxT || H <= 0 || H > kMaxGridY || in_f <= 0 ||
+        in_f % kProjKAlign != 0)
+        return KDA_ERR_SHAPE;
+    const void* w[6] = {w_q, w_k, w_v, w_fa, w_ga, w_b};
+    float* out[6] = {q_raw, k_raw, v_raw, f_down, g_down, beta_raw};
+    if (!x) return KDA_ERR_NULL;
+    for (int i = 0; i < 6; ++i)
+        if (!w[i] || !out[i]) return KDA_ERR_NULL;
+    if (!aligned16(x)) return KDA_ERR_ALIGN;
+    for (int i = 0; i < 6; ++i)
+        if (!aligned16(w[i])) return KDA_ERR_ALIGN;
+    if (workspace == nullptr || workspace_bytes < proj_workspace_bytes(t, in_f))
+        return KDA_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return KDA_ERR_ALIGN;
+    if (const int sd = check_stream_device(stream)) return sd;
+    Proj6Args a{};
+    a.x = x;
+    const int rows[6] = {H * kHeadDim, H * kHeadDim, H * kHeadDim, kHeadDim, kHeadDim, H};
+    for (int i = 0; i < 6; ++i) {
+        a.w[i] = w[i];
+        a.out[i] = out[i];
+        a.rows[i] = rows[i];
+    }
+    a.t = t;
+    a.in_f = in_f;
+    a.ws = workspace;
+    a.err = dev_err_ptr();
+    return cuda_status(launch_proj6(a, static_cast<cudaStream_t>(stream)));
+}
+
 int kda_scan_varlen_static(const float* q_hat, const float* k_hat, const float* v_hat,
                            const float* g, int gate_mode, const float* beta,
                            const float* state_in, float* state_out, float* o,

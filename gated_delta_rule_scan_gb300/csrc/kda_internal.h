@@ -113,6 +113,27 @@ bool make_tensor_map_2d_any(CUtensorMap* m, const void* base, bool bf16, long ro
 // The U rows of the chunked scan's workspace blocks: f32 [nblocks][32 tokens][128 values] at
 // `base` (the first block's U region), block stride block_bytes; box [1][32][32], 128-byte swizzle.
 bool make_tensor_map_blocks_ut(CUtensorMap* m, void* base, long nblocks, size_t block_bytes);
+// The layer input's six projections (kda_proj.cu).  Weights are bf16 [rows_i, in_f]; outputs f32
+// [t, rows_i]; x f32 [t, in_f]; ws holds x split into bf16 hi / lo images of t_pad rows.
+struct Proj6Args {
+    const float* x;
+    const void* w[6];
+    float* out[6];
+    int rows[6];
+    int t; int in_f;
+    void* ws;
+    int* err;
+};
+constexpr int kProjMaxT = 256;          // token rows per call: the MMA's N
+constexpr int kProjKAlign = 128;        // in_f must be a multiple of this
+inline int proj_t_pad(int t) { return (t + 15) / 16 * 16; }
+inline size_t proj_workspace_bytes(int t, int in_f) {
+    return 2 * (size_t)proj_t_pad(t) * (size_t)in_f * 2;   // x hi and x lo, bf16
+}
+cudaError_t launch_proj6(const Proj6Args& a, cudaStream_t s);
+// 2-D bf16 tensor map over [rows, cols] with a [box_rows][64] box in the 128-byte swizzle
+bool make_tensor_map_2d_bf16_sw128(CUtensorMap* m, const void* base, long rows, long cols,
+                                   int box_rows);
 cudaError_t launch_gated_rmsnorm(const NormArgs& a, cudaStream_t s);
 cudaError_t launch_decode_fused(const DecodeArgs& a, cudaStream_t s);
 
@@ -122,7 +143,7 @@ constexpr int kDecodeMaxT = 16;   // tokens one fused decode/verify call may car
 // CUDA event before and after it on the launch stream while timing is enabled.
 enum KernelId {
     kKPrep, kKRingRoll, kKScanSeq, kKChunkOffsets, kKChunkIntra, kKChunkInter, kKRmsNorm,
-    kKDecode, kKPrepIntra, kKernelCount
+    kKDecode, kKPrepIntra, kKProjSplit, kKProj6, kKernelCount
 };
 class KernelTimer {
 public:

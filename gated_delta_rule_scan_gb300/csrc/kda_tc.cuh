@@ -64,6 +64,22 @@ __device__ __forceinline__ uint64_t tc_smem_desc(uint32_t smem_addr, uint32_t lb
     return d;
 }
 
+// Shared-memory matrix descriptor of a K-major bf16 tile written by a TMA load in the 128-byte
+// swizzle: rows of 128 bytes (64 elements), 8-row groups 1024 bytes apart (SBO), the leading
+// offset unused (K of one MMA, 16 elements = 32 bytes, stays inside a swizzle row), swizzle mode 2
+// (128-byte) in bits 61..63.  The tile must start 1024-byte aligned; the K-step ks of 16 elements
+// starts 32 * ks bytes further (the hardware applies the swizzle to the computed address, as the
+// TMA did when it wrote the tile).
+__device__ __forceinline__ uint64_t tc_smem_desc_sw128(uint32_t smem_addr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((smem_addr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)1 << 16;                 // leading byte offset: 16 B (ignored here)
+    d |= (uint64_t)(1024 >> 4) << 32;       // stride byte offset: 1024 B
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;                 // 128-byte swizzle
+    return d;
+}
+
 // Instruction descriptor, kind::f16: bf16 A and B, f32 accumulator, both K-major, dense.
 __host__ __device__ constexpr uint32_t tc_idesc_bf16(int M, int N) {
     return (1u << 4)                    // D format: f32

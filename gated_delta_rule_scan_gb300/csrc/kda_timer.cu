@@ -45,7 +45,8 @@ cudaEvent_t take_event(int dev) {
 const char* const kNames[kKernelCount] = {
     "kda_prep_kernel",        "kda_ring_roll_kernel",   "kda_scan_seq_kernel",
     "kda_chunk_offsets_kernel", "kda_chunk_intra_kernel", "kda_chunk_inter_kernel",
-    "kda_gated_rmsnorm_kernel", "kda_decode_fused_kernel", "kda_chunk_prep_intra_kernel"};
+    "kda_gated_rmsnorm_kernel", "kda_decode_fused_kernel", "kda_chunk_prep_intra_kernel",
+    "kda_proj_split_kernel",  "kda_proj6_kernel"};
 
 }  // namespace
 

@@ -87,6 +87,11 @@ _lib.kda_scan_gqa.argtypes = [_P, _P, _P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I
 _lib.kda_scan_varlen_gqa.restype = _I
 _lib.kda_scan_varlen_gqa.argtypes = [_P, _P, _P, _P, _I, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I,
                                      _I, _F, _I, _P, _Z, _P]
+_lib.kda_proj6_workspace_bytes.restype = _Z
+_lib.kda_proj6_workspace_bytes.argtypes = [_I, _I]
+_lib.kda_proj6.restype = _I
+_lib.kda_proj6.argtypes = [_P, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _P,
+                           _Z, _P]
 _lib.kda_selftest_wait_timeout.restype = _I
 _lib.kda_selftest_wait_timeout.argtypes = [_P]
 
@@ -97,7 +102,8 @@ EXPORTED = ("kda_abi_version", "kda_status_string", "kda_conv_l2norm_prep",
             "kda_scan_varlen_static", "kda_prefill_workspace_bytes", "kda_prefill_fused",
             "kda_prefill_fused_varlen", "kda_kernel_timing", "kda_kernel_times",
             "kda_kernel_name", "kda_verify_rollback", "kda_gated_rmsnorm_silu_out",
-            "kda_selftest_wait_timeout", "kda_scan_gqa", "kda_scan_varlen_gqa")
+            "kda_selftest_wait_timeout", "kda_scan_gqa", "kda_scan_varlen_gqa",
+            "kda_proj6_workspace_bytes", "kda_proj6")
 
 
 class KdaError(RuntimeError):
@@ -339,6 +345,30 @@ def kda_prefill_fused_varlen(q_raw, k_raw, v_raw, conv_w, ring_in, ring_out, f_r
         _ptr(beta_raw), _ptr(state_in), _ptr(state_out), _ptr(norm_w), _ptr(gate_raw), _ptr(y),
         _ptr(cu_seqlens), _ptr(cu_seqlens_host), N, total, H, D, K, l2_eps, scale, rms_eps,
         _ptr(workspace), _ws_bytes(workspace), st)
+
+
+PROJ_MAX_T = 256
+
+
+def kda_proj6_workspace_bytes(t, in_f) -> int:
+    return int(_lib.kda_proj6_workspace_bytes(t, in_f))
+
+
+def proj6_workspace(t, in_f, device):
+    """A device byte buffer large enough for kda_proj6 over t token rows of width in_f."""
+    return torch.empty(max(kda_proj6_workspace_bytes(t, in_f), 16), dtype=torch.uint8,
+                       device=device)
+
+
+def kda_proj6(x, w_q, w_k, w_v, w_fa, w_ga, w_b, q_raw, k_raw, v_raw, f_down, g_down, beta_raw,
+              workspace, *, H, D=HEAD_DIM, stream=None):
+    """The six projections of x [t, in_f] (f32) by bf16 weights into f32 outputs."""
+    t, in_f = x.shape
+    st = _stream(stream, q_raw)
+    _call("kda_proj6", q_raw,
+          _ptr(x), t, in_f, _ptr(w_q), _ptr(w_k), _ptr(w_v), _ptr(w_fa), _ptr(w_ga), _ptr(w_b),
+          _ptr(q_raw), _ptr(k_raw), _ptr(v_raw), _ptr(f_down), _ptr(g_down), _ptr(beta_raw), H, D,
+          _ptr(workspace), _ws_bytes(workspace), st)
 
 
 def kernel_timing(enable: bool) -> bool:

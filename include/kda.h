@@ -375,6 +375,34 @@ int kda_verify_rollback(const void* q_raw, const void* k_raw, const void* v_raw,
                         int D, int K, float l2_eps, float scale, float rms_eps, void* stream);
 
 /*
+ * kda_proj6 -- stage 1 of kda_core_gated: the six projections of the layer input that the mixer
+ * reads, in one call (Engine::kda_proj_fused6, its bf16-weight arm; the shapes are the
+ * KdaAttnLayer field docs of "memra_engine/kda.rs"): for every token row s < t,
+ *     out[s][r] = sum_{k < in_f} W[r][k] * x[s][k]
+ * for W = w_q, w_k, w_v [H*D, in_f] -> q_raw, k_raw, v_raw [t, H*D]; W = w_fa, w_ga [D, in_f] ->
+ * f_down, g_down [t, D] (the forget and output gates' down-projections, which the layer's own
+ * low-rank up-projections widen to [t, H*D]); W = w_b [H, in_f] -> beta_raw [t, H].  The outputs
+ * are what kda_decode_fused / kda_prefill_fused take as q_raw, k_raw, v_raw (raw_dtype f32) and
+ * beta_raw.
+ *
+ * x            [t, in_f] f32 [16B], t = 1..256 token rows (a decode or verify batch), in_f a
+ *              multiple of 128 (40005 otherwise).
+ * w_*          bf16 (raw 16-bit patterns), row-major [rows, in_f] [16B].
+ * outputs      f32 row-major, written for the t rows only.
+ * H heads, D = 128 (40001 otherwise).
+ * workspace    device scratch [16B] of at least kda_proj6_workspace_bytes(t, in_f) bytes (40009
+ *              otherwise): x split into bf16 hi + lo images.  Calls sharing it must not overlap.
+ * Precision: the weights' bf16 values enter the products exactly; x enters as hi + lo (about 16
+ * significant bits); the sums accumulate in f32.  One token row's result does not depend on the
+ * other rows of the call.
+ */
+size_t kda_proj6_workspace_bytes(int t, int in_f);
+int kda_proj6(const float* x, int t, int in_f, const void* w_q, const void* w_k, const void* w_v,
+              const void* w_fa, const void* w_ga, const void* w_b, float* q_raw, float* k_raw,
+              float* v_raw, float* f_down, float* g_down, float* beta_raw, int H, int D,
+              void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * kda_selftest_wait_timeout -- a self-test of failure detection (no counterpart in the pages):
  * launches one kernel whose single thread waits, with the bounded wait every kernel here uses,
  * on a barrier that nothing completes.  The wait gives up after about a second, raises the device

@@ -171,3 +171,29 @@ def test_kernel_timer_host(kda):
     names = [lib.kda_kernel_name(i).decode() for i in range(n)]
     assert "kda_chunk_inter_kernel" in names and "kda_prep_kernel" in names
     assert lib.kda_kernel_name(n) is None and lib.kda_kernel_name(-1) is None
+
+
+def test_proj6_contract(kda):
+    """kda_proj6 refuses bad shapes, null or misaligned pointers and a short workspace on the host,
+    before any device call."""
+    lib = kda.library()
+    ws_need = kda.kda_proj6_workspace_bytes(3, 256)
+    assert ws_need == 2 * 16 * 256 * 2               # hi and lo images of 16 padded rows
+    assert kda.kda_proj6_workspace_bytes(0, 256) == 0
+    assert kda.kda_proj6_workspace_bytes(257, 256) == 0
+    assert kda.kda_proj6_workspace_bytes(4, 100) == 0
+
+    def call(x=FAKE, t=3, in_f=256, w0=FAKE, H=2, D=128, ws=FAKE, wsb=None):
+        return lib.kda_proj6(x, t, in_f, w0, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                             FAKE, FAKE, H, D, ws, ws_need if wsb is None else wsb, None)
+    assert call(D=64) == 40001
+    assert call(t=0) == 40005
+    assert call(t=257) == 40005
+    assert call(in_f=100) == 40005
+    assert call(H=0) == 40005
+    assert call(x=None) == 40004
+    assert call(w0=None) == 40004
+    assert call(w0=FAKE + 8) == 40010
+    assert call(x=FAKE + 4) == 40010
+    assert call(wsb=ws_need - 1) == 40009
+    assert call(ws=None) == 40009
