@@ -306,6 +306,7 @@ int decode_impl(const void* q_raw, const void* k_raw, const void* v_raw, int raw
     a.keep = keep;
     a.norm_silu = norm_silu ? 1 : 0;
     if (const int sd = check_stream_device(stream)) return sd;
+    a.err = dev_err_ptr();
     return cuda_status(launch_decode_fused(a, static_cast<cudaStream_t>(stream)));
 }
 

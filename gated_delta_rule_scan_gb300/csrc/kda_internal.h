@@ -73,6 +73,7 @@ struct DecodeArgs {
     const int* keep;         // rollback: tokens of sequence n to take (device [N], clamped to
                              // 0..T; rows keep their stride T), or null for all T
     int norm_silu;           // RMSNorm gate: 0 sigmoid (KDA), 1 SiLU (GDN's gated_rmsnorm)
+    int* err;                // device error word (bounded waits)
 };
 
 cudaError_t launch_prep(const PrepArgs& a, cudaStream_t s);

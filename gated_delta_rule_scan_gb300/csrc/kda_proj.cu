@@ -15,11 +15,12 @@
 // are exact in the product, so the result carries only the f32 accumulation and the split's
 // ~2^-17 relative residue.
 //
-// One CTA per 128-row tile of one weight (the six weights' tiles in one grid): warp 0's lane 0
-// streams K-stages of 64 (16 KB of weights plus the x images) through a ring of mbarrier-guarded
-// shared-memory slots, warp 1's lane 0 issues the MMAs and frees each slot with a commit, and all
-// four warps read the accumulator back (TMEM lane = weight row, column = token) and store the
-// outputs, each warp writing 32 consecutive floats per token.  A tile's shared memory stays near
+// One CTA per 128-row tile of one weight (the six weights' tiles in one grid), launched as a
+// programmatic dependent of the split pre-pass so that its set-up and first weight loads overlap
+// the split: warp 0's lane 0 streams K-stages of 64 (16 KB of weights plus the x images) through
+// a ring of mbarrier-guarded shared-memory slots, warp 1's lane 0 issues the MMAs and frees each
+// slot with a commit, and all four warps read the accumulator back (TMEM lane = weight row,
+// column = token) and store the outputs, each warp writing 32 consecutive floats per token.  A tile's shared memory stays near
 // 100 KB for t <= 64, so two tiles share an SM and the grid (195 tiles at 64 heads) is resident at
 // once.  Every wait is bounded; a wait that gives up raises the device error word.
 #include <cuda_bf16.h>
@@ -58,6 +59,8 @@ __global__ void __launch_bounds__(256) kda_proj_split_kernel(const float* __rest
                                                              int t_pad, int in_f,
                                                              __nv_bfloat16* __restrict__ hi,
                                                              __nv_bfloat16* __restrict__ lo) {
+    // the projection kernel may start now: it loads weights until it needs these images
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const long n4 = (long)t_pad * in_f / 4;
     const long live4 = (long)t * in_f / 4;
     for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < n4;
@@ -108,18 +111,28 @@ kda_proj6_kernel(const __grid_constant__ Proj6Maps maps, const __grid_constant__
     const uint32_t tbase = *tmem_slot;
 
     if (tid == 0) {
-        // producer: K-stage kb into slot kb % stages once the MMAs of kb - stages have read it
+        // producer: K-stage kb into slot kb % stages once the MMAs of kb - stages have read it.
+        // The first ring of weight tiles goes out before the x images exist: the split kernel
+        // launched just before this one may still be running (programmatic dependent launch);
+        // griddepcontrol.wait returns once it has finished and its writes are visible.
         prefetch_tensormap(&maps.w[wi]);
         prefetch_tensormap(&maps.xh);
         prefetch_tensormap(&maps.xl);
+        const int first = nk < p.stages ? nk : p.stages;
+        for (int kb = 0; kb < first; ++kb) {
+            mbar_arrive_expect_tx(&full[kb], (uint32_t)stage_bytes);
+            tma_load_2d(base + kb * stage_bytes, &maps.w[wi], kb * kPK, row0, &full[kb]);
+        }
+        asm volatile("griddepcontrol.wait;" ::: "memory");
         for (int kb = 0; kb < nk; ++kb) {
             const int s = kb % p.stages;
-            if (kb >= p.stages &&
-                !mbar_wait_bounded(&empty[s], (uint32_t)(((kb / p.stages) & 1) ^ 1), p.err))
-                break;
             unsigned char* st = base + s * stage_bytes;
-            mbar_arrive_expect_tx(&full[s], (uint32_t)stage_bytes);
-            tma_load_2d(st, &maps.w[wi], kb * kPK, row0, &full[s]);
+            if (kb >= first) {
+                if (!mbar_wait_bounded(&empty[s], (uint32_t)(((kb / p.stages) & 1) ^ 1), p.err))
+                    break;
+                mbar_arrive_expect_tx(&full[s], (uint32_t)stage_bytes);
+                tma_load_2d(st, &maps.w[wi], kb * kPK, row0, &full[s]);
+            }
             tma_load_2d(st + kPStageW, &maps.xh, kb * kPK, 0, &full[s]);
             tma_load_2d(st + kPStageW + stage_x, &maps.xl, kb * kPK, 0, &full[s]);
         }
@@ -226,9 +239,20 @@ cudaError_t launch_proj6(const Proj6Args& a, cudaStream_t s) {
             }
         }
     }
+    // launched as a programmatic dependent of the split kernel: its CTAs may start (and stream
+    // weights) while the split is still running
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)tiles);
+    cfg.blockDim = dim3(kPThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     KernelTimer kt(kKProj6, s);
-    kda_proj6_kernel<<<tiles, kPThreads, smem, s>>>(maps, p);
-    return cudaGetLastError();
+    return cudaLaunchKernelEx(&cfg, kda_proj6_kernel, maps, p);
 }
 
 }  // namespace kda
