@@ -239,13 +239,16 @@ def proj6(x, w_q, w_k, w_v, w_fa, w_ga, w_b):
 def forward(*, q_raw, k_raw, v_raw, f_raw, dt_bias, a_log, beta_raw, state_in, H, D,
             conv_w=None, ring_in=None, cu_seqlens=None, gate_mode=0, gate_lb=-5.0,
             norm_w=None, gate_raw=None, l2_eps=1e-6, rms_eps=1e-6, scale=None,
-            scalar_scan=False, norm_gate="sigmoid"):
+            scalar_scan=False, norm_gate="sigmoid", Hk=None):
     """The mixer from projected channels to the gated output, in the pages' stage order
     (conv+SiLU -> ring roll -> l2 norm -> gates -> scan -> gated RMSNorm).
 
     q_raw/k_raw/v_raw: [rows, C] raw (pre-conv) channels, C = H*D.
-    conv_w: [3C, K] fused q,k,v conv weights or None (then no conv / SiLU and no ring).
-    ring_in: [N, 3C, K-1].
+    Hk: grouped queries (gdn_ops.rs `gdn_delta_rule_into` doc): q_raw and k_raw hold Hk heads
+        ([rows, Hk*D]) and value head h reads query/key head h % Hk; None means Hk = H.  The conv
+        planes and the ring then hold Hk*D q channels, Hk*D k channels and C v channels.
+    conv_w: [2*Hk*D + C, K] fused q,k,v conv weights or None (then no conv / SiLU and no ring).
+    ring_in: [N, 2*Hk*D + C, K-1].
     f_raw: [rows, C] (gate_mode 0, KDA) or [rows, H] (gate_mode 1, GDN).
     dt_bias: [C] (KDA) or [H] (GDN); a_log: [H]; beta_raw: [rows, H].
     state_in: [N, H, D, D] (M[j][i] layout).
@@ -255,17 +258,21 @@ def forward(*, q_raw, k_raw, v_raw, f_raw, dt_bias, a_log, beta_raw, state_in, H
     Returns a dict with q_hat, k_hat, v_hat, g, beta, o, y (or None), state_out, ring_out.
     """
     C = H * D
+    Hk = H if Hk is None else Hk
+    Cq = Hk * D
     q_raw, k_raw, v_raw = _f64(q_raw), _f64(k_raw), _f64(v_raw)
     rows = q_raw.shape[0]
     cu = _cu(cu_seqlens, rows)
     N = cu.size - 1
     planes = [q_raw, k_raw, v_raw]
-    conv = [np.empty((rows, C)) for _ in range(3)]
+    widths = [Cq, Cq, C]                      # channels of the q, k and v planes
+    offs = [0, Cq, 2 * Cq]                    # their first row in conv_w and the ring
+    conv = [np.empty((rows, w)) for w in widths]
     ring_out = None
     if conv_w is not None:
         conv_w = _f64(conv_w)
         K = conv_w.shape[1]
-        ring_in = _f64(ring_in).reshape(N, 3 * C, K - 1)
+        ring_in = _f64(ring_in).reshape(N, 2 * Cq + C, K - 1)
         ring_out = np.empty_like(ring_in)
     for n in range(N):
         r0, r1 = int(cu[n]), int(cu[n + 1])
@@ -273,13 +280,17 @@ def forward(*, q_raw, k_raw, v_raw, f_raw, dt_bias, a_log, beta_raw, state_in, H
             if conv_w is None:
                 y, _ = conv_silu(planes[p][r0:r1], None, None)
             else:
-                sl = slice(p * C, (p + 1) * C)
+                sl = slice(offs[p], offs[p] + widths[p])
                 y, ro = conv_silu(planes[p][r0:r1], conv_w[sl], ring_in[n, sl])
                 ring_out[n, sl] = ro
             conv[p][r0:r1] = y
     q_hat = l2norm(conv[0], D, l2_eps)
     k_hat = l2norm(conv[1], D, l2_eps)
     v_hat = conv[2]
+    # value head h reads query/key head h % Hk (the tiled order of gdn_delta_rule_into)
+    qk_head = np.arange(H) % Hk
+    q_scan = q_hat.reshape(rows, Hk, D)[:, qk_head]
+    k_scan = k_hat.reshape(rows, Hk, D)[:, qk_head]
     if gate_mode == 0:
         g = gate_kda(f_raw, dt_bias, a_log, gate_lb)
     else:
@@ -287,19 +298,18 @@ def forward(*, q_raw, k_raw, v_raw, f_raw, dt_bias, a_log, beta_raw, state_in, H
     beta = sigmoid(beta_raw).reshape(rows, H)
     shp = (rows, H, D)
     if gate_mode == 0:
-        o, st = scan_kda(q_hat.reshape(shp), k_hat.reshape(shp), v_hat.reshape(shp),
-                         g.reshape(shp), beta, state_in, cu, scale)
+        o, st = scan_kda(q_scan, k_scan, v_hat.reshape(shp), g.reshape(shp), beta, state_in, cu,
+                         scale)
     elif scalar_scan:
-        o, st = scan_gdn(q_hat.reshape(shp), k_hat.reshape(shp), v_hat.reshape(shp),
-                         g.reshape(rows, H), beta, state_in, cu, scale)
+        o, st = scan_gdn(q_scan, k_scan, v_hat.reshape(shp), g.reshape(rows, H), beta, state_in,
+                         cu, scale)
     else:  # the KDA routine with the per-head gate broadcast over the key dim
         gb = np.repeat(g.reshape(rows, H, 1), D, axis=2)
-        o, st = scan_kda(q_hat.reshape(shp), k_hat.reshape(shp), v_hat.reshape(shp), gb, beta,
-                         state_in, cu, scale)
+        o, st = scan_kda(q_scan, k_scan, v_hat.reshape(shp), gb, beta, state_in, cu, scale)
     y = None
     if norm_w is not None:
         y = gated_rmsnorm(o.reshape(rows, C), norm_w, gate_raw, rms_eps,
                           norm_gate).reshape(rows, C)
-    return dict(q_hat=q_hat.reshape(rows, C), k_hat=k_hat.reshape(rows, C),
+    return dict(q_hat=q_hat.reshape(rows, Cq), k_hat=k_hat.reshape(rows, Cq),
                 v_hat=v_hat.reshape(rows, C), g=g, beta=beta, o=o.reshape(rows, C), y=y,
                 state_out=st, ring_out=ring_out)

@@ -15,6 +15,8 @@ Which pin covers which oracle routine:
   gated_rmsnorm_silu   the SiLU-gated mode at hand values (sigmoid(ln 3) = 3/4) and z -> +inf.
   forward         split-at-every-point state carry (bit-equal); T-token call equals T chained
                   one-token calls (bit-equal).
+  forward (Hk)    grouped queries equal the plain mixer on q/k heads replicated in the tiled
+                  order h % Hk (outputs, state, ring).
   matvec_rows     one-hot weight rows select inputs exactly; small-integer case equals exact
   (proj6)         integer dot products; a band matrix's closed form; the six outputs' order.
 Every check is a plain function so test_oracle_mutations.py can run it against mutated oracle
@@ -463,6 +465,40 @@ def check_proj6_order_and_shapes():
         np.testing.assert_array_equal(o, np.full_like(o, (i + 1) * in_f))
 
 
+def check_gqa_equals_replicated_heads():
+    """Grouped queries (value head h reads query/key head h % Hk) equal the plain mixer run on
+    q/k raw channels, conv weights and ring rows replicated to H heads in that tiled order: the
+    outputs, the state and the v part of the ring agree, and each replicated q/k ring row equals
+    its source head's."""
+    rng = _rng(43)
+    D, H, Hk, K, T = 4, 6, 2, 3, 7
+    C, Cq = H * D, Hk * D
+    tiled = np.arange(H) % Hk
+    chan = np.concatenate([np.arange(h * D, (h + 1) * D) for h in tiled])   # q/k channel per slot
+    q = rng.standard_normal((T, Cq))
+    k = rng.standard_normal((T, Cq))
+    v = rng.standard_normal((T, C))
+    wq, wk, wv = (rng.standard_normal((Cq, K)), rng.standard_normal((Cq, K)),
+                  rng.standard_normal((C, K)))
+    rq, rk, rv = (rng.standard_normal((Cq, K - 1)), rng.standard_normal((Cq, K - 1)),
+                  rng.standard_normal((C, K - 1)))
+    shared = dict(f_raw=rng.standard_normal((T, C)), dt_bias=rng.standard_normal(C),
+                  a_log=np.log(rng.uniform(1, 16, H)), beta_raw=rng.standard_normal((T, H)),
+                  state_in=0.1 * rng.standard_normal((1, H, D, D)), norm_w=1 + rng.standard_normal(D),
+                  gate_raw=rng.standard_normal((T, C)), D=D, H=H)
+    gqa = orc.forward(q_raw=q, k_raw=k, v_raw=v, conv_w=np.concatenate([wq, wk, wv]),
+                      ring_in=np.concatenate([rq, rk, rv])[None], Hk=Hk, **shared)
+    full = orc.forward(q_raw=q[:, chan], k_raw=k[:, chan], v_raw=v,
+                       conv_w=np.concatenate([wq[chan], wk[chan], wv]),
+                       ring_in=np.concatenate([rq[chan], rk[chan], rv])[None], **shared)
+    for key in ("y", "o", "state_out"):
+        np.testing.assert_array_equal(gqa[key], full[key])
+    np.testing.assert_array_equal(gqa["ring_out"][0, 2 * Cq:], full["ring_out"][0, 2 * C:])
+    np.testing.assert_array_equal(gqa["ring_out"][0, :Cq][chan], full["ring_out"][0, :C])
+    np.testing.assert_array_equal(gqa["ring_out"][0, Cq:2 * Cq][chan], full["ring_out"][0, C:2 * C])
+    assert gqa["q_hat"].shape == (T, Cq)
+
+
 ALL_CHECKS = [
     check_three_token_golden, check_three_token_embedded, check_beta_zero_closed_form,
     check_orthonormal_recall, check_dense_product_form, check_chunked_form_every_chunk_size,
@@ -471,7 +507,7 @@ ALL_CHECKS = [
     check_gated_rmsnorm_silu,
     check_split_state_carry, check_chained_single_tokens_equal_multi_token,
     check_varlen_equals_separate_calls, check_matvec_one_hot_rows, check_matvec_exact_integers,
-    check_matvec_band, check_proj6_order_and_shapes,
+    check_matvec_band, check_proj6_order_and_shapes, check_gqa_equals_replicated_heads,
 ]
 
 
