@@ -78,12 +78,14 @@ int prep_build(const void* q_raw, const void* k_raw, const void* v_raw, int raw_
                const float* dt_bias, const float* a_log, int gate_mode, float gate_lb,
                const float* beta_raw, float* q_hat, float* k_hat, float* v_hat, float* g,
                float* beta, const SeqLayout& seq, int H, int D, int K, float l2_eps,
-               bool planes, PrepArgs& a) {
+               bool planes, PrepArgs& a, int Hk = 0) {
     a = PrepArgs{};
     a.seq = seq;
     if (D != kHeadDim) return KDA_ERR_HEAD_DIM;
     if (seq.N < 0 || seq.N > kMaxGridY || seq.total_rows < 0 || H <= 0 || H > kMaxGridY)
         return KDA_ERR_SHAPE;
+    if (Hk == 0) Hk = H;
+    if (Hk < 1 || Hk > H) return KDA_ERR_SHAPE;
     if (raw_dtype != KDA_DTYPE_F32 && raw_dtype != KDA_DTYPE_BF16) return KDA_ERR_ENUM;
     if (gate_mode < 0 || gate_mode > (KDA_GATE_PER_HEAD | KDA_GATE_EXP)) return KDA_ERR_ENUM;
     if (conv_w != nullptr && (K < 2 || K > kMaxConvK)) return KDA_ERR_CONV_K;
@@ -104,15 +106,17 @@ int prep_build(const void* q_raw, const void* k_raw, const void* v_raw, int raw_
             return KDA_ERR_ALIGN;
     }
     if (conv_w != nullptr && ring_in != ring_out) {
-        const size_t rb = (size_t)seq.N * 3 * H * kHeadDim * (K - 1) * sizeof(float);
+        const size_t rb = (size_t)seq.N * ring_channels(H, Hk) * (K - 1) * sizeof(float);
         if (overlap(ring_in, ring_out, rb)) return KDA_ERR_STATE_ALIAS;
     }
+    a.Hk = Hk;
     a.q_raw = q_raw; a.k_raw = k_raw; a.v_raw = v_raw; a.raw_bf16 = raw_dtype == KDA_DTYPE_BF16;
     a.conv_w = conv_w; a.ring_in = ring_in; a.ring_out = ring_out;
     a.f_raw = f_raw; a.dt_bias = dt_bias; a.a_log = a_log; a.gate_mode = gate_mode;
     a.gate_lb = gate_lb; a.beta_raw = beta_raw;
     a.q_hat = q_hat; a.k_hat = k_hat; a.v_hat = v_hat; a.g = g; a.beta = beta;
     a.seq = seq; a.H = H; a.K = conv_w ? K : 1; a.l2_eps = l2_eps;
+    a.Hk = Hk;
     return KDA_OK;
 }
 
@@ -121,11 +125,11 @@ int prep_impl(const void* q_raw, const void* k_raw, const void* v_raw, int raw_d
               const float* dt_bias, const float* a_log, int gate_mode, float gate_lb,
               const float* beta_raw, float* q_hat, float* k_hat, float* v_hat, float* g,
               float* beta, const SeqLayout& seq, int H, int D, int K, float l2_eps,
-              void* stream) {
+              void* stream, int Hk = 0) {
     PrepArgs a;
     const int rc = prep_build(q_raw, k_raw, v_raw, raw_dtype, conv_w, ring_in, ring_out, f_raw,
                               dt_bias, a_log, gate_mode, gate_lb, beta_raw, q_hat, k_hat, v_hat,
-                              g, beta, seq, H, D, K, l2_eps, true, a);
+                              g, beta, seq, H, D, K, l2_eps, true, a, Hk);
     if (rc != KDA_OK || seq.N == 0) return rc;
     if (const int sd = check_stream_device(stream)) return sd;
     return cuda_status(launch_prep(a, static_cast<cudaStream_t>(stream)));
@@ -209,7 +213,8 @@ int prefill_impl(const void* q_raw, const void* k_raw, const void* v_raw, int ra
                  const float* beta_raw, const float* state_in, float* state_out,
                  const float* norm_w, const float* gate_raw, float* y, const SeqLayout& seq,
                  const int* cu_host, int H, int D, int K, float l2_eps, float scale,
-                 float norm_eps, void* workspace, size_t workspace_bytes, void* stream) {
+                 float norm_eps, void* workspace, size_t workspace_bytes, void* stream,
+                 int Hk = 0) {
     if (D != kHeadDim) return KDA_ERR_HEAD_DIM;
     if (seq.N < 0 || seq.N > kMaxGridY || seq.total_rows < 0 || H <= 0 || H > kMaxGridY)
         return KDA_ERR_SHAPE;
@@ -225,7 +230,7 @@ int prefill_impl(const void* q_raw, const void* k_raw, const void* v_raw, int ra
     PrepArgs pa;
     int rc = prep_build(q_raw, k_raw, v_raw, raw_dtype, conv_w, ring_in, ring_out, f_raw, dt_bias,
                         a_log, gate_mode, gate_lb, beta_raw, nullptr, nullptr, nullptr, nullptr,
-                        nullptr, seq, H, D, K, l2_eps, false, pa);
+                        nullptr, seq, H, D, K, l2_eps, false, pa, Hk);
     if (rc != KDA_OK) return rc;
     // the fused kernel copies bf16 raw rows into shared memory 16 bytes at a time
     if (seq.total_rows > 0 && pa.raw_bf16 &&
@@ -243,6 +248,7 @@ int prefill_impl(const void* q_raw, const void* k_raw, const void* v_raw, int ra
     unsigned char* w = static_cast<unsigned char*>(workspace);
     float* oh = reinterpret_cast<float*>(w + L.o);
     ScanArgs a{};
+    a.Hk = pa.Hk;
     a.gate_mode = gate_mode; a.state_in = state_in; a.state_out = state_out; a.o = oh;
     a.seq = seq; a.H = H; a.scale = scale; a.order = nullptr; a.err = dev_err_ptr();
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -271,10 +277,13 @@ int decode_impl(const void* q_raw, const void* k_raw, const void* v_raw, int raw
                 const float* beta_raw, const float* state_in, float* state_out,
                 const float* norm_w, const float* gate_raw, float* y, int N, int T, int H, int D,
                 int K, float l2_eps, float scale, float rms_eps, const int* keep, bool rollback,
-                void* stream) {
+                void* stream, int Hk = 0) {
     if (D != kHeadDim) return KDA_ERR_HEAD_DIM;
     if (N < 0 || N > kMaxGridY || H <= 0 || H > kMaxGridY || T < 1 || T > kDecodeMaxT)
         return KDA_ERR_SHAPE;
+    if (Hk == 0) Hk = H;
+    if (Hk < 1 || Hk > H) return KDA_ERR_SHAPE;
+    if ((long)N * H >= (1L << 31)) return KDA_ERR_SHAPE;
     if (raw_dtype != KDA_DTYPE_F32 && raw_dtype != KDA_DTYPE_BF16) return KDA_ERR_ENUM;
     const bool norm_silu = (gate_mode & KDA_NORM_SILU) != 0;
     gate_mode &= ~KDA_NORM_SILU;
@@ -292,10 +301,15 @@ int decode_impl(const void* q_raw, const void* k_raw, const void* v_raw, int raw
     // head) block before it stores the same elements; a partial overlap is not
     if (state_in != state_out && overlap(state_in, state_out, sb)) return KDA_ERR_STATE_ALIAS;
     if (ring_in != ring_out) {
-        const size_t rb = (size_t)N * 3 * H * kHeadDim * (K - 1) * sizeof(float);
+        const size_t rb = (size_t)N * ring_channels(H, Hk) * (K - 1) * sizeof(float);
         if (overlap(ring_in, ring_out, rb)) return KDA_ERR_STATE_ALIAS;
+    } else if (Hk < H) {
+        // grouped queries: several value heads read one q/k ring row that only one of them
+        // rewrites, so the ring cannot be rolled in place
+        return KDA_ERR_STATE_ALIAS;
     }
     DecodeArgs a{};
+    a.Hk = Hk;
     a.q_raw = q_raw; a.k_raw = k_raw; a.v_raw = v_raw; a.raw_bf16 = raw_dtype == KDA_DTYPE_BF16;
     a.conv_w = conv_w; a.ring_in = ring_in; a.ring_out = ring_out;
     a.f_raw = f_raw; a.dt_bias = dt_bias; a.a_log = a_log; a.gate_mode = gate_mode;
@@ -517,6 +531,106 @@ int kda_verify_rollback(const void* q_raw, const void* k_raw, const void* v_raw,
     return decode_impl(q_raw, k_raw, v_raw, raw_dtype, conv_w, ring_in, ring_out, f_raw, dt_bias,
                        a_log, gate_mode, gate_lb, beta_raw, state_in, state_out, norm_w, gate_raw,
                        y, N, T, H, D, K, l2_eps, scale, rms_eps, keep, true, stream);
+}
+
+int kda_conv_l2norm_prep_gqa(const void* q_raw, const void* k_raw, const void* v_raw,
+                             int raw_dtype, const float* conv_w, const float* ring_in,
+                             float* ring_out, const float* f_raw, const float* dt_bias,
+                             const float* a_log, int gate_mode, float gate_lb,
+                             const float* beta_raw, float* q_hat, float* k_hat, float* v_hat,
+                             float* g, float* beta, int N, int T, int H, int Hk, int D, int K,
+                             float l2_eps, void* stream) {
+    if (N < 0 || T < 0 || Hk <= 0) return KDA_ERR_SHAPE;
+    SeqLayout seq{nullptr, T, N, (long)N * T};
+    return prep_impl(q_raw, k_raw, v_raw, raw_dtype, conv_w, ring_in, ring_out, f_raw, dt_bias,
+                     a_log, gate_mode, gate_lb, beta_raw, q_hat, k_hat, v_hat, g, beta, seq, H,
+                     D, K, l2_eps, stream, Hk);
+}
+
+int kda_conv_l2norm_prep_varlen_gqa(const void* q_raw, const void* k_raw, const void* v_raw,
+                                    int raw_dtype, const float* conv_w, const float* ring_in,
+                                    float* ring_out, const float* f_raw, const float* dt_bias,
+                                    const float* a_log, int gate_mode, float gate_lb,
+                                    const float* beta_raw, float* q_hat, float* k_hat,
+                                    float* v_hat, float* g, float* beta, const int* cu_seqlens,
+                                    const int* cu_seqlens_host, int N, int total_T, int H,
+                                    int Hk, int D, int K, float l2_eps, void* stream) {
+    if (N < 0 || total_T < 0 || Hk <= 0) return KDA_ERR_SHAPE;
+    if (N > 0) {
+        if (cu_seqlens == nullptr) return KDA_ERR_NULL;
+        const int rc = check_cu(cu_seqlens_host, N, total_T);
+        if (rc) return rc;
+    }
+    SeqLayout seq{cu_seqlens, 0, N, (long)total_T};
+    return prep_impl(q_raw, k_raw, v_raw, raw_dtype, conv_w, ring_in, ring_out, f_raw, dt_bias,
+                     a_log, gate_mode, gate_lb, beta_raw, q_hat, k_hat, v_hat, g, beta, seq, H,
+                     D, K, l2_eps, stream, Hk);
+}
+
+int kda_prefill_fused_gqa(const void* q_raw, const void* k_raw, const void* v_raw, int raw_dtype,
+                          const float* conv_w, const float* ring_in, float* ring_out,
+                          const float* f_raw, const float* dt_bias, const float* a_log,
+                          int gate_mode, float gate_lb, const float* beta_raw,
+                          const float* state_in, float* state_out, const float* norm_w,
+                          const float* gate_raw, float* y, int N, int T, int H, int Hk, int D,
+                          int K, float l2_eps, float scale, float rms_eps, void* workspace,
+                          size_t workspace_bytes, void* stream) {
+    if (N < 0 || T < 0 || Hk <= 0) return KDA_ERR_SHAPE;
+    SeqLayout seq{nullptr, T, N, (long)N * T};
+    return prefill_impl(q_raw, k_raw, v_raw, raw_dtype, conv_w, ring_in, ring_out, f_raw, dt_bias,
+                        a_log, gate_mode, gate_lb, beta_raw, state_in, state_out, norm_w, gate_raw,
+                        y, seq, nullptr, H, D, K, l2_eps, scale, rms_eps, workspace,
+                        workspace_bytes, stream, Hk);
+}
+
+int kda_prefill_fused_varlen_gqa(const void* q_raw, const void* k_raw, const void* v_raw,
+                                 int raw_dtype, const float* conv_w, const float* ring_in,
+                                 float* ring_out, const float* f_raw, const float* dt_bias,
+                                 const float* a_log, int gate_mode, float gate_lb,
+                                 const float* beta_raw, const float* state_in, float* state_out,
+                                 const float* norm_w, const float* gate_raw, float* y,
+                                 const int* cu_seqlens, const int* cu_seqlens_host, int N,
+                                 int total_T, int H, int Hk, int D, int K, float l2_eps,
+                                 float scale, float rms_eps, void* workspace,
+                                 size_t workspace_bytes, void* stream) {
+    if (N < 0 || total_T < 0 || Hk <= 0) return KDA_ERR_SHAPE;
+    if (N > 0) {
+        if (cu_seqlens == nullptr) return KDA_ERR_NULL;
+        const int rc = check_cu(cu_seqlens_host, N, total_T);
+        if (rc) return rc;
+    }
+    SeqLayout seq{cu_seqlens, 0, N, (long)total_T};
+    return prefill_impl(q_raw, k_raw, v_raw, raw_dtype, conv_w, ring_in, ring_out, f_raw, dt_bias,
+                        a_log, gate_mode, gate_lb, beta_raw, state_in, state_out, norm_w, gate_raw,
+                        y, seq, cu_seqlens_host, H, D, K, l2_eps, scale, rms_eps, workspace,
+                        workspace_bytes, stream, Hk);
+}
+
+int kda_decode_fused_gqa(const void* q_raw, const void* k_raw, const void* v_raw, int raw_dtype,
+                         const float* conv_w, const float* ring_in, float* ring_out,
+                         const float* f_raw, const float* dt_bias, const float* a_log,
+                         int gate_mode, float gate_lb, const float* beta_raw,
+                         const float* state_in, float* state_out, const float* norm_w,
+                         const float* gate_raw, float* y, int N, int T, int H, int Hk, int D, int K,
+                         float l2_eps, float scale, float rms_eps, void* stream) {
+    if (Hk <= 0) return KDA_ERR_SHAPE;
+    return decode_impl(q_raw, k_raw, v_raw, raw_dtype, conv_w, ring_in, ring_out, f_raw, dt_bias,
+                       a_log, gate_mode, gate_lb, beta_raw, state_in, state_out, norm_w, gate_raw,
+                       y, N, T, H, D, K, l2_eps, scale, rms_eps, nullptr, false, stream, Hk);
+}
+
+int kda_verify_rollback_gqa(const void* q_raw, const void* k_raw, const void* v_raw,
+                            int raw_dtype, const float* conv_w, const float* ring_in,
+                            float* ring_out, const float* f_raw, const float* dt_bias,
+                            const float* a_log, int gate_mode, float gate_lb,
+                            const float* beta_raw, const float* state_in, float* state_out,
+                            const float* norm_w, const float* gate_raw, float* y, const int* keep,
+                            int N, int T, int H, int Hk, int D, int K, float l2_eps, float scale,
+                            float rms_eps, void* stream) {
+    if (Hk <= 0) return KDA_ERR_SHAPE;
+    return decode_impl(q_raw, k_raw, v_raw, raw_dtype, conv_w, ring_in, ring_out, f_raw, dt_bias,
+                       a_log, gate_mode, gate_lb, beta_raw, state_in, state_out, norm_w, gate_raw,
+                       y, N, T, H, D, K, l2_eps, scale, rms_eps, keep, true, stream, Hk);
 }
 
 int kda_selftest_wait_timeout(void* stream) {

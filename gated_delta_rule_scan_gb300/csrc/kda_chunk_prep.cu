@@ -265,11 +265,11 @@ struct RawMaps {
 // halo from the ring before the sequence start, and tokens past the chunk end are masked).
 template <int KW>
 __device__ __forceinline__ void stage_raw(RawStage<KW>& st, const RawMaps& m, const TaskPos& tp,
-                                          uint64_t* bar) {
+                                          int Hk, uint64_t* bar) {
     mbar_arrive_expect_tx(bar, 3u * RawStage<KW>::kRows * kHeadDim * sizeof(__nv_bfloat16));
-    const int x = tp.h * kHeadDim, y = (int)tp.row0 - (KW - 1);
-    tma_load_2d(&st.v[0][0][0], &m.q, x, y, bar);
-    tma_load_2d(&st.v[1][0][0], &m.k, x, y, bar);
+    const int xq = (tp.h % Hk) * kHeadDim, x = tp.h * kHeadDim, y = (int)tp.row0 - (KW - 1);
+    tma_load_2d(&st.v[0][0][0], &m.q, xq, y, bar);
+    tma_load_2d(&st.v[1][0][0], &m.k, xq, y, bar);
     tma_load_2d(&st.v[2][0][0], &m.v, x, y, bar);
 }
 
@@ -333,7 +333,9 @@ __device__ __forceinline__ void stage_params(ParamStage& ps, const PrepArgs& p, 
         for (int idx = tid; idx < 3 * per; idx += kThrF) {
             const int pl = idx / per, r = idx - pl * per;
             const int ch = K == 4 ? r >> 2 : r / K, j = r - ch * K;
-            cp_async4(&ps.w[pl][j * kHeadDim + ch], p.conv_w + (pl * C + (long)h * kHeadDim) * K + r);
+            const long hp = pl < 2 ? h % prep_qk_heads(H, p.Hk) : h;   // the plane's head
+            cp_async4(&ps.w[pl][j * kHeadDim + ch],
+                      p.conv_w + (plane_offset(H, p.Hk, pl) + hp * kHeadDim) * K + r);
         }
     }
     if (GATE_MODE == 0) {
@@ -396,6 +398,10 @@ kda_chunk_prep_intra_kernel(PrepArgs p, ScanArgs a, const int* chunk_off, unsign
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int H = a.H;
     const long C = (long)H * kHeadDim;
+    // grouped queries: the q and k planes hold Hk heads ([rows, Cq]); task head h reads q/k head
+    // h % Hk, and the conv weights and ring rows are [q | k | v] = [Cq | Cq | C]
+    const int Hk = prep_qk_heads(H, p.Hk);
+    const long Cq = (long)Hk * kHeadDim;
     const long ntasks = nchunks * H;
     const int kq = 4 * lane;                     // first of this lane's channels within the head
     const int t0 = kTokW * warp;                 // the warp's first token within the chunk
@@ -419,7 +425,7 @@ kda_chunk_prep_intra_kernel(PrepArgs p, ScanArgs a, const int* chunk_off, unsign
             prefetch_tensormap(&maps.q);
             prefetch_tensormap(&maps.k);
             prefetch_tensormap(&maps.v);
-            stage_raw<KW>(stage, maps, tp, &smf.bar_raw);
+            stage_raw<KW>(stage, maps, tp, Hk, &smf.bar_raw);
             if (GATE_MODE == 0) stage_f(sm.scr, maps, tp, &smf.bar_f);
         }
         stage_params<GATE_MODE, PW>(ps, p, H, C, tp);
@@ -433,7 +439,8 @@ kda_chunk_prep_intra_kernel(PrepArgs p, ScanArgs a, const int* chunk_off, unsign
     const long begin = tp.begin, row0 = tp.row0;
     const long c = (row0 - begin) / kCc;
     unsigned char* blk = ws + ((long)gid * H + h) * kBlkBytes;
-    const long c4 = (long)h * kHeadDim + kq;     // this lane's first channel within the plane
+    const long c4 = (long)h * kHeadDim + kq;     // this lane's first channel within the v plane
+    const long cq4 = (long)(h % Hk) * kHeadDim + kq;   // ... and within the q and k planes
     const int ntok = max(0, min(kTokW, nt - t0));
 
     // ---- loads: the gate input and beta; raw q, k, v (staged, or direct) -----------------------
@@ -451,7 +458,7 @@ kda_chunk_prep_intra_kernel(PrepArgs p, ScanArgs a, const int* chunk_off, unsign
             sm.gs[tid] = live ? gdn_gate_f(p.f_raw[(row0 + tid) * H + h], p.dt_bias[h], p.a_log[h]) : 0.0f;
     }
     const long pos0 = c * kCc + t0;
-    const long rr = (long)n * 3 * C * R;
+    const long rr = (long)n * (2 * Cq + C) * R;
     PlaneRaw<BF16, KW> rq, rk, rv;               // direct loads (no staging)
     if constexpr (PF) {
         bool ld_ok = mbar_wait_bounded(&smf.bar_raw, ph_ld, a.err);
@@ -473,9 +480,9 @@ kda_chunk_prep_intra_kernel(PrepArgs p, ScanArgs a, const int* chunk_off, unsign
                                  : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
         }
     } else {
-        plane_load<BF16, CONV, KW>(rq, p.q_raw, C, c4, begin, pos0, ntok, p.ring_in, rr + (0 * C + c4) * R, R);
-        plane_load<BF16, CONV, KW>(rk, p.k_raw, C, c4, begin, pos0, ntok, p.ring_in, rr + (1 * C + c4) * R, R);
-        plane_load<BF16, CONV, KW>(rv, p.v_raw, C, c4, begin, pos0, ntok, p.ring_in, rr + (2 * C + c4) * R, R);
+        plane_load<BF16, CONV, KW>(rq, p.q_raw, Cq, cq4, begin, pos0, ntok, p.ring_in, rr + (0 * Cq + cq4) * R, R);
+        plane_load<BF16, CONV, KW>(rk, p.k_raw, Cq, cq4, begin, pos0, ntok, p.ring_in, rr + (1 * Cq + cq4) * R, R);
+        plane_load<BF16, CONV, KW>(rv, p.v_raw, C, c4, begin, pos0, ntok, p.ring_in, rr + (2 * Cq + c4) * R, R);
     }
 
     // ---- conv + SiLU; l2 norm of q and k over the head (one warp = one token group) ------------
@@ -487,17 +494,18 @@ kda_chunk_prep_intra_kernel(PrepArgs p, ScanArgs a, const int* chunk_off, unsign
 #pragma unroll
             for (int pl = 2; pl >= 0; --pl) {
                 PlaneRaw<true, KW> pr;
-                plane_from_stage<KW>(pr, stage, pl, t0, kq, pos0, Rr, p.ring_in, rr + (pl * C + c4) * R);
+                const long crow = pl * Cq + (pl < 2 ? cq4 : c4);   // conv / ring row of channel
+                plane_from_stage<KW>(pr, stage, pl, t0, kq, pos0, Rr, p.ring_in, rr + crow * R);
                 if constexpr (PW) plane_weights_t<KW>(ps.w[pl], kq, K, w);
-                else if constexpr (CONV) plane_weights<KW>(p.conv_w, pl * C + c4, K, w);
+                else if constexpr (CONV) plane_weights<KW>(p.conv_w, crow, K, w);
                 plane_conv<true, CONV, KW>(pr, w, K, pl == 2 ? v : (pl == 1 ? k : q));
             }
         } else {
-            if constexpr (CONV) plane_weights<KW>(p.conv_w, 2 * C + c4, K, w);
+            if constexpr (CONV) plane_weights<KW>(p.conv_w, 2 * Cq + c4, K, w);
             plane_conv<BF16, CONV, KW>(rv, w, K, v);
-            if constexpr (CONV) plane_weights<KW>(p.conv_w, 1 * C + c4, K, w);
+            if constexpr (CONV) plane_weights<KW>(p.conv_w, 1 * Cq + cq4, K, w);
             plane_conv<BF16, CONV, KW>(rk, w, K, k);
-            if constexpr (CONV) plane_weights<KW>(p.conv_w, 0 * C + c4, K, w);
+            if constexpr (CONV) plane_weights<KW>(p.conv_w, 0 * Cq + cq4, K, w);
             plane_conv<BF16, CONV, KW>(rq, w, K, q);
         }
     }
@@ -723,7 +731,7 @@ kda_chunk_prep_intra_kernel(PrepArgs p, ScanArgs a, const int* chunk_off, unsign
         if (PF && next < ntasks) {
             const TaskPos np = task_pos(a.seq, chunk_off, next, nchunks);
             ld_pending = true;
-            if (tid == 0) stage_raw<KW>(stage, maps, np, &smf.bar_raw);
+            if (tid == 0) stage_raw<KW>(stage, maps, np, Hk, &smf.bar_raw);
             stage_params<GATE_MODE, PW>(ps, p, H, C, np);
         }
     }, [&]() {
@@ -763,9 +771,10 @@ static cudaError_t launch_prep_intra_t(const PrepArgs& p, const ScanArgs& a, con
         return cudaErrorInvalidValue;
     if (BF16) {                                  // the staged form reads through tensor maps
         const long rows = a.seq.total_rows, C = (long)a.H * kHeadDim;
+        const long Cq = plane_width(a.H, p.Hk, 0);
         constexpr int kRows = RawStage<KW>::kRows;
-        if (!make_tensor_map_2d_any(&maps.q, p.q_raw, true, rows, C, kHeadDim, kRows) ||
-            !make_tensor_map_2d_any(&maps.k, p.k_raw, true, rows, C, kHeadDim, kRows) ||
+        if (!make_tensor_map_2d_any(&maps.q, p.q_raw, true, rows, Cq, kHeadDim, kRows) ||
+            !make_tensor_map_2d_any(&maps.k, p.k_raw, true, rows, Cq, kHeadDim, kRows) ||
             !make_tensor_map_2d_any(&maps.v, p.v_raw, true, rows, C, kHeadDim, kRows) ||
             (GM == 0 && !make_tensor_map_2d_any(&maps.f, p.f_raw, false, rows, C, kHeadDim, kCc)))
             return cudaErrorInvalidValue;

@@ -6,13 +6,11 @@
 // conv + SiLU over the ring and the new rows, ring roll, l2 norm of q and k, the KDA (or GDN) gate
 // and beta, the delta-rule recurrence, the sigmoid-gated RMSNorm.
 //
-// GB300 layout.  Decode is bound by the 64 KiB state read + write per (sequence, head).  The grid
-// is persistent: two 256-thread CTAs per SM walk the (sequence, head) units, and while one unit is
-// computed the next unit's state block (64 KiB, contiguous) is already on its way into shared
-// memory by one bulk copy, so the state stream never waits for the per-token chain (at T > 1 the
-// chain is as long as the state transfer itself).  8 lanes share 4 value columns with 16 key-dim
-// elements each, and the per-token step is the sequential prefill scan's (kda_scan_core.cuh),
-// instruction for instruction.
+// GB300 layout.  Decode is bound by the 64 KiB state read + write per (sequence, head), so one CTA
+// owns one (sequence, head) and issues its whole state column block as streaming 128-bit loads at
+// entry, before the prologue runs, so the HBM latency overlaps the conv / norm / gate work.  256
+// threads; 8 lanes share 4 value columns with 16 key-dim elements each, and the per-token step is
+// the sequential prefill scan's (kda_scan_core.cuh), instruction for instruction.
 // The prologue and epilogue use the same device functions as the prep and epilogue kernels, so
 // this kernel's outputs equal prep + scan + gated-RMSNorm launched separately, bit for bit, and a
 // T-token launch equals T one-token launches bit for bit.
@@ -22,27 +20,9 @@ namespace kda {
 
 constexpr int kDecThreads = 256;
 
-constexpr int kDecStateBytes = kHeadDim * kHeadDim * 4;   // one (sequence, head) state block
-
-// Load the 4 columns of this lane's group from the staged state block (the layout of col4_load).
-__device__ __forceinline__ void col4_load_smem(Col4& S, const float* col0, int r) {
-#pragma unroll
-    for (int c = 0; c < 4; ++c)
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-            const float4 x = *reinterpret_cast<const float4*>(col0 + c * kHeadDim + 4 * r + 32 * m);
-            S.s[c][2 * m] = lo2(x);
-            S.s[c][2 * m + 1] = hi2(x);
-        }
-}
-
 // KW: register window width of the conv (4 when K <= 4, else 8).
 template <bool BF16, int GATE_MODE, int KW>
 __global__ void __launch_bounds__(kDecThreads, 2) kda_decode_fused_kernel(DecodeArgs a) {
-    extern __shared__ unsigned char dec_smem_raw[];
-    float* sbuf = reinterpret_cast<float*>(
-        (reinterpret_cast<uintptr_t>(dec_smem_raw) + 127) & ~uintptr_t(127));
-    uint64_t* sbar = reinterpret_cast<uint64_t*>(sbuf + kHeadDim * kHeadDim);
     __shared__ __align__(16) float qh[kDecodeMaxT][kHeadDim];
     __shared__ __align__(16) float kh[kDecodeMaxT][kHeadDim];
     __shared__ __align__(16) float av[kDecodeMaxT][kHeadDim];
@@ -53,214 +33,168 @@ __global__ void __launch_bounds__(kDecThreads, 2) kda_decode_fused_kernel(Decode
     __shared__ float part[2][2][kDecodeMaxT];
     __shared__ float inv_s[2][kDecodeMaxT];
 
+    const int h = blockIdx.x, n = blockIdx.y;
     const int tid = threadIdx.x;
     const int H = a.H, K = a.K, R = a.K - 1;
     const long C = (long)H * kHeadDim;
-    const int units = a.N * H;                   // unit u = (sequence u / H, head u % H)
+    const long row0 = (long)n * a.T;             // rows of sequence n: stride T in every mode
+    // tokens taken: all T, or (rollback) the first keep[n]
+    const int T = a.keep != nullptr ? min(max(a.keep[n], 0), a.T) : a.T;
     const int warp = tid >> 5, lane = tid & 31;
     const int grp = lane >> 3, r = lane & 7;
-    const int cw = warp * 16 + grp * 4;          // the group's first column
 
-    if (tid == 0) {
-        mbar_init(sbar, 1);
-        fence_mbar_init();
+    // ---- issue the state loads first: 4 columns x 16 elements per lane -------------------
+    const int cw = warp * 16 + grp * 4;      // the group's first column
+    const long col0 = (((long)n * H + h) * kHeadDim + cw) * kHeadDim;
+    Col4 S;
+    col4_load(S, a.state_in + col0, r);
+
+    // ---- prologue: 64 threads per task, each on a channel pair (2i, 2i+1) --------------------
+    //      threads 0-63 q plane, 64-127 k plane, 128-191 v plane (+ beta), 192-255 the gate.
+    //      Grouped queries: the q and k planes hold Hk heads and this value head reads q/k head
+    //      h % Hk; only the CTAs of heads h < Hk write those heads' ring rows.
+    const int task = tid >> 6, i0 = 2 * (tid & 63);
+    const int c = h * kHeadDim + i0;
+    if (task < 3) {
+        const void* raw = task == 0 ? a.q_raw : (task == 1 ? a.k_raw : a.v_raw);
+        const long Cp = plane_width(H, a.Hk, task);        // row width of this plane
+        const int cp = (task < 2 ? h % prep_qk_heads(H, a.Hk) : h) * kHeadDim + i0;
+        const bool ring_owner = task == 2 || h < prep_qk_heads(H, a.Hk);
+        float wr[2][KW], win[2][KW];
+        const long ring_row =
+            ((long)n * ring_channels(H, a.Hk) + plane_offset(H, a.Hk, task) + cp) * R;
+#pragma unroll
+        for (int m = 0; m < KW; ++m) {
+            const int jj = m - (KW - K);
+            const int d = KW - m;
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                wr[e][m] = jj >= 0 ? a.conv_w[(plane_offset(H, a.Hk, task) + cp + e) * K + jj] : 0.0f;
+                win[e][m] = d <= R ? a.ring_in[ring_row + e * R + (R - d)] : 0.0f;
+            }
+        }
+        float (*dst)[kHeadDim] = task == 0 ? qh : (task == 1 ? kh : vh);
+        for (int t = 0; t < T; ++t) {
+            const float2 x = load_raw2<BF16>(raw, (row0 + t) * Cp + cp);
+            window_push(win[0], x.x);
+            window_push(win[1], x.y);
+            *reinterpret_cast<float2*>(&dst[t][i0]) =
+                make_float2(silu_f(conv_taps_f(wr[0], win[0], K)), silu_f(conv_taps_f(wr[1], win[1], K)));
+        }
+#pragma unroll
+        for (int m = 0; m < KW; ++m) {
+            const int d = KW - 1 - m;  // win[m] = sample d steps before the last one
+            if (d < R && ring_owner) {
+                a.ring_out[ring_row + (R - 1 - d)] = win[0][m];
+                a.ring_out[ring_row + R + (R - 1 - d)] = win[1][m];
+            }
+        }
+        if (task == 2 && (tid & 63) < T) {
+            const int t = tid & 63;
+            beta_s[t] = sigmoid_f(a.beta_raw[(row0 + t) * H + h]);
+            if (GATE_MODE == 1)
+                ascal[t] = decay_f(gdn_gate_f(a.f_raw[(row0 + t) * H + h], a.dt_bias[h], a.a_log[h]));
+        }
+    } else if (GATE_MODE == 0) {
+        const float rate = expf(a.a_log[h]);
+        const float2 dt = *reinterpret_cast<const float2*>(a.dt_bias + c);
+        for (int t = 0; t < T; ++t) {
+            const float2 f = *reinterpret_cast<const float2*>(a.f_raw + (row0 + t) * C + c);
+            *reinterpret_cast<float2*>(&av[t][i0]) =
+                make_float2(decay_f(kda_gate_f(f.x, dt.x, rate, a.gate_lb)),
+                            decay_f(kda_gate_f(f.y, dt.y, rate, a.gate_lb)));
+        }
     }
     __syncthreads();
-    // the first unit's state block on its way while the loop starts
-    if (tid == 0 && (int)blockIdx.x < units) {
-        mbar_arrive_expect_tx(sbar, kDecStateBytes);
-        bulk_load(sbuf, a.state_in + (long)blockIdx.x * kHeadDim * kHeadDim, kDecStateBytes, sbar);
+    // ---- l2 norm of q (warps 0-1) and k (warps 2-3) ----------------------------------------
+    if (task < 2) {
+        float (*x)[kHeadDim] = task == 0 ? qh : kh;
+        for (int t = 0; t < T; ++t) {
+            const float2 v = *reinterpret_cast<const float2*>(&x[t][i0]);
+            const float ssum = warp_sum(pair_sumsq(v.x, v.y));
+            if (lane == 0) part[task][warp & 1][t] = ssum;
+        }
     }
-    uint32_t phase = 0;
-    bool pending = (int)blockIdx.x < units;      // thread 0: a state copy is in flight
-    for (int u = blockIdx.x; u < units; u += gridDim.x) {
-        const int h = u % H, n = u / H;
-        const long row0 = (long)n * a.T;         // rows of sequence n: stride T in every mode
-        // tokens taken: all T, or (rollback) the first keep[n]
-        const int T = a.keep != nullptr ? min(max(a.keep[n], 0), a.T) : a.T;
-        const long col0 = (((long)n * H + h) * kHeadDim + cw) * kHeadDim;
-
-        // ---- this unit's state from the staged block into registers; then the next unit's copy
-        const bool ok = mbar_wait_bounded(sbar, phase, a.err);
-        Col4 S;
-        col4_load_smem(S, sbuf + cw * kHeadDim, r);
-        if (__syncthreads_or(!ok)) break;        // a copy that never landed (still pending): stop
-        phase ^= 1u;
-        if (tid == 0) {
-            pending = false;
-            const int un = u + gridDim.x;
-            if (un < units) {
-                mbar_arrive_expect_tx(sbar, kDecStateBytes);
-                bulk_load(sbuf, a.state_in + (long)un * kHeadDim * kHeadDim, kDecStateBytes, sbar);
-                pending = true;
-            }
-        }
-        // ---- prologue: 64 threads per task, each on a channel pair (2i, 2i+1) --------------------
-        //      threads 0-63 q plane, 64-127 k plane, 128-191 v plane (+ beta), 192-255 the gate
-        const int task = tid >> 6, i0 = 2 * (tid & 63);
-        const int c = h * kHeadDim + i0;
-        if (task < 3) {
-            const void* raw = task == 0 ? a.q_raw : (task == 1 ? a.k_raw : a.v_raw);
-            float wr[2][KW], win[2][KW];
-            const long ring_row = ((long)n * 3 * C + task * C + c) * R;   // channel c; c+1 is R later
-#pragma unroll
-            for (int m = 0; m < KW; ++m) {
-                const int jj = m - (KW - K);
-                const int d = KW - m;
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    wr[e][m] = jj >= 0 ? a.conv_w[(task * C + c + e) * K + jj] : 0.0f;
-                    win[e][m] = d <= R ? a.ring_in[ring_row + e * R + (R - d)] : 0.0f;
-                }
-            }
-            float (*dst)[kHeadDim] = task == 0 ? qh : (task == 1 ? kh : vh);
-            for (int t = 0; t < T; ++t) {
-                const float2 x = load_raw2<BF16>(raw, (row0 + t) * C + c);
-                window_push(win[0], x.x);
-                window_push(win[1], x.y);
-                *reinterpret_cast<float2*>(&dst[t][i0]) =
-                    make_float2(silu_f(conv_taps_f(wr[0], win[0], K)), silu_f(conv_taps_f(wr[1], win[1], K)));
-            }
-#pragma unroll
-            for (int m = 0; m < KW; ++m) {
-                const int d = KW - 1 - m;  // win[m] = sample d steps before the last one
-                if (d < R) {
-                    a.ring_out[ring_row + (R - 1 - d)] = win[0][m];
-                    a.ring_out[ring_row + R + (R - 1 - d)] = win[1][m];
-                }
-            }
-            if (task == 2 && (tid & 63) < T) {
-                const int t = tid & 63;
-                beta_s[t] = sigmoid_f(a.beta_raw[(row0 + t) * H + h]);
-                if (GATE_MODE == 1)
-                    ascal[t] = decay_f(gdn_gate_f(a.f_raw[(row0 + t) * H + h], a.dt_bias[h], a.a_log[h]));
-            }
-        } else if (GATE_MODE == 0) {
-            const float rate = expf(a.a_log[h]);
-            const float2 dt = *reinterpret_cast<const float2*>(a.dt_bias + c);
-            for (int t = 0; t < T; ++t) {
-                const float2 f = *reinterpret_cast<const float2*>(a.f_raw + (row0 + t) * C + c);
-                *reinterpret_cast<float2*>(&av[t][i0]) =
-                    make_float2(decay_f(kda_gate_f(f.x, dt.x, rate, a.gate_lb)),
-                                decay_f(kda_gate_f(f.y, dt.y, rate, a.gate_lb)));
-            }
-        }
-        __syncthreads();
-        // ---- l2 norm of q (warps 0-1) and k (warps 2-3) ----------------------------------------
-        if (task < 2) {
-            float (*x)[kHeadDim] = task == 0 ? qh : kh;
-            for (int t = 0; t < T; ++t) {
-                const float2 v = *reinterpret_cast<const float2*>(&x[t][i0]);
-                const float ssum = warp_sum(pair_sumsq(v.x, v.y));
-                if (lane == 0) part[task][warp & 1][t] = ssum;
-            }
-        }
-        __syncthreads();
-        if (tid < 2 * kDecodeMaxT) {
-            const int pl = tid / kDecodeMaxT, t = tid % kDecodeMaxT;
-            if (t < T) inv_s[pl][t] = l2_inv_f(part[pl][0][t] + part[pl][1][t], a.l2_eps);
-        }
-        __syncthreads();
-        if (task < 2) {
-            float (*x)[kHeadDim] = task == 0 ? qh : kh;
-            for (int t = 0; t < T; ++t) {
-                const float2 v = *reinterpret_cast<const float2*>(&x[t][i0]);
-                *reinterpret_cast<float2*>(&x[t][i0]) =
-                    make_float2(__fmul_rn(v.x, inv_s[task][t]), __fmul_rn(v.y, inv_s[task][t]));
-            }
-        }
-        __syncthreads();
-
-        // ---- the recurrence, token by token ---------------------------------------------------
-        {
-            TokView vw;
-            vw.k = &kh[0][0];
-            vw.a = &av[0][0];
-            vw.q = &qh[0][0];
-            vw.a_scal = ascal;
-            vw.v = &vh[0][0];
-            vw.beta = beta_s;
-            vw.out = &os[0][0];
-            vw.row_stride = kHeadDim;
-            vw.v_stride = kHeadDim;
-            vw.v_col0 = cw;
-            vw.out_stride = kHeadDim;
-            vw.out_col0 = cw;
-            col4_tokens<GATE_MODE == 0, false>(S, T, vw, a.scale, r, lane);
-        }
-        col4_store(S, a.state_out + col0, r);
-        __syncthreads();
-        // ---- epilogue: gated RMSNorm, one warp per token row -----------------------------------
-        for (int t = warp; t < T; t += kDecThreads / 32) {
-            const float4 o4 = *reinterpret_cast<const float4*>(&os[t][4 * lane]);
-            float ss = __fmul_rn(o4.x, o4.x);
-            ss = ss + __fmul_rn(o4.y, o4.y);
-            ss = ss + __fmul_rn(o4.z, o4.z);
-            ss = ss + __fmul_rn(o4.w, o4.w);
-            const float inv = rms_inv_f(warp_sum(ss), a.rms_eps);
-            const long base = (row0 + t) * C + h * kHeadDim + 4 * lane;
-            const float4 w4 = *reinterpret_cast<const float4*>(a.norm_w + 4 * lane);
-            const float4 z4 = *reinterpret_cast<const float4*>(a.gate_raw + base);
-            float4 y4;
-            if (a.norm_silu) {
-                y4.x = gated_norm_f<true>(o4.x, inv, w4.x, z4.x);
-                y4.y = gated_norm_f<true>(o4.y, inv, w4.y, z4.y);
-                y4.z = gated_norm_f<true>(o4.z, inv, w4.z, z4.z);
-                y4.w = gated_norm_f<true>(o4.w, inv, w4.w, z4.w);
-            } else {
-                y4.x = gated_norm_f(o4.x, inv, w4.x, z4.x);
-                y4.y = gated_norm_f(o4.y, inv, w4.y, z4.y);
-                y4.z = gated_norm_f(o4.z, inv, w4.z, z4.z);
-                y4.w = gated_norm_f(o4.w, inv, w4.w, z4.w);
-            }
-            *reinterpret_cast<float4*>(a.y + base) = y4;
-        }
-        __syncthreads();                         // os, qh, ... are rewritten by the next unit
+    __syncthreads();
+    if (tid < 2 * kDecodeMaxT) {
+        const int pl = tid / kDecodeMaxT, t = tid % kDecodeMaxT;
+        if (t < T) inv_s[pl][t] = l2_inv_f(part[pl][0][t] + part[pl][1][t], a.l2_eps);
     }
-    if (tid == 0 && pending) mbar_wait_bounded(sbar, phase, nullptr);   // drain (bounded)
-}
-
-constexpr size_t kDecDynSmem = 128 + kDecStateBytes + 16;   // alignment, state block, mbarrier
-
-// one instantiation per kernel variant, so that each variant's attribute is set on each device
-template <bool BF16, int GM, int KW>
-static cudaError_t dec_launch(const DecodeArgs& a, cudaStream_t s) {
-    auto kern = kda_decode_fused_kernel<BF16, GM, KW>;
-    static PerDevice<int> attr_done;
-    static PerDevice<int> sm_count;
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    const bool cached = dev >= 0 && dev < kMaxDevices;
-    int sms = cached ? sm_count[dev].load(std::memory_order_acquire) : 0;
-    if (sms == 0) {
-        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        if (e != cudaSuccess) return e;
-        if (cached) sm_count[dev].store(sms, std::memory_order_release);
+    __syncthreads();
+    if (task < 2) {
+        float (*x)[kHeadDim] = task == 0 ? qh : kh;
+        for (int t = 0; t < T; ++t) {
+            const float2 v = *reinterpret_cast<const float2*>(&x[t][i0]);
+            *reinterpret_cast<float2*>(&x[t][i0]) =
+                make_float2(__fmul_rn(v.x, inv_s[task][t]), __fmul_rn(v.y, inv_s[task][t]));
+        }
     }
-    if (!cached || !attr_done[dev].load(std::memory_order_acquire)) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)kDecDynSmem);
-        if (e != cudaSuccess) return e;
-        if (cached) attr_done[dev].store(1, std::memory_order_release);
+    __syncthreads();
+
+    // ---- the recurrence, token by token ---------------------------------------------------
+    {
+        TokView vw;
+        vw.k = &kh[0][0];
+        vw.a = &av[0][0];
+        vw.q = &qh[0][0];
+        vw.a_scal = ascal;
+        vw.v = &vh[0][0];
+        vw.beta = beta_s;
+        vw.out = &os[0][0];
+        vw.row_stride = kHeadDim;
+        vw.v_stride = kHeadDim;
+        vw.v_col0 = cw;
+        vw.out_stride = kHeadDim;
+        vw.out_col0 = cw;
+        col4_tokens<GATE_MODE == 0, false>(S, T, vw, a.scale, r, lane);
     }
-    const long units = (long)a.N * a.H;
-    const int grid = (int)(units < 2L * sms ? units : 2L * sms);   // two resident CTAs per SM
-    KernelTimer kt(kKDecode, s);
-    kern<<<grid, kDecThreads, kDecDynSmem, s>>>(a);
-    return cudaGetLastError();
+    col4_store(S, a.state_out + col0, r);
+    __syncthreads();
+    // ---- epilogue: gated RMSNorm, one warp per token row -----------------------------------
+    for (int t = warp; t < T; t += kDecThreads / 32) {
+        const float4 o4 = *reinterpret_cast<const float4*>(&os[t][4 * lane]);
+        float ss = __fmul_rn(o4.x, o4.x);
+        ss = ss + __fmul_rn(o4.y, o4.y);
+        ss = ss + __fmul_rn(o4.z, o4.z);
+        ss = ss + __fmul_rn(o4.w, o4.w);
+        const float inv = rms_inv_f(warp_sum(ss), a.rms_eps);
+        const long base = (row0 + t) * C + h * kHeadDim + 4 * lane;
+        const float4 w4 = *reinterpret_cast<const float4*>(a.norm_w + 4 * lane);
+        const float4 z4 = *reinterpret_cast<const float4*>(a.gate_raw + base);
+        float4 y4;
+        if (a.norm_silu) {
+            y4.x = gated_norm_f<true>(o4.x, inv, w4.x, z4.x);
+            y4.y = gated_norm_f<true>(o4.y, inv, w4.y, z4.y);
+            y4.z = gated_norm_f<true>(o4.z, inv, w4.z, z4.z);
+            y4.w = gated_norm_f<true>(o4.w, inv, w4.w, z4.w);
+        } else {
+            y4.x = gated_norm_f(o4.x, inv, w4.x, z4.x);
+            y4.y = gated_norm_f(o4.y, inv, w4.y, z4.y);
+            y4.z = gated_norm_f(o4.z, inv, w4.z, z4.z);
+            y4.w = gated_norm_f(o4.w, inv, w4.w, z4.w);
+        }
+        *reinterpret_cast<float4*>(a.y + base) = y4;
+    }
 }
 
 template <bool BF16, int GM>
-static cudaError_t launch_dec_t(const DecodeArgs& a, cudaStream_t s) {
-    if (a.K <= 4) return dec_launch<BF16, GM, 4>(a, s);
-    return dec_launch<BF16, GM, kMaxConvK>(a, s);
+static void launch_dec_t(const DecodeArgs& a, cudaStream_t s) {
+    dim3 grid((unsigned)a.H, (unsigned)a.N);
+    KernelTimer kt(kKDecode, s);
+    if (a.K <= 4) kda_decode_fused_kernel<BF16, GM, 4><<<grid, kDecThreads, 0, s>>>(a);
+    else kda_decode_fused_kernel<BF16, GM, kMaxConvK><<<grid, kDecThreads, 0, s>>>(a);
 }
 
 cudaError_t launch_decode_fused(const DecodeArgs& a, cudaStream_t s) {
     if (a.N == 0 || a.T == 0) return cudaSuccess;
-    if (a.raw_bf16) return a.gate_mode == 0 ? launch_dec_t<true, 0>(a, s) : launch_dec_t<true, 1>(a, s);
-    return a.gate_mode == 0 ? launch_dec_t<false, 0>(a, s) : launch_dec_t<false, 1>(a, s);
+    if (a.raw_bf16) {
+        if (a.gate_mode == 0) launch_dec_t<true, 0>(a, s);
+        else launch_dec_t<true, 1>(a, s);
+    } else {
+        if (a.gate_mode == 0) launch_dec_t<false, 0>(a, s);
+        else launch_dec_t<false, 1>(a, s);
+    }
+    return cudaGetLastError();
 }
 
 }  // namespace kda

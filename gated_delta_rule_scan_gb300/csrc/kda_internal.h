@@ -40,7 +40,23 @@ struct PrepArgs {
     float* q_hat; float* k_hat; float* v_hat; float* g; float* beta;
     SeqLayout seq;
     int H; int K; float l2_eps;
+    int Hk;                  // heads of the q and k planes (grouped queries: value head h reads
+                             // q/k head h % Hk); 0 means H
 };
+
+// Channel layout of the three conv planes under grouped queries: q and k hold Hk heads, v holds H;
+// conv_w rows and ring rows are [q | k | v] = [Hk*D | Hk*D | H*D] (gdn_ops.rs gdn_delta_rule_into
+// doc: q, k are [num_k_heads * head_k_dim], v is [num_v_heads * head_v_dim]).
+__host__ __device__ inline int prep_qk_heads(int H, int Hk) { return Hk > 0 ? Hk : H; }
+__host__ __device__ inline long plane_width(int H, int Hk, int p) {
+    return (long)(p < 2 ? prep_qk_heads(H, Hk) : H) * kHeadDim;
+}
+__host__ __device__ inline long plane_offset(int H, int Hk, int p) {
+    return (long)p * prep_qk_heads(H, Hk) * kHeadDim;
+}
+__host__ __device__ inline long ring_channels(int H, int Hk) {
+    return (2L * prep_qk_heads(H, Hk) + H) * kHeadDim;
+}
 
 struct ScanArgs {
     const float* q; const float* k; const float* v; const float* g; int gate_mode;
@@ -72,6 +88,7 @@ struct DecodeArgs {
     int N; int T; int H; int K; float l2_eps; float scale; float rms_eps;
     const int* keep;         // rollback: tokens of sequence n to take (device [N], clamped to
                              // 0..T; rows keep their stride T), or null for all T
+    int Hk;                  // heads of the q and k planes (grouped queries); 0 means H
     int norm_silu;           // RMSNorm gate: 0 sigmoid (KDA), 1 SiLU (GDN's gated_rmsnorm)
     int* err;                // device error word (bounded waits)
 };

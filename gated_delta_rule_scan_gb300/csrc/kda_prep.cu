@@ -117,6 +117,11 @@ __global__ void __launch_bounds__(kPrepThreads) kda_prep_kernel(PrepArgs a) {
     const int nr = (int)min((long)kRun, rows - r0);
     const int H = a.H;
     const long C = (long)H * kHeadDim;
+    // grouped queries: the q and k planes hold Hk heads (rows Cq wide); the CTAs of heads h < Hk
+    // also compute q/k head h, the others only their v head, gate and beta
+    const long Cq = plane_width(H, a.Hk, 0);
+    const bool has_qk = h < prep_qk_heads(H, a.Hk);
+    const long RC = ring_channels(H, a.Hk);
     const int c = h * kHeadDim + 4 * lane;     // first of this lane's 4 channels in a plane
     const int K = a.K, R = a.K - 1;
 
@@ -129,15 +134,17 @@ __global__ void __launch_bounds__(kPrepThreads) kda_prep_kernel(PrepArgs a) {
 #pragma unroll
             for (int m = 0; m < KW; ++m) {
                 const int j = m - (KW - K);
-                pq.w[e][m] = j >= 0 ? a.conv_w[(0 * C + c + e) * K + j] : 0.0f;
-                pk.w[e][m] = j >= 0 ? a.conv_w[(1 * C + c + e) * K + j] : 0.0f;
-                pv.w[e][m] = j >= 0 ? a.conv_w[(2 * C + c + e) * K + j] : 0.0f;
+                pq.w[e][m] = j >= 0 && has_qk ? a.conv_w[(0 * Cq + c + e) * K + j] : 0.0f;
+                pk.w[e][m] = j >= 0 && has_qk ? a.conv_w[(1 * Cq + c + e) * K + j] : 0.0f;
+                pv.w[e][m] = j >= 0 ? a.conv_w[(2 * Cq + c + e) * K + j] : 0.0f;
             }
         seq_of_row(a.seq, r0, n, begin, end);
-        const long rr = (long)n * 3 * C * R;
-        pw_fill<BF16, KW>(pq, a.q_raw, C, c, a.ring_in, rr + (0 * C + c) * R, R, begin, r0 - begin);
-        pw_fill<BF16, KW>(pk, a.k_raw, C, c, a.ring_in, rr + (1 * C + c) * R, R, begin, r0 - begin);
-        pw_fill<BF16, KW>(pv, a.v_raw, C, c, a.ring_in, rr + (2 * C + c) * R, R, begin, r0 - begin);
+        const long rr = (long)n * RC * R;
+        if (has_qk) {
+            pw_fill<BF16, KW>(pq, a.q_raw, Cq, c, a.ring_in, rr + (0 * Cq + c) * R, R, begin, r0 - begin);
+            pw_fill<BF16, KW>(pk, a.k_raw, Cq, c, a.ring_in, rr + (1 * Cq + c) * R, R, begin, r0 - begin);
+        }
+        pw_fill<BF16, KW>(pv, a.v_raw, C, c, a.ring_in, rr + (2 * Cq + c) * R, R, begin, r0 - begin);
     }
     float rate = 0.0f;
     float4 dt = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
@@ -147,8 +154,9 @@ __global__ void __launch_bounds__(kPrepThreads) kda_prep_kernel(PrepArgs a) {
     }
 
     // row-ahead prefetch of the raw samples and f
-    float4 nq = load_raw4<BF16>(a.q_raw, r0 * C + c);
-    float4 nk = load_raw4<BF16>(a.k_raw, r0 * C + c);
+    const float4 z4 = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    float4 nq = has_qk ? load_raw4<BF16>(a.q_raw, r0 * Cq + c) : z4;
+    float4 nk = has_qk ? load_raw4<BF16>(a.k_raw, r0 * Cq + c) : z4;
     float4 nv = load_raw4<BF16>(a.v_raw, r0 * C + c);
     float4 nf = GATE_MODE == 0 ? *reinterpret_cast<const float4*>(a.f_raw + r0 * C + c)
                                : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
@@ -156,8 +164,10 @@ __global__ void __launch_bounds__(kPrepThreads) kda_prep_kernel(PrepArgs a) {
         const long r = r0 + i;
         const float4 cq = nq, ck = nk, cv = nv, cf = nf;
         if (i + 1 < nr) {
-            nq = load_raw4<BF16>(a.q_raw, (r + 1) * C + c);
-            nk = load_raw4<BF16>(a.k_raw, (r + 1) * C + c);
+            if (has_qk) {
+                nq = load_raw4<BF16>(a.q_raw, (r + 1) * Cq + c);
+                nk = load_raw4<BF16>(a.k_raw, (r + 1) * Cq + c);
+            }
             nv = load_raw4<BF16>(a.v_raw, (r + 1) * C + c);
             if (GATE_MODE == 0) nf = *reinterpret_cast<const float4*>(a.f_raw + (r + 1) * C + c);
         }
@@ -165,16 +175,21 @@ __global__ void __launch_bounds__(kPrepThreads) kda_prep_kernel(PrepArgs a) {
         if constexpr (CONV) {
             if (r >= end) {  // entered the next non-empty sequence: restart the windows
                 seq_of_row(a.seq, r, n, begin, end);
-                const long rr = (long)n * 3 * C * R;
-                pw_fill<BF16, KW>(pq, a.q_raw, C, c, a.ring_in, rr + (0 * C + c) * R, R, begin, 0);
-                pw_fill<BF16, KW>(pk, a.k_raw, C, c, a.ring_in, rr + (1 * C + c) * R, R, begin, 0);
-                pw_fill<BF16, KW>(pv, a.v_raw, C, c, a.ring_in, rr + (2 * C + c) * R, R, begin, 0);
+                const long rr = (long)n * RC * R;
+                if (has_qk) {
+                    pw_fill<BF16, KW>(pq, a.q_raw, Cq, c, a.ring_in, rr + (0 * Cq + c) * R, R, begin, 0);
+                    pw_fill<BF16, KW>(pk, a.k_raw, Cq, c, a.ring_in, rr + (1 * Cq + c) * R, R, begin, 0);
+                }
+                pw_fill<BF16, KW>(pv, a.v_raw, C, c, a.ring_in, rr + (2 * Cq + c) * R, R, begin, 0);
             }
-            pw_push(pq, cq);
-            pw_push(pk, ck);
+            xq = xk = z4;
+            if (has_qk) {
+                pw_push(pq, cq);
+                pw_push(pk, ck);
+                xq = pw_conv_silu(pq, K);
+                xk = pw_conv_silu(pk, K);
+            }
             pw_push(pv, cv);
-            xq = pw_conv_silu(pq, K);
-            xk = pw_conv_silu(pk, K);
             xv = pw_conv_silu(pv, K);
         } else {
             xq = cq;
@@ -182,16 +197,18 @@ __global__ void __launch_bounds__(kPrepThreads) kda_prep_kernel(PrepArgs a) {
             xv = cv;
         }
         *reinterpret_cast<float4*>(a.v_hat + r * C + c) = xv;
-        float sq = __fmul_rn(xq.x, xq.x);
-        sq = fmaf(xq.y, xq.y, sq); sq = fmaf(xq.z, xq.z, sq); sq = fmaf(xq.w, xq.w, sq);
-        float sk = __fmul_rn(xk.x, xk.x);
-        sk = fmaf(xk.y, xk.y, sk); sk = fmaf(xk.z, xk.z, sk); sk = fmaf(xk.w, xk.w, sk);
-        const float iq = l2_inv_f(warp_sum(sq), a.l2_eps);
-        const float ik = l2_inv_f(warp_sum(sk), a.l2_eps);
-        *reinterpret_cast<float4*>(a.q_hat + r * C + c) =
-            make_float4(xq.x * iq, xq.y * iq, xq.z * iq, xq.w * iq);
-        *reinterpret_cast<float4*>(a.k_hat + r * C + c) =
-            make_float4(xk.x * ik, xk.y * ik, xk.z * ik, xk.w * ik);
+        if (has_qk) {
+            float sq = __fmul_rn(xq.x, xq.x);
+            sq = fmaf(xq.y, xq.y, sq); sq = fmaf(xq.z, xq.z, sq); sq = fmaf(xq.w, xq.w, sq);
+            float sk = __fmul_rn(xk.x, xk.x);
+            sk = fmaf(xk.y, xk.y, sk); sk = fmaf(xk.z, xk.z, sk); sk = fmaf(xk.w, xk.w, sk);
+            const float iq = l2_inv_f(warp_sum(sq), a.l2_eps);
+            const float ik = l2_inv_f(warp_sum(sk), a.l2_eps);
+            *reinterpret_cast<float4*>(a.q_hat + r * Cq + c) =
+                make_float4(xq.x * iq, xq.y * iq, xq.z * iq, xq.w * iq);
+            *reinterpret_cast<float4*>(a.k_hat + r * Cq + c) =
+                make_float4(xk.x * ik, xk.y * ik, xk.z * ik, xk.w * ik);
+        }
         if constexpr (GATE_MODE == 0) {
             float4 g = make_float4(kda_gate_f(cf.x, dt.x, rate, a.gate_lb), kda_gate_f(cf.y, dt.y, rate, a.gate_lb),
                                    kda_gate_f(cf.z, dt.z, rate, a.gate_lb), kda_gate_f(cf.w, dt.w, rate, a.gate_lb));
@@ -212,15 +229,16 @@ __global__ void __launch_bounds__(kPrepThreads) kda_prep_kernel(PrepArgs a) {
 // Ring roll, one thread per (sequence, fused channel) (kda_ring.cuh).
 template <bool BF16>
 __global__ void __launch_bounds__(256) kda_ring_roll_kernel(PrepArgs a) {
-    const long C = (long)a.H * kHeadDim;
+    const long Cq = plane_width(a.H, a.Hk, 0);
     const long idx = (long)blockIdx.x * blockDim.x + threadIdx.x;
-    if (idx >= 3 * C) return;
-    ring_roll_one<BF16>(a, blockIdx.y, (int)(idx / C), idx % C);
+    if (idx >= ring_channels(a.H, a.Hk)) return;
+    const int p = idx < Cq ? 0 : (idx < 2 * Cq ? 1 : 2);
+    ring_roll_one<BF16>(a, blockIdx.y, p, idx - plane_offset(a.H, a.Hk, p));
 }
 
 cudaError_t launch_ring_roll(const PrepArgs& a, cudaStream_t s) {
     if (a.conv_w == nullptr || a.seq.N == 0) return cudaSuccess;
-    const long C3 = 3L * a.H * kHeadDim;
+    const long C3 = ring_channels(a.H, a.Hk);
     dim3 grid((unsigned)((C3 + 255) / 256), (unsigned)a.seq.N);
     KernelTimer kt(kKRingRoll, s);
     if (a.raw_bf16) kda_ring_roll_kernel<true><<<grid, 256, 0, s>>>(a);

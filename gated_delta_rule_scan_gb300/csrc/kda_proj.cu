@@ -15,14 +15,16 @@
 // are exact in the product, so the result carries only the f32 accumulation and the split's
 // ~2^-17 relative residue.
 //
-// One CTA per 128-row tile of one weight (the six weights' tiles in one grid), launched as a
-// programmatic dependent of the split pre-pass so that its set-up and first weight loads overlap
-// the split: warp 0's lane 0 streams K-stages of 64 (16 KB of weights plus the x images) through
-// a ring of mbarrier-guarded shared-memory slots, warp 1's lane 0 issues the MMAs and frees each
-// slot with a commit, and all four warps read the accumulator back (TMEM lane = weight row,
-// column = token) and store the outputs, each warp writing 32 consecutive floats per token.  A tile's shared memory stays near
-// 100 KB for t <= 64, so two tiles share an SM and the grid (195 tiles at 64 heads) is resident at
-// once.  Every wait is bounded; a wait that gives up raises the device error word.
+// Two CTAs per 128-row tile of one weight, each on half of K (the six weights' tiles in one grid),
+// launched as a programmatic dependent of the split pre-pass so that its set-up and first weight
+// loads overlap the split: warp 0's lane 0 streams K-stages of 64 (16 KB of weights plus the x
+// images) through a ring of mbarrier-guarded shared-memory slots, warp 1's lane 0 issues the MMAs
+// and frees each slot with a commit, and all four warps read the accumulator back (TMEM lane =
+// weight row, column = token) and add it into the outputs (zeroed by the pre-pass), each warp
+// covering 32 consecutive floats per token.  Exactly two partial sums meet in each output and
+// float addition is commutative, so the result is deterministic.  A CTA's ring stays near 66 KB
+// for t <= 64, so three CTAs share an SM and the grid (390 CTAs at 64 heads) is resident at once.
+// Every wait is bounded; a wait that gives up raises the device error word.
 #include <cuda_bf16.h>
 
 #include "kda_device.cuh"
@@ -37,7 +39,8 @@ constexpr int kPRows = 128;                    // weight rows per tile = MMA M =
 constexpr int kPK = 64;                        // K per stage: one 128-byte swizzle row of bf16
 constexpr int kPThreads = 128;
 constexpr int kPStageW = kPRows * kPK * 2;     // 16 KB of weights per stage
-constexpr int kPSmemTarget = 100 * 1024;       // stage ring budget: two tiles per SM up to t = 64
+constexpr int kPSmemTarget = 66 * 1024;        // stage ring budget: three CTAs per SM up to t = 64
+constexpr int kPKSplit = 2;                    // CTAs per weight tile, each on half of K
 
 struct Proj6Maps {
     CUtensorMap w[6];
@@ -47,7 +50,7 @@ struct Proj6Maps {
 struct Proj6Params {
     float* out[6];
     int rows[6];
-    int tile_start[7];      // first tile of each weight; tile_start[6] = the grid
+    int tile_start[7];      // first tile of each weight; tile_start[6] = the tiles
     int t, t_pad, in_f;
     int stages;
     uint32_t tmem_cols;
@@ -55,16 +58,18 @@ struct Proj6Params {
 };
 
 // x [t, in_f] f32 -> hi, lo [t_pad, in_f] bf16 with hi + lo ~= x; rows t .. t_pad-1 are zero.
-__global__ void __launch_bounds__(256) kda_proj_split_kernel(const float* __restrict__ x, int t,
-                                                             int t_pad, int in_f,
+// Also zeroes the six outputs, which the projection kernel's two K halves then add into.
+__global__ void __launch_bounds__(256) kda_proj_split_kernel(const float* __restrict__ x,
                                                              __nv_bfloat16* __restrict__ hi,
-                                                             __nv_bfloat16* __restrict__ lo) {
+                                                             __nv_bfloat16* __restrict__ lo,
+                                                             const __grid_constant__ Proj6Params p) {
     // the projection kernel may start now: it loads weights until it needs these images
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    const long n4 = (long)t_pad * in_f / 4;
-    const long live4 = (long)t * in_f / 4;
-    for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < n4;
-         i += (long)gridDim.x * blockDim.x) {
+    const long n4 = (long)p.t_pad * p.in_f / 4;
+    const long live4 = (long)p.t * p.in_f / 4;
+    const long stride = (long)gridDim.x * blockDim.x;
+    const long i0 = blockIdx.x * (long)blockDim.x + threadIdx.x;
+    for (long i = i0; i < n4; i += stride) {
         float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
         if (i < live4) v = __ldg(reinterpret_cast<const float4*>(x) + i);
         uint2 h, l;
@@ -72,6 +77,11 @@ __global__ void __launch_bounds__(256) kda_proj_split_kernel(const float* __rest
         split_bf16x2(v.z, v.w, h.y, l.y);
         reinterpret_cast<uint2*>(hi)[i] = h;
         reinterpret_cast<uint2*>(lo)[i] = l;
+    }
+#pragma unroll 1
+    for (int w = 0; w < 6; ++w) {
+        const long n = (long)p.t * p.rows[w];
+        for (long i = i0; i < n; i += stride) p.out[w][i] = 0.0f;
     }
 }
 
@@ -88,10 +98,13 @@ kda_proj6_kernel(const __grid_constant__ Proj6Maps maps, const __grid_constant__
     uint64_t* done = empty + p.stages;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
 
+    // CTA pair (2 tile, 2 tile + 1): the tile's two K halves
+    const int tile = (int)blockIdx.x / kPKSplit, half = (int)blockIdx.x % kPKSplit;
     int wi = 0;
-    while (wi < 5 && (int)blockIdx.x >= p.tile_start[wi + 1]) ++wi;
-    const int row0 = ((int)blockIdx.x - p.tile_start[wi]) * kPRows;
-    const int nk = p.in_f / kPK;
+    while (wi < 5 && tile >= p.tile_start[wi + 1]) ++wi;
+    const int row0 = (tile - p.tile_start[wi]) * kPRows;
+    const int nk = p.in_f / kPK / kPKSplit;       // K-stages of this CTA
+    const int kb0 = half * nk;                     // its first K-stage of the weight rows
 
     if (warp == 0) {
         tmem_alloc(tmem_slot, p.tmem_cols);
@@ -121,20 +134,21 @@ kda_proj6_kernel(const __grid_constant__ Proj6Maps maps, const __grid_constant__
         const int first = nk < p.stages ? nk : p.stages;
         for (int kb = 0; kb < first; ++kb) {
             mbar_arrive_expect_tx(&full[kb], (uint32_t)stage_bytes);
-            tma_load_2d(base + kb * stage_bytes, &maps.w[wi], kb * kPK, row0, &full[kb]);
+            tma_load_2d(base + kb * stage_bytes, &maps.w[wi], (kb0 + kb) * kPK, row0, &full[kb]);
         }
         asm volatile("griddepcontrol.wait;" ::: "memory");
         for (int kb = 0; kb < nk; ++kb) {
             const int s = kb % p.stages;
             unsigned char* st = base + s * stage_bytes;
+            const int kx = (kb0 + kb) * kPK;
             if (kb >= first) {
                 if (!mbar_wait_bounded(&empty[s], (uint32_t)(((kb / p.stages) & 1) ^ 1), p.err))
                     break;
                 mbar_arrive_expect_tx(&full[s], (uint32_t)stage_bytes);
-                tma_load_2d(st, &maps.w[wi], kb * kPK, row0, &full[s]);
+                tma_load_2d(st, &maps.w[wi], kx, row0, &full[s]);
             }
-            tma_load_2d(st + kPStageW, &maps.xh, kb * kPK, 0, &full[s]);
-            tma_load_2d(st + kPStageW + stage_x, &maps.xl, kb * kPK, 0, &full[s]);
+            tma_load_2d(st + kPStageW, &maps.xh, kx, 0, &full[s]);
+            tma_load_2d(st + kPStageW + stage_x, &maps.xl, kx, 0, &full[s]);
         }
     } else if (tid == 32) {
         // MMA issuer: D[row][token] += W[row][k] * (hi + lo)[token][k], four K-steps per stage
@@ -160,7 +174,9 @@ kda_proj6_kernel(const __grid_constant__ Proj6Maps maps, const __grid_constant__
     const bool ok = mbar_wait_bounded(done, 0, p.err);
     tc_fence_after();
 
-    // epilogue: thread (warp w, lane l) owns weight row row0 + 32 w + l
+    // epilogue: thread (warp w, lane l) owns weight row row0 + 32 w + l and adds its K half's
+    // partial sums into the zeroed outputs.  Two partials meet in each output element, and
+    // (0 + a) + b == (0 + b) + a exactly, so the result does not depend on which half lands first.
     const int rows = p.rows[wi];
     const int row = row0 + 32 * warp + lane;
     float* out = p.out[wi];
@@ -172,7 +188,7 @@ kda_proj6_kernel(const __grid_constant__ Proj6Maps maps, const __grid_constant__
         if (ok && row < rows) {
 #pragma unroll
             for (int j = 0; j < 16; ++j)
-                if (n0 + j < p.t) out[(long)(n0 + j) * rows + row] = v[j];
+                if (n0 + j < p.t) atomicAdd(out + (long)(n0 + j) * rows + row, v[j]);
         }
     }
     tc_fence_before();
@@ -208,6 +224,7 @@ cudaError_t launch_proj6(const Proj6Args& a, cudaStream_t s) {
     const int stage_bytes = kPStageW + 2 * t_pad * kPK * 2;
     int stages = kPSmemTarget / stage_bytes;
     stages = stages < 2 ? 2 : (stages > 6 ? 6 : stages);
+    if (stages > a.in_f / kPK / kPKSplit) stages = a.in_f / kPK / kPKSplit < 2 ? 2 : a.in_f / kPK / kPKSplit;
     p.stages = stages;
     uint32_t cols = 32;
     while ((int)cols < t_pad) cols <<= 1;
@@ -218,7 +235,7 @@ cudaError_t launch_proj6(const Proj6Args& a, cudaStream_t s) {
         const long n4 = (long)t_pad * a.in_f / 4;
         const int blocks = (int)((n4 + 255) / 256 < 1024 ? (n4 + 255) / 256 : 1024);
         KernelTimer kt(kKProjSplit, s);
-        kda_proj_split_kernel<<<blocks, 256, 0, s>>>(a.x, a.t, t_pad, a.in_f, xh, xl);
+        kda_proj_split_kernel<<<blocks, 256, 0, s>>>(a.x, xh, xl, p);
         const cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
@@ -242,7 +259,7 @@ cudaError_t launch_proj6(const Proj6Args& a, cudaStream_t s) {
     // launched as a programmatic dependent of the split kernel: its CTAs may start (and stream
     // weights) while the split is still running
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)tiles);
+    cfg.gridDim = dim3((unsigned)(tiles * kPKSplit));
     cfg.blockDim = dim3(kPThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;

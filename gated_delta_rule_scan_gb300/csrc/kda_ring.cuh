@@ -9,12 +9,13 @@
 
 namespace kda {
 
-// ring_out[n][p C + c][s] = xt[L_n + s] for s < K-1, where xt = (ring_in[n][p C + c][0 .. K-2],
-// plane p's raw rows of sequence n) and L_n its length.  Every old slot is read before any is
-// written, so the roll is safe in place (ring_out == ring_in).
+// ring_out[n][off_p + c][s] = xt[L_n + s] for s < K-1, where xt = (ring_in[n][off_p + c][0 .. K-2],
+// plane p's raw rows of sequence n), L_n its length and off_p the plane's first ring row (q, k of
+// Hk heads, then v of H heads).  Every old slot is read before any is written, so the roll is safe
+// in place (ring_out == ring_in).
 template <bool BF16>
 __device__ __forceinline__ void ring_roll_one(const PrepArgs& a, int n, int p, long c) {
-    const long C = (long)a.H * kHeadDim;
+    const long C = plane_width(a.H, a.Hk, p);          // row width of plane p's raw rows
     const int R = a.K - 1;
     long begin, end;
     if (a.seq.cu_seqlens == nullptr) {
@@ -26,7 +27,7 @@ __device__ __forceinline__ void ring_roll_one(const PrepArgs& a, int n, int p, l
     }
     const long Ln = end - begin;
     const void* raw = p == 0 ? a.q_raw : (p == 1 ? a.k_raw : a.v_raw);
-    const long base = ((long)n * 3 * C + p * C + c) * R;
+    const long base = ((long)n * ring_channels(a.H, a.Hk) + plane_offset(a.H, a.Hk, p) + c) * R;
     float old[kMaxConvK - 1];
 #pragma unroll
     for (int s2 = 0; s2 < kMaxConvK - 1; ++s2) old[s2] = s2 < R ? a.ring_in[base + s2] : 0.0f;

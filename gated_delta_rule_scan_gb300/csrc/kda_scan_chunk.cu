@@ -388,7 +388,10 @@ kda_chunk_inter_kernel(ScanArgs a, const int* chunk_off, const unsigned char* ws
     // the fused prefill's conv ring roll of this (sequence, head) while the first MMA-1 runs (the
     // prep kernel that read ring_in has finished)
     if (ring.conv_w != nullptr) {
-        for (int i = tid; i < 3 * kHeadDim; i += kThrInter) {
+        // grouped queries: the q and k ring rows of head h exist (and are rolled here) only for
+        // h < Hk; every value head rolls its v rows
+        const int p0 = h < prep_qk_heads(ring.H, ring.Hk) ? 0 : 2;
+        for (int i = tid + p0 * kHeadDim; i < 3 * kHeadDim; i += kThrInter) {
             const int p = i / kHeadDim;
             const long c = (long)h * kHeadDim + i % kHeadDim;
             if (ring.raw_bf16) ring_roll_one<true>(ring, n, p, c);

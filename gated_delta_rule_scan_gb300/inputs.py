@@ -56,6 +56,7 @@ class KdaInputs:
     gate_mode: int                    # 0 = per-channel (KDA), 1 = per-head (GDN)
     split_points: np.ndarray | None = None
     meta: dict = field(default_factory=dict)
+    Hk: int | None = None             # grouped queries: q/k planes of Hk heads (None: H)
 
     @property
     def rows(self) -> int:
@@ -83,11 +84,14 @@ def make_inputs(seed: int, *, H: int, N: int = 1, T: int | None = None,
                 lengths: tuple[int, int] | None = None, D: int = D_HEAD, K: int = CONV_K,
                 raw_dtype: str = "f32", conv: bool = True, ring: str = "zero",
                 gate_mode: int = 0, state: str = "zero", epilogue: bool = True,
-                split: bool = False) -> KdaInputs:
+                split: bool = False, Hk: int | None = None) -> KdaInputs:
     """Draw one workload.  Exactly one of ``T`` (N sequences of T tokens) and ``lengths``
-    (N sequence lengths drawn uniformly from [lo, hi], packed with cu_seqlens) is given."""
+    (N sequence lengths drawn uniformly from [lo, hi], packed with cu_seqlens) is given.
+    ``Hk``: grouped queries -- the q and k planes (and their conv weight and ring rows) hold Hk
+    heads, v and everything per value head H."""
     rng = np.random.default_rng(seed)
     C = H * D
+    Cq = C if Hk is None else Hk * D
     if lengths is not None:
         L = rng.integers(lengths[0], lengths[1], size=N, endpoint=True).astype(np.int64)
     else:
@@ -96,16 +100,16 @@ def make_inputs(seed: int, *, H: int, N: int = 1, T: int | None = None,
     cu[1:] = np.cumsum(L)
     rows = int(cu[-1])
 
-    planes = [_normal(rng, (rows, C)) for _ in range(3)]
+    planes = [_normal(rng, (rows, w)) for w in (Cq, Cq, C)]
     if raw_dtype == "bf16":
         planes = [p.to(torch.bfloat16) for p in planes]
     elif raw_dtype != "f32":
         raise ValueError(raw_dtype)
     conv_w = ring_in = None
     if conv:
-        conv_w = _normal(rng, (3 * C, K), 0.5)
-        ring_in = (_normal(rng, (N, 3 * C, K - 1)) if ring == "randn"
-                   else torch.zeros(N, 3 * C, K - 1))
+        conv_w = _normal(rng, (2 * Cq + C, K), 0.5)
+        ring_in = (_normal(rng, (N, 2 * Cq + C, K - 1)) if ring == "randn"
+                   else torch.zeros(N, 2 * Cq + C, K - 1))
     if gate_mode == 0:
         f_raw = _normal(rng, (rows, C))
         dt_bias = _normal(rng, (C,), 0.5)
@@ -128,7 +132,7 @@ def make_inputs(seed: int, *, H: int, N: int = 1, T: int | None = None,
                      v_raw=planes[2], conv_w=conv_w, ring_in=ring_in, f_raw=f_raw,
                      dt_bias=dt_bias, a_log=a_log, beta_raw=beta_raw, state_in=state_in,
                      norm_w=norm_w, gate_raw=gate_raw, gate_mode=gate_mode, split_points=splits,
-                     meta=dict(seed=seed, raw_dtype=raw_dtype))
+                     meta=dict(seed=seed, raw_dtype=raw_dtype), Hk=Hk)
 
 
 # ------------------------------------------------------------------------------------------

@@ -26,7 +26,7 @@ def kda_forward(*, q_raw, k_raw, v_raw, f_raw, dt_bias, a_log, beta_raw, state_i
                 cu_seqlens_host=None, N=None, T=None, K=4, gate_mode=0, gate_lb=-5.0,
                 l2_eps=1e-6, rms_eps=1e-6, scale=None, algo=kda.ALGO_AUTO, state_out=None,
                 ring_out=None, out=None, gate_exp=None, workspace=None, stream=None,
-                norm_gate="sigmoid"):
+                norm_gate="sigmoid", Hk=None):
     """Run the mixer on device tensors.  Either (N, T) for N sequences of T tokens, or
     cu_seqlens (int32 device) + cu_seqlens_host (int32 CPU) for packed sequences.
     gate_exp: hand the gate from the prep to the scan as decay factors exp(log-decay) (the
@@ -36,10 +36,12 @@ def kda_forward(*, q_raw, k_raw, v_raw, f_raw, dt_bias, a_log, beta_raw, state_i
     workspace: scratch for the chunked form; allocated here when algo is AUTO or CHUNK and none
     is given.
     norm_gate: the RMSNorm's gate, "sigmoid" (KDA) or "silu" (GDN's gated_rmsnorm).
+    Hk: grouped queries (q_raw / k_raw of Hk heads, value head h reads q/k head h % Hk).
     Returns a dict with q_hat, k_hat, v_hat, g, beta, o, y (None without an epilogue),
     state_out and ring_out."""
     D = kda.HEAD_DIM
     C = H * D
+    Cq = (H if Hk is None else Hk) * D
     rows = q_raw.shape[0]
     varlen = cu_seqlens is not None
     if not varlen:
@@ -50,8 +52,8 @@ def kda_forward(*, q_raw, k_raw, v_raw, f_raw, dt_bias, a_log, beta_raw, state_i
     def take(name, shape):
         t = buf.get(name)
         return t if t is not None else _empty(shape, q_raw)
-    q_hat = take("q_hat", (rows, C))
-    k_hat = take("k_hat", (rows, C))
+    q_hat = take("q_hat", (rows, Cq))
+    k_hat = take("k_hat", (rows, Cq))
     v_hat = take("v_hat", (rows, C))
     g = take("g", (rows, C) if gate_mode == 0 else (rows, H))
     beta = take("beta", (rows, H))
@@ -65,20 +67,27 @@ def kda_forward(*, q_raw, k_raw, v_raw, f_raw, dt_bias, a_log, beta_raw, state_i
     if gate_exp is None:
         gate_exp = algo == kda.ALGO_SEQ
     gm = gate_mode | (kda.GATE_EXP if gate_exp else 0)
-    common = dict(H=H, K=K, gate_mode=gm, gate_lb=gate_lb, l2_eps=l2_eps, stream=stream)
+    common = dict(H=H, K=K, gate_mode=gm, gate_lb=gate_lb, l2_eps=l2_eps, stream=stream, Hk=Hk)
+    scan_kw = dict(H=H, gate_mode=gm, scale=scale, algo=algo, workspace=workspace, stream=stream)
     if varlen:
         kda.kda_conv_l2norm_prep_varlen(q_raw, k_raw, v_raw, conv_w, ring_in, ring_out, f_raw,
                                         dt_bias, a_log, beta_raw, q_hat, k_hat, v_hat, g, beta,
                                         cu_seqlens, cu_seqlens_host, **common)
-        kda.kda_scan_varlen(q_hat, k_hat, v_hat, g, beta, state_in, state_out, o, cu_seqlens,
-                            cu_seqlens_host, H=H, gate_mode=gm, scale=scale, algo=algo,
-                            workspace=workspace, stream=stream)
+        scan_args = (q_hat, k_hat, v_hat, g, beta, state_in, state_out, o, cu_seqlens,
+                     cu_seqlens_host)
+        if Hk is None:
+            kda.kda_scan_varlen(*scan_args, **scan_kw)
+        else:
+            kda.kda_scan_varlen_gqa(*scan_args, Hk=Hk, **scan_kw)
     else:
         kda.kda_conv_l2norm_prep(q_raw, k_raw, v_raw, conv_w, ring_in, ring_out, f_raw, dt_bias,
                                  a_log, beta_raw, q_hat, k_hat, v_hat, g, beta, N=N, T=T,
                                  **common)
-        kda.kda_scan(q_hat, k_hat, v_hat, g, beta, state_in, state_out, o, N=N, T=T, H=H,
-                     gate_mode=gm, scale=scale, algo=algo, workspace=workspace, stream=stream)
+        scan_args = (q_hat, k_hat, v_hat, g, beta, state_in, state_out, o)
+        if Hk is None:
+            kda.kda_scan(*scan_args, N=N, T=T, **scan_kw)
+        else:
+            kda.kda_scan_gqa(*scan_args, N=N, T=T, Hk=Hk, **scan_kw)
     y = None
     if norm_w is not None:
         y = take("y", (rows, C))
@@ -93,7 +102,7 @@ def kda_prefill(*, q_raw, k_raw, v_raw, f_raw, dt_bias, a_log, beta_raw, state_i
                 ring_in, norm_w, gate_raw, cu_seqlens=None, cu_seqlens_host=None, N=None, T=None,
                 K=4, gate_mode=0, gate_lb=-5.0, l2_eps=1e-6, rms_eps=1e-6, scale=None,
                 state_out=None, ring_out=None, y=None, workspace=None, stream=None,
-                norm_gate="sigmoid"):
+                norm_gate="sigmoid", Hk=None):
     """The whole mixer for a prefill in one library call (kda_prefill_fused[_varlen]): conv +
     SiLU, l2 norm, gates, the chunked scan and the gated RMSNorm, the intermediates kept in the
     workspace.  Either (N, T) or cu_seqlens (int32 device) + cu_seqlens_host (int32
@@ -117,7 +126,7 @@ def kda_prefill(*, q_raw, k_raw, v_raw, f_raw, dt_bias, a_log, beta_raw, state_i
     args = (q_raw, k_raw, v_raw, conv_w, ring_in, ring_out, f_raw, dt_bias, a_log, beta_raw,
             state_in, state_out, norm_w, gate_raw, y, workspace)
     common = dict(H=H, K=K, gate_mode=gate_mode | _norm_flag(norm_gate), gate_lb=gate_lb,
-                  l2_eps=l2_eps, scale=scale, rms_eps=rms_eps, stream=stream)
+                  l2_eps=l2_eps, scale=scale, rms_eps=rms_eps, stream=stream, Hk=Hk)
     if varlen:
         kda.kda_prefill_fused_varlen(*args, cu_seqlens, cu_seqlens_host, **common)
     else:
@@ -128,7 +137,7 @@ def kda_prefill(*, q_raw, k_raw, v_raw, f_raw, dt_bias, a_log, beta_raw, state_i
 def kda_decode(*, q_raw, k_raw, v_raw, conv_w, ring_in, f_raw, dt_bias, a_log, beta_raw,
                state_in, norm_w, gate_raw, N, T, H, K=4, gate_mode=0, gate_lb=-5.0,
                l2_eps=1e-6, rms_eps=1e-6, scale=None, state_out=None, ring_out=None, y=None,
-               stream=None, norm_gate="sigmoid"):
+               stream=None, norm_gate="sigmoid", Hk=None):
     """One fused decode (T=1) or T-token verify launch.  ring_out may be ring_in and state_out
     state_in (in place).  norm_gate: "sigmoid" (KDA) or "silu" (GDN's gated_rmsnorm)."""
     if state_out is None:
@@ -141,14 +150,14 @@ def kda_decode(*, q_raw, k_raw, v_raw, conv_w, ring_in, f_raw, dt_bias, a_log, b
                          beta_raw, state_in, state_out, norm_w, gate_raw, y, N=N, T=T, H=H, K=K,
                          gate_mode=gate_mode | _norm_flag(norm_gate), gate_lb=gate_lb,
                          l2_eps=l2_eps, scale=scale,
-                         rms_eps=rms_eps, stream=stream)
+                         rms_eps=rms_eps, stream=stream, Hk=Hk)
     return dict(y=y, state_out=state_out, ring_out=ring_out)
 
 
 def kda_verify_rollback(*, q_raw, k_raw, v_raw, conv_w, ring_in, f_raw, dt_bias, a_log,
                         beta_raw, state_in, norm_w, gate_raw, keep, N, T, H, K=4, gate_mode=0,
                         gate_lb=-5.0, l2_eps=1e-6, rms_eps=1e-6, scale=None, state_out=None,
-                        ring_out=None, y=None, stream=None, norm_gate="sigmoid"):
+                        ring_out=None, y=None, stream=None, norm_gate="sigmoid", Hk=None):
     """Roll a T-token verify round back to the accepted prefixes: keep (int32 device [N]) tokens
     of each sequence, from the pre-round state_in and ring_in.  ring_out may be ring_in."""
     if state_out is None:
@@ -162,7 +171,7 @@ def kda_verify_rollback(*, q_raw, k_raw, v_raw, conv_w, ring_in, f_raw, dt_bias,
                             a_log, beta_raw, state_in, state_out, norm_w, gate_raw, y, keep,
                             N=N, T=T, H=H, K=K, gate_mode=gate_mode | _norm_flag(norm_gate),
                             gate_lb=gate_lb, l2_eps=l2_eps, scale=scale, rms_eps=rms_eps,
-                            stream=stream)
+                            stream=stream, Hk=Hk)
     return dict(y=y, state_out=state_out, ring_out=ring_out)
 
 

@@ -375,6 +375,68 @@ int kda_verify_rollback(const void* q_raw, const void* k_raw, const void* v_raw,
                         int D, int K, float l2_eps, float scale, float rms_eps, void* stream);
 
 /*
+ * Grouped queries through the whole mixer (the GDN page's head mapping, aprender-serve gdn_ops.rs
+ * `gdn_delta_rule_into` doc: q and k hold num_k_heads heads and value head h reads query/key head
+ * h % num_k_heads; beta and the gate are per value head).  Each entry equals the entry without the
+ * suffix, with Hk (1 <= Hk <= H, 40005 otherwise) q/k heads:
+ *   q_raw, k_raw  [rows, Hk*D] (the staged prep's q_hat, k_hat outputs likewise; they feed
+ *                 kda_scan_gqa / kda_scan_varlen_gqa);
+ *   v_raw, f_raw, gate_raw, y, the state, beta: H value heads as before;
+ *   conv_w        [2*Hk*D + H*D, K], rows [q | k | v];  ring [N, 2*Hk*D + H*D, K-1], same order.
+ * Hk == H is the entry without the suffix.  kda_decode_fused_gqa and kda_verify_rollback_gqa with
+ * Hk < H cannot roll the ring in place (several value heads read one q/k ring row that only one of
+ * them rewrites): ring_in == ring_out returns 40003 there.
+ */
+int kda_conv_l2norm_prep_gqa(const void* q_raw, const void* k_raw, const void* v_raw,
+                             int raw_dtype, const float* conv_w, const float* ring_in,
+                             float* ring_out, const float* f_raw, const float* dt_bias,
+                             const float* a_log, int gate_mode, float gate_lb,
+                             const float* beta_raw, float* q_hat, float* k_hat, float* v_hat,
+                             float* g, float* beta, int N, int T, int H, int Hk, int D, int K,
+                             float l2_eps, void* stream);
+int kda_conv_l2norm_prep_varlen_gqa(const void* q_raw, const void* k_raw, const void* v_raw,
+                                    int raw_dtype, const float* conv_w, const float* ring_in,
+                                    float* ring_out, const float* f_raw, const float* dt_bias,
+                                    const float* a_log, int gate_mode, float gate_lb,
+                                    const float* beta_raw, float* q_hat, float* k_hat,
+                                    float* v_hat, float* g, float* beta, const int* cu_seqlens,
+                                    const int* cu_seqlens_host, int N, int total_T, int H,
+                                    int Hk, int D, int K, float l2_eps, void* stream);
+int kda_prefill_fused_gqa(const void* q_raw, const void* k_raw, const void* v_raw, int raw_dtype,
+                          const float* conv_w, const float* ring_in, float* ring_out,
+                          const float* f_raw, const float* dt_bias, const float* a_log,
+                          int gate_mode, float gate_lb, const float* beta_raw,
+                          const float* state_in, float* state_out, const float* norm_w,
+                          const float* gate_raw, float* y, int N, int T, int H, int Hk, int D,
+                          int K, float l2_eps, float scale, float rms_eps, void* workspace,
+                          size_t workspace_bytes, void* stream);
+int kda_prefill_fused_varlen_gqa(const void* q_raw, const void* k_raw, const void* v_raw,
+                                 int raw_dtype, const float* conv_w, const float* ring_in,
+                                 float* ring_out, const float* f_raw, const float* dt_bias,
+                                 const float* a_log, int gate_mode, float gate_lb,
+                                 const float* beta_raw, const float* state_in, float* state_out,
+                                 const float* norm_w, const float* gate_raw, float* y,
+                                 const int* cu_seqlens, const int* cu_seqlens_host, int N,
+                                 int total_T, int H, int Hk, int D, int K, float l2_eps,
+                                 float scale, float rms_eps, void* workspace,
+                                 size_t workspace_bytes, void* stream);
+int kda_decode_fused_gqa(const void* q_raw, const void* k_raw, const void* v_raw, int raw_dtype,
+                         const float* conv_w, const float* ring_in, float* ring_out,
+                         const float* f_raw, const float* dt_bias, const float* a_log,
+                         int gate_mode, float gate_lb, const float* beta_raw,
+                         const float* state_in, float* state_out, const float* norm_w,
+                         const float* gate_raw, float* y, int N, int T, int H, int Hk, int D, int K,
+                         float l2_eps, float scale, float rms_eps, void* stream);
+int kda_verify_rollback_gqa(const void* q_raw, const void* k_raw, const void* v_raw,
+                            int raw_dtype, const float* conv_w, const float* ring_in,
+                            float* ring_out, const float* f_raw, const float* dt_bias,
+                            const float* a_log, int gate_mode, float gate_lb,
+                            const float* beta_raw, const float* state_in, float* state_out,
+                            const float* norm_w, const float* gate_raw, float* y, const int* keep,
+                            int N, int T, int H, int Hk, int D, int K, float l2_eps, float scale,
+                            float rms_eps, void* stream);
+
+/*
  * kda_proj6 -- stage 1 of kda_core_gated: the six projections of the layer input that the mixer
  * reads, in one call (Engine::kda_proj_fused6, its bf16-weight arm; the shapes are the
  * KdaAttnLayer field docs of "memra_engine/kda.rs"): for every token row s < t,

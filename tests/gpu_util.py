@@ -41,6 +41,8 @@ def gpu_forward(inp: KdaInputs, *, varlen=None, algo=0, **kw):
         extra = dict(cu_seqlens=cu_h.to("cuda"), cu_seqlens_host=cu_h)
     else:
         extra = dict(N=inp.N, T=T)
+    if inp.Hk is not None:
+        kw = dict(kw, Hk=inp.Hk)
     out = mixer.kda_forward(H=inp.H, K=inp.K, gate_mode=inp.gate_mode, algo=algo, **d, **extra,
                             **kw)
     torch.cuda.synchronize()
@@ -59,6 +61,8 @@ def gpu_prefill(inp: KdaInputs, *, varlen=None, **kw):
         extra = dict(cu_seqlens=cu_h.to("cuda"), cu_seqlens_host=cu_h)
     else:
         extra = dict(N=inp.N, T=T)
+    if inp.Hk is not None:
+        kw = dict(kw, Hk=inp.Hk)
     out = mixer.kda_prefill(H=inp.H, K=inp.K, gate_mode=inp.gate_mode, **d, **extra, **kw)
     torch.cuda.synchronize()
     return out
@@ -69,9 +73,17 @@ def head_channels(heads, D=128):
 
 
 def oracle_forward(inp: KdaInputs, heads=None, **kw):
-    """The f64 oracle on the workload (all heads, or the listed ones)."""
+    """The f64 oracle on the workload (all heads, or the listed ones; grouped-query workloads
+    run on all heads)."""
     from oracle import oracle as orc
     H, D = inp.H, inp.D
+    if inp.Hk is not None:
+        assert heads is None or list(heads) == list(range(H)), "grouped queries: all heads"
+        return orc.forward(
+            q_raw=inp.q_raw, k_raw=inp.k_raw, v_raw=inp.v_raw, f_raw=inp.f_raw,
+            dt_bias=inp.dt_bias, a_log=inp.a_log, beta_raw=inp.beta_raw, state_in=inp.state_in,
+            H=H, D=D, conv_w=inp.conv_w, ring_in=inp.ring_in, cu_seqlens=inp.cu_seqlens,
+            gate_mode=inp.gate_mode, norm_w=inp.norm_w, gate_raw=inp.gate_raw, Hk=inp.Hk, **kw)
     heads = list(range(H)) if heads is None else list(heads)
     ch = head_channels(heads, D)
     C = H * D
@@ -103,11 +115,24 @@ def check_all_heads(out, inp: KdaInputs, keys, tol=TOL, ring_exact=True, budget=
     bit-equal.  Returns the errors per key."""
     H, D = inp.H, inp.D
     rows = max(inp.rows, 1)
-    per_head = rows * D * 8 * 16            # about sixteen f64 [rows, D] planes per head
-    group = max(1, min(H, budget // per_head))
     host = {}
     for k in keys:
         host[k] = out[k].detach().cpu() if isinstance(out[k], torch.Tensor) else out[k]
+    if inp.Hk is not None:                   # grouped queries: one oracle run over every head
+        ref = oracle_forward(inp, **kw)
+        errs = {}
+        for k in keys:
+            g = host[k].double().numpy()
+            assert g.shape == ref[k].shape, (k, g.shape, ref[k].shape)
+            if k == "ring_out" and ring_exact:
+                assert np.array_equal(g, ref[k]), "ring_out not bit-equal"
+                errs[k] = 0.0
+            else:
+                errs[k] = rel_linf(g, ref[k])
+        assert max(errs.values()) <= tol, errs
+        return errs
+    per_head = rows * D * 8 * 16            # about sixteen f64 [rows, D] planes per head
+    group = max(1, min(H, budget // per_head))
     num = {k: 0.0 for k in keys}
     den = {k: 0.0 for k in keys}
     C = H * D
