@@ -774,6 +774,8 @@ def run_ours(args):
                                "frac": proj_bytes / (proj_ms / 1e3) / 1e9 / peaks["hbm_gbs"],
                                "bytes_per_launch": proj_bytes,
                                "weight_bytes": proj_w_bytes,
+                               "traffic": _traffic("kda_proj6_kernel",
+                                                   KERNEL_SOURCES["kda_proj6_kernel"]),
                                "bytes": "bf16 weights read once, x read and the six outputs "
                                         "written once (the x hi/lo images are intermediates)"}},
         "clocks": clocks,
