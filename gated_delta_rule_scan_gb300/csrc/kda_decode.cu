@@ -20,6 +20,21 @@ namespace kda {
 
 constexpr int kDecThreads = 256;
 
+// Asynchronous 4- or 8-byte copies global -> shared (cp.async, completion waited per thread).
+__device__ __forceinline__ void cp_async_4(void* dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)),
+                 "l"(reinterpret_cast<uint64_t>(src))
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_8(void* dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_u32(dst)),
+                 "l"(reinterpret_cast<uint64_t>(src))
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit_wait() {
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_all;" ::: "memory");
+}
+
 // KW: register window width of the conv (4 when K <= 4, else 8).
 template <bool BF16, int GATE_MODE, int KW>
 __global__ void __launch_bounds__(kDecThreads, 2) kda_decode_fused_kernel(DecodeArgs a) {
@@ -49,14 +64,31 @@ __global__ void __launch_bounds__(kDecThreads, 2) kda_decode_fused_kernel(Decode
     Col4 S;
     col4_load(S, a.state_in + col0, r);
 
-    // ---- prologue: 64 threads per task, each on a channel pair (2i, 2i+1) --------------------
-    //      threads 0-63 q plane, 64-127 k plane, 128-191 v plane (+ beta), 192-255 the gate.
-    //      Grouped queries: the q and k planes hold Hk heads and this value head reads q/k head
-    //      h % Hk; only the CTAs of heads h < Hk write those heads' ring rows.
+    // ---- the prologue's per-token rows, all T at once: each thread copies its channel pair of
+    //      every token into the slot its result will take (raw q / k / v into qh / kh / vh, the
+    //      gate input into av), so the token loop below waits on no global load
     const int task = tid >> 6, i0 = 2 * (tid & 63);
     const int c = h * kHeadDim + i0;
     if (task < 3) {
         const void* raw = task == 0 ? a.q_raw : (task == 1 ? a.k_raw : a.v_raw);
+        const long Cp = plane_width(H, a.Hk, task);
+        const int cp = (task < 2 ? h % prep_qk_heads(H, a.Hk) : h) * kHeadDim + i0;
+        float (*dst)[kHeadDim] = task == 0 ? qh : (task == 1 ? kh : vh);
+        for (int t = 0; t < T; ++t) {
+            if (BF16)
+                cp_async_4(&dst[t][i0], reinterpret_cast<const __nv_bfloat16*>(raw) + (row0 + t) * Cp + cp);
+            else
+                cp_async_8(&dst[t][i0], reinterpret_cast<const float*>(raw) + (row0 + t) * Cp + cp);
+        }
+    } else if (GATE_MODE == 0) {
+        for (int t = 0; t < T; ++t) cp_async_8(&av[t][i0], a.f_raw + (row0 + t) * C + c);
+    }
+
+    // ---- prologue: 64 threads per task, each on a channel pair (2i, 2i+1) --------------------
+    //      threads 0-63 q plane, 64-127 k plane, 128-191 v plane (+ beta), 192-255 the gate.
+    //      Grouped queries: the q and k planes hold Hk heads and this value head reads q/k head
+    //      h % Hk; only the CTAs of heads h < Hk write those heads' ring rows.
+    if (task < 3) {
         const long Cp = plane_width(H, a.Hk, task);        // row width of this plane
         const int cp = (task < 2 ? h % prep_qk_heads(H, a.Hk) : h) * kHeadDim + i0;
         const bool ring_owner = task == 2 || h < prep_qk_heads(H, a.Hk);
@@ -74,8 +106,11 @@ __global__ void __launch_bounds__(kDecThreads, 2) kda_decode_fused_kernel(Decode
             }
         }
         float (*dst)[kHeadDim] = task == 0 ? qh : (task == 1 ? kh : vh);
+        cp_async_commit_wait();
         for (int t = 0; t < T; ++t) {
-            const float2 x = load_raw2<BF16>(raw, (row0 + t) * Cp + cp);
+            float2 x;
+            if (BF16) x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&dst[t][i0]));
+            else x = *reinterpret_cast<const float2*>(&dst[t][i0]);
             window_push(win[0], x.x);
             window_push(win[1], x.y);
             *reinterpret_cast<float2*>(&dst[t][i0]) =
@@ -98,8 +133,9 @@ __global__ void __launch_bounds__(kDecThreads, 2) kda_decode_fused_kernel(Decode
     } else if (GATE_MODE == 0) {
         const float rate = expf(a.a_log[h]);
         const float2 dt = *reinterpret_cast<const float2*>(a.dt_bias + c);
+        cp_async_commit_wait();
         for (int t = 0; t < T; ++t) {
-            const float2 f = *reinterpret_cast<const float2*>(a.f_raw + (row0 + t) * C + c);
+            const float2 f = *reinterpret_cast<const float2*>(&av[t][i0]);
             *reinterpret_cast<float2*>(&av[t][i0]) =
                 make_float2(decay_f(kda_gate_f(f.x, dt.x, rate, a.gate_lb)),
                             decay_f(kda_gate_f(f.y, dt.y, rate, a.gate_lb)));
