@@ -58,43 +58,27 @@ __global__ void __launch_bounds__(kDecThreads, 2) kda_decode_fused_kernel(Decode
     const int warp = tid >> 5, lane = tid & 31;
     const int grp = lane >> 3, r = lane & 7;
 
-    // ---- issue the state loads first: 4 columns x 16 elements per lane -------------------
-    const int cw = warp * 16 + grp * 4;      // the group's first column
-    const long col0 = (((long)n * H + h) * kHeadDim + cw) * kHeadDim;
-    Col4 S;
-    col4_load(S, a.state_in + col0, r);
-
-    // ---- the prologue's per-token rows, all T at once: each thread copies its channel pair of
-    //      every token into the slot its result will take (raw q / k / v into qh / kh / vh, the
-    //      gate input into av), so the token loop below waits on no global load
+    // ---- the prologue's inputs first, so that they return ahead of the state stream and the
+    //      conv / norm / gate work overlaps the state transfer: conv weights and ring slots into
+    //      registers; every token's raw q / k / v (and gate input) channel pair copied into the
+    //      slot its result will take (qh / kh / vh, av); beta and the scalar gate inputs.
+    //      64 threads per task, each on a channel pair (2i, 2i+1): threads 0-63 q plane, 64-127
+    //      k plane, 128-191 v plane (+ beta), 192-255 the gate.  Grouped queries: the q and k
+    //      planes hold Hk heads and this value head reads q/k head h % Hk; only the CTAs of heads
+    //      h < Hk write those heads' ring rows.
     const int task = tid >> 6, i0 = 2 * (tid & 63);
     const int c = h * kHeadDim + i0;
+    float wr[2][KW], win[2][KW];
+    long ring_row = 0;
+    bool ring_owner = false;
+    float braw = 0.0f, fgate = 0.0f, dtb = 0.0f, alog = 0.0f;
+    float2 dt = make_float2(0.0f, 0.0f);
     if (task < 3) {
         const void* raw = task == 0 ? a.q_raw : (task == 1 ? a.k_raw : a.v_raw);
-        const long Cp = plane_width(H, a.Hk, task);
-        const int cp = (task < 2 ? h % prep_qk_heads(H, a.Hk) : h) * kHeadDim + i0;
-        float (*dst)[kHeadDim] = task == 0 ? qh : (task == 1 ? kh : vh);
-        for (int t = 0; t < T; ++t) {
-            if (BF16)
-                cp_async_4(&dst[t][i0], reinterpret_cast<const __nv_bfloat16*>(raw) + (row0 + t) * Cp + cp);
-            else
-                cp_async_8(&dst[t][i0], reinterpret_cast<const float*>(raw) + (row0 + t) * Cp + cp);
-        }
-    } else if (GATE_MODE == 0) {
-        for (int t = 0; t < T; ++t) cp_async_8(&av[t][i0], a.f_raw + (row0 + t) * C + c);
-    }
-
-    // ---- prologue: 64 threads per task, each on a channel pair (2i, 2i+1) --------------------
-    //      threads 0-63 q plane, 64-127 k plane, 128-191 v plane (+ beta), 192-255 the gate.
-    //      Grouped queries: the q and k planes hold Hk heads and this value head reads q/k head
-    //      h % Hk; only the CTAs of heads h < Hk write those heads' ring rows.
-    if (task < 3) {
         const long Cp = plane_width(H, a.Hk, task);        // row width of this plane
         const int cp = (task < 2 ? h % prep_qk_heads(H, a.Hk) : h) * kHeadDim + i0;
-        const bool ring_owner = task == 2 || h < prep_qk_heads(H, a.Hk);
-        float wr[2][KW], win[2][KW];
-        const long ring_row =
-            ((long)n * ring_channels(H, a.Hk) + plane_offset(H, a.Hk, task) + cp) * R;
+        ring_owner = task == 2 || h < prep_qk_heads(H, a.Hk);
+        ring_row = ((long)n * ring_channels(H, a.Hk) + plane_offset(H, a.Hk, task) + cp) * R;
 #pragma unroll
         for (int m = 0; m < KW; ++m) {
             const int jj = m - (KW - K);
@@ -105,6 +89,36 @@ __global__ void __launch_bounds__(kDecThreads, 2) kda_decode_fused_kernel(Decode
                 win[e][m] = d <= R ? a.ring_in[ring_row + e * R + (R - d)] : 0.0f;
             }
         }
+        float (*dst)[kHeadDim] = task == 0 ? qh : (task == 1 ? kh : vh);
+        for (int t = 0; t < T; ++t) {
+            if (BF16)
+                cp_async_4(&dst[t][i0], reinterpret_cast<const __nv_bfloat16*>(raw) + (row0 + t) * Cp + cp);
+            else
+                cp_async_8(&dst[t][i0], reinterpret_cast<const float*>(raw) + (row0 + t) * Cp + cp);
+        }
+        if (task == 2 && (tid & 63) < T) {
+            const long rw = (row0 + (tid & 63)) * H + h;
+            braw = a.beta_raw[rw];
+            if (GATE_MODE == 1) {
+                fgate = a.f_raw[rw];
+                dtb = a.dt_bias[h];
+                alog = a.a_log[h];
+            }
+        }
+    } else if (GATE_MODE == 0) {
+        alog = a.a_log[h];
+        dt = *reinterpret_cast<const float2*>(a.dt_bias + c);
+        for (int t = 0; t < T; ++t) cp_async_8(&av[t][i0], a.f_raw + (row0 + t) * C + c);
+    }
+
+    // ---- then the state loads: 4 columns x 16 elements per lane -----------------------------
+    const int cw = warp * 16 + grp * 4;      // the group's first column
+    const long col0 = (((long)n * H + h) * kHeadDim + cw) * kHeadDim;
+    Col4 S;
+    col4_load(S, a.state_in + col0, r);
+
+    // ---- prologue: conv + SiLU and the ring roll, beta, the gate -------------------------------
+    if (task < 3) {
         float (*dst)[kHeadDim] = task == 0 ? qh : (task == 1 ? kh : vh);
         cp_async_commit_wait();
         for (int t = 0; t < T; ++t) {
@@ -126,13 +140,11 @@ __global__ void __launch_bounds__(kDecThreads, 2) kda_decode_fused_kernel(Decode
         }
         if (task == 2 && (tid & 63) < T) {
             const int t = tid & 63;
-            beta_s[t] = sigmoid_f(a.beta_raw[(row0 + t) * H + h]);
-            if (GATE_MODE == 1)
-                ascal[t] = decay_f(gdn_gate_f(a.f_raw[(row0 + t) * H + h], a.dt_bias[h], a.a_log[h]));
+            beta_s[t] = sigmoid_f(braw);
+            if (GATE_MODE == 1) ascal[t] = decay_f(gdn_gate_f(fgate, dtb, alog));
         }
     } else if (GATE_MODE == 0) {
-        const float rate = expf(a.a_log[h]);
-        const float2 dt = *reinterpret_cast<const float2*>(a.dt_bias + c);
+        const float rate = expf(alog);
         cp_async_commit_wait();
         for (int t = 0; t < T; ++t) {
             const float2 f = *reinterpret_cast<const float2*>(&av[t][i0]);
@@ -184,6 +196,12 @@ __global__ void __launch_bounds__(kDecThreads, 2) kda_decode_fused_kernel(Decode
         vw.out_col0 = cw;
         col4_tokens<GATE_MODE == 0, false>(S, T, vw, a.scale, r, lane);
     }
+    // the epilogue's first gate row and the norm weight are requested before the state stores go
+    // out, so their latency overlaps the stores and the barrier
+    const float4 w4 = *reinterpret_cast<const float4*>(a.norm_w + 4 * lane);
+    float4 z_first = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    if (warp < T)
+        z_first = *reinterpret_cast<const float4*>(a.gate_raw + (row0 + warp) * C + h * kHeadDim + 4 * lane);
     col4_store(S, a.state_out + col0, r);
     __syncthreads();
     // ---- epilogue: gated RMSNorm, one warp per token row -----------------------------------
@@ -195,8 +213,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) kda_decode_fused_kernel(Decode
         ss = ss + __fmul_rn(o4.w, o4.w);
         const float inv = rms_inv_f(warp_sum(ss), a.rms_eps);
         const long base = (row0 + t) * C + h * kHeadDim + 4 * lane;
-        const float4 w4 = *reinterpret_cast<const float4*>(a.norm_w + 4 * lane);
-        const float4 z4 = *reinterpret_cast<const float4*>(a.gate_raw + base);
+        const float4 z4 = t == warp ? z_first : *reinterpret_cast<const float4*>(a.gate_raw + base);
         float4 y4;
         if (a.norm_silu) {
             y4.x = gated_norm_f<true>(o4.x, inv, w4.x, z4.x);
