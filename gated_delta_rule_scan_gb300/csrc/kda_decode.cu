@@ -156,11 +156,26 @@ __global__ void __launch_bounds__(kDecThreads, 2) kda_decode_fused_kernel(Decode
     __syncthreads();
     // ---- l2 norm of q (warps 0-1) and k (warps 2-3) ----------------------------------------
     if (task < 2) {
+        // four tokens' butterflies at a time, so their shuffles overlap (each value still goes
+        // through its own warp_sum, so the bits do not depend on the grouping)
         float (*x)[kHeadDim] = task == 0 ? qh : kh;
-        for (int t = 0; t < T; ++t) {
-            const float2 v = *reinterpret_cast<const float2*>(&x[t][i0]);
-            const float ssum = warp_sum(pair_sumsq(v.x, v.y));
-            if (lane == 0) part[task][warp & 1][t] = ssum;
+        for (int t0 = 0; t0 < T; t0 += 4) {
+            float ssum[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                ssum[j] = 0.0f;
+                if (t0 + j < T) {
+                    const float2 v = *reinterpret_cast<const float2*>(&x[t0 + j][i0]);
+                    ssum[j] = pair_sumsq(v.x, v.y);
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) ssum[j] = warp_sum(ssum[j]);
+            if (lane == 0) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    if (t0 + j < T) part[task][warp & 1][t0 + j] = ssum[j];
+            }
         }
     }
     __syncthreads();

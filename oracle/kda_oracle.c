@@ -234,6 +234,62 @@ void orc_scan_kda(const double* q, const double* k, const double* v, const doubl
     }
 }
 
+/*
+ * The same recurrence with a key width Dk and a value width Dv of their own ([GDN]
+ * `gdn_delta_rule_into` doc: q and k are num_k_heads * head_k_dim wide, v and the output
+ * num_v_heads * head_v_dim, the state num_v_heads * head_v_dim * head_k_dim).  S is Dk x Dv
+ * (rows i = key dim, columns j = value dim); the buffer stores M[j][i] = S[i][j], Dv rows of Dk.
+ * q, k, g: [rows][H][Dk]; v, o: [rows][H][Dv]; beta: [rows][H]; state [N][H][Dv][Dk].
+ * Written out on its own (not through the square routine), token by token, in the same order:
+ * decay, u = v - S^T k, rank-1 update, readout.
+ */
+void orc_scan_kda_rect(const double* q, const double* k, const double* v, const double* g,
+                       const double* beta, const int64_t* cu, int N, int H, int Dk, int Dv,
+                       const double* state_in, double* state_out, double* o, double scale) {
+    const long Ck = (long)H * Dk, Cv = (long)H * Dv;
+    const long SS = (long)Dk * Dv;
+    long units = (long)N * H;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (long un = 0; un < units; ++un) {
+        const int n = (int)(un / H), h = (int)(un % H);
+        const long r0 = cu[n];
+        const int T = (int)(cu[n + 1] - cu[n]);
+        const double* min = state_in + ((long)n * H + h) * SS;
+        double* mout = state_out + ((long)n * H + h) * SS;
+        double* S = (double*)malloc(sizeof(double) * (size_t)SS);   /* S[i*Dv + j] */
+        double* uu = (double*)malloc(sizeof(double) * (size_t)Dv);
+        for (int i = 0; i < Dk; ++i)
+            for (int j = 0; j < Dv; ++j) S[(long)i * Dv + j] = min[(long)j * Dk + i];
+        for (int t = 0; t < T; ++t) {
+            const double* qt = q + (r0 + t) * Ck + (long)h * Dk;
+            const double* kt = k + (r0 + t) * Ck + (long)h * Dk;
+            const double* gt = g + (r0 + t) * Ck + (long)h * Dk;
+            const double* vt = v + (r0 + t) * Cv + (long)h * Dv;
+            const double bt = beta[(r0 + t) * H + h];
+            for (int i = 0; i < Dk; ++i) {
+                const double decay = exp(gt[i]);
+                for (int j = 0; j < Dv; ++j) S[(long)i * Dv + j] *= decay;
+            }
+            for (int j = 0; j < Dv; ++j) {
+                double sk = 0.0;
+                for (int i = 0; i < Dk; ++i) sk += S[(long)i * Dv + j] * kt[i];
+                uu[j] = vt[j] - sk;
+            }
+            for (int i = 0; i < Dk; ++i)
+                for (int j = 0; j < Dv; ++j) S[(long)i * Dv + j] += bt * kt[i] * uu[j];
+            for (int j = 0; j < Dv; ++j) {
+                double sq = 0.0;
+                for (int i = 0; i < Dk; ++i) sq += S[(long)i * Dv + j] * qt[i];
+                o[(r0 + t) * Cv + (long)h * Dv + j] = scale * sq;
+            }
+        }
+        for (int i = 0; i < Dk; ++i)
+            for (int j = 0; j < Dv; ++j) mout[(long)j * Dk + i] = S[(long)i * Dv + j];
+        free(uu);
+        free(S);
+    }
+}
+
 /* ------------------------------------------------------------------------------------------ */
 /* a5 (GDN): the scalar-gate delta rule, written separately                                     */
 /* ------------------------------------------------------------------------------------------ */

@@ -69,6 +69,8 @@ def _bind(path: str):
         fn.argtypes = [dp, dp, dp, dp, dp, lp, I, I, I, dp, dp, dp, D]
     lib.orc_gated_rmsnorm.argtypes = [dp, dp, dp, dp, L, I, D, I]
     lib.orc_matvec_rows.argtypes = [dp, dp, dp, L, L, I]
+    lib.orc_scan_kda_rect.argtypes = [dp, dp, dp, dp, dp, lp, I, I, I, I, dp, dp, dp, D]
+    lib.orc_scan_kda_rect.restype = None
     for name in ("orc_conv_silu", "orc_l2norm", "orc_gate_kda", "orc_gate_gdn",
                  "orc_sigmoid", "orc_scan_kda", "orc_scan_gdn", "orc_gated_rmsnorm",
                  "orc_matvec_rows"):
@@ -183,6 +185,24 @@ def scan_kda(q, k, v, g, beta, state_in, cu_seqlens=None, scale=None):
     return o, st
 
 
+def scan_kda_rect(q, k, v, g, beta, state_in, cu_seqlens=None, scale=None):
+    """a5 with a value width of its own: q, k, g [rows, H, Dk]; v [rows, H, Dv]; beta [rows, H];
+    state_in [N, H, Dv, Dk] (M[j][i] = S[i][j]).  Returns (o [rows, H, Dv], state_out)."""
+    q, k, v, g, beta = (_f64(a) for a in (q, k, v, g, beta))
+    state_in = _f64(state_in)
+    N, H, Dv, Dk = state_in.shape
+    rows = q.size // (H * Dk)
+    cu = _cu(cu_seqlens, rows)
+    assert cu.size == N + 1 and cu[-1] == rows
+    scale = Dk ** -0.5 if scale is None else float(scale)
+    o = np.empty((rows, H, Dv))
+    st = np.empty_like(state_in)
+    _load().orc_scan_kda_rect(_p(q), _p(k), _p(v), _p(g), _p(beta),
+                              cu.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), N, H, Dk, Dv,
+                              _p(state_in), _p(st), _p(o), scale)
+    return o, st
+
+
 def scan_gdn(q, k, v, g, beta, state_in, cu_seqlens=None, scale=None):
     """a5, separate scalar-gate GDN scan.  g: [rows, H] (one log-decay per token and head)."""
     q, k, v, g, beta = (_f64(a) for a in (q, k, v, g, beta))
@@ -239,7 +259,7 @@ def proj6(x, w_q, w_k, w_v, w_fa, w_ga, w_b):
 def forward(*, q_raw, k_raw, v_raw, f_raw, dt_bias, a_log, beta_raw, state_in, H, D,
             conv_w=None, ring_in=None, cu_seqlens=None, gate_mode=0, gate_lb=-5.0,
             norm_w=None, gate_raw=None, l2_eps=1e-6, rms_eps=1e-6, scale=None,
-            scalar_scan=False, norm_gate="sigmoid", Hk=None):
+            scalar_scan=False, norm_gate="sigmoid", Hk=None, Dv=None):
     """The mixer from projected channels to the gated output, in the pages' stage order
     (conv+SiLU -> ring roll -> l2 norm -> gates -> scan -> gated RMSNorm).
 
@@ -247,8 +267,12 @@ def forward(*, q_raw, k_raw, v_raw, f_raw, dt_bias, a_log, beta_raw, state_in, H
     Hk: grouped queries (gdn_ops.rs `gdn_delta_rule_into` doc): q_raw and k_raw hold Hk heads
         ([rows, Hk*D]) and value head h reads query/key head h % Hk; None means Hk = H.  The conv
         planes and the ring then hold Hk*D q channels, Hk*D k channels and C v channels.
-    conv_w: [2*Hk*D + C, K] fused q,k,v conv weights or None (then no conv / SiLU and no ring).
-    ring_in: [N, 2*Hk*D + C, K-1].
+    Dv: the value head width when it differs from the key width D (gdn_ops.rs
+        `gdn_delta_rule_into` doc: head_k_dim and head_v_dim are separate): v_raw, gate_raw and y
+        are [rows, H*Dv], state_in [N, H, Dv, D], norm_w [Dv], and the v conv plane and ring rows
+        hold H*Dv channels.  None means Dv = D.
+    conv_w: [2*Hk*D + H*Dv, K] fused q,k,v conv weights or None (then no conv / SiLU and no ring).
+    ring_in: [N, 2*Hk*D + H*Dv, K-1].
     f_raw: [rows, C] (gate_mode 0, KDA) or [rows, H] (gate_mode 1, GDN).
     dt_bias: [C] (KDA) or [H] (GDN); a_log: [H]; beta_raw: [rows, H].
     state_in: [N, H, D, D] (M[j][i] layout).
@@ -260,19 +284,21 @@ def forward(*, q_raw, k_raw, v_raw, f_raw, dt_bias, a_log, beta_raw, state_in, H
     C = H * D
     Hk = H if Hk is None else Hk
     Cq = Hk * D
+    Dv = D if Dv is None else Dv
+    Cv = H * Dv
     q_raw, k_raw, v_raw = _f64(q_raw), _f64(k_raw), _f64(v_raw)
     rows = q_raw.shape[0]
     cu = _cu(cu_seqlens, rows)
     N = cu.size - 1
     planes = [q_raw, k_raw, v_raw]
-    widths = [Cq, Cq, C]                      # channels of the q, k and v planes
+    widths = [Cq, Cq, Cv]                     # channels of the q, k and v planes
     offs = [0, Cq, 2 * Cq]                    # their first row in conv_w and the ring
     conv = [np.empty((rows, w)) for w in widths]
     ring_out = None
     if conv_w is not None:
         conv_w = _f64(conv_w)
         K = conv_w.shape[1]
-        ring_in = _f64(ring_in).reshape(N, 2 * Cq + C, K - 1)
+        ring_in = _f64(ring_in).reshape(N, 2 * Cq + Cv, K - 1)
         ring_out = np.empty_like(ring_in)
     for n in range(N):
         r0, r1 = int(cu[n]), int(cu[n + 1])
@@ -297,7 +323,12 @@ def forward(*, q_raw, k_raw, v_raw, f_raw, dt_bias, a_log, beta_raw, state_in, H
         g = gate_gdn(f_raw, dt_bias, a_log)
     beta = sigmoid(beta_raw).reshape(rows, H)
     shp = (rows, H, D)
-    if gate_mode == 0:
+    if Dv != D:                               # separate value width: the rectangular routine
+        assert not scalar_scan, "the scalar-gate routine is square"
+        gk = g.reshape(shp) if gate_mode == 0 else np.repeat(g.reshape(rows, H, 1), D, axis=2)
+        o, st = scan_kda_rect(q_scan, k_scan, v_hat.reshape(rows, H, Dv), gk, beta, state_in,
+                              cu, scale)
+    elif gate_mode == 0:
         o, st = scan_kda(q_scan, k_scan, v_hat.reshape(shp), g.reshape(shp), beta, state_in, cu,
                          scale)
     elif scalar_scan:
@@ -308,8 +339,8 @@ def forward(*, q_raw, k_raw, v_raw, f_raw, dt_bias, a_log, beta_raw, state_in, H
         o, st = scan_kda(q_scan, k_scan, v_hat.reshape(shp), gb, beta, state_in, cu, scale)
     y = None
     if norm_w is not None:
-        y = gated_rmsnorm(o.reshape(rows, C), norm_w, gate_raw, rms_eps,
-                          norm_gate).reshape(rows, C)
+        y = gated_rmsnorm(o.reshape(rows, Cv), norm_w, gate_raw, rms_eps,
+                          norm_gate).reshape(rows, Cv)
     return dict(q_hat=q_hat.reshape(rows, Cq), k_hat=k_hat.reshape(rows, Cq),
-                v_hat=v_hat.reshape(rows, C), g=g, beta=beta, o=o.reshape(rows, C), y=y,
+                v_hat=v_hat.reshape(rows, Cv), g=g, beta=beta, o=o.reshape(rows, Cv), y=y,
                 state_out=st, ring_out=ring_out)

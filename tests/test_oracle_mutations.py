@@ -61,6 +61,10 @@ MUTATIONS = [
     ("matvec_first_token_only", "* x[(long)s * in_f + k];", "* x[k];"),
     ("matvec_weight_column_shifted", "acc += w[r * in_f + k] * x",
      "acc += w[r * in_f + (k + 1) % in_f] * x"),
+    ("rect_value_stride_uses_key_width", "const double* vt = v + (r0 + t) * Cv + (long)h * Dv;",
+     "const double* vt = v + (r0 + t) * Cv + (long)h * Dk;"),
+    ("rect_state_transposed", "S[(long)i * Dv + j] = min[(long)j * Dk + i];",
+     "S[(long)i * Dv + j] = min[(long)i * Dv + j];"),
 ]
 
 

@@ -17,6 +17,10 @@ Which pin covers which oracle routine:
                   one-token calls (bit-equal).
   forward (Hk)    grouped queries equal the plain mixer on q/k heads replicated in the tiled
                   order h % Hk (outputs, state, ring).
+  scan_kda_rect   (value width Dv != key width) equals the square routine on each value-column
+  (forward Dv)    block, bit for bit; the dense product form with a Dk x Dv state; the whole
+                  mixer with Dv = 2D equals two mixers on the halves of each value head, and its
+                  y is the gated RMSNorm over the full width.
   matvec_rows     one-hot weight rows select inputs exactly; small-integer case equals exact
   (proj6)         integer dot products; a band matrix's closed form; the six outputs' order.
 Every check is a plain function so test_oracle_mutations.py can run it against mutated oracle
@@ -499,6 +503,82 @@ def check_gqa_equals_replicated_heads():
     assert gqa["q_hat"].shape == (T, Cq)
 
 
+def check_rect_scan_is_column_blocks():
+    """A value width Dv = 3 Dk: every value column of S evolves on its own, so the rectangular
+    routine equals the square routine run on each Dk-wide block of value columns, bit for bit
+    (state blocks and outputs), and with Dv = Dk it is the square routine itself."""
+    rng = _rng(44)
+    T, H, Dk, m = 6, 2, 4, 3
+    Dv = m * Dk
+    q, k = _unit_rows(rng, (T, H, Dk)), _unit_rows(rng, (T, H, Dk))
+    v = rng.standard_normal((T, H, Dv))
+    g = -rng.random((T, H, Dk))
+    b = rng.random((T, H))
+    s0 = rng.standard_normal((1, H, Dv, Dk))
+    o, st = orc.scan_kda_rect(q, k, v, g, b, s0)
+    assert o.shape == (T, H, Dv) and st.shape == (1, H, Dv, Dk)
+    for j in range(m):
+        sl = slice(j * Dk, (j + 1) * Dk)
+        oj, sj = orc.scan_kda(q, k, v[:, :, sl], g, b, s0[:, :, sl], scale=Dk ** -0.5)
+        np.testing.assert_array_equal(o[:, :, sl], oj)
+        np.testing.assert_array_equal(st[:, :, sl], sj)
+
+
+def check_rect_scan_dense_product():
+    """The rectangular routine against the dense product form written out here:
+    S <- (I - b k k^T) Diag(a) S + b k v^T with S of shape Dk x Dv, readout scale S^T q."""
+    rng = _rng(45)
+    T, Dk, Dv = 5, 3, 7
+    q, k = _unit_rows(rng, (T, 1, Dk)), _unit_rows(rng, (T, 1, Dk))
+    v = rng.standard_normal((T, 1, Dv))
+    g = -rng.random((T, 1, Dk))
+    b = rng.random((T, 1))
+    S = rng.standard_normal((Dk, Dv))
+    o, st = orc.scan_kda_rect(q, k, v, g, b, np.ascontiguousarray(S.T)[None, None], scale=1.0)
+    for t in range(T):
+        kt, bt = k[t, 0], b[t, 0]
+        S = (np.eye(Dk) - bt * np.outer(kt, kt)) @ np.diag(np.exp(g[t, 0])) @ S + bt * np.outer(kt, v[t, 0])
+        np.testing.assert_allclose(o[t, 0], S.T @ q[t, 0], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(st[0, 0], S.T, rtol=0, atol=1e-12)
+
+
+def check_forward_value_width():
+    """The whole mixer with Dv = 2 D: its readout and state equal two mixers run on the halves of
+    every value head (v raw channels, conv weight and ring rows, state), and y is the gated RMSNorm
+    of that readout over each full 2 D-wide head."""
+    rng = _rng(46)
+    D, H, K, T = 4, 2, 3, 6
+    Dv = 2 * D
+    C, Cv = H * D, H * Dv
+    q, k = rng.standard_normal((T, C)), rng.standard_normal((T, C))
+    v = rng.standard_normal((T, Cv))
+    wq, wk, wv = (rng.standard_normal((C, K)), rng.standard_normal((C, K)),
+                  rng.standard_normal((Cv, K)))
+    rq, rk, rv = (rng.standard_normal((C, K - 1)), rng.standard_normal((C, K - 1)),
+                  rng.standard_normal((Cv, K - 1)))
+    s0 = 0.1 * rng.standard_normal((1, H, Dv, D))
+    shared = dict(f_raw=rng.standard_normal((T, C)), dt_bias=rng.standard_normal(C),
+                  a_log=np.log(rng.uniform(1, 16, H)), beta_raw=rng.standard_normal((T, H)), D=D,
+                  H=H)
+    w_norm, z = 1 + rng.standard_normal(Dv), rng.standard_normal((T, Cv))
+    full = orc.forward(q_raw=q, k_raw=k, v_raw=v, conv_w=np.concatenate([wq, wk, wv]),
+                       ring_in=np.concatenate([rq, rk, rv])[None], state_in=s0, Dv=Dv,
+                       norm_w=w_norm, gate_raw=z, **shared)
+    for half in range(2):
+        ch = np.concatenate([np.arange(h * Dv + half * D, h * Dv + (half + 1) * D)
+                             for h in range(H)])
+        part = orc.forward(q_raw=q, k_raw=k, v_raw=v[:, ch],
+                           conv_w=np.concatenate([wq, wk, wv[ch]]),
+                           ring_in=np.concatenate([rq, rk, rv[ch]])[None],
+                           state_in=np.ascontiguousarray(s0[:, :, half * D:(half + 1) * D]),
+                           scale=D ** -0.5, **shared)
+        np.testing.assert_array_equal(full["o"][:, ch], part["o"])
+        np.testing.assert_array_equal(full["state_out"][:, :, half * D:(half + 1) * D],
+                                      part["state_out"])
+        np.testing.assert_array_equal(full["ring_out"][0, 2 * C:][ch], part["ring_out"][0, 2 * C:])
+    np.testing.assert_array_equal(full["y"], orc.gated_rmsnorm(full["o"], w_norm, z))
+
+
 ALL_CHECKS = [
     check_three_token_golden, check_three_token_embedded, check_beta_zero_closed_form,
     check_orthonormal_recall, check_dense_product_form, check_chunked_form_every_chunk_size,
@@ -508,6 +588,7 @@ ALL_CHECKS = [
     check_split_state_carry, check_chained_single_tokens_equal_multi_token,
     check_varlen_equals_separate_calls, check_matvec_one_hot_rows, check_matvec_exact_integers,
     check_matvec_band, check_proj6_order_and_shapes, check_gqa_equals_replicated_heads,
+    check_rect_scan_is_column_blocks, check_rect_scan_dense_product, check_forward_value_width,
 ]
 
 
