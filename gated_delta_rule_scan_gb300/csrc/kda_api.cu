@@ -16,6 +16,7 @@ using namespace kda;
 __device__ int g_kda_dev_err;
 
 constexpr int kMaxGridY = 65535;  // sequences (and heads) map to gridDim.y
+constexpr int kMaxValueWidth = 1024;   // widest value head: 8 sub-heads of 128
 
 // the current device's error word (its address is looked up once per device)
 int* dev_err_ptr() {
@@ -78,14 +79,16 @@ int prep_build(const void* q_raw, const void* k_raw, const void* v_raw, int raw_
                const float* dt_bias, const float* a_log, int gate_mode, float gate_lb,
                const float* beta_raw, float* q_hat, float* k_hat, float* v_hat, float* g,
                float* beta, const SeqLayout& seq, int H, int D, int K, float l2_eps,
-               bool planes, PrepArgs& a, int Hk = 0) {
+               bool planes, PrepArgs& a, int Hk = 0, int Hg = 0) {
     a = PrepArgs{};
     a.seq = seq;
     if (D != kHeadDim) return KDA_ERR_HEAD_DIM;
     if (seq.N < 0 || seq.N > kMaxGridY || seq.total_rows < 0 || H <= 0 || H > kMaxGridY)
         return KDA_ERR_SHAPE;
-    if (Hk == 0) Hk = H;
-    if (Hk < 1 || Hk > H) return KDA_ERR_SHAPE;
+    if (Hg == 0) Hg = H;                      // H: 128-wide value sub-heads; Hg: value heads
+    if (Hg < 1 || Hg > H || H % Hg != 0) return KDA_ERR_SHAPE;
+    if (Hk == 0) Hk = Hg;
+    if (Hk < 1 || Hk > Hg) return KDA_ERR_SHAPE;
     if (raw_dtype != KDA_DTYPE_F32 && raw_dtype != KDA_DTYPE_BF16) return KDA_ERR_ENUM;
     if (gate_mode < 0 || gate_mode > (KDA_GATE_PER_HEAD | KDA_GATE_EXP)) return KDA_ERR_ENUM;
     if (conv_w != nullptr && (K < 2 || K > kMaxConvK)) return KDA_ERR_CONV_K;
@@ -117,6 +120,7 @@ int prep_build(const void* q_raw, const void* k_raw, const void* v_raw, int raw_
     a.q_hat = q_hat; a.k_hat = k_hat; a.v_hat = v_hat; a.g = g; a.beta = beta;
     a.seq = seq; a.H = H; a.K = conv_w ? K : 1; a.l2_eps = l2_eps;
     a.Hk = Hk;
+    a.Hg = Hg;
     return KDA_OK;
 }
 
@@ -125,11 +129,11 @@ int prep_impl(const void* q_raw, const void* k_raw, const void* v_raw, int raw_d
               const float* dt_bias, const float* a_log, int gate_mode, float gate_lb,
               const float* beta_raw, float* q_hat, float* k_hat, float* v_hat, float* g,
               float* beta, const SeqLayout& seq, int H, int D, int K, float l2_eps,
-              void* stream, int Hk = 0) {
+              void* stream, int Hk = 0, int Hg = 0) {
     PrepArgs a;
     const int rc = prep_build(q_raw, k_raw, v_raw, raw_dtype, conv_w, ring_in, ring_out, f_raw,
                               dt_bias, a_log, gate_mode, gate_lb, beta_raw, q_hat, k_hat, v_hat,
-                              g, beta, seq, H, D, K, l2_eps, true, a, Hk);
+                              g, beta, seq, H, D, K, l2_eps, true, a, Hk, Hg);
     if (rc != KDA_OK || seq.N == 0) return rc;
     if (const int sd = check_stream_device(stream)) return sd;
     return cuda_status(launch_prep(a, static_cast<cudaStream_t>(stream)));
@@ -153,10 +157,11 @@ long max_len(const SeqLayout& seq, const int* cu_host) {
 int scan_impl(const float* q, const float* k, const float* v, const float* g, int gate_mode,
               const float* beta, const float* state_in, float* state_out, float* o,
               const SeqLayout& seq, const int* cu_host, int H, int D, float scale, int algo,
-              void* workspace, size_t workspace_bytes, void* stream, int Hk = 0) {
+              void* workspace, size_t workspace_bytes, void* stream, int Hk = 0, int vsub = 1) {
     if (D != kHeadDim) return KDA_ERR_HEAD_DIM;
     if (seq.N < 0 || seq.N > kMaxGridY || seq.total_rows < 0 || H <= 0) return KDA_ERR_SHAPE;
-    if (Hk == 0) Hk = H;
+    if (vsub < 1 || H % vsub != 0) return KDA_ERR_SHAPE;
+    if (Hk == 0) Hk = H / vsub;
     if (Hk < 1 || Hk > kMaxGridY) return KDA_ERR_SHAPE;
     if (gate_mode < 0 || gate_mode > (KDA_GATE_PER_HEAD | KDA_GATE_EXP)) return KDA_ERR_ENUM;
     if (algo != KDA_ALGO_AUTO && algo != KDA_ALGO_SEQ && algo != KDA_ALGO_CHUNK) return KDA_ERR_ENUM;
@@ -174,6 +179,7 @@ int scan_impl(const float* q, const float* k, const float* v, const float* g, in
     }
     ScanArgs a{};
     a.Hk = Hk;
+    a.vsub = vsub;
     a.q = q; a.k = k; a.v = v; a.g = g; a.gate_mode = gate_mode; a.beta = beta;
     a.state_in = state_in; a.state_out = state_out; a.o = o;
     a.seq = seq; a.H = H; a.scale = scale; a.order = nullptr;
@@ -260,14 +266,15 @@ int prefill_impl(const void* q_raw, const void* k_raw, const void* v_raw, int ra
 
 int norm_impl(const float* o, const float* norm_w, const float* gate_raw, float* y, long rows,
               int D, float eps, bool silu, void* stream) {
-    if (D != kHeadDim) return KDA_ERR_HEAD_DIM;
+    // D: the value head width, a multiple of 128 up to kMaxValueWidth
+    if (D <= 0 || D % kHeadDim != 0 || D > kMaxValueWidth) return KDA_ERR_HEAD_DIM;
     if (rows < 0) return KDA_ERR_SHAPE;
     if (rows == 0) return KDA_OK;
     if (!o || !norm_w || !gate_raw || !y) return KDA_ERR_NULL;
     if (!aligned16(o) || !aligned16(norm_w) || !aligned16(gate_raw) || !aligned16(y))
         return KDA_ERR_ALIGN;
     if (const int sd = check_stream_device(stream)) return sd;
-    NormArgs a{o, norm_w, gate_raw, y, rows, eps, silu ? 1 : 0};
+    NormArgs a{o, norm_w, gate_raw, y, rows, eps, silu ? 1 : 0, D};
     return cuda_status(launch_gated_rmsnorm(a, static_cast<cudaStream_t>(stream)));
 }
 
@@ -631,6 +638,86 @@ int kda_verify_rollback_gqa(const void* q_raw, const void* k_raw, const void* v_
     return decode_impl(q_raw, k_raw, v_raw, raw_dtype, conv_w, ring_in, ring_out, f_raw, dt_bias,
                        a_log, gate_mode, gate_lb, beta_raw, state_in, state_out, norm_w, gate_raw,
                        y, N, T, H, D, K, l2_eps, scale, rms_eps, keep, true, stream, Hk);
+}
+
+// a value head width Dv = m * 128 (m = 1..8) with a key width of 128: the number of 128-wide
+// value sub-heads, or 0 for a width that is not built
+static int value_subheads(int Dk, int Dv) {
+    if (Dk != kHeadDim || Dv <= 0 || Dv % kHeadDim != 0 || Dv > kMaxValueWidth) return 0;
+    return Dv / kHeadDim;
+}
+
+int kda_conv_l2norm_prep_dv(const void* q_raw, const void* k_raw, const void* v_raw,
+                            int raw_dtype, const float* conv_w, const float* ring_in,
+                            float* ring_out, const float* f_raw, const float* dt_bias,
+                            const float* a_log, int gate_mode, float gate_lb,
+                            const float* beta_raw, float* q_hat, float* k_hat, float* v_hat,
+                            float* g, float* beta, int N, int T, int H, int Hk, int Dk, int Dv,
+                            int K, float l2_eps, void* stream) {
+    const int m = value_subheads(Dk, Dv);
+    if (m == 0) return KDA_ERR_HEAD_DIM;
+    if (N < 0 || T < 0 || H <= 0 || Hk <= 0 || Hk > H || (long)H * m > kMaxGridY) return KDA_ERR_SHAPE;
+    SeqLayout seq{nullptr, T, N, (long)N * T};
+    return prep_impl(q_raw, k_raw, v_raw, raw_dtype, conv_w, ring_in, ring_out, f_raw, dt_bias,
+                     a_log, gate_mode, gate_lb, beta_raw, q_hat, k_hat, v_hat, g, beta, seq,
+                     H * m, kHeadDim, K, l2_eps, stream, Hk, H);
+}
+
+int kda_conv_l2norm_prep_varlen_dv(const void* q_raw, const void* k_raw, const void* v_raw,
+                                   int raw_dtype, const float* conv_w, const float* ring_in,
+                                   float* ring_out, const float* f_raw, const float* dt_bias,
+                                   const float* a_log, int gate_mode, float gate_lb,
+                                   const float* beta_raw, float* q_hat, float* k_hat,
+                                   float* v_hat, float* g, float* beta, const int* cu_seqlens,
+                                   const int* cu_seqlens_host, int N, int total_T, int H, int Hk,
+                                   int Dk, int Dv, int K, float l2_eps, void* stream) {
+    const int m = value_subheads(Dk, Dv);
+    if (m == 0) return KDA_ERR_HEAD_DIM;
+    if (N < 0 || total_T < 0 || H <= 0 || Hk <= 0 || Hk > H || (long)H * m > kMaxGridY)
+        return KDA_ERR_SHAPE;
+    if (N > 0) {
+        if (cu_seqlens == nullptr) return KDA_ERR_NULL;
+        const int rc = check_cu(cu_seqlens_host, N, total_T);
+        if (rc) return rc;
+    }
+    SeqLayout seq{cu_seqlens, 0, N, (long)total_T};
+    return prep_impl(q_raw, k_raw, v_raw, raw_dtype, conv_w, ring_in, ring_out, f_raw, dt_bias,
+                     a_log, gate_mode, gate_lb, beta_raw, q_hat, k_hat, v_hat, g, beta, seq,
+                     H * m, kHeadDim, K, l2_eps, stream, Hk, H);
+}
+
+int kda_scan_dv(const float* q_hat, const float* k_hat, const float* v_hat, const float* g,
+                int gate_mode, const float* beta, const float* state_in, float* state_out,
+                float* o, int N, int T, int H, int Hk, int Dk, int Dv, float scale, int algo,
+                void* workspace, size_t workspace_bytes, void* stream) {
+    const int m = value_subheads(Dk, Dv);
+    if (m == 0) return KDA_ERR_HEAD_DIM;
+    if (N < 0 || T < 0 || H <= 0 || Hk <= 0 || Hk > H || (long)H * m > kMaxGridY) return KDA_ERR_SHAPE;
+    SeqLayout seq{nullptr, T, N, (long)N * T};
+    return scan_impl(q_hat, k_hat, v_hat, g, gate_mode, beta, state_in, state_out, o, seq,
+                     nullptr, H * m, kHeadDim, scale, algo, workspace, workspace_bytes, stream, Hk,
+                     m);
+}
+
+int kda_scan_varlen_dv(const float* q_hat, const float* k_hat, const float* v_hat,
+                       const float* g, int gate_mode, const float* beta, const float* state_in,
+                       float* state_out, float* o, const int* cu_seqlens,
+                       const int* cu_seqlens_host, int N, int total_T, int H, int Hk, int Dk,
+                       int Dv, float scale, int algo, void* workspace, size_t workspace_bytes,
+                       void* stream) {
+    const int m = value_subheads(Dk, Dv);
+    if (m == 0) return KDA_ERR_HEAD_DIM;
+    if (N < 0 || total_T < 0 || H <= 0 || Hk <= 0 || Hk > H || (long)H * m > kMaxGridY)
+        return KDA_ERR_SHAPE;
+    if (N > 0) {
+        if (cu_seqlens == nullptr) return KDA_ERR_NULL;
+        const int rc = check_cu(cu_seqlens_host, N, total_T);
+        if (rc) return rc;
+    }
+    SeqLayout seq{cu_seqlens, 0, N, (long)total_T};
+    return scan_impl(q_hat, k_hat, v_hat, g, gate_mode, beta, state_in, state_out, o, seq,
+                     cu_seqlens_host, H * m, kHeadDim, scale, algo, workspace, workspace_bytes,
+                     stream, Hk, m);
 }
 
 int kda_selftest_wait_timeout(void* stream) {

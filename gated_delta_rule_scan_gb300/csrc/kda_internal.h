@@ -42,7 +42,12 @@ struct PrepArgs {
     int H; int K; float l2_eps;
     int Hk;                  // heads of the q and k planes (grouped queries: value head h reads
                              // q/k head h % Hk); 0 means H
+    int Hg;                  // heads of the gate and beta (a value head wider than 128 is H / Hg
+                             // 128-wide sub-heads that share them); 0 means H
 };
+
+// Gate / beta heads of a prep call (the value heads); H counts 128-wide value sub-heads.
+__host__ __device__ inline int prep_gate_heads(const PrepArgs& a) { return a.Hg > 0 ? a.Hg : a.H; }
 
 // Channel layout of the three conv planes under grouped queries: q and k hold Hk heads, v holds H;
 // conv_w rows and ring rows are [q | k | v] = [Hk*D | Hk*D | H*D] (gdn_ops.rs gdn_delta_rule_into
@@ -68,14 +73,25 @@ struct ScanArgs {
     int* err;                // device error word
     int Hk;                  // heads of q and k (grouped queries: value head h reads q/k head
                              // h % Hk; rows of q and k are Hk * D wide); 0 means H
+    int vsub;                // 128-wide sub-heads per value head (value width vsub * 128): unit h
+                             // is value head h / vsub, which owns the gate and beta and reads q/k
+                             // head (h / vsub) % Hk; 0 means 1
 };
 
 // the heads of q and k, and the one value head h reads
 __host__ __device__ inline int qk_heads(const ScanArgs& a) { return a.Hk > 0 ? a.Hk : a.H; }
+__host__ __device__ inline int value_sub(const ScanArgs& a) { return a.vsub > 0 ? a.vsub : 1; }
+// the value head (gate and beta head) of unit h, the number of such heads, and the q/k head
+__host__ __device__ inline int gate_head(const ScanArgs& a, int h) { return h / value_sub(a); }
+__host__ __device__ inline int gate_heads(const ScanArgs& a) { return a.H / value_sub(a); }
+__host__ __device__ inline int unit_qk_head(const ScanArgs& a, int h) {
+    return gate_head(a, h) % qk_heads(a);
+}
 
 struct NormArgs {
     const float* o; const float* w; const float* z; float* y; long rows; float eps;
     int silu;                // gate: 0 sigmoid (KDA), 1 SiLU (GDN's gated_rmsnorm)
+    int width;               // row length, a multiple of 128 (0 means 128)
 };
 
 struct DecodeArgs {

@@ -121,6 +121,11 @@ __global__ void __launch_bounds__(kPrepThreads) kda_prep_kernel(PrepArgs a) {
     // also compute q/k head h, the others only their v head, gate and beta
     const long Cq = plane_width(H, a.Hk, 0);
     const bool has_qk = h < prep_qk_heads(H, a.Hk);
+    // value heads wider than 128 (H counts 128-wide sub-heads): the CTAs of heads h < Hg also
+    // compute value head h's gate and beta, whose rows are Cg = Hg * 128 (or Hg) wide
+    const int Hg = prep_gate_heads(a);
+    const bool has_gate = h < Hg;
+    const long Cg = (long)Hg * kHeadDim;
     const long RC = ring_channels(H, a.Hk);
     const int c = h * kHeadDim + 4 * lane;     // first of this lane's 4 channels in a plane
     const int K = a.K, R = a.K - 1;
@@ -148,7 +153,7 @@ __global__ void __launch_bounds__(kPrepThreads) kda_prep_kernel(PrepArgs a) {
     }
     float rate = 0.0f;
     float4 dt = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-    if constexpr (GATE_MODE == 0) {
+    if (GATE_MODE == 0 && has_gate) {
         rate = expf(a.a_log[h]);
         dt = *reinterpret_cast<const float4*>(a.dt_bias + c);
     }
@@ -158,7 +163,7 @@ __global__ void __launch_bounds__(kPrepThreads) kda_prep_kernel(PrepArgs a) {
     float4 nq = has_qk ? load_raw4<BF16>(a.q_raw, r0 * Cq + c) : z4;
     float4 nk = has_qk ? load_raw4<BF16>(a.k_raw, r0 * Cq + c) : z4;
     float4 nv = load_raw4<BF16>(a.v_raw, r0 * C + c);
-    float4 nf = GATE_MODE == 0 ? *reinterpret_cast<const float4*>(a.f_raw + r0 * C + c)
+    float4 nf = GATE_MODE == 0 && has_gate ? *reinterpret_cast<const float4*>(a.f_raw + r0 * Cg + c)
                                : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
     for (int i = 0; i < nr; ++i) {
         const long r = r0 + i;
@@ -169,7 +174,8 @@ __global__ void __launch_bounds__(kPrepThreads) kda_prep_kernel(PrepArgs a) {
                 nk = load_raw4<BF16>(a.k_raw, (r + 1) * Cq + c);
             }
             nv = load_raw4<BF16>(a.v_raw, (r + 1) * C + c);
-            if (GATE_MODE == 0) nf = *reinterpret_cast<const float4*>(a.f_raw + (r + 1) * C + c);
+            if (GATE_MODE == 0 && has_gate)
+                nf = *reinterpret_cast<const float4*>(a.f_raw + (r + 1) * Cg + c);
         }
         float4 xq, xk, xv;
         if constexpr (CONV) {
@@ -209,19 +215,19 @@ __global__ void __launch_bounds__(kPrepThreads) kda_prep_kernel(PrepArgs a) {
             *reinterpret_cast<float4*>(a.k_hat + r * Cq + c) =
                 make_float4(xk.x * ik, xk.y * ik, xk.z * ik, xk.w * ik);
         }
-        if constexpr (GATE_MODE == 0) {
+        if (GATE_MODE == 0 && has_gate) {
             float4 g = make_float4(kda_gate_f(cf.x, dt.x, rate, a.gate_lb), kda_gate_f(cf.y, dt.y, rate, a.gate_lb),
                                    kda_gate_f(cf.z, dt.z, rate, a.gate_lb), kda_gate_f(cf.w, dt.w, rate, a.gate_lb));
             if (EXP) g = make_float4(decay_f(g.x), decay_f(g.y), decay_f(g.z), decay_f(g.w));
-            *reinterpret_cast<float4*>(a.g + r * C + c) = g;
+            *reinterpret_cast<float4*>(a.g + r * Cg + c) = g;
         }
     }
-    if (lane < nr) {
+    if (lane < nr && has_gate) {
         const long r = r0 + lane;
-        a.beta[r * H + h] = sigmoid_f(a.beta_raw[r * H + h]);
+        a.beta[r * Hg + h] = sigmoid_f(a.beta_raw[r * Hg + h]);
         if constexpr (GATE_MODE == 1) {
-            const float gl = gdn_gate_f(a.f_raw[r * H + h], a.dt_bias[h], a.a_log[h]);
-            a.g[r * H + h] = EXP ? decay_f(gl) : gl;
+            const float gl = gdn_gate_f(a.f_raw[r * Hg + h], a.dt_bias[h], a.a_log[h]);
+            a.g[r * Hg + h] = EXP ? decay_f(gl) : gl;
         }
     }
 }

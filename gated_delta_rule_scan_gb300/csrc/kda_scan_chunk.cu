@@ -70,8 +70,11 @@ kda_chunk_intra_kernel(ScanArgs a, const int* chunk_off, unsigned char* ws) {
     const int nt = (int)min((long)kCc, end - row0);
     unsigned char* blk = ws + ((long)gid * H + h) * kBlkBytes;
     const long hoff = row0 * C + (long)h * kHeadDim;
-    const long Ck = (long)qk_heads(a) * kHeadDim;     // q and k rows: the head h % Hk
-    const long qkoff = row0 * Ck + (long)(h % qk_heads(a)) * kHeadDim;
+    const long Ck = (long)qk_heads(a) * kHeadDim;     // q and k rows: the head (h / vsub) % Hk
+    const long qkoff = row0 * Ck + (long)unit_qk_head(a, h) * kHeadDim;
+    const int gh = gate_head(a, h), Hg = gate_heads(a);   // the value head: gate and beta
+    const long Cg = (long)Hg * kHeadDim;
+    const long goff = row0 * Cg + (long)gh * kHeadDim;
 
     // ---- every global load of the chunk is issued before any store ---------------------------
     // column role: channel tid over the chunk's 32 tokens
@@ -81,7 +84,7 @@ kda_chunk_intra_kernel(ScanArgs a, const int* chunk_off, unsigned char* ws) {
         const bool live = t < nt;
         kc[t] = live ? __ldg(a.k + qkoff + t * Ck + tid) : 0.0f;
         vc[t] = live ? __ldg(a.v + hoff + t * C + tid) : 0.0f;
-        if (GATE_MODE == 0) gc[t] = live ? __ldg(a.g + hoff + t * C + tid) : (EXP ? 1.0f : 0.0f);
+        if (GATE_MODE == 0) gc[t] = live ? __ldg(a.g + goff + t * Cg + tid) : (EXP ? 1.0f : 0.0f);
     }
     // row role: tokens tr + 8j (j = 0..3), channels k0 .. k0+7
     const int tr = tid >> 4, k0 = (tid & 15) * 8;
@@ -100,9 +103,9 @@ kda_chunk_intra_kernel(ScanArgs a, const int* chunk_off, unsigned char* ws) {
     }
     if (tid < kCc) {
         const bool live = tid < nt;
-        sm.beta[tid] = live ? a.beta[(row0 + tid) * H + h] : 0.0f;
+        sm.beta[tid] = live ? a.beta[(row0 + tid) * Hg + gh] : 0.0f;
         if (GATE_MODE == 1) {
-            const float x = live ? a.g[(row0 + tid) * H + h] : (EXP ? 1.0f : 0.0f);
+            const float x = live ? a.g[(row0 + tid) * Hg + gh] : (EXP ? 1.0f : 0.0f);
             sm.gs[tid] = EXP ? logf(x) : x;
         }
     }

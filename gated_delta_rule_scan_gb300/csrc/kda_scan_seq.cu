@@ -64,7 +64,9 @@ kda_scan_seq_kernel(ScanArgs a, const __grid_constant__ CUtensorMap tq,
     const int cw = (warp * (32 / kScanG) + grp) * 4;   // first of the group's 4 columns in the CTA
     const int H = a.H;
     const long C = (long)H * kHeadDim;
-    const int kh = h % qk_heads(a);             // the q / k head this value head reads
+    const int gh = gate_head(a, h);             // the value head: its gate and beta
+    const int Hg = gate_heads(a);
+    const int kh = unit_qk_head(a, h);          // the q / k head this value head reads
 
     long begin, end;
     if (a.seq.cu_seqlens == nullptr) {
@@ -100,15 +102,15 @@ kda_scan_seq_kernel(ScanArgs a, const __grid_constant__ CUtensorMap tq,
         mbar_arrive_expect_tx(&sm.bar[st], kTxBytes);
         tma_load_2d(&sm.q[st][0][0], &tq, kh * kHeadDim, row, &sm.bar[st]);
         tma_load_2d(&sm.k[st][0][0], &tk, kh * kHeadDim, row, &sm.bar[st]);
-        if (GATE_MODE == 0) tma_load_2d(&sm.g[st][0][0], &tg, h * kHeadDim, row, &sm.bar[st]);
+        if (GATE_MODE == 0) tma_load_2d(&sm.g[st][0][0], &tg, gh * kHeadDim, row, &sm.bar[st]);
         tma_load_2d(&sm.v[st][0][0], &tv, h * kHeadDim + cb * kScanCols, row, &sm.bar[st]);
     };
     if (tid == 0 && nblk > 0) issue(0, 0);
 
     float bpre = 0.0f, gpre = 0.0f;
     if (tid < kScanTB && tid < L) {
-        bpre = a.beta[(begin + tid) * H + h];
-        if (GATE_MODE == 1) gpre = a.g[(begin + tid) * H + h];
+        bpre = a.beta[(begin + tid) * Hg + gh];
+        if (GATE_MODE == 1) gpre = a.g[(begin + tid) * Hg + gh];
     }
 
     for (int b = 0; b < nblk; ++b) {
@@ -120,8 +122,8 @@ kda_scan_seq_kernel(ScanArgs a, const __grid_constant__ CUtensorMap tq,
             if (GATE_MODE == 1) sm.ascal[st][tid] = EXP_DONE ? gpre : decay_f(gpre);
             const long rn = row0 + kScanTB + tid;
             if (rn < end) {
-                bpre = a.beta[rn * H + h];
-                if (GATE_MODE == 1) gpre = a.g[rn * H + h];
+                bpre = a.beta[rn * Hg + gh];
+                if (GATE_MODE == 1) gpre = a.g[rn * Hg + gh];
             }
         }
         const bool arrived = mbar_wait_bounded(&sm.bar[st], (uint32_t)((b >> 1) & 1), a.err);
@@ -238,7 +240,8 @@ static cudaError_t launch_t(const ScanArgs& a, cudaStream_t s) {
         !make_tensor_map_2d(&tv, a.v, rows, C, kScanCols, kScanTB))
         return cudaErrorInvalidValue;
     if (GM == 0) {
-        if (!make_tensor_map_2d(&tg, a.g, rows, C, kHeadDim, kScanTB)) return cudaErrorInvalidValue;
+        const long Cg = (long)gate_heads(a) * kHeadDim;   // gate rows: the value heads
+        if (!make_tensor_map_2d(&tg, a.g, rows, Cg, kHeadDim, kScanTB)) return cudaErrorInvalidValue;
     } else {
         tg = tq;  // unused
     }

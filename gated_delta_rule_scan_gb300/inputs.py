@@ -19,6 +19,10 @@ set of tensors on every machine:
  11. gate_raw (z)            N(0, 1), [rows, C]            (epilogue on)
  12. split points            integers in [1, L-1] per sequence (varlen only)
 
+A value head width Dv (a multiple of D) widens the v plane, its conv/ring rows, gate_raw and norm_w
+to Dv per head and the state to [N, H, Dv, D]; the gate stays D (the key dim) per head.  With Dv = D
+the draws are the ones above, value for value.
+
 Tensors come back as CPU torch tensors (f32, or bf16 for the raw q/k/v planes when asked);
 callers move them to the device themselves.
 """
@@ -57,6 +61,7 @@ class KdaInputs:
     split_points: np.ndarray | None = None
     meta: dict = field(default_factory=dict)
     Hk: int | None = None             # grouped queries: q/k planes of Hk heads (None: H)
+    Dv: int | None = None             # value head width (None: D)
 
     @property
     def rows(self) -> int:
@@ -64,7 +69,7 @@ class KdaInputs:
 
     @property
     def C(self) -> int:
-        return self.H * self.D
+        return self.H * (self.D if self.Dv is None else self.Dv)
 
     @property
     def uniform_T(self) -> int | None:
@@ -84,14 +89,16 @@ def make_inputs(seed: int, *, H: int, N: int = 1, T: int | None = None,
                 lengths: tuple[int, int] | None = None, D: int = D_HEAD, K: int = CONV_K,
                 raw_dtype: str = "f32", conv: bool = True, ring: str = "zero",
                 gate_mode: int = 0, state: str = "zero", epilogue: bool = True,
-                split: bool = False, Hk: int | None = None) -> KdaInputs:
+                split: bool = False, Hk: int | None = None,
+                Dv: int | None = None) -> KdaInputs:
     """Draw one workload.  Exactly one of ``T`` (N sequences of T tokens) and ``lengths``
     (N sequence lengths drawn uniformly from [lo, hi], packed with cu_seqlens) is given.
     ``Hk``: grouped queries -- the q and k planes (and their conv weight and ring rows) hold Hk
-    heads, v and everything per value head H."""
+    heads, v and everything per value head H.  ``Dv``: value heads Dv wide (q/k stay D)."""
     rng = np.random.default_rng(seed)
-    C = H * D
-    Cq = C if Hk is None else Hk * D
+    Cg = H * D                                  # per-channel gate: the key dim of each value head
+    C = H * (D if Dv is None else Dv)           # the v plane, gate_raw, y
+    Cq = Cg if Hk is None else Hk * D
     if lengths is not None:
         L = rng.integers(lengths[0], lengths[1], size=N, endpoint=True).astype(np.int64)
     else:
@@ -111,18 +118,19 @@ def make_inputs(seed: int, *, H: int, N: int = 1, T: int | None = None,
         ring_in = (_normal(rng, (N, 2 * Cq + C, K - 1)) if ring == "randn"
                    else torch.zeros(N, 2 * Cq + C, K - 1))
     if gate_mode == 0:
-        f_raw = _normal(rng, (rows, C))
-        dt_bias = _normal(rng, (C,), 0.5)
+        f_raw = _normal(rng, (rows, Cg))
+        dt_bias = _normal(rng, (Cg,), 0.5)
     else:
         f_raw = _normal(rng, (rows, H))
         dt_bias = _normal(rng, (H,), 0.5)
     a_log = torch.from_numpy(np.log(rng.uniform(1.0, 16.0, size=H)).astype(np.float32))
     beta_raw = _normal(rng, (rows, H))
-    state_in = (_normal(rng, (N, H, D, D), 0.02) if state == "randn"
-                else torch.zeros(N, H, D, D))
+    Dvw = D if Dv is None else Dv
+    state_in = (_normal(rng, (N, H, Dvw, D), 0.02) if state == "randn"
+                else torch.zeros(N, H, Dvw, D))
     norm_w = gate_raw = None
     if epilogue:
-        norm_w = 1.0 + _normal(rng, (D,), 0.1)
+        norm_w = 1.0 + _normal(rng, (Dvw,), 0.1)
         gate_raw = _normal(rng, (rows, C))
     splits = None
     if split:
@@ -132,7 +140,7 @@ def make_inputs(seed: int, *, H: int, N: int = 1, T: int | None = None,
                      v_raw=planes[2], conv_w=conv_w, ring_in=ring_in, f_raw=f_raw,
                      dt_bias=dt_bias, a_log=a_log, beta_raw=beta_raw, state_in=state_in,
                      norm_w=norm_w, gate_raw=gate_raw, gate_mode=gate_mode, split_points=splits,
-                     meta=dict(seed=seed, raw_dtype=raw_dtype), Hk=Hk)
+                     meta=dict(seed=seed, raw_dtype=raw_dtype), Hk=Hk, Dv=Dv)
 
 
 # ------------------------------------------------------------------------------------------

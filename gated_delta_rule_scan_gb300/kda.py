@@ -113,6 +113,19 @@ _lib.kda_proj6_workspace_bytes.argtypes = [_I, _I]
 _lib.kda_proj6.restype = _I
 _lib.kda_proj6.argtypes = [_P, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _P,
                            _Z, _P]
+_lib.kda_conv_l2norm_prep_dv.restype = _I
+_lib.kda_conv_l2norm_prep_dv.argtypes = [_P, _P, _P, _I, _P, _P, _P, _P, _P, _P, _I, _F, _P, _P,
+                                         _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P]
+_lib.kda_conv_l2norm_prep_varlen_dv.restype = _I
+_lib.kda_conv_l2norm_prep_varlen_dv.argtypes = [_P, _P, _P, _I, _P, _P, _P, _P, _P, _P, _I, _F,
+                                                _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I,
+                                                _I, _I, _I, _F, _P]
+_lib.kda_scan_dv.restype = _I
+_lib.kda_scan_dv.argtypes = [_P, _P, _P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I,
+                             _P, _Z, _P]
+_lib.kda_scan_varlen_dv.restype = _I
+_lib.kda_scan_varlen_dv.argtypes = [_P, _P, _P, _P, _I, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I,
+                                    _I, _I, _F, _I, _P, _Z, _P]
 _lib.kda_selftest_wait_timeout.restype = _I
 _lib.kda_selftest_wait_timeout.argtypes = [_P]
 
@@ -126,7 +139,9 @@ EXPORTED = ("kda_abi_version", "kda_status_string", "kda_conv_l2norm_prep",
             "kda_selftest_wait_timeout", "kda_scan_gqa", "kda_scan_varlen_gqa",
             "kda_proj6_workspace_bytes", "kda_proj6", "kda_conv_l2norm_prep_gqa",
             "kda_conv_l2norm_prep_varlen_gqa", "kda_prefill_fused_gqa",
-            "kda_prefill_fused_varlen_gqa", "kda_decode_fused_gqa", "kda_verify_rollback_gqa")
+            "kda_prefill_fused_varlen_gqa", "kda_decode_fused_gqa", "kda_verify_rollback_gqa",
+            "kda_conv_l2norm_prep_dv", "kda_conv_l2norm_prep_varlen_dv", "kda_scan_dv",
+            "kda_scan_varlen_dv")
 
 
 class KdaError(RuntimeError):
@@ -278,6 +293,62 @@ def kda_scan_varlen(q_hat, k_hat, v_hat, g, beta, state_in, state_out, o, cu_seq
         _ptr(q_hat), _ptr(k_hat), _ptr(v_hat), _ptr(g), gate_mode, _ptr(beta), _ptr(state_in),
         _ptr(state_out), _ptr(o), _ptr(cu_seqlens), _ptr(cu_seqlens_host), N, total, H, D, scale,
         algo, _ptr(workspace), ws_bytes, st)
+
+
+def kda_conv_l2norm_prep_dv(q_raw, k_raw, v_raw, conv_w, ring_in, ring_out, f_raw, dt_bias,
+                            a_log, beta_raw, q_hat, k_hat, v_hat, g, beta, *, N, T, H, Dv,
+                            Hk=None, K=4, gate_mode=0, gate_lb=-5.0, l2_eps=1e-6, Dk=HEAD_DIM,
+                            stream=None):
+    """The prep with value heads Dv wide (a multiple of 128) and q/k heads Dk = 128 wide."""
+    st = _stream(stream, q_hat)
+    _call("kda_conv_l2norm_prep_dv", q_hat,
+        _ptr(q_raw), _ptr(k_raw), _ptr(v_raw), _raw_dtype(q_raw), _ptr(conv_w), _ptr(ring_in),
+        _ptr(ring_out), _ptr(f_raw), _ptr(dt_bias), _ptr(a_log), gate_mode, gate_lb,
+        _ptr(beta_raw), _ptr(q_hat), _ptr(k_hat), _ptr(v_hat), _ptr(g), _ptr(beta), N, T, H,
+        H if Hk is None else Hk, Dk, Dv, K, l2_eps, st)
+
+
+def kda_conv_l2norm_prep_varlen_dv(q_raw, k_raw, v_raw, conv_w, ring_in, ring_out, f_raw,
+                                   dt_bias, a_log, beta_raw, q_hat, k_hat, v_hat, g, beta,
+                                   cu_seqlens, cu_seqlens_host, *, H, Dv, Hk=None, K=4,
+                                   gate_mode=0, gate_lb=-5.0, l2_eps=1e-6, Dk=HEAD_DIM,
+                                   stream=None):
+    """kda_conv_l2norm_prep_dv over packed sequences."""
+    N = cu_seqlens_host.numel() - 1
+    total = int(cu_seqlens_host[-1])
+    st = _stream(stream, q_hat)
+    _call("kda_conv_l2norm_prep_varlen_dv", q_hat,
+        _ptr(q_raw), _ptr(k_raw), _ptr(v_raw), _raw_dtype(q_raw), _ptr(conv_w), _ptr(ring_in),
+        _ptr(ring_out), _ptr(f_raw), _ptr(dt_bias), _ptr(a_log), gate_mode, gate_lb,
+        _ptr(beta_raw), _ptr(q_hat), _ptr(k_hat), _ptr(v_hat), _ptr(g), _ptr(beta),
+        _ptr(cu_seqlens), _ptr(cu_seqlens_host), N, total, H, H if Hk is None else Hk, Dk, Dv, K,
+        l2_eps, st)
+
+
+def kda_scan_dv(q_hat, k_hat, v_hat, g, beta, state_in, state_out, o, *, N, T, H, Dv, Hk=None,
+                gate_mode=0, scale=None, algo=ALGO_AUTO, workspace=None, Dk=HEAD_DIM,
+                stream=None):
+    """kda_scan with a Dk x Dv state per value head (state [N, H, Dv, Dk])."""
+    scale = Dk ** -0.5 if scale is None else scale
+    st = _stream(stream, state_out)
+    _call("kda_scan_dv", state_out,
+        _ptr(q_hat), _ptr(k_hat), _ptr(v_hat), _ptr(g), gate_mode, _ptr(beta), _ptr(state_in),
+        _ptr(state_out), _ptr(o), N, T, H, H if Hk is None else Hk, Dk, Dv, scale, algo,
+        _ptr(workspace), _ws_bytes(workspace), st)
+
+
+def kda_scan_varlen_dv(q_hat, k_hat, v_hat, g, beta, state_in, state_out, o, cu_seqlens,
+                       cu_seqlens_host, *, H, Dv, Hk=None, gate_mode=0, scale=None,
+                       algo=ALGO_AUTO, workspace=None, Dk=HEAD_DIM, stream=None):
+    """kda_scan_dv over packed sequences."""
+    N = cu_seqlens_host.numel() - 1
+    total = int(cu_seqlens_host[-1])
+    scale = Dk ** -0.5 if scale is None else scale
+    st = _stream(stream, state_out)
+    _call("kda_scan_varlen_dv", state_out,
+        _ptr(q_hat), _ptr(k_hat), _ptr(v_hat), _ptr(g), gate_mode, _ptr(beta), _ptr(state_in),
+        _ptr(state_out), _ptr(o), _ptr(cu_seqlens), _ptr(cu_seqlens_host), N, total, H,
+        H if Hk is None else Hk, Dk, Dv, scale, algo, _ptr(workspace), _ws_bytes(workspace), st)
 
 
 def kda_scan_varlen_static(q_hat, k_hat, v_hat, g, beta, state_in, state_out, o, cu_seqlens,

@@ -26,7 +26,7 @@ def kda_forward(*, q_raw, k_raw, v_raw, f_raw, dt_bias, a_log, beta_raw, state_i
                 cu_seqlens_host=None, N=None, T=None, K=4, gate_mode=0, gate_lb=-5.0,
                 l2_eps=1e-6, rms_eps=1e-6, scale=None, algo=kda.ALGO_AUTO, state_out=None,
                 ring_out=None, out=None, gate_exp=None, workspace=None, stream=None,
-                norm_gate="sigmoid", Hk=None):
+                norm_gate="sigmoid", Hk=None, Dv=None):
     """Run the mixer on device tensors.  Either (N, T) for N sequences of T tokens, or
     cu_seqlens (int32 device) + cu_seqlens_host (int32 CPU) for packed sequences.
     gate_exp: hand the gate from the prep to the scan as decay factors exp(log-decay) (the
@@ -37,10 +37,14 @@ def kda_forward(*, q_raw, k_raw, v_raw, f_raw, dt_bias, a_log, beta_raw, state_i
     is given.
     norm_gate: the RMSNorm's gate, "sigmoid" (KDA) or "silu" (GDN's gated_rmsnorm).
     Hk: grouped queries (q_raw / k_raw of Hk heads, value head h reads q/k head h % Hk).
+    Dv: value heads Dv wide (a multiple of 128; q/k heads stay 128 wide; state [N, H, Dv, 128]).
     Returns a dict with q_hat, k_hat, v_hat, g, beta, o, y (None without an epilogue),
     state_out and ring_out."""
     D = kda.HEAD_DIM
-    C = H * D
+    wide = Dv is not None
+    Dv = D if Dv is None else Dv
+    C = H * Dv
+    Cg = H * D                      # per-channel gate rows: the key dim of every value head
     Cq = (H if Hk is None else Hk) * D
     rows = q_raw.shape[0]
     varlen = cu_seqlens is not None
@@ -55,7 +59,7 @@ def kda_forward(*, q_raw, k_raw, v_raw, f_raw, dt_bias, a_log, beta_raw, state_i
     q_hat = take("q_hat", (rows, Cq))
     k_hat = take("k_hat", (rows, Cq))
     v_hat = take("v_hat", (rows, C))
-    g = take("g", (rows, C) if gate_mode == 0 else (rows, H))
+    g = take("g", (rows, Cg) if gate_mode == 0 else (rows, H))
     beta = take("beta", (rows, H))
     o = take("o", (rows, C))
     if state_out is None:
@@ -63,13 +67,29 @@ def kda_forward(*, q_raw, k_raw, v_raw, f_raw, dt_bias, a_log, beta_raw, state_i
     if conv_w is not None and ring_out is None:
         ring_out = torch.empty_like(ring_in)
     if workspace is None and algo != kda.ALGO_SEQ:
-        workspace = kda.scan_workspace(n_seq, rows, H, q_raw.device, algo)
+        workspace = kda.scan_workspace(n_seq, rows, H * Dv // D, q_raw.device, algo)
     if gate_exp is None:
         gate_exp = algo == kda.ALGO_SEQ
     gm = gate_mode | (kda.GATE_EXP if gate_exp else 0)
     common = dict(H=H, K=K, gate_mode=gm, gate_lb=gate_lb, l2_eps=l2_eps, stream=stream, Hk=Hk)
     scan_kw = dict(H=H, gate_mode=gm, scale=scale, algo=algo, workspace=workspace, stream=stream)
-    if varlen:
+    if wide:
+        common.update(Dv=Dv)
+        scan_kw.update(Hk=Hk, Dv=Dv)
+        if varlen:
+            kda.kda_conv_l2norm_prep_varlen_dv(q_raw, k_raw, v_raw, conv_w, ring_in, ring_out,
+                                               f_raw, dt_bias, a_log, beta_raw, q_hat, k_hat,
+                                               v_hat, g, beta, cu_seqlens, cu_seqlens_host,
+                                               **common)
+            kda.kda_scan_varlen_dv(q_hat, k_hat, v_hat, g, beta, state_in, state_out, o,
+                                   cu_seqlens, cu_seqlens_host, **scan_kw)
+        else:
+            kda.kda_conv_l2norm_prep_dv(q_raw, k_raw, v_raw, conv_w, ring_in, ring_out, f_raw,
+                                        dt_bias, a_log, beta_raw, q_hat, k_hat, v_hat, g, beta,
+                                        N=N, T=T, **common)
+            kda.kda_scan_dv(q_hat, k_hat, v_hat, g, beta, state_in, state_out, o, N=N, T=T,
+                            **scan_kw)
+    elif varlen:
         kda.kda_conv_l2norm_prep_varlen(q_raw, k_raw, v_raw, conv_w, ring_in, ring_out, f_raw,
                                         dt_bias, a_log, beta_raw, q_hat, k_hat, v_hat, g, beta,
                                         cu_seqlens, cu_seqlens_host, **common)
@@ -93,7 +113,7 @@ def kda_forward(*, q_raw, k_raw, v_raw, f_raw, dt_bias, a_log, beta_raw, state_i
         y = take("y", (rows, C))
         _norm_flag(norm_gate)
         norm = kda.kda_gated_rmsnorm_silu_out if norm_gate == "silu" else kda.kda_gated_rmsnorm_out
-        norm(o, norm_w, gate_raw, y, rows=rows * H, eps=rms_eps, stream=stream)
+        norm(o, norm_w, gate_raw, y, rows=rows * H, eps=rms_eps, D=Dv, stream=stream)
     return dict(q_hat=q_hat, k_hat=k_hat, v_hat=v_hat, g=g, beta=beta, o=o, y=y,
                 state_out=state_out, ring_out=ring_out, n_seq=n_seq)
 

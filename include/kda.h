@@ -255,6 +255,8 @@ int kda_scan_varlen_static(const float* q_hat, const float* k_hat, const float* 
  * sigmoid; the gate is not normalised.
  * o, gate_raw, y   [rows, D] f32 [16B] (rows = tokens * heads);  norm_w [D] f32 [16B], shared by
  * all heads.  y may alias o.
+ * D                the value head width: 128 * m for m = 1..8 (40001 otherwise); the mean runs over
+ *                  the whole row of D values.
  */
 int kda_gated_rmsnorm_out(const float* o, const float* norm_w, const float* gate_raw, float* y,
                           long rows, int D, float eps, void* stream);
@@ -435,6 +437,49 @@ int kda_verify_rollback_gqa(const void* q_raw, const void* k_raw, const void* v_
                             const float* norm_w, const float* gate_raw, float* y, const int* keep,
                             int N, int T, int H, int Hk, int D, int K, float l2_eps, float scale,
                             float rms_eps, void* stream);
+
+/*
+ * A value head wider than the key head (the GDN page's head dims, aprender-serve gdn_ops.rs
+ * `gdn_delta_rule_into` doc: q and k are num_k_heads * head_k_dim wide, v num_v_heads *
+ * head_v_dim, and the state of one value head is head_v_dim x head_k_dim).  Dk = 128 and
+ * Dv = 128 * m, m = 1..8 (40001 otherwise); H value heads, Hk q/k heads (1 <= Hk <= H, value head
+ * h reads q/k head h % Hk; 40005 otherwise).  Layouts, row-major f32 unless stated:
+ *   q_raw, k_raw, q_hat, k_hat  [rows, Hk*Dk];  v_raw, v_hat, o  [rows, H*Dv];
+ *   f_raw, g   [rows, H*Dk] (gate_mode 0: the decay is over the key dim) or [rows, H] (mode 1);
+ *   dt_bias    [H*Dk] (mode 0) or [H];  a_log, beta_raw rows, beta rows  [H] per row;
+ *   conv_w     [2*Hk*Dk + H*Dv, K], rows [q | k | v];  ring [N, 2*Hk*Dk + H*Dv, K-1];
+ *   state      [N, H, Dv, Dk] f32 [16B]: state[n][h][j][i] couples value column j and key row i.
+ * The scan is kda_scan's recurrence with a Dk x Dv state per value head, run as m independent
+ * 128-wide value column blocks (column block b of value head h is unit h*m + b of a kda_scan with
+ * H*m heads, sharing value head h's gate, beta and q/k head: the recurrence's columns never mix).
+ * The workspace for the chunked form is kda_scan_workspace_bytes(N, total_T, H*m, 128, ...).
+ * The gated RMSNorm over rows of Dv values is kda_gated_rmsnorm_out / _silu_out with D = Dv.
+ */
+int kda_conv_l2norm_prep_dv(const void* q_raw, const void* k_raw, const void* v_raw,
+                            int raw_dtype, const float* conv_w, const float* ring_in,
+                            float* ring_out, const float* f_raw, const float* dt_bias,
+                            const float* a_log, int gate_mode, float gate_lb,
+                            const float* beta_raw, float* q_hat, float* k_hat, float* v_hat,
+                            float* g, float* beta, int N, int T, int H, int Hk, int Dk, int Dv,
+                            int K, float l2_eps, void* stream);
+int kda_conv_l2norm_prep_varlen_dv(const void* q_raw, const void* k_raw, const void* v_raw,
+                                   int raw_dtype, const float* conv_w, const float* ring_in,
+                                   float* ring_out, const float* f_raw, const float* dt_bias,
+                                   const float* a_log, int gate_mode, float gate_lb,
+                                   const float* beta_raw, float* q_hat, float* k_hat,
+                                   float* v_hat, float* g, float* beta, const int* cu_seqlens,
+                                   const int* cu_seqlens_host, int N, int total_T, int H, int Hk,
+                                   int Dk, int Dv, int K, float l2_eps, void* stream);
+int kda_scan_dv(const float* q_hat, const float* k_hat, const float* v_hat, const float* g,
+                int gate_mode, const float* beta, const float* state_in, float* state_out,
+                float* o, int N, int T, int H, int Hk, int Dk, int Dv, float scale, int algo,
+                void* workspace, size_t workspace_bytes, void* stream);
+int kda_scan_varlen_dv(const float* q_hat, const float* k_hat, const float* v_hat,
+                       const float* g, int gate_mode, const float* beta, const float* state_in,
+                       float* state_out, float* o, const int* cu_seqlens,
+                       const int* cu_seqlens_host, int N, int total_T, int H, int Hk, int Dk,
+                       int Dv, float scale, int algo, void* workspace, size_t workspace_bytes,
+                       void* stream);
 
 /*
  * kda_proj6 -- stage 1 of kda_core_gated: the six projections of the layer input that the mixer

@@ -43,6 +43,8 @@ def gpu_forward(inp: KdaInputs, *, varlen=None, algo=0, **kw):
         extra = dict(N=inp.N, T=T)
     if inp.Hk is not None:
         kw = dict(kw, Hk=inp.Hk)
+    if inp.Dv is not None:
+        kw = dict(kw, Dv=inp.Dv)
     out = mixer.kda_forward(H=inp.H, K=inp.K, gate_mode=inp.gate_mode, algo=algo, **d, **extra,
                             **kw)
     torch.cuda.synchronize()
@@ -73,17 +75,18 @@ def head_channels(heads, D=128):
 
 
 def oracle_forward(inp: KdaInputs, heads=None, **kw):
-    """The f64 oracle on the workload (all heads, or the listed ones; grouped-query workloads
-    run on all heads)."""
+    """The f64 oracle on the workload (all heads, or the listed ones; grouped-query and
+    value-width workloads run on all heads)."""
     from oracle import oracle as orc
     H, D = inp.H, inp.D
-    if inp.Hk is not None:
+    if inp.Hk is not None or inp.Dv is not None:
         assert heads is None or list(heads) == list(range(H)), "grouped queries: all heads"
         return orc.forward(
             q_raw=inp.q_raw, k_raw=inp.k_raw, v_raw=inp.v_raw, f_raw=inp.f_raw,
             dt_bias=inp.dt_bias, a_log=inp.a_log, beta_raw=inp.beta_raw, state_in=inp.state_in,
             H=H, D=D, conv_w=inp.conv_w, ring_in=inp.ring_in, cu_seqlens=inp.cu_seqlens,
-            gate_mode=inp.gate_mode, norm_w=inp.norm_w, gate_raw=inp.gate_raw, Hk=inp.Hk, **kw)
+            gate_mode=inp.gate_mode, norm_w=inp.norm_w, gate_raw=inp.gate_raw, Hk=inp.Hk,
+            Dv=inp.Dv, **kw)
     heads = list(range(H)) if heads is None else list(heads)
     ch = head_channels(heads, D)
     C = H * D
@@ -118,7 +121,7 @@ def check_all_heads(out, inp: KdaInputs, keys, tol=TOL, ring_exact=True, budget=
     host = {}
     for k in keys:
         host[k] = out[k].detach().cpu() if isinstance(out[k], torch.Tensor) else out[k]
-    if inp.Hk is not None:                   # grouped queries: one oracle run over every head
+    if inp.Hk is not None or inp.Dv is not None:   # one oracle run over every head
         ref = oracle_forward(inp, **kw)
         errs = {}
         for k in keys:

@@ -197,3 +197,34 @@ def test_proj6_contract(kda):
     assert call(x=FAKE + 4) == 40010
     assert call(wsb=ws_need - 1) == 40009
     assert call(ws=None) == 40009
+
+
+def test_value_width_contract(kda):
+    """The value-width entries take Dk = 128 and Dv = 128 * m (m = 1..8), 1 <= Hk <= H."""
+    lib = kda.library()
+    F = ctypes.c_float
+    scan = lambda **kw: lib.kda_scan_dv(  # noqa: E731
+        FAKE, FAKE, FAKE, FAKE, 0, FAKE, FAKE, FAKE * 8, FAKE, 1, 4, kw.get("H", 2),
+        kw.get("Hk", 1), kw.get("Dk", 128), kw.get("Dv", 256), F(0.1), 1, None, 0, None)
+    for dv in (0, 64, 192, 1152, -128):
+        assert scan(Dv=dv) == 40001, dv
+    assert scan(Dk=64) == 40001
+    assert scan(Hk=3) == 40005
+    assert scan(Hk=0) == 40005
+    assert scan(H=0) == 40005
+    prep = lambda **kw: lib.kda_conv_l2norm_prep_dv(  # noqa: E731
+        FAKE, FAKE, FAKE, 1, FAKE, FAKE, FAKE * 2, FAKE, FAKE, FAKE, 0, F(-5.0), FAKE, FAKE, FAKE,
+        FAKE, FAKE, FAKE, 1, 4, 2, kw.get("Hk", 2), 128, kw.get("Dv", 256), kw.get("K", 4),
+        F(1e-6), None)
+    assert prep(Dv=320) == 40001
+    assert prep(Hk=5) == 40005
+    assert prep(K=1) == 40002
+    cu = (ctypes.c_int * 3)(0, 3, 2)
+    rc = lib.kda_scan_varlen_dv(FAKE, FAKE, FAKE, FAKE, 0, FAKE, FAKE, FAKE * 8, FAKE, FAKE,
+                                ctypes.cast(cu, ctypes.c_void_p), 2, 2, 2, 2, 128, 256, F(0.1), 1,
+                                None, 0, None)
+    assert rc == 40006
+    for d in (192, 1152, 0):
+        norm = lib.kda_gated_rmsnorm_out(FAKE, FAKE, FAKE, FAKE, ctypes.c_long(4), d, F(1e-6),
+                                         None)
+        assert norm == 40001, d
