@@ -220,7 +220,8 @@ int prefill_impl(const void* q_raw, const void* k_raw, const void* v_raw, int ra
                  const float* norm_w, const float* gate_raw, float* y, const SeqLayout& seq,
                  const int* cu_host, int H, int D, int K, float l2_eps, float scale,
                  float norm_eps, void* workspace, size_t workspace_bytes, void* stream,
-                 int Hk = 0) {
+                 int Hk = 0, int Hg = 0) {
+    // H: 128-wide value units; Hg: value heads (H / Hg units each), 0 meaning H
     if (D != kHeadDim) return KDA_ERR_HEAD_DIM;
     if (seq.N < 0 || seq.N > kMaxGridY || seq.total_rows < 0 || H <= 0 || H > kMaxGridY)
         return KDA_ERR_SHAPE;
@@ -236,8 +237,9 @@ int prefill_impl(const void* q_raw, const void* k_raw, const void* v_raw, int ra
     PrepArgs pa;
     int rc = prep_build(q_raw, k_raw, v_raw, raw_dtype, conv_w, ring_in, ring_out, f_raw, dt_bias,
                         a_log, gate_mode, gate_lb, beta_raw, nullptr, nullptr, nullptr, nullptr,
-                        nullptr, seq, H, D, K, l2_eps, false, pa, Hk);
+                        nullptr, seq, H, D, K, l2_eps, false, pa, Hk, Hg);
     if (rc != KDA_OK) return rc;
+    const int vsub = H / pa.Hg;                  // prep_build checked that Hg divides H
     // the fused kernel copies bf16 raw rows into shared memory 16 bytes at a time
     if (seq.total_rows > 0 && pa.raw_bf16 &&
         (!aligned16(q_raw) || !aligned16(k_raw) || !aligned16(v_raw)))
@@ -255,12 +257,14 @@ int prefill_impl(const void* q_raw, const void* k_raw, const void* v_raw, int ra
     float* oh = reinterpret_cast<float*>(w + L.o);
     ScanArgs a{};
     a.Hk = pa.Hk;
+    a.vsub = vsub;
     a.gate_mode = gate_mode; a.state_in = state_in; a.state_out = state_out; a.o = oh;
     a.seq = seq; a.H = H; a.scale = scale; a.order = nullptr; a.err = dev_err_ptr();
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
     rc = cuda_status(launch_prefill_chunk(pa, a, cu_host, w + L.chunk, st));
     if (rc != KDA_OK || seq.total_rows == 0) return rc;
-    NormArgs na{oh, norm_w, gate_raw, y, seq.total_rows * H, norm_eps, norm_silu ? 1 : 0};
+    NormArgs na{oh, norm_w, gate_raw, y, seq.total_rows * pa.Hg, norm_eps, norm_silu ? 1 : 0,
+                vsub * kHeadDim};
     return cuda_status(launch_gated_rmsnorm(na, static_cast<cudaStream_t>(stream)));
 }
 
@@ -284,12 +288,16 @@ int decode_impl(const void* q_raw, const void* k_raw, const void* v_raw, int raw
                 const float* beta_raw, const float* state_in, float* state_out,
                 const float* norm_w, const float* gate_raw, float* y, int N, int T, int H, int D,
                 int K, float l2_eps, float scale, float rms_eps, const int* keep, bool rollback,
-                void* stream, int Hk = 0) {
+                void* stream, int Hk = 0, int Hg = 0) {
+    // H: 128-wide value units; Hg: value heads of H / Hg units each (0 meaning H)
     if (D != kHeadDim) return KDA_ERR_HEAD_DIM;
     if (N < 0 || N > kMaxGridY || H <= 0 || H > kMaxGridY || T < 1 || T > kDecodeMaxT)
         return KDA_ERR_SHAPE;
-    if (Hk == 0) Hk = H;
-    if (Hk < 1 || Hk > H) return KDA_ERR_SHAPE;
+    if (Hg == 0) Hg = H;
+    if (Hg < 1 || Hg > H || H % Hg != 0 || H / Hg > kMaxValueWidth / kHeadDim)
+        return KDA_ERR_SHAPE;
+    if (Hk == 0) Hk = Hg;
+    if (Hk < 1 || Hk > Hg) return KDA_ERR_SHAPE;
     if ((long)N * H >= (1L << 31)) return KDA_ERR_SHAPE;
     if (raw_dtype != KDA_DTYPE_F32 && raw_dtype != KDA_DTYPE_BF16) return KDA_ERR_ENUM;
     const bool norm_silu = (gate_mode & KDA_NORM_SILU) != 0;
@@ -311,12 +319,13 @@ int decode_impl(const void* q_raw, const void* k_raw, const void* v_raw, int raw
         const size_t rb = (size_t)N * ring_channels(H, Hk) * (K - 1) * sizeof(float);
         if (overlap(ring_in, ring_out, rb)) return KDA_ERR_STATE_ALIAS;
     } else if (Hk < H) {
-        // grouped queries: several value heads read one q/k ring row that only one of them
-        // rewrites, so the ring cannot be rolled in place
+        // grouped queries or value heads of several units: several units read one q/k ring row
+        // that only one of them rewrites, so the ring cannot be rolled in place
         return KDA_ERR_STATE_ALIAS;
     }
     DecodeArgs a{};
     a.Hk = Hk;
+    a.vsub = H / Hg;
     a.q_raw = q_raw; a.k_raw = k_raw; a.v_raw = v_raw; a.raw_bf16 = raw_dtype == KDA_DTYPE_BF16;
     a.conv_w = conv_w; a.ring_in = ring_in; a.ring_out = ring_out;
     a.f_raw = f_raw; a.dt_bias = dt_bias; a.a_log = a_log; a.gate_mode = gate_mode;
@@ -718,6 +727,84 @@ int kda_scan_varlen_dv(const float* q_hat, const float* k_hat, const float* v_ha
     return scan_impl(q_hat, k_hat, v_hat, g, gate_mode, beta, state_in, state_out, o, seq,
                      cu_seqlens_host, H * m, kHeadDim, scale, algo, workspace, workspace_bytes,
                      stream, Hk, m);
+}
+
+int kda_prefill_fused_dv(const void* q_raw, const void* k_raw, const void* v_raw, int raw_dtype,
+                         const float* conv_w, const float* ring_in, float* ring_out,
+                         const float* f_raw, const float* dt_bias, const float* a_log,
+                         int gate_mode, float gate_lb, const float* beta_raw,
+                         const float* state_in, float* state_out, const float* norm_w,
+                         const float* gate_raw, float* y, int N, int T, int H, int Hk, int Dk,
+                         int Dv, int K, float l2_eps, float scale, float rms_eps, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+    const int m = value_subheads(Dk, Dv);
+    if (m == 0) return KDA_ERR_HEAD_DIM;
+    if (N < 0 || T < 0 || H <= 0 || Hk <= 0 || Hk > H || (long)H * m > kMaxGridY)
+        return KDA_ERR_SHAPE;
+    SeqLayout seq{nullptr, T, N, (long)N * T};
+    return prefill_impl(q_raw, k_raw, v_raw, raw_dtype, conv_w, ring_in, ring_out, f_raw, dt_bias,
+                        a_log, gate_mode, gate_lb, beta_raw, state_in, state_out, norm_w, gate_raw,
+                        y, seq, nullptr, H * m, kHeadDim, K, l2_eps, scale, rms_eps, workspace,
+                        workspace_bytes, stream, Hk, H);
+}
+
+int kda_prefill_fused_varlen_dv(const void* q_raw, const void* k_raw, const void* v_raw,
+                                int raw_dtype, const float* conv_w, const float* ring_in,
+                                float* ring_out, const float* f_raw, const float* dt_bias,
+                                const float* a_log, int gate_mode, float gate_lb,
+                                const float* beta_raw, const float* state_in, float* state_out,
+                                const float* norm_w, const float* gate_raw, float* y,
+                                const int* cu_seqlens, const int* cu_seqlens_host, int N,
+                                int total_T, int H, int Hk, int Dk, int Dv, int K, float l2_eps,
+                                float scale, float rms_eps, void* workspace,
+                                size_t workspace_bytes, void* stream) {
+    const int m = value_subheads(Dk, Dv);
+    if (m == 0) return KDA_ERR_HEAD_DIM;
+    if (N < 0 || total_T < 0 || H <= 0 || Hk <= 0 || Hk > H || (long)H * m > kMaxGridY)
+        return KDA_ERR_SHAPE;
+    if (N > 0) {
+        if (cu_seqlens == nullptr) return KDA_ERR_NULL;
+        const int rc = check_cu(cu_seqlens_host, N, total_T);
+        if (rc) return rc;
+    }
+    SeqLayout seq{cu_seqlens, 0, N, (long)total_T};
+    return prefill_impl(q_raw, k_raw, v_raw, raw_dtype, conv_w, ring_in, ring_out, f_raw, dt_bias,
+                        a_log, gate_mode, gate_lb, beta_raw, state_in, state_out, norm_w, gate_raw,
+                        y, seq, cu_seqlens_host, H * m, kHeadDim, K, l2_eps, scale, rms_eps,
+                        workspace, workspace_bytes, stream, Hk, H);
+}
+
+int kda_decode_fused_dv(const void* q_raw, const void* k_raw, const void* v_raw, int raw_dtype,
+                        const float* conv_w, const float* ring_in, float* ring_out,
+                        const float* f_raw, const float* dt_bias, const float* a_log,
+                        int gate_mode, float gate_lb, const float* beta_raw,
+                        const float* state_in, float* state_out, const float* norm_w,
+                        const float* gate_raw, float* y, int N, int T, int H, int Hk, int Dk,
+                        int Dv, int K, float l2_eps, float scale, float rms_eps, void* stream) {
+    const int m = value_subheads(Dk, Dv);
+    if (m == 0) return KDA_ERR_HEAD_DIM;
+    if (H <= 0 || Hk <= 0 || Hk > H || (long)H * m > kMaxGridY) return KDA_ERR_SHAPE;
+    return decode_impl(q_raw, k_raw, v_raw, raw_dtype, conv_w, ring_in, ring_out, f_raw, dt_bias,
+                       a_log, gate_mode, gate_lb, beta_raw, state_in, state_out, norm_w, gate_raw,
+                       y, N, T, H * m, kHeadDim, K, l2_eps, scale, rms_eps, nullptr, false, stream,
+                       Hk, H);
+}
+
+int kda_verify_rollback_dv(const void* q_raw, const void* k_raw, const void* v_raw,
+                           int raw_dtype, const float* conv_w, const float* ring_in,
+                           float* ring_out, const float* f_raw, const float* dt_bias,
+                           const float* a_log, int gate_mode, float gate_lb,
+                           const float* beta_raw, const float* state_in, float* state_out,
+                           const float* norm_w, const float* gate_raw, float* y, const int* keep,
+                           int N, int T, int H, int Hk, int Dk, int Dv, int K, float l2_eps,
+                           float scale, float rms_eps, void* stream) {
+    const int m = value_subheads(Dk, Dv);
+    if (m == 0) return KDA_ERR_HEAD_DIM;
+    if (H <= 0 || Hk <= 0 || Hk > H || (long)H * m > kMaxGridY) return KDA_ERR_SHAPE;
+    return decode_impl(q_raw, k_raw, v_raw, raw_dtype, conv_w, ring_in, ring_out, f_raw, dt_bias,
+                       a_log, gate_mode, gate_lb, beta_raw, state_in, state_out, norm_w, gate_raw,
+                       y, N, T, H * m, kHeadDim, K, l2_eps, scale, rms_eps, keep, true, stream,
+                       Hk, H);
 }
 
 int kda_selftest_wait_timeout(void* stream) {

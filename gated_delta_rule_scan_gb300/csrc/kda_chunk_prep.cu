@@ -188,18 +188,23 @@ __device__ __forceinline__ void chunk_task(const SeqLayout& L, const int* chunk_
 }
 
 // A task of the persistent kernel: (global chunk gid, head h), task = h * nchunks + gid, and the
-// chunk's sequence n, rows and token count.  The host keeps h * nchunks + gid below 2^31.
+// chunk's sequence n, rows and token count.  The host keeps h * nchunks + gid below 2^31.  h is
+// a 128-wide value unit: with value heads vs * 128 wide it is column block h % vs of value head
+// gh = h / vs, whose gate, beta and q/k head hq = gh % Hk it reads.
 struct TaskPos {
     long begin, end, row0, gid;
     int n, h, nt;
+    int gh, hq;
 };
 
 __device__ __forceinline__ TaskPos task_pos(const SeqLayout& L, const int* chunk_off, long task,
-                                            long nchunks) {
+                                            long nchunks, int vs, int Hk) {
     TaskPos t;
     const unsigned tk = (unsigned)task, nc = (unsigned)nchunks;
     t.h = (int)(tk / nc);
     t.gid = (long)(tk - (unsigned)t.h * nc);
+    t.gh = vs == 1 ? t.h : t.h / vs;
+    t.hq = t.gh < Hk ? t.gh : t.gh % Hk;
     chunk_task(L, chunk_off, t.gid, t.n, t.begin, t.end, t.row0, t.nt);
     return t;
 }
@@ -252,8 +257,8 @@ __device__ __forceinline__ void pair_rows(const float (&x)[kTokW][4], float (&ro
         }
 }
 
-// Tensor maps of the raw rows: q, k, v [rows, C] bf16 with a [kRows, 128] box, and (KDA) the
-// gate input f [rows, C] f32 with a [32, 128] box.
+// Tensor maps of the raw rows: q, k [rows, Cq] and v [rows, C] bf16 with a [kRows, 128] box, and
+// (KDA) the gate input f [rows, Cg] f32 with a [32, 128] box.
 struct RawMaps {
     CUtensorMap q, k, v, f;
     CUtensorMap ut;              // the workspace blocks' U rows (the MMA tail's epilogue)
@@ -265,9 +270,9 @@ struct RawMaps {
 // halo from the ring before the sequence start, and tokens past the chunk end are masked).
 template <int KW>
 __device__ __forceinline__ void stage_raw(RawStage<KW>& st, const RawMaps& m, const TaskPos& tp,
-                                          int Hk, uint64_t* bar) {
+                                          uint64_t* bar) {
     mbar_arrive_expect_tx(bar, 3u * RawStage<KW>::kRows * kHeadDim * sizeof(__nv_bfloat16));
-    const int xq = (tp.h % Hk) * kHeadDim, x = tp.h * kHeadDim, y = (int)tp.row0 - (KW - 1);
+    const int xq = tp.hq * kHeadDim, x = tp.h * kHeadDim, y = (int)tp.row0 - (KW - 1);
     tma_load_2d(&st.v[0][0][0], &m.q, xq, y, bar);
     tma_load_2d(&st.v[1][0][0], &m.k, xq, y, bar);
     tma_load_2d(&st.v[2][0][0], &m.v, x, y, bar);
@@ -278,7 +283,7 @@ __device__ __forceinline__ void stage_raw(RawStage<KW>& st, const RawMaps& m, co
 __device__ __forceinline__ void stage_f(float* dst, const RawMaps& m, const TaskPos& tp,
                                         uint64_t* bar) {
     mbar_arrive_expect_tx(bar, kCc * kHeadDim * sizeof(float));
-    tma_load_2d(dst, &m.f, tp.h * kHeadDim, (int)tp.row0, bar);
+    tma_load_2d(dst, &m.f, tp.gh * kHeadDim, (int)tp.row0, bar);
 }
 
 __device__ __forceinline__ void cp_async4(void* dst, const void* src) {
@@ -322,31 +327,35 @@ constexpr size_t kPrepIntraSmemBytes = sizeof(PrepIntraSmem) + 1024;
 // two resident CTAs per SM: 228 KB of shared memory per SM, 1 KB of it reserved per CTA
 static_assert(2 * (kPrepIntraSmemBytes + 1024) <= 228 * 1024, "two CTAs per SM");
 
-// Issue the cp.async copies of task tp's small inputs into the parameter stage.
+// Issue the cp.async copies of task tp's small inputs into the parameter stage (H units, Hg gate
+// heads).
 template <int GATE_MODE, bool CONV>
-__device__ __forceinline__ void stage_params(ParamStage& ps, const PrepArgs& p, int H, long C,
+__device__ __forceinline__ void stage_params(ParamStage& ps, const PrepArgs& p, int H, int Hg,
                                              const TaskPos& tp) {
-    const int tid = threadIdx.x, h = tp.h, nt = tp.nt;
+    const int tid = threadIdx.x, h = tp.h, gh = tp.gh, nt = tp.nt;
     const long row0 = tp.row0;
     if constexpr (CONV) {
         const int K = p.K, per = kHeadDim * K;   // one plane's rows of this head, contiguous
-        for (int idx = tid; idx < 3 * per; idx += kThrF) {
-            const int pl = idx / per, r = idx - pl * per;
-            const int ch = K == 4 ? r >> 2 : r / K, j = r - ch * K;
-            const long hp = pl < 2 ? h % prep_qk_heads(H, p.Hk) : h;   // the plane's head
-            cp_async4(&ps.w[pl][j * kHeadDim + ch],
-                      p.conv_w + (plane_offset(H, p.Hk, pl) + hp * kHeadDim) * K + r);
+        const int hq = tp.hq;                    // the q and k planes' head
+#pragma unroll 1
+        for (int pl = 0; pl < 3; ++pl) {
+            const float* src =
+                p.conv_w + (plane_offset(H, p.Hk, pl) + (long)(pl < 2 ? hq : h) * kHeadDim) * K;
+            for (int r = tid; r < per; r += kThrF) {
+                const int ch = K == 4 ? r >> 2 : r / K, j = r - ch * K;
+                cp_async4(&ps.w[pl][j * kHeadDim + ch], src + r);
+            }
         }
     }
     if (GATE_MODE == 0) {
-        if (tid < kHeadDim / 4) cp_async16(&ps.dt[4 * tid], p.dt_bias + (long)h * kHeadDim + 4 * tid);
+        if (tid < kHeadDim / 4) cp_async16(&ps.dt[4 * tid], p.dt_bias + (long)gh * kHeadDim + 4 * tid);
     } else if (tid == kThrF - 1) {
-        cp_async4(&ps.dt[0], p.dt_bias + h);
+        cp_async4(&ps.dt[0], p.dt_bias + gh);
     }
-    if (tid == kThrF - 2) cp_async4(&ps.alog, p.a_log + h);
+    if (tid == kThrF - 2) cp_async4(&ps.alog, p.a_log + gh);
     if (tid < nt) {
-        cp_async4(&ps.braw[tid], p.beta_raw + (row0 + tid) * H + h);
-        if (GATE_MODE == 1) cp_async4(&ps.fraw[tid], p.f_raw + (row0 + tid) * H + h);
+        cp_async4(&ps.braw[tid], p.beta_raw + (row0 + tid) * Hg + gh);
+        if (GATE_MODE == 1) cp_async4(&ps.fraw[tid], p.f_raw + (row0 + tid) * Hg + gh);
     }
     cp_async_commit();
 }
@@ -402,6 +411,11 @@ kda_chunk_prep_intra_kernel(PrepArgs p, ScanArgs a, const int* chunk_off, unsign
     // h % Hk, and the conv weights and ring rows are [q | k | v] = [Cq | Cq | C]
     const int Hk = prep_qk_heads(H, p.Hk);
     const long Cq = (long)Hk * kHeadDim;
+    // value heads wider than 128: H counts 128-wide units, vs of them per value head; the gate
+    // rows (KDA) are Cg = Hg * 128 wide and beta (and the GDN gate) Hg per row
+    const int vs = value_sub(a);
+    const int Hg = prep_gate_heads(p);
+    const long Cg = (long)Hg * kHeadDim;
     const long ntasks = nchunks * H;
     const int kq = 4 * lane;                     // first of this lane's channels within the head
     const int t0 = kTokW * warp;                 // the warp's first token within the chunk
@@ -420,27 +434,28 @@ kda_chunk_prep_intra_kernel(PrepArgs p, ScanArgs a, const int* chunk_off, unsign
     uint32_t phase = 0, ph_ld = 0;               // MMA commits; staged loads (one per task)
     bool ld_pending = false;                     // a task's loads issued and not yet waited on
     if (PF && (long)blockIdx.x < ntasks) {
-        const TaskPos tp = task_pos(a.seq, chunk_off, blockIdx.x, nchunks);
+        const TaskPos tp = task_pos(a.seq, chunk_off, blockIdx.x, nchunks, vs, Hk);
         if (tid == 0) {
             prefetch_tensormap(&maps.q);
             prefetch_tensormap(&maps.k);
             prefetch_tensormap(&maps.v);
-            stage_raw<KW>(stage, maps, tp, Hk, &smf.bar_raw);
+            stage_raw<KW>(stage, maps, tp, &smf.bar_raw);
             if (GATE_MODE == 0) stage_f(sm.scr, maps, tp, &smf.bar_f);
         }
-        stage_params<GATE_MODE, PW>(ps, p, H, C, tp);
+        stage_params<GATE_MODE, PW>(ps, p, H, Hg, tp);
     }
     __syncthreads();
 
     for (long task = blockIdx.x; task < ntasks; task += gridDim.x) {
-    const TaskPos tp = task_pos(a.seq, chunk_off, task, nchunks);
+    const TaskPos tp = task_pos(a.seq, chunk_off, task, nchunks, vs, Hk);
     const long gid = tp.gid;                     // global chunk index
-    const int h = tp.h, n = tp.n, nt = tp.nt;
+    const int h = tp.h, gh = tp.gh, n = tp.n, nt = tp.nt;
     const long begin = tp.begin, row0 = tp.row0;
     const long c = (row0 - begin) / kCc;
     unsigned char* blk = ws + ((long)gid * H + h) * kBlkBytes;
     const long c4 = (long)h * kHeadDim + kq;     // this lane's first channel within the v plane
-    const long cq4 = (long)(h % Hk) * kHeadDim + kq;   // ... and within the q and k planes
+    const long cq4 = (long)tp.hq * kHeadDim + kq;   // ... and within the q and k planes
+    const long cg4 = (long)gh * kHeadDim + kq;      // ... and within the gate rows
     const int ntok = max(0, min(kTokW, nt - t0));
 
     // ---- loads: the gate input and beta; raw q, k, v (staged, or direct) -----------------------
@@ -448,14 +463,14 @@ kda_chunk_prep_intra_kernel(PrepArgs p, ScanArgs a, const int* chunk_off, unsign
     if (GATE_MODE == 0 && !PF) {
 #pragma unroll
         for (int i = 0; i < kTokW; ++i)
-            fr[i] = i < ntok ? __ldg(reinterpret_cast<const float4*>(p.f_raw + (row0 + t0 + i) * C + c4))
+            fr[i] = i < ntok ? __ldg(reinterpret_cast<const float4*>(p.f_raw + (row0 + t0 + i) * Cg + cg4))
                              : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
     }
     if (!PF && tid < kCc) {
         const bool live = tid < nt;
-        sm.beta[tid] = live ? sigmoid_f(p.beta_raw[(row0 + tid) * H + h]) : 0.0f;
+        sm.beta[tid] = live ? sigmoid_f(p.beta_raw[(row0 + tid) * Hg + gh]) : 0.0f;
         if (GATE_MODE == 1)
-            sm.gs[tid] = live ? gdn_gate_f(p.f_raw[(row0 + tid) * H + h], p.dt_bias[h], p.a_log[h]) : 0.0f;
+            sm.gs[tid] = live ? gdn_gate_f(p.f_raw[(row0 + tid) * Hg + gh], p.dt_bias[gh], p.a_log[gh]) : 0.0f;
     }
     const long pos0 = c * kCc + t0;
     const long rr = (long)n * (2 * Cq + C) * R;
@@ -540,9 +555,9 @@ kda_chunk_prep_intra_kernel(PrepArgs p, ScanArgs a, const int* chunk_off, unsign
     float GCh = 0.0f;                            // per-head gate: the chunk's total
     float cref_l[4], ecr_l[4];                   // KDA: c = G_C / 2 and e^c of this lane's channels
     if (GATE_MODE == 0) {
-        const float rate = expf(PF ? ps.alog : p.a_log[h]);
+        const float rate = expf(PF ? ps.alog : p.a_log[gh]);
         const float4 dt = PF ? *reinterpret_cast<const float4*>(&ps.dt[kq])
-                             : *reinterpret_cast<const float4*>(p.dt_bias + c4);
+                             : *reinterpret_cast<const float4*>(p.dt_bias + cg4);
         const float dtv[4] = {dt.x, dt.y, dt.z, dt.w};
         float g[kTokW][4];
 #pragma unroll
@@ -729,14 +744,14 @@ kda_chunk_prep_intra_kernel(PrepArgs p, ScanArgs a, const int* chunk_off, unsign
     const long next = task + gridDim.x;
     const bool ok = intra_mma_tail<GATE_MODE, kThrF, true>(sm, a.err, blk, phase, [&]() {
         if (PF && next < ntasks) {
-            const TaskPos np = task_pos(a.seq, chunk_off, next, nchunks);
+            const TaskPos np = task_pos(a.seq, chunk_off, next, nchunks, vs, Hk);
             ld_pending = true;
-            if (tid == 0) stage_raw<KW>(stage, maps, np, Hk, &smf.bar_raw);
-            stage_params<GATE_MODE, PW>(ps, p, H, C, np);
+            if (tid == 0) stage_raw<KW>(stage, maps, np, &smf.bar_raw);
+            stage_params<GATE_MODE, PW>(ps, p, H, Hg, np);
         }
     }, [&]() {
         if (PF && GATE_MODE == 0 && next < ntasks && tid == 0)
-            stage_f(sm.scr, maps, task_pos(a.seq, chunk_off, next, nchunks), &smf.bar_f);
+            stage_f(sm.scr, maps, task_pos(a.seq, chunk_off, next, nchunks, vs, Hk), &smf.bar_f);
     }, &maps.ut, (int)(gid * H + h));
     if (!ok) break;
     }   // task loop
@@ -776,7 +791,8 @@ static cudaError_t launch_prep_intra_t(const PrepArgs& p, const ScanArgs& a, con
         if (!make_tensor_map_2d_any(&maps.q, p.q_raw, true, rows, Cq, kHeadDim, kRows) ||
             !make_tensor_map_2d_any(&maps.k, p.k_raw, true, rows, Cq, kHeadDim, kRows) ||
             !make_tensor_map_2d_any(&maps.v, p.v_raw, true, rows, C, kHeadDim, kRows) ||
-            (GM == 0 && !make_tensor_map_2d_any(&maps.f, p.f_raw, false, rows, C, kHeadDim, kCc)))
+            (GM == 0 && !make_tensor_map_2d_any(&maps.f, p.f_raw, false, rows,
+                                                (long)prep_gate_heads(p) * kHeadDim, kHeadDim, kCc)))
             return cudaErrorInvalidValue;
     }
     KernelTimer kt(kKPrepIntra, s);

@@ -12,8 +12,10 @@
 // threads; 8 lanes share 4 value columns with 16 key-dim elements each, and the per-token step is
 // the sequential prefill scan's (kda_scan_core.cuh), instruction for instruction.
 // The prologue and epilogue use the same device functions as the prep and epilogue kernels, so
-// this kernel's outputs equal prep + scan + gated-RMSNorm launched separately, bit for bit, and a
-// T-token launch equals T one-token launches bit for bit.
+// this kernel's outputs equal prep + scan + gated-RMSNorm launched separately to f32 rounding (the
+// standalone sequential scan groups 16 lanes per column, this kernel 8, so their key-dimension
+// sums round differently; the ring is bit-equal), and a T-token launch equals T one-token
+// launches bit for bit.
 #include "kda_scan_core.cuh"
 
 namespace kda {
@@ -35,8 +37,25 @@ __device__ __forceinline__ void cp_async_commit_wait() {
     asm volatile("cp.async.commit_group;\n\tcp.async.wait_all;" ::: "memory");
 }
 
-// KW: register window width of the conv (4 when K <= 4, else 8).
-template <bool BF16, int GATE_MODE, int KW>
+// Thread-block cluster barrier (every thread of every CTA of the cluster arrives; release /
+// acquire order the shared-memory writes before it with the remote reads after it).
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// A float in the shared memory of the cluster's CTA `rank`, at the address of `local` there.
+__device__ __forceinline__ float ld_cluster_f32(const float* local, uint32_t rank) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+    return v;
+}
+
+// KW: register window width of the conv (4 when K <= 4, else 8).  WIDE: value heads of
+// a.vsub > 1 units, launched as clusters of a.vsub CTAs.
+template <bool BF16, int GATE_MODE, int KW, bool WIDE>
 __global__ void __launch_bounds__(kDecThreads, 2) kda_decode_fused_kernel(DecodeArgs a) {
     __shared__ __align__(16) float qh[kDecodeMaxT][kHeadDim];
     __shared__ __align__(16) float kh[kDecodeMaxT][kHeadDim];
@@ -47,11 +66,20 @@ __global__ void __launch_bounds__(kDecThreads, 2) kda_decode_fused_kernel(Decode
     __shared__ float ascal[kDecodeMaxT];
     __shared__ float part[2][2][kDecodeMaxT];
     __shared__ float inv_s[2][kDecodeMaxT];
+    __shared__ float nss[kDecodeMaxT];           // this unit's RMSNorm sums of squares (vs > 1)
 
+    // unit h: value column block h % vs of value head gh = h / vs, whose gate and beta it reads,
+    // and q/k head hq = gh % Hk (vs = 1: the value head itself)
     const int h = blockIdx.x, n = blockIdx.y;
+    const int vs = WIDE ? a.vsub : 1;
+    const int gh = WIDE ? h / vs : h;
     const int tid = threadIdx.x;
     const int H = a.H, K = a.K, R = a.K - 1;
     const long C = (long)H * kHeadDim;
+    const int Hg = H / vs;                       // value heads
+    const long Cg = (long)Hg * kHeadDim;         // per-channel gate rows
+    const int Hkq = prep_qk_heads(Hg, a.Hk);
+    const int hq = gh < Hkq ? gh : gh % Hkq;
     const long row0 = (long)n * a.T;             // rows of sequence n: stride T in every mode
     // tokens taken: all T, or (rollback) the first keep[n]
     const int T = a.keep != nullptr ? min(max(a.keep[n], 0), a.T) : a.T;
@@ -67,7 +95,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) kda_decode_fused_kernel(Decode
     //      planes hold Hk heads and this value head reads q/k head h % Hk; only the CTAs of heads
     //      h < Hk write those heads' ring rows.
     const int task = tid >> 6, i0 = 2 * (tid & 63);
-    const int c = h * kHeadDim + i0;
+    const int cg = gh * kHeadDim + i0;           // channel pair in the gate rows
     float wr[2][KW], win[2][KW];
     long ring_row = 0;
     bool ring_owner = false;
@@ -76,8 +104,9 @@ __global__ void __launch_bounds__(kDecThreads, 2) kda_decode_fused_kernel(Decode
     if (task < 3) {
         const void* raw = task == 0 ? a.q_raw : (task == 1 ? a.k_raw : a.v_raw);
         const long Cp = plane_width(H, a.Hk, task);        // row width of this plane
-        const int cp = (task < 2 ? h % prep_qk_heads(H, a.Hk) : h) * kHeadDim + i0;
-        ring_owner = task == 2 || h < prep_qk_heads(H, a.Hk);
+        const int cp = (task < 2 ? hq : h) * kHeadDim + i0;
+        // the q / k ring rows of head hq are rolled by one unit: the first of value head hq
+        ring_owner = task == 2 || (h == gh * vs && gh < Hkq);
         ring_row = ((long)n * ring_channels(H, a.Hk) + plane_offset(H, a.Hk, task) + cp) * R;
 #pragma unroll
         for (int m = 0; m < KW; ++m) {
@@ -97,18 +126,18 @@ __global__ void __launch_bounds__(kDecThreads, 2) kda_decode_fused_kernel(Decode
                 cp_async_8(&dst[t][i0], reinterpret_cast<const float*>(raw) + (row0 + t) * Cp + cp);
         }
         if (task == 2 && (tid & 63) < T) {
-            const long rw = (row0 + (tid & 63)) * H + h;
+            const long rw = (row0 + (tid & 63)) * Hg + gh;
             braw = a.beta_raw[rw];
             if (GATE_MODE == 1) {
                 fgate = a.f_raw[rw];
-                dtb = a.dt_bias[h];
-                alog = a.a_log[h];
+                dtb = a.dt_bias[gh];
+                alog = a.a_log[gh];
             }
         }
     } else if (GATE_MODE == 0) {
-        alog = a.a_log[h];
-        dt = *reinterpret_cast<const float2*>(a.dt_bias + c);
-        for (int t = 0; t < T; ++t) cp_async_8(&av[t][i0], a.f_raw + (row0 + t) * C + c);
+        alog = a.a_log[gh];
+        dt = *reinterpret_cast<const float2*>(a.dt_bias + cg);
+        for (int t = 0; t < T; ++t) cp_async_8(&av[t][i0], a.f_raw + (row0 + t) * Cg + cg);
     }
 
     // ---- then the state loads: 4 columns x 16 elements per lane -----------------------------
@@ -213,20 +242,44 @@ __global__ void __launch_bounds__(kDecThreads, 2) kda_decode_fused_kernel(Decode
     }
     // the epilogue's first gate row and the norm weight are requested before the state stores go
     // out, so their latency overlaps the stores and the barrier
-    const float4 w4 = *reinterpret_cast<const float4*>(a.norm_w + 4 * lane);
+    // (the unit's column block of the norm weight: blockIdx.x % vsub, from the launch parameters)
+    const float4 w4 = *reinterpret_cast<const float4*>(
+        a.norm_w + (WIDE ? (int)blockIdx.x % a.vsub : 0) * kHeadDim + 4 * lane);
     float4 z_first = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
     if (warp < T)
         z_first = *reinterpret_cast<const float4*>(a.gate_raw + (row0 + warp) * C + h * kHeadDim + 4 * lane);
     col4_store(S, a.state_out + col0, r);
     __syncthreads();
     // ---- epilogue: gated RMSNorm, one warp per token row -----------------------------------
+    // A value head of vs units: each unit's sum of squares of a row goes to its shared memory,
+    // and after a cluster barrier every unit adds the vs sums in unit order (the order of the
+    // standalone RMSNorm over rows of vs * 128), for the mean over the whole value row.
+    if constexpr (WIDE) {
+        for (int t = warp; t < T; t += kDecThreads / 32) {
+            const float4 o4 = *reinterpret_cast<const float4*>(&os[t][4 * lane]);
+            float ss = __fmul_rn(o4.x, o4.x);
+            ss = ss + __fmul_rn(o4.y, o4.y);
+            ss = ss + __fmul_rn(o4.z, o4.z);
+            ss = ss + __fmul_rn(o4.w, o4.w);
+            ss = warp_sum(ss);
+            if (lane == 0) nss[t] = ss;
+        }
+        cluster_sync_all();
+    }
     for (int t = warp; t < T; t += kDecThreads / 32) {
         const float4 o4 = *reinterpret_cast<const float4*>(&os[t][4 * lane]);
-        float ss = __fmul_rn(o4.x, o4.x);
-        ss = ss + __fmul_rn(o4.y, o4.y);
-        ss = ss + __fmul_rn(o4.z, o4.z);
-        ss = ss + __fmul_rn(o4.w, o4.w);
-        const float inv = rms_inv_f(warp_sum(ss), a.rms_eps);
+        float inv;
+        if constexpr (WIDE) {
+            float tot = 0.0f;
+            for (int b = 0; b < a.vsub; ++b) tot = tot + ld_cluster_f32(&nss[t], (uint32_t)b);
+            inv = rms_inv_w(tot, a.rms_eps, a.vsub * kHeadDim);
+        } else {
+            float ss = __fmul_rn(o4.x, o4.x);
+            ss = ss + __fmul_rn(o4.y, o4.y);
+            ss = ss + __fmul_rn(o4.z, o4.z);
+            ss = ss + __fmul_rn(o4.w, o4.w);
+            inv = rms_inv_f(warp_sum(ss), a.rms_eps);
+        }
         const long base = (row0 + t) * C + h * kHeadDim + 4 * lane;
         const float4 z4 = t == warp ? z_first : *reinterpret_cast<const float4*>(a.gate_raw + base);
         float4 y4;
@@ -243,26 +296,48 @@ __global__ void __launch_bounds__(kDecThreads, 2) kda_decode_fused_kernel(Decode
         }
         *reinterpret_cast<float4*>(a.y + base) = y4;
     }
+    if constexpr (WIDE) cluster_sync_all();      // the other units have read this unit's sums
+}
+
+// A value head of vsub > 1 units is one thread-block cluster of vsub CTAs along x.
+template <typename Kern>
+static cudaError_t launch_dec_kernel(Kern kernel, const DecodeArgs& a, cudaStream_t s) {
+    dim3 grid((unsigned)a.H, (unsigned)a.N);
+    if (a.vsub <= 1) {
+        kernel<<<grid, kDecThreads, 0, s>>>(a);
+        return cudaGetLastError();
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kDecThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)a.vsub;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, a);
 }
 
 template <bool BF16, int GM>
-static void launch_dec_t(const DecodeArgs& a, cudaStream_t s) {
-    dim3 grid((unsigned)a.H, (unsigned)a.N);
+static cudaError_t launch_dec_t(const DecodeArgs& a, cudaStream_t s) {
     KernelTimer kt(kKDecode, s);
-    if (a.K <= 4) kda_decode_fused_kernel<BF16, GM, 4><<<grid, kDecThreads, 0, s>>>(a);
-    else kda_decode_fused_kernel<BF16, GM, kMaxConvK><<<grid, kDecThreads, 0, s>>>(a);
+    if (a.vsub > 1) {
+        if (a.K <= 4) return launch_dec_kernel(kda_decode_fused_kernel<BF16, GM, 4, true>, a, s);
+        return launch_dec_kernel(kda_decode_fused_kernel<BF16, GM, kMaxConvK, true>, a, s);
+    }
+    if (a.K <= 4) return launch_dec_kernel(kda_decode_fused_kernel<BF16, GM, 4, false>, a, s);
+    return launch_dec_kernel(kda_decode_fused_kernel<BF16, GM, kMaxConvK, false>, a, s);
 }
 
 cudaError_t launch_decode_fused(const DecodeArgs& a, cudaStream_t s) {
     if (a.N == 0 || a.T == 0) return cudaSuccess;
-    if (a.raw_bf16) {
-        if (a.gate_mode == 0) launch_dec_t<true, 0>(a, s);
-        else launch_dec_t<true, 1>(a, s);
-    } else {
-        if (a.gate_mode == 0) launch_dec_t<false, 0>(a, s);
-        else launch_dec_t<false, 1>(a, s);
-    }
-    return cudaGetLastError();
+    if (a.raw_bf16)
+        return a.gate_mode == 0 ? launch_dec_t<true, 0>(a, s) : launch_dec_t<true, 1>(a, s);
+    return a.gate_mode == 0 ? launch_dec_t<false, 0>(a, s) : launch_dec_t<false, 1>(a, s);
 }
 
 }  // namespace kda

@@ -58,6 +58,11 @@ __device__ __forceinline__ float rms_inv_f(float ss, float eps) {
     return rsqrtf(__fmul_rn(ss, 1.0f / kHeadDim) + eps);
 }
 
+// the same over a row of `width` values (equal to rms_inv_f at width 128)
+__device__ __forceinline__ float rms_inv_w(float ss, float eps, int width) {
+    return rsqrtf(__fmul_rn(ss, 1.0f / (float)width) + eps);
+}
+
 // one gated-RMSNorm output element: ((o * inv) * w) * gate(z), gate = sigmoid (KDA) or SiLU
 // (GDN's gated_rmsnorm)
 template <bool SILU = false>

@@ -37,23 +37,26 @@ __global__ void __launch_bounds__(256) kda_gated_rmsnorm_kernel(NormArgs a) {
 }
 
 // Rows of m * 128 values (a value head wider than the key head): one warp per row, lane l on the
-// float4s at 4l + 128 j (j < m), the sum of squares taken over j in order, then the butterfly;
-// the mean over the whole row.
+// float4s at 4l + 128 j (j < m).  The sum of squares of each 128-block is the square kernel's
+// (four products, then the butterfly); the blocks' sums are added in block order from 0, the
+// order in which the fused decode's thread-block cluster adds its CTAs' sums; the mean is over the
+// whole row.
 template <bool SILU>
 __global__ void __launch_bounds__(256) kda_gated_rmsnorm_wide_kernel(NormArgs a, int m) {
     const long row = (long)blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (row >= a.rows) return;
     const long base = row * (long)a.width + 4 * lane;
-    float ss = 0.0f;
+    float tot = 0.0f;
     for (int j = 0; j < m; ++j) {
         const float4 o4 = __ldcs(reinterpret_cast<const float4*>(a.o + base + kHeadDim * j));
-        ss = ss + __fmul_rn(o4.x, o4.x);
+        float ss = __fmul_rn(o4.x, o4.x);
         ss = ss + __fmul_rn(o4.y, o4.y);
         ss = ss + __fmul_rn(o4.z, o4.z);
         ss = ss + __fmul_rn(o4.w, o4.w);
+        tot = tot + warp_sum(ss);
     }
-    const float inv = rsqrtf(__fmul_rn(warp_sum(ss), 1.0f / (float)a.width) + a.eps);
+    const float inv = rms_inv_w(tot, a.eps, a.width);
     for (int j = 0; j < m; ++j) {
         const long off = base + kHeadDim * j;
         const float4 o4 = __ldcs(reinterpret_cast<const float4*>(a.o + off));

@@ -107,6 +107,9 @@ struct DecodeArgs {
     int Hk;                  // heads of the q and k planes (grouped queries); 0 means H
     int norm_silu;           // RMSNorm gate: 0 sigmoid (KDA), 1 SiLU (GDN's gated_rmsnorm)
     int* err;                // device error word (bounded waits)
+    int vsub;                // 128-wide units per value head (H counts units); 0 means 1.  A
+                             // value head's units run as one thread-block cluster, which sums the
+                             // RMSNorm's squares over the whole value row
 };
 
 cudaError_t launch_prep(const PrepArgs& a, cudaStream_t s);

@@ -292,13 +292,52 @@ __device__ __forceinline__ void tmem_put_split16(uint32_t col_hi, uint32_t col_l
     tmem_st8(col_lo, lw);
 }
 
-// Threads: 256.  Thread (half hf = tid / 128, value row v = tid % 128) owns TMEM lane v; it keeps
-// key columns 32 hf .. 32 hf + 31 and 64 + 32 hf .. 64 + 32 hf + 31 of state row v in registers
-// (srow[0..31], srow[32..63]) and handles tokens 16 hf .. 16 hf + 15 of each chunk's U' and o.
-// The state update runs in two passes, keys 0..63 then 64..127, so that the next chunk's MMA-1
-// takes its first four K-steps while the second pass runs.  Thread 0 issues the MMAs, thread 32 the workspace loads, and the
-// lanes of warp 2 the o rows' bulk stores (lane t: token t of the chunk).
-constexpr int kThrInter = 256;
+// the same for NV = 4, 8, 16 or a multiple of 32 values
+template <int NV>
+__device__ __forceinline__ void tmem_put_split_n(uint32_t col_hi, uint32_t col_lo, const float* v) {
+    if constexpr (NV == 4) {
+        uint32_t hw[2], lw[2];
+        split_bf16x2(v[0], v[1], hw[0], lw[0]);
+        split_bf16x2(v[2], v[3], hw[1], lw[1]);
+        tmem_st2(col_hi, hw);
+        tmem_st2(col_lo, lw);
+    } else if constexpr (NV == 8) {
+        uint32_t hw[4], lw[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) split_bf16x2(v[2 * i], v[2 * i + 1], hw[i], lw[i]);
+        tmem_st4(col_hi, hw);
+        tmem_st4(col_lo, lw);
+    } else if constexpr (NV == 16) {
+        tmem_put_split16(col_hi, col_lo, v);
+    } else {
+        tmem_put_split<NV>(col_hi, col_lo, v);
+    }
+}
+
+// N = 4, 8 or a multiple of 16 consecutive columns of this thread's lane
+template <int N>
+__device__ __forceinline__ void tmem_ld_n(uint32_t taddr, float* v) {
+    if constexpr (N == 4) {
+        tmem_ld4(taddr, *reinterpret_cast<float(*)[4]>(v));
+    } else if constexpr (N == 8) {
+        tmem_ld8(taddr, *reinterpret_cast<float(*)[8]>(v));
+    } else {
+#pragma unroll
+        for (int b = 0; b < N / 16; ++b)
+            tmem_ld16(taddr + 16 * b, *reinterpret_cast<float(*)[16]>(v + 16 * b));
+    }
+}
+
+// Threads: 128 * kInterKq.  Thread (key group qf = tid / 128, value row v = tid % 128) owns TMEM
+// lane v (warps w, w + 4, ... share lane quarter w % 4); with KPP = 64 / kInterKq it keeps key
+// columns KPP qf .. KPP qf + KPP - 1 and 64 + KPP qf .. of state row v in registers and handles
+// tokens TPT qf .. TPT qf + TPT - 1 (TPT = 32 / kInterKq) of each chunk's U' and o.  The state
+// update runs in two passes, keys 0..63 then 64..127, so that the next chunk's MMA-1 takes its
+// first four K-steps while the second pass runs.  More threads per value row shorten each
+// thread's share of the chunk's dependent register / TMEM work.  Thread 0 issues the MMAs,
+// thread 32 the workspace loads, and the lanes of warp 2 the o rows' bulk stores.
+constexpr int kInterKq = 4;
+constexpr int kThrInter = 128 * kInterKq;
 
 template <int GATE_MODE>
 __global__ void __launch_bounds__(kThrInter, 1)
@@ -307,8 +346,10 @@ kda_chunk_inter_kernel(ScanArgs a, const int* chunk_off, const unsigned char* ws
     extern __shared__ unsigned char smem_raw[];
     InterSmem& sm = *reinterpret_cast<InterSmem*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+    constexpr int KPP = 64 / kInterKq;           // keys per thread and pass
+    constexpr int TPT = kCc / kInterKq;          // tokens per thread
     const int tid = threadIdx.x, warp = tid >> 5;
-    const int v = tid & 127, hf = tid >> 7;
+    const int v = tid & 127, qf = tid >> 7;
     const int h = blockIdx.x;
     const int n = a.order ? a.order[blockIdx.y] : (int)blockIdx.y;
     const int H = a.H;
@@ -328,23 +369,29 @@ kda_chunk_inter_kernel(ScanArgs a, const int* chunk_off, const unsigned char* ws
         mbar_init(&sm.bar_mma, 1);
         fence_mbar_init();
     }
-    float srow[64];
+    float srow[2 * KPP];             // keys 64 pass + KPP qf + j at srow[KPP pass + j]
     {
         const float* srow_in = a.state_in + (((long)n * H + h) * kHeadDim + v) * kHeadDim;
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            const float4 x = __ldcs(reinterpret_cast<const float4*>(
-                srow_in + (j < 8 ? 32 * hf : 64 + 32 * hf - 32) + 4 * j));
-            srow[4 * j] = x.x; srow[4 * j + 1] = x.y; srow[4 * j + 2] = x.z; srow[4 * j + 3] = x.w;
-        }
+        for (int pass = 0; pass < 2; ++pass)
+#pragma unroll
+            for (int j = 0; j < KPP / 4; ++j) {
+                const float4 x = __ldcs(reinterpret_cast<const float4*>(
+                    srow_in + 64 * pass + KPP * qf + 4 * j));
+                float* d = srow + KPP * pass + 4 * j;
+                d[0] = x.x; d[1] = x.y; d[2] = x.z; d[3] = x.w;
+            }
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tbase = sm.tmem_base;
     const uint32_t tl = tbase + ((uint32_t)(32 * (warp & 3)) << 16);
-    tmem_put_split<32>(tl + kTA1 + 16 * hf, tl + kTA1 + 64 + 16 * hf, srow);
-    tmem_put_split<32>(tl + kTA1 + 32 + 16 * hf, tl + kTA1 + 96 + 16 * hf, srow + 32);
+#pragma unroll
+    for (int pass = 0; pass < 2; ++pass) {
+        const int k0 = 64 * pass + KPP * qf;
+        tmem_put_split_n<KPP>(tl + kTA1 + k0 / 2, tl + kTA1 + 64 + k0 / 2, srow + KPP * pass);
+    }
     tmem_st_wait();
 
     auto issue = [&](int c, int st) {
@@ -436,21 +483,21 @@ kda_chunk_inter_kernel(ScanArgs a, const int* chunk_off, const unsigned char* ws
         tc_fence_after();
         if (__syncthreads_or(!ok || late_fail)) { failed = true; break; }
         if (ostore_lane && c > 0) flush_o(c - 1);   // its o rows were written before the barrier
-        // O1 and X for tokens 16 hf ..; O1 waits in the output tile; U' = U - X into TMEM as
+        // O1 and X for tokens TPT qf ..; O1 waits in the output tile; U' = U - X into TMEM as
         // MMA-2's A operand
-        float* ot = &sm.otile[c % 3][16 * hf][v];
+        float* ot = &sm.otile[c % 3][TPT * qf][v];
         {
-            float x[16], o1[16];
-            tmem_ld16(tl + kTD1 + 16 * hf, o1);
-            tmem_ld16(tl + kTD1 + 32 + 16 * hf, x);
+            float x[TPT], o1[TPT];
+            tmem_ld_n<TPT>(tl + kTD1 + TPT * qf, o1);
+            tmem_ld_n<TPT>(tl + kTD1 + 32 + TPT * qf, x);
             tmem_ld_wait();
 #pragma unroll
-            for (int t = 0; t < 16; ++t) ot[t * 128] = o1[t];
-            const float* ut = reinterpret_cast<const float*>(B + kOffUT) + (16 * hf) * 128 + v;
-            float up[16];
+            for (int t = 0; t < TPT; ++t) ot[t * 128] = o1[t];
+            const float* ut = reinterpret_cast<const float*>(B + kOffUT) + (TPT * qf) * 128 + v;
+            float up[TPT];
 #pragma unroll
-            for (int t = 0; t < 16; ++t) up[t] = ut[t * 128] - x[t];
-            tmem_put_split16(tl + kTA2 + 8 * hf, tl + kTA2 + 16 + 8 * hf, up);
+            for (int t = 0; t < TPT; ++t) up[t] = ut[t * 128] - x[t];
+            tmem_put_split_n<TPT>(tl + kTA2 + TPT / 2 * qf, tl + kTA2 + 16 + TPT / 2 * qf, up);
             tmem_st_wait();
         }
         tc_fence_before();
@@ -471,29 +518,28 @@ kda_chunk_inter_kernel(ScanArgs a, const int* chunk_off, const unsigned char* ws
             late_fail = late_fail || !ok2;
         }
         tc_fence_after();
-        float o2[16];
+        float o2[TPT];
         bool next_ok = false;            // thread 0: the next chunk's block landed, MMA-1 going
         // S <- S e^{G_C} + dS, keys 0..63 (srow[0..31]) then 64..127 (srow[32..63]); after the
         // first pass thread 0 starts the next chunk's MMA-1 on keys 0..63
         const float4* eg4 = reinterpret_cast<const float4*>(B + kOffEG);
 #pragma unroll
         for (int pass = 0; pass < 2; ++pass) {
-            const int k0 = 64 * pass + 32 * hf;      // this thread's first key of the pass
-            float d[32];
-            tmem_ld16(tl + kTD2 + k0, *reinterpret_cast<float(*)[16]>(&d[0]));
-            tmem_ld16(tl + kTD2 + k0 + 16, *reinterpret_cast<float(*)[16]>(&d[16]));
-            if (pass == 1) tmem_ld16(tl + kTD2 + 128 + 16 * hf, o2);
+            const int k0 = 64 * pass + KPP * qf;     // this thread's first key of the pass
+            float d[KPP];
+            tmem_ld_n<KPP>(tl + kTD2 + k0, d);
+            if (pass == 1) tmem_ld_n<TPT>(tl + kTD2 + 128 + TPT * qf, o2);
             tmem_ld_wait();
-            float* sr = srow + 32 * pass;
+            float* sr = srow + KPP * pass;
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
+            for (int q = 0; q < KPP / 4; ++q) {
                 const float4 e4 = eg4[k0 / 4 + q];
                 sr[4 * q] = fmaf(sr[4 * q], e4.x, d[4 * q]);
                 sr[4 * q + 1] = fmaf(sr[4 * q + 1], e4.y, d[4 * q + 1]);
                 sr[4 * q + 2] = fmaf(sr[4 * q + 2], e4.z, d[4 * q + 2]);
                 sr[4 * q + 3] = fmaf(sr[4 * q + 3], e4.w, d[4 * q + 3]);
             }
-            tmem_put_split<32>(tl + kTA1 + k0 / 2, tl + kTA1 + 64 + k0 / 2, sr);
+            tmem_put_split_n<KPP>(tl + kTA1 + k0 / 2, tl + kTA1 + 64 + k0 / 2, sr);
             tmem_st_wait();
             tc_fence_before();
             __syncthreads();   // pass 1: block st consumed; S^T in place for the next MMA-1
@@ -512,11 +558,11 @@ kda_chunk_inter_kernel(ScanArgs a, const int* chunk_off, const unsigned char* ws
         }
         if (tid == 32 && c + kInterStages < nch) issue(c + kInterStages, st);
         // the chunk's o rows into the staging tile while the next MMA-1 runs
-        float ov[16];
+        float ov[TPT];
 #pragma unroll
-        for (int t = 0; t < 16; ++t) ov[t] = __fmul_rn(scale, ot[t * 128] + o2[t]);
+        for (int t = 0; t < TPT; ++t) ov[t] = __fmul_rn(scale, ot[t * 128] + o2[t]);
 #pragma unroll
-        for (int t = 0; t < 16; ++t) ot[t * 128] = ov[t];
+        for (int t = 0; t < TPT; ++t) ot[t * 128] = ov[t];
         fence_proxy_async_smem();
     }
     failed = __syncthreads_or(failed || late_fail) != 0;
@@ -527,9 +573,13 @@ kda_chunk_inter_kernel(ScanArgs a, const int* chunk_off, const unsigned char* ws
     if (!failed) {
         float* srow_out = a.state_out + (((long)n * H + h) * kHeadDim + v) * kHeadDim;
 #pragma unroll
-        for (int j = 0; j < 16; ++j)
-            __stcs(reinterpret_cast<float4*>(srow_out + (j < 8 ? 32 * hf : 64 + 32 * hf - 32) + 4 * j),
-                   make_float4(srow[4 * j], srow[4 * j + 1], srow[4 * j + 2], srow[4 * j + 3]));
+        for (int pass = 0; pass < 2; ++pass)
+#pragma unroll
+            for (int j = 0; j < KPP / 4; ++j) {
+                const float* x = srow + KPP * pass + 4 * j;
+                __stcs(reinterpret_cast<float4*>(srow_out + 64 * pass + KPP * qf + 4 * j),
+                       make_float4(x[0], x[1], x[2], x[3]));
+            }
     } else {
         mbar_wait_bounded(&sm.bar_mma, mph, nullptr);   // let in-flight MMAs drain (bounded)
     }

@@ -126,6 +126,21 @@ _lib.kda_scan_dv.argtypes = [_P, _P, _P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I,
 _lib.kda_scan_varlen_dv.restype = _I
 _lib.kda_scan_varlen_dv.argtypes = [_P, _P, _P, _P, _I, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I,
                                     _I, _I, _F, _I, _P, _Z, _P]
+_lib.kda_prefill_fused_dv.restype = _I
+_lib.kda_prefill_fused_dv.argtypes = [_P, _P, _P, _I, _P, _P, _P, _P, _P, _P, _I, _F, _P, _P, _P,
+                                      _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _F, _F, _P, _Z,
+                                      _P]
+_lib.kda_prefill_fused_varlen_dv.restype = _I
+_lib.kda_prefill_fused_varlen_dv.argtypes = [_P, _P, _P, _I, _P, _P, _P, _P, _P, _P, _I, _F, _P,
+                                             _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I,
+                                             _I, _F, _F, _F, _P, _Z, _P]
+_lib.kda_decode_fused_dv.restype = _I
+_lib.kda_decode_fused_dv.argtypes = [_P, _P, _P, _I, _P, _P, _P, _P, _P, _P, _I, _F, _P, _P, _P,
+                                     _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _F, _F, _P]
+_lib.kda_verify_rollback_dv.restype = _I
+_lib.kda_verify_rollback_dv.argtypes = [_P, _P, _P, _I, _P, _P, _P, _P, _P, _P, _I, _F, _P, _P,
+                                        _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _F,
+                                        _F, _P]
 _lib.kda_selftest_wait_timeout.restype = _I
 _lib.kda_selftest_wait_timeout.argtypes = [_P]
 
@@ -141,7 +156,8 @@ EXPORTED = ("kda_abi_version", "kda_status_string", "kda_conv_l2norm_prep",
             "kda_conv_l2norm_prep_varlen_gqa", "kda_prefill_fused_gqa",
             "kda_prefill_fused_varlen_gqa", "kda_decode_fused_gqa", "kda_verify_rollback_gqa",
             "kda_conv_l2norm_prep_dv", "kda_conv_l2norm_prep_varlen_dv", "kda_scan_dv",
-            "kda_scan_varlen_dv")
+            "kda_scan_varlen_dv", "kda_prefill_fused_dv", "kda_prefill_fused_varlen_dv",
+            "kda_decode_fused_dv", "kda_verify_rollback_dv")
 
 
 class KdaError(RuntimeError):
@@ -200,9 +216,12 @@ def _raw_dtype(t) -> int:
     return DTYPE_BF16 if t.dtype == torch.bfloat16 else DTYPE_F32
 
 
-def _heads(H, Hk):
-    """(name suffix, head arguments) of an entry point: the _gqa form when Hk is given."""
-    return ("", (H,)) if Hk is None else ("_gqa", (H, Hk))
+def _heads(H, Hk, D, Dv=None):
+    """(name suffix, head arguments before K) of an entry point: the plain form (H, D), the _gqa
+    form (H, Hk, D) when Hk is given, the _dv form (H, Hk, Dk = D, Dv) when Dv is given."""
+    if Dv is not None:
+        return "_dv", (H, H if Hk is None else Hk, D, Dv)
+    return ("", (H, D)) if Hk is None else ("_gqa", (H, Hk, D))
 
 
 def kda_conv_l2norm_prep(q_raw, k_raw, v_raw, conv_w, ring_in, ring_out, f_raw, dt_bias, a_log,
@@ -210,12 +229,12 @@ def kda_conv_l2norm_prep(q_raw, k_raw, v_raw, conv_w, ring_in, ring_out, f_raw, 
                          gate_lb=-5.0, l2_eps=1e-6, D=HEAD_DIM, stream=None, Hk=None):
     """Hk: grouped queries (q/k planes of Hk heads; kda_conv_l2norm_prep_gqa)."""
     st = _stream(stream, q_hat)
-    sfx, heads = _heads(H, Hk)
+    sfx, heads = _heads(H, Hk, D)
     _call("kda_conv_l2norm_prep" + sfx, q_hat,
         _ptr(q_raw), _ptr(k_raw), _ptr(v_raw), _raw_dtype(q_raw), _ptr(conv_w), _ptr(ring_in),
         _ptr(ring_out), _ptr(f_raw), _ptr(dt_bias), _ptr(a_log), gate_mode, gate_lb,
         _ptr(beta_raw), _ptr(q_hat), _ptr(k_hat), _ptr(v_hat), _ptr(g), _ptr(beta), N, T, *heads,
-        D, K, l2_eps, st)
+        K, l2_eps, st)
 
 
 def kda_conv_l2norm_prep_varlen(q_raw, k_raw, v_raw, conv_w, ring_in, ring_out, f_raw, dt_bias,
@@ -226,12 +245,12 @@ def kda_conv_l2norm_prep_varlen(q_raw, k_raw, v_raw, conv_w, ring_in, ring_out, 
     N = cu_seqlens_host.numel() - 1
     total = int(cu_seqlens_host[-1])
     st = _stream(stream, q_hat)
-    sfx, heads = _heads(H, Hk)
+    sfx, heads = _heads(H, Hk, D)
     _call("kda_conv_l2norm_prep_varlen" + sfx, q_hat,
         _ptr(q_raw), _ptr(k_raw), _ptr(v_raw), _raw_dtype(q_raw), _ptr(conv_w), _ptr(ring_in),
         _ptr(ring_out), _ptr(f_raw), _ptr(dt_bias), _ptr(a_log), gate_mode, gate_lb,
         _ptr(beta_raw), _ptr(q_hat), _ptr(k_hat), _ptr(v_hat), _ptr(g), _ptr(beta),
-        _ptr(cu_seqlens), _ptr(cu_seqlens_host), N, total, *heads, D, K, l2_eps, st)
+        _ptr(cu_seqlens), _ptr(cu_seqlens_host), N, total, *heads, K, l2_eps, st)
 
 
 def kda_scan_workspace_bytes(N, total_T, H, gate_mode=0, algo=ALGO_AUTO, D=HEAD_DIM) -> int:
@@ -381,30 +400,30 @@ def kda_gated_rmsnorm_silu_out(o, norm_w, gate_raw, y, *, rows, eps=1e-6, D=HEAD
 def kda_decode_fused(q_raw, k_raw, v_raw, conv_w, ring_in, ring_out, f_raw, dt_bias, a_log,
                      beta_raw, state_in, state_out, norm_w, gate_raw, y, *, N, T, H, K=4,
                      gate_mode=0, gate_lb=-5.0, l2_eps=1e-6, scale=None, rms_eps=1e-6,
-                     D=HEAD_DIM, stream=None, Hk=None):
+                     D=HEAD_DIM, stream=None, Hk=None, Dv=None):
     scale = D ** -0.5 if scale is None else scale
     st = _stream(stream, y)
-    sfx, heads = _heads(H, Hk)
+    sfx, heads = _heads(H, Hk, D, Dv)
     _call("kda_decode_fused" + sfx, y,
         _ptr(q_raw), _ptr(k_raw), _ptr(v_raw), _raw_dtype(q_raw), _ptr(conv_w), _ptr(ring_in),
         _ptr(ring_out), _ptr(f_raw), _ptr(dt_bias), _ptr(a_log), gate_mode, gate_lb,
         _ptr(beta_raw), _ptr(state_in), _ptr(state_out), _ptr(norm_w), _ptr(gate_raw), _ptr(y),
-        N, T, *heads, D, K, l2_eps, scale, rms_eps, st)
+        N, T, *heads, K, l2_eps, scale, rms_eps, st)
 
 
 def kda_verify_rollback(q_raw, k_raw, v_raw, conv_w, ring_in, ring_out, f_raw, dt_bias, a_log,
                         beta_raw, state_in, state_out, norm_w, gate_raw, y, keep, *, N, T, H, K=4,
                         gate_mode=0, gate_lb=-5.0, l2_eps=1e-6, scale=None, rms_eps=1e-6,
-                        D=HEAD_DIM, stream=None, Hk=None):
+                        D=HEAD_DIM, stream=None, Hk=None, Dv=None):
     """keep: int32 device tensor [N], tokens accepted per sequence of the T-token verify batch."""
     scale = D ** -0.5 if scale is None else scale
     st = _stream(stream, y)
-    sfx, heads = _heads(H, Hk)
+    sfx, heads = _heads(H, Hk, D, Dv)
     _call("kda_verify_rollback" + sfx, y,
         _ptr(q_raw), _ptr(k_raw), _ptr(v_raw), _raw_dtype(q_raw), _ptr(conv_w), _ptr(ring_in),
         _ptr(ring_out), _ptr(f_raw), _ptr(dt_bias), _ptr(a_log), gate_mode, gate_lb,
         _ptr(beta_raw), _ptr(state_in), _ptr(state_out), _ptr(norm_w), _ptr(gate_raw), _ptr(y),
-        _ptr(keep), N, T, *heads, D, K, l2_eps, scale, rms_eps, st)
+        _ptr(keep), N, T, *heads, K, l2_eps, scale, rms_eps, st)
 
 
 def kda_prefill_workspace_bytes(N, total_T, H, gate_mode=0, D=HEAD_DIM) -> int:
@@ -424,32 +443,32 @@ def _ws_bytes(workspace):
 def kda_prefill_fused(q_raw, k_raw, v_raw, conv_w, ring_in, ring_out, f_raw, dt_bias, a_log,
                       beta_raw, state_in, state_out, norm_w, gate_raw, y, workspace, *, N, T, H,
                       K=4, gate_mode=0, gate_lb=-5.0, l2_eps=1e-6, scale=None, rms_eps=1e-6,
-                      D=HEAD_DIM, stream=None, Hk=None):
+                      D=HEAD_DIM, stream=None, Hk=None, Dv=None):
     scale = D ** -0.5 if scale is None else scale
     st = _stream(stream, y)
-    sfx, heads = _heads(H, Hk)
+    sfx, heads = _heads(H, Hk, D, Dv)
     _call("kda_prefill_fused" + sfx, y,
         _ptr(q_raw), _ptr(k_raw), _ptr(v_raw), _raw_dtype(q_raw), _ptr(conv_w), _ptr(ring_in),
         _ptr(ring_out), _ptr(f_raw), _ptr(dt_bias), _ptr(a_log), gate_mode, gate_lb,
         _ptr(beta_raw), _ptr(state_in), _ptr(state_out), _ptr(norm_w), _ptr(gate_raw), _ptr(y),
-        N, T, *heads, D, K, l2_eps, scale, rms_eps, _ptr(workspace), _ws_bytes(workspace), st)
+        N, T, *heads, K, l2_eps, scale, rms_eps, _ptr(workspace), _ws_bytes(workspace), st)
 
 
 def kda_prefill_fused_varlen(q_raw, k_raw, v_raw, conv_w, ring_in, ring_out, f_raw, dt_bias,
                              a_log, beta_raw, state_in, state_out, norm_w, gate_raw, y,
                              workspace, cu_seqlens, cu_seqlens_host, *, H, K=4, gate_mode=0,
                              gate_lb=-5.0, l2_eps=1e-6, scale=None, rms_eps=1e-6, D=HEAD_DIM,
-                             stream=None, Hk=None):
+                             stream=None, Hk=None, Dv=None):
     N = cu_seqlens_host.numel() - 1
     total = int(cu_seqlens_host[-1])
     scale = D ** -0.5 if scale is None else scale
     st = _stream(stream, y)
-    sfx, heads = _heads(H, Hk)
+    sfx, heads = _heads(H, Hk, D, Dv)
     _call("kda_prefill_fused_varlen" + sfx, y,
         _ptr(q_raw), _ptr(k_raw), _ptr(v_raw), _raw_dtype(q_raw), _ptr(conv_w), _ptr(ring_in),
         _ptr(ring_out), _ptr(f_raw), _ptr(dt_bias), _ptr(a_log), gate_mode, gate_lb,
         _ptr(beta_raw), _ptr(state_in), _ptr(state_out), _ptr(norm_w), _ptr(gate_raw), _ptr(y),
-        _ptr(cu_seqlens), _ptr(cu_seqlens_host), N, total, *heads, D, K, l2_eps, scale, rms_eps,
+        _ptr(cu_seqlens), _ptr(cu_seqlens_host), N, total, *heads, K, l2_eps, scale, rms_eps,
         _ptr(workspace), _ws_bytes(workspace), st)
 
 

@@ -122,14 +122,16 @@ def kda_prefill(*, q_raw, k_raw, v_raw, f_raw, dt_bias, a_log, beta_raw, state_i
                 ring_in, norm_w, gate_raw, cu_seqlens=None, cu_seqlens_host=None, N=None, T=None,
                 K=4, gate_mode=0, gate_lb=-5.0, l2_eps=1e-6, rms_eps=1e-6, scale=None,
                 state_out=None, ring_out=None, y=None, workspace=None, stream=None,
-                norm_gate="sigmoid", Hk=None):
+                norm_gate="sigmoid", Hk=None, Dv=None):
     """The whole mixer for a prefill in one library call (kda_prefill_fused[_varlen]): conv +
     SiLU, l2 norm, gates, the chunked scan and the gated RMSNorm, the intermediates kept in the
     workspace.  Either (N, T) or cu_seqlens (int32 device) + cu_seqlens_host (int32
     CPU).  workspace: from kda.prefill_workspace (allocated here when None).
     norm_gate: the RMSNorm's gate, "sigmoid" (KDA) or "silu" (GDN's gated_rmsnorm).
+    Dv: value heads Dv wide (the _dv entries; the workspace counts H * Dv / 128 units).
     Returns a dict with y, state_out and ring_out."""
-    C = H * kda.HEAD_DIM
+    units = H if Dv is None else H * Dv // kda.HEAD_DIM
+    C = units * kda.HEAD_DIM
     rows = q_raw.shape[0]
     varlen = cu_seqlens is not None
     if not varlen:
@@ -142,11 +144,11 @@ def kda_prefill(*, q_raw, k_raw, v_raw, f_raw, dt_bias, a_log, beta_raw, state_i
     if ring_out is None and conv_w is not None:
         ring_out = torch.empty_like(ring_in)
     if workspace is None:
-        workspace = kda.prefill_workspace(n_seq, rows, H, q_raw.device, gate_mode)
+        workspace = kda.prefill_workspace(n_seq, rows, units, q_raw.device, gate_mode)
     args = (q_raw, k_raw, v_raw, conv_w, ring_in, ring_out, f_raw, dt_bias, a_log, beta_raw,
             state_in, state_out, norm_w, gate_raw, y, workspace)
     common = dict(H=H, K=K, gate_mode=gate_mode | _norm_flag(norm_gate), gate_lb=gate_lb,
-                  l2_eps=l2_eps, scale=scale, rms_eps=rms_eps, stream=stream, Hk=Hk)
+                  l2_eps=l2_eps, scale=scale, rms_eps=rms_eps, stream=stream, Hk=Hk, Dv=Dv)
     if varlen:
         kda.kda_prefill_fused_varlen(*args, cu_seqlens, cu_seqlens_host, **common)
     else:
@@ -157,27 +159,29 @@ def kda_prefill(*, q_raw, k_raw, v_raw, f_raw, dt_bias, a_log, beta_raw, state_i
 def kda_decode(*, q_raw, k_raw, v_raw, conv_w, ring_in, f_raw, dt_bias, a_log, beta_raw,
                state_in, norm_w, gate_raw, N, T, H, K=4, gate_mode=0, gate_lb=-5.0,
                l2_eps=1e-6, rms_eps=1e-6, scale=None, state_out=None, ring_out=None, y=None,
-               stream=None, norm_gate="sigmoid", Hk=None):
+               stream=None, norm_gate="sigmoid", Hk=None, Dv=None):
     """One fused decode (T=1) or T-token verify launch.  ring_out may be ring_in and state_out
-    state_in (in place).  norm_gate: "sigmoid" (KDA) or "silu" (GDN's gated_rmsnorm)."""
+    state_in (in place).  norm_gate: "sigmoid" (KDA) or "silu" (GDN's gated_rmsnorm).
+    Dv: value heads Dv wide (kda_decode_fused_dv)."""
     if state_out is None:
         state_out = torch.empty_like(state_in)
     if ring_out is None:
         ring_out = torch.empty_like(ring_in)
     if y is None:
-        y = _empty((q_raw.shape[0], H * kda.HEAD_DIM), q_raw)
+        y = _empty((q_raw.shape[0], H * (kda.HEAD_DIM if Dv is None else Dv)), q_raw)
     kda.kda_decode_fused(q_raw, k_raw, v_raw, conv_w, ring_in, ring_out, f_raw, dt_bias, a_log,
                          beta_raw, state_in, state_out, norm_w, gate_raw, y, N=N, T=T, H=H, K=K,
                          gate_mode=gate_mode | _norm_flag(norm_gate), gate_lb=gate_lb,
                          l2_eps=l2_eps, scale=scale,
-                         rms_eps=rms_eps, stream=stream, Hk=Hk)
+                         rms_eps=rms_eps, stream=stream, Hk=Hk, Dv=Dv)
     return dict(y=y, state_out=state_out, ring_out=ring_out)
 
 
 def kda_verify_rollback(*, q_raw, k_raw, v_raw, conv_w, ring_in, f_raw, dt_bias, a_log,
                         beta_raw, state_in, norm_w, gate_raw, keep, N, T, H, K=4, gate_mode=0,
                         gate_lb=-5.0, l2_eps=1e-6, rms_eps=1e-6, scale=None, state_out=None,
-                        ring_out=None, y=None, stream=None, norm_gate="sigmoid", Hk=None):
+                        ring_out=None, y=None, stream=None, norm_gate="sigmoid", Hk=None,
+                        Dv=None):
     """Roll a T-token verify round back to the accepted prefixes: keep (int32 device [N]) tokens
     of each sequence, from the pre-round state_in and ring_in.  ring_out may be ring_in."""
     if state_out is None:
@@ -185,13 +189,13 @@ def kda_verify_rollback(*, q_raw, k_raw, v_raw, conv_w, ring_in, f_raw, dt_bias,
     if ring_out is None:
         ring_out = torch.empty_like(ring_in)
     if y is None:
-        y = torch.zeros((q_raw.shape[0], H * kda.HEAD_DIM), dtype=torch.float32,
-                        device=q_raw.device)
+        y = torch.zeros((q_raw.shape[0], H * (kda.HEAD_DIM if Dv is None else Dv)),
+                        dtype=torch.float32, device=q_raw.device)
     kda.kda_verify_rollback(q_raw, k_raw, v_raw, conv_w, ring_in, ring_out, f_raw, dt_bias,
                             a_log, beta_raw, state_in, state_out, norm_w, gate_raw, y, keep,
                             N=N, T=T, H=H, K=K, gate_mode=gate_mode | _norm_flag(norm_gate),
                             gate_lb=gate_lb, l2_eps=l2_eps, scale=scale, rms_eps=rms_eps,
-                            stream=stream, Hk=Hk)
+                            stream=stream, Hk=Hk, Dv=Dv)
     return dict(y=y, state_out=state_out, ring_out=ring_out)
 
 

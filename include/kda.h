@@ -336,8 +336,9 @@ const char* kda_kernel_name(int id);
  * kda_decode_fused -- one decode step (T = 1) or a T-token speculative verify (2 <= T <= 16) of
  * N sequences in ONE launch: kda_conv_l2norm_prep + kda_scan + kda_gated_rmsnorm_out with the
  * same arguments, computed without round-tripping the intermediates through memory.  Its outputs
- * equal those three calls bit for bit, and a T-token call equals T chained one-token calls bit
- * for bit (the decode == verify identity of the KDA module doc).
+ * equal those three calls to f32 rounding (the ring bit for bit; the two scans sum the key
+ * dimension over different lane groupings), and a T-token call equals T chained one-token calls
+ * bit for bit (the decode == verify identity of the KDA module doc).
  * Argument meanings and layouts as in the three calls; rows = N*T; conv_w must not be NULL.
  * ring_in / ring_out may be the same buffer, and so may state_in / state_out (an in-place step:
  * with stable pointers a decode step can be captured once in a CUDA graph and replayed); buffers
@@ -454,6 +455,16 @@ int kda_verify_rollback_gqa(const void* q_raw, const void* k_raw, const void* v_
  * H*m heads, sharing value head h's gate, beta and q/k head: the recurrence's columns never mix).
  * The workspace for the chunked form is kda_scan_workspace_bytes(N, total_T, H*m, 128, ...).
  * The gated RMSNorm over rows of Dv values is kda_gated_rmsnorm_out / _silu_out with D = Dv.
+ * The fused entries take the same layouts, plus
+ *   norm_w     [Dv];  gate_raw, y  [rows, H*Dv];  the RMSNorm's mean over the whole Dv row.
+ *   kda_prefill_fused_dv / _varlen_dv: workspace of kda_prefill_workspace_bytes(N, total_T, H*m,
+ *   128, gate_mode) bytes; outputs equal kda_conv_l2norm_prep_dv + kda_scan_dv (KDA_ALGO_CHUNK)
+ *   + kda_gated_rmsnorm_out(D = Dv) bit for bit.
+ *   kda_decode_fused_dv / kda_verify_rollback_dv: one launch in which each value head is a
+ *   thread-block cluster of m CTAs (one per 128-wide column block) that sum the RMSNorm's squares
+ *   across the cluster; decode == verify bit for bit and the staged path to f32 rounding, as for
+ *   Dv = 128.  With
+ *   m > 1 or Hk < H the ring cannot be rolled in place (ring_in == ring_out returns 40003).
  */
 int kda_conv_l2norm_prep_dv(const void* q_raw, const void* k_raw, const void* v_raw,
                             int raw_dtype, const float* conv_w, const float* ring_in,
@@ -480,6 +491,39 @@ int kda_scan_varlen_dv(const float* q_hat, const float* k_hat, const float* v_ha
                        const int* cu_seqlens_host, int N, int total_T, int H, int Hk, int Dk,
                        int Dv, float scale, int algo, void* workspace, size_t workspace_bytes,
                        void* stream);
+int kda_prefill_fused_dv(const void* q_raw, const void* k_raw, const void* v_raw, int raw_dtype,
+                         const float* conv_w, const float* ring_in, float* ring_out,
+                         const float* f_raw, const float* dt_bias, const float* a_log,
+                         int gate_mode, float gate_lb, const float* beta_raw,
+                         const float* state_in, float* state_out, const float* norm_w,
+                         const float* gate_raw, float* y, int N, int T, int H, int Hk, int Dk,
+                         int Dv, int K, float l2_eps, float scale, float rms_eps, void* workspace,
+                         size_t workspace_bytes, void* stream);
+int kda_prefill_fused_varlen_dv(const void* q_raw, const void* k_raw, const void* v_raw,
+                                int raw_dtype, const float* conv_w, const float* ring_in,
+                                float* ring_out, const float* f_raw, const float* dt_bias,
+                                const float* a_log, int gate_mode, float gate_lb,
+                                const float* beta_raw, const float* state_in, float* state_out,
+                                const float* norm_w, const float* gate_raw, float* y,
+                                const int* cu_seqlens, const int* cu_seqlens_host, int N,
+                                int total_T, int H, int Hk, int Dk, int Dv, int K, float l2_eps,
+                                float scale, float rms_eps, void* workspace,
+                                size_t workspace_bytes, void* stream);
+int kda_decode_fused_dv(const void* q_raw, const void* k_raw, const void* v_raw, int raw_dtype,
+                        const float* conv_w, const float* ring_in, float* ring_out,
+                        const float* f_raw, const float* dt_bias, const float* a_log,
+                        int gate_mode, float gate_lb, const float* beta_raw,
+                        const float* state_in, float* state_out, const float* norm_w,
+                        const float* gate_raw, float* y, int N, int T, int H, int Hk, int Dk,
+                        int Dv, int K, float l2_eps, float scale, float rms_eps, void* stream);
+int kda_verify_rollback_dv(const void* q_raw, const void* k_raw, const void* v_raw,
+                           int raw_dtype, const float* conv_w, const float* ring_in,
+                           float* ring_out, const float* f_raw, const float* dt_bias,
+                           const float* a_log, int gate_mode, float gate_lb,
+                           const float* beta_raw, const float* state_in, float* state_out,
+                           const float* norm_w, const float* gate_raw, float* y, const int* keep,
+                           int N, int T, int H, int Hk, int Dk, int Dv, int K, float l2_eps,
+                           float scale, float rms_eps, void* stream);
 
 /*
  * kda_proj6 -- stage 1 of kda_core_gated: the six projections of the layer input that the mixer

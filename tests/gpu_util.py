@@ -65,6 +65,8 @@ def gpu_prefill(inp: KdaInputs, *, varlen=None, **kw):
         extra = dict(N=inp.N, T=T)
     if inp.Hk is not None:
         kw = dict(kw, Hk=inp.Hk)
+    if inp.Dv is not None:
+        kw = dict(kw, Dv=inp.Dv)
     out = mixer.kda_prefill(H=inp.H, K=inp.K, gate_mode=inp.gate_mode, **d, **extra, **kw)
     torch.cuda.synchronize()
     return out

@@ -228,3 +228,28 @@ def test_value_width_contract(kda):
         norm = lib.kda_gated_rmsnorm_out(FAKE, FAKE, FAKE, FAKE, ctypes.c_long(4), d, F(1e-6),
                                          None)
         assert norm == 40001, d
+
+
+def test_value_width_fused_contract(kda):
+    """The fused value-width entries check Dk, Dv and Hk on the host."""
+    lib = kda.library()
+    F = ctypes.c_float
+    pre = lambda **kw: lib.kda_prefill_fused_dv(  # noqa: E731
+        FAKE, FAKE, FAKE, 1, FAKE, FAKE, FAKE * 2, FAKE, FAKE, FAKE, 0, F(-5.0), FAKE, FAKE,
+        FAKE * 64, FAKE, FAKE, FAKE, 1, 4, 2, kw.get("Hk", 1), kw.get("Dk", 128),
+        kw.get("Dv", 256), 4, F(1e-6), F(0.1), F(1e-6), None, 0, None)
+    assert pre(Dv=192) == 40001
+    assert pre(Dk=256) == 40001
+    assert pre(Hk=3) == 40005
+    dec = lambda **kw: lib.kda_decode_fused_dv(  # noqa: E731
+        FAKE, FAKE, FAKE, 1, FAKE, FAKE, FAKE * 2, FAKE, FAKE, FAKE, 0, F(-5.0), FAKE, FAKE,
+        FAKE * 64, FAKE, FAKE, FAKE, 2, kw.get("T", 1), 2, kw.get("Hk", 1), 128,
+        kw.get("Dv", 256), 4, F(1e-6), F(0.1), F(1e-6), None)
+    assert dec(Dv=2048) == 40001
+    assert dec(Hk=0) == 40005
+    assert dec(T=17) == 40005
+    rb = lib.kda_verify_rollback_dv(
+        FAKE, FAKE, FAKE, 1, FAKE, FAKE, FAKE * 2, FAKE, FAKE, FAKE, 0, F(-5.0), FAKE, FAKE,
+        FAKE * 64, FAKE, FAKE, FAKE, None, 2, 4, 2, 1, 128, 256, 4, F(1e-6), F(0.1), F(1e-6),
+        None)
+    assert rb == 40004                       # keep is required

@@ -14,7 +14,7 @@ import pytest
 import torch
 
 from gated_delta_rule_scan_gb300 import inputs
-from tests.gpu_util import check_all_heads, gpu_forward
+from tests.gpu_util import check_all_heads, gpu_forward, rel_linf
 
 pytestmark = pytest.mark.gpu
 
@@ -116,7 +116,6 @@ def test_value_width_norm_rows():
     """The gated RMSNorm over rows of 256 and 1024 values against the oracle's norm."""
     from gated_delta_rule_scan_gb300 import kda
     from oracle import oracle as orc
-    from tests.gpu_util import rel_linf
     rng = np.random.default_rng(77)
     for width, rows, silu in ((256, 37, False), (1024, 9, True), (512, 1, False)):
         o = rng.standard_normal((rows, width)).astype(np.float32)
@@ -129,3 +128,126 @@ def test_value_width_norm_rows():
         torch.cuda.synchronize()
         ref = orc.gated_rmsnorm(o, w, z, 1e-6, gate="silu" if silu else "sigmoid")
         assert rel_linf(y, ref) <= 1e-5, width
+
+
+# ---- the fused entries: prefill (prep + chunked scan + RMSNorm over Dv) and decode / verify /
+#      rollback (a value head = a thread-block cluster of Dv / 128 CTAs) ---------------------------
+
+from tests.gpu_util import gpu_prefill, to_dev  # noqa: E402
+
+FUSED = ("y", "state_out", "ring_out")
+
+
+@pytest.mark.parametrize("H,Hk,Dv,gate_mode", [(2, None, 256, 0), (2, 1, 384, 1), (3, 3, 256, 0)])
+def test_value_width_fused_prefill(H, Hk, Dv, gate_mode):
+    """kda_prefill_fused_dv against the oracle and bit-equal to the staged chunked path (prep_dv,
+    scan_dv, the RMSNorm over Dv); two sequences of 75 tokens, random state and ring."""
+    inp = inputs.make_inputs(400 + 7 * H + Dv // 128, H=H, N=2, T=75, raw_dtype="bf16",
+                             conv=True, ring="randn", gate_mode=gate_mode, state="randn",
+                             epilogue=True, Hk=Hk, Dv=Dv)
+    fused = gpu_prefill(inp)
+    check_all_heads(fused, inp, FUSED)
+    staged = gpu_forward(inp, algo=2)
+    for k in FUSED:
+        assert torch.equal(fused[k], staged[k]), k
+
+
+def test_value_width_fused_prefill_varlen():
+    """Packed sequences with empty ones and lengths around the conv window and the chunk."""
+    lengths = [5, 0, 1, 2, 33, 64, 70]
+    H, Hk, Dv = 2, 1, 256
+    cu = np.concatenate([[0], np.cumsum(lengths)])
+    rows = int(cu[-1])
+    inp = inputs.make_inputs(431, H=H, N=len(lengths), lengths=(0, 1), raw_dtype="bf16",
+                             conv=True, ring="randn", state="randn", epilogue=True, Hk=Hk, Dv=Dv)
+    rng = np.random.default_rng(1431)
+
+    def draw(shape):
+        return torch.from_numpy(rng.standard_normal(shape).astype(np.float32))
+    inp.q_raw = draw((rows, Hk * 128)).to(torch.bfloat16)
+    inp.k_raw = draw((rows, Hk * 128)).to(torch.bfloat16)
+    inp.v_raw = draw((rows, H * Dv)).to(torch.bfloat16)
+    inp.f_raw = draw((rows, H * 128))
+    inp.beta_raw = draw((rows, H))
+    inp.gate_raw = draw((rows, H * Dv))
+    inp.cu_seqlens = cu
+    fused = gpu_prefill(inp, varlen=True)
+    check_all_heads(fused, inp, FUSED)
+    staged = gpu_forward(inp, varlen=True, algo=2)
+    for k in FUSED:
+        assert torch.equal(fused[k], staged[k]), k
+
+
+def _decode_step(d, N, T, t, H, Hk, Dv, state, ring, norm_gate="sigmoid", gate_mode=0):
+    from gated_delta_rule_scan_gb300 import mixer
+    rows = torch.arange(N, device="cuda") * T + t
+    step = {k: d[k] for k in ("conv_w", "dt_bias", "a_log", "norm_w")}
+    for k in ("q_raw", "k_raw", "v_raw", "f_raw", "beta_raw", "gate_raw"):
+        step[k] = d[k][rows].contiguous()
+    return mixer.kda_decode(N=N, T=1, H=H, Hk=Hk, Dv=Dv, state_in=state, ring_in=ring,
+                            norm_gate=norm_gate, gate_mode=gate_mode, **step)
+
+
+@pytest.mark.parametrize("H,Hk,Dv,T,gate_mode", [(2, 1, 256, 1, 0), (3, 3, 256, 4, 0),
+                                                 (2, 2, 512, 4, 1), (1, 1, 1024, 2, 0)])
+def test_value_width_decode_verify(H, Hk, Dv, T, gate_mode):
+    """kda_decode_fused_dv against the oracle; a T-token call bit-equal to T chained one-token
+    calls; the staged sequential path (prep_dv, scan_dv, RMSNorm over Dv) equal to f32 rounding,
+    the ring bit for bit (the two scans sum the key dimension over different lane groupings)."""
+    from gated_delta_rule_scan_gb300 import mixer
+    N = 5
+    ng = "silu" if gate_mode == 1 else "sigmoid"
+    inp = inputs.make_inputs(440 + T + Dv // 128, H=H, N=N, T=T, raw_dtype="bf16", conv=True,
+                             ring="randn", gate_mode=gate_mode, state="randn", epilogue=True,
+                             Hk=Hk, Dv=Dv)
+    d = to_dev(inp)
+    full = mixer.kda_decode(N=N, T=T, H=H, Hk=Hk, Dv=Dv, norm_gate=ng, gate_mode=gate_mode, **d)
+    torch.cuda.synchronize()
+    check_all_heads(full, inp, FUSED, norm_gate=ng)
+    staged = gpu_forward(inp, algo=1, norm_gate=ng)
+    assert torch.equal(full["ring_out"], staged["ring_out"])
+    for k in ("y", "state_out"):
+        assert rel_linf(full[k], staged[k]) <= 1e-5, k
+    state, ring = d["state_in"], d["ring_in"]
+    ys = []
+    for t in range(T):
+        r = _decode_step(d, N, T, t, H, Hk, Dv, state, ring, ng, gate_mode)
+        state, ring = r["state_out"], r["ring_out"]
+        ys.append(r["y"].view(N, 1, -1))
+    torch.cuda.synchronize()
+    assert torch.equal(torch.cat(ys, dim=1).view(N * T, -1), full["y"])
+    assert torch.equal(state, full["state_out"])
+    assert torch.equal(ring, full["ring_out"])
+
+
+def test_value_width_rollback_and_in_place_refusal():
+    """kda_verify_rollback_dv equals keep[n] chained one-token decodes; rolling the ring in place
+    is refused when a value head spans several units (40003)."""
+    from gated_delta_rule_scan_gb300 import kda, mixer
+    N, H, Hk, Dv, T = 4, 2, 2, 256, 4
+    inp = inputs.make_inputs(450, H=H, N=N, T=T, raw_dtype="bf16", conv=True, ring="randn",
+                             state="randn", epilogue=True, Hk=Hk, Dv=Dv)
+    d = to_dev(inp)
+    keep_h = np.array([0, 1, 3, 4], dtype=np.int32)
+    keep = torch.from_numpy(keep_h).cuda()
+    rb = mixer.kda_verify_rollback(N=N, T=T, H=H, Hk=Hk, Dv=Dv, keep=keep, **d)
+    torch.cuda.synchronize()
+    for n in range(N):
+        state = d["state_in"][n:n + 1]
+        ring = d["ring_in"][n:n + 1]
+        for t in range(int(keep_h[n])):
+            row = slice(n * T + t, n * T + t + 1)
+            step = {k: d[k] for k in ("conv_w", "dt_bias", "a_log", "norm_w")}
+            for k in ("q_raw", "k_raw", "v_raw", "f_raw", "beta_raw", "gate_raw"):
+                step[k] = d[k][row].contiguous()
+            r = mixer.kda_decode(N=1, T=1, H=H, Hk=Hk, Dv=Dv, state_in=state, ring_in=ring,
+                                 **step)
+            assert torch.equal(r["y"], rb["y"][row])
+            state, ring = r["state_out"], r["ring_out"]
+        torch.cuda.synchronize()
+        assert torch.equal(state, rb["state_out"][n:n + 1])
+        assert torch.equal(ring, rb["ring_out"][n:n + 1])
+    ring = d["ring_in"].clone()
+    with pytest.raises(kda.KdaError) as e:
+        mixer.kda_decode(N=N, T=T, H=H, Hk=Hk, Dv=Dv, ring_out=ring, **dict(d, ring_in=ring))
+    assert e.value.status == 40003
