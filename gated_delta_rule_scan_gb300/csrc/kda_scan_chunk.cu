@@ -423,7 +423,11 @@ kda_chunk_inter_kernel(ScanArgs a, const int* chunk_off, const unsigned char* ws
         mma1_half(st, 4);
         tc_commit(&sm.bar_mma);
     };
-    // the state is in TMEM; the first chunk's MMA-1 goes out as soon as its block lands
+    // the state is in TMEM (the barrier orders every thread's stores before the first MMA-1); the
+    // first chunk's MMA-1 goes out as soon as its block lands
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
     if (tid == 0 && nch > 0) {
         for (int i = 0; i < kInterStages && i < nch; ++i) issue(i, i);
         tc_fence_before();
