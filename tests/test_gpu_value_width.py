@@ -138,13 +138,18 @@ from tests.gpu_util import gpu_prefill, to_dev  # noqa: E402
 FUSED = ("y", "state_out", "ring_out")
 
 
-@pytest.mark.parametrize("H,Hk,Dv,gate_mode", [(2, None, 256, 0), (2, 1, 384, 1), (3, 3, 256, 0)])
-def test_value_width_fused_prefill(H, Hk, Dv, gate_mode):
+@pytest.mark.parametrize("H,Hk,Dv,gate_mode,raw,K", [(2, None, 256, 0, "bf16", 4),
+                                                    (2, 1, 384, 1, "bf16", 4),
+                                                    (3, 3, 256, 0, "bf16", 4),
+                                                    (2, 1, 256, 0, "f32", 4),
+                                                    (2, 2, 256, 1, "bf16", 6)])
+def test_value_width_fused_prefill(H, Hk, Dv, gate_mode, raw, K):
     """kda_prefill_fused_dv against the oracle and bit-equal to the staged chunked path (prep_dv,
-    scan_dv, the RMSNorm over Dv); two sequences of 75 tokens, random state and ring."""
-    inp = inputs.make_inputs(400 + 7 * H + Dv // 128, H=H, N=2, T=75, raw_dtype="bf16",
+    scan_dv, the RMSNorm over Dv); two sequences of 75 tokens, random state and ring; bf16 raw
+    rows (staged by TMA) and f32 raw rows (loaded directly), conv widths 4 and 6."""
+    inp = inputs.make_inputs(400 + 7 * H + Dv // 128 + K, H=H, N=2, T=75, raw_dtype=raw,
                              conv=True, ring="randn", gate_mode=gate_mode, state="randn",
-                             epilogue=True, Hk=Hk, Dv=Dv)
+                             epilogue=True, Hk=Hk, Dv=Dv, K=K)
     fused = gpu_prefill(inp)
     check_all_heads(fused, inp, FUSED)
     staged = gpu_forward(inp, algo=2)
@@ -178,30 +183,34 @@ def test_value_width_fused_prefill_varlen():
         assert torch.equal(fused[k], staged[k]), k
 
 
-def _decode_step(d, N, T, t, H, Hk, Dv, state, ring, norm_gate="sigmoid", gate_mode=0):
+def _decode_step(d, N, T, t, H, Hk, Dv, state, ring, norm_gate="sigmoid", gate_mode=0, K=4):
     from gated_delta_rule_scan_gb300 import mixer
     rows = torch.arange(N, device="cuda") * T + t
     step = {k: d[k] for k in ("conv_w", "dt_bias", "a_log", "norm_w")}
     for k in ("q_raw", "k_raw", "v_raw", "f_raw", "beta_raw", "gate_raw"):
         step[k] = d[k][rows].contiguous()
-    return mixer.kda_decode(N=N, T=1, H=H, Hk=Hk, Dv=Dv, state_in=state, ring_in=ring,
+    return mixer.kda_decode(N=N, T=1, H=H, Hk=Hk, Dv=Dv, K=K, state_in=state, ring_in=ring,
                             norm_gate=norm_gate, gate_mode=gate_mode, **step)
 
 
-@pytest.mark.parametrize("H,Hk,Dv,T,gate_mode", [(2, 1, 256, 1, 0), (3, 3, 256, 4, 0),
-                                                 (2, 2, 512, 4, 1), (1, 1, 1024, 2, 0)])
-def test_value_width_decode_verify(H, Hk, Dv, T, gate_mode):
+@pytest.mark.parametrize("H,Hk,Dv,T,gate_mode,raw,K", [(2, 1, 256, 1, 0, "bf16", 4),
+                                                       (3, 3, 256, 4, 0, "bf16", 4),
+                                                       (2, 2, 512, 4, 1, "bf16", 4),
+                                                       (1, 1, 1024, 2, 0, "bf16", 4),
+                                                       (2, 1, 256, 3, 0, "f32", 6)])
+def test_value_width_decode_verify(H, Hk, Dv, T, gate_mode, raw, K):
     """kda_decode_fused_dv against the oracle; a T-token call bit-equal to T chained one-token
     calls; the staged sequential path (prep_dv, scan_dv, RMSNorm over Dv) equal to f32 rounding,
     the ring bit for bit (the two scans sum the key dimension over different lane groupings)."""
     from gated_delta_rule_scan_gb300 import mixer
     N = 5
     ng = "silu" if gate_mode == 1 else "sigmoid"
-    inp = inputs.make_inputs(440 + T + Dv // 128, H=H, N=N, T=T, raw_dtype="bf16", conv=True,
+    inp = inputs.make_inputs(440 + T + Dv // 128, H=H, N=N, T=T, raw_dtype=raw, conv=True,
                              ring="randn", gate_mode=gate_mode, state="randn", epilogue=True,
-                             Hk=Hk, Dv=Dv)
+                             Hk=Hk, Dv=Dv, K=K)
     d = to_dev(inp)
-    full = mixer.kda_decode(N=N, T=T, H=H, Hk=Hk, Dv=Dv, norm_gate=ng, gate_mode=gate_mode, **d)
+    full = mixer.kda_decode(N=N, T=T, H=H, Hk=Hk, Dv=Dv, K=K, norm_gate=ng, gate_mode=gate_mode,
+                            **d)
     torch.cuda.synchronize()
     check_all_heads(full, inp, FUSED, norm_gate=ng)
     staged = gpu_forward(inp, algo=1, norm_gate=ng)
@@ -211,7 +220,7 @@ def test_value_width_decode_verify(H, Hk, Dv, T, gate_mode):
     state, ring = d["state_in"], d["ring_in"]
     ys = []
     for t in range(T):
-        r = _decode_step(d, N, T, t, H, Hk, Dv, state, ring, ng, gate_mode)
+        r = _decode_step(d, N, T, t, H, Hk, Dv, state, ring, ng, gate_mode, K)
         state, ring = r["state_out"], r["ring_out"]
         ys.append(r["y"].view(N, 1, -1))
     torch.cuda.synchronize()
