@@ -28,10 +28,16 @@
 //     [dS^T | O2^T] = U'^T  (K e^{G_C-G} | Aqk)    M=128,              N=160, K=32
 //     S^T <- S^T Diag(e^{G_C}) + dS^T,   o = scale (O1 + O2)
 // with S^T and U'^T held in tensor memory as the MMAs' A operands and the state row kept in f32
-// registers.  All operands are bf16 split as x = hi + lo and every product is
-// hi*hi + hi*lo + lo*hi (about 16 significant bits; relative error ~1e-5, inside the 1e-3 parity
-// bound, where one bf16 pass gives ~4e-3).  Shared-memory operands are K-major, no swizzle,
-// 8-row x 16-byte core matrices (kda_tc.cuh).
+// registers.  Precision.  The intra kernel's products (A, Aqk, W, U) take both operands as bf16
+// hi + lo and sum hi*hi + hi*lo + lo*hi (about 16 significant bits).  The chain's two MMAs take
+// the f32 state and U' split as f16 hi + lo (22 bits) against single f16 images of their other
+// operand (11 bits): two products per K-step instead of three, 20 MMA instructions per chunk
+// instead of 30.  The chain's error is then the f16 rounding of (Q e^G | W) and
+// (K e^{G_C-G} | Aqk), a few 1e-4 relative at every length (measured 2.4e-4 .. 4.8e-4 on the
+// stated workloads, inside the 1e-3 parity bound), where bf16 images there gave 2e-3 .. 3e-3.
+// Every operand of those images is at most 1 in magnitude (e^{G} <= 1, l2-normalised q and k)
+// or a small multiple (W); the state and U' must stay below f16's 65504.  Shared-memory operands
+// are K-major, no swizzle, 8-row x 16-byte core matrices (kda_tc.cuh).
 //
 // Range.  The intra-chunk products pair k_t e^{G_t - c} with k_s e^{c - G_s}, c = half the
 // chunk's total gate per channel, so each factor stays below e^{|G_C|/2}.  For the per-channel
@@ -54,17 +60,27 @@ constexpr uint32_t kSboKt = 528;
 constexpr int kDevErrRange = 2;          // device error word bit: chunk gate outside f32 range
 
 // ---- workspace block of one (chunk, head) ----------------------------------------------------
-constexpr int kQWBytes = 64 * 128 * 2;             // [Q e^G (32 rows) ; W (32 rows)] x 128 k
-constexpr int kB2Bytes = (128 + kCc) * kCc * 2;    // [(K e^{G_C-G})^T (128 rows) ; Aqk (32)] x 32
+// The inter kernel's two B operands are single f16 images (its MMAs pair them with the state and
+// U' split into f16 hi + lo, two products per K-step); U and e^{G_C} are f32.
+constexpr int kQWBytes = 64 * 128 * 2;             // [Q e^G (32 rows) ; W (32 rows)] x 128 k, f16
+constexpr int kB2Bytes = (128 + kCc) * kCc * 2;    // [(K e^{G_C-G})^T (128 rows) ; Aqk (32)] x 32, f16
 constexpr int kUTBytes = 128 * kCc * 4;            // U f32 [32 t][128 v]
 constexpr int kEGBytes = 128 * 4;                  // e^{G_C} f32 [128]
-constexpr int kOffQW = 0;                          // hi, then lo at + kQWBytes
-constexpr int kOffB2 = 2 * kQWBytes;               // hi, then lo at + kB2Bytes
-constexpr int kOffUT = kOffB2 + 2 * kB2Bytes;
+constexpr int kOffQW = 0;
+constexpr int kOffB2 = kQWBytes;
+constexpr int kOffUT = kOffB2 + kB2Bytes;
 constexpr int kOffEG = kOffUT + kUTBytes;
-constexpr int kBlkBytes = kOffEG + kEGBytes;       // 70144
+constexpr int kBlkBytes = kOffEG + kEGBytes;       // 43520
 static_assert(kBlkBytes % 128 == 0, "workspace blocks stay 128-byte aligned");
+static_assert(kBlkBytes == kChunkBlockBytes, "the workspace sizing uses the same block size");
 constexpr int kHeaderAlign = 256;
+
+// store 8 values (one 16-byte core-matrix row) as f16 at byte offset off of an image
+__device__ __forceinline__ void put8h(unsigned char* img, uint32_t off, const float (&x)[8]) {
+    *reinterpret_cast<uint4*>(img + off) =
+        make_uint4(f16x2_rn(x[0], x[1]), f16x2_rn(x[2], x[3]), f16x2_rn(x[4], x[5]),
+                   f16x2_rn(x[6], x[7]));
+}
 
 // store 8 values (one 16-byte core-matrix row) as bf16 hi / lo at byte offset off of two images
 __device__ __forceinline__ void put8x(unsigned char* hi_img, unsigned char* lo_img, uint32_t off,
@@ -109,16 +125,14 @@ __device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint
         : "memory");
 }
 
-// D (+)= A * B^T, bf16x3, A in tensor memory (hi at a_hi, lo at a_lo; 8 columns per K-step of
-// 16), B in shared memory
-__device__ __forceinline__ void mma3_ts(uint32_t d, uint32_t a_hi, uint32_t a_lo, uint64_t b_hi,
-                                        uint64_t b_lo, int nks, uint32_t idesc) {
-    const uint32_t as[3] = {a_hi, a_hi, a_lo};
-    const uint64_t bs[3] = {b_hi, b_lo, b_hi};
-#pragma unroll
-    for (int p = 0; p < 3; ++p)
-        for (int ks = 0; ks < nks; ++ks)
-            tc_mma_ts(d, as[p] + 8 * ks, tc_desc_advance(bs[p], 256 * ks), idesc, p > 0 || ks > 0);
+// D = A * B^T, f16 x 2: A in tensor memory split as hi (at a_hi) + lo (at a_lo), 8 columns per
+// K-step of 16; B one f16 image in shared memory; the first product starts the sum
+__device__ __forceinline__ void mma2_ts(uint32_t d, uint32_t a_hi, uint32_t a_lo, uint64_t b,
+                                        int nks, uint32_t idesc) {
+    for (int ks = 0; ks < nks; ++ks) {
+        tc_mma_ts(d, a_hi + 8 * ks, tc_desc_advance(b, 256 * ks), idesc, ks > 0);
+        tc_mma_ts(d, a_lo + 8 * ks, tc_desc_advance(b, 256 * ks), idesc, true);
+    }
 }
 
 __device__ __forceinline__ void seq_range(const SeqLayout& L, int n, long& begin, long& end) {
@@ -244,8 +258,7 @@ __device__ __forceinline__ bool intra_mma_tail(IntraSmem& sm, int* err, unsigned
                 am[t * kLd + s] = s < t ? bt * d[s] * fac : 0.0f;
             }
         } else {
-            unsigned char* b2h = blk + kOffB2;
-            unsigned char* b2l = blk + kOffB2 + kB2Bytes;
+            unsigned char* b2 = blk + kOffB2;
 #pragma unroll
             for (int sb = 0; sb < kCc / 8; ++sb) {
                 float x[8];
@@ -255,7 +268,7 @@ __device__ __forceinline__ bool intra_mma_tail(IntraSmem& sm, int* err, unsigned
                     const float fac = GATE_MODE == 1 ? __expf(fminf(Gt - sm.gsc[s], 0.0f)) : 1.0f;
                     x[e] = s <= t ? d[s] * fac : 0.0f;
                 }
-                put8x(b2h, b2l, tc_offset(128 + t, 8 * sb, kSbo32), x);
+                put8h(b2, tc_offset(128 + t, 8 * sb, kSbo32), x);
             }
         }
     }
@@ -348,10 +361,10 @@ __device__ __forceinline__ bool intra_mma_tail(IntraSmem& sm, int* err, unsigned
             tmem_ld16(tlane + col0 + 16 * q, *reinterpret_cast<float(*)[16]>(&x[16 * q]));
         tmem_ld_wait();
         if (PRE_A) {        // staged in sm.ktv (free once MMA-b has completed), copied out in bulk
-            if (col0 < 128) {   // W row t: rows 0..31 of an image of 32 rows (hi, lo at +8 KB)
+            if (col0 < 128) {   // W row t: rows 0..31 of an f16 image of 32 rows
 #pragma unroll
                 for (int cb = 0; cb < CW / 8; ++cb)
-                    put8x(sm.ktv[1], sm.ktv[1] + kCc * kSbo128 / 8, tc_offset(t, col0 + 8 * cb, kSbo128),
+                    put8h(sm.ktv[1], tc_offset(t, col0 + 8 * cb, kSbo128),
                           *reinterpret_cast<const float(*)[8]>(&x[8 * cb]));
             } else {            // U row t: a [32 t][32 v] f32 tile, 16-byte pieces 128B-swizzled
                 unsigned char* tile = sm.ktv[0] + (col0 - 128) * 128;   // 1024-byte aligned
@@ -361,11 +374,10 @@ __device__ __forceinline__ bool intra_mma_tail(IntraSmem& sm, int* err, unsigned
                         make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
             }
         } else if (col0 < 128) {   // W row t, channels col0 .. : QW image rows 32 + t
-            unsigned char* qwh = blk + kOffQW;
-            unsigned char* qwl = blk + kOffQW + kQWBytes;
+            unsigned char* qw = blk + kOffQW;
 #pragma unroll
             for (int cb = 0; cb < CW / 8; ++cb)
-                put8x(qwh, qwl, tc_offset(kCc + t, col0 + 8 * cb, kSbo128),
+                put8h(qw, tc_offset(kCc + t, col0 + 8 * cb, kSbo128),
                       *reinterpret_cast<const float(*)[8]>(&x[8 * cb]));
         } else {            // U row t, values col0 - 128 .. : f32 [32 t][128 v]
             float4* ut = reinterpret_cast<float4*>(blk + kOffUT) + t * 32 + (col0 - 128) / 4;
@@ -377,10 +389,9 @@ done:
     tc_fence_before();
     if (PRE_A) fence_proxy_async_smem();
     ok = __syncthreads_or(!ok) == 0;
-    if (PRE_A && ok && tid == 0) {   // W: QW rows 32..63 (hi, lo); U: four [32 t][32 v] tiles
+    if (PRE_A && ok && tid == 0) {   // W: QW rows 32..63; U: four [32 t][32 v] tiles
         constexpr uint32_t kW = kCc * kSbo128 / 8;   // 8 KB: 4 groups of 8 rows
         bulk_store(blk + kOffQW + kW, sm.ktv[1], kW);
-        bulk_store(blk + kOffQW + kQWBytes + kW, sm.ktv[1] + kW, kW);
 #pragma unroll
         for (int j = 0; j < 4; ++j) tma_store_3d(umap, sm.ktv[0] + 4096 * j, 32 * j, 0, ublock);
         bulk_commit();

@@ -696,7 +696,7 @@ kda_chunk_prep_intra_kernel(PrepArgs p, ScanArgs a, const int* chunk_off, unsign
             put8x(sm.kb[0], sm.kb[1], tc_offset(t, k0, kSbo128), xb);
             put8x(sm.bia[0], sm.bia[1], tc_offset(t, k0, kSbo128), xk);
             put8x(sm.bia[0], sm.bia[1], tc_offset(kCc + t, k0, kSbo128), xq);
-            put8x(blk + kOffQW, blk + kOffQW + kQWBytes, tc_offset(t, k0, kSbo128), xg);
+            put8h(blk + kOffQW, tc_offset(t, k0, kSbo128), xg);
         }
     }
     // ---- MMA-a on the row images ---------------------------------------------------------------
@@ -729,15 +729,15 @@ kda_chunk_prep_intra_kernel(PrepArgs p, ScanArgs a, const int* chunk_off, unsign
             }
             put4x(sm.ktv[0], sm.ktv[1], tc_offset(kq + e, t0, kSboKt), xt);
             put4x(sm.ktv[0], sm.ktv[1], tc_offset(128 + kq + e, t0, kSboKt), xv);
-            put4x(b2s, b2s + kB2KBytes, tc_offset(kq + e, t0, kSbo32), xc);
+            *reinterpret_cast<uint2*>(b2s + tc_offset(kq + e, t0, kSbo32)) =
+                make_uint2(f16x2_rn(xc[0], xc[1]), f16x2_rn(xc[2], xc[3]));
         }
     }
-    // the first 128 rows of the B2 images (K e^{G_C-G}, hi and lo) leave in two bulk copies
+    // the first 128 rows of the B2 image (K e^{G_C-G}, f16) leave in one bulk copy
     fence_proxy_async_smem();
     __syncthreads();
     if (tid == 0) {
         bulk_store(blk + kOffB2, b2s, kB2KBytes);
-        bulk_store(blk + kOffB2 + kB2Bytes, b2s + kB2KBytes, kB2KBytes);
         bulk_commit();
     }
 

@@ -139,7 +139,7 @@ cudaError_t launch_ring_roll(const PrepArgs& a, cudaStream_t s);
 constexpr size_t kStaticScratchBytes = (size_t)32 << 20;
 cudaError_t static_scratch(void** ptr);
 constexpr int kChunkTokens = 32;        // tokens per chunk of the chunked scan
-constexpr size_t kChunkBlockBytes = 70144;  // workspace bytes per (chunk, head)
+constexpr size_t kChunkBlockBytes = 43520;  // workspace bytes per (chunk, head)
 
 // 2-D f32 tensor map over [rows, cols] (row stride = cols), box [box_rows, box_cols], no swizzle.
 bool make_tensor_map_2d(CUtensorMap* m, const float* base, long rows, long cols, int box_cols,

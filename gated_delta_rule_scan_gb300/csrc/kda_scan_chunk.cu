@@ -184,7 +184,7 @@ kda_chunk_intra_kernel(ScanArgs a, const int* chunk_off, unsigned char* ws) {
             }
             put8x(sm.ktv[0], sm.ktv[1], tc_offset(tid, 8 * j, kSboKt), xt);
             put8x(sm.ktv[0], sm.ktv[1], tc_offset(128 + tid, 8 * j, kSboKt), xv);
-            put8x(blk + kOffB2, blk + kOffB2 + kB2Bytes, tc_offset(tid, 8 * j, kSbo32), xc);
+            put8h(blk + kOffB2, tc_offset(tid, 8 * j, kSbo32), xc);
         }
     }
     if (GATE_MODE == 1) __syncthreads();          // gsc
@@ -238,7 +238,7 @@ kda_chunk_intra_kernel(ScanArgs a, const int* chunk_off, unsigned char* ws) {
         put8x(sm.kb[0], sm.kb[1], tc_offset(t, k0, kSbo128), xb);
         put8x(sm.bia[0], sm.bia[1], tc_offset(t, k0, kSbo128), xk);
         put8x(sm.bia[0], sm.bia[1], tc_offset(kCc + t, k0, kSbo128), xq);
-        put8x(blk + kOffQW, blk + kOffQW + kQWBytes, tc_offset(t, k0, kSbo128), xg);
+        put8h(blk + kOffQW, tc_offset(t, k0, kSbo128), xg);
     }
     uint32_t phase = 0;
     intra_mma_tail<GATE_MODE, kThr>(sm, a.err, blk, phase);
@@ -265,52 +265,42 @@ constexpr uint32_t kTA2 = 128;    // U'^T hi (16) then lo (16)
 constexpr uint32_t kTD1 = 160;    // [O1^T | X^T]  64
 constexpr uint32_t kTD2 = 224;    // [dS^T | O2^T] 160
 
-// write NV f32 values (NV multiple of 32) as packed bf16 hi words at col_hi and lo words at col_lo
-template <int NV>
-__device__ __forceinline__ void tmem_put_split(uint32_t col_hi, uint32_t col_lo, const float* v) {
-#pragma unroll
-    for (int b = 0; b < NV / 32; ++b) {
-        float hw[16], lw[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            uint32_t hu, lu;
-            split_bf16x2(v[32 * b + 2 * i], v[32 * b + 2 * i + 1], hu, lu);
-            hw[i] = __uint_as_float(hu);
-            lw[i] = __uint_as_float(lu);
-        }
-        tmem_st16(col_hi + 16 * b, hw);
-        tmem_st16(col_lo + 16 * b, lw);
-    }
-}
-
-// write 16 f32 values as 8 packed bf16 hi words at col_hi and 8 lo words at col_lo
-__device__ __forceinline__ void tmem_put_split16(uint32_t col_hi, uint32_t col_lo, const float* v) {
-    uint32_t hw[8], lw[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) split_bf16x2(v[2 * i], v[2 * i + 1], hw[i], lw[i]);
-    tmem_st8(col_hi, hw);
-    tmem_st8(col_lo, lw);
-}
-
-// the same for NV = 4, 8, 16 or a multiple of 32 values
+// Write NV f32 values (NV = 4, 8, 16 or a multiple of 32) as packed f16 hi words at col_hi and
+// lo words at col_lo: the inter kernel's A operands (the state S^T, U'^T) in TMEM.
 template <int NV>
 __device__ __forceinline__ void tmem_put_split_n(uint32_t col_hi, uint32_t col_lo, const float* v) {
     if constexpr (NV == 4) {
         uint32_t hw[2], lw[2];
-        split_bf16x2(v[0], v[1], hw[0], lw[0]);
-        split_bf16x2(v[2], v[3], hw[1], lw[1]);
+        split_f16x2(v[0], v[1], hw[0], lw[0]);
+        split_f16x2(v[2], v[3], hw[1], lw[1]);
         tmem_st2(col_hi, hw);
         tmem_st2(col_lo, lw);
     } else if constexpr (NV == 8) {
         uint32_t hw[4], lw[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) split_bf16x2(v[2 * i], v[2 * i + 1], hw[i], lw[i]);
+        for (int i = 0; i < 4; ++i) split_f16x2(v[2 * i], v[2 * i + 1], hw[i], lw[i]);
         tmem_st4(col_hi, hw);
         tmem_st4(col_lo, lw);
     } else if constexpr (NV == 16) {
-        tmem_put_split16(col_hi, col_lo, v);
+        uint32_t hw[8], lw[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) split_f16x2(v[2 * i], v[2 * i + 1], hw[i], lw[i]);
+        tmem_st8(col_hi, hw);
+        tmem_st8(col_lo, lw);
     } else {
-        tmem_put_split<NV>(col_hi, col_lo, v);
+#pragma unroll
+        for (int b = 0; b < NV / 32; ++b) {
+            float hw[16], lw[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                uint32_t hu, lu;
+                split_f16x2(v[32 * b + 2 * i], v[32 * b + 2 * i + 1], hu, lu);
+                hw[i] = __uint_as_float(hu);
+                lw[i] = __uint_as_float(lu);
+            }
+            tmem_st16(col_hi + 16 * b, hw);
+            tmem_st16(col_lo + 16 * b, lw);
+        }
     }
 }
 
@@ -397,25 +387,23 @@ kda_chunk_inter_kernel(ScanArgs a, const int* chunk_off, const unsigned char* ws
     auto issue = [&](int c, int st) {
         const unsigned char* src = ws + ((gbase + c) * H + h) * (long)kBlkBytes;
         mbar_arrive_expect_tx(&sm.bar_ld[st], kBlkBytes);
-        bulk_load(&sm.blk[st][kOffQW], src + kOffQW, 2 * kQWBytes, &sm.bar_ld[st]);
-        bulk_load(&sm.blk[st][kOffB2], src + kOffB2, 2 * kB2Bytes, &sm.bar_ld[st]);
+        bulk_load(&sm.blk[st][kOffQW], src + kOffQW, kQWBytes, &sm.bar_ld[st]);
+        bulk_load(&sm.blk[st][kOffB2], src + kOffB2, kB2Bytes, &sm.bar_ld[st]);
         bulk_load(&sm.blk[st][kOffUT], src + kOffUT, kUTBytes + kEGBytes, &sm.bar_ld[st]);
     };
-    const uint32_t id1 = tc_idesc_bf16(128, 2 * kCc), id2 = tc_idesc_bf16(128, 160);
+    const uint32_t id1 = tc_idesc_f16(128, 2 * kCc), id2 = tc_idesc_f16(128, 160);
     // MMA-1: [O1^T | X^T] = S^T (Q e^G | W)^T for the chunk in stage st, K-steps ks0 .. ks0+3
-    // (keys 16 ks0 ..), bf16x3 per K-step; the first product of K-step 0 starts the sum.  (One
-    // N = 64 group: the tensor pipe's cost here follows the instruction count, so two N = 32
-    // groups are slower.)
+    // (keys 16 ks0 ..), S^T as f16 hi + lo against the f16 image per K-step; the first product of
+    // K-step 0 starts the sum.  (One N = 64 group: the tensor pipe's cost here follows the
+    // instruction count, so two N = 32 groups are slower.)
     auto mma1_half = [&](int st, int ks0) {
         const unsigned char* B = sm.blk[st];
-        const uint64_t bh = tc_smem_desc(smem_u32(B + kOffQW), 128, kSbo128);
-        const uint64_t bl = tc_smem_desc(smem_u32(B + kOffQW + kQWBytes), 128, kSbo128);
+        const uint64_t bq = tc_smem_desc(smem_u32(B + kOffQW), 128, kSbo128);
 #pragma unroll
         for (int ks = ks0; ks < ks0 + 4; ++ks) {
             const uint32_t ah = tbase + kTA1 + 8 * ks, al = tbase + kTA1 + 64 + 8 * ks;
-            tc_mma_ts(tbase + kTD1, ah, tc_desc_advance(bh, 256 * ks), id1, ks > 0);
-            tc_mma_ts(tbase + kTD1, ah, tc_desc_advance(bl, 256 * ks), id1, true);
-            tc_mma_ts(tbase + kTD1, al, tc_desc_advance(bh, 256 * ks), id1, true);
+            tc_mma_ts(tbase + kTD1, ah, tc_desc_advance(bq, 256 * ks), id1, ks > 0);
+            tc_mma_ts(tbase + kTD1, al, tc_desc_advance(bq, 256 * ks), id1, true);
         }
     };
     auto mma1 = [&](int st) {
@@ -509,9 +497,8 @@ kda_chunk_inter_kernel(ScanArgs a, const int* chunk_off, const unsigned char* ws
         tc_fence_after();
         // MMA-2: [dS^T | O2^T] = U'^T (K e^{G_C-G} | Aqk)
         if (tid == 0) {
-            mma3_ts(tbase + kTD2, tbase + kTA2, tbase + kTA2 + 16,
-                    tc_smem_desc(smem_u32(B + kOffB2), 128, kSbo32),
-                    tc_smem_desc(smem_u32(B + kOffB2 + kB2Bytes), 128, kSbo32), 2, id2);
+            mma2_ts(tbase + kTD2, tbase + kTA2, tbase + kTA2 + 16,
+                    tc_smem_desc(smem_u32(B + kOffB2), 128, kSbo32), 2, id2);
             tc_commit(&sm.bar_mma);
         }
         // every thread observes MMA-2's completion itself (no barrier needed for the TMEM reads

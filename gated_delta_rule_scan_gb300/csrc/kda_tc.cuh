@@ -80,6 +80,13 @@ __device__ __forceinline__ uint64_t tc_smem_desc_sw128(uint32_t smem_addr) {
     return d;
 }
 
+// Instruction descriptor, kind::f16: f16 A and B, f32 accumulator, both K-major, dense.
+__host__ __device__ constexpr uint32_t tc_idesc_f16(int M, int N) {
+    return (1u << 4)                    // D format: f32 (A and B format fields 0: f16)
+           | ((uint32_t)(N >> 3) << 17) // N / 8
+           | ((uint32_t)(M >> 4) << 24); // M / 16
+}
+
 // Instruction descriptor, kind::f16: bf16 A and B, f32 accumulator, both K-major, dense.
 __host__ __device__ constexpr uint32_t tc_idesc_bf16(int M, int N) {
     return (1u << 4)                    // D format: f32
@@ -196,6 +203,21 @@ __device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t& hi, u
     const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
     const float2 hf = __bfloat1622float2(h);
     const __nv_bfloat162 l = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
+    hi = *reinterpret_cast<const uint32_t*>(&h);
+    lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+
+// Two values as an f16x2 word (round to nearest), and as f16 hi + f16 lo words with hi + lo == x
+// to ~22 significant bits (lo is subnormal below 2^-14 * 2^11 of x's scale; the product error of
+// such small entries stays below the result's rounding).
+__device__ __forceinline__ uint32_t f16x2_rn(float x0, float x1) {
+    const __half2 h = __floats2half2_rn(x0, x1);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+__device__ __forceinline__ void split_f16x2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+    const __half2 h = __floats2half2_rn(x0, x1);
+    const float2 hf = __half22float2(h);
+    const __half2 l = __floats2half2_rn(x0 - hf.x, x1 - hf.y);
     hi = *reinterpret_cast<const uint32_t*>(&h);
     lo = *reinterpret_cast<const uint32_t*>(&l);
 }

@@ -257,6 +257,13 @@ def kda_scan_workspace_bytes(N, total_T, H, gate_mode=0, algo=ALGO_AUTO, D=HEAD_
     return int(_lib.kda_scan_workspace_bytes(N, total_T, H, D, gate_mode, algo))
 
 
+def chunk_block_bytes() -> int:
+    """Workspace bytes of one (32-token chunk, head) block of the chunked form: a one-head,
+    one-chunk varlen problem is sized for two blocks (a sequence may straddle one more chunk) plus
+    the 256-byte header of chunk offsets."""
+    return (kda_scan_workspace_bytes(1, 32, 1, algo=ALGO_CHUNK) - 256) // 2
+
+
 def scan_workspace(N, total_T, H, device, algo=ALGO_AUTO):
     """A device byte buffer large enough for kda_scan / kda_scan_varlen (None when none is
     needed)."""

@@ -147,7 +147,7 @@ int kda_conv_l2norm_prep_varlen(const void* q_raw, const void* k_raw, const void
 /*
  * Workspace bytes that suffice for kda_scan / kda_scan_varlen over N sequences holding total_T
  * tokens in all (an upper bound for any split of total_T into N lengths): 0 for KDA_ALGO_SEQ,
- * else the chunked form's scratch, about 2.1 KB per (token, head).  Returns 0 for invalid
+ * else the chunked form's scratch, about 1.4 KB per (token, head).  Returns 0 for invalid
  * arguments.
  */
 size_t kda_scan_workspace_bytes(int N, int total_T, int H, int D, int gate_mode, int algo);
@@ -174,7 +174,12 @@ size_t kda_scan_workspace_bytes(int N, int total_T, int H, int D, int gate_mode,
  *                      form on the tensor cores (module doc's chunked twin); needs workspace;
  *                      for the per-channel gate every 32-token chunk's total log-decay must stay
  *                      above -170 per channel (a bounded gate such as KDA's >= -5 per token
- *                      satisfies it), otherwise kda_device_status reports 40008.
+ *                      satisfies it), otherwise kda_device_status reports 40008.  Precision: the
+ *                      intra-chunk products are bf16 x 3 (about 16 significant bits); the state
+ *                      chain pairs the state and U' = U - W S, split into f16 hi + lo, with f16
+ *                      images of its other operands (about 11 bits), so results carry a
+ *                      relative error of a few 1e-4 of their scale (inside the 1e-3 parity
+ *                      bound), and state and U' entries must stay below 65504 in magnitude.
  *                      KDA_ALGO_AUTO takes the chunked form when a large-enough workspace is given
  *                      and the longest sequence has at least 128 tokens (64 when N * H >= 512),
  *                      else the sequential one: the measured crossover on GB300.
@@ -230,8 +235,8 @@ int kda_scan_varlen_gqa(const float* q_hat, const float* k_hat, const float* v_h
  * Arguments, layouts, results and errors as in kda_scan_varlen (algo and workspace are implied).
  * The results equal kda_scan_varlen with KDA_ALGO_CHUNK bit for bit.
  * Size limit: the problem's chunked scratch -- kda_scan_workspace_bytes for its exact lengths,
- * a 256-byte header plus 70,144 bytes per (32-token chunk, head), about
- * H * sum_n ceil(len_n / 32) <= 478 -- must fit KDA_STATIC_SCRATCH_BYTES; a larger problem
+ * a 256-byte header plus 43,520 bytes per (32-token chunk, head), about
+ * H * sum_n ceil(len_n / 32) <= 771 -- must fit KDA_STATIC_SCRATCH_BYTES; a larger problem
  * returns 40011 and launches nothing.
  * Setup: the first call on each device looks up the array's address once, with that device
  * current (a failure returns 10000 + its cudaError_t); the stream must belong to that device

@@ -142,7 +142,8 @@ def test_static_scan_contract(kda):
     exceeds KDA_STATIC_SCRATCH_BYTES, besides kda_scan_varlen's own contract."""
     lib = kda.library()
     a = [FAKE] * 4 + [0, FAKE, FAKE, FAKE * 8, FAKE]
-    per_block = 70144
+    per_block = kda.chunk_block_bytes()
+    assert per_block == 43520
     cap_blocks = (kda.STATIC_SCRATCH_BYTES - 256) // per_block
 
     def call(cu, H, D=128):

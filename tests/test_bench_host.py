@@ -1,7 +1,7 @@
 """Host checks of the benchmark's bookkeeping (no GPU): the method bytes behind each roofline
 fraction equal the per-unit figures of the prefill workload worked out by hand (T = 4096 tokens,
 H = 64 heads, D = 128, conv K = 4), the library's intermediate traffic (128 chunks of 32 tokens,
-70,144-byte workspace blocks) is counted apart from them, and every kernel the benchmark reports
+43,520-byte workspace blocks) is counted apart from them, and every kernel the benchmark reports
 has its source list on disk."""
 
 import importlib.util
@@ -44,12 +44,12 @@ def test_prefill_method_bytes(bench):
 
 
 def test_prefill_impl_bytes(bench):
-    """The library's own intermediates, reported apart: the chunk workspace (one 70,144-byte
+    """The library's own intermediates, reported apart: the chunk workspace (one 43,520-byte
     block per (32-token chunk, head)) and the readout plane o."""
-    ib = bench._impl_bytes(4096, 64, 70144, 128)
-    blocks = 128 * 64 * 70144
+    ib = bench._impl_bytes(4096, 64, 43520, 128)
+    blocks = 128 * 64 * 43520
     plane = 4096 * 8192 * 4
-    assert blocks == 574_619_648
+    assert blocks == 356_515_840
     assert ib["kda_chunk_prep_intra_kernel"] == blocks
     assert ib["kda_chunk_inter_kernel"] == blocks + plane
     assert ib["kda_gated_rmsnorm_kernel"] == plane

@@ -85,7 +85,7 @@ def test_static_scratch_equals_workspace_path():
 
 def test_static_scratch_limit():
     dev = torch.device("cuda:0")
-    over = kda.STATIC_SCRATCH_BYTES // 70144 + 1      # one (chunk, head) block past the limit
+    over = kda.STATIC_SCRATCH_BYTES // kda.chunk_block_bytes() + 1   # one block past the limit
     c = _case(23, [32 * over], 1, kda.GATE_PER_CHANNEL, dev)
     with pytest.raises(kda.KdaError) as err:
         _static(c)
@@ -99,7 +99,7 @@ def test_static_scratch_exactly_at_limit():
     workspace path bit for bit (an off-by-one in the size check, or a write past the array's end,
     would show here)."""
     dev = torch.device("cuda:0")
-    cap_blocks = (kda.STATIC_SCRATCH_BYTES - 256) // 70144
+    cap_blocks = (kda.STATIC_SCRATCH_BYTES - 256) // kda.chunk_block_bytes()
     c = _case(24, [32 * cap_blocks - 5], 1, kda.GATE_PER_CHANNEL, dev)
     _static(c)
     kda.kda_scan_varlen(c["q"], c["k"], c["v"], c["g"], c["beta"], c["s0"], c["s_ws"], c["o_ws"],
