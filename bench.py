@@ -269,8 +269,9 @@ def _impl_bytes(T, H, blk_bytes, chunks, K=4):
 
 def _chunk_flops(T, H):
     """Products the chunked form's tensor cores compute per launch (one pass, i.e. before the
-    bf16 x3 split that triples the MMA instructions), for 32-token chunks: intra = A and Aqk
-    ([K;Q] (64 x 128) times K^T) plus [W | U] = Tm times [beta K e^G | beta V] (32 x 32 x 256);
+    operand splits: bf16 x3 in the intra-chunk products, f16 x2 in the state chain's), for
+    32-token chunks: intra = A and Aqk ([K;Q] (64 x 128) times K^T) plus [W | U] = Tm times
+    [beta K e^G | beta V] (32 x 32 x 256);
     inter = MMA-1 (S^T, 128 x 128, times 64 rows) plus MMA-2 (U'^T, 128 x 32, times 160 rows)."""
     chunks_h = (T + 31) // 32 * H
     intra = 2 * 64 * 128 * 32 + 2 * 32 * 32 * 256
@@ -703,8 +704,9 @@ def run_ours(args):
         "metric": METRIC, "value": tokens_per_s, "unit": "tokens/s", "n_gpus": ws,
         "steps": K, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
-        "dtype": ("f32 state and elementwise; tensor-core products bf16 x3 "
-                  "(hi*hi + hi*lo + lo*hi, f32 accumulate); bf16 raw q/k/v" if fused
+        "dtype": ("f32 state and elementwise; tensor-core products with f32 accumulate: "
+                  "intra-chunk bf16 x3 (hi*hi + hi*lo + lo*hi), state chain f16 x2 (state and "
+                  "U' split f16 hi + lo against single f16 images); bf16 raw q/k/v" if fused
                   else "f32 (FP32 FMA scan); bf16 raw q/k/v"),
         "data": "synthetic (seeded numpy default_rng; bf16 raw q/k/v, f32 gates, state, norm)",
         "config": {"workload": f"prefill: 1 sequence x 4096 tokens, H={H}, head_dim=128, conv K=4,"
