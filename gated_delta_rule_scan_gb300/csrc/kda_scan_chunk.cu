@@ -476,20 +476,22 @@ kda_chunk_inter_kernel(ScanArgs a, const int* chunk_off, const unsigned char* ws
         tc_fence_after();
         if (__syncthreads_or(!ok || late_fail)) { failed = true; break; }
         if (ostore_lane && c > 0) flush_o(c - 1);   // its o rows were written before the barrier
-        // O1 and X for tokens TPT qf ..; O1 waits in the output tile; U' = U - X into TMEM as
-        // MMA-2's A operand
+        // O1 and X for tokens TPT qf ..; O1 stays in registers until the chunk's o rows are
+        // formed; U' = U - X into TMEM as MMA-2's A operand.  (The U rows are read from shared
+        // memory before the TMEM wait, which orders every memory access after it.)
         float* ot = &sm.otile[c % 3][TPT * qf][v];
+        float o1[TPT];
         {
-            float x[TPT], o1[TPT];
+            const float* ut = reinterpret_cast<const float*>(B + kOffUT) + (TPT * qf) * 128 + v;
+            float up[TPT];
+#pragma unroll
+            for (int t = 0; t < TPT; ++t) up[t] = ut[t * 128];
+            float x[TPT];
             tmem_ld_n<TPT>(tl + kTD1 + TPT * qf, o1);
             tmem_ld_n<TPT>(tl + kTD1 + 32 + TPT * qf, x);
             tmem_ld_wait();
 #pragma unroll
-            for (int t = 0; t < TPT; ++t) ot[t * 128] = o1[t];
-            const float* ut = reinterpret_cast<const float*>(B + kOffUT) + (TPT * qf) * 128 + v;
-            float up[TPT];
-#pragma unroll
-            for (int t = 0; t < TPT; ++t) up[t] = ut[t * 128] - x[t];
+            for (int t = 0; t < TPT; ++t) up[t] -= x[t];
             tmem_put_split_n<TPT>(tl + kTA2 + TPT / 2 * qf, tl + kTA2 + 16 + TPT / 2 * qf, up);
             tmem_st_wait();
         }
@@ -550,11 +552,8 @@ kda_chunk_inter_kernel(ScanArgs a, const int* chunk_off, const unsigned char* ws
         }
         if (tid == 32 && c + kInterStages < nch) issue(c + kInterStages, st);
         // the chunk's o rows into the staging tile while the next MMA-1 runs
-        float ov[TPT];
 #pragma unroll
-        for (int t = 0; t < TPT; ++t) ov[t] = __fmul_rn(scale, ot[t * 128] + o2[t]);
-#pragma unroll
-        for (int t = 0; t < TPT; ++t) ot[t * 128] = ov[t];
+        for (int t = 0; t < TPT; ++t) ot[t * 128] = __fmul_rn(scale, o1[t] + o2[t]);
         fence_proxy_async_smem();
     }
     failed = __syncthreads_or(failed || late_fail) != 0;
