@@ -103,7 +103,7 @@ __device__ __forceinline__ void plane_load(PlaneRaw<BF16, KW>& P, const void* ra
 // conv + SiLU of one plane for the warp's 4 tokens (or the raw samples without a conv).
 template <bool BF16, bool CONV, int KW>
 __device__ __forceinline__ void plane_conv(const PlaneRaw<BF16, KW>& P, const float (&w)[4][KW],
-                                           int K, float (&y)[kTokW][4]) {
+                                           float (&y)[kTokW][4]) {
     float4 cur[kTokW];
 #pragma unroll
     for (int i = 0; i < kTokW; ++i) cur[i] = raw_unpack<BF16>(P.cur[i]);
@@ -118,7 +118,13 @@ __device__ __forceinline__ void plane_conv(const PlaneRaw<BF16, KW>& P, const fl
                     const int idx = i + m;            // window slot m = sample at token i-(KW-1)+m
                     win[m] = idx < KW - 1 ? f4c(P.halo[idx], e) : f4c(cur[idx - (KW - 1)], e);
                 }
-                y[i][e] = silu_f(conv_taps_f(w[e], win, K));
+                // a K-tap conv (K < KW) meets zero weights and zero samples in its first KW - K
+                // slots, so every slot runs unpredicated, adding exact zeros: the same sum as the
+                // prep kernel's K taps, without a per-tap test
+                float acc = 0.0f;
+#pragma unroll
+                for (int m = 0; m < KW; ++m) acc = fmaf(w[e][m], win[m], acc);
+                y[i][e] = silu_f(acc);
             } else {
                 y[i][e] = f4c(cur[i], e);
             }
@@ -126,14 +132,13 @@ __device__ __forceinline__ void plane_conv(const PlaneRaw<BF16, KW>& P, const fl
     }
 }
 
-// The staged (transposed) weights of channels kq .. kq+3: one 16-byte load per tap.
+// The staged (transposed) weights of channels kq .. kq+3: one 16-byte load per tap slot (tap j of
+// a K-tap conv sits in slot j + KW - K, the slots before it hold zeros).
 template <int KW>
-__device__ __forceinline__ void plane_weights_t(const float* wt, int kq, int K, float (&w)[4][KW]) {
+__device__ __forceinline__ void plane_weights_t(const float* wt, int kq, float (&w)[4][KW]) {
 #pragma unroll
     for (int m = 0; m < KW; ++m) {
-        const int j = m - (KW - K);
-        const float4 x = j >= 0 ? *reinterpret_cast<const float4*>(wt + j * kHeadDim + kq)
-                                : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        const float4 x = *reinterpret_cast<const float4*>(wt + m * kHeadDim + kq);
         w[0][m] = x.x; w[1][m] = x.y; w[2][m] = x.z; w[3][m] = x.w;
     }
 }
@@ -293,7 +298,8 @@ __device__ __forceinline__ void cp_async4(void* dst, const void* src) {
 }
 
 // Staged small inputs of one task: the head's conv weights (K <= 4 taps, transposed to
-// [plane][tap][channel] so a lane reads its 4 channels' tap as one conflict-free 16-byte load),
+// [plane][tap slot][channel] so a lane reads its 4 channels' tap as one conflict-free 16-byte load;
+// tap j in slot j + 4 - K, the leading slots zeroed once per CTA),
 // dt_bias (KDA: the head's 128 channels; GDN: one value), A_log of the head, and the chunk's raw
 // beta and (GDN) gate inputs.  Filled during the previous task's MMA tail, so that the front half
 // waits on no global load; a region of its own, read only by the front half.
@@ -329,7 +335,7 @@ static_assert(2 * (kPrepIntraSmemBytes + 1024) <= 228 * 1024, "two CTAs per SM")
 
 // Issue the cp.async copies of task tp's small inputs into the parameter stage (H units, Hg gate
 // heads).
-template <int GATE_MODE, bool CONV>
+template <int GATE_MODE, bool CONV, int KW>
 __device__ __forceinline__ void stage_params(ParamStage& ps, const PrepArgs& p, int H, int Hg,
                                              const TaskPos& tp) {
     const int tid = threadIdx.x, h = tp.h, gh = tp.gh, nt = tp.nt;
@@ -343,7 +349,7 @@ __device__ __forceinline__ void stage_params(ParamStage& ps, const PrepArgs& p, 
                 p.conv_w + (plane_offset(H, p.Hk, pl) + (long)(pl < 2 ? hq : h) * kHeadDim) * K;
             for (int r = tid; r < per; r += kThrF) {
                 const int ch = K == 4 ? r >> 2 : r / K, j = r - ch * K;
-                cp_async4(&ps.w[pl][j * kHeadDim + ch], src + r);
+                cp_async4(&ps.w[pl][(j + KW - K) * kHeadDim + ch], src + r);
             }
         }
     }
@@ -369,6 +375,12 @@ __device__ __forceinline__ void plane_from_stage(PlaneRaw<true, KW>& P, const Ra
 #pragma unroll
     for (int i = 0; i < kTokW; ++i)
         P.cur[i] = *reinterpret_cast<const uint2*>(&st.v[pl][t0 + i + KW - 1][kq]);
+    if (pos0 >= KW - 1 && R == KW - 1) {        // the whole window inside the sequence
+#pragma unroll
+        for (int m = 0; m < KW - 1; ++m)
+            P.halo[m] = raw_unpack<true>(*reinterpret_cast<const uint2*>(&st.v[pl][t0 + m][kq]));
+        return;
+    }
 #pragma unroll
     for (int m = 0; m < KW - 1; ++m) {
         const int d = KW - 1 - m;
@@ -433,6 +445,10 @@ kda_chunk_prep_intra_kernel(PrepArgs p, ScanArgs a, const int* chunk_off, unsign
     }
     uint32_t phase = 0, ph_ld = 0;               // MMA commits; staged loads (one per task)
     bool ld_pending = false;                     // a task's loads issued and not yet waited on
+    if constexpr (PW) {                          // leading weight slots of a conv shorter than KW
+        for (int i = tid; i < 3 * (KW - K) * kHeadDim; i += kThrF)
+            ps.w[i / ((KW - K) * kHeadDim)][i % ((KW - K) * kHeadDim)] = 0.0f;
+    }
     if (PF && (long)blockIdx.x < ntasks) {
         const TaskPos tp = task_pos(a.seq, chunk_off, blockIdx.x, nchunks, vs, Hk);
         if (tid == 0) {
@@ -442,7 +458,7 @@ kda_chunk_prep_intra_kernel(PrepArgs p, ScanArgs a, const int* chunk_off, unsign
             stage_raw<KW>(stage, maps, tp, &smf.bar_raw);
             if (GATE_MODE == 0) stage_f(sm.scr, maps, tp, &smf.bar_f);
         }
-        stage_params<GATE_MODE, PW>(ps, p, H, Hg, tp);
+        stage_params<GATE_MODE, PW, KW>(ps, p, H, Hg, tp);
     }
     __syncthreads();
 
@@ -511,17 +527,17 @@ kda_chunk_prep_intra_kernel(PrepArgs p, ScanArgs a, const int* chunk_off, unsign
                 PlaneRaw<true, KW> pr;
                 const long crow = pl * Cq + (pl < 2 ? cq4 : c4);   // conv / ring row of channel
                 plane_from_stage<KW>(pr, stage, pl, t0, kq, pos0, Rr, p.ring_in, rr + crow * R);
-                if constexpr (PW) plane_weights_t<KW>(ps.w[pl], kq, K, w);
+                if constexpr (PW) plane_weights_t<KW>(ps.w[pl], kq, w);
                 else if constexpr (CONV) plane_weights<KW>(p.conv_w, crow, K, w);
-                plane_conv<true, CONV, KW>(pr, w, K, pl == 2 ? v : (pl == 1 ? k : q));
+                plane_conv<true, CONV, KW>(pr, w, pl == 2 ? v : (pl == 1 ? k : q));
             }
         } else {
             if constexpr (CONV) plane_weights<KW>(p.conv_w, 2 * Cq + c4, K, w);
-            plane_conv<BF16, CONV, KW>(rv, w, K, v);
+            plane_conv<BF16, CONV, KW>(rv, w, v);
             if constexpr (CONV) plane_weights<KW>(p.conv_w, 1 * Cq + cq4, K, w);
-            plane_conv<BF16, CONV, KW>(rk, w, K, k);
+            plane_conv<BF16, CONV, KW>(rk, w, k);
             if constexpr (CONV) plane_weights<KW>(p.conv_w, 0 * Cq + cq4, K, w);
-            plane_conv<BF16, CONV, KW>(rq, w, K, q);
+            plane_conv<BF16, CONV, KW>(rq, w, q);
         }
     }
     {
@@ -747,7 +763,7 @@ kda_chunk_prep_intra_kernel(PrepArgs p, ScanArgs a, const int* chunk_off, unsign
             const TaskPos np = task_pos(a.seq, chunk_off, next, nchunks, vs, Hk);
             ld_pending = true;
             if (tid == 0) stage_raw<KW>(stage, maps, np, &smf.bar_raw);
-            stage_params<GATE_MODE, PW>(ps, p, H, Hg, np);
+            stage_params<GATE_MODE, PW, KW>(ps, p, H, Hg, np);
         }
     }, [&]() {
         if (PF && GATE_MODE == 0 && next < ntasks && tid == 0)
