@@ -15,7 +15,9 @@
 // channels of one token) pair lane l with l^1 by shuffles.  The per-channel running sum of the
 // gate passes from warp to warp through shared memory in token order, the order of the chunked
 // scan's own intra kernel.  The output blocks therefore equal those of the prep kernel followed
-// by the intra kernel bit for bit.
+// by the intra kernel bit for bit in the rows of live tokens; the rows of tokens past a sequence's
+// end (zero beta and gates, so zero U' rows, and readout rows that are never stored) may differ,
+// and the results (readout, state, ring) are equal.
 #include <cstddef>
 #include <cstring>
 
@@ -497,6 +499,17 @@ kda_chunk_prep_intra_kernel(PrepArgs p, ScanArgs a, const int* chunk_off, unsign
         ph_ld ^= 1u;
         ld_pending = false;
         cp_async_wait_all();
+        if (nt < kCc && ld_ok) {
+            // a ragged chunk: its stage rows past the last token (the next sequence's rows, or
+            // zeros past the tensor) are cleared, so that whatever they held, every value computed
+            // for a token past the end stays finite (those tokens meet zero beta and zero gates)
+            constexpr int kPieces = kHeadDim / 4;        // 8-byte pieces of a stage row
+            const int dead = kCc - nt;
+            for (int i = tid; i < 3 * dead * kPieces; i += kThrF) {
+                const int pl = i / (dead * kPieces), r = (i / kPieces) % dead, c = i % kPieces;
+                *reinterpret_cast<uint2*>(&stage.v[pl][KW - 1 + nt + r][4 * c]) = make_uint2(0u, 0u);
+            }
+        }
         if (__syncthreads_or(!ld_ok)) break;     // every piece of the stage has landed
         if (tid < kCc) {
             const bool live = tid < nt;
@@ -504,11 +517,10 @@ kda_chunk_prep_intra_kernel(PrepArgs p, ScanArgs a, const int* chunk_off, unsign
             if (GATE_MODE == 1)
                 sm.gs[tid] = live ? gdn_gate_f(ps.fraw[tid], ps.dt[0], ps.alog) : 0.0f;
         }
-        if (GATE_MODE == 0) {
+        if (GATE_MODE == 0) {                    // (rows past the end: their gates are masked)
 #pragma unroll
             for (int i = 0; i < kTokW; ++i)
-                fr[i] = i < ntok ? *reinterpret_cast<const float4*>(&sm.scr[(t0 + i) * kHeadDim + kq])
-                                 : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                fr[i] = *reinterpret_cast<const float4*>(&sm.scr[(t0 + i) * kHeadDim + kq]);
         }
     } else {
         plane_load<BF16, CONV, KW>(rq, p.q_raw, Cq, cq4, begin, pos0, ntok, p.ring_in, rr + (0 * Cq + cq4) * R, R);
@@ -556,12 +568,12 @@ kda_chunk_prep_intra_kernel(PrepArgs p, ScanArgs a, const int* chunk_off, unsign
         for (int i = 0; i < kTokW; ++i) {
             const float iq = l2_inv_f(__shfl_sync(0xffffffffu, part, 4 * i), p.l2_eps);
             const float ik = l2_inv_f(__shfl_sync(0xffffffffu, part, 4 * (kTokW + i)), p.l2_eps);
-            const bool live = i < ntok;
+            // a token past the sequence end keeps its (finite) values: its beta and gates are zero,
+            // so it adds nothing to A, W, U or the state, and its readout rows are never stored
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                q[i][e] = live ? q[i][e] * iq : 0.0f;
-                k[i][e] = live ? k[i][e] * ik : 0.0f;
-                v[i][e] = live ? v[i][e] : 0.0f;
+                q[i][e] *= iq;
+                k[i][e] *= ik;
             }
         }
     }
