@@ -64,6 +64,39 @@ def test_prefill_fused_varlen_edges():
     _check(gpu_prefill(inp, varlen=True), inp, varlen=True)
 
 
+@pytest.mark.parametrize("varlen", [False, True])
+def test_prefill_nonfinite_rows_after_a_ragged_chunk(varlen):
+    """A sequence's ragged last chunk is staged together with the rows that follow it (the next
+    sequence's); when those rows hold inf and NaN (the next sequence's own data), the first
+    sequence must not see them: its readout, state and ring equal the oracle's on it alone (and
+    stay finite) through the fused prefill, the staged chunked path and the sequential scan."""
+    import dataclasses
+    T, H = 45, 2
+    inp = inputs.make_inputs(74, H=H, N=2, T=T, raw_dtype="bf16", conv=True, ring="randn",
+                             state="randn", epilogue=True)
+    bad = slice(T, T + 19)                       # the rows that share the ragged chunk's tile
+    for name, val in (("q_raw", float("inf")), ("k_raw", float("nan")), ("v_raw", -float("inf")),
+                      ("f_raw", float("nan")), ("beta_raw", float("nan")),
+                      ("gate_raw", float("inf"))):
+        t = getattr(inp, name).clone()
+        t[bad] = val
+        setattr(inp, name, t)
+    first = dataclasses.replace(
+        inp, N=1, cu_seqlens=inp.cu_seqlens[:2].copy(),
+        **{k: getattr(inp, k)[:T] for k in ("q_raw", "k_raw", "v_raw", "f_raw", "beta_raw",
+                                            "gate_raw")},
+        ring_in=inp.ring_in[:1], state_in=inp.state_in[:1])
+    if varlen:
+        inp = dataclasses.replace(inp, cu_seqlens=np.array([0, T, 2 * T], dtype=np.int64))
+    runs = [gpu_prefill(inp, varlen=varlen)] + [gpu_forward(inp, varlen=varlen, algo=a)
+                                                for a in (1, 2)]
+    for out in runs:
+        mine = {"y": out["y"][:T], "state_out": out["state_out"][:1], "ring_out": out["ring_out"][:1]}
+        for k, v in mine.items():
+            assert torch.isfinite(v).all(), k
+        check_all_heads(mine, first, ("y", "state_out", "ring_out"))
+
+
 def test_prefill_fused_gdn():
     """The per-head (Gated DeltaNet) gate through the fused path."""
     inp = inputs.make_inputs(72, H=4, N=1, T=300, raw_dtype="f32", conv=True, ring="randn",
