@@ -467,15 +467,12 @@ kda_chunk_inter_kernel(ScanArgs a, const int* chunk_off, const unsigned char* ws
         const int st = c % kInterStages;
         const unsigned char* B = sm.blk[st];
         // the block landed before thread 0 issued this chunk's MMA-1; each thread still observes
-        // its barrier before reading it
+        // its barrier before reading it, and MMA-1's completion itself (no barrier here: a wait
+        // that gave up is agreed on at the U' barrier below)
         bool ok = mbar_wait_bounded(&sm.bar_ld[st], (uint32_t)((c / kInterStages) & 1), a.err);
-        if (ostore_lane) bulk_wait_read1();   // only the last o store may still read its tile:
-                                              // the one of chunk c-3 (tile c % 3) is free
         ok = ok && mbar_wait_bounded(&sm.bar_mma, mph, a.err);
         if (ok) mph ^= 1u;
         tc_fence_after();
-        if (__syncthreads_or(!ok || late_fail)) { failed = true; break; }
-        if (ostore_lane && c > 0) flush_o(c - 1);   // its o rows were written before the barrier
         // O1 and X for tokens TPT qf ..; O1 stays in registers until the chunk's o rows are
         // formed; U' = U - X into TMEM as MMA-2's A operand.  (The U rows are read from shared
         // memory before the TMEM wait, which orders every memory access after it.)
@@ -496,8 +493,13 @@ kda_chunk_inter_kernel(ScanArgs a, const int* chunk_off, const unsigned char* ws
             tmem_st_wait();
         }
         tc_fence_before();
-        __syncthreads();
+        if (__syncthreads_or(!ok || late_fail)) { failed = true; break; }
         tc_fence_after();
+        if (ostore_lane) {
+            if (c > 0) flush_o(c - 1);           // its o rows were written before the barrier
+            bulk_wait_read1();                   // only that store may still read its tile: the
+                                                 // one of chunk c-3 (tile c % 3) is free
+        }
         // MMA-2: [dS^T | O2^T] = U'^T (K e^{G_C-G} | Aqk)
         if (tid == 0) {
             mma2_ts(tbase + kTD2, tbase + kTA2, tbase + kTA2 + 16,
