@@ -82,6 +82,8 @@ __device__ __forceinline__ void plane_load(PlaneRaw<BF16, KW>& P, const void* ra
 #pragma unroll
     for (int i = 0; i < kTokW; ++i)
         P.cur[i] = i < ntok ? raw_ld<BF16>(raw, (begin + pos0 + i) * C + c4) : raw_zero<BF16>();
+#pragma unroll
+    for (int m = 0; m < KW - 1; ++m) P.halo[m] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
     if (CONV && ntok > 0) {                       // (a warp past the sequence end loads nothing)
 #pragma unroll
         for (int m = 0; m < KW - 1; ++m) {

@@ -97,6 +97,20 @@ def test_prefill_nonfinite_rows_after_a_ragged_chunk(varlen):
         check_all_heads(mine, first, ("y", "state_out", "ring_out"))
 
 
+@pytest.mark.parametrize("raw,gate_mode", [("f32", 1), ("f32", 0), ("bf16", 1)])
+def test_prefill_fused_repeatable(raw, gate_mode):
+    """Repeated fused prefills of a sequence whose last chunk holds 12 tokens (whole warps of the
+    chunk past the end) give the same bits every time, and the staged path's: the values computed
+    for tokens past the end are fixed zeros or finite, never left over from an earlier task."""
+    inp = inputs.make_inputs(75, H=4, N=1, T=300, raw_dtype=raw, conv=True, ring="randn",
+                             gate_mode=gate_mode, state="randn", epilogue=True)
+    unf = gpu_forward(inp, algo=2)
+    for _ in range(6):
+        fused = gpu_prefill(inp)
+        for k in ("y", "state_out", "ring_out"):
+            assert torch.equal(fused[k], unf[k]), k
+
+
 def test_prefill_fused_gdn():
     """The per-head (Gated DeltaNet) gate through the fused path."""
     inp = inputs.make_inputs(72, H=4, N=1, T=300, raw_dtype="f32", conv=True, ring="randn",
