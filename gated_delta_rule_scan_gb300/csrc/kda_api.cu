@@ -141,9 +141,9 @@ int prep_impl(const void* q_raw, const void* k_raw, const void* v_raw, int raw_d
 
 // AUTO takes the chunked form when the longest sequence has at least kAutoChunkMinLen tokens, or
 // at least kAutoChunkMinLenWide when there are kAutoWidePairs or more (sequence, head) pairs.
-// Measured on GB300 (H = 64): one sequence crosses over between 96 and 128 tokens, 16 or more
-// sequences between 48 and 64.
-constexpr long kAutoChunkMinLen = 128;
+// Measured on GB300 (H = 64): one sequence crosses over at about 96 tokens, 16 or more sequences
+// between 32 and 64 (the chunked form's margin below 64 is within the spread between boxes).
+constexpr long kAutoChunkMinLen = 96;
 constexpr long kAutoChunkMinLenWide = 64;
 constexpr long kAutoWidePairs = 512;
 

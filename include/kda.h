@@ -181,7 +181,7 @@ size_t kda_scan_workspace_bytes(int N, int total_T, int H, int D, int gate_mode,
  *                      relative error of a few 1e-4 of their scale (inside the 1e-3 parity
  *                      bound), and state and U' entries must stay below 65504 in magnitude.
  *                      KDA_ALGO_AUTO takes the chunked form when a large-enough workspace is given
- *                      and the longest sequence has at least 128 tokens (64 when N * H >= 512),
+ *                      and the longest sequence has at least 96 tokens (64 when N * H >= 512),
  *                      else the sequential one: the measured crossover on GB300.
  * workspace            device scratch [16B], at least kda_scan_workspace_bytes(...) bytes for
  *                      KDA_ALGO_CHUNK (40009 otherwise), or NULL.  Its contents are overwritten;
