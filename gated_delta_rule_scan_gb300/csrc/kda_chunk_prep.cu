@@ -776,11 +776,13 @@ kda_chunk_prep_intra_kernel(PrepArgs p, ScanArgs a, const int* chunk_off, unsign
         if (PF && next < ntasks) {
             const TaskPos np = task_pos(a.seq, chunk_off, next, nchunks, vs, Hk);
             ld_pending = true;
-            if (tid == 0) stage_raw<KW>(stage, maps, np, &smf.bar_raw);
+            // issued from warp 7, idle here, not from thread 0, whose warp extracts A next (a
+            // clock-stamped probe saw thread 0 spend ~2,900 cycles in this hook)
+            if (tid == kThrF - 32) stage_raw<KW>(stage, maps, np, &smf.bar_raw);
             stage_params<GATE_MODE, PW, KW>(ps, p, H, Hg, np);
         }
     }, [&]() {
-        if (PF && GATE_MODE == 0 && next < ntasks && tid == 0)
+        if (PF && GATE_MODE == 0 && next < ntasks && tid == kThrF - 32)
             stage_f(sm.scr, maps, task_pos(a.seq, chunk_off, next, nchunks, vs, Hk), &smf.bar_f);
     }, &maps.ut, (int)(gid * H + h));
     if (!ok) break;
