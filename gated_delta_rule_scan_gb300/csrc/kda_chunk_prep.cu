@@ -246,24 +246,23 @@ __device__ __forceinline__ void put4x(unsigned char* hi_img, unsigned char* lo_i
     *reinterpret_cast<uint2*>(lo_img + off) = lo;
 }
 
-// The 8-channel rows of this lane's half of the warp's tokens (even lane: tokens 0-1, odd lane:
-// tokens 2-3): own 4 channels plus the partner lane's 4, in channel order.  row[j] is token
-// j ^ sw of the half (sw is the same for both lanes of a pair), so that lanes with sw set write
-// their two rows in the other order and a 16-byte store of the warp touches four row slots of the
-// core matrices instead of two.
-__device__ __forceinline__ void pair_rows(const float (&x)[kTokW][4], float (&row)[2][8], bool sw) {
+// One 8-channel row of this lane's half of the warp's tokens (even lane: tokens 0-1, odd lane:
+// tokens 2-3): own 4 channels plus the partner lane's 4, in channel order.  Row j is token j ^ sw
+// of the half (sw is the same for both lanes of a pair), so that lanes with sw set write their two
+// rows in the other order and a 16-byte store of the warp touches four row slots of the core
+// matrices instead of two.  One row at a time: the row images then fit in 128 registers without
+// a spill (both rows at once spilled, and measured 2 % slower).
+__device__ __forceinline__ void pair_row(const float (&x)[kTokW][4], float (&row)[8], bool sw, int j) {
     const bool odd = (threadIdx.x & 1) != 0;
 #pragma unroll
-    for (int j = 0; j < 2; ++j)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const float lo_t = sw ? x[1 - j][e] : x[j][e];          // token j ^ sw
-            const float hi_t = sw ? x[3 - j][e] : x[2 + j][e];      // token 2 + (j ^ sw)
-            const float send = odd ? lo_t : hi_t;
-            const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
-            row[j][e] = odd ? recv : lo_t;
-            row[j][4 + e] = odd ? hi_t : recv;
-        }
+    for (int e = 0; e < 4; ++e) {
+        const float lo_t = sw ? x[1 - j][e] : x[j][e];          // token j ^ sw
+        const float hi_t = sw ? x[3 - j][e] : x[2 + j][e];      // token 2 + (j ^ sw)
+        const float send = odd ? lo_t : hi_t;
+        const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
+        row[e] = odd ? recv : lo_t;
+        row[4 + e] = odd ? hi_t : recv;
+    }
 }
 
 // Tensor maps of the raw rows: q, k [rows, Cq] and v [rows, C] bf16 with a [kRows, 128] box, and
@@ -669,13 +668,10 @@ kda_chunk_prep_intra_kernel(PrepArgs p, ScanArgs a, const int* chunk_off, unsign
     // ---- row images: tokens t0 + 2*(lane&1) + (j ^ sw), channels k0 .. k0+7 --------------------
     {
         const bool sw = ((lane >> 1) & 1) != 0;
-        float kr[2][8], qr[2][8];
-        pair_rows(k, kr, sw);
-        pair_rows(q, qr, sw);
         const int k0 = 8 * (lane >> 1);
         const int tb = t0 + 2 * (lane & 1);
         const int tj[2] = {tb + (sw ? 1 : 0), tb + (sw ? 0 : 1)};
-        float crv[8], ecv[8], gtv[2][8];
+        float crv[8], ecv[8];
         if (GATE_MODE == 0) {
             // channels k0 .. k0+7 = this lane pair's: the even lane's 4 then the odd lane's 4
             const bool odd = (lane & 1) != 0;
@@ -688,39 +684,35 @@ kda_chunk_prep_intra_kernel(PrepArgs p, ScanArgs a, const int* chunk_off, unsign
                 ecv[e] = odd ? oe : ecr_l[e];
                 ecv[4 + e] = odd ? ecr_l[e] : oe;
             }
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const float4 a0 = *reinterpret_cast<const float4*>(&sm.scr[tj[j] * 128 + k0]);
-                const float4 a1 = *reinterpret_cast<const float4*>(&sm.scr[tj[j] * 128 + k0 + 4]);
-                gtv[j][0] = a0.x; gtv[j][1] = a0.y; gtv[j][2] = a0.z; gtv[j][3] = a0.w;
-                gtv[j][4] = a1.x; gtv[j][5] = a1.y; gtv[j][6] = a1.z; gtv[j][7] = a1.w;
-            }
-        } else {
-#pragma unroll
-            for (int j = 0; j < 2; ++j) gtv[j][0] = sm.gsc[tj[j]];
         }
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
+        for (int j = 0; j < 2; ++j) {            // one token row at a time
             const int t = tj[j];
+            float kr[8], qr[8];
+            pair_row(k, kr, sw, j);
+            pair_row(q, qr, sw, j);
             float xb[8], xk[8], xq[8], xg[8];
             if (GATE_MODE == 0) {
+                const float4 a0 = *reinterpret_cast<const float4*>(&sm.scr[t * 128 + k0]);
+                const float4 a1 = *reinterpret_cast<const float4*>(&sm.scr[t * 128 + k0 + 4]);
+                const float gtv[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                    const float gt = gtv[j][e], cr = crv[e];
+                    const float gt = gtv[e], cr = crv[e];
                     const float ef = __expf(gt - cr), eb = __expf(cr - gt);
-                    xb[e] = kr[j][e] * eb;
-                    xk[e] = kr[j][e] * ef;
-                    xq[e] = qr[j][e] * ef;
-                    xg[e] = qr[j][e] * (ef * ecv[e]);
+                    xb[e] = kr[e] * eb;
+                    xk[e] = kr[e] * ef;
+                    xq[e] = qr[e] * ef;
+                    xg[e] = qr[e] * (ef * ecv[e]);
                 }
             } else {
-                const float eg = __expf(gtv[j][0]);
+                const float eg = __expf(sm.gsc[t]);
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                    xb[e] = kr[j][e];
-                    xk[e] = kr[j][e];
-                    xq[e] = qr[j][e];
-                    xg[e] = qr[j][e] * eg;
+                    xb[e] = kr[e];
+                    xk[e] = kr[e];
+                    xq[e] = qr[e];
+                    xg[e] = qr[e] * eg;
                 }
             }
             put8x(sm.kb[0], sm.kb[1], tc_offset(t, k0, kSbo128), xb);
