@@ -336,3 +336,33 @@ def test_contract_errors_on_device_pointers():
     assert lib.kda_scan(p(x), p(x), p(x), p(x), 0, p(b), s2.data_ptr() + 4, p(s), p(x), 1, 4, 1,
                         128, 1.0, 1, None, 0, None) == 40010
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("N,T,form", [(1, 95, "seq"), (1, 96, "chunk"), (4, 64, "seq"),
+                                      (8, 63, "seq"), (8, 64, "chunk")])
+def test_auto_form_follows_the_crossover(N, T, form):
+    """KDA_ALGO_AUTO with a workspace large enough for either form takes the chunked one from 96
+    tokens per sequence, or from 64 when sequences x heads >= 512 (H = 64), else the sequential
+    one: the kernels that ran (the library's kernel timer) show which."""
+    from gated_delta_rule_scan_gb300 import kda
+    H, D, dev = 64, 128, "cuda"
+    rows, C = N * T, H * D
+    gen = torch.Generator(device=dev).manual_seed(7)
+    unit = lambda: torch.nn.functional.normalize(  # noqa: E731
+        torch.randn(rows, H, D, device=dev, generator=gen), dim=-1).reshape(rows, C)
+    q, k = unit(), unit()
+    v = torch.randn(rows, C, device=dev, generator=gen)
+    g = -5.0 * torch.sigmoid(torch.randn(rows, C, device=dev, generator=gen))
+    beta = torch.sigmoid(torch.randn(rows, H, device=dev, generator=gen))
+    s0 = torch.zeros(N, H, D, D, device=dev)
+    s1, o = torch.empty_like(s0), torch.empty(rows, C, device=dev)
+    ws = kda.scan_workspace(N, rows, H, dev, algo=kda.ALGO_CHUNK)
+    kda.kernel_timing(True)
+    try:
+        kda.kda_scan(q, k, v, g, beta, s0, s1, o, N=N, T=T, H=H, algo=kda.ALGO_AUTO, workspace=ws)
+        torch.cuda.synchronize()
+        ran = kda.kernel_times()
+    finally:
+        kda.kernel_timing(False)
+    assert ("kda_chunk_inter_kernel" in ran) == (form == "chunk"), ran
+    assert ("kda_scan_seq_kernel" in ran) == (form == "seq"), ran
