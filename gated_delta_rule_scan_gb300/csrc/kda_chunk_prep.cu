@@ -608,23 +608,21 @@ kda_chunk_prep_intra_kernel(PrepArgs p, ScanArgs a, const int* chunk_off, unsign
         float* gtot = &smf.gtot[0][0];
         *reinterpret_cast<float4*>(&gtot[warp * kHeadDim + kq]) = make_float4(run[0], run[1], run[2], run[3]);
         __syncthreads();
-        float pre[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-        for (int w2 = 0; w2 < warp; ++w2) {
+        // one pass over the warps' totals in order from 0: the prefix before this warp (pre) and,
+        // in every warp from the same additions as warp 7's last token (so the same bits), the
+        // chunk total -- the reference c = G_C / 2 and e^c of this lane's channels, for the row
+        // images without another barrier
+        float pre[4] = {0.0f, 0.0f, 0.0f, 0.0f}, tot[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+        for (int w2 = 0; w2 < kThrF / 32; ++w2) {
             const float4 t4 = *reinterpret_cast<const float4*>(&gtot[w2 * kHeadDim + kq]);
-            pre[0] += t4.x; pre[1] += t4.y; pre[2] += t4.z; pre[3] += t4.w;
+            if (w2 == warp) { pre[0] = tot[0]; pre[1] = tot[1]; pre[2] = tot[2]; pre[3] = tot[3]; }
+            tot[0] += t4.x; tot[1] += t4.y; tot[2] += t4.z; tot[3] += t4.w;
         }
 #pragma unroll
         for (int i = 0; i < kTokW; ++i)
 #pragma unroll
             for (int e = 0; e < 4; ++e) G[i][e] = pre[e] + G[i][e];
-        // G over the whole chunk, in every warp from the same additions as warp 7's last token
-        // (so the same bits): the reference c = G_C / 2 and e^c of this lane's channels, for the
-        // row images without another barrier
-        float tot[4] = {pre[0], pre[1], pre[2], pre[3]};
-        for (int w2 = warp; w2 < kThrF / 32; ++w2) {
-            const float4 t4 = *reinterpret_cast<const float4*>(&gtot[w2 * kHeadDim + kq]);
-            tot[0] += t4.x; tot[1] += t4.y; tot[2] += t4.z; tot[3] += t4.w;
-        }
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             cref_l[e] = 0.5f * tot[e];
