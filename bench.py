@@ -214,10 +214,12 @@ def _traffic(kernel, files):
     return d.get("dram_bytes_per_launch")
 
 
-def _method_bytes(T, H, K=4):
+def _method_bytes(T, H, K=4, norm_folded=True):
     """The method's own HBM bytes per prefill step (T tokens, H heads, one sequence, conv K taps,
     bf16 raw q/k/v), split by the kernel that moves them: every input read once, every output
-    written once, no intermediate.  What the library writes and reads back between its own
+    written once, no intermediate.  norm_folded: the fused prefill's inter kernel writes y itself
+    (128-wide value heads), so z, the norm weight and y are its bytes; the RMSNorm kernel's entry
+    serves the staged path.  What the library writes and reads back between its own
     kernels (the chunk workspace, the readout plane o, the staged path's prepared planes) is
     implementation traffic, reported apart by _impl_bytes."""
     C = H * D
@@ -233,8 +235,8 @@ def _method_bytes(T, H, K=4):
     return {
         # fused path: raw q, k, v, f, beta, conv weights, ring in, gate parameters
         "kda_chunk_prep_intra_kernel": raw + plane + beta + conv + ring + small,
-        # state in and out, the rolled ring out
-        "kda_chunk_inter_kernel": 2 * state + ring,
+        # state in and out, the rolled ring out (and, folded, the RMSNorm's z and weight in, y out)
+        "kda_chunk_inter_kernel": 2 * state + ring + (norm + plane if norm_folded else 0),
         # z and the norm weight in, y out
         "kda_gated_rmsnorm_kernel": norm + plane,
         # staged path: prep reads what the fused prep reads and writes the ring; the scan moves
@@ -247,17 +249,18 @@ def _method_bytes(T, H, K=4):
     }
 
 
-def _impl_bytes(T, H, blk_bytes, chunks, K=4):
+def _impl_bytes(T, H, blk_bytes, chunks, K=4, norm_folded=True):
     """Intermediate bytes each kernel of the prefill step writes or reads back (not the method's
     I/O): the chunk workspace (one block per (chunk, head)), the readout plane o between the scan
-    and the RMSNorm, and the staged path's prepared q, k, v, g, beta planes."""
+    and the RMSNorm (none when the inter kernel writes y itself), and the staged path's prepared
+    q, k, v, g, beta planes."""
     C = H * D
     plane = T * C * 4
     ws = chunks * H * blk_bytes
     prepared = 4 * plane + T * H * 4
     return {
         "kda_chunk_prep_intra_kernel": ws,
-        "kda_chunk_inter_kernel": ws + plane,
+        "kda_chunk_inter_kernel": ws + (0 if norm_folded else plane),
         "kda_gated_rmsnorm_kernel": plane,
         "kda_prep_kernel": prepared,
         "kda_ring_roll_kernel": 3 * C * (K - 1) * (2 + 4 + 4),
@@ -643,8 +646,10 @@ def run_ours(args):
         return None
 
     cpu = None if args.skip_cpu else cpu_baseline(pre, args.cpu_sample_heads)
-    mbytes = _method_bytes(T, H)
-    ibytes = _impl_bytes(T, H, blk_bytes, chunks)
+    # the fused prefill normalises inside its inter kernel (no RMSNorm launch in the step)
+    folded = fused and "kda_gated_rmsnorm_kernel" not in ktimes
+    mbytes = _method_bytes(T, H, norm_folded=folded)
+    ibytes = _impl_bytes(T, H, blk_bytes, chunks, norm_folded=folded)
     cflops = _chunk_flops(T, H)
     tensor_peak = peaks["bf16_tflops_sustained"]
     total_kms = sum(v[1] for v in ktimes.values())
@@ -663,8 +668,8 @@ def run_ours(args):
             ent.update(tensor_flop_per_launch=cflops[name], tensor_tflops=tf,
                        frac_tensor=tf / tensor_peak)
         kernels.append(ent)
-    step_bytes = sum(mbytes[k] for k in ("kda_chunk_prep_intra_kernel", "kda_chunk_inter_kernel",
-                                         "kda_gated_rmsnorm_kernel"))
+    step_bytes = sum(mbytes[k] for k in ("kda_chunk_prep_intra_kernel", "kda_chunk_inter_kernel")
+                     + (() if folded else ("kda_gated_rmsnorm_kernel",)))
     method_tflops = scan_flop / (ms_step / 1e3) / 1e12
     step = {"method_bytes": step_bytes, "method_gbs": step_bytes / (ms_step / 1e3) / 1e9,
             "frac_hbm": step_bytes / (ms_step / 1e3) / 1e9 / peaks["hbm_gbs"],
@@ -685,7 +690,7 @@ def run_ours(args):
                              "weights, ring in); its workspace writes are impl_bytes_per_launch",
                     "timing": "library CUDA-event timer around each launch, timed region"}
         # the prefill's fraction of the tensor-pipe roofline: the method's flop over the step
-        roofline_tensor = {"bound": "tensor", "kernel": "whole step (prep + intra, inter, "
+        roofline_tensor = {"bound": "tensor", "kernel": "whole step (prep + intra, inter + "
                                                         "RMSNorm)",
                            "achieved": method_tflops, "peak": tensor_peak, "unit": "TFLOP/s",
                            "frac": method_tflops / tensor_peak,

@@ -198,8 +198,10 @@ int scan_impl(const float* q, const float* k, const float* v, const float* g, in
                              : launch_scan_seq(a, static_cast<cudaStream_t>(stream)));
 }
 
-// Byte offsets of the pieces of kda_prefill_fused's workspace: the scan's readout o, then the
-// chunked scan's scratch (the prepared q, k, v, g never leave the chunk kernel).
+// Byte offsets of the pieces of kda_prefill_fused's workspace: the scan's readout o (written only
+// when value heads are wider than 128 and the RMSNorm kernel reads it back; 128-wide heads are
+// normalised inside the chunk kernel), then the chunked scan's scratch (the prepared q, k, v, g
+// never leave the chunk kernel).
 struct PrefillLayout {
     size_t o, chunk;
 };
@@ -260,9 +262,25 @@ int prefill_impl(const void* q_raw, const void* k_raw, const void* v_raw, int ra
     a.vsub = vsub;
     a.gate_mode = gate_mode; a.state_in = state_in; a.state_out = state_out; a.o = oh;
     a.seq = seq; a.H = H; a.scale = scale; a.order = nullptr; a.err = dev_err_ptr();
+    // 128-wide value heads and at least one (sequence, head) chain per SM: the chunk kernel
+    // writes y itself (the RMSNorm of a row needs only that row; its ~200 instructions a row, spread
+    // over every SM, cost less than the readout's round trip through HBM).  With fewer chains
+    // they would lengthen each chain on the SMs it has, and value heads wider than 128 need the
+    // whole row: there the RMSNorm kernel runs apart.
+    bool fold_norm = false;
+    if (vsub == 1) {
+        int dev = 0, sms = 0;
+        if (cudaGetDevice(&dev) == cudaSuccess &&
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
+            fold_norm = sms > 0 && (long)seq.N * H >= sms;
+    }
+    if (fold_norm) {
+        a.norm_w = norm_w; a.norm_z = gate_raw; a.norm_y = y; a.norm_eps = norm_eps;
+        a.norm_silu = norm_silu ? 1 : 0;
+    }
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
     rc = cuda_status(launch_prefill_chunk(pa, a, cu_host, w + L.chunk, st));
-    if (rc != KDA_OK || seq.total_rows == 0) return rc;
+    if (rc != KDA_OK || seq.total_rows == 0 || fold_norm) return rc;
     NormArgs na{oh, norm_w, gate_raw, y, seq.total_rows * pa.Hg, norm_eps, norm_silu ? 1 : 0,
                 vsub * kHeadDim};
     return cuda_status(launch_gated_rmsnorm(na, static_cast<cudaStream_t>(stream)));

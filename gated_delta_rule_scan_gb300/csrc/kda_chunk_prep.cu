@@ -218,14 +218,6 @@ __device__ __forceinline__ TaskPos task_pos(const SeqLayout& L, const int* chunk
     return t;
 }
 
-__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)),
-                 "l"(reinterpret_cast<uint64_t>(src))
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
-
 // Staged bf16 raw rows of one task: [plane][row][128 channels], row r = chunk token r - (KW-1)
 // (the conv halo first).  Lives in sm.bia[1] + sm.kb (32 KB), free from the end of one task's
 // MMA-a to the next task's conv.

@@ -76,6 +76,10 @@ struct ScanArgs {
     int vsub;                // 128-wide sub-heads per value head (value width vsub * 128): unit h
                              // is value head h / vsub, which owns the gate and beta and reads q/k
                              // head (h / vsub) % Hk; 0 means 1
+    // the gated RMSNorm folded into the chunked scan's readout (fused prefill, 128-wide value
+    // heads): with norm_y set the chunk kernel writes y = rmsnorm(o) * w * gate(z) in place of o
+    const float* norm_w; const float* norm_z; float* norm_y; float norm_eps;
+    int norm_silu;           // gate: 0 sigmoid (KDA), 1 SiLU (GDN's gated_rmsnorm)
 };
 
 // the heads of q and k, and the one value head h reads

@@ -3,6 +3,7 @@
 // q, k, v, g planes and the sequential inter-chunk kernel, with their launchers.  The method,
 // the workspace layout and the shared device code are in kda_chunk_common.cuh.
 #include <cstring>
+#include <type_traits>
 
 #include "kda_chunk_common.cuh"
 #include "kda_ring.cuh"
@@ -255,6 +256,7 @@ constexpr int kInterStages = 3;                  // workspace blocks in flight p
 struct __align__(128) InterSmem {
     unsigned char blk[kInterStages][kBlkBytes];
     float otile[3][kCc][128];                    // chunks' o rows on their way out (c % 3)
+    float ztile[kCc][128];                       // NORM: the RMSNorm gate z of the next o rows
     uint64_t bar_ld[kInterStages];
     uint64_t bar_mma;                            // MMA-1, then MMA-2
     uint32_t tmem_base;
@@ -326,11 +328,14 @@ __device__ __forceinline__ void tmem_ld_n(uint32_t taddr, float* v) {
 // update runs in two passes, keys 0..63 then 64..127, so that the next chunk's MMA-1 takes its
 // first four K-steps while the second pass runs.  More threads per value row shorten each
 // thread's share of the chunk's dependent register / TMEM work.  Thread 0 issues the MMAs,
-// thread 32 the workspace loads, and the lanes of warp 2 the o rows' bulk stores.
+// thread 32 the workspace loads, and the lanes of warp 2 the o rows' bulk stores.  With NORM (the
+// fused prefill, 128-wide value heads) no o row leaves: while MMA-2 of chunk c runs, each warp
+// turns two o rows of chunk c-1 into y rows of the gated RMSNorm, their z rows copied into shared
+// memory (cp.async) a chunk ahead.
 constexpr int kInterKq = 4;
 constexpr int kThrInter = 128 * kInterKq;
 
-template <int GATE_MODE>
+template <int GATE_MODE, bool NORM>
 __global__ void __launch_bounds__(kThrInter, 1)
 kda_chunk_inter_kernel(ScanArgs a, const int* chunk_off, const unsigned char* ws,
                        const __grid_constant__ CUtensorMap tmo, const __grid_constant__ PrepArgs ring) {
@@ -463,6 +468,56 @@ kda_chunk_inter_kernel(ScanArgs a, const int* chunk_off, const unsigned char* ws
         }
         bulk_commit();
     };
+    // NORM: the gated RMSNorm of chunk cp's o rows (staged in otile[cp % 3]), rows 2 warp and
+    // 2 warp + 1, one float4 per lane -- the RMSNorm kernel's arithmetic on the same o values,
+    // so y has the bits that storing o and normalising it there gives.  Each lane reads back
+    // only the z float4s it copied itself (load_z), so its own wait suffices.
+    constexpr int kRowsPerWarp = kCc / (kThrInter / 32);
+    auto norm_rows = [&](int cp, auto silu) {
+        const long r0 = begin + (long)cp * kCc;
+        const int ntp = (int)min((long)kCc, L - (long)cp * kCc);
+        const float4 w4 = *reinterpret_cast<const float4*>(a.norm_w + 4 * olane);
+        cp_async_wait_all();
+#pragma unroll
+        for (int j = 0; j < kRowsPerWarp; ++j) {
+            const int t = kRowsPerWarp * warp + j;
+            if (t >= ntp) break;
+            const float4 o4 = reinterpret_cast<const float4*>(sm.otile[cp % 3][t])[olane];
+            float ss = __fmul_rn(o4.x, o4.x);
+            ss = ss + __fmul_rn(o4.y, o4.y);
+            ss = ss + __fmul_rn(o4.z, o4.z);
+            ss = ss + __fmul_rn(o4.w, o4.w);
+            const float inv = rms_inv_f(warp_sum(ss), a.norm_eps);
+            const long base = (r0 + t) * C + h * kHeadDim + 4 * olane;
+            const float4 z4 = reinterpret_cast<const float4*>(sm.ztile[t])[olane];
+            constexpr bool SILU = decltype(silu)::value;
+            float4 y4;
+            y4.x = gated_norm_f<SILU>(o4.x, inv, w4.x, z4.x);
+            y4.y = gated_norm_f<SILU>(o4.y, inv, w4.y, z4.y);
+            y4.z = gated_norm_f<SILU>(o4.z, inv, w4.z, z4.z);
+            y4.w = gated_norm_f<SILU>(o4.w, inv, w4.w, z4.w);
+            __stcs(reinterpret_cast<float4*>(a.norm_y + base), y4);
+        }
+    };
+    auto norm_chunk = [&](int cp) {
+        if (a.norm_silu) norm_rows(cp, std::true_type{});
+        else norm_rows(cp, std::false_type{});
+    };
+    // NORM: chunk c's z rows (this warp's two) into ztile, a chunk before norm_rows reads them;
+    // issued after the lane's reads of the previous rows there
+    auto load_z = [&](int c) {
+        const long r0 = begin + (long)c * kCc;
+        const int ntp = (int)min((long)kCc, L - (long)c * kCc);
+#pragma unroll
+        for (int j = 0; j < kRowsPerWarp; ++j) {
+            const int t = kRowsPerWarp * warp + j;
+            if (t < ntp)
+                cp_async16(reinterpret_cast<float4*>(sm.ztile[t]) + olane,
+                           a.norm_z + (r0 + t) * C + h * kHeadDim + 4 * olane);
+        }
+        cp_async_commit();
+    };
+    if (NORM && nch > 0) load_z(0);
     for (int c = 0; c < nch; ++c) {
         const int st = c % kInterStages;
         const unsigned char* B = sm.blk[st];
@@ -495,7 +550,7 @@ kda_chunk_inter_kernel(ScanArgs a, const int* chunk_off, const unsigned char* ws
         tc_fence_before();
         if (__syncthreads_or(!ok || late_fail)) { failed = true; break; }
         tc_fence_after();
-        if (ostore_lane) {
+        if (!NORM && ostore_lane) {
             if (c > 0) flush_o(c - 1);           // its o rows were written before the barrier
             bulk_wait_read1();                   // only that store may still read its tile: the
                                                  // one of chunk c-3 (tile c % 3) is free
@@ -505,6 +560,12 @@ kda_chunk_inter_kernel(ScanArgs a, const int* chunk_off, const unsigned char* ws
             mma2_ts(tbase + kTD2, tbase + kTA2, tbase + kTA2 + 16,
                     tc_smem_desc(smem_u32(B + kOffB2), 128, kSbo32), 2, id2);
             tc_commit(&sm.bar_mma);
+        }
+        if constexpr (NORM) {                    // while MMA-2 runs: its o rows were written
+            if (c > 0) {                         // before the barrier above
+                norm_chunk(c - 1);
+                load_z(c);
+            }
         }
         // every thread observes MMA-2's completion itself (no barrier needed for the TMEM reads
         // below); a wait that gave up is carried to the next barrier that can end the loop
@@ -559,10 +620,12 @@ kda_chunk_inter_kernel(ScanArgs a, const int* chunk_off, const unsigned char* ws
         fence_proxy_async_smem();
     }
     failed = __syncthreads_or(failed || late_fail) != 0;
-    if (ostore_lane) {
+    if (!NORM && ostore_lane) {
         if (!failed && nch > 0) flush_o(nch - 1);
         bulk_wait_all();
     }
+    if (NORM && !failed && nch > 0) norm_chunk(nch - 1);
+    if (NORM) cp_async_wait_all();               // no copy may land after the CTA has left
     if (!failed) {
         float* srow_out = a.state_out + (((long)n * H + h) * kHeadDim + v) * kHeadDim;
 #pragma unroll
@@ -610,19 +673,19 @@ cudaError_t launch_chunk_offsets(const SeqLayout& seq, void* workspace, int** ch
     return cudaGetLastError();
 }
 
-template <int GM>
+template <int GM, bool NORM>
 static cudaError_t launch_inter_t(const ScanArgs& a, const int* chunk_off,
                                   const unsigned char* blocks, const PrepArgs& ring, cudaStream_t s) {
     const size_t smem2 = sizeof(InterSmem) + 128;
     static PerDevice<int> done2;
-    cudaError_t e = set_smem(kda_chunk_inter_kernel<GM>, smem2, done2);
+    cudaError_t e = set_smem(kda_chunk_inter_kernel<GM, NORM>, smem2, done2);
     if (e != cudaSuccess) return e;
     dim3 g2((unsigned)a.H, (unsigned)a.seq.N);
     CUtensorMap tmo;
     if (!make_tensor_map_2d(&tmo, a.o, a.seq.total_rows, (long)a.H * kHeadDim, kHeadDim, kCc))
         return cudaErrorInvalidValue;
     KernelTimer kt(kKChunkInter, s);
-    kda_chunk_inter_kernel<GM><<<g2, kThrInter, smem2, s>>>(a, chunk_off, blocks, tmo, ring);
+    kda_chunk_inter_kernel<GM, NORM><<<g2, kThrInter, smem2, s>>>(a, chunk_off, blocks, tmo, ring);
     return cudaGetLastError();
 }
 
@@ -631,8 +694,11 @@ cudaError_t launch_chunk_inter(const ScanArgs& a, const int* chunk_off,
     PrepArgs none;
     std::memset(&none, 0, sizeof(none));
     const PrepArgs& r = ring != nullptr ? *ring : none;
-    return (a.gate_mode & 1) == 0 ? launch_inter_t<0>(a, chunk_off, blocks, r, s)
-                                  : launch_inter_t<1>(a, chunk_off, blocks, r, s);
+    if (a.norm_y != nullptr)
+        return (a.gate_mode & 1) == 0 ? launch_inter_t<0, true>(a, chunk_off, blocks, r, s)
+                                      : launch_inter_t<1, true>(a, chunk_off, blocks, r, s);
+    return (a.gate_mode & 1) == 0 ? launch_inter_t<0, false>(a, chunk_off, blocks, r, s)
+                                  : launch_inter_t<1, false>(a, chunk_off, blocks, r, s);
 }
 
 template <int GM, bool EXP>

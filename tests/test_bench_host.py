@@ -36,23 +36,31 @@ def test_prefill_method_bytes(bench):
     state = 64 * 128 * 128 * 4              # one direction
     params = 8192 * 4 + 64 * 4 + 128 * 4    # dt_bias, A_log, norm weight
     assert mb["kda_chunk_prep_intra_kernel"] == raw + plane + beta + conv + ring + 8192 * 4 + 64 * 4
-    assert mb["kda_chunk_inter_kernel"] == 2 * state + ring
-    assert mb["kda_gated_rmsnorm_kernel"] == 2 * plane + 128 * 4
-    step = sum(mb[k] for k in ("kda_chunk_prep_intra_kernel", "kda_chunk_inter_kernel",
-                               "kda_gated_rmsnorm_kernel"))
+    # the fused prefill's inter kernel writes y itself: z, the norm weight and y are its bytes
+    assert mb["kda_chunk_inter_kernel"] == 2 * state + ring + 2 * plane + 128 * 4
+    step = mb["kda_chunk_prep_intra_kernel"] + mb["kda_chunk_inter_kernel"]
     assert step == raw + 3 * plane + beta + conv + 2 * ring + 2 * state + params == 614_433_536
+    # with the RMSNorm as a kernel of its own, the same total split three ways
+    mu = bench._method_bytes(4096, 64, norm_folded=False)
+    assert mu["kda_chunk_inter_kernel"] == 2 * state + ring
+    assert mu["kda_gated_rmsnorm_kernel"] == 2 * plane + 128 * 4
+    assert sum(mu[k] for k in ("kda_chunk_prep_intra_kernel", "kda_chunk_inter_kernel",
+                               "kda_gated_rmsnorm_kernel")) == step
 
 
 def test_prefill_impl_bytes(bench):
     """The library's own intermediates, reported apart: the chunk workspace (one 43,520-byte
-    block per (32-token chunk, head)) and the readout plane o."""
+    block per (32-token chunk, head)), and the readout plane o only where the RMSNorm runs as a
+    kernel of its own."""
     ib = bench._impl_bytes(4096, 64, 43520, 128)
     blocks = 128 * 64 * 43520
     plane = 4096 * 8192 * 4
     assert blocks == 356_515_840
     assert ib["kda_chunk_prep_intra_kernel"] == blocks
-    assert ib["kda_chunk_inter_kernel"] == blocks + plane
-    assert ib["kda_gated_rmsnorm_kernel"] == plane
+    assert ib["kda_chunk_inter_kernel"] == blocks
+    iu = bench._impl_bytes(4096, 64, 43520, 128, norm_folded=False)
+    assert iu["kda_chunk_inter_kernel"] == blocks + plane
+    assert iu["kda_gated_rmsnorm_kernel"] == plane
 
 
 def test_chunk_flops(bench):

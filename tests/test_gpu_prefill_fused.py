@@ -97,6 +97,48 @@ def test_prefill_nonfinite_rows_after_a_ragged_chunk(varlen):
         check_all_heads(mine, first, ("y", "state_out", "ring_out"))
 
 
+def _sms():
+    return torch.cuda.get_device_properties(0).multi_processor_count
+
+
+@pytest.mark.parametrize("norm_gate,gate_mode", [("sigmoid", 0), ("silu", 1)])
+def test_prefill_folded_norm(norm_gate, gate_mode):
+    """With at least one (sequence, head) chain per SM the inter kernel writes y through the
+    gated RMSNorm itself (no RMSNorm launch): packed sequences with ragged last chunks, one
+    shorter than a chunk and one empty; y, state and ring equal the staged path's (chunked scan,
+    then the RMSNorm kernel) bit for bit, and the oracle's on every head."""
+    from gated_delta_rule_scan_gb300 import kda
+    H = 64
+    lengths = [40, 90, 0, 17, 75]
+    N = -(-_sms() // H) + 1                      # N * H >= the SM count
+    lengths = (lengths * N)[:N]
+    inp = inputs.make_inputs(76 + gate_mode, H=H, N=N, lengths=(0, 1), raw_dtype="bf16",
+                             conv=True, ring="randn", gate_mode=gate_mode, state="randn",
+                             epilogue=True)
+    cu = np.concatenate([[0], np.cumsum(lengths)])
+    rows, C = int(cu[-1]), H * 128
+    rng = np.random.default_rng(1076)
+    for k in ("q_raw", "k_raw", "v_raw"):
+        setattr(inp, k, torch.from_numpy(rng.standard_normal((rows, C)).astype(np.float32))
+                .to(torch.bfloat16))
+    inp.f_raw = torch.from_numpy(rng.standard_normal((rows, C if gate_mode == 0 else H))
+                                 .astype(np.float32))
+    inp.beta_raw = torch.from_numpy(rng.standard_normal((rows, H)).astype(np.float32))
+    inp.gate_raw = torch.from_numpy(rng.standard_normal((rows, C)).astype(np.float32))
+    inp.cu_seqlens = cu
+    kda.kernel_timing(True)
+    try:
+        fused = gpu_prefill(inp, varlen=True, norm_gate=norm_gate)
+        times = kda.kernel_times()
+    finally:
+        kda.kernel_timing(False)
+    assert "kda_gated_rmsnorm_kernel" not in times and "kda_chunk_inter_kernel" in times, times
+    unf = gpu_forward(inp, varlen=True, algo=2, norm_gate=norm_gate)
+    for k in ("y", "state_out", "ring_out"):
+        assert torch.equal(fused[k], unf[k]), k
+    check_all_heads(fused, inp, ("y", "state_out", "ring_out"), norm_gate=norm_gate)
+
+
 @pytest.mark.parametrize("raw,gate_mode", [("f32", 1), ("f32", 0), ("bf16", 1)])
 def test_prefill_fused_repeatable(raw, gate_mode):
     """Repeated fused prefills of a sequence whose last chunk holds 12 tokens (whole warps of the
@@ -212,7 +254,8 @@ def test_prefill_fused_contract():
 def test_kernel_timer_counts_fused_launches():
     """With timing on, one fused prefill of two packed sequences records exactly its kernels:
     chunk offsets, the fused prep + intra-chunk kernel, inter (which also rolls the conv ring)
-    and the RMSNorm, once each (no separate prep or ring-roll kernel)."""
+    and the RMSNorm, once each (no separate prep or ring-roll kernel): with fewer (sequence, head)
+    chains than SMs the RMSNorm runs as a kernel of its own."""
     from gated_delta_rule_scan_gb300 import kda
     inp = inputs.make_inputs(74, H=2, N=2, lengths=(40, 90), raw_dtype="bf16", conv=True,
                              ring="randn", state="randn", epilogue=True)
