@@ -199,9 +199,9 @@ int scan_impl(const float* q, const float* k, const float* v, const float* g, in
 }
 
 // Byte offsets of the pieces of kda_prefill_fused's workspace: the scan's readout o (written only
-// when value heads are wider than 128 and the RMSNorm kernel reads it back; 128-wide heads are
-// normalised inside the chunk kernel), then the chunked scan's scratch (the prepared q, k, v, g
-// never leave the chunk kernel).
+// when the RMSNorm kernel reads it back: value heads wider than 128, or fewer (sequence, head)
+// chains than SMs; otherwise the chunk kernel normalises it as it leaves), then the chunked
+// scan's scratch (the prepared q, k, v, g never leave the chunk kernel).
 struct PrefillLayout {
     size_t o, chunk;
 };
