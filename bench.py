@@ -218,10 +218,11 @@ def _method_bytes(T, H, K=4, norm_folded=True):
     """The method's own HBM bytes per prefill step (T tokens, H heads, one sequence, conv K taps,
     bf16 raw q/k/v), split by the kernel that moves them: every input read once, every output
     written once, no intermediate.  norm_folded: the fused prefill's inter kernel writes y itself
-    (128-wide value heads and N * H at least the SM count), so z, the norm weight and y are its
-    bytes; otherwise, and on the staged path, they are the RMSNorm kernel's.  What the library writes and reads back between its own
-    kernels (the chunk workspace, the readout plane o, the staged path's prepared planes) is
-    implementation traffic, reported apart by _impl_bytes."""
+    (128-wide value heads, N * H at least two thirds of the SM count), so z, the norm weight and
+    y are its bytes; otherwise, and on the staged path, they are the RMSNorm kernel's.  What the
+    library writes and reads back between its own kernels (the chunk workspace, the readout
+    plane o, the staged path's prepared planes) is implementation traffic, reported apart by
+    _impl_bytes."""
     C = H * D
     f32, bf16 = 4, 2
     plane = T * C * f32

@@ -199,8 +199,9 @@ int scan_impl(const float* q, const float* k, const float* v, const float* g, in
 }
 
 // Byte offsets of the pieces of kda_prefill_fused's workspace: the scan's readout o (written only
-// when the RMSNorm kernel reads it back: value heads wider than 128, or fewer (sequence, head)
-// chains than SMs; otherwise the chunk kernel normalises it as it leaves), then the chunked
+// when the RMSNorm kernel reads it back: value heads wider than 128, or (sequence, head) chains
+// on fewer than two thirds of the SMs; otherwise the chunk kernel normalises it as it leaves),
+// then the chunked
 // scan's scratch (the prepared q, k, v, g never leave the chunk kernel).
 struct PrefillLayout {
     size_t o, chunk;
@@ -262,17 +263,19 @@ int prefill_impl(const void* q_raw, const void* k_raw, const void* v_raw, int ra
     a.vsub = vsub;
     a.gate_mode = gate_mode; a.state_in = state_in; a.state_out = state_out; a.o = oh;
     a.seq = seq; a.H = H; a.scale = scale; a.order = nullptr; a.err = dev_err_ptr();
-    // 128-wide value heads and at least one (sequence, head) chain per SM: the chunk kernel
-    // writes y itself (the RMSNorm of a row needs only that row; its ~200 instructions a row, spread
-    // over every SM, cost less than the readout's round trip through HBM).  With fewer chains
-    // they would lengthen each chain on the SMs it has, and value heads wider than 128 need the
-    // whole row: there the RMSNorm kernel runs apart.
+    // 128-wide value heads and (sequence, head) chains on at least two thirds of the SMs: the
+    // chunk kernel writes y itself (the RMSNorm of a row needs only that row; its ~200
+    // instructions a row, spread over most SMs, cost less than the readout's round trip through
+    // HBM; measured at full length: 64 chains on 152 SMs 6 % slower folded, 128 to 1,024 chains
+    // 1-3 % faster but for 192, one wave and a small second, 1 % slower).  With fewer chains they
+    // would lengthen each chain on the SMs it has, and value heads wider than 128 need the whole
+    // row: there the RMSNorm kernel runs apart.
     bool fold_norm = false;
     if (vsub == 1) {
         int dev = 0, sms = 0;
         if (cudaGetDevice(&dev) == cudaSuccess &&
             cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
-            fold_norm = sms > 0 && (long)seq.N * H >= sms;
+            fold_norm = sms > 0 && 3 * (long)seq.N * H >= 2L * sms;
     }
     if (fold_norm) {
         a.norm_w = norm_w; a.norm_z = gate_raw; a.norm_y = y; a.norm_eps = norm_eps;

@@ -289,10 +289,10 @@ size_t kda_prefill_workspace_bytes(int N, int total_T, int H, int D, int gate_mo
  * kda_core_gated (conv + SiLU, l2 norm, gates and beta, the chunked scan, gated RMSNorm), the
  * same computation as kda_conv_l2norm_prep + kda_scan with KDA_ALGO_CHUNK +
  * kda_gated_rmsnorm_out with the same arguments.  The prepared q, k, v and gates are computed
- * inside the chunked scan's first kernel and never reach memory.  With N * H at least the
- * device's SM count the readout is normalised inside the chunked scan's second kernel as it
- * leaves (the RMSNorm of a row needs only that row); with fewer (sequence, head) pairs it passes
- * through the workspace to the RMSNorm kernel.  y is the same either way.
+ * inside the chunked scan's first kernel and never reach memory.  With N * H at least two thirds
+ * of the device's SM count the readout is normalised inside the chunked scan's second kernel as
+ * it leaves (the RMSNorm of a row needs only that row); with fewer (sequence, head) pairs it
+ * passes through the workspace to the RMSNorm kernel.  y is the same either way.
  * Arguments and layouts as in those three calls, except that bf16 q_raw, k_raw and v_raw must be
  * [16B] here (40010 otherwise; the staged prep needs 8 bytes); gate_mode is KDA_GATE_PER_CHANNEL
  * or KDA_GATE_PER_HEAD (the KDA_GATE_EXP flag is not accepted, 40007); norm_w [D] f32 [16B];

@@ -103,7 +103,7 @@ def _sms():
 
 @pytest.mark.parametrize("norm_gate,gate_mode", [("sigmoid", 0), ("silu", 1)])
 def test_prefill_folded_norm(norm_gate, gate_mode):
-    """With at least one (sequence, head) chain per SM the inter kernel writes y through the
+    """With (sequence, head) chains on every SM the inter kernel writes y through the
     gated RMSNorm itself (no RMSNorm launch): packed sequences with ragged last chunks, one
     shorter than a chunk and one empty; y, state and ring equal the staged path's (chunked scan,
     then the RMSNorm kernel) bit for bit, and the oracle's on every head."""
@@ -254,8 +254,8 @@ def test_prefill_fused_contract():
 def test_kernel_timer_counts_fused_launches():
     """With timing on, one fused prefill of two packed sequences records exactly its kernels:
     chunk offsets, the fused prep + intra-chunk kernel, inter (which also rolls the conv ring)
-    and the RMSNorm, once each (no separate prep or ring-roll kernel): with fewer (sequence, head)
-    chains than SMs the RMSNorm runs as a kernel of its own."""
+    and the RMSNorm, once each (no separate prep or ring-roll kernel): with (sequence, head)
+    chains on fewer than two thirds of the SMs the RMSNorm runs as a kernel of its own."""
     from gated_delta_rule_scan_gb300 import kda
     inp = inputs.make_inputs(74, H=2, N=2, lengths=(40, 90), raw_dtype="bf16", conv=True,
                              ring="randn", state="randn", epilogue=True)
